@@ -1,0 +1,145 @@
+/*
+ * oracle.h -- plain, slow CPU reference for the MoE dispatch/combine path.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product library may include,
+ * link or call this code; only the test-suite, the smoke check and the
+ * benchmark's CPU-baseline leg use it.  It shares no source with the CUDA
+ * path: its own types, its own bf16 conversion, its own loops.
+ *
+ * Every floating-point result is accumulated in IEEE double and rounded once
+ * (round-to-nearest-even) to the output type.  All loops run in the order the
+ * definitions below state; there is no blocking, fusion or reordering.
+ *
+ * Sources (web pages, cited by title and section):
+ *  [MOE-OPS]  "从零理解 MoE 算子：路由、专家并行与 Token 重排"
+ *             (www.171host.com/746420.html) -- a from-scratch MoE operator
+ *             tutorial: §3 Router, §7 GroupedMatMul, §8 expert FFN,
+ *             §11-13 rank-major / expert-major, §16 top-k merge.
+ *  [COMBINE]  "03 · Combine 与 forward / backward 对称性"
+ *             (llm-infra-atlas.github.io/parallel/05_ep/03_combine_and_backward/)
+ *             -- §1 combine formula, §2.1 sort_chunks inverse, §2.3
+ *             unpermute = scatter_add, §4 backward symmetry table.
+ *  [DISPATCH] "token dispatcher + fuse_a2a" (obnotes-4iw.pages.dev, Megatron
+ *             transformer-moe notes) -- §1.1 Alltoall: the permute()
+ *             walk-through (transposed routing map, masked_select, index_select)
+ *             and its worked example.
+ *
+ * Conventions: tensors are row-major and contiguous.  bf16 values are passed
+ * as their 16-bit patterns (uint16_t).  An expert id of -1 in topk_idx marks an
+ * empty slot: it routes nothing and its slot position is -1.
+ * Return value: 0 on success, a negative number on invalid arguments.
+ */
+#ifndef MOE_ORACLE_H
+#define MOE_ORACLE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum { ORACLE_F32 = 0, ORACLE_BF16 = 1 };
+
+/* Round each double to bf16 (nearest, ties to even; subnormals and overflow
+ * to infinity handled).  Exported so tests can pin it to a library routine. */
+int oracle_bf16_from_double(const double* v, int64_t n, uint16_t* out);
+
+/* [MOE-OPS] §3: topk_scores, topk_indices = topk(router_logits, k);
+ * topk_weights = softmax(topk_scores).
+ * Slot order: descending logit; equal logits go to the lower expert id.
+ * Softmax over the k chosen scores, stabilised by the largest one, in double;
+ * topk_w is that value rounded to float, topk_w_f64 (nullable) the double. */
+int oracle_topk_softmax(const float* logits, int64_t T, int E, int k,
+                        int32_t* topk_idx, float* topk_w, double* topk_w_f64);
+
+/* From topk_idx [T,k] build, following [DISPATCH] §1.1 and [MOE-OPS] §7:
+ *  routing_map [T,E]   1 where expert e is among token t's choices (nullable)
+ *  counts [E]          tokens per expert (column sums of the routing map)
+ *  offsets [E+1]       exclusive prefix of counts, offsets[0] = 0
+ *  group_list [E]      inclusive prefix of counts
+ *  sorted_indices [T*k] token ids, expert-major, ascending token inside an
+ *                      expert (the order of a row-major scan of the
+ *                      transposed routing map); entries past offsets[E] = -1
+ *  slot_pos [T,k]      position of (t, topk_idx[t,j]) in sorted_indices, -1
+ *                      for an empty slot
+ *  permuted_probs [T*k] topk_w rearranged into sorted_indices order; entries
+ *                      past offsets[E] = 0 (nullable; needs topk_w)
+ * Fails on an expert id outside [-1, E) or a token naming an expert twice. */
+int oracle_route_indices(const int32_t* topk_idx, const float* topk_w,
+                         int64_t T, int E, int k, uint8_t* routing_map,
+                         int32_t* counts, int32_t* offsets, int32_t* group_list,
+                         int32_t* sorted_indices, int32_t* slot_pos,
+                         float* permuted_probs);
+
+/* [DISPATCH] §1.1 permuted_input = tokens.index_select(0, sorted_indices):
+ * out[p] = x[sorted_indices[p]] for p < n_rows; elem_size 4 or 2 bytes. */
+int oracle_permute(const void* x, int elem_size, int64_t T, int64_t H,
+                   const int32_t* sorted_indices, int64_t n_rows, void* out);
+
+/* Chunk orders for a [R source ranks x L local experts] split matrix,
+ * [COMBINE] §2.1 and [MOE-OPS] §11-13:
+ *  inverse = 0: rank-major -> expert-major, idxs[l*R + r] = r*L + l
+ *  inverse = 1: expert-major -> rank-major, idxs[r*L + l] = l*R + r          */
+int oracle_chunk_idxs(int R, int L, int inverse, int32_t* idxs);
+
+/* sort_chunks_by_idxs: cut `in` [N rows] into C consecutive chunks of
+ * split_sizes[c] rows, then write chunk sorted_idxs[0], sorted_idxs[1], ...
+ * back to back into `out`.  Requires sum(split_sizes) == N and sorted_idxs a
+ * permutation of 0..C-1. */
+int oracle_sort_chunks(const void* in, int64_t row_bytes, int64_t N,
+                       const int32_t* split_sizes, const int32_t* sorted_idxs,
+                       int C, void* out);
+
+/* [COMBINE] §1, [MOE-OPS] §16:
+ * out[t] = sum_{j=0..k-1} topk_w[t,j] * y[slot_pos[t,j]], accumulated in
+ * double in slot order j = 0..k-1, rounded once to `dtype`.
+ * topk_w = NULL gives the unweighted sum.  out_f64 (nullable) keeps the
+ * double sums. */
+int oracle_combine(const void* y, int dtype, int64_t T, int64_t H, int k,
+                   const int32_t* slot_pos, const float* topk_w, void* out,
+                   double* out_f64);
+
+/* [COMBINE] §2.3 unpermute as a scatter-add: out = zeros([T,H]);
+ * out[sorted_indices[p]] += probs[p] * y[p] for p < n_valid (probs NULL = 1),
+ * in double, in ascending p, rounded once.  A second statement of the same
+ * combine, used to cross-check oracle_combine. */
+int oracle_unpermute(const void* y, int dtype, int64_t T, int64_t H,
+                     const int32_t* sorted_indices, const float* probs,
+                     int64_t n_valid, void* out, double* out_f64);
+
+/* [COMBINE] §4 (the backward of the linear combine is its transpose):
+ *  grad_y[slot_pos[t,j]] = topk_w[t,j] * grad_out[t]      (rounded once)
+ *  grad_probs[t,j]       = sum_h grad_out[t,h] * y[slot_pos[t,j],h]
+ *                          (double, ascending h, rounded to float)
+ * topk_w = NULL means every weight is 1.  Empty slots give grad_probs 0 and
+ * write no row.  grad_probs_f64 (nullable) keeps the double dots. */
+int oracle_combine_backward(const void* grad_out, const void* y, int dtype,
+                            int64_t T, int64_t H, int k,
+                            const int32_t* slot_pos, const float* topk_w,
+                            void* grad_y, float* grad_probs,
+                            double* grad_probs_f64);
+
+/* Stand-in expert: y[p] = x_perm[p] * scale[e] for offsets[e] <= p <
+ * offsets[e+1], product in double, rounded once. */
+int oracle_expert_scale(const void* x_perm, int dtype, int64_t H, int E,
+                        const int32_t* offsets, const float* scale, void* y);
+
+/* [MOE-OPS] §7-8 GMM1 -> SwiGLU -> GMM2 per expert over group_list segments:
+ *  gate_up = X_e @ w_up[e]            [n, 2I]  (double)
+ *  gate, up = gate_up[:, :I], gate_up[:, I:]
+ *  hidden = silu(gate) * up           rounded to bf16 (the stored activation)
+ *  y_e = hidden @ w_down[e]           [n, H]   (double, rounded to bf16)
+ * x [N,H], w_up [E,H,2I], w_down [E,I,H], y [N,H], all bf16 patterns.
+ * rows (nullable): compute only these n_rows row ids; otherwise every row in
+ * [0, offsets[E]).  y_f64 (nullable) has the same layout as y. */
+int oracle_grouped_swiglu(const uint16_t* x, const uint16_t* w_up,
+                          const uint16_t* w_down, const int32_t* offsets,
+                          int E, int64_t H, int64_t I,
+                          const int64_t* rows, int64_t n_rows,
+                          uint16_t* y, double* y_f64);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_ORACLE_H */
