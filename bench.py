@@ -1,0 +1,400 @@
+"""Benchmark of the MoE dispatch/combine hot path on GB300.
+
+One step = one pass of the whole path over one batch of the DeepSeek-shaped
+workload (T=16384 tokens, H=7168, E=256 experts, top-8, bf16, Zipf-biased
+router): moe_route (top-k + softmax + counts/offsets + expert-major indices),
+moe_permute, moe_combine (the expert being the identity, so expert_out is the
+permuted buffer) and moe_combine_backward.  value = routed tokens (T*k) per
+second over whole steps, inputs resident in HBM.  The step's working set is
+about 4.5 GB, far larger than the 129 MB L2, so no L2 flush is needed.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+For N > 1 launch under torchrun: every rank runs an independent replica of
+the workload on its own GPU (the path has no cross-GPU exchange), timing is
+bracketed by a barrier and the max over ranks is reported.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "permute+combine routed-tokens/s and achieved HBM GB/s vs GB300 peak (1 GPU)"
+UNIT = "routed-tokens/s"
+WORKLOAD = "skewed"
+FALLBACK_HBM_GBS = 6800.0
+ROUTE_LAUNCHES = 3       # top-k, scan, scatter
+STEP_LAUNCHES = ROUTE_LAUNCHES + 3
+
+
+# ------------------------------------------------------------ host-side logic
+
+def algorithmic_bytes(T, H, E, k, b):
+    """Bytes each op must move: every source row read once, every
+    destination row written once, plus the 4-byte index/probability arrays."""
+    N = T * k
+    return {
+        "route": T * E * 4 + N * 4 * 5 + E * 4 * 3,
+        "permute": T * H * b + N * H * b + N * 4,
+        "combine": N * H * b + T * H * b + N * 8,
+        "combine_backward": T * H * b + 2 * N * H * b + N * 12,
+    }
+
+
+def job_value(units_per_rank_step: float, world: int, steps: int, max_elapsed_s: float) -> float:
+    """Whole-job throughput: units every rank processed over the slowest rank's time."""
+    return units_per_rank_step * world * steps / max_elapsed_s
+
+
+def reduce_max(value: float, device=None) -> float:
+    """Max of a float over the ranks of the default process group (or itself)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def source_digest(*files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel_key: str, digest: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current source (the summary records the source digest)."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    m = re.search(rf"^{re.escape(kernel_key)}\s+digest=(\w+)\s+bytes_per_launch=([0-9.eE+]+)",
+                  text, re.M)
+    if not m or m.group(1) != digest:
+        return None
+    return float(m.group(2))
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle sampling while the timed region runs."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, period_ms: int = 50):
+        self.gpu = gpu_index
+        self.period = period_ms
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", str(self.period)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in (getattr(self, "out", "") or "").splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ our arm
+
+def run_ours(args, rank, world, local_rank):
+    import numpy as np
+    import torch
+
+    import unpermute_combine_gb300 as moe
+    import workloads as wl
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    d = wl.make(WORKLOAD, with_grad=True, T=args.tokens)
+    W = d["workload"]
+    T, H, E, k, b = d["x"].shape[0], W.H, W.E, W.k, 2
+    N = T * k
+
+    bf = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)
+    h_logits = torch.from_numpy(d["logits"]).pin_memory()
+    h_x = bf(d["x"]).pin_memory()
+    h_g = bf(d["grad_out"]).pin_memory()
+    logits, x, g = h_logits.to(dev), h_x.to(dev), h_g.to(dev)
+
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        r = moe.moe_route(logits, k)
+        xp = torch.empty((N, H), dtype=torch.bfloat16, device=dev)
+        out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+        gy = torch.empty((N, H), dtype=torch.bfloat16, device=dev)
+        gp = torch.empty((T, k), dtype=torch.float32, device=dev)
+    names = ["route", "permute", "combine", "combine_backward"]
+
+    def step(lg, xx, gg, ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        moe.moe_route(lg, k, out=r, stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+        moe.moe_permute(xx, r.slot_pos, out=xp, stream=stream)
+        if ev is not None:
+            ev[2].record(stream)
+        moe.moe_combine(xp, r.slot_pos, r.topk_w, out=out, stream=stream)
+        if ev is not None:
+            ev[3].record(stream)
+        moe.moe_combine_backward(gg, xp, r.slot_pos, r.topk_w, grad_expert_out=gy,
+                                 grad_probs=gp, stream=stream)
+        if ev is not None:
+            ev[4].record(stream)
+
+    import torch.distributed as dist
+    dist_on = dist.is_available() and dist.is_initialized()
+
+    def barrier():
+        torch.cuda.synchronize(dev)
+        if dist_on:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    for _ in range(args.warmup):
+        step(logits, x, g)
+    barrier()
+
+    # -------- device-resident timed region
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local_rank) as clk:
+        barrier()
+        t_start.record(stream)
+        for i in range(args.steps):
+            step(logits, x, g, evs[i])
+        t_end.record(stream)
+        barrier()
+    elapsed = t_start.elapsed_time(t_end) / 1e3
+    per = {n: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(args.steps)) / 1e3
+           for j, n in enumerate(names)}
+    max_elapsed = reduce_max(elapsed, dev)
+
+    # -------- end to end through the public API from pinned host buffers
+    h_out = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
+    h_gp = torch.empty((T, k), dtype=torch.float32).pin_memory()
+    h2d = h_logits.numel() * 4 + h_x.numel() * 2 + h_g.numel() * 2
+    d2h = h_out.numel() * 2 + h_gp.numel() * 4
+    e2e_steps = 0 if args.no_e2e else max(1, min(args.steps, 20))
+
+    def e2e_step():
+        with torch.cuda.stream(stream):
+            lg = h_logits.to(dev, non_blocking=True)
+            xx = h_x.to(dev, non_blocking=True)
+            gg = h_g.to(dev, non_blocking=True)
+        step(lg, xx, gg)
+        with torch.cuda.stream(stream):
+            h_out.copy_(out, non_blocking=True)
+            h_gp.copy_(gp, non_blocking=True)
+
+    e2e_elapsed = float("nan")
+    if e2e_steps:
+        for _ in range(2):
+            e2e_step()
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        barrier()
+        e2e_elapsed = reduce_max(e0.elapsed_time(e1) / 1e3, dev)
+
+    if rank != 0:
+        return None
+
+    value = job_value(N, world, args.steps, max_elapsed)
+    e2e_value = job_value(N, world, e2e_steps, e2e_elapsed) if e2e_steps else None
+    peak, peak_kind = measured_peak()
+    alg = algorithmic_bytes(T, H, E, k, b)
+    kern = {}
+    for n in names:
+        gbs = alg[n] / per[n] / 1e9
+        kern[n] = {"us": round(per[n] * 1e6, 2), "alg_bytes": alg[n], "GB_s": round(gbs, 1),
+                   "frac": round(gbs / peak, 4)}
+    dominant = max(names, key=lambda n: per[n])
+    digest = source_digest("unpermute_combine_gb300/csrc/combine.cu",
+                           "unpermute_combine_gb300/csrc/permute.cu",
+                           "unpermute_combine_gb300/csrc/route.cu",
+                           "unpermute_combine_gb300/csrc/common.cuh")
+    traffic = recorded_traffic(dominant, digest)
+    ach = alg[dominant] / per[dominant] / 1e9
+    pc_time = per["permute"] + per["combine"]
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": max_elapsed / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded; DeepSeek-shaped shapes, no dataset or weights)",
+        "config": {"workload": f"{WORKLOAD}: T={T} H={H} E={E} k={k} bf16, router logits fp32 "
+                               "with 2*log-Zipf(1.1) expert bias",
+                   "T": T, "H": H, "E": E, "k": k, "routed_tokens_per_step": N,
+                   "step": "moe_route + moe_permute + moe_combine + moe_combine_backward",
+                   "l2": "no flush: step working set ~4.5 GB >> 129 MB L2",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "roofline": {"bound": "hbm", "kernel": dominant, "achieved": round(ach, 1),
+                     "peak": peak, "unit": "GB/s", "frac": round(ach / peak, 4),
+                     "peak_source": f"{peak_kind} hbm_gbs", "traffic": traffic},
+        "kernels": kern,
+        "permute_combine_routed_tokens_per_s": N / pc_time,
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                "path": "pinned host logits/x/grad_out -> device -> step -> out, grad_probs to host"},
+        "gpu_launches": STEP_LAUNCHES * args.steps,
+        "clocks": clk.summary(),
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args.cpu_tokens)
+    return line
+
+
+# ------------------------------------------------------------ oracle timing
+
+def cpu_baseline(tokens: int):
+    """The CPU oracle, as it stands, on the first `tokens` tokens of the same
+    workload: route, permute, combine and combine backward, single-threaded."""
+    import numpy as np
+
+    import oracle
+    import workloads as wl
+
+    d = wl.make(WORKLOAD, with_grad=True)
+    W = d["workload"]
+    x, lg, g = d["x"][:tokens], d["logits"][:tokens], d["grad_out"][:tokens]
+    t0 = time.perf_counter()
+    r = oracle.route(lg, W.k)
+    xp = oracle.permute(x, r["sorted_indices"])
+    out, _ = oracle.combine(xp, r["slot_pos"], r["topk_w"])
+    oracle.combine_backward(g, xp, r["slot_pos"], r["topk_w"])
+    dt = time.perf_counter() - t0
+    n = tokens * W.k
+    return {"value": n / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"first {tokens} of {W.T} tokens ({n} routed rows), one full step, "
+                      f"{dt:.1f} s single-threaded C (host has {os.cpu_count()} cores)"}
+
+
+def run_reference(args, rank):
+    """Reference arm: the CPU oracle timed as it stands on host cores."""
+    if rank != 0:
+        return None
+    import workloads as wl
+    W = wl.WORKLOADS[WORKLOAD]
+    for _ in range(args.warmup):
+        cpu_baseline(args.ref_tokens)
+    vals = [cpu_baseline(args.ref_tokens) for _ in range(args.steps)]
+    n = args.ref_tokens * W.k
+    total = sum(n / v["value"] for v in vals)
+    value = n * args.steps / total
+    cb = dict(vals[-1])
+    cb["value"] = value
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": total / args.steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded)",
+            "config": {"workload": f"{WORKLOAD}: T={W.T} H={W.H} E={W.E} k={W.k} bf16, first "
+                                   f"{args.ref_tokens} tokens per step",
+                       "T": W.T, "H": W.H, "E": W.E, "k": W.k},
+            "cpu_baseline": cb,
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-tokens", type=int, default=16384)
+    ap.add_argument("--ref-tokens", type=int, default=2048)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="use only the first TOKENS tokens (small cases for profiling)")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("at least 3 warm-up steps")
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        line = run_reference(args, rank)
+    else:
+        if world > 1:
+            import torch
+            import torch.distributed as dist
+            torch.cuda.set_device(local_rank)
+            dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+        line = run_ours(args, rank, world, local_rank)
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

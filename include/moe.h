@@ -1,0 +1,204 @@
+/*
+ * moe.h -- C ABI of libmoe, the GB300 (sm_103a) MoE token dispatch/combine
+ * library.  One GPU, one stream per call, hand-written CUDA kernels only.
+ *
+ * Sources (web pages, cited by title and section):
+ *  [MOE-OPS]  "从零理解 MoE 算子：路由、专家并行与 Token 重排"
+ *             (www.171host.com/746420.html): §3 Router and top-k, §6 grouping
+ *             tokens by expert, §7 GroupedMatMul and group_list, §8 expert
+ *             FFN (GMM1 -> SwiGLU -> GMM2), §11-13 rank-major / expert-major
+ *             permute and unpermute, §16 merging the top-k outputs, §26 edge
+ *             cases.
+ *  [COMBINE]  "03 · Combine 与 forward / backward 对称性"
+ *             (llm-infra-atlas.github.io/parallel/05_ep/03_combine_and_backward/):
+ *             §1 the combine formula, §2.1 unpermute-2 with transposed splits,
+ *             §2.3 unpermute as a (weighted) scatter-add, §4 the backward
+ *             symmetry table.
+ *  [DISPATCH] "token dispatcher + fuse_a2a" (obnotes-4iw.pages.dev, Megatron
+ *             transformer-moe notes): §1.1 the permute() walk-through.
+ *
+ * Conventions for every entry point
+ *  - Tensors are caller-owned DEVICE pointers (unless a parameter says
+ *    "host"), row-major and contiguous.  The library never allocates device
+ *    memory; scratch space is a caller-provided workspace whose size the
+ *    matching *_workspace_size call returns.  Workspaces must be 256-byte
+ *    aligned and may be reused across calls on the same stream.
+ *  - Every call is asynchronous on `stream` (a cudaStream_t passed as void*;
+ *    NULL = the legacy default stream).  Host-side validation happens before
+ *    any launch and returns MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED /
+ *    MOE_ERR_WORKSPACE with nothing launched.  A failed launch returns
+ *    MOE_ERR_CUDA.  Problems only the device can see (an expert id out of
+ *    range, splits that do not add up) are recorded in the workspace's
+ *    status word and read back with moe_workspace_status(); device code never
+ *    traps.
+ *  - Sizes: T tokens, H hidden elements per row, E experts, k = top_k.
+ *    1 <= k <= min(E, 32), 1 <= E <= 1024, T*k < 2^31, H*element < 2^31.
+ *    T = 0 and H = 0 are valid and do nothing (routing outputs still zeroed).
+ *  - Activations are MOE_F32 or MOE_BF16; logits, weights and probabilities
+ *    are float32; indices int32.  Rows whose byte length is a multiple of 16
+ *    and whose base pointers are 16-byte aligned take the vectorised path;
+ *    anything else takes an element-wise path with identical results.
+ */
+#ifndef MOE_H
+#define MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,   /* bad pointer, size or dtype: nothing launched */
+    MOE_ERR_UNSUPPORTED = 2,   /* outside the supported ranges above           */
+    MOE_ERR_WORKSPACE = 3,     /* workspace missing, too small or misaligned   */
+    MOE_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed         */
+    MOE_ERR_TIMEOUT = 5,       /* a bounded device wait gave up                */
+    MOE_ERR_DEVICE_CHECK = 6   /* the device found invalid data (see above)    */
+} moe_status_t;
+
+typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype_t;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* moe_status_string(moe_status_t status);
+
+/* ABI version of this header (bumped on any signature change). */
+int moe_abi_version(void);
+
+/* ------------------------------------------------------------------ route
+ * [MOE-OPS] §3: topk_scores, topk_indices = topk(router_logits, k);
+ * topk_weights = softmax(topk_scores).  [DISPATCH] §1.1 and [MOE-OPS] §7:
+ * routing map, tokens per expert, group_list, and the expert-major
+ * sorted_indices that a masked_select over the transposed routing map yields.
+ *
+ * Inputs
+ *   logits [T,E] float32 (finite values).
+ * Outputs (all device, caller-owned, written completely)
+ *   topk_idx [T,k] int32   chosen experts, descending logit; equal logits go
+ *                          to the lower expert id
+ *   topk_w [T,k] float32   softmax over the k chosen logits (fp32, stabilised
+ *                          by the largest); rows sum to 1
+ *   counts [E] int32       tokens routed to each expert
+ *   offsets [E+1] int32    exclusive prefix of counts (offsets[0] = 0): expert
+ *                          e owns permuted rows [offsets[e], offsets[e+1])
+ *   group_list [E] int32   inclusive prefix of counts ([3,2,4] -> [3,5,9])
+ *   sorted_indices [T*k]   source token of each permuted row: expert-major,
+ *                          ascending token inside an expert; entries past
+ *                          offsets[E] are -1
+ *   slot_pos [T,k] int32   permuted row of (t, slot j); -1 for an empty slot.
+ *                          sorted_indices[slot_pos[t,j]] == t.
+ *   permuted_probs [T*k]   topk_w[t,j] stored at row slot_pos[t,j]; 0 past
+ *                          offsets[E]
+ *   routing_map [T,E] u8   1 where token t picked expert e (NULL: not written)
+ * Every integer output is bit-exact and independent of launch order.
+ * Workspace: moe_route_workspace_size(T, E, k) bytes. */
+moe_status_t moe_route_workspace_size(int64_t T, int E, int k, size_t* bytes);
+
+moe_status_t moe_route(const float* logits, int64_t T, int E, int k,
+                       int32_t* topk_idx, float* topk_w,
+                       int32_t* counts, int32_t* offsets, int32_t* group_list,
+                       int32_t* sorted_indices, int32_t* slot_pos,
+                       float* permuted_probs, uint8_t* routing_map,
+                       void* workspace, size_t workspace_bytes, void* stream);
+
+/* The index half of moe_route for a caller that already has the top-k
+ * choices.  topk_idx [T,k] may contain -1 for an empty slot; topk_w (nullable)
+ * only feeds permuted_probs (NULL: permuted_probs is not written and may be
+ * NULL).  An id outside [-1, E) or an expert named twice by one token marks
+ * the workspace status MOE_ERR_DEVICE_CHECK and that slot is treated as
+ * empty. */
+moe_status_t moe_route_indices(const int32_t* topk_idx, const float* topk_w,
+                               int64_t T, int E, int k,
+                               int32_t* counts, int32_t* offsets, int32_t* group_list,
+                               int32_t* sorted_indices, int32_t* slot_pos,
+                               float* permuted_probs, uint8_t* routing_map,
+                               void* workspace, size_t workspace_bytes, void* stream);
+
+/* ---------------------------------------------------------------- permute
+ * [DISPATCH] §1.1 permuted_input = tokens.index_select(0, sorted_indices),
+ * computed token by token: every row x[t] is read once and written to rows
+ * slot_pos[t, 0..k-1] of `out` (the dedup form: one read, k writes).
+ *   x [T,H] (dtype), slot_pos [T,k] (from moe_route), out [T*k,H] (dtype).
+ * Rows of `out` that no slot names are left untouched.  Entries of slot_pos
+ * outside [0, T*k) are skipped. */
+moe_status_t moe_permute(const void* x, moe_dtype_t dtype, int64_t T, int64_t H, int k,
+                         const int32_t* slot_pos, void* out, void* stream);
+
+/* ------------------------------------------------------------ sort_chunks
+ * [COMBINE] §2.1 and [MOE-OPS] §11-13: cut `in` [N,H] into C consecutive
+ * chunks of split_sizes[c] rows and write chunk sorted_idxs[0],
+ * sorted_idxs[1], ... back to back into `out` [N,H].
+ *   split_sizes [C] int32 (device), sorted_idxs [C] int32 (device).
+ * If the sizes do not add up to N, or sorted_idxs is not a permutation of
+ * 0..C-1, nothing is written and the workspace status becomes
+ * MOE_ERR_DEVICE_CHECK.  1 <= C <= 65536.
+ * Workspace: moe_sort_chunks_workspace_size(C) bytes. */
+moe_status_t moe_sort_chunks_workspace_size(int C, size_t* bytes);
+
+moe_status_t moe_sort_chunks(const void* in, moe_dtype_t dtype, int64_t N, int64_t H,
+                             const int32_t* split_sizes, const int32_t* sorted_idxs, int C,
+                             void* out, void* workspace, size_t workspace_bytes,
+                             void* stream);
+
+/* Host helper: chunk orders for an [R source ranks x L local experts] split
+ * matrix M (row-major, M.ravel() are the rank-major splits).
+ *   inverse = 0: rank-major -> expert-major, idxs[l*R + r] = r*L + l
+ *   inverse = 1: expert-major -> rank-major (use the splits M.T.ravel()),
+ *                idxs[r*L + l] = l*R + r.
+ * The two orders are mutually inverse ([COMBINE] §2.1).  idxs is HOST memory
+ * of R*L ints. */
+moe_status_t moe_chunk_idxs(int R, int L, int inverse, int32_t* idxs);
+
+/* ---------------------------------------------------------------- combine
+ * [COMBINE] §1 and [MOE-OPS] §16:
+ *   out[t] = sum_{j=0..k-1} topk_w[t,j] * expert_out[slot_pos[t,j]]
+ * A deterministic gather-reduce that replaces the scatter-add of [COMBINE]
+ * §2.3.  Accumulation is float32 in slot order with a certified rounding
+ * test; elements the test cannot certify are recomputed in double in the same
+ * order.  The result is the double slot-order sum rounded once to `dtype`.
+ * topk_w = NULL gives the plain sum (the unweighted combine, and the backward
+ * of moe_permute).  Empty slots (-1) contribute nothing; a token with no valid
+ * slot gets a zero row.
+ *   expert_out [T*k,H], slot_pos [T,k], topk_w [T,k] or NULL, out [T,H]. */
+moe_status_t moe_combine(const void* expert_out, moe_dtype_t dtype, int64_t T, int64_t H,
+                         int k, const int32_t* slot_pos, const float* topk_w, void* out,
+                         void* stream);
+
+/* [COMBINE] §4: the combine is linear in expert_out and in the weights, so
+ *   grad_expert_out[slot_pos[t,j]] = topk_w[t,j] * grad_out[t]
+ *                                    (exact product rounded once to dtype)
+ *   grad_probs[t,j] = sum_h grad_out[t,h] * expert_out[slot_pos[t,j],h]
+ *                     (float32 with error-free compensated summation)
+ * topk_w = NULL means weights of 1.  Empty slots write no row and give
+ * grad_probs 0.
+ *   grad_out [T,H], expert_out [T*k,H], grad_expert_out [T*k,H] (dtype);
+ *   grad_probs [T,k] float32. */
+moe_status_t moe_combine_backward(const void* grad_out, const void* expert_out,
+                                  moe_dtype_t dtype, int64_t T, int64_t H, int k,
+                                  const int32_t* slot_pos, const float* topk_w,
+                                  void* grad_expert_out, float* grad_probs, void* stream);
+
+/* ---------------------------------------------------------- stand-in expert
+ * A per-expert elementwise scale on expert-contiguous rows, used as a
+ * stand-in for the expert FFN when exercising dispatch and combine:
+ *   out[p] = in[p] * scale[e] for offsets[e] <= p < offsets[e+1]
+ * (exact product rounded once to dtype).  Rows at or past offsets[E] are
+ * untouched.  in, out [n_rows,H]; offsets [E+1] and scale [E] on the device;
+ * n_rows bounds the rows the kernel may touch (normally T*k). */
+moe_status_t moe_expert_scale(const void* in, moe_dtype_t dtype, int64_t n_rows, int64_t H,
+                              int E, const int32_t* offsets, const float* scale, void* out,
+                              void* stream);
+
+/* ------------------------------------------------- workspace status word
+ * Waits for `stream`, then reads the status a previous call left in
+ * `workspace`: MOE_OK, MOE_ERR_DEVICE_CHECK or MOE_ERR_TIMEOUT.  Each call
+ * that takes a workspace resets its status word. */
+moe_status_t moe_workspace_status(const void* workspace, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_H */

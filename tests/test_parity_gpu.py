@@ -1,0 +1,397 @@
+"""GPU (sm_103a) vs CPU oracle parity through the C ABI.
+
+Integer, index and row-movement outputs must be bit-exact.  The combine is
+bit-exact too (it reaches the double slot-order sum rounded once); the
+routing softmax must be within 1e-6 absolute; grad_probs within one bf16 ulp
+of the oracle's double dot.  Inputs are seeded and synthetic (workloads/);
+the oracle never sees anything the GPU produced, except where a test says it
+feeds both sides the same bytes."""
+import numpy as np
+import pytest
+
+import oracle
+import workloads as wl
+from moe_testutil import (bf16_ulp_diff, bf16_ulp_of, f32_ulp_diff, to_dev, to_host,
+                          within_one_bf16_ulp)
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+import unpermute_combine_gb300 as moe  # noqa: E402
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.fail("GPU tests need a CUDA device")
+    from unpermute_combine_gb300 import build
+    build.build()
+    moe.load_library()
+
+
+def _route_both(logits, k, routing_map=True):
+    r = moe.moe_route(to_dev(logits), k, routing_map=routing_map)
+    torch.cuda.synchronize()
+    o = oracle.route(logits, k)
+    return r, o
+
+
+def _assert_route_equal(r, o, E):
+    assert (to_host(r.topk_idx) == o["topk_idx"]).all()
+    assert np.abs(to_host(r.topk_w) - o["topk_w"]).max(initial=0) <= 1e-6
+    for name in ("counts", "offsets", "group_list", "sorted_indices", "slot_pos"):
+        got = to_host(getattr(r, name))
+        assert (got == o[name]).all(), name
+    if r.routing_map is not None:
+        assert (to_host(r.routing_map) == o["routing_map"]).all()
+    # permuted probabilities: the GPU's own weights, moved bit-exactly
+    n = int(o["offsets"][E])
+    pp = to_host(r.permuted_probs)
+    w = to_host(r.topk_w)
+    sp = o["slot_pos"]
+    valid = sp >= 0
+    assert (pp[sp[valid]] == w[valid]).all()
+    assert (pp[n:] == 0).all()
+    assert np.abs(pp - o["permuted_probs"]).max(initial=0) <= 1e-6
+
+
+# ---------------------------------------------------------------------- route
+
+@pytest.mark.parametrize("name", ["tiny", "mid", "skewed", "vep8", "layer"])
+def test_route_full_workloads(name):
+    d = wl.make(name)
+    w_ = d["workload"]
+    r, o = _route_both(d["logits"], w_.k)
+    _assert_route_equal(r, o, w_.E)
+    assert moe.moe_workspace_status(r.workspace) == 0
+
+
+@pytest.mark.parametrize("T,E,k", [(1, 64, 6), (127, 256, 8), (129, 64, 6), (1000, 256, 8),
+                                   (333, 9, 3), (77, 33, 5)])
+def test_route_forced_ties(T, E, k):
+    logits = wl.tie_logits(T * 7 + E, T, E)
+    r, o = _route_both(logits, k)
+    _assert_route_equal(r, o, E)
+
+
+@pytest.mark.parametrize("T,E,k", [(0, 8, 2), (1, 1, 1), (5, 4, 4), (260, 1024, 32), (40000, 64, 4),
+                                   (33000, 300, 6),
+                                   (300, 100, 7), (513, 32, 32), (64, 2, 1)])
+def test_route_edge_shapes(T, E, k):
+    rng = np.random.default_rng(T + 31 * E + k)
+    logits = rng.standard_normal((T, E)).astype(np.float32)
+    r, o = _route_both(logits, k)
+    _assert_route_equal(r, o, E)
+
+
+def test_route_all_tokens_on_one_expert():
+    T, E, k = 1000, 64, 1
+    logits = np.random.default_rng(1).standard_normal((T, E)).astype(np.float32)
+    logits[:, 37] += 100.0
+    r, o = _route_both(logits, k)
+    _assert_route_equal(r, o, E)
+    c = to_host(r.counts)
+    assert c[37] == T and c.sum() == T
+
+
+def test_route_indices_dispatcher_worked_example(golden):
+    g = golden("dispatcher_permute_example.json")
+    idx = np.array(g["topk_idx_k2"], np.int32)
+    r = moe.moe_route_indices(to_dev(idx), None, g["num_experts"], routing_map=True)
+    torch.cuda.synchronize()
+    n = int(to_host(r.offsets)[-1])
+    assert to_host(r.routing_map).tolist() == g["routing_map"]
+    assert to_host(r.sorted_indices)[:n].tolist() == g["sorted_indices"]
+    assert (to_host(r.sorted_indices)[n:] == -1).all()
+    assert to_host(r.group_list).tolist() == [2, 5, 7]
+    tokens = np.repeat(np.arange(4, dtype=np.float32)[:, None], 8, axis=1)
+    xp = to_host(moe.moe_permute(to_dev(tokens), r.slot_pos))
+    assert xp[:n, 0].astype(int).tolist() == g["permuted_input_token_rows"]
+
+
+def test_route_indices_group_list_example(golden):
+    g = golden("moe_ops_group_list.json")
+    experts = np.concatenate([np.full(c, e) for e, c in enumerate(g["tokens_per_expert"])])
+    np.random.default_rng(3).shuffle(experts)
+    r = moe.moe_route_indices(to_dev(experts[:, None].astype(np.int32)), None, 3)
+    assert to_host(r.group_list).tolist() == g["group_list"]
+
+
+@pytest.mark.parametrize("T,E,k,drop", [(1000, 64, 4, 0.2), (257, 256, 8, 0.5), (31, 5, 5, 0.0)])
+def test_route_indices_with_empty_slots(T, E, k, drop):
+    idx, w = wl.random_routing(T + E, T, E, k, empty_frac=drop)
+    r = moe.moe_route_indices(to_dev(idx), to_dev(w), E, routing_map=True)
+    torch.cuda.synchronize()
+    o = oracle.route_indices(idx, w, E)
+    for name in ("counts", "offsets", "group_list", "sorted_indices", "slot_pos",
+                 "routing_map", "permuted_probs"):
+        assert (to_host(getattr(r, name)) == o[name]).all(), name
+    assert moe.moe_workspace_status(r.workspace) == 0
+
+
+def test_route_indices_flags_invalid_ids():
+    idx = np.array([[0, 1], [1, 1], [2, 9], [-3, 0], [1, -1]], np.int32)
+    r = moe.moe_route_indices(to_dev(idx), None, 4)
+    assert moe.moe_workspace_status(r.workspace) == 6
+    clean = np.array([[0, 1], [1, -1], [2, -1], [-1, 0], [1, -1]], np.int32)
+    o = oracle.route_indices(clean, None, 4)
+    for name in ("counts", "offsets", "sorted_indices", "slot_pos"):
+        assert (to_host(getattr(r, name)) == o[name]).all(), name
+    # a clean call on the same workspace resets the status
+    moe.moe_route_indices(to_dev(clean), None, 4, workspace=r.workspace)
+    assert moe.moe_workspace_status(r.workspace) == 0
+
+
+# -------------------------------------------------------------------- permute
+
+@pytest.mark.parametrize("dtype,T,H,E,k", [("bf16", 1000, 4096, 64, 2), ("bf16", 257, 7168, 256, 8),
+                                           ("f32", 256, 128, 8, 2), ("bf16", 100, 13, 8, 3),
+                                           ("f32", 129, 7, 16, 4), ("bf16", 64, 8, 4, 4)])
+def test_permute_bit_exact(dtype, T, H, E, k):
+    x = wl.random_activation(T + H, (T, H), dtype)
+    idx, _ = wl.random_routing(T * 3 + k, T, E, k, empty_frac=0.1)
+    o = oracle.route_indices(idx, None, E)
+    n = int(o["offsets"][E])
+    r = moe.moe_route_indices(to_dev(idx), None, E)
+    got = to_host(moe.moe_permute(to_dev(x), r.slot_pos))
+    assert got[:n].tobytes() == oracle.permute(x, o["sorted_indices"], n).tobytes()
+
+
+def test_permute_then_unweighted_combine_k1_identity():
+    for dtype in ("bf16", "f32"):
+        T, H, E = 777, 1024, 16
+        x = wl.random_activation(5, (T, H), dtype)
+        idx, _ = wl.random_routing(6, T, E, 1)
+        r = moe.moe_route_indices(to_dev(idx), None, E)
+        xp = moe.moe_permute(to_dev(x), r.slot_pos)
+        back = moe.moe_combine(xp, r.slot_pos, None)
+        ones = moe.moe_combine(xp, r.slot_pos, torch.ones((T, 1), device="cuda"))
+        assert to_host(back).tobytes() == x.tobytes()
+        assert to_host(ones).tobytes() == x.tobytes()
+
+
+# -------------------------------------------------------------------- combine
+
+@pytest.mark.parametrize("dtype,T,H,E,k,drop,weighted",
+                         [("bf16", 1000, 4096, 64, 2, 0.0, True),
+                          ("bf16", 300, 7168, 256, 8, 0.1, True),
+                          ("bf16", 500, 1000, 32, 6, 0.2, False),
+                          ("bf16", 129, 36, 8, 3, 0.0, True),    # 72-byte rows: element path
+                          ("f32", 256, 128, 8, 2, 0.0, True),
+                          ("f32", 99, 33, 8, 5, 0.3, True),
+                          ("bf16", 64, 256, 40, 32, 0.1, True)])
+def test_combine_bit_exact(dtype, T, H, E, k, drop, weighted):
+    idx, w = wl.random_routing(T + 5 * k, T, E, k, empty_frac=drop)
+    if not weighted:
+        w = None
+    r = moe.moe_route_indices(to_dev(idx), None, E)
+    o = oracle.route_indices(idx, None, E)
+    y = wl.random_activation(H + k, (T * k, H), dtype)     # random signs: cancellation
+    out = to_host(moe.moe_combine(to_dev(y), r.slot_pos, None if w is None else to_dev(w)))
+    ref, ref64 = oracle.combine(y, o["slot_pos"], w)
+    if dtype == "bf16":
+        d = bf16_ulp_diff(out, ref)
+    else:
+        d = f32_ulp_diff(out, ref)
+    assert d.max() == 0, f"max ulp {d.max()}, {np.count_nonzero(d)} mismatches"
+
+
+def test_combine_deterministic_and_stable_across_calls():
+    T, H, E, k = 2000, 2048, 64, 8
+    idx, w = wl.random_routing(1, T, E, k)
+    r = moe.moe_route_indices(to_dev(idx), None, E)
+    y = to_dev(wl.random_activation(2, (T * k, H), "bf16"))
+    a = moe.moe_combine(y, r.slot_pos, to_dev(w))
+    b = moe.moe_combine(y, r.slot_pos, to_dev(w))
+    g = to_dev(wl.random_activation(3, (T, H), "bf16"))
+    ga, pa = moe.moe_combine_backward(g, y, r.slot_pos, to_dev(w))
+    gb, pb = moe.moe_combine_backward(g, y, r.slot_pos, to_dev(w))
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    assert torch.equal(ga.view(torch.int16), gb.view(torch.int16))
+    assert torch.equal(pa.view(torch.int32), pb.view(torch.int32))
+
+
+@pytest.mark.parametrize("dtype,T,H,E,k,drop,weighted",
+                         [("bf16", 600, 4096, 64, 2, 0.0, True),
+                          ("bf16", 300, 7168, 256, 8, 0.1, True),
+                          ("bf16", 200, 1000, 16, 4, 0.0, False),
+                          ("bf16", 77, 20, 8, 3, 0.2, True),     # element path
+                          ("f32", 256, 128, 8, 2, 0.0, True),
+                          ("f32", 50, 45, 6, 3, 0.2, True),
+                          ("bf16", 40, 512, 64, 32, 0.0, True)])
+def test_combine_backward(dtype, T, H, E, k, drop, weighted):
+    idx, w = wl.random_routing(T + k, T, E, k, empty_frac=drop)
+    if not weighted:
+        w = None
+    r = moe.moe_route_indices(to_dev(idx), None, E)
+    o = oracle.route_indices(idx, None, E)
+    n = int(o["offsets"][E])
+    y = wl.random_activation(11, (T * k, H), dtype)
+    g = wl.random_activation(12, (T, H), dtype)
+    gy, gp = moe.moe_combine_backward(to_dev(g), to_dev(y), r.slot_pos,
+                                      None if w is None else to_dev(w))
+    gy, gp = to_host(gy), to_host(gp)
+    gy_o, gp_o, gp64 = oracle.combine_backward(g, y, o["slot_pos"], w)
+    assert gy[:n].tobytes() == gy_o[:n].tobytes()
+    assert within_one_bf16_ulp(gp, gp64).all()
+    assert (gp[o["slot_pos"] < 0] == 0).all()
+    # in practice the compensated dot lands within a few float32 ulps
+    assert f32_ulp_diff(gp, gp_o).max() <= 64
+
+
+def test_expert_scale_bit_exact():
+    for dtype in ("bf16", "f32"):
+        T, H, E, k = 300, 520, 16, 4
+        idx, _ = wl.random_routing(4, T, E, k, empty_frac=0.1)
+        o = oracle.route_indices(idx, None, E)
+        r = moe.moe_route_indices(to_dev(idx), None, E)
+        x = wl.random_activation(5, (T * k, H), dtype)
+        scale = np.random.default_rng(6).uniform(-2, 2, E).astype(np.float32)
+        got = to_host(moe.moe_expert_scale(to_dev(x), r.offsets, to_dev(scale)))
+        ref = oracle.expert_scale(x, o["offsets"], scale)
+        n = int(o["offsets"][E])
+        assert got[:n].tobytes() == ref[:n].tobytes()
+
+
+# ---------------------------------------------------------------- sort_chunks
+
+def _virtual_rank_buffers(d, R=8, L=8):
+    """Rank-major receive buffers of each virtual rank from the oracle's
+    routing of 8 source slices (test infrastructure)."""
+    w_ = d["workload"]
+    T, k = w_.T, w_.k
+    per = T // R
+    idx, _, _ = oracle.topk_softmax(d["logits"], k)
+    bufs = []
+    for r_ in range(R):
+        M = np.zeros((R, L), np.int32)
+        rows = []
+        for src in range(R):
+            toks = np.arange(src * per, (src + 1) * per)
+            for le in range(L):
+                e = r_ * L + le
+                sel = toks[(idx[toks] == e).any(axis=1)]
+                M[src, le] = sel.size
+                rows.append(sel)
+        order = np.concatenate(rows)
+        bufs.append((M, np.ascontiguousarray(d["x"][order])))
+    return bufs
+
+
+def test_sort_chunks_virtual_ep8_round_trip():
+    d = wl.make("vep8")
+    R = L = 8
+    fwd = np.array(moe.moe_chunk_idxs(R, L, False), np.int32)
+    inv = np.array(moe.moe_chunk_idxs(R, L, True), np.int32)
+    for M, buf in _virtual_rank_buffers(d, R, L):
+        xd = to_dev(buf)
+        em = moe.moe_sort_chunks(xd, to_dev(M.ravel().copy()), to_dev(fwd))
+        back = moe.moe_sort_chunks(em, to_dev(M.T.ravel().copy()), to_dev(inv))
+        torch.cuda.synchronize()
+        assert moe.moe_workspace_status(em._moe_workspace) == 0
+        ref = oracle.sort_chunks(buf, M.ravel(), oracle.chunk_idxs(R, L, False))
+        assert to_host(em).tobytes() == ref.tobytes()
+        assert to_host(back).tobytes() == buf.tobytes()
+
+
+@pytest.mark.parametrize("R,L,H,dtype", [(3, 5, 100, "bf16"), (2, 2, 16, "f32"), (1, 9, 64, "bf16"),
+                                         (16, 16, 1024, "bf16")])
+def test_sort_chunks_asymmetric(R, L, H, dtype):
+    rng = np.random.default_rng(R * 100 + L)
+    M = rng.integers(0, 40, (R, L)).astype(np.int32)
+    M[0, -1] = 0
+    N = int(M.sum())
+    x = wl.random_activation(R + L, (N, H), dtype)
+    fwd = oracle.chunk_idxs(R, L, False)
+    em = moe.moe_sort_chunks(to_dev(x), to_dev(M.ravel().copy()), to_dev(fwd))
+    ref = oracle.sort_chunks(x, M.ravel(), fwd)
+    assert to_host(em).tobytes() == ref.tobytes()
+    back = moe.moe_sort_chunks(em, to_dev(M.T.ravel().copy()),
+                               to_dev(oracle.chunk_idxs(R, L, True)))
+    assert to_host(back).tobytes() == x.tobytes()
+
+
+def test_sort_chunks_rejects_bad_splits_on_device():
+    x = to_dev(wl.random_activation(1, (10, 64), "bf16"))
+    sentinel = torch.full_like(x, 3.0)
+    out = moe.moe_sort_chunks(x, to_dev(np.array([4, 4], np.int32)),
+                              to_dev(np.array([1, 0], np.int32)), out=sentinel.clone())
+    assert moe.moe_workspace_status(out._moe_workspace) == 6
+    assert torch.equal(out, sentinel)
+    out = moe.moe_sort_chunks(x, to_dev(np.array([4, 6], np.int32)),
+                              to_dev(np.array([1, 1], np.int32)), out=sentinel.clone())
+    assert moe.moe_workspace_status(out._moe_workspace) == 6
+
+
+# ------------------------------------------------------------------ pipelines
+
+def _pipeline_gpu(d, with_grad):
+    w_ = d["workload"]
+    r = moe.moe_route(to_dev(d["logits"]), w_.k)
+    xp = moe.moe_permute(to_dev(d["x"]), r.slot_pos)
+    y = moe.moe_expert_scale(xp, r.offsets, to_dev(d["scale"]))
+    out = moe.moe_combine(y, r.slot_pos, r.topk_w)
+    res = {"r": r, "xp": xp, "y": y, "out": out}
+    if with_grad:
+        res["gy"], res["gp"] = moe.moe_combine_backward(to_dev(d["grad_out"]), y, r.slot_pos,
+                                                        r.topk_w)
+    torch.cuda.synchronize()
+    return res
+
+
+@pytest.mark.parametrize("name", ["tiny", "mid"])
+def test_pipeline_full_compare(name):
+    d = wl.make(name)
+    w_ = d["workload"]
+    g = _pipeline_gpu(d, with_grad=False)
+    o = oracle.route(d["logits"], w_.k)
+    _assert_route_equal(g["r"], o, w_.E)
+    n = int(o["offsets"][w_.E])
+    xp_o = oracle.permute(d["x"], o["sorted_indices"], n)
+    assert to_host(g["xp"])[:n].tobytes() == xp_o.tobytes()
+    y_o = oracle.expert_scale(xp_o, o["offsets"], d["scale"])
+    assert to_host(g["y"])[:n].tobytes() == y_o.tobytes()
+    out_o, out64 = oracle.combine(y_o, o["slot_pos"], o["topk_w"])
+    got = to_host(g["out"])
+    # the two sides used their own softmax weights (within 1e-6): 1 ulp
+    if got.dtype == np.uint16:
+        assert bf16_ulp_diff(got, out_o).max() <= 1
+    else:
+        assert within_one_bf16_ulp(got, out64).all()
+    # round trip: the stand-in closed form out[t] = x[t] * sum_j w_j (e_j+1)/E.
+    # Each stand-in row is rounded once (relative 2^-9 in bf16, 2^-24 in f32)
+    # and the sum once more, so allow 2 ulps of the exact value.
+    factor = (o["topk_w_f64"] * (o["topk_idx"] + 1) / w_.E).sum(axis=1)
+    exact = wl.activation_to_f64(d["x"]) * factor[:, None]
+    err = np.abs(wl.activation_to_f64(got) - exact)
+    assert (err <= 2 * bf16_ulp_of(exact)).all()
+
+
+def test_pipeline_skewed_sampled():
+    """The DeepSeek-shaped workload at full size in the benchmark's launch
+    configuration; the oracle checks every routing output and a seeded sample
+    of tokens for the row outputs."""
+    d = wl.make("skewed", with_grad=True)
+    w_ = d["workload"]
+    g = _pipeline_gpu(d, with_grad=True)
+    o = oracle.route(d["logits"], w_.k)
+    _assert_route_equal(g["r"], o, w_.E)
+    counts = o["counts"]
+    assert (counts == 0).sum() > 0 and counts.max() > 4 * w_.N / w_.E   # skewed as intended
+    rng = np.random.default_rng(2024)
+    toks = np.sort(rng.choice(w_.T, 256, replace=False))
+    toks[-1] = w_.T - 1
+    sp = o["slot_pos"][toks]
+    rows = sp.ravel()
+    xp = to_host(g["xp"][torch.from_numpy(rows).long().cuda()])
+    assert (xp == d["x"][np.repeat(toks, w_.k)]).all()
+    y_rows = to_host(g["y"])                      # whole buffer, host copy
+    w_gpu = to_host(g["r"].topk_w)[toks]
+    # combine on the sampled tokens: same y and weights as the GPU used -> bit-exact
+    sp_local = np.arange(toks.size * w_.k, dtype=np.int32).reshape(toks.size, w_.k)
+    out_o, _ = oracle.combine(np.ascontiguousarray(y_rows[rows]), sp_local, w_gpu)
+    assert (to_host(g["out"])[toks] == out_o).all()
+    gy_o, gp_o, gp64 = oracle.combine_backward(np.ascontiguousarray(d["grad_out"][toks]),
+                                               np.ascontiguousarray(y_rows[rows]), sp_local, w_gpu)
+    assert (to_host(g["gy"][torch.from_numpy(rows).long().cuda()]) == gy_o).all()
+    assert within_one_bf16_ulp(to_host(g["gp"])[toks], gp64).all()

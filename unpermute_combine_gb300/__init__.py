@@ -1,0 +1,361 @@
+"""unpermute_combine_gb300 -- GB300 (sm_103a) MoE token dispatch/combine.
+
+A thin binding over libmoe's C ABI (include/moe.h), one Python function per C
+entry point with the same name.  It only marshals arguments: it checks
+devices, dtypes and shapes, allocates outputs and workspaces with torch, and
+passes raw pointers and the current CUDA stream.  Every step of the path runs
+in libmoe's CUDA kernels; there is no CPU or PyTorch fallback, and calling any
+op without the built library raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+from . import build as _build
+
+__all__ = [
+    "MoeError", "library_path", "load_library", "moe_abi_version", "moe_status_string",
+    "moe_route_workspace_size", "moe_route", "moe_route_indices", "moe_permute",
+    "moe_sort_chunks_workspace_size", "moe_sort_chunks", "moe_chunk_idxs", "moe_combine",
+    "moe_combine_backward", "moe_expert_scale", "moe_workspace_status", "RouteResult",
+]
+
+MOE_OK = 0
+_DT = {torch.float32: 0, torch.bfloat16: 1}
+
+
+class MoeError(RuntimeError):
+    def __init__(self, name, status):
+        self.status = status
+        super().__init__(f"{name} failed: {moe_status_string(status)} ({status})")
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load_library():
+    """Load libmoe.so (built in-tree by unpermute_combine_gb300.build)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(_build.LIB):
+            raise RuntimeError(
+                f"libmoe.so is not built ({_build.LIB}); run "
+                "`python -m unpermute_combine_gb300.build` or __graft_entry__.build()")
+        lib = ctypes.CDLL(_build.LIB)
+        P, I, I64, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
+        PSZ = ctypes.POINTER(ctypes.c_size_t)
+        sigs = {
+            "moe_status_string": ([I], ctypes.c_char_p),
+            "moe_abi_version": ([], I),
+            "moe_route_workspace_size": ([I64, I, I, PSZ], I),
+            "moe_route": ([P, I64, I, I, P, P, P, P, P, P, P, P, P, P, SZ, P], I),
+            "moe_route_indices": ([P, P, I64, I, I, P, P, P, P, P, P, P, P, SZ, P], I),
+            "moe_permute": ([P, I, I64, I64, I, P, P, P], I),
+            "moe_sort_chunks_workspace_size": ([I, PSZ], I),
+            "moe_sort_chunks": ([P, I, I64, I64, P, P, I, P, P, SZ, P], I),
+            "moe_chunk_idxs": ([I, I, I, P], I),
+            "moe_combine": ([P, I, I64, I64, I, P, P, P, P], I),
+            "moe_combine_backward": ([P, P, I, I64, I64, I, P, P, P, P, P], I),
+            "moe_expert_scale": ([P, I, I64, I64, I, P, P, P, P], I),
+            "moe_workspace_status": ([P, P], I),
+        }
+        for name, (args, res) in sigs.items():
+            fn = getattr(lib, name)
+            fn.argtypes = args
+            fn.restype = res
+        _lib = lib
+        return lib
+
+
+def moe_status_string(status: int) -> str:
+    return load_library().moe_status_string(int(status)).decode()
+
+
+def moe_abi_version() -> int:
+    return load_library().moe_abi_version()
+
+
+# ------------------------------------------------------------------ helpers
+
+def _p(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ok(name, status):
+    if status != MOE_OK:
+        raise MoeError(name, status)
+
+
+def _cuda(t, name, dtype=None, ndim=None):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got {t.dim()}")
+    return t
+
+
+def _act(t, name):
+    _cuda(t, name, ndim=2)
+    if t.dtype not in _DT:
+        raise ValueError(f"{name} must be float32 or bfloat16, got {t.dtype}")
+    return _DT[t.dtype]
+
+
+def _empty(shape, dtype, like):
+    return torch.empty(shape, dtype=dtype, device=like.device)
+
+
+def _workspace(nbytes, like, given):
+    if given is not None:
+        _cuda(given, "workspace", torch.uint8)
+        if given.numel() < nbytes:
+            raise ValueError(f"workspace needs {nbytes} bytes, got {given.numel()}")
+        return given
+    return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=like.device)
+
+
+# -------------------------------------------------------------------- route
+
+@dataclass
+class RouteResult:
+    topk_idx: Optional[torch.Tensor]
+    topk_w: Optional[torch.Tensor]
+    counts: torch.Tensor
+    offsets: torch.Tensor
+    group_list: torch.Tensor
+    sorted_indices: torch.Tensor
+    slot_pos: torch.Tensor
+    permuted_probs: Optional[torch.Tensor]
+    routing_map: Optional[torch.Tensor]
+    workspace: torch.Tensor
+
+
+def moe_route_workspace_size(T: int, E: int, k: int) -> int:
+    n = ctypes.c_size_t(0)
+    _ok("moe_route_workspace_size",
+        load_library().moe_route_workspace_size(T, E, k, ctypes.byref(n)))
+    return n.value
+
+
+def moe_route(logits: torch.Tensor, k: int, *, routing_map: bool = False,
+              workspace: Optional[torch.Tensor] = None, out: Optional[RouteResult] = None,
+              stream=None) -> RouteResult:
+    """Top-k + softmax over the k scores, counts, offsets/group_list,
+    expert-major sorted_indices, slot_pos and permuted_probs (moe.h)."""
+    _cuda(logits, "logits", torch.float32, 2)
+    T, E = logits.shape
+    ws_bytes = moe_route_workspace_size(T, E, k)
+    ws = _workspace(ws_bytes, logits, workspace if out is None else out.workspace)
+    if out is None:
+        i32 = torch.int32
+        out = RouteResult(
+            topk_idx=_empty((T, k), i32, logits), topk_w=_empty((T, k), torch.float32, logits),
+            counts=_empty((E,), i32, logits), offsets=_empty((E + 1,), i32, logits),
+            group_list=_empty((E,), i32, logits), sorted_indices=_empty((T * k,), i32, logits),
+            slot_pos=_empty((T, k), i32, logits),
+            permuted_probs=_empty((T * k,), torch.float32, logits),
+            routing_map=_empty((T, E), torch.uint8, logits) if routing_map else None,
+            workspace=ws)
+    _ok("moe_route", load_library().moe_route(
+        _p(logits), T, E, k, _p(out.topk_idx), _p(out.topk_w), _p(out.counts), _p(out.offsets),
+        _p(out.group_list), _p(out.sorted_indices), _p(out.slot_pos), _p(out.permuted_probs),
+        _p(out.routing_map), _p(ws), ws.numel(), _stream(stream)))
+    return out
+
+
+def moe_route_indices(topk_idx: torch.Tensor, topk_w: Optional[torch.Tensor], E: int, *,
+                      routing_map: bool = False, workspace: Optional[torch.Tensor] = None,
+                      stream=None) -> RouteResult:
+    """Index outputs of moe_route from given top-k choices (-1 = empty slot)."""
+    _cuda(topk_idx, "topk_idx", torch.int32, 2)
+    T, k = topk_idx.shape
+    if topk_w is not None:
+        _cuda(topk_w, "topk_w", torch.float32, 2)
+        if tuple(topk_w.shape) != (T, k):
+            raise ValueError("topk_w must match topk_idx")
+    ws = _workspace(moe_route_workspace_size(T, E, k), topk_idx, workspace)
+    i32 = torch.int32
+    r = RouteResult(
+        topk_idx=topk_idx, topk_w=topk_w, counts=_empty((E,), i32, topk_idx),
+        offsets=_empty((E + 1,), i32, topk_idx), group_list=_empty((E,), i32, topk_idx),
+        sorted_indices=_empty((T * k,), i32, topk_idx), slot_pos=_empty((T, k), i32, topk_idx),
+        permuted_probs=_empty((T * k,), torch.float32, topk_idx) if topk_w is not None else None,
+        routing_map=_empty((T, E), torch.uint8, topk_idx) if routing_map else None,
+        workspace=ws)
+    _ok("moe_route_indices", load_library().moe_route_indices(
+        _p(topk_idx), _p(topk_w), T, E, k, _p(r.counts), _p(r.offsets), _p(r.group_list),
+        _p(r.sorted_indices), _p(r.slot_pos), _p(r.permuted_probs), _p(r.routing_map), _p(ws),
+        ws.numel(), _stream(stream)))
+    return r
+
+
+# ------------------------------------------------------------------ permute
+
+def moe_permute(x: torch.Tensor, slot_pos: torch.Tensor, out: Optional[torch.Tensor] = None,
+                stream=None) -> torch.Tensor:
+    """permuted[slot_pos[t,j]] = x[t]; out has T*k rows (rows no slot names
+    are left as they were)."""
+    dt = _act(x, "x")
+    _cuda(slot_pos, "slot_pos", torch.int32, 2)
+    T, H = x.shape
+    k = slot_pos.shape[1]
+    if slot_pos.shape[0] != T:
+        raise ValueError("slot_pos must have one row per token")
+    if out is None:
+        out = _empty((T * k, H), x.dtype, x)
+    else:
+        _cuda(out, "out", x.dtype, 2)
+        if tuple(out.shape) != (T * k, H):
+            raise ValueError("out must be [T*k, H]")
+    _ok("moe_permute", load_library().moe_permute(_p(x), dt, T, H, k, _p(slot_pos), _p(out),
+                                                  _stream(stream)))
+    return out
+
+
+# -------------------------------------------------------------- sort_chunks
+
+def moe_sort_chunks_workspace_size(C: int) -> int:
+    n = ctypes.c_size_t(0)
+    _ok("moe_sort_chunks_workspace_size",
+        load_library().moe_sort_chunks_workspace_size(C, ctypes.byref(n)))
+    return n.value
+
+
+def moe_sort_chunks(x: torch.Tensor, split_sizes: torch.Tensor, sorted_idxs: torch.Tensor,
+                    out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                    stream=None) -> torch.Tensor:
+    """out = cat([x.split(split_sizes)[i] for i in sorted_idxs]); split_sizes
+    and sorted_idxs are int32 CUDA tensors (no host synchronisation)."""
+    dt = _act(x, "x")
+    _cuda(split_sizes, "split_sizes", torch.int32, 1)
+    _cuda(sorted_idxs, "sorted_idxs", torch.int32, 1)
+    C = split_sizes.numel()
+    if sorted_idxs.numel() != C:
+        raise ValueError("split_sizes and sorted_idxs must have the same length")
+    N, H = x.shape
+    if out is None:
+        out = torch.empty_like(x)
+    else:
+        _cuda(out, "out", x.dtype, 2)
+        if out.shape != x.shape:
+            raise ValueError("out must match x")
+    ws = _workspace(moe_sort_chunks_workspace_size(C), x, workspace)
+    _ok("moe_sort_chunks", load_library().moe_sort_chunks(
+        _p(x), dt, N, H, _p(split_sizes), _p(sorted_idxs), C, _p(out), _p(ws), ws.numel(),
+        _stream(stream)))
+    out._moe_workspace = ws  # keeps the status word reachable for moe_workspace_status
+    return out
+
+
+def moe_chunk_idxs(R: int, L: int, inverse: bool = False) -> list:
+    """Host helper: rank-major -> expert-major chunk order of an [R x L] split
+    matrix (inverse=True: the way back, used with the transposed splits)."""
+    buf = (ctypes.c_int32 * (R * L))()
+    _ok("moe_chunk_idxs", load_library().moe_chunk_idxs(R, L, int(bool(inverse)), buf))
+    return list(buf)
+
+
+# ------------------------------------------------------------------ combine
+
+def moe_combine(expert_out: torch.Tensor, slot_pos: torch.Tensor,
+                topk_w: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
+                stream=None) -> torch.Tensor:
+    """out[t] = sum_j topk_w[t,j] * expert_out[slot_pos[t,j]] (topk_w=None: plain sum)."""
+    dt = _act(expert_out, "expert_out")
+    _cuda(slot_pos, "slot_pos", torch.int32, 2)
+    T, k = slot_pos.shape
+    H = expert_out.shape[1]
+    if expert_out.shape[0] != T * k:
+        raise ValueError("expert_out must have T*k rows")
+    if topk_w is not None:
+        _cuda(topk_w, "topk_w", torch.float32, 2)
+        if tuple(topk_w.shape) != (T, k):
+            raise ValueError("topk_w must be [T, k]")
+    if out is None:
+        out = _empty((T, H), expert_out.dtype, expert_out)
+    else:
+        _cuda(out, "out", expert_out.dtype, 2)
+        if tuple(out.shape) != (T, H):
+            raise ValueError("out must be [T, H]")
+    _ok("moe_combine", load_library().moe_combine(
+        _p(expert_out), dt, T, H, k, _p(slot_pos), _p(topk_w), _p(out), _stream(stream)))
+    return out
+
+
+def moe_combine_backward(grad_out: torch.Tensor, expert_out: torch.Tensor,
+                         slot_pos: torch.Tensor, topk_w: Optional[torch.Tensor] = None,
+                         grad_expert_out: Optional[torch.Tensor] = None,
+                         grad_probs: Optional[torch.Tensor] = None, stream=None):
+    """(grad_expert_out, grad_probs) of the combine; rows no slot names are
+    left as they were."""
+    dt = _act(expert_out, "expert_out")
+    _act(grad_out, "grad_out")
+    if grad_out.dtype != expert_out.dtype:
+        raise ValueError("grad_out and expert_out must share a dtype")
+    _cuda(slot_pos, "slot_pos", torch.int32, 2)
+    T, k = slot_pos.shape
+    H = expert_out.shape[1]
+    if tuple(grad_out.shape) != (T, H) or expert_out.shape[0] != T * k:
+        raise ValueError("grad_out must be [T, H] and expert_out [T*k, H]")
+    if topk_w is not None:
+        _cuda(topk_w, "topk_w", torch.float32, 2)
+    if grad_expert_out is None:
+        grad_expert_out = torch.empty_like(expert_out)
+    else:
+        _cuda(grad_expert_out, "grad_expert_out", expert_out.dtype, 2)
+    if grad_probs is None:
+        grad_probs = _empty((T, k), torch.float32, expert_out)
+    else:
+        _cuda(grad_probs, "grad_probs", torch.float32, 2)
+    _ok("moe_combine_backward", load_library().moe_combine_backward(
+        _p(grad_out), _p(expert_out), dt, T, H, k, _p(slot_pos), _p(topk_w),
+        _p(grad_expert_out), _p(grad_probs), _stream(stream)))
+    return grad_expert_out, grad_probs
+
+
+# ---------------------------------------------------------- stand-in expert
+
+def moe_expert_scale(x_perm: torch.Tensor, offsets: torch.Tensor, scale: torch.Tensor,
+                     out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """out[p] = x_perm[p] * scale[e] over the expert segments given by offsets."""
+    dt = _act(x_perm, "x_perm")
+    _cuda(offsets, "offsets", torch.int32, 1)
+    _cuda(scale, "scale", torch.float32, 1)
+    E = scale.numel()
+    if offsets.numel() != E + 1:
+        raise ValueError("offsets must have E+1 entries")
+    n, H = x_perm.shape
+    if out is None:
+        out = torch.empty_like(x_perm)
+    _ok("moe_expert_scale", load_library().moe_expert_scale(
+        _p(x_perm), dt, n, H, E, _p(offsets), _p(scale), _p(out), _stream(stream)))
+    return out
+
+
+def moe_workspace_status(workspace: torch.Tensor, stream=None) -> int:
+    """Synchronise the stream and return the status word a call left in the
+    workspace (0 = MOE_OK, 6 = MOE_ERR_DEVICE_CHECK, 5 = MOE_ERR_TIMEOUT)."""
+    _cuda(workspace, "workspace", torch.uint8)
+    return load_library().moe_workspace_status(_p(workspace), _stream(stream))

@@ -1,0 +1,506 @@
+// combine.cu -- moe_combine and moe_combine_backward.
+//
+// The combine of "03 · Combine 与 forward / backward 对称性" §1,
+//   out[t] = sum_j w[t,j] * y[slot_pos[t,j]],
+// done as a deterministic gather-reduce (one warp per token reads its k rows
+// and writes one) instead of the scatter-add of §2.3.
+//
+// Accuracy contract: the result is the double-precision slot-order sum
+// rounded once to the output type.  The fast path accumulates s = sum w*y
+// with float FMAs in slot order together with a = sum |w|*|y|.  The float
+// error of s is at most k*2^-24*(1+2^-15)*a (plus the double sum's own error,
+// far smaller), so if the whole interval [s-B, s+B] rounds to a single bf16
+// value, that value is the rounding of the double sum (rounding is monotone).
+// Elements whose interval straddles a rounding boundary -- about 2^-12 of them
+// on typical data -- are recomputed in double in the same slot order.
+// float32 outputs always take the double path.
+//
+// The backward (§4): grad_y[slot_pos[t,j]] = w[t,j]*grad_out[t] is the exact
+// product rounded once (float product plus an error-free tie check), and
+// grad_probs[t,j] = <grad_out[t], y[slot_pos[t,j]]> is a double-float
+// (Knuth TwoSum) accumulation per lane followed by a fixed butterfly of
+// double-float additions, so it is deterministic and far more accurate than
+// a plain float dot.
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr uint32_t kFull = 0xFFFFFFFFu;
+
+int grid_for(const void* kernel, int threads, int64_t work_blocks) {
+    int per_sm = 0;
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, 0);
+    if (per_sm < 1) per_sm = 1;
+    const int64_t cap = int64_t(sm_count()) * per_sm;
+    return int(work_blocks < cap ? (work_blocks > 0 ? work_blocks : 1) : cap);
+}
+
+// Float error bound factor for a k-term FMA chain, rounded up (see header).
+float combine_bound_factor(int k) { return float(k) * 0x1p-24f * (1.0f + 0x1p-15f); }
+
+// Stage the token's slot rows and weights in shared memory (lanes < k).
+__device__ __forceinline__ void stage_slots(int32_t* s_pos, float* s_w, const int32_t* slot_pos,
+                                            const float* topk_w, int64_t t, int k,
+                                            int64_t n_rows, int lane) {
+    if (lane < k) {
+        const int32_t p = slot_pos[t * k + lane];
+        s_pos[lane] = (p >= 0 && p < n_rows) ? p : -1;
+        s_w[lane] = topk_w ? topk_w[t * k + lane] : 1.0f;
+    }
+    __syncwarp();
+}
+
+// -------------------------------------------------------- combine, bf16 rows
+
+constexpr int kU = 2;   // 16-byte vectors per lane per batch
+constexpr int kJ = 4;   // slot rows loaded per batch
+
+__device__ __forceinline__ float unpack_bf16(const uint4& d, int i) {
+    const uint32_t w = i < 2 ? d.x : i < 4 ? d.y : i < 6 ? d.z : d.w;
+    return (i & 1) ? bf16hi_to_f32(w) : bf16lo_to_f32(w);
+}
+
+__device__ __forceinline__ void set_word(uint4& d, int q, uint32_t v) {
+    if (q == 0) d.x = v; else if (q == 1) d.y = v; else if (q == 2) d.z = v; else d.w = v;
+}
+
+// Double path for one bf16 element: exact slot order, one rounding.
+__device__ __noinline__ uint16_t combine_elem_f64_bf16(const uint16_t* y, int64_t H, int64_t h,
+                                                       const int32_t* s_pos, const float* s_w,
+                                                       int k) {
+    double acc = 0.0;
+    for (int j = 0; j < k; ++j) {
+        const int32_t p = s_pos[j];
+        if (p < 0) continue;
+        acc = fma(double(s_w[j]), double(bf16_to_f32(y[int64_t(p) * H + h])), acc);
+    }
+    return f64_to_bf16_rn(acc);
+}
+
+__global__ void __launch_bounds__(kThreads)
+combine_bf16_vec_kernel(const uint4* __restrict__ y, int64_t T, int64_t nvec, int k,
+                        const int32_t* __restrict__ slot_pos, const float* __restrict__ topk_w,
+                        uint4* __restrict__ out, float cbound) {
+    __shared__ int32_t s_pos[kWarps][kMaxTopK];
+    __shared__ float s_w[kWarps][kMaxTopK];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t n_rows = T * k;
+    const int64_t H = nvec * 8;
+    for (int64_t t = int64_t(blockIdx.x) * kWarps + warp; t < T;
+         t += int64_t(gridDim.x) * kWarps) {
+        stage_slots(s_pos[warp], s_w[warp], slot_pos, topk_w, t, k, n_rows, lane);
+        for (int64_t v0 = lane; v0 < nvec; v0 += 32 * kU) {
+            float s[kU][8], a[kU][8];
+#pragma unroll
+            for (int u = 0; u < kU; ++u)
+#pragma unroll
+                for (int i = 0; i < 8; ++i) { s[u][i] = 0.0f; a[u][i] = 0.0f; }
+            for (int j0 = 0; j0 < k; j0 += kJ) {
+                uint4 d[kJ][kU];
+#pragma unroll
+                for (int jj = 0; jj < kJ; ++jj) {
+                    const int j = j0 + jj;
+                    const int32_t p = j < k ? s_pos[warp][j] : -1;
+#pragma unroll
+                    for (int u = 0; u < kU; ++u) {
+                        const int64_t v = v0 + 32 * u;
+                        d[jj][u] = (p >= 0 && v < nvec) ? __ldcs(y + int64_t(p) * nvec + v)
+                                                        : make_uint4(0, 0, 0, 0);
+                    }
+                }
+#pragma unroll
+                for (int jj = 0; jj < kJ; ++jj) {
+                    const int j = j0 + jj;
+                    if (j >= k || s_pos[warp][j] < 0) continue;
+                    const float w = s_w[warp][j];
+                    const float aw = fabsf(w);
+#pragma unroll
+                    for (int u = 0; u < kU; ++u)
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const float yv = unpack_bf16(d[jj][u], i);
+                            s[u][i] = __fmaf_rn(w, yv, s[u][i]);
+                            a[u][i] = __fmaf_rn(aw, fabsf(yv), a[u][i]);
+                        }
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < kU; ++u) {
+                const int64_t v = v0 + 32 * u;
+                if (v >= nvec) continue;
+                uint4 res;
+                uint32_t open = 0;           // bit q: word q not certified
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const float b0 = __fmaf_ru(a[u][2 * q], cbound, 0x1p-126f);
+                    const float b1 = __fmaf_ru(a[u][2 * q + 1], cbound, 0x1p-126f);
+                    const uint32_t lo = pack_bf16x2_rn(__fsub_rd(s[u][2 * q], b0),
+                                                       __fsub_rd(s[u][2 * q + 1], b1));
+                    const uint32_t hi = pack_bf16x2_rn(__fadd_ru(s[u][2 * q], b0),
+                                                       __fadd_ru(s[u][2 * q + 1], b1));
+                    set_word(res, q, lo);
+                    if (lo != hi) open |= 1u << q;
+                }
+                if (open) {
+                    const uint16_t* yb = reinterpret_cast<const uint16_t*>(y);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        if (!(open & (1u << q))) continue;
+                        const int64_t h = v * 8 + 2 * q;
+                        const uint32_t e0 = combine_elem_f64_bf16(yb, H, h, s_pos[warp], s_w[warp], k);
+                        const uint32_t e1 = combine_elem_f64_bf16(yb, H, h + 1, s_pos[warp], s_w[warp], k);
+                        set_word(res, q, e0 | (e1 << 16));
+                    }
+                }
+                __stcs(out + t * nvec + v, res);
+            }
+        }
+        __syncwarp();
+    }
+}
+
+// ---------------------------------------------- combine, element-wise paths
+// float32 rows (any alignment) and bf16 rows that are not 16-byte multiples:
+// the double slot-order sum, rounded once.
+template <typename E>
+__global__ void __launch_bounds__(kThreads)
+combine_elem_kernel(const E* __restrict__ y, int64_t T, int64_t H, int k,
+                    const int32_t* __restrict__ slot_pos, const float* __restrict__ topk_w,
+                    E* __restrict__ out) {
+    __shared__ int32_t s_pos[kWarps][kMaxTopK];
+    __shared__ float s_w[kWarps][kMaxTopK];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t n_rows = T * k;
+    for (int64_t t = int64_t(blockIdx.x) * kWarps + warp; t < T;
+         t += int64_t(gridDim.x) * kWarps) {
+        stage_slots(s_pos[warp], s_w[warp], slot_pos, topk_w, t, k, n_rows, lane);
+        for (int64_t h = lane; h < H; h += 32) {
+            double acc = 0.0;
+            for (int j = 0; j < k; ++j) {
+                const int32_t p = s_pos[warp][j];
+                if (p < 0) continue;
+                double yv;
+                if constexpr (sizeof(E) == 4) yv = double(y[int64_t(p) * H + h]);
+                else yv = double(bf16_to_f32(y[int64_t(p) * H + h]));
+                acc = fma(double(s_w[warp][j]), yv, acc);
+            }
+            if constexpr (sizeof(E) == 4) out[t * H + h] = f64_to_f32_rn(acc);
+            else out[t * H + h] = f64_to_bf16_rn(acc);
+        }
+        __syncwarp();
+    }
+}
+
+// ---------------------------------------------------------------- backward
+
+// Knuth TwoSum: s + e == a + b exactly.
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
+    s = __fadd_rn(a, b);
+    const float bp = __fsub_rn(s, a);
+    e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bp)), __fsub_rn(b, bp));
+}
+
+// Double-float accumulate: (hi, lo) += q.
+__device__ __forceinline__ void dd_add1(float& hi, float& lo, float q) {
+    float s, e;
+    two_sum(hi, q, s, e);
+    hi = s;
+    lo = __fadd_rn(lo, e);
+}
+
+// Butterfly sum of a double-float over the warp; every lane ends with the
+// same bits (TwoSum's error term does not depend on operand order).
+__device__ __forceinline__ float dd_warp_sum(float hi, float lo) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const float h2 = __shfl_xor_sync(kFull, hi, off);
+        const float l2 = __shfl_xor_sync(kFull, lo, off);
+        float s, e;
+        two_sum(hi, h2, s, e);
+        e = __fadd_rn(e, __fadd_rn(lo, l2));
+        hi = __fadd_rn(s, e);
+        lo = __fsub_rn(e, __fsub_rn(hi, s));
+    }
+    return __fadd_rn(hi, lo);
+}
+
+// bf16 of the exact product a*b (see expert_scale in permute.cu for the
+// argument): the float product rounds correctly unless it sits on a midpoint.
+__device__ __forceinline__ uint32_t mul_bf16_rn_bits(float a, float b) {
+    const float p = __fmul_rn(a, b);
+    const uint32_t u = __float_as_uint(p);
+    if ((u & 0xFFFFu) == 0x8000u) {
+        const float e = __fmaf_rn(a, b, -p);
+        if (e != 0.0f) {
+            const bool same = ((__float_as_uint(e) ^ u) & 0x80000000u) == 0;
+            return (same ? u + 0x8000u : u - 0x8000u) >> 16;
+        }
+    }
+    return f32_to_bf16_rn(p);
+}
+
+// Two floats in one 64-bit register (low word = even element): Blackwell's
+// packed f32x2 add/sub/mul run two lanes of float arithmetic per instruction.
+typedef unsigned long long f2_t;
+
+__device__ __forceinline__ f2_t f2_pack(float lo, float hi) {
+    f2_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2_unpack(f2_t v, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ f2_t f2_add(f2_t a, f2_t b) {
+    f2_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ f2_t f2_sub(f2_t a, f2_t b) {
+    f2_t r;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ f2_t f2_mul(f2_t a, f2_t b) {
+    f2_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+// bf16 pair (low half = even element) -> two floats
+__device__ __forceinline__ f2_t f2_from_bf16x2(uint32_t p) {
+    return f2_pack(bf16lo_to_f32(p), bf16hi_to_f32(p));
+}
+// Knuth TwoSum on both lanes: (hi, lo) += q with the rounding error of
+// hi + q kept exactly in lo's input.
+__device__ __forceinline__ void f2_two_sum_acc(f2_t& hi, f2_t& lo, f2_t q) {
+    const f2_t s = f2_add(hi, q);
+    const f2_t bp = f2_sub(s, hi);
+    const f2_t e = f2_add(f2_sub(hi, f2_sub(s, bp)), f2_sub(q, bp));
+    hi = s;
+    lo = f2_add(lo, e);
+}
+
+// w * (g0, g1) -> bf16 pair of the exact products.  The packed float products
+// are correctly rounded floats; a bf16 midpoint (low half 0x8000) in either
+// one sends the pair to the error-free tie break.
+__device__ __forceinline__ uint32_t scale_pair_bf16_f2(f2_t w2, f2_t g2) {
+    float p0, p1;
+    f2_unpack(f2_mul(w2, g2), p0, p1);
+    const uint32_t lows = __byte_perm(__float_as_uint(p0), __float_as_uint(p1), 0x5410) ^ 0x80008000u;
+    if (((lows - 0x00010001u) & ~lows & 0x80008000u) != 0) {   // a half equal to 0x8000
+        float w, w_hi, g0, g1;
+        f2_unpack(w2, w, w_hi);
+        f2_unpack(g2, g0, g1);
+        return mul_bf16_rn_bits(w, g0) | (mul_bf16_rn_bits(w, g1) << 16);
+    }
+    return pack_bf16x2_rn(p0, p1);
+}
+
+// k <= 8: every slot row of the current 16-byte column is loaded before any
+// arithmetic, so a lane keeps k loads in flight.
+template <int KMAX>
+__global__ void __launch_bounds__(kThreads)
+combine_bwd_bf16_vec_kernel(const uint4* __restrict__ gout, const uint4* __restrict__ y,
+                            int64_t T, int64_t nvec, int k, const int32_t* __restrict__ slot_pos,
+                            const float* __restrict__ topk_w, uint4* __restrict__ gy,
+                            float* __restrict__ grad_probs) {
+    static_assert(KMAX <= 8, "packed accumulators for up to 8 slots");
+    __shared__ int32_t s_pos[kWarps][kMaxTopK];
+    __shared__ float s_w[kWarps][kMaxTopK];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t n_rows = T * k;
+    for (int64_t t = int64_t(blockIdx.x) * kWarps + warp; t < T;
+         t += int64_t(gridDim.x) * kWarps) {
+        stage_slots(s_pos[warp], s_w[warp], slot_pos, topk_w, t, k, n_rows, lane);
+        int32_t pj[KMAX];
+        f2_t wj[KMAX], hi[KMAX], lo[KMAX];
+#pragma unroll
+        for (int j = 0; j < KMAX; ++j) {
+            pj[j] = j < k ? s_pos[warp][j] : -1;
+            const float w = j < k ? s_w[warp][j] : 0.0f;
+            wj[j] = f2_pack(w, w);
+            hi[j] = 0ull;
+            lo[j] = 0ull;
+        }
+        for (int64_t v = lane; v < nvec; v += 32) {
+            const uint4 gv = __ldcs(gout + t * nvec + v);
+            uint4 yv[KMAX];
+#pragma unroll
+            for (int j = 0; j < KMAX; ++j)
+                yv[j] = pj[j] >= 0 ? __ldcs(y + int64_t(pj[j]) * nvec + v) : make_uint4(0, 0, 0, 0);
+            const f2_t g0 = f2_from_bf16x2(gv.x), g1 = f2_from_bf16x2(gv.y);
+            const f2_t g2 = f2_from_bf16x2(gv.z), g3 = f2_from_bf16x2(gv.w);
+#pragma unroll
+            for (int j = 0; j < KMAX; ++j) {
+                if (pj[j] < 0) continue;
+                uint4 r;
+                r.x = scale_pair_bf16_f2(wj[j], g0);
+                r.y = scale_pair_bf16_f2(wj[j], g1);
+                r.z = scale_pair_bf16_f2(wj[j], g2);
+                r.w = scale_pair_bf16_f2(wj[j], g3);
+                __stcs(gy + int64_t(pj[j]) * nvec + v, r);
+                // bf16 x bf16 products have 16 significant bits: exact in float
+                f2_two_sum_acc(hi[j], lo[j], f2_mul(g0, f2_from_bf16x2(yv[j].x)));
+                f2_two_sum_acc(hi[j], lo[j], f2_mul(g1, f2_from_bf16x2(yv[j].y)));
+                f2_two_sum_acc(hi[j], lo[j], f2_mul(g2, f2_from_bf16x2(yv[j].z)));
+                f2_two_sum_acc(hi[j], lo[j], f2_mul(g3, f2_from_bf16x2(yv[j].w)));
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < KMAX; ++j) {
+            if (j >= k) break;
+            float h0, h1, l0, l1;
+            f2_unpack(hi[j], h0, h1);
+            f2_unpack(lo[j], l0, l1);
+            float s, e;
+            two_sum(h0, h1, s, e);                     // fold the odd lane into the even one
+            e = __fadd_rn(e, __fadd_rn(l0, l1));
+            const float r = dd_warp_sum(s, e);
+            if (lane == 0) grad_probs[t * k + j] = pj[j] >= 0 ? r : 0.0f;
+        }
+        __syncwarp();
+    }
+}
+
+// Element-wise backward (float32 rows, or bf16 rows that are not 16-byte
+// multiples): same arithmetic, one element per lane step.
+template <typename E, int KMAX>
+__global__ void __launch_bounds__(kThreads)
+combine_bwd_elem_kernel(const E* __restrict__ gout, const E* __restrict__ y, int64_t T,
+                        int64_t H, int k, const int32_t* __restrict__ slot_pos,
+                        const float* __restrict__ topk_w, E* __restrict__ gy,
+                        float* __restrict__ grad_probs) {
+    __shared__ int32_t s_pos[kWarps][kMaxTopK];
+    __shared__ float s_w[kWarps][kMaxTopK];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t n_rows = T * k;
+    for (int64_t t = int64_t(blockIdx.x) * kWarps + warp; t < T;
+         t += int64_t(gridDim.x) * kWarps) {
+        stage_slots(s_pos[warp], s_w[warp], slot_pos, topk_w, t, k, n_rows, lane);
+        float hi[KMAX], lo[KMAX];
+#pragma unroll
+        for (int j = 0; j < KMAX; ++j) { hi[j] = 0.0f; lo[j] = 0.0f; }
+        for (int64_t h = lane; h < H; h += 32) {
+            float g;
+            if constexpr (sizeof(E) == 4) g = gout[t * H + h];
+            else g = bf16_to_f32(gout[t * H + h]);
+#pragma unroll
+            for (int j = 0; j < KMAX; ++j) {
+                if (j >= k) break;
+                const int32_t p = s_pos[warp][j];
+                if (p < 0) continue;
+                const float w = s_w[warp][j];
+                const int64_t at = int64_t(p) * H + h;
+                float yv;
+                if constexpr (sizeof(E) == 4) {
+                    yv = y[at];
+                    gy[at] = __fmul_rn(w, g);
+                    const float q = __fmul_rn(g, yv);
+                    const float eq = __fmaf_rn(g, yv, -q);     // exact product = q + eq
+                    dd_add1(hi[j], lo[j], q);
+                    lo[j] = __fadd_rn(lo[j], eq);
+                } else {
+                    yv = bf16_to_f32(y[at]);
+                    gy[at] = uint16_t(mul_bf16_rn_bits(w, g));
+                    dd_add1(hi[j], lo[j], __fmul_rn(g, yv));
+                }
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < KMAX; ++j) {
+            if (j >= k) break;
+            const float r = dd_warp_sum(hi[j], lo[j]);
+            if (lane == 0) grad_probs[t * k + j] = s_pos[warp][j] >= 0 ? r : 0.0f;
+        }
+        __syncwarp();
+    }
+}
+
+moe_status_t check_common(const void* a, const void* b, moe_dtype_t dtype, int64_t T, int64_t H,
+                          int k, const int32_t* slot_pos) {
+    if (!dtype_ok(dtype) || T < 0 || H < 0 || k < 1) return MOE_ERR_INVALID_ARG;
+    if (k > kMaxTopK || T * int64_t(k) >= (int64_t(1) << 31)) return MOE_ERR_UNSUPPORTED;
+    if (T > 0 && (!slot_pos || (H > 0 && (!a || !b)))) return MOE_ERR_INVALID_ARG;
+    return MOE_OK;
+}
+
+template <int KMAX>
+void launch_bwd(const void* gout, const void* y, moe_dtype_t dtype, int64_t T, int64_t H, int k,
+                const int32_t* slot_pos, const float* topk_w, void* gy, float* gp,
+                bool vec, cudaStream_t s) {
+    const int64_t want = (T + kWarps - 1) / kWarps;
+    if (vec && KMAX <= 8) {
+        const auto kern = combine_bwd_bf16_vec_kernel<(KMAX <= 8 ? KMAX : 8)>;
+        kern<<<grid_for((const void*)kern, kThreads, want), kThreads, 0, s>>>(
+            static_cast<const uint4*>(gout), static_cast<const uint4*>(y), T, H / 8, k, slot_pos,
+            topk_w, static_cast<uint4*>(gy), gp);
+    } else if (dtype == MOE_F32) {
+        const auto kern = combine_bwd_elem_kernel<float, KMAX>;
+        kern<<<grid_for((const void*)kern, kThreads, want), kThreads, 0, s>>>(
+            static_cast<const float*>(gout), static_cast<const float*>(y), T, H, k, slot_pos,
+            topk_w, static_cast<float*>(gy), gp);
+    } else {
+        const auto kern = combine_bwd_elem_kernel<uint16_t, KMAX>;
+        kern<<<grid_for((const void*)kern, kThreads, want), kThreads, 0, s>>>(
+            static_cast<const uint16_t*>(gout), static_cast<const uint16_t*>(y), T, H, k,
+            slot_pos, topk_w, static_cast<uint16_t*>(gy), gp);
+    }
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" moe_status_t moe_combine(const void* expert_out, moe_dtype_t dtype, int64_t T,
+                                    int64_t H, int k, const int32_t* slot_pos,
+                                    const float* topk_w, void* out, void* stream) {
+    const moe_status_t st = check_common(expert_out, out, dtype, T, H, k, slot_pos);
+    if (st != MOE_OK) return st;
+    if (T == 0 || H == 0) return MOE_OK;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int64_t want = (T + kWarps - 1) / kWarps;
+    const size_t row = size_t(H) * elem_size(dtype);
+    if (dtype == MOE_BF16 && row % 16 == 0 && aligned16(expert_out) && aligned16(out)) {
+        combine_bf16_vec_kernel<<<grid_for((const void*)combine_bf16_vec_kernel, kThreads, want),
+                                  kThreads, 0, s>>>(
+            static_cast<const uint4*>(expert_out), T, H / 8, k, slot_pos, topk_w,
+            static_cast<uint4*>(out), combine_bound_factor(k));
+    } else if (dtype == MOE_F32) {
+        const auto kern = combine_elem_kernel<float>;
+        kern<<<grid_for((const void*)kern, kThreads, want), kThreads, 0, s>>>(
+            static_cast<const float*>(expert_out), T, H, k, slot_pos, topk_w,
+            static_cast<float*>(out));
+    } else {
+        const auto kern = combine_elem_kernel<uint16_t>;
+        kern<<<grid_for((const void*)kern, kThreads, want), kThreads, 0, s>>>(
+            static_cast<const uint16_t*>(expert_out), T, H, k, slot_pos, topk_w,
+            static_cast<uint16_t*>(out));
+    }
+    return launch_status();
+}
+
+extern "C" moe_status_t moe_combine_backward(const void* grad_out, const void* expert_out,
+                                             moe_dtype_t dtype, int64_t T, int64_t H, int k,
+                                             const int32_t* slot_pos, const float* topk_w,
+                                             void* grad_expert_out, float* grad_probs,
+                                             void* stream) {
+    moe_status_t st = check_common(grad_out, expert_out, dtype, T, H, k, slot_pos);
+    if (st != MOE_OK) return st;
+    if (T == 0) return MOE_OK;
+    if (!grad_probs || (H > 0 && !grad_expert_out)) return MOE_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t row = size_t(H) * elem_size(dtype);
+    const bool vec = dtype == MOE_BF16 && row % 16 == 0 && aligned16(grad_out) &&
+                     aligned16(expert_out) && aligned16(grad_expert_out);
+    if (k <= 1) launch_bwd<1>(grad_out, expert_out, dtype, T, H, k, slot_pos, topk_w, grad_expert_out, grad_probs, vec, s);
+    else if (k <= 2) launch_bwd<2>(grad_out, expert_out, dtype, T, H, k, slot_pos, topk_w, grad_expert_out, grad_probs, vec, s);
+    else if (k <= 4) launch_bwd<4>(grad_out, expert_out, dtype, T, H, k, slot_pos, topk_w, grad_expert_out, grad_probs, vec, s);
+    else if (k <= 8) launch_bwd<8>(grad_out, expert_out, dtype, T, H, k, slot_pos, topk_w, grad_expert_out, grad_probs, vec, s);
+    else if (k <= 16) launch_bwd<16>(grad_out, expert_out, dtype, T, H, k, slot_pos, topk_w, grad_expert_out, grad_probs, vec, s);
+    else launch_bwd<32>(grad_out, expert_out, dtype, T, H, k, slot_pos, topk_w, grad_expert_out, grad_probs, vec, s);
+    return launch_status();
+}

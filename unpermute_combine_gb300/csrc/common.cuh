@@ -1,0 +1,101 @@
+// common.cuh -- helpers shared by the libmoe CUDA sources (sm_103a only).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "moe.h"
+
+namespace moe {
+
+// ------------------------------------------------------------------ host side
+
+constexpr int kMaxTopK = 32;
+constexpr int kMaxExperts = 1024;
+constexpr size_t kWsAlign = 256;
+
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+inline size_t elem_size(moe_dtype_t d) { return d == MOE_F32 ? 4 : 2; }
+
+inline bool dtype_ok(int d) { return d == MOE_F32 || d == MOE_BF16; }
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Number of SMs of the current device (cached per device id).
+int sm_count();
+
+// Launch-error check after a kernel launch.
+inline moe_status_t launch_status() {
+    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+// Workspace header: the first 256 bytes of every workspace.
+struct WsHeader {
+    uint32_t status;      // moe_status_t of the last call that used the workspace
+    uint32_t detail;      // call-specific detail (first offending index, ...)
+    uint32_t reserved[62];
+};
+static_assert(sizeof(WsHeader) == kWsAlign, "header is one alignment unit");
+
+// --------------------------------------------------------------- device side
+
+// bf16 <-> f32 on packed pairs (bit manipulation; exact).
+__device__ __forceinline__ float bf16lo_to_f32(uint32_t pair) { return __uint_as_float(pair << 16); }
+__device__ __forceinline__ float bf16hi_to_f32(uint32_t pair) { return __uint_as_float(pair & 0xFFFF0000u); }
+__device__ __forceinline__ float bf16_to_f32(uint16_t b) { return __uint_as_float(uint32_t(b) << 16); }
+
+// Round two floats to bf16 (nearest even) and pack: low half = a, high = b.
+__device__ __forceinline__ uint32_t pack_bf16x2_rn(float a, float b) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(b), "f"(a));
+    return r;
+}
+
+__device__ __forceinline__ uint16_t f32_to_bf16_rn(float a) {
+    return __bfloat16_as_ushort(__float2bfloat16_rn(a));
+}
+
+// double -> bf16, one rounding to nearest even, via round-to-odd: truncate to
+// float (24 significant bits) and set the last bit if anything was dropped;
+// rounding that float to bf16 (8 bits) is then the correct rounding of the
+// double (Boldo & Melquiond, "Emulation of FMA and correctly rounded sums:
+// proved algorithms using rounding to odd", 2008).
+__device__ __forceinline__ uint16_t f64_to_bf16_rn(double v) {
+    float t;
+    asm("cvt.rz.f32.f64 %0, %1;" : "=f"(t) : "d"(v));
+    uint32_t u = __float_as_uint(t);
+    if ((double)t != v && (u & 0x7F800000u) != 0x7F800000u) u |= 1u;
+    if (v != v) return 0x7FC0u;
+    return f32_to_bf16_rn(__uint_as_float(u));
+}
+
+__device__ __forceinline__ float f64_to_f32_rn(double v) { return __double2float_rn(v); }
+
+// Streaming 16-byte global accesses.
+__device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ uint4 ld_v4(const void* p) {
+    uint4 r;
+    asm volatile("ld.global.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ void st_v4(void* p, uint4 v) {
+    asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};"
+                 :: "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+}
+
+__device__ __forceinline__ unsigned lane_id() { return threadIdx.x & 31u; }
+
+__host__ __device__ __forceinline__ int64_t min64(int64_t a, int64_t b) { return a < b ? a : b; }
+__host__ __device__ __forceinline__ int64_t max64(int64_t a, int64_t b) { return a > b ? a : b; }
+
+}  // namespace moe

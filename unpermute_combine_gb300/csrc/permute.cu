@@ -1,0 +1,370 @@
+// permute.cu -- moe_permute, moe_sort_chunks, moe_chunk_idxs, moe_expert_scale.
+//
+// Row movement is HBM-bound: every source row is read once and every
+// destination row written once, in 16-byte vectors, coalesced along the row.
+// permute is token-centric ("token dispatcher + fuse_a2a" §1.1
+// index_select, done in the dedup direction): one warp per token reads x[t]
+// once and writes it to its k permuted rows.
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kUnroll = 4;     // 16-byte vectors in flight per lane
+
+// One warp per token; lane l moves vectors l, l+32, ... of the row.
+template <typename V>
+__global__ void __launch_bounds__(kThreads)
+permute_kernel(const V* __restrict__ x, int64_t T, int64_t nvec, int k,
+               const int32_t* __restrict__ slot_pos, V* __restrict__ out) {
+    __shared__ int32_t s_pos[kWarps][kMaxTopK];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t n_rows = T * k;
+    for (int64_t t = int64_t(blockIdx.x) * kWarps + warp; t < T;
+         t += int64_t(gridDim.x) * kWarps) {
+        if (lane < k) {
+            const int32_t p = slot_pos[t * k + lane];
+            s_pos[warp][lane] = (p >= 0 && p < n_rows) ? p : -1;
+        }
+        __syncwarp();
+        const V* src = x + t * nvec;
+        for (int64_t v0 = lane; v0 < nvec; v0 += 32 * kUnroll) {
+            V d[kUnroll];
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                const int64_t v = v0 + 32 * u;
+                if (v < nvec) d[u] = __ldcs(src + v);
+            }
+            for (int j = 0; j < k; ++j) {
+                const int32_t p = s_pos[warp][j];
+                if (p < 0) continue;
+                V* dst = out + int64_t(p) * nvec;
+#pragma unroll
+                for (int u = 0; u < kUnroll; ++u) {
+                    const int64_t v = v0 + 32 * u;
+                    if (v < nvec) __stcs(dst + v, d[u]);
+                }
+            }
+        }
+        __syncwarp();
+    }
+}
+
+int grid_for(const void* kernel, int threads, size_t smem, int64_t work_blocks) {
+    int per_sm = 0;
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem);
+    if (per_sm < 1) per_sm = 1;
+    const int64_t cap = int64_t(sm_count()) * per_sm;
+    return int(work_blocks < cap ? (work_blocks > 0 ? work_blocks : 1) : cap);
+}
+
+// ----------------------------------------------------------------- sort_chunks
+// Prep kernel (one block): validate the splits and the chunk order, then write
+// per output chunk i: dst_start[i] (exclusive prefix of split_sizes[idx[i]],
+// dst_start[C] = N) and src_start[i] (start row of chunk idx[i] in `in`).
+struct ChunkPlan {
+    int32_t* dst_start;   // [C+1]
+    int32_t* src_start;   // [C]
+    int32_t* src_prefix;  // [C+1] exclusive prefix of split_sizes in input order
+};
+
+constexpr int kPrepThreads = 1024;
+constexpr int kMaxChunks = 65536;
+
+__device__ int32_t block_scan_exclusive_1024(int32_t v, int32_t* s_warp, int32_t* total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int32_t incl = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int32_t o = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+        if (lane >= off) incl += o;
+    }
+    if (lane == 31) s_warp[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        int32_t w = s_warp[lane];
+        int32_t wi = w;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int32_t o = __shfl_up_sync(0xFFFFFFFFu, wi, off);
+            if (lane >= off) wi += o;
+        }
+        s_warp[lane] = wi - w;              // exclusive warp prefix
+        if (lane == 31) s_warp[32] = wi;    // block total
+    }
+    __syncthreads();
+    const int32_t r = s_warp[warp] + incl - v;
+    *total = s_warp[32];
+    __syncthreads();
+    return r;
+}
+
+__global__ void __launch_bounds__(kPrepThreads)
+sort_chunks_prep_kernel(const int32_t* __restrict__ split_sizes,
+                        const int32_t* __restrict__ sorted_idxs, int C, int64_t N,
+                        ChunkPlan plan, WsHeader* __restrict__ header) {
+    __shared__ int32_t s_warp[33];
+    __shared__ uint32_t s_seen[kMaxChunks / 32];
+    __shared__ int s_bad;
+    for (int i = threadIdx.x; i < (C + 31) / 32; i += kPrepThreads) s_seen[i] = 0;
+    if (threadIdx.x == 0) s_bad = 0;
+    __syncthreads();
+    bool bad = false;
+    for (int i = threadIdx.x; i < C; i += kPrepThreads) {
+        const int32_t c = sorted_idxs[i];
+        if (c < 0 || c >= C || split_sizes[i] < 0) { bad = true; continue; }
+        const uint32_t bit = 1u << (c & 31);
+        if (atomicOr(&s_seen[c >> 5], bit) & bit) bad = true;   // named twice
+    }
+    if (bad) atomicOr(&s_bad, 1);
+    __syncthreads();
+    // prefix of split_sizes in input order (64-bit guard against overflow)
+    int64_t carry = 0;
+    for (int base = 0; base < C; base += kPrepThreads) {
+        const int i = base + threadIdx.x;
+        const int32_t v = i < C ? split_sizes[i] : 0;
+        int32_t total;
+        const int32_t ex = block_scan_exclusive_1024(v, s_warp, &total);
+        if (i < C) plan.src_prefix[i] = int32_t(carry + ex);
+        carry += total;
+    }
+    if (threadIdx.x == 0) {
+        plan.src_prefix[C] = int32_t(carry);
+        if (carry != N) s_bad = 1;
+    }
+    __syncthreads();
+    // prefix of split_sizes[idx[i]] in output order
+    int64_t carry2 = 0;
+    for (int base = 0; base < C; base += kPrepThreads) {
+        const int i = base + threadIdx.x;
+        int32_t c = i < C ? sorted_idxs[i] : 0;
+        c = (c >= 0 && c < C) ? c : 0;
+        const int32_t v = i < C ? split_sizes[c] : 0;
+        int32_t total;
+        const int32_t ex = block_scan_exclusive_1024(v, s_warp, &total);
+        if (i < C) {
+            plan.dst_start[i] = int32_t(carry2 + ex);
+            plan.src_start[i] = plan.src_prefix[c];
+        }
+        carry2 += total;
+    }
+    if (threadIdx.x == 0) {
+        plan.dst_start[C] = int32_t(carry2);
+        header->status = s_bad ? MOE_ERR_DEVICE_CHECK : MOE_OK;
+        header->detail = 0;
+    }
+}
+
+// Copy kernel: each warp owns a contiguous range of output rows; it finds the
+// chunk of its first row by binary search and walks forward.
+template <typename V>
+__global__ void __launch_bounds__(kThreads)
+sort_chunks_copy_kernel(const V* __restrict__ in, int64_t N, int64_t nvec, int C,
+                        ChunkPlan plan, const WsHeader* __restrict__ header,
+                        V* __restrict__ out) {
+    if (header->status != MOE_OK) return;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t nwarps = int64_t(gridDim.x) * kWarps;
+    const int64_t gw = int64_t(blockIdx.x) * kWarps + warp;
+    const int64_t per = (N + nwarps - 1) / nwarps;
+    const int64_t r0 = gw * per, r1 = min64(N, r0 + per);
+    if (r0 >= r1) return;
+    // last chunk i with dst_start[i] <= r0
+    int lo = 0, hi = C - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (plan.dst_start[mid] <= r0) lo = mid; else hi = mid - 1;
+    }
+    int i = lo;
+    int64_t chunk_end = plan.dst_start[i + 1];
+    for (int64_t r = r0; r < r1; ++r) {
+        while (r >= chunk_end) { ++i; chunk_end = plan.dst_start[i + 1]; }
+        const int64_t s = plan.src_start[i] + (r - plan.dst_start[i]);
+        const V* src = in + s * nvec;
+        V* dst = out + r * nvec;
+        for (int64_t v0 = lane; v0 < nvec; v0 += 32 * kUnroll) {
+            V d[kUnroll];
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                const int64_t v = v0 + 32 * u;
+                if (v < nvec) d[u] = __ldcs(src + v);
+            }
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                const int64_t v = v0 + 32 * u;
+                if (v < nvec) __stcs(dst + v, d[u]);
+            }
+        }
+    }
+}
+
+size_t chunk_plan_bytes(int C) {
+    return align_up(sizeof(int32_t) * (size_t(C + 1) * 2 + size_t(C)), kWsAlign);
+}
+
+ChunkPlan chunk_plan(void* ws, int C) {
+    int32_t* base = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + kWsAlign);
+    return ChunkPlan{base, base + (C + 1), base + (C + 1) + C};
+}
+
+// -------------------------------------------------------------- expert scale
+// Round the exact product a*b to bf16.  p = fl(a*b) is within half a float
+// ulp of it, so p rounds like the exact product unless p sits exactly on a
+// bf16 midpoint; then the sign of the product's error e = fma(a,b,-p) breaks
+// the tie (Dekker/Knuth error-free product).
+__device__ __forceinline__ uint16_t mul_bf16_rn(float a, float b) {
+    const float p = __fmul_rn(a, b);
+    const uint32_t u = __float_as_uint(p);
+    if ((u & 0xFFFFu) == 0x8000u) {
+        const float e = __fmaf_rn(a, b, -p);
+        if (e != 0.0f) {
+            const bool same = ((__float_as_uint(e) ^ u) & 0x80000000u) == 0;
+            return uint16_t((same ? u + 0x8000u : u - 0x8000u) >> 16);
+        }
+    }
+    return f32_to_bf16_rn(p);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads)
+expert_scale_kernel(const T* __restrict__ in, int64_t n_rows, int64_t H, int E,
+                    const int32_t* __restrict__ offsets, const float* __restrict__ scale,
+                    T* __restrict__ out) {
+    __shared__ int32_t s_off[kMaxExperts + 1];
+    __shared__ float s_scale[kMaxExperts];
+    for (int e = threadIdx.x; e <= E; e += kThreads) s_off[e] = offsets[e];
+    for (int e = threadIdx.x; e < E; e += kThreads) s_scale[e] = scale[e];
+    __syncthreads();
+    const int64_t rows = min64(n_rows, s_off[E]);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int64_t p = int64_t(blockIdx.x) * kWarps + warp; p < rows;
+         p += int64_t(gridDim.x) * kWarps) {
+        int lo = 0, hi = E - 1;          // last e with offsets[e] <= p
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (s_off[mid] <= p) lo = mid; else hi = mid - 1;
+        }
+        const float s = s_scale[lo];
+        for (int64_t h = lane; h < H; h += 32) {
+            if constexpr (sizeof(T) == 4) {
+                out[p * H + h] = __fmul_rn(in[p * H + h], s);
+            } else {
+                out[p * H + h] = mul_bf16_rn(bf16_to_f32(in[p * H + h]), s);
+            }
+        }
+    }
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" moe_status_t moe_permute(const void* x, moe_dtype_t dtype, int64_t T, int64_t H, int k,
+                                    const int32_t* slot_pos, void* out, void* stream) {
+    if (!dtype_ok(dtype) || T < 0 || H < 0 || k < 1) return MOE_ERR_INVALID_ARG;
+    if (k > kMaxTopK || T * int64_t(k) >= (int64_t(1) << 31)) return MOE_ERR_UNSUPPORTED;
+    if (T == 0 || H == 0) return MOE_OK;
+    if (!x || !slot_pos || !out) return MOE_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t row = size_t(H) * elem_size(dtype);
+    const int64_t blocks = (T + kWarps - 1) / kWarps;
+    if (row % 16 == 0 && aligned16(x) && aligned16(out)) {
+        const int g = grid_for((const void*)permute_kernel<uint4>, kThreads, 0, blocks);
+        permute_kernel<uint4><<<g, kThreads, 0, s>>>(
+            static_cast<const uint4*>(x), T, int64_t(row / 16), k, slot_pos,
+            static_cast<uint4*>(out));
+    } else if (dtype == MOE_F32) {
+        const int g = grid_for((const void*)permute_kernel<float>, kThreads, 0, blocks);
+        permute_kernel<float><<<g, kThreads, 0, s>>>(
+            static_cast<const float*>(x), T, H, k, slot_pos, static_cast<float*>(out));
+    } else {
+        const int g = grid_for((const void*)permute_kernel<uint16_t>, kThreads, 0, blocks);
+        permute_kernel<uint16_t><<<g, kThreads, 0, s>>>(
+            static_cast<const uint16_t*>(x), T, H, k, slot_pos, static_cast<uint16_t*>(out));
+    }
+    return launch_status();
+}
+
+extern "C" moe_status_t moe_sort_chunks_workspace_size(int C, size_t* bytes) {
+    if (!bytes || C < 1) return MOE_ERR_INVALID_ARG;
+    if (C > kMaxChunks) return MOE_ERR_UNSUPPORTED;
+    *bytes = kWsAlign + chunk_plan_bytes(C);
+    return MOE_OK;
+}
+
+extern "C" moe_status_t moe_sort_chunks(const void* in, moe_dtype_t dtype, int64_t N, int64_t H,
+                                        const int32_t* split_sizes, const int32_t* sorted_idxs,
+                                        int C, void* out, void* workspace,
+                                        size_t workspace_bytes, void* stream) {
+    if (!dtype_ok(dtype) || N < 0 || H < 0 || C < 1) return MOE_ERR_INVALID_ARG;
+    if (C > kMaxChunks || N >= (int64_t(1) << 31)) return MOE_ERR_UNSUPPORTED;
+    if (!split_sizes || !sorted_idxs) return MOE_ERR_INVALID_ARG;
+    if (N > 0 && H > 0 && (!in || !out)) return MOE_ERR_INVALID_ARG;
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & (kWsAlign - 1)) ||
+        workspace_bytes < kWsAlign + chunk_plan_bytes(C))
+        return MOE_ERR_WORKSPACE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    WsHeader* header = static_cast<WsHeader*>(workspace);
+    const ChunkPlan plan = chunk_plan(workspace, C);
+    sort_chunks_prep_kernel<<<1, kPrepThreads, 0, s>>>(split_sizes, sorted_idxs, C, N, plan,
+                                                      header);
+    if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
+    if (N == 0 || H == 0) return MOE_OK;
+    const size_t row = size_t(H) * elem_size(dtype);
+    const int64_t want = (N + kWarps - 1) / kWarps;
+    if (row % 16 == 0 && aligned16(in) && aligned16(out)) {
+        const int g = grid_for((const void*)sort_chunks_copy_kernel<uint4>, kThreads, 0, want);
+        sort_chunks_copy_kernel<uint4><<<g, kThreads, 0, s>>>(
+            static_cast<const uint4*>(in), N, int64_t(row / 16), C, plan, header,
+            static_cast<uint4*>(out));
+    } else if (dtype == MOE_F32) {
+        const int g = grid_for((const void*)sort_chunks_copy_kernel<float>, kThreads, 0, want);
+        sort_chunks_copy_kernel<float><<<g, kThreads, 0, s>>>(
+            static_cast<const float*>(in), N, H, C, plan, header, static_cast<float*>(out));
+    } else {
+        const int g = grid_for((const void*)sort_chunks_copy_kernel<uint16_t>, kThreads, 0, want);
+        sort_chunks_copy_kernel<uint16_t><<<g, kThreads, 0, s>>>(
+            static_cast<const uint16_t*>(in), N, H, C, plan, header,
+            static_cast<uint16_t*>(out));
+    }
+    return launch_status();
+}
+
+extern "C" moe_status_t moe_chunk_idxs(int R, int L, int inverse, int32_t* idxs) {
+    if (R < 1 || L < 1 || !idxs) return MOE_ERR_INVALID_ARG;
+    if (int64_t(R) * L > kMaxChunks) return MOE_ERR_UNSUPPORTED;
+    // Numbering an [A x B] grid row-major and reading it column by column
+    // puts entry (a, b) = a*B + b at position b*A + a.
+    for (int r = 0; r < R; ++r)
+        for (int l = 0; l < L; ++l) {
+            if (!inverse) idxs[l * R + r] = r * L + l;
+            else idxs[r * L + l] = l * R + r;
+        }
+    return MOE_OK;
+}
+
+extern "C" moe_status_t moe_expert_scale(const void* in, moe_dtype_t dtype, int64_t n_rows,
+                                         int64_t H, int E, const int32_t* offsets,
+                                         const float* scale, void* out, void* stream) {
+    if (!dtype_ok(dtype) || n_rows < 0 || H < 0 || E < 1) return MOE_ERR_INVALID_ARG;
+    if (E > kMaxExperts || n_rows >= (int64_t(1) << 31)) return MOE_ERR_UNSUPPORTED;
+    if (!offsets || !scale) return MOE_ERR_INVALID_ARG;
+    if (n_rows == 0 || H == 0) return MOE_OK;
+    if (!in || !out) return MOE_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int64_t want = (n_rows + kWarps - 1) / kWarps;
+    if (dtype == MOE_F32) {
+        const int g = grid_for((const void*)expert_scale_kernel<float>, kThreads, 0, want);
+        expert_scale_kernel<float><<<g, kThreads, 0, s>>>(
+            static_cast<const float*>(in), n_rows, H, E, offsets, scale, static_cast<float*>(out));
+    } else {
+        const int g = grid_for((const void*)expert_scale_kernel<uint16_t>, kThreads, 0, want);
+        expert_scale_kernel<uint16_t><<<g, kThreads, 0, s>>>(
+            static_cast<const uint16_t*>(in), n_rows, H, E, offsets, scale,
+            static_cast<uint16_t*>(out));
+    }
+    return launch_status();
+}
