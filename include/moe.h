@@ -116,6 +116,36 @@ moe_status_t moe_route_indices(const int32_t* topk_idx, const float* topk_w,
                                float* permuted_probs, uint8_t* routing_map,
                                void* workspace, size_t workspace_bytes, void* stream);
 
+/* The same routing as moe_route for callers that cannot allocate device
+ * memory: a plugin or runtime that works inside a fixed, pre-reserved memory
+ * budget and has no allocator of its own, or code that must not call
+ * cudaMalloc because cudaMalloc can synchronise the device.  (The pages have
+ * no counterpart: this is a property of the library, not of the method.)
+ * The caller still passes every input and output; the scratch space that
+ * moe_route takes as a workspace comes instead from a fixed array of
+ * MOE_ROUTE_NOALLOC_SCRATCH_BYTES inside the library, which every GPU that
+ * loads the library keeps until the process exits.
+ *  - Problems needing more than that (moe_route_workspace_size(T, E, k) >
+ *    MOE_ROUTE_NOALLOC_SCRATCH_BYTES; e.g. T = 16384, E = 256 needs 132 KB)
+ *    return MOE_ERR_UNSUPPORTED before anything runs.
+ *  - It allocates nothing: no cudaMalloc, no cudaFree, no allocating library
+ *    call.  Its first call on each device looks up the array's device address
+ *    (once per device, with that device current); make that first call before
+ *    any stream capture.
+ *  - Every call shares the one array.  Each call writes all the scratch it
+ *    reads, so nothing has to be cleared between calls, but calls that
+ *    overlap on the GPU (other streams, other host threads) race: serialise
+ *    them.
+ *  - Routing from logits records no device-side status, so there is no
+ *    workspace to pass to moe_workspace_status. */
+#define MOE_ROUTE_NOALLOC_SCRATCH_BYTES (1u << 20)
+
+moe_status_t moe_route_noalloc(const float* logits, int64_t T, int E, int k,
+                               int32_t* topk_idx, float* topk_w,
+                               int32_t* counts, int32_t* offsets, int32_t* group_list,
+                               int32_t* sorted_indices, int32_t* slot_pos,
+                               float* permuted_probs, uint8_t* routing_map, void* stream);
+
 /* ---------------------------------------------------------------- permute
  * [DISPATCH] §1.1 permuted_input = tokens.index_select(0, sorted_indices),
  * computed token by token: every row x[t] is read once and written to rows

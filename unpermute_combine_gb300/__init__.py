@@ -24,7 +24,11 @@ __all__ = [
     "moe_route_workspace_size", "moe_route", "moe_route_indices", "moe_permute",
     "moe_sort_chunks_workspace_size", "moe_sort_chunks", "moe_chunk_idxs", "moe_combine",
     "moe_combine_backward", "moe_expert_scale", "moe_workspace_status", "RouteResult",
+    "moe_route_noalloc", "MOE_ROUTE_NOALLOC_SCRATCH_BYTES",
 ]
+
+# Size of the library's built-in scratch array used by moe_route_noalloc.
+MOE_ROUTE_NOALLOC_SCRATCH_BYTES = 1 << 20
 
 MOE_OK = 0
 _DT = {torch.float32: 0, torch.bfloat16: 1}
@@ -63,6 +67,7 @@ def load_library():
             "moe_route_workspace_size": ([I64, I, I, PSZ], I),
             "moe_route": ([P, I64, I, I, P, P, P, P, P, P, P, P, P, P, SZ, P], I),
             "moe_route_indices": ([P, P, I64, I, I, P, P, P, P, P, P, P, P, SZ, P], I),
+            "moe_route_noalloc": ([P, I64, I, I, P, P, P, P, P, P, P, P, P, P], I),
             "moe_permute": ([P, I, I64, I64, I, P, P, P], I),
             "moe_sort_chunks_workspace_size": ([I, PSZ], I),
             "moe_sort_chunks": ([P, I, I64, I64, P, P, I, P, P, SZ, P], I),
@@ -208,6 +213,31 @@ def moe_route_indices(topk_idx: torch.Tensor, topk_w: Optional[torch.Tensor], E:
         _p(topk_idx), _p(topk_w), T, E, k, _p(r.counts), _p(r.offsets), _p(r.group_list),
         _p(r.sorted_indices), _p(r.slot_pos), _p(r.permuted_probs), _p(r.routing_map), _p(ws),
         ws.numel(), _stream(stream)))
+    return r
+
+
+def moe_route_noalloc(logits: torch.Tensor, k: int, *, routing_map: bool = False,
+                      stream=None) -> RouteResult:
+    """moe_route without a workspace, for callers that cannot allocate device
+    memory for scratch: the library's built-in scratch array is used instead
+    (calls that overlap on the GPU must be serialised).  The outputs are
+    allocated here only because this binding returns new tensors; the C entry
+    point itself allocates nothing."""
+    _cuda(logits, "logits", torch.float32, 2)
+    T, E = logits.shape
+    i32 = torch.int32
+    r = RouteResult(
+        topk_idx=_empty((T, k), i32, logits), topk_w=_empty((T, k), torch.float32, logits),
+        counts=_empty((E,), i32, logits), offsets=_empty((E + 1,), i32, logits),
+        group_list=_empty((E,), i32, logits), sorted_indices=_empty((T * k,), i32, logits),
+        slot_pos=_empty((T, k), i32, logits),
+        permuted_probs=_empty((T * k,), torch.float32, logits),
+        routing_map=_empty((T, E), torch.uint8, logits) if routing_map else None,
+        workspace=None)
+    _ok("moe_route_noalloc", load_library().moe_route_noalloc(
+        _p(logits), T, E, k, _p(r.topk_idx), _p(r.topk_w), _p(r.counts), _p(r.offsets),
+        _p(r.group_list), _p(r.sorted_indices), _p(r.slot_pos), _p(r.permuted_probs),
+        _p(r.routing_map), _stream(stream)))
     return r
 
 

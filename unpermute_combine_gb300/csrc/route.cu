@@ -604,3 +604,53 @@ extern "C" moe_status_t moe_route_indices(const int32_t* topk_idx, const float* 
     return finish_route(topk_idx, topk_w, T, E, k, true, hist, header, counts, offsets,
                         group_list, sorted_indices, slot_pos, permuted_probs, s);
 }
+
+// ------------------------------------------------------- no-allocation route
+// moe_route for callers that cannot provide a workspace.  The histogram
+// scratch lives in a fixed array in this library's device image instead of
+// caller memory: every GPU that loads the library holds it until the process
+// exits.  Nothing in it needs to start at zero -- each call writes every
+// scratch byte before it reads it -- but all calls share it, so calls that
+// overlap on the GPU (different streams, or different host threads) race.
+#include <mutex>
+
+static __device__ __align__(256) unsigned char g_route_scratch[MOE_ROUTE_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+constexpr int kNoallocMaxDevices = 64;
+std::mutex g_noalloc_mutex;
+void* g_noalloc_scratch[kNoallocMaxDevices] = {};
+
+// Device address of g_route_scratch on the current device, looked up once
+// per device (host code cannot use the array's name as an address).
+moe_status_t noalloc_scratch(void** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+    if (dev < 0 || dev >= kNoallocMaxDevices) return MOE_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (!g_noalloc_scratch[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_route_scratch) != cudaSuccess || !p) return MOE_ERR_CUDA;
+        g_noalloc_scratch[dev] = p;
+    }
+    *out = g_noalloc_scratch[dev];
+    return MOE_OK;
+}
+}  // namespace
+
+extern "C" moe_status_t moe_route_noalloc(const float* logits, int64_t T, int E, int k,
+                                          int32_t* topk_idx, float* topk_w, int32_t* counts,
+                                          int32_t* offsets, int32_t* group_list,
+                                          int32_t* sorted_indices, int32_t* slot_pos,
+                                          float* permuted_probs, uint8_t* routing_map,
+                                          void* stream) {
+    const moe_status_t st = validate_sizes(T, E, k);
+    if (st != MOE_OK) return st;
+    if (kWsAlign + hist_bytes(T, E) > MOE_ROUTE_NOALLOC_SCRATCH_BYTES) return MOE_ERR_UNSUPPORTED;
+    void* scratch = nullptr;
+    const moe_status_t sst = noalloc_scratch(&scratch);
+    if (sst != MOE_OK) return sst;
+    return moe_route(logits, T, E, k, topk_idx, topk_w, counts, offsets, group_list,
+                     sorted_indices, slot_pos, permuted_probs, routing_map, scratch,
+                     MOE_ROUTE_NOALLOC_SCRATCH_BYTES, stream);
+}
