@@ -1,0 +1,83 @@
+"""bench.py's host-side logic without a GPU: the max-over-ranks timing and
+whole-job value of the replica mode over two gloo ranks, the algorithmic byte
+counts, clock parsing and the reference arm's rank gating."""
+import os
+import socket
+import types
+
+import pytest
+
+import bench
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def _worker(rank, world, port, q):
+    import torch.distributed as dist
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    elapsed = 1.0 + rank                    # rank 1 is the slow replica
+    m = bench.reduce_max(elapsed)
+    v = bench.job_value(131072, world, 10, m)
+    q.put((rank, m, v))
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_replicas_report_the_slowest_rank_over_gloo():
+    mp = pytest.importorskip("torch.multiprocessing")
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    got = sorted(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=120)
+        assert p.exitcode == 0
+    assert [g[1] for g in got] == [2.0, 2.0]
+    # whole-job throughput: both ranks' units over the slowest rank's time
+    assert got[0][2] == pytest.approx(131072 * 2 * 10 / 2.0)
+
+
+def test_reduce_max_without_a_process_group_is_identity():
+    assert bench.reduce_max(3.5) == 3.5
+
+
+def test_algorithmic_bytes_at_the_deepseek_shape():
+    a = bench.algorithmic_bytes(16384, 7168, 256, 8, 2)
+    N = 16384 * 8
+    assert a["permute"] == 16384 * 7168 * 2 + N * 7168 * 2 + 4 * N
+    assert abs(a["permute"] / 1e6 - 2114.45) < 0.01
+    assert abs(a["combine_backward"] / 1e6 - 3994.55) < 0.01
+    assert a["combine"] - a["permute"] == 4 * N
+
+
+def test_clock_summary_parses_nvidia_smi_lines():
+    c = bench.ClockSampler(0)
+    c.out = ("0, 2070, 2070, 900.1, 0x0, Not Active, Not Active, Not Active, Not Active\n"
+             "0, 1980, 2070, 1300.0, 0x4, Not Active, Not Active, Not Active, Active\n"
+             "0, 2010, 2070, 1200.0, 0x0, Not Active, Not Active, Not Active, Not Active\n")
+    s = c.summary()
+    assert s["sm_mhz"] == 2010 and s["sm_max_mhz"] == 2070 and s["samples"] == 3
+    assert s["reasons"] == ["sw_power_cap"]
+
+
+def test_reference_arm_runs_on_rank_zero_only():
+    args = types.SimpleNamespace(steps=1, warmup=3, ref_tokens=8)
+    assert bench.run_reference(args, rank=1) is None
+
+
+def test_recorded_traffic_is_void_for_a_changed_source(tmp_path, monkeypatch):
+    d = bench.source_digest(*bench.KERNEL_SOURCES["combine_backward"])
+    assert bench.recorded_traffic("combine_backward", "0" * 16) is None
+    got = bench.recorded_traffic("combine_backward", d)
+    assert got is None or got > 1e9
