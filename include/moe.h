@@ -221,6 +221,36 @@ moe_status_t moe_expert_scale(const void* in, moe_dtype_t dtype, int64_t n_rows,
                               int E, const int32_t* offsets, const float* scale, void* out,
                               void* stream);
 
+/* --------------------------------------------------------- grouped SwiGLU
+ * [MOE-OPS] §8 (and §7 for the segments): each expert e applies its SwiGLU
+ * FFN to its rows [offsets[e], offsets[e+1]) of the permuted activations:
+ *   gate_up = x_e @ w_up[e]            [n_e, 2I]  (fp32 accumulation)
+ *   hidden  = silu(gate) * up          gate = first I columns, up = last I;
+ *                                      stored as bf16
+ *   y_e     = hidden @ w_down[e]       [n_e, H]   (fp32 accumulation, bf16 out)
+ * on the tcgen05 tensor cores.  Weights are prepacked once (a model-load
+ * step, not part of the per-batch path) by moe_grouped_swiglu_pack:
+ *   w_up [E,H,2I] bf16  -> w_up_packed [E,2I,H]  (K-major; rows in blocks of
+ *                          256 = [128 gate rows | the matching 128 up rows])
+ *   w_down [E,I,H] bf16 -> w_down_packed [E,H,I] (K-major)
+ * Shapes: H a multiple of 256, I a multiple of 128, E <= 1024, all bf16
+ * 16-byte aligned.  offsets [E+1] int32 stays on the device (no host sync):
+ * rows past offsets[E] of y are untouched.  x, y [N,H].  Workspace
+ * (moe_grouped_swiglu_workspace_size) holds the bf16 hidden [N,I] and the
+ * status word (MOE_ERR_TIMEOUT if a bounded tensor-core pipeline wait gave
+ * up; read with moe_workspace_status). */
+moe_status_t moe_grouped_swiglu_pack(const void* w_up, const void* w_down, int E, int64_t H,
+                                     int64_t I, void* w_up_packed, void* w_down_packed,
+                                     void* stream);
+
+moe_status_t moe_grouped_swiglu_workspace_size(int64_t N, int E, int64_t H, int64_t I,
+                                               size_t* bytes);
+
+moe_status_t moe_grouped_swiglu(const void* x, const void* w_up_packed,
+                                const void* w_down_packed, const int32_t* offsets,
+                                int64_t N, int E, int64_t H, int64_t I, void* y,
+                                void* workspace, size_t workspace_bytes, void* stream);
+
 /* ------------------------------------------------- workspace status word
  * Waits for `stream`, then reads the status a previous call left in
  * `workspace`: MOE_OK, MOE_ERR_DEVICE_CHECK or MOE_ERR_TIMEOUT.  Each call

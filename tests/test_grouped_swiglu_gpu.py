@@ -1,0 +1,131 @@
+"""Grouped SwiGLU (tcgen05 tensor cores) vs the CPU oracle through the C ABI.
+
+Bar: relative Frobenius error <= 2e-2 against the oracle's double-accumulated
+result (the hidden activation is rounded to bf16 on both sides).  The prepack
+is a pure rearrangement and must be bit-exact."""
+import numpy as np
+import pytest
+
+import oracle
+import workloads as wl
+from moe_testutil import to_dev, to_host
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+import unpermute_combine_gb300 as moe  # noqa: E402
+
+TOL = 2e-2
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.fail("GPU tests need a CUDA device")
+    from unpermute_combine_gb300 import build
+    build.build()
+    moe.load_library()
+
+
+def _weights(seed, E, H, I, std=0.05):
+    rng = np.random.default_rng(seed)
+    up = wl.f32_to_bf16_bits((rng.standard_normal((E, H, 2 * I)) * std).astype(np.float32))
+    down = wl.f32_to_bf16_bits((rng.standard_normal((E, I, H)) * std).astype(np.float32))
+    return up, down
+
+
+def _rel_frob(got_bits, ref64):
+    g = wl.bf16_bits_to_f32(got_bits).astype(np.float64)
+    return np.linalg.norm(g - ref64) / max(np.linalg.norm(ref64), 1e-30)
+
+
+def test_pack_layout_bit_exact():
+    E, H, I = 2, 256, 256
+    up, down = _weights(1, E, H, I)
+    up_p, down_p = moe.moe_grouped_swiglu_pack(to_dev(up), to_dev(down))
+    up_p, down_p = to_host(up_p), to_host(down_p)
+    # expected: rows of w_up^T, regrouped per 128 hidden columns as [gate | up]
+    upT = np.transpose(up, (0, 2, 1))           # [E, 2I, H]
+    exp_up = np.empty_like(upT)
+    for b in range(I // 128):
+        exp_up[:, b * 256:b * 256 + 128] = upT[:, b * 128:(b + 1) * 128]
+        exp_up[:, b * 256 + 128:(b + 1) * 256] = upT[:, I + b * 128:I + (b + 1) * 128]
+    assert (up_p == exp_up).all()
+    assert (down_p == np.transpose(down, (0, 2, 1))).all()
+
+
+@pytest.mark.parametrize("counts,H,I", [([128], 256, 128),            # one tile
+                                        ([130, 0, 300], 256, 128),    # ragged, an empty expert
+                                        ([1, 255, 0, 0, 77], 512, 256),
+                                        ([0, 0, 64], 256, 384)])
+def test_grouped_swiglu_small(counts, H, I):
+    E = len(counts)
+    N = sum(counts)
+    offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    rng = np.random.default_rng(N + H + I)
+    x = wl.f32_to_bf16_bits(rng.standard_normal((N, H)).astype(np.float32))
+    up, down = _weights(N + E, E, H, I)
+    up_p, down_p = moe.moe_grouped_swiglu_pack(to_dev(up), to_dev(down))
+    sentinel = torch.full((N + 3, H), 5.0, dtype=torch.bfloat16, device="cuda")
+    y = moe.moe_grouped_swiglu(to_dev(x), up_p, down_p, to_dev(offsets),
+                               out=sentinel[:N] if N else None)
+    torch.cuda.synchronize()
+    assert moe.moe_workspace_status(y._moe_workspace) == 0
+    y_o, y64 = oracle.grouped_swiglu(x, up, down, offsets)
+    err = _rel_frob(to_host(y), y64)
+    assert err <= TOL, err
+    # per-expert too, so a wrong segment cannot hide behind a big neighbour
+    for e in range(E):
+        a, b = offsets[e], offsets[e + 1]
+        if b > a:
+            assert _rel_frob(to_host(y)[a:b], y64[a:b]) <= TOL
+    # rows past the routed rows are untouched
+    assert (to_host(sentinel[N:]) == wl.f32_to_bf16_bits(np.full((3, H), 5.0, np.float32))).all()
+
+
+def test_grouped_swiglu_layer_workload_sampled():
+    """Full-size MoE layer workload (T=4096, H=2048, E=64, k=6, I=1408):
+    GPU route -> permute -> grouped SwiGLU -> combine, against the oracle on a
+    seeded sample of tokens."""
+    d = wl.make("layer", with_weights=True)
+    W = d["workload"]
+    r = moe.moe_route(to_dev(d["logits"]), W.k)
+    xp = moe.moe_permute(to_dev(d["x"]), r.slot_pos)
+    up_p, down_p = moe.moe_grouped_swiglu_pack(to_dev(d["w_up"]), to_dev(d["w_down"]))
+    y = moe.moe_grouped_swiglu(xp, up_p, down_p, r.offsets)
+    out = moe.moe_combine(y, r.slot_pos, r.topk_w)
+    torch.cuda.synchronize()
+    assert moe.moe_workspace_status(y._moe_workspace) == 0
+
+    o = oracle.route(d["logits"], W.k)
+    n = int(o["offsets"][W.E])
+    xp_o = oracle.permute(d["x"], o["sorted_indices"], n)
+    rng = np.random.default_rng(77)
+    toks = np.sort(rng.choice(W.T, 24, replace=False))
+    rows = o["slot_pos"][toks].ravel()
+    y_o, y64 = oracle.grouped_swiglu(xp_o, d["w_up"], d["w_down"], o["offsets"], rows=rows)
+    y_gpu = to_host(y)
+    assert _rel_frob(y_gpu[rows], y64[rows]) <= TOL
+    for p in rows[:12]:
+        assert _rel_frob(y_gpu[p:p + 1], y64[p:p + 1]) <= TOL
+    # combine of the sampled tokens from the oracle's expert outputs
+    sp_local = np.arange(rows.size, dtype=np.int32).reshape(toks.size, W.k)
+    out_o, out64 = oracle.combine(np.ascontiguousarray(y_o[rows]), sp_local, o["topk_w"][toks])
+    assert _rel_frob(to_host(out)[toks], out64) <= TOL
+
+
+def test_grouped_swiglu_e1_is_a_dense_ffn():
+    """With one expert the layer is a plain SwiGLU FFN; torch (cuBLAS) gives
+    an independent reference on the GPU."""
+    N, H, I = 384, 512, 256
+    rng = np.random.default_rng(5)
+    x = wl.f32_to_bf16_bits(rng.standard_normal((N, H)).astype(np.float32))
+    up, down = _weights(6, 1, H, I)
+    up_p, down_p = moe.moe_grouped_swiglu_pack(to_dev(up), to_dev(down))
+    y = moe.moe_grouped_swiglu(to_dev(x), up_p, down_p,
+                               to_dev(np.array([0, N], np.int32)))
+    xf = to_dev(x).float()
+    gu = xf @ to_dev(up).float()[0]
+    h = (torch.nn.functional.silu(gu[:, :I]) * gu[:, I:]).bfloat16().float()
+    ref = (h @ to_dev(down).float()[0]).double().cpu().numpy()
+    assert _rel_frob(to_host(y), ref) <= TOL

@@ -24,7 +24,8 @@ __all__ = [
     "moe_route_workspace_size", "moe_route", "moe_route_indices", "moe_permute",
     "moe_sort_chunks_workspace_size", "moe_sort_chunks", "moe_chunk_idxs", "moe_combine",
     "moe_combine_backward", "moe_expert_scale", "moe_workspace_status", "RouteResult",
-    "moe_route_noalloc", "MOE_ROUTE_NOALLOC_SCRATCH_BYTES",
+    "moe_route_noalloc", "MOE_ROUTE_NOALLOC_SCRATCH_BYTES", "moe_grouped_swiglu_pack",
+    "moe_grouped_swiglu_workspace_size", "moe_grouped_swiglu",
 ]
 
 # Size of the library's built-in scratch array used by moe_route_noalloc.
@@ -76,6 +77,9 @@ def load_library():
             "moe_combine_backward": ([P, P, I, I64, I64, I, P, P, P, P, P], I),
             "moe_expert_scale": ([P, I, I64, I64, I, P, P, P, P], I),
             "moe_workspace_status": ([P, P], I),
+            "moe_grouped_swiglu_pack": ([P, P, I, I64, I64, P, P, P], I),
+            "moe_grouped_swiglu_workspace_size": ([I64, I, I64, I64, PSZ], I),
+            "moe_grouped_swiglu": ([P, P, P, P, I64, I, I64, I64, P, P, SZ, P], I),
         }
         for name, (args, res) in sigs.items():
             fn = getattr(lib, name)
@@ -381,6 +385,54 @@ def moe_expert_scale(x_perm: torch.Tensor, offsets: torch.Tensor, scale: torch.T
         out = torch.empty_like(x_perm)
     _ok("moe_expert_scale", load_library().moe_expert_scale(
         _p(x_perm), dt, n, H, E, _p(offsets), _p(scale), _p(out), _stream(stream)))
+    return out
+
+
+# ----------------------------------------------------------- grouped SwiGLU
+
+def moe_grouped_swiglu_pack(w_up: torch.Tensor, w_down: torch.Tensor, stream=None):
+    """One-time weight prepack: w_up [E,H,2I] -> [E,2I,H] (gate/up interleaved
+    in 128-row blocks), w_down [E,I,H] -> [E,H,I]; both bf16."""
+    _cuda(w_up, "w_up", torch.bfloat16, 3)
+    _cuda(w_down, "w_down", torch.bfloat16, 3)
+    E, H, I2 = w_up.shape
+    I = I2 // 2
+    if tuple(w_down.shape) != (E, I, H) or I2 != 2 * I:
+        raise ValueError("w_up must be [E,H,2I] and w_down [E,I,H]")
+    up_p = torch.empty((E, 2 * I, H), dtype=torch.bfloat16, device=w_up.device)
+    down_p = torch.empty((E, H, I), dtype=torch.bfloat16, device=w_up.device)
+    _ok("moe_grouped_swiglu_pack", load_library().moe_grouped_swiglu_pack(
+        _p(w_up), _p(w_down), E, H, I, _p(up_p), _p(down_p), _stream(stream)))
+    return up_p, down_p
+
+
+def moe_grouped_swiglu_workspace_size(N: int, E: int, H: int, I: int) -> int:
+    n = ctypes.c_size_t(0)
+    _ok("moe_grouped_swiglu_workspace_size",
+        load_library().moe_grouped_swiglu_workspace_size(N, E, H, I, ctypes.byref(n)))
+    return n.value
+
+
+def moe_grouped_swiglu(x: torch.Tensor, w_up_packed: torch.Tensor, w_down_packed: torch.Tensor,
+                       offsets: torch.Tensor, out: Optional[torch.Tensor] = None,
+                       workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """y = per-expert SwiGLU FFN over the expert segments of x (see moe.h)."""
+    _cuda(x, "x", torch.bfloat16, 2)
+    _cuda(w_up_packed, "w_up_packed", torch.bfloat16, 3)
+    _cuda(w_down_packed, "w_down_packed", torch.bfloat16, 3)
+    _cuda(offsets, "offsets", torch.int32, 1)
+    N, H = x.shape
+    E, I2, H2 = w_up_packed.shape
+    I = I2 // 2
+    if H2 != H or tuple(w_down_packed.shape) != (E, H, I) or offsets.numel() != E + 1:
+        raise ValueError("packed weights / offsets do not match x")
+    if out is None:
+        out = torch.empty_like(x)
+    ws = _workspace(moe_grouped_swiglu_workspace_size(N, E, H, I), x, workspace)
+    _ok("moe_grouped_swiglu", load_library().moe_grouped_swiglu(
+        _p(x), _p(w_up_packed), _p(w_down_packed), _p(offsets), N, E, H, I, _p(out), _p(ws),
+        ws.numel(), _stream(stream)))
+    out._moe_workspace = ws
     return out
 
 

@@ -1,0 +1,525 @@
+// grouped_swiglu.cu -- moe_grouped_swiglu_pack, moe_grouped_swiglu.
+//
+// The expert FFN of "从零理解 MoE 算子" §8 over expert-contiguous rows
+// (group_list segments, §7): GMM1 (x @ w_up[e], [n,2I]) -> hidden =
+// silu(gate) * up (gate = first I columns, up = last I) -> GMM2 (hidden @
+// w_down[e], [n,H]).
+//
+// Tensor-core path for sm_103a: each CTA owns one SM (persistent), tiles of
+// 128 rows x 256 columns, fp32 accumulators in tensor memory.
+//   warp 0       TMA producer: 128x64 A and 256x64 B bf16 tiles (128-byte
+//                swizzle) into a 4-stage shared-memory ring
+//   warp 1       one thread issues tcgen05.mma (M=128, N=256, K=16) and
+//                tcgen05.commit to release ring stages / publish the tile
+//   warp 2       allocates / frees the 256 tensor-memory columns
+//   warps 4..7   epilogue: tcgen05.ld of their 32-lane quadrant, SwiGLU (GMM1)
+//                or conversion (GMM2), bf16 stores, rows past the expert's
+//                segment masked
+// Both operands are K-major: moe_grouped_swiglu_pack lays the weights out
+// once as w_up_packed [E, 2I, H] (rows in 128-blocks [gate j0..j0+127 | up
+// j0..j0+127], so one 256-column tile holds matching gate and up columns) and
+// w_down_packed [E, H, I].  The tile schedule is built on the device from
+// offsets (no host synchronisation): experts in order, within an expert the
+// N tiles, within those the M tiles, so the CTAs running at once share an
+// expert's weights through L2.
+// Every wait on an mbarrier is bounded; a wait that gives up records
+// MOE_ERR_TIMEOUT in the workspace status word and the kernel winds down.
+#include <cuda.h>
+
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int BM = 128;             // rows per tile (TMEM lanes)
+constexpr int BN = 256;             // columns per tile (TMEM columns)
+constexpr int BK = 64;              // K per stage: one 128-byte swizzle row
+constexpr int kStages = 4;
+constexpr int kThreads = 256;
+constexpr int kTileABytes = BM * BK * 2;      // 16 KB
+constexpr int kTileBBytes = BN * BK * 2;      // 32 KB
+constexpr int kStageBytes = kTileABytes + kTileBBytes;
+constexpr int kSmemBytes = kStages * kStageBytes + 1024;  // + alignment slack
+constexpr uint32_t kSpinLimit = 1u << 20;     // each try_wait suspends at most ~1 us
+
+// ------------------------------------------------------------- PTX helpers
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
+                 :: "r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(bar) : "memory");
+}
+
+// Bounded wait for the phase of the given parity; false if it gave up.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+    for (uint32_t i = 0; i < kSpinLimit; ++i) {
+        uint32_t done;
+        asm volatile(
+            "{\n .reg .pred p;\n"
+            " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+            " selp.u32 %0, 1, 0, p;\n}"
+            : "=r"(done) : "r"(bar), "r"(parity) : "memory");
+        if (done) return true;
+    }
+    return false;
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
+                                            uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];"
+        :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
+        : "memory");
+}
+
+// Shared-memory matrix descriptor, K-major operand with 128-byte swizzle:
+// start address >> 4 in bits 0-13, leading byte offset (unused for swizzled
+// K-major; 16 B) in bits 16-29, stride byte offset (1024 B between 8-row
+// groups) >> 4 in bits 32-45, descriptor version 1 in bits 46-47, layout
+// SWIZZLE_128B (2) in bits 61-63.
+__device__ __forceinline__ uint64_t smem_desc_k128(uint32_t addr) {
+    uint64_t d = 0;
+    d |= uint64_t((addr >> 4) & 0x3FFFu);
+    d |= uint64_t(1) << 16;
+    d |= uint64_t(1024 >> 4) << 32;
+    d |= uint64_t(1) << 46;
+    d |= uint64_t(2) << 61;
+    return d;
+}
+
+// Instruction descriptor for kind::f16: D f32 (bits 4-5 = 1), A and B bf16
+// (bits 7-9 = 1, 10-12 = 1), both K-major (bits 15, 16 = 0), N >> 3 in bits
+// 17-22, M >> 4 in bits 24-28.
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(BN >> 3) << 17) |
+                            (uint32_t(BM >> 4) << 24);
+
+__device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
+                                         uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}"
+        :: "r"(tmem_d), "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate) : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                 :: "r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// 32 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// ------------------------------------------------------------- tile schedule
+
+// Tile t -> (expert e, m tile m, n tile n).  s_tile_start[e] = first tile of
+// expert e (prefix of ceil(n_e/BM) * n_tiles), s_tile_start[E] = total.
+__device__ __forceinline__ void tile_coords(int t, const int* s_tile_start, const int* s_mt,
+                                            int E, int n_tiles, int& e, int& m, int& n) {
+    int lo = 0, hi = E - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (s_tile_start[mid] <= t) lo = mid; else hi = mid - 1;
+    }
+    e = lo;
+    const int r = t - s_tile_start[e];
+    n = r / s_mt[e];
+    m = r % s_mt[e];
+}
+
+struct GemmArgs {
+    const int32_t* offsets;     // [E+1] row segments
+    int E;
+    int K;                      // reduction length (H for GMM1, I for GMM2)
+    int n_tiles;                // BN-column tiles per expert
+    int64_t w_rows_per_expert;  // rows of the packed weight per expert (2I or H)
+    void* out;                  // bf16 [N_rows, out_cols]
+    int64_t out_cols;           // I (GMM1, after SwiGLU) or H (GMM2)
+    WsHeader* header;
+};
+
+template <bool SWIGLU>
+__global__ void __launch_bounds__(kThreads, 1)
+grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
+                    const __grid_constant__ CUtensorMap map_b, GemmArgs args) {
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t full_bar[kStages];
+    __shared__ __align__(8) uint64_t empty_bar[kStages];
+    __shared__ __align__(8) uint64_t tmem_full_bar;
+    __shared__ __align__(8) uint64_t tmem_empty_bar;
+    __shared__ uint32_t s_tmem_base;
+    __shared__ int s_tile_start[kMaxExperts + 1];
+    __shared__ int s_mt[kMaxExperts];
+    __shared__ int s_row0[kMaxExperts + 1];
+    __shared__ int s_failed;
+
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~uintptr_t(1023));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int E = args.E;
+
+    // schedule from the device-side offsets (single warp scan, E <= 1024)
+    if (warp == 0) {
+        int carry = 0;
+        for (int base = 0; base < E; base += 32) {
+            const int e = base + lane;
+            int mt = 0;
+            if (e < E) {
+                const int r0 = args.offsets[e], r1 = args.offsets[e + 1];
+                mt = r1 > r0 ? (r1 - r0 + BM - 1) / BM : 0;
+                s_mt[e] = mt > 0 ? mt : 1;
+                s_row0[e] = r0;
+            }
+            int incl = mt * args.n_tiles;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int o = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+                if (lane >= off) incl += o;
+            }
+            if (e < E) s_tile_start[e] = carry + incl - mt * args.n_tiles;
+            carry += __shfl_sync(0xFFFFFFFFu, incl, 31);
+        }
+        if (lane == 0) {
+            s_tile_start[E] = carry;
+            s_row0[E] = args.offsets[E];
+            s_failed = 0;
+        }
+    }
+    if (threadIdx.x == 32) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(smem_addr(&full_bar[s]), 1);
+            mbar_init(smem_addr(&empty_bar[s]), 1);
+        }
+        mbar_init(smem_addr(&tmem_full_bar), 1);
+        mbar_init(smem_addr(&tmem_empty_bar), 128);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 2) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                     :: "r"(smem_addr(&s_tmem_base)), "r"(BN) : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+
+    const int total_tiles = s_tile_start[E];
+    const int k_steps = args.K / BK;
+    const uint32_t tmem_base = s_tmem_base;
+
+    if (warp == 0 && lane == 0) {
+        // ------------------------------------------------------ TMA producer
+        uint32_t it = 0;
+        for (int t = blockIdx.x; t < total_tiles && !s_failed; t += gridDim.x) {
+            int e, m, n;
+            tile_coords(t, s_tile_start, s_mt, E, args.n_tiles, e, m, n);
+            const int row_a = s_row0[e] + m * BM;
+            const int row_b = int(e * args.w_rows_per_expert) + n * BN;
+            for (int ks = 0; ks < k_steps; ++ks, ++it) {
+                const int s = it % kStages;
+                const uint32_t ph = (it / kStages) & 1u;
+                if (!mbar_wait(smem_addr(&empty_bar[s]), ph ^ 1u)) { s_failed = 1; break; }
+                const uint32_t a_dst = smem_addr(smem + s * kStageBytes);
+                const uint32_t b_dst = a_dst + kTileABytes;
+                const uint32_t fb = smem_addr(&full_bar[s]);
+                mbar_expect_tx(fb, kStageBytes);
+                tma_load_2d(a_dst, &map_a, ks * BK, row_a, fb);
+                tma_load_2d(b_dst, &map_b, ks * BK, row_b, fb);
+            }
+        }
+    } else if (warp == 1 && lane == 0) {
+        // ------------------------------------------------------ MMA issuer
+        uint32_t it = 0, tile_iter = 0;
+        for (int t = blockIdx.x; t < total_tiles && !s_failed; t += gridDim.x, ++tile_iter) {
+            if (!mbar_wait(smem_addr(&tmem_empty_bar), (tile_iter & 1u) ^ 1u)) { s_failed = 1; break; }
+            tc_fence_after();
+            for (int ks = 0; ks < k_steps; ++ks, ++it) {
+                const int s = it % kStages;
+                const uint32_t ph = (it / kStages) & 1u;
+                if (!mbar_wait(smem_addr(&full_bar[s]), ph)) { s_failed = 1; break; }
+                tc_fence_after();
+                const uint32_t a_base = smem_addr(smem + s * kStageBytes);
+                const uint32_t b_base = a_base + kTileABytes;
+#pragma unroll
+                for (int kk = 0; kk < BK / 16; ++kk) {
+                    // advance 16 bf16 = 32 bytes along K inside the swizzled row
+                    mma_bf16(tmem_base, smem_desc_k128(a_base + kk * 32),
+                             smem_desc_k128(b_base + kk * 32), (ks | kk) != 0);
+                }
+                mma_commit(smem_addr(&empty_bar[s]));     // frees the stage when done
+            }
+            if (s_failed) break;
+            mma_commit(smem_addr(&tmem_full_bar));        // the tile's accumulator is ready
+        }
+    } else if (warp >= 4) {
+        // ------------------------------------------------------ epilogue
+        const int q = warp - 4;                           // TMEM lane quadrant
+        const uint32_t lane_base = uint32_t(q * 32) << 16;
+        uint32_t tile_iter = 0;
+        for (int t = blockIdx.x; t < total_tiles; t += gridDim.x, ++tile_iter) {
+            if (s_failed || !mbar_wait(smem_addr(&tmem_full_bar), tile_iter & 1u)) {
+                s_failed = 1;
+                break;
+            }
+            tc_fence_after();
+            int e, m, n;
+            tile_coords(t, s_tile_start, s_mt, E, args.n_tiles, e, m, n);
+            const int64_t row = int64_t(s_row0[e]) + m * BM + q * 32 + lane;
+            const bool row_ok = row < s_row0[e + 1];
+            uint16_t* out = static_cast<uint16_t*>(args.out);
+            if (SWIGLU) {
+                // columns [0,128) gate, [128,256) up, for hidden j0 = n*128
+#pragma unroll 1
+                for (int c = 0; c < BN / 2; c += 32) {
+                    float g[32], u[32];
+                    tmem_ld32(tmem_base + lane_base + c, g);
+                    tmem_ld32(tmem_base + lane_base + BN / 2 + c, u);
+                    if (row_ok) {
+                        uint4* dst = reinterpret_cast<uint4*>(out + row * args.out_cols +
+                                                              int64_t(n) * (BN / 2) + c);
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            uint32_t w[4];
+#pragma unroll
+                            for (int h = 0; h < 4; ++h) {
+                                const int i0 = v * 8 + 2 * h;
+                                const float h0 = g[i0] / (1.0f + expf(-g[i0])) * u[i0];
+                                const float h1 = g[i0 + 1] / (1.0f + expf(-g[i0 + 1])) * u[i0 + 1];
+                                w[h] = pack_bf16x2_rn(h0, h1);
+                            }
+                            dst[v] = make_uint4(w[0], w[1], w[2], w[3]);
+                        }
+                    }
+                }
+            } else {
+#pragma unroll 1
+                for (int c = 0; c < BN; c += 32) {
+                    float a[32];
+                    tmem_ld32(tmem_base + lane_base + c, a);
+                    if (row_ok) {
+                        uint4* dst = reinterpret_cast<uint4*>(out + row * args.out_cols +
+                                                              int64_t(n) * BN + c);
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            const int i0 = v * 8;
+                            dst[v] = make_uint4(pack_bf16x2_rn(a[i0], a[i0 + 1]),
+                                                pack_bf16x2_rn(a[i0 + 2], a[i0 + 3]),
+                                                pack_bf16x2_rn(a[i0 + 4], a[i0 + 5]),
+                                                pack_bf16x2_rn(a[i0 + 6], a[i0 + 7]));
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(smem_addr(&tmem_empty_bar));
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (s_failed && threadIdx.x == 0) {
+        args.header->status = MOE_ERR_TIMEOUT;
+        args.header->detail = blockIdx.x;
+    }
+    if (warp == 2) {
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;"
+                     :: "r"(tmem_base), "r"(BN) : "memory");
+    }
+}
+
+__global__ void reset_status_kernel(WsHeader* header) {
+    header->status = MOE_OK;
+    header->detail = 0;
+}
+
+// --------------------------------------------------------------- prepack
+// w_up [E,H,2I] -> [E,2I,H] with rows in 128-blocks [gate | up];
+// w_down [E,I,H] -> [E,H,I].  32x32 tiles through shared memory.
+__global__ void pack_transpose_kernel(const uint16_t* __restrict__ src, uint16_t* __restrict__ dst,
+                                      int64_t R, int64_t C, int interleave_I) {
+    // src [E][R][C] -> dst [E][C'][R] where C' is C with the gate/up
+    // interleave applied when interleave_I > 0 (then C = 2I)
+    __shared__ uint16_t tile[32][33];
+    const int64_t e = blockIdx.z;
+    const int64_t r0 = int64_t(blockIdx.y) * 32, c0 = int64_t(blockIdx.x) * 32;
+    const uint16_t* s = src + e * R * C;
+    uint16_t* d = dst + e * R * C;
+    for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+        const int64_t r = r0 + i, c = c0 + threadIdx.x;
+        if (r < R && c < C) tile[i][threadIdx.x] = s[r * C + c];
+    }
+    __syncthreads();
+    for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+        const int64_t c = c0 + i, r = r0 + threadIdx.x;
+        if (r < R && c < C) {
+            int64_t pr = c;
+            if (interleave_I > 0) {
+                const int64_t I = interleave_I;
+                const int64_t j = c < I ? c : c - I;
+                pr = (j / 128) * 256 + (c < I ? 0 : 128) + (j % 128);
+            }
+            d[pr * R + r] = tile[threadIdx.x][i];
+        }
+    }
+}
+
+// ------------------------------------------------------------ tensor maps
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return nullptr;
+        fn = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    return fn;
+}
+
+// 2D bf16 map over a row-major [rows, cols] matrix, box [box_rows, 64 cols],
+// 128-byte swizzle; reads past the last row return zeros.
+bool make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {cuuint64_t(cols), cuuint64_t(rows)};
+    const cuuint64_t strides[1] = {cuuint64_t(cols) * 2};
+    const cuuint32_t box[2] = {cuuint32_t(BK), cuuint32_t(box_rows)};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+}
+
+moe_status_t check_shapes(int64_t N, int E, int64_t H, int64_t I) {
+    if (N < 0 || E < 1 || H < 1 || I < 1) return MOE_ERR_INVALID_ARG;
+    if (E > kMaxExperts || H % BN != 0 || I % 128 != 0 || H % BK != 0 || I % BK != 0)
+        return MOE_ERR_UNSUPPORTED;
+    if (N >= (int64_t(1) << 31) || int64_t(E) * 2 * I >= (int64_t(1) << 31) ||
+        int64_t(E) * H >= (int64_t(1) << 31))
+        return MOE_ERR_UNSUPPORTED;
+    return MOE_OK;
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" moe_status_t moe_grouped_swiglu_pack(const void* w_up, const void* w_down, int E,
+                                                int64_t H, int64_t I, void* w_up_packed,
+                                                void* w_down_packed, void* stream) {
+    const moe_status_t st = check_shapes(0, E, H, I);
+    if (st != MOE_OK) return st;
+    if (!w_up || !w_down || !w_up_packed || !w_down_packed) return MOE_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const dim3 block(32, 8);
+    const dim3 g_up(unsigned((2 * I + 31) / 32), unsigned((H + 31) / 32), unsigned(E));
+    pack_transpose_kernel<<<g_up, block, 0, s>>>(static_cast<const uint16_t*>(w_up),
+                                                 static_cast<uint16_t*>(w_up_packed), H, 2 * I,
+                                                 int(I));
+    if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
+    const dim3 g_down(unsigned((H + 31) / 32), unsigned((I + 31) / 32), unsigned(E));
+    pack_transpose_kernel<<<g_down, block, 0, s>>>(static_cast<const uint16_t*>(w_down),
+                                                   static_cast<uint16_t*>(w_down_packed), I, H, 0);
+    return launch_status();
+}
+
+extern "C" moe_status_t moe_grouped_swiglu_workspace_size(int64_t N, int E, int64_t H, int64_t I,
+                                                          size_t* bytes) {
+    if (!bytes) return MOE_ERR_INVALID_ARG;
+    const moe_status_t st = check_shapes(N, E, H, I);
+    if (st != MOE_OK) return st;
+    *bytes = kWsAlign + align_up(size_t(N > 0 ? N : 1) * size_t(I) * 2, kWsAlign);
+    return MOE_OK;
+}
+
+extern "C" moe_status_t moe_grouped_swiglu(const void* x, const void* w_up_packed,
+                                           const void* w_down_packed, const int32_t* offsets,
+                                           int64_t N, int E, int64_t H, int64_t I, void* y,
+                                           void* workspace, size_t workspace_bytes,
+                                           void* stream) {
+    moe_status_t st = check_shapes(N, E, H, I);
+    if (st != MOE_OK) return st;
+    if (!offsets || (N > 0 && (!x || !w_up_packed || !w_down_packed || !y)))
+        return MOE_ERR_INVALID_ARG;
+    size_t need = 0;
+    moe_grouped_swiglu_workspace_size(N, E, H, I, &need);
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & (kWsAlign - 1)) ||
+        workspace_bytes < need)
+        return MOE_ERR_WORKSPACE;
+    if (!aligned16(x) || !aligned16(w_up_packed) || !aligned16(w_down_packed) || !aligned16(y))
+        return MOE_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    WsHeader* header = static_cast<WsHeader*>(workspace);
+    reset_status_kernel<<<1, 1, 0, s>>>(header);
+    if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
+    if (N == 0) return MOE_OK;
+    void* hidden = static_cast<char*>(workspace) + kWsAlign;
+
+    CUtensorMap m_x, m_up, m_h, m_down;
+    if (!make_map(&m_x, x, N, H, BM) || !make_map(&m_up, w_up_packed, int64_t(E) * 2 * I, H, BN) ||
+        !make_map(&m_h, hidden, N, I, BM) || !make_map(&m_down, w_down_packed, int64_t(E) * H, I, BN))
+        return MOE_ERR_CUDA;
+
+    static bool attr_set[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+        if (cudaFuncSetAttribute(grouped_gemm_kernel<true>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess ||
+            cudaFuncSetAttribute(grouped_gemm_kernel<false>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        attr_set[dev] = true;
+    }
+    const int grid = sm_count();
+    GemmArgs a1{offsets, E, int(H), int(I / 128), 2 * I, hidden, I, header};
+    grouped_gemm_kernel<true><<<grid, kThreads, kSmemBytes, s>>>(m_x, m_up, a1);
+    if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
+    GemmArgs a2{offsets, E, int(I), int(H / BN), H, y, H, header};
+    grouped_gemm_kernel<false><<<grid, kThreads, kSmemBytes, s>>>(m_h, m_down, a2);
+    return launch_status();
+}
