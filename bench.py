@@ -36,7 +36,6 @@ UNIT = "routed-tokens/s"
 WORKLOAD = "skewed"
 FALLBACK_HBM_GBS = 6800.0
 ROUTE_LAUNCHES = 2       # top-k, scatter (the scan is fused for up to 256 token blocks)
-STEP_LAUNCHES = ROUTE_LAUNCHES + 3
 
 
 # ------------------------------------------------------------ host-side logic
@@ -169,6 +168,24 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ our arm
 
+def layer_flops_bytes(N, H, E, I):
+    """Grouped SwiGLU: 2*N*H*2I (GMM1) + 2*N*I*H (GMM2) flops; bytes = both
+    weight sets once, x once, hidden written and read once, y once."""
+    flops = 6 * N * H * I
+    byts = E * (H * 2 * I + I * H) * 2 + N * H * 2 + 2 * N * I * 2 + N * H * 2
+    return flops, byts
+
+
+def measured_tensor_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops_sustained"]), float(d["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 1700.0, 1900.0, "fallback"
+
+
 def run_ours(args, rank, world, local_rank):
     import numpy as np
     import torch
@@ -178,7 +195,8 @@ def run_ours(args, rank, world, local_rank):
 
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
-    d = wl.make(WORKLOAD, with_grad=True, T=args.tokens)
+    layer = args.workload == "layer"
+    d = wl.make(args.workload, with_grad=not layer, with_weights=layer, T=args.tokens)
     W = d["workload"]
     T, H, E, k, b = d["x"].shape[0], W.H, W.E, W.k, 2
     N = T * k
@@ -186,34 +204,48 @@ def run_ours(args, rank, world, local_rank):
     bf = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)
     h_logits = torch.from_numpy(d["logits"]).pin_memory()
     h_x = bf(d["x"]).pin_memory()
-    h_g = bf(d["grad_out"]).pin_memory()
-    logits, x, g = h_logits.to(dev), h_x.to(dev), h_g.to(dev)
+    h_g = None if layer else bf(d["grad_out"]).pin_memory()
+    logits, x = h_logits.to(dev), h_x.to(dev)
+    g = None if layer else h_g.to(dev)
 
     stream = torch.cuda.Stream(device=dev)
     with torch.cuda.stream(stream):
         r = moe.moe_route(logits, k)
         xp = torch.empty((N, H), dtype=torch.bfloat16, device=dev)
         out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
-        gy = torch.empty((N, H), dtype=torch.bfloat16, device=dev)
-        gp = torch.empty((T, k), dtype=torch.float32, device=dev)
-    names = ["route", "permute", "combine", "combine_backward"]
+        if layer:
+            # one-time weight layout (model-load step, outside the timed region)
+            up_p, down_p = moe.moe_grouped_swiglu_pack(bf(d["w_up"]).to(dev),
+                                                       bf(d["w_down"]).to(dev), stream=stream)
+            y = torch.empty((N, H), dtype=torch.bfloat16, device=dev)
+            gs_ws = torch.empty(moe.moe_grouped_swiglu_workspace_size(N, E, H, W.I),
+                                dtype=torch.uint8, device=dev)
+        else:
+            gy = torch.empty((N, H), dtype=torch.bfloat16, device=dev)
+            gp = torch.empty((T, k), dtype=torch.float32, device=dev)
+    names = (["route", "permute", "grouped_swiglu", "combine"] if layer else
+             ["route", "permute", "combine", "combine_backward"])
 
     def step(lg, xx, gg, ev=None):
-        if ev is not None:
-            ev[0].record(stream)
+        def mark(i):
+            if ev is not None:
+                ev[i].record(stream)
+        mark(0)
         moe.moe_route(lg, k, out=r, stream=stream)
-        if ev is not None:
-            ev[1].record(stream)
+        mark(1)
         moe.moe_permute(xx, r.slot_pos, out=xp, stream=stream)
-        if ev is not None:
-            ev[2].record(stream)
-        moe.moe_combine(xp, r.slot_pos, r.topk_w, out=out, stream=stream)
-        if ev is not None:
-            ev[3].record(stream)
-        moe.moe_combine_backward(gg, xp, r.slot_pos, r.topk_w, grad_expert_out=gy,
-                                 grad_probs=gp, stream=stream)
-        if ev is not None:
-            ev[4].record(stream)
+        mark(2)
+        if layer:
+            moe.moe_grouped_swiglu(xp, up_p, down_p, r.offsets, out=y, workspace=gs_ws,
+                                   stream=stream)
+            mark(3)
+            moe.moe_combine(y, r.slot_pos, r.topk_w, out=out, stream=stream)
+        else:
+            moe.moe_combine(xp, r.slot_pos, r.topk_w, out=out, stream=stream)
+            mark(3)
+            moe.moe_combine_backward(gg, xp, r.slot_pos, r.topk_w, grad_expert_out=gy,
+                                     grad_probs=gp, stream=stream)
+        mark(4)
 
     import torch.distributed as dist
     dist_on = dist.is_available() and dist.is_initialized()
@@ -242,23 +274,26 @@ def run_ours(args, rank, world, local_rank):
     per = {n: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(args.steps)) / 1e3
            for j, n in enumerate(names)}
     max_elapsed = reduce_max(elapsed, dev)
+    if layer:
+        assert moe.moe_workspace_status(gs_ws, stream) == 0, "grouped SwiGLU pipeline timed out"
 
     # -------- end to end through the public API from pinned host buffers
     h_out = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
-    h_gp = torch.empty((T, k), dtype=torch.float32).pin_memory()
-    h2d = h_logits.numel() * 4 + h_x.numel() * 2 + h_g.numel() * 2
-    d2h = h_out.numel() * 2 + h_gp.numel() * 4
+    h_gp = None if layer else torch.empty((T, k), dtype=torch.float32).pin_memory()
+    h2d = h_logits.numel() * 4 + h_x.numel() * 2 + (0 if layer else h_g.numel() * 2)
+    d2h = h_out.numel() * 2 + (0 if layer else h_gp.numel() * 4)
     e2e_steps = 0 if args.no_e2e else max(1, min(args.steps, 20))
 
     def e2e_step():
         with torch.cuda.stream(stream):
             lg = h_logits.to(dev, non_blocking=True)
             xx = h_x.to(dev, non_blocking=True)
-            gg = h_g.to(dev, non_blocking=True)
+            gg = None if layer else h_g.to(dev, non_blocking=True)
         step(lg, xx, gg)
         with torch.cuda.stream(stream):
             h_out.copy_(out, non_blocking=True)
-            h_gp.copy_(gp, non_blocking=True)
+            if not layer:
+                h_gp.copy_(gp, non_blocking=True)
 
     e2e_elapsed = float("nan")
     if e2e_steps:
@@ -280,38 +315,58 @@ def run_ours(args, rank, world, local_rank):
     e2e_value = job_value(N, world, e2e_steps, e2e_elapsed) if e2e_steps else None
     peak, peak_kind = measured_peak()
     alg = algorithmic_bytes(T, H, E, k, b)
+    if layer:
+        fl, by = layer_flops_bytes(N, H, E, W.I)
+        alg["grouped_swiglu"] = by
     kern = {}
     for n in names:
         gbs = alg[n] / per[n] / 1e9
         kern[n] = {"us": round(per[n] * 1e6, 2), "alg_bytes": alg[n], "GB_s": round(gbs, 1),
                    "frac": round(gbs / peak, 4)}
     dominant = max(names, key=lambda n: per[n])
-    traffic = recorded_traffic(dominant, source_digest(*KERNEL_SOURCES[dominant]))
-    ach = alg[dominant] / per[dominant] / 1e9
     pc_time = per["permute"] + per["combine"]
+    if layer:
+        t_sus, t_burst, t_kind = measured_tensor_peak()
+        tf = fl / per["grouped_swiglu"] / 1e12
+        kern["grouped_swiglu"].update({"TFLOP_s": round(tf, 1), "flops": fl,
+                                       "frac_tensor_sustained": round(tf / t_sus, 4),
+                                       "frac_tensor_burst": round(tf / t_burst, 4)})
+        roof = {"bound": "tensor", "kernel": "grouped_swiglu", "achieved": round(tf, 1),
+                "peak": t_sus, "unit": "TFLOP/s", "frac": round(tf / t_sus, 4),
+                "peak_source": f"{t_kind} bf16_tflops_sustained (burst {t_burst})",
+                "hbm_frac": kern["grouped_swiglu"]["frac"], "traffic": None}
+        workload = (f"layer: T={T} H={H} E={E} k={k} I={W.I} bf16, full MoE layer forward "
+                    "(route, permute, grouped SwiGLU on tcgen05, combine)")
+        step_desc = "moe_route + moe_permute + moe_grouped_swiglu + moe_combine"
+    else:
+        ach = alg[dominant] / per[dominant] / 1e9
+        roof = {"bound": "hbm", "kernel": dominant, "achieved": round(ach, 1),
+                "peak": peak, "unit": "GB/s", "frac": round(ach / peak, 4),
+                "peak_source": f"{peak_kind} hbm_gbs",
+                "traffic": recorded_traffic(dominant, source_digest(*KERNEL_SOURCES[dominant]))}
+        workload = (f"skewed: T={T} H={H} E={E} k={k} bf16, router logits fp32 with "
+                    "2*log-Zipf(1.1) expert bias")
+        step_desc = "moe_route + moe_permute + moe_combine + moe_combine_backward"
+    launches = ROUTE_LAUNCHES + (1 + 3 + 1 if layer else 3)   # grouped SwiGLU: reset + 2 GEMMs
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": max_elapsed / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded; DeepSeek-shaped shapes, no dataset or weights)",
-        "config": {"workload": f"{WORKLOAD}: T={T} H={H} E={E} k={k} bf16, router logits fp32 "
-                               "with 2*log-Zipf(1.1) expert bias",
-                   "T": T, "H": H, "E": E, "k": k, "routed_tokens_per_step": N,
-                   "step": "moe_route + moe_permute + moe_combine + moe_combine_backward",
-                   "l2": "no flush: step working set ~4.5 GB >> 129 MB L2",
+        "config": {"workload": workload, "T": T, "H": H, "E": E, "k": k,
+                   "routed_tokens_per_step": N, "step": step_desc,
+                   "l2": "no flush: step working set is several GB >> 129 MB L2",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
-        "roofline": {"bound": "hbm", "kernel": dominant, "achieved": round(ach, 1),
-                     "peak": peak, "unit": "GB/s", "frac": round(ach / peak, 4),
-                     "peak_source": f"{peak_kind} hbm_gbs", "traffic": traffic},
+        "roofline": roof,
         "kernels": kern,
         "permute_combine_routed_tokens_per_s": N / pc_time,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps,
-                "path": "pinned host logits/x/grad_out -> device -> step -> out, grad_probs to host"},
-        "gpu_launches": STEP_LAUNCHES * args.steps,
+                "path": "pinned host inputs -> device -> step -> outputs to host"},
+        "gpu_launches": launches * args.steps,
         "clocks": clk.summary(),
     }
-    if not args.no_cpu_baseline:
+    if not args.no_cpu_baseline and not layer:
         line["cpu_baseline"] = cpu_baseline(args.cpu_tokens)
     return line
 
@@ -380,6 +435,9 @@ def main(argv=None):
     ap.add_argument("--tokens", type=int, default=None,
                     help="use only the first TOKENS tokens (small cases for profiling)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg")
+    ap.add_argument("--workload", choices=["skewed", "layer"], default=WORKLOAD,
+                    help="skewed: the dispatch/combine step (default); layer: the full MoE "
+                         "layer forward with the grouped SwiGLU")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("at least 3 warm-up steps")

@@ -196,6 +196,33 @@ def test_combine_bit_exact(dtype, T, H, E, k, drop, weighted):
     assert d.max() == 0, f"max ulp {d.max()}, {np.count_nonzero(d)} mismatches"
 
 
+@pytest.mark.parametrize("k", [2, 4, 8])
+def test_combine_bit_exact_under_cancellation(k):
+    """Rows built to cancel (exactly, or down to a few ulps): every tier of
+    the combine -- float fast path, double-float middle tier, double last
+    resort -- must still give the oracle's double slot-order sum rounded once."""
+    T, H, E = 700, 512, 16
+    rng = np.random.default_rng(100 + k)
+    idx, _ = wl.random_routing(200 + k, T, E, k)
+    r = moe.moe_route_indices(to_dev(idx), None, E)
+    o = oracle.route_indices(idx, None, E)
+    w = np.full((T, k), 0.5, np.float32)
+    w[:, 1::2] = rng.choice([0.5, 0.25, 0.375], size=(T, k // 2)).astype(np.float32)
+    base = rng.standard_normal((T, H)).astype(np.float32)
+    y32 = np.zeros((T * k, H), np.float32)
+    for t in range(T):
+        for j in range(k):
+            p = o["slot_pos"][t, j]
+            sign = 1.0 if j % 2 == 0 else -1.0
+            wiggle = 1.0 + (rng.integers(-3, 4) * 2.0 ** -8 if t % 3 else 0.0)
+            y32[p] = sign * base[t] * (0.5 / w[t, j]) * wiggle
+    y = wl.f32_to_bf16_bits(y32)
+    out = to_host(moe.moe_combine(to_dev(y), r.slot_pos, to_dev(w)))
+    ref, _ = oracle.combine(y, o["slot_pos"], w)
+    d = bf16_ulp_diff(out, ref)
+    assert d.max() == 0, f"max ulp {d.max()}, {np.count_nonzero(d)} mismatches"
+
+
 def test_combine_deterministic_and_stable_across_calls():
     T, H, E, k = 2000, 2048, 64, 8
     idx, w = wl.random_routing(1, T, E, k)

@@ -41,6 +41,12 @@ int grid_for(const void* kernel, int threads, int64_t work_blocks) {
 // Float error bound factor for a k-term FMA chain, rounded up (see header).
 float combine_bound_factor(int k) { return float(k) * 0x1p-24f * (1.0f + 0x1p-15f); }
 
+// Double-float error bound factor (see dd_sum_bf16), rounded up generously.
+float dd_bound_factor(int k) {
+    const float n = 2.0f * float(k);
+    return 4.0f * n * n * 0x1p-48f + float(k) * 0x1p-52f;
+}
+
 // Stage the token's slot rows and weights in shared memory (lanes < k).
 __device__ __forceinline__ void stage_slots(int32_t* s_pos, float* s_w, const int32_t* slot_pos,
                                             const float* topk_w, int64_t t, int k,
@@ -78,6 +84,134 @@ __device__ __noinline__ uint16_t combine_elem_f64_bf16(const uint16_t* y, int64_
         acc = fma(double(s_w[j]), double(bf16_to_f32(y[int64_t(p) * H + h])), acc);
     }
     return f64_to_bf16_rn(acc);
+}
+
+// Knuth TwoSum: s + e == a + b exactly.
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
+    s = __fadd_rn(a, b);
+    const float bp = __fsub_rn(s, a);
+    e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bp)), __fsub_rn(b, bp));
+}
+
+// Middle tier for an element the float fast path could not certify: the
+// slot-order sum in double-float arithmetic (Dekker/Knuth error-free
+// TwoProduct and TwoSum, all on the float pipes), certified against the exact
+// bf16 rounding midpoints around it.  Its error is below
+// 2*(2k*2^-24)^2 * sum|w*y| (Ogita-Rump-Oishi Sum2 bound), plus the double
+// sum's own k*2^-53 * sum|w*y|; if the whole interval lies strictly between
+// the two midpoints of one bf16 value, that value is the rounding of the
+// double slot-order sum.  Returns false when it cannot decide.
+__device__ __forceinline__ bool dd_sum_bf16(const float* w, const float* y, const bool* valid,
+                                            int n, float dd_bound, uint16_t* out) {
+    float hi = 0.0f, lo = 0.0f, a = 0.0f;
+    for (int j = 0; j < n; ++j) {
+        if (!valid[j]) continue;
+        const float p = __fmul_rn(w[j], y[j]);
+        const float ep = __fmaf_rn(w[j], y[j], -p);          // w*y == p + ep exactly
+        float sum, es;
+        two_sum(hi, p, sum, es);
+        hi = sum;
+        lo = __fadd_rn(lo, __fadd_rn(es, ep));
+        a = __fmaf_rn(fabsf(w[j]), fabsf(y[j]), a);
+    }
+    const float s = __fadd_rn(hi, lo);
+    const float b = __fmaf_ru(a, dd_bound, 0x1p-126f);
+    // r = bf16(s); its rounding midpoints m_lo < r < m_hi are exact floats
+    const uint16_t r = f32_to_bf16_rn(s);
+    const float rv = bf16_to_f32(r);
+    const float up = bf16_to_f32(uint16_t(r + 1)), dn = bf16_to_f32(uint16_t(r - 1));
+    const float m_hi = rv >= 0 ? __fmul_rn(__fadd_rn(rv, up), 0.5f) : __fmul_rn(__fadd_rn(rv, dn), 0.5f);
+    const float m_lo = rv >= 0 ? __fmul_rn(__fadd_rn(rv, dn), 0.5f) : __fmul_rn(__fadd_rn(rv, up), 0.5f);
+    if (!(fabsf(rv) > 0x1p-120f && fabsf(rv) < 0x1p120f)) return false;   // leave extremes to double
+    // (hi + lo) - b > m_lo and (hi + lo) + b < m_hi, evaluated so that rounding
+    // can only make the test fail: hi - m_lo is exact (Sterbenz), then round down
+    const float below = __fadd_rd(__fsub_rn(hi, m_lo), __fsub_rd(lo, b));
+    const float above = __fadd_rd(__fsub_rn(m_hi, hi), __fsub_rd(-lo, b));
+    if (below > 0.0f && above > 0.0f) { *out = r; return true; }
+    return false;
+}
+
+// k <= 8: one 16-byte column per lane step with every slot row of it held in
+// registers, so an element whose rounding cannot be certified is recomputed
+// in double from the same registers (no reload).
+template <int KMAX>
+__global__ void __launch_bounds__(kThreads)
+combine_bf16_regs_kernel(const uint4* __restrict__ y, int64_t T, int64_t nvec, int k,
+                         const int32_t* __restrict__ slot_pos, const float* __restrict__ topk_w,
+                         uint4* __restrict__ out, float cbound, float dd_bound) {
+    __shared__ int32_t s_pos[kWarps][kMaxTopK];
+    __shared__ float s_w[kWarps][kMaxTopK];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t n_rows = T * k;
+    for (int64_t t = int64_t(blockIdx.x) * kWarps + warp; t < T;
+         t += int64_t(gridDim.x) * kWarps) {
+        stage_slots(s_pos[warp], s_w[warp], slot_pos, topk_w, t, k, n_rows, lane);
+        int32_t pj[KMAX];
+        float wj[KMAX];
+#pragma unroll
+        for (int j = 0; j < KMAX; ++j) {
+            pj[j] = j < k ? s_pos[warp][j] : -1;
+            wj[j] = j < k ? s_w[warp][j] : 0.0f;
+        }
+        for (int64_t v = lane; v < nvec; v += 32) {
+            uint4 d[KMAX];
+#pragma unroll
+            for (int j = 0; j < KMAX; ++j)
+                d[j] = pj[j] >= 0 ? __ldcs(y + int64_t(pj[j]) * nvec + v) : make_uint4(0, 0, 0, 0);
+            float s[8], a[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) { s[i] = 0.0f; a[i] = 0.0f; }
+#pragma unroll
+            for (int j = 0; j < KMAX; ++j) {
+                if (pj[j] < 0) continue;
+                const float w = wj[j], aw = fabsf(w);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float yv = unpack_bf16(d[j], i);
+                    s[i] = __fmaf_rn(w, yv, s[i]);
+                    a[i] = __fmaf_rn(aw, fabsf(yv), a[i]);
+                }
+            }
+            uint4 res;
+            uint32_t open = 0;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float b0 = __fmaf_ru(a[2 * q], cbound, 0x1p-126f);
+                const float b1 = __fmaf_ru(a[2 * q + 1], cbound, 0x1p-126f);
+                const uint32_t lo = pack_bf16x2_rn(__fsub_rd(s[2 * q], b0), __fsub_rd(s[2 * q + 1], b1));
+                const uint32_t hi = pack_bf16x2_rn(__fadd_ru(s[2 * q], b0), __fadd_ru(s[2 * q + 1], b1));
+                set_word(res, q, lo);
+                if (lo != hi) open |= 1u << q;
+            }
+            if (open) {
+                bool valid[KMAX];
+#pragma unroll
+                for (int j = 0; j < KMAX; ++j) valid[j] = pj[j] >= 0;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    if (!(open & (1u << q))) continue;
+                    uint16_t half[2];
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        float yv[KMAX];
+#pragma unroll
+                        for (int j = 0; j < KMAX; ++j) yv[j] = unpack_bf16(d[j], 2 * q + h);
+                        if (!dd_sum_bf16(wj, yv, valid, KMAX, dd_bound, &half[h])) {
+                            // last resort: double, slot order, one rounding
+                            double acc = 0.0;
+#pragma unroll
+                            for (int j = 0; j < KMAX; ++j)
+                                if (valid[j]) acc = fma(double(wj[j]), double(yv[j]), acc);
+                            half[h] = f64_to_bf16_rn(acc);
+                        }
+                    }
+                    set_word(res, q, uint32_t(half[0]) | (uint32_t(half[1]) << 16));
+                }
+            }
+            __stcs(out + t * nvec + v, res);
+        }
+        __syncwarp();
+    }
 }
 
 __global__ void __launch_bounds__(kThreads)
@@ -195,13 +329,6 @@ combine_elem_kernel(const E* __restrict__ y, int64_t T, int64_t H, int k,
 }
 
 // ---------------------------------------------------------------- backward
-
-// Knuth TwoSum: s + e == a + b exactly.
-__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
-    s = __fadd_rn(a, b);
-    const float bp = __fsub_rn(s, a);
-    e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bp)), __fsub_rn(b, bp));
-}
 
 // Double-float accumulate: (hi, lo) += q.
 __device__ __forceinline__ void dd_add1(float& hi, float& lo, float q) {
@@ -465,10 +592,18 @@ extern "C" moe_status_t moe_combine(const void* expert_out, moe_dtype_t dtype, i
     const int64_t want = (T + kWarps - 1) / kWarps;
     const size_t row = size_t(H) * elem_size(dtype);
     if (dtype == MOE_BF16 && row % 16 == 0 && aligned16(expert_out) && aligned16(out)) {
-        combine_bf16_vec_kernel<<<grid_for((const void*)combine_bf16_vec_kernel, kThreads, want),
-                                  kThreads, 0, s>>>(
-            static_cast<const uint4*>(expert_out), T, H / 8, k, slot_pos, topk_w,
-            static_cast<uint4*>(out), combine_bound_factor(k));
+        const uint4* yv = static_cast<const uint4*>(expert_out);
+        uint4* ov = static_cast<uint4*>(out);
+        const float cb = combine_bound_factor(k);
+        if (k <= 8) {
+            const auto kern = k <= 1 ? combine_bf16_regs_kernel<1> : k <= 2 ? combine_bf16_regs_kernel<2>
+                            : k <= 4 ? combine_bf16_regs_kernel<4> : combine_bf16_regs_kernel<8>;
+            kern<<<grid_for((const void*)kern, kThreads, want), kThreads, 0, s>>>(
+                yv, T, H / 8, k, slot_pos, topk_w, ov, cb, dd_bound_factor(k));
+        } else {
+            combine_bf16_vec_kernel<<<grid_for((const void*)combine_bf16_vec_kernel, kThreads, want),
+                                      kThreads, 0, s>>>(yv, T, H / 8, k, slot_pos, topk_w, ov, cb);
+        }
     } else if (dtype == MOE_F32) {
         const auto kern = combine_elem_kernel<float>;
         kern<<<grid_for((const void*)kern, kThreads, want), kThreads, 0, s>>>(

@@ -11,7 +11,9 @@
 //                swizzle) into a 4-stage shared-memory ring
 //   warp 1       one thread issues tcgen05.mma (M=128, N=256, K=16) and
 //                tcgen05.commit to release ring stages / publish the tile
-//   warp 2       allocates / frees the 256 tensor-memory columns
+//   warp 2       allocates / frees 512 tensor-memory columns: two 256-column
+//                accumulators, so the MMAs of the next tile run while the
+//                epilogue drains the previous one
 //   warps 4..7   epilogue: tcgen05.ld of their 32-lane quadrant, SwiGLU (GMM1)
 //                or conversion (GMM2), bf16 stores, rows past the expert's
 //                segment masked
@@ -40,6 +42,7 @@ constexpr int kTileABytes = BM * BK * 2;      // 16 KB
 constexpr int kTileBBytes = BN * BK * 2;      // 32 KB
 constexpr int kStageBytes = kTileABytes + kTileBBytes;
 constexpr int kSmemBytes = kStages * kStageBytes + 1024;  // + alignment slack
+constexpr int kTmemCols = 2 * BN;              // double-buffered accumulator
 constexpr uint32_t kSpinLimit = 1u << 20;     // each try_wait suspends at most ~1 us
 
 // ------------------------------------------------------------- PTX helpers
@@ -179,8 +182,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t full_bar[kStages];
     __shared__ __align__(8) uint64_t empty_bar[kStages];
-    __shared__ __align__(8) uint64_t tmem_full_bar;
-    __shared__ __align__(8) uint64_t tmem_empty_bar;
+    __shared__ __align__(8) uint64_t tmem_full_bar[2];
+    __shared__ __align__(8) uint64_t tmem_empty_bar[2];
     __shared__ uint32_t s_tmem_base;
     __shared__ int s_tile_start[kMaxExperts + 1];
     __shared__ int s_mt[kMaxExperts];
@@ -224,13 +227,15 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
             mbar_init(smem_addr(&full_bar[s]), 1);
             mbar_init(smem_addr(&empty_bar[s]), 1);
         }
-        mbar_init(smem_addr(&tmem_full_bar), 1);
-        mbar_init(smem_addr(&tmem_empty_bar), 128);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_addr(&tmem_full_bar[b]), 1);
+            mbar_init(smem_addr(&tmem_empty_bar[b]), 128);
+        }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 2) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
-                     :: "r"(smem_addr(&s_tmem_base)), "r"(BN) : "memory");
+                     :: "r"(smem_addr(&s_tmem_base)), "r"(kTmemCols) : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
     tc_fence_before();
@@ -265,8 +270,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
         // ------------------------------------------------------ MMA issuer
         uint32_t it = 0, tile_iter = 0;
         for (int t = blockIdx.x; t < total_tiles && !s_failed; t += gridDim.x, ++tile_iter) {
-            if (!mbar_wait(smem_addr(&tmem_empty_bar), (tile_iter & 1u) ^ 1u)) { s_failed = 1; break; }
+            const uint32_t buf = tile_iter & 1u, use = tile_iter >> 1;
+            if (!mbar_wait(smem_addr(&tmem_empty_bar[buf]), (use & 1u) ^ 1u)) { s_failed = 1; break; }
             tc_fence_after();
+            const uint32_t tmem_d = tmem_base + buf * BN;
             for (int ks = 0; ks < k_steps; ++ks, ++it) {
                 const int s = it % kStages;
                 const uint32_t ph = (it / kStages) & 1u;
@@ -277,13 +284,13 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
 #pragma unroll
                 for (int kk = 0; kk < BK / 16; ++kk) {
                     // advance 16 bf16 = 32 bytes along K inside the swizzled row
-                    mma_bf16(tmem_base, smem_desc_k128(a_base + kk * 32),
+                    mma_bf16(tmem_d, smem_desc_k128(a_base + kk * 32),
                              smem_desc_k128(b_base + kk * 32), (ks | kk) != 0);
                 }
                 mma_commit(smem_addr(&empty_bar[s]));     // frees the stage when done
             }
             if (s_failed) break;
-            mma_commit(smem_addr(&tmem_full_bar));        // the tile's accumulator is ready
+            mma_commit(smem_addr(&tmem_full_bar[buf]));   // the tile's accumulator is ready
         }
     } else if (warp >= 4) {
         // ------------------------------------------------------ epilogue
@@ -291,11 +298,13 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
         const uint32_t lane_base = uint32_t(q * 32) << 16;
         uint32_t tile_iter = 0;
         for (int t = blockIdx.x; t < total_tiles; t += gridDim.x, ++tile_iter) {
-            if (s_failed || !mbar_wait(smem_addr(&tmem_full_bar), tile_iter & 1u)) {
+            const uint32_t buf = tile_iter & 1u, use = tile_iter >> 1;
+            if (s_failed || !mbar_wait(smem_addr(&tmem_full_bar[buf]), use & 1u)) {
                 s_failed = 1;
                 break;
             }
             tc_fence_after();
+            const uint32_t tmem_acc = tmem_base + buf * BN;
             int e, m, n;
             tile_coords(t, s_tile_start, s_mt, E, args.n_tiles, e, m, n);
             const int64_t row = int64_t(s_row0[e]) + m * BM + q * 32 + lane;
@@ -306,8 +315,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
 #pragma unroll 1
                 for (int c = 0; c < BN / 2; c += 32) {
                     float g[32], u[32];
-                    tmem_ld32(tmem_base + lane_base + c, g);
-                    tmem_ld32(tmem_base + lane_base + BN / 2 + c, u);
+                    tmem_ld32(tmem_acc + lane_base + c, g);
+                    tmem_ld32(tmem_acc + lane_base + BN / 2 + c, u);
                     if (row_ok) {
                         uint4* dst = reinterpret_cast<uint4*>(out + row * args.out_cols +
                                                               int64_t(n) * (BN / 2) + c);
@@ -317,8 +326,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
 #pragma unroll
                             for (int h = 0; h < 4; ++h) {
                                 const int i0 = v * 8 + 2 * h;
-                                const float h0 = g[i0] / (1.0f + expf(-g[i0])) * u[i0];
-                                const float h1 = g[i0 + 1] / (1.0f + expf(-g[i0 + 1])) * u[i0 + 1];
+                                const float h0 = __fdividef(g[i0], 1.0f + __expf(-g[i0])) * u[i0];
+                                const float h1 =
+                                    __fdividef(g[i0 + 1], 1.0f + __expf(-g[i0 + 1])) * u[i0 + 1];
                                 w[h] = pack_bf16x2_rn(h0, h1);
                             }
                             dst[v] = make_uint4(w[0], w[1], w[2], w[3]);
@@ -329,7 +339,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
 #pragma unroll 1
                 for (int c = 0; c < BN; c += 32) {
                     float a[32];
-                    tmem_ld32(tmem_base + lane_base + c, a);
+                    tmem_ld32(tmem_acc + lane_base + c, a);
                     if (row_ok) {
                         uint4* dst = reinterpret_cast<uint4*>(out + row * args.out_cols +
                                                               int64_t(n) * BN + c);
@@ -345,7 +355,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                 }
             }
             tc_fence_before();
-            mbar_arrive(smem_addr(&tmem_empty_bar));
+            mbar_arrive(smem_addr(&tmem_empty_bar[buf]));
         }
     }
     tc_fence_before();
@@ -357,7 +367,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
     }
     if (warp == 2) {
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;"
-                     :: "r"(tmem_base), "r"(BN) : "memory");
+                     :: "r"(tmem_base), "r"(kTmemCols) : "memory");
     }
 }
 
