@@ -152,7 +152,9 @@ moe_status_t moe_route_noalloc(const float* logits, int64_t T, int E, int k,
  * slot_pos[t, 0..k-1] of `out` (the dedup form: one read, k writes).
  *   x [T,H] (dtype), slot_pos [T,k] (from moe_route), out [T*k,H] (dtype).
  * Rows of `out` that no slot names are left untouched.  Entries of slot_pos
- * outside [0, T*k) are skipped. */
+ * outside [0, T*k) are skipped.  Rows that are 16-byte multiples move with
+ * bulk copies (one load and one store instruction per row piece); a wait on
+ * such a copy that gives up is reported by moe_device_status. */
 moe_status_t moe_permute(const void* x, moe_dtype_t dtype, int64_t T, int64_t H, int k,
                          const int32_t* slot_pos, void* out, void* stream);
 
@@ -256,6 +258,12 @@ moe_status_t moe_grouped_swiglu(const void* x, const void* w_up_packed,
  * `workspace`: MOE_OK, MOE_ERR_DEVICE_CHECK or MOE_ERR_TIMEOUT.  Each call
  * that takes a workspace resets its status word. */
 moe_status_t moe_workspace_status(const void* workspace, void* stream);
+
+/* Waits for `stream`, then reads and clears the library's device status word
+ * of the current device, which kernels that take no workspace (the bulk-copy
+ * permute) set when one of their bounded pipeline waits gives up: MOE_OK or
+ * MOE_ERR_TIMEOUT.  One word per device, shared by all streams. */
+moe_status_t moe_device_status(void* stream);
 
 #ifdef __cplusplus
 }

@@ -155,6 +155,7 @@ def test_permute_bit_exact(dtype, T, H, E, k):
     r = moe.moe_route_indices(to_dev(idx), None, E)
     got = to_host(moe.moe_permute(to_dev(x), r.slot_pos))
     assert got[:n].tobytes() == oracle.permute(x, o["sorted_indices"], n).tobytes()
+    assert moe.moe_device_status() == 0          # no bounded copy wait gave up
 
 
 def test_permute_then_unweighted_combine_k1_identity():

@@ -25,7 +25,7 @@ __all__ = [
     "moe_sort_chunks_workspace_size", "moe_sort_chunks", "moe_chunk_idxs", "moe_combine",
     "moe_combine_backward", "moe_expert_scale", "moe_workspace_status", "RouteResult",
     "moe_route_noalloc", "MOE_ROUTE_NOALLOC_SCRATCH_BYTES", "moe_grouped_swiglu_pack",
-    "moe_grouped_swiglu_workspace_size", "moe_grouped_swiglu",
+    "moe_grouped_swiglu_workspace_size", "moe_grouped_swiglu", "moe_device_status",
 ]
 
 # Size of the library's built-in scratch array used by moe_route_noalloc.
@@ -77,6 +77,7 @@ def load_library():
             "moe_combine_backward": ([P, P, I, I64, I64, I, P, P, P, P, P], I),
             "moe_expert_scale": ([P, I, I64, I64, I, P, P, P, P], I),
             "moe_workspace_status": ([P, P], I),
+            "moe_device_status": ([P], I),
             "moe_grouped_swiglu_pack": ([P, P, I, I64, I64, P, P, P], I),
             "moe_grouped_swiglu_workspace_size": ([I64, I, I64, I64, PSZ], I),
             "moe_grouped_swiglu": ([P, P, P, P, I64, I, I64, I64, P, P, SZ, P], I),
@@ -441,3 +442,9 @@ def moe_workspace_status(workspace: torch.Tensor, stream=None) -> int:
     workspace (0 = MOE_OK, 6 = MOE_ERR_DEVICE_CHECK, 5 = MOE_ERR_TIMEOUT)."""
     _cuda(workspace, "workspace", torch.uint8)
     return load_library().moe_workspace_status(_p(workspace), _stream(stream))
+
+
+def moe_device_status(stream=None) -> int:
+    """Synchronise the stream, then read and clear the library's device status
+    word (0 = MOE_OK, 5 = MOE_ERR_TIMEOUT from a kernel without a workspace)."""
+    return load_library().moe_device_status(_stream(stream))

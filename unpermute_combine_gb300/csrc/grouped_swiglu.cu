@@ -26,9 +26,7 @@
 // expert's weights through L2.
 // Every wait on an mbarrier is bounded; a wait that gives up records
 // MOE_ERR_TIMEOUT in the workspace status word and the kernel winds down.
-#include <cuda.h>
-
-#include "common.cuh"
+#include "pipeline.cuh"
 
 namespace moe {
 namespace {
@@ -43,40 +41,8 @@ constexpr int kTileBBytes = BN * BK * 2;      // 32 KB
 constexpr int kStageBytes = kTileABytes + kTileBBytes;
 constexpr int kSmemBytes = kStages * kStageBytes + 1024;  // + alignment slack
 constexpr int kTmemCols = 2 * BN;              // double-buffered accumulator
-constexpr uint32_t kSpinLimit = 1u << 20;     // each try_wait suspends at most ~1 us
 
 // ------------------------------------------------------------- PTX helpers
-
-__device__ __forceinline__ uint32_t smem_addr(const void* p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(bar), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
-                 :: "r"(bar), "r"(bytes) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(bar) : "memory");
-}
-
-// Bounded wait for the phase of the given parity; false if it gave up.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-    for (uint32_t i = 0; i < kSpinLimit; ++i) {
-        uint32_t done;
-        asm volatile(
-            "{\n .reg .pred p;\n"
-            " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-            " selp.u32 %0, 1, 0, p;\n}"
-            : "=r"(done) : "r"(bar), "r"(parity) : "memory");
-        if (done) return true;
-    }
-    return false;
-}
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
                                             uint32_t bar) {
@@ -231,7 +197,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
             mbar_init(smem_addr(&tmem_full_bar[b]), 1);
             mbar_init(smem_addr(&tmem_empty_bar[b]), 128);
         }
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        mbar_fence_init();
     }
     if (warp == 2) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"

@@ -5,7 +5,7 @@
 // permute is token-centric ("token dispatcher + fuse_a2a" §1.1
 // index_select, done in the dedup direction): one warp per token reads x[t]
 // once and writes it to its k permuted rows.
-#include "common.cuh"
+#include "pipeline.cuh"
 
 namespace moe {
 namespace {
@@ -50,6 +50,88 @@ permute_kernel(const V* __restrict__ x, int64_t T, int64_t nvec, int k,
         }
         __syncwarp();
     }
+}
+
+// Bulk-copy permute: one warp per CTA.  Lane 0 loads x[t] (in pieces of at
+// most kPieceMax bytes) into a ring of shared-memory stages with bulk copies;
+// once a piece has landed, lanes 0..k-1 each write it to their slot row with
+// a bulk store, so a whole row leaves in one instruction per slot instead of
+// one 16-byte store per lane.  A stage is refilled only after this lane's
+// stores from it have finished reading it (bulk wait_group.read).  Waits on
+// the stage mbarriers are bounded; a timeout stops the CTA and is recorded in
+// *status.
+constexpr int kPieceMax = 16384;
+constexpr int kPermStages = 3;
+
+__global__ void __launch_bounds__(32)
+permute_bulk_kernel(const uint8_t* __restrict__ x, int64_t T, int64_t row_bytes, int piece,
+                    int pieces, int k, const int32_t* __restrict__ slot_pos,
+                    uint8_t* __restrict__ out, uint32_t* __restrict__ status) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ __align__(8) uint64_t full_bar[kPermStages];
+    const int lane = threadIdx.x;
+    const int64_t n_rows = T * k;
+    const int64_t total = T * pieces;
+    const int64_t first = blockIdx.x;
+    const int64_t my_items = first < total ? (total - first + gridDim.x - 1) / gridDim.x : 0;
+    const uint32_t smem0 = smem_addr(smem);
+    if (lane == 0) {
+        for (int s = 0; s < kPermStages; ++s) mbar_init(smem_addr(&full_bar[s]), 1);
+        mbar_fence_init();
+    }
+    __syncwarp();
+
+    auto item_coords = [&](int64_t q, int64_t& t, uint32_t& off, uint32_t& bytes) {
+        const int64_t item = first + q * gridDim.x;
+        t = item / pieces;
+        off = uint32_t(item % pieces) * uint32_t(piece);
+        bytes = uint32_t(min64(piece, row_bytes - off));
+    };
+    auto issue_load = [&](int64_t q) {
+        int64_t t;
+        uint32_t off, bytes;
+        item_coords(q, t, off, bytes);
+        const int s = int(q % kPermStages);
+        const uint32_t fb = smem_addr(&full_bar[s]);
+        mbar_expect_tx(fb, bytes);
+        bulk_load(smem0 + uint32_t(s) * uint32_t(piece), x + t * row_bytes + off, bytes, fb);
+    };
+    auto slot_of = [&](int64_t q) -> int32_t {
+        if (q >= my_items || lane >= k) return -1;
+        int64_t t;
+        uint32_t off, bytes;
+        item_coords(q, t, off, bytes);
+        const int32_t p = slot_pos[t * k + lane];
+        return (p >= 0 && p < n_rows) ? p : -1;
+    };
+
+    if (lane == 0)
+        for (int64_t q = 0; q < my_items && q < kPermStages; ++q) issue_load(q);
+    int32_t p_cur = slot_of(0);
+    bool failed = false;
+    for (int64_t q = 0; q < my_items; ++q) {
+        const int32_t p_next = slot_of(q + 1);               // in flight meanwhile
+        const int s = int(q % kPermStages);
+        const uint32_t ph = uint32_t(q / kPermStages) & 1u;
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(smem_addr(&full_bar[s]), ph))) {
+            failed = true;
+            break;
+        }
+        int64_t t;
+        uint32_t off, bytes;
+        item_coords(q, t, off, bytes);
+        if (p_cur >= 0)
+            bulk_store(out + int64_t(p_cur) * row_bytes + off, smem0 + uint32_t(s) * uint32_t(piece),
+                       bytes);
+        bulk_commit();
+        // the stores of item q-1 have read their stage: refill it with item q-1+S
+        bulk_wait_read<1>();
+        __syncwarp();
+        if (lane == 0 && q >= 1 && q - 1 + kPermStages < my_items) issue_load(q - 1 + kPermStages);
+        p_cur = p_next;
+    }
+    bulk_wait_all();
+    if (failed && lane == 0 && status) atomicExch(status, uint32_t(MOE_ERR_TIMEOUT));
 }
 
 int grid_for(const void* kernel, int threads, size_t smem, int64_t work_blocks) {
@@ -272,10 +354,22 @@ extern "C" moe_status_t moe_permute(const void* x, moe_dtype_t dtype, int64_t T,
     const size_t row = size_t(H) * elem_size(dtype);
     const int64_t blocks = (T + kWarps - 1) / kWarps;
     if (row % 16 == 0 && aligned16(x) && aligned16(out)) {
-        const int g = grid_for((const void*)permute_kernel<uint4>, kThreads, 0, blocks);
-        permute_kernel<uint4><<<g, kThreads, 0, s>>>(
-            static_cast<const uint4*>(x), T, int64_t(row / 16), k, slot_pos,
-            static_cast<uint4*>(out));
+        const int pieces = int((row + kPieceMax - 1) / kPieceMax);
+        const int piece = int(((row + pieces - 1) / pieces + 15) / 16 * 16);
+        const size_t smem = size_t(kPermStages) * piece;
+        static bool attr_set[64] = {};
+        int dev = 0;
+        cudaGetDevice(&dev);
+        if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+            cudaFuncSetAttribute(permute_bulk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kPermStages * kPieceMax);
+            attr_set[dev] = true;
+        }
+        const int64_t items = T * pieces;
+        const int g = int(min64(items, int64_t(sm_count()) * 4));
+        permute_bulk_kernel<<<g, 32, smem, s>>>(static_cast<const uint8_t*>(x), T, int64_t(row),
+                                                piece, pieces, k, slot_pos,
+                                                static_cast<uint8_t*>(out), device_status_word());
     } else if (dtype == MOE_F32) {
         const int g = grid_for((const void*)permute_kernel<float>, kThreads, 0, blocks);
         permute_kernel<float><<<g, kThreads, 0, s>>>(

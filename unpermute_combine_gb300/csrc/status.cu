@@ -1,8 +1,28 @@
 // status.cu -- status strings, ABI version, workspace status read-back, and
 // the per-device SM count used to size persistent grids.
-#include "common.cuh"
+#include <mutex>
+
+#include "pipeline.cuh"
+
+// Status word of kernels that take no workspace (set to MOE_ERR_TIMEOUT by a
+// bounded wait that gave up; read and cleared by moe_device_status).
+static __device__ uint32_t g_device_status;
 
 namespace moe {
+
+uint32_t* device_status_word() {
+    static std::mutex m;
+    static uint32_t* cached[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lock(m);
+    if (!cached[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return nullptr;
+        cached[dev] = static_cast<uint32_t*>(p);
+    }
+    return cached[dev];
+}
 
 int sm_count() {
     static int cached[64] = {};
@@ -48,4 +68,16 @@ extern "C" moe_status_t moe_workspace_status(const void* workspace, void* stream
         case MOE_ERR_TIMEOUT: return static_cast<moe_status_t>(word);
     }
     return MOE_ERR_DEVICE_CHECK;
+}
+
+extern "C" moe_status_t moe_device_status(void* stream) {
+    uint32_t* word = moe::device_status_word();
+    if (!word) return MOE_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint32_t v = 0;
+    if (cudaMemcpyAsync(&v, word, sizeof v, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaMemsetAsync(word, 0, sizeof v, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    return v == 0 ? MOE_OK : MOE_ERR_TIMEOUT;
 }
