@@ -208,6 +208,7 @@ def run_ours(args, rank, world, local_rank):
     logits, x = h_logits.to(dev), h_x.to(dev)
     g = None if layer else h_g.to(dev)
 
+    groups = tuple(int(v) for v in args.route_groups.split(":")) if args.route_groups else None
     stream = torch.cuda.Stream(device=dev)
     with torch.cuda.stream(stream):
         r = moe.moe_route(logits, k)
@@ -231,7 +232,10 @@ def run_ours(args, rank, world, local_rank):
             if ev is not None:
                 ev[i].record(stream)
         mark(0)
-        moe.moe_route(lg, k, out=r, stream=stream)
+        if groups:
+            moe.moe_route_grouped(lg, k, groups[0], groups[1], out=r, stream=stream)
+        else:
+            moe.moe_route(lg, k, out=r, stream=stream)
         mark(1)
         moe.moe_permute(xx, r.slot_pos, out=xp, stream=stream)
         mark(2)
@@ -347,6 +351,9 @@ def run_ours(args, rank, world, local_rank):
         workload = (f"skewed: T={T} H={H} E={E} k={k} bf16, router logits fp32 with "
                     "2*log-Zipf(1.1) expert bias")
         step_desc = "moe_route + moe_permute + moe_combine + moe_combine_backward"
+        if groups:
+            step_desc = step_desc.replace("moe_route", f"moe_route_grouped({groups[0]} groups, "
+                                                       f"{groups[1]} kept)", 1)
     launches = ROUTE_LAUNCHES + (1 + 3 + 1 if layer else 3)   # grouped SwiGLU: reset + 2 GEMMs
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -435,6 +442,8 @@ def main(argv=None):
     ap.add_argument("--tokens", type=int, default=None,
                     help="use only the first TOKENS tokens (small cases for profiling)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg")
+    ap.add_argument("--route-groups", default=None, metavar="G:KG",
+                    help="route with group-limited routing: G expert groups, KG kept")
     ap.add_argument("--workload", choices=["skewed", "layer"], default=WORKLOAD,
                     help="skewed: the dispatch/combine step (default); layer: the full MoE "
                          "layer forward with the grouped SwiGLU")

@@ -103,6 +103,21 @@ moe_status_t moe_route(const float* logits, int64_t T, int E, int k,
                        float* permuted_probs, uint8_t* routing_map,
                        void* workspace, size_t workspace_bytes, void* stream);
 
+/* Group-limited routing, [MOE-OPS] §21: the E experts form n_groups
+ * consecutive groups of E/n_groups (n_groups <= 32, E % n_groups == 0); a
+ * group's score is its largest logit; the topk_groups best groups are kept
+ * (equal scores: the lower group id) and the k experts are chosen among the
+ * kept groups' experts only (k <= topk_groups * E/n_groups), with the same
+ * tie rule, softmax and outputs as moe_route.  n_groups = topk_groups gives
+ * exactly moe_route.  Workspace: moe_route_workspace_size(T, E, k). */
+moe_status_t moe_route_grouped(const float* logits, int64_t T, int E, int k,
+                               int n_groups, int topk_groups,
+                               int32_t* topk_idx, float* topk_w,
+                               int32_t* counts, int32_t* offsets, int32_t* group_list,
+                               int32_t* sorted_indices, int32_t* slot_pos,
+                               float* permuted_probs, uint8_t* routing_map,
+                               void* workspace, size_t workspace_bytes, void* stream);
+
 /* The index half of moe_route for a caller that already has the top-k
  * choices.  topk_idx [T,k] may contain -1 for an empty slot; topk_w (nullable)
  * only feeds permuted_probs (NULL: permuted_probs is not written and may be

@@ -52,6 +52,7 @@ def _load():
             sig = {
                 "oracle_bf16_from_double": [P, I64, P],
                 "oracle_topk_softmax": [P, I64, I, I, P, P, P],
+                "oracle_topk_softmax_grouped": [P, I64, I, I, I, I, P, P, P],
                 "oracle_route_indices": [P, P, I64, I, I, P, P, P, P, P, P, P],
                 "oracle_permute": [P, I, I64, I64, P, I64, P],
                 "oracle_chunk_idxs": [I, I, I, P],
@@ -107,6 +108,20 @@ def topk_softmax(logits, k):
     w64 = np.empty((T, k), np.float64)
     _check(_load().oracle_topk_softmax(_ptr(logits), T, E, k, _ptr(idx), _ptr(w), _ptr(w64)),
            "topk_softmax")
+    return idx, w, w64
+
+
+def topk_softmax_grouped(logits, k, n_groups, topk_groups):
+    """Group-limited top-k: keep the best topk_groups of n_groups consecutive
+    expert groups (scored by their largest logit), then top-k inside them."""
+    logits = _c(logits, np.float32)
+    T, E = logits.shape
+    idx = np.empty((T, k), np.int32)
+    w = np.empty((T, k), np.float32)
+    w64 = np.empty((T, k), np.float64)
+    _check(_load().oracle_topk_softmax_grouped(_ptr(logits), T, E, k, n_groups, topk_groups,
+                                               _ptr(idx), _ptr(w), _ptr(w64)),
+           "topk_softmax_grouped")
     return idx, w, w64
 
 

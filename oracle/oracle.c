@@ -115,6 +115,61 @@ int oracle_topk_softmax(const float* logits, int64_t T, int E, int k,
     return 0;
 }
 
+int oracle_topk_softmax_grouped(const float* logits, int64_t T, int E, int k, int n_groups,
+                                int topk_groups, int32_t* topk_idx, float* topk_w,
+                                double* topk_w_f64) {
+    if (T < 0 || E < 1 || k < 1 || n_groups < 1 || E % n_groups != 0) return -1;
+    if (topk_groups < 1 || topk_groups > n_groups) return -1;
+    const int gsize = E / n_groups;
+    if (k > topk_groups * gsize) return -1;
+    if (T > 0 && (!logits || !topk_idx || !topk_w)) return -1;
+    scored_expert* groups = (scored_expert*)malloc(sizeof(scored_expert) * (size_t)n_groups);
+    scored_expert* row = (scored_expert*)malloc(sizeof(scored_expert) * (size_t)E);
+    uint8_t* keep = (uint8_t*)malloc((size_t)n_groups);
+    double* ex = (double*)malloc(sizeof(double) * (size_t)k);
+    if (!groups || !row || !keep || !ex) { free(groups); free(row); free(keep); free(ex); return -2; }
+    for (int64_t t = 0; t < T; ++t) {
+        const float* l = logits + t * E;
+        /* score every group by its largest logit, then keep the best groups */
+        for (int g = 0; g < n_groups; ++g) {
+            float best = l[g * gsize];
+            for (int i = 1; i < gsize; ++i)
+                if (l[g * gsize + i] > best) best = l[g * gsize + i];
+            groups[g].value = best;
+            groups[g].id = g;
+        }
+        qsort(groups, (size_t)n_groups, sizeof(scored_expert), by_score_then_id);
+        memset(keep, 0, (size_t)n_groups);
+        for (int i = 0; i < topk_groups; ++i) keep[groups[i].id] = 1;
+        /* top-k among the experts of the kept groups */
+        int n = 0;
+        for (int e = 0; e < E; ++e) {
+            if (!keep[e / gsize]) continue;
+            row[n].value = l[e];
+            row[n].id = e;
+            ++n;
+        }
+        qsort(row, (size_t)n, sizeof(scored_expert), by_score_then_id);
+        double s0 = (double)row[0].value;
+        double total = 0.0;
+        for (int j = 0; j < k; ++j) {
+            ex[j] = exp((double)row[j].value - s0);
+            total += ex[j];
+        }
+        for (int j = 0; j < k; ++j) {
+            double w = ex[j] / total;
+            topk_idx[t * k + j] = row[j].id;
+            topk_w[t * k + j] = (float)w;
+            if (topk_w_f64) topk_w_f64[t * k + j] = w;
+        }
+    }
+    free(groups);
+    free(row);
+    free(keep);
+    free(ex);
+    return 0;
+}
+
 /* ------------------------------------------------------ routing indices */
 
 int oracle_route_indices(const int32_t* topk_idx, const float* topk_w,

@@ -52,6 +52,17 @@ int oracle_bf16_from_double(const double* v, int64_t n, uint16_t* out);
 int oracle_topk_softmax(const float* logits, int64_t T, int E, int k,
                         int32_t* topk_idx, float* topk_w, double* topk_w_f64);
 
+/* Group-limited top-k, [MOE-OPS] §21: the E experts form n_groups
+ * consecutive groups of E/n_groups; a group's score is its largest logit;
+ * the topk_groups groups with the largest scores are kept (equal scores: the
+ * lower group id); then top-k as in oracle_topk_softmax over the experts of
+ * the kept groups only, and the softmax over those k scores.
+ * Requires E % n_groups == 0, 1 <= topk_groups <= n_groups and
+ * k <= topk_groups * (E / n_groups). */
+int oracle_topk_softmax_grouped(const float* logits, int64_t T, int E, int k, int n_groups,
+                                int topk_groups, int32_t* topk_idx, float* topk_w,
+                                double* topk_w_f64);
+
 /* From topk_idx [T,k] build, following [DISPATCH] §1.1 and [MOE-OPS] §7:
  *  routing_map [T,E]   1 where expert e is among token t's choices (nullable)
  *  counts [E]          tokens per expert (column sums of the routing map)

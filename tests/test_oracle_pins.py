@@ -176,6 +176,48 @@ def test_softmax_closed_forms():
     np.testing.assert_allclose(w2, w, atol=1e-6)
 
 
+def test_grouped_topk_with_all_groups_is_plain_topk():
+    rng = np.random.default_rng(21)
+    logits = rng.standard_normal((50, 24)).astype(np.float32)
+    for n_groups in (1, 2, 3, 4, 6, 8, 24):
+        idx, w, _ = oracle.topk_softmax_grouped(logits, 5, n_groups, n_groups)
+        idx0, w0, _ = oracle.topk_softmax(logits, 5)
+        assert (idx == idx0).all() and (w == w0).all()
+
+
+def test_grouped_topk_brute_force_tiny():
+    for seed in range(30):
+        rng = np.random.default_rng(400 + seed)
+        n_groups = int(rng.integers(2, 5))
+        gsize = int(rng.integers(1, 4))
+        E = n_groups * gsize
+        G = int(rng.integers(1, n_groups + 1))
+        k = int(rng.integers(1, G * gsize + 1))
+        T = 4
+        if seed % 2:
+            logits = rng.integers(0, 3, (T, E)).astype(np.float32)      # ties
+        else:
+            logits = rng.standard_normal((T, E)).astype(np.float32)
+        idx, w, w64 = oracle.topk_softmax_grouped(logits, k, n_groups, G)
+        for t in range(T):
+            score = [max(logits[t, g * gsize:(g + 1) * gsize]) for g in range(n_groups)]
+            # the kept groups: the best G by (score desc, id asc), over all G-subsets
+            best = max(itertools.combinations(range(n_groups), G),
+                       key=lambda s: sorted(((score[g], -g) for g in s), reverse=True))
+            allowed = [e for e in range(E) if e // gsize in best]
+            ref = sorted(allowed, key=lambda e: (-logits[t, e], e))[:k]
+            assert idx[t].tolist() == ref
+            np.testing.assert_allclose(w64[t].sum(), 1.0, rtol=1e-14)
+
+
+def test_grouped_topk_rejects_bad_shapes():
+    z = np.zeros((2, 12), np.float32)
+    with pytest.raises(ValueError):
+        oracle.topk_softmax_grouped(z, 2, 5, 2)      # 12 experts do not split into 5 groups
+    with pytest.raises(ValueError):
+        oracle.topk_softmax_grouped(z, 7, 4, 2)      # 2 groups of 3 cannot give 7 experts
+
+
 def test_topk_rejects_bad_k():
     with pytest.raises(ValueError):
         oracle.topk_softmax(np.zeros((2, 4), np.float32), 5)

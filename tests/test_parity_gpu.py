@@ -94,6 +94,30 @@ def test_route_all_tokens_on_one_expert():
     assert c[37] == T and c.sum() == T
 
 
+@pytest.mark.parametrize("T,E,k,G,KG,ties", [(16384, 256, 8, 8, 4, False), (3000, 64, 6, 4, 2, False),
+                                              (777, 256, 8, 8, 4, True), (500, 96, 4, 32, 3, False),
+                                              (300, 40, 5, 5, 5, False), (129, 1024, 16, 16, 2, False),
+                                              (64, 8, 2, 2, 1, True)])
+def test_route_grouped(T, E, k, G, KG, ties):
+    if ties:
+        logits = wl.tie_logits(T + E, T, E)
+    else:
+        logits = np.random.default_rng(T + G).standard_normal((T, E)).astype(np.float32)
+    r = moe.moe_route_grouped(to_dev(logits), k, G, KG, routing_map=True)
+    torch.cuda.synchronize()
+    idx, w, w64 = oracle.topk_softmax_grouped(logits, k, G, KG)
+    o = oracle.route_indices(idx, w, E)
+    o.update(topk_idx=idx, topk_w=w)
+    _assert_route_equal(r, o, E)
+
+
+def test_route_grouped_rejects_bad_groups():
+    x = to_dev(np.zeros((4, 12), np.float32))
+    for args in [(2, 5, 2), (7, 4, 2), (2, 3, 4), (2, 0, 1)]:
+        with pytest.raises(moe.MoeError):
+            moe.moe_route_grouped(x, *args)
+
+
 def test_route_indices_dispatcher_worked_example(golden):
     g = golden("dispatcher_permute_example.json")
     idx = np.array(g["topk_idx_k2"], np.int32)

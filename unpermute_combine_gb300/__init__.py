@@ -26,6 +26,7 @@ __all__ = [
     "moe_combine_backward", "moe_expert_scale", "moe_workspace_status", "RouteResult",
     "moe_route_noalloc", "MOE_ROUTE_NOALLOC_SCRATCH_BYTES", "moe_grouped_swiglu_pack",
     "moe_grouped_swiglu_workspace_size", "moe_grouped_swiglu", "moe_device_status",
+    "moe_route_grouped",
 ]
 
 # Size of the library's built-in scratch array used by moe_route_noalloc.
@@ -69,6 +70,7 @@ def load_library():
             "moe_route": ([P, I64, I, I, P, P, P, P, P, P, P, P, P, P, SZ, P], I),
             "moe_route_indices": ([P, P, I64, I, I, P, P, P, P, P, P, P, P, SZ, P], I),
             "moe_route_noalloc": ([P, I64, I, I, P, P, P, P, P, P, P, P, P, P], I),
+            "moe_route_grouped": ([P, I64, I, I, I, I, P, P, P, P, P, P, P, P, P, P, SZ, P], I),
             "moe_permute": ([P, I, I64, I64, I, P, P, P], I),
             "moe_sort_chunks_workspace_size": ([I, PSZ], I),
             "moe_sort_chunks": ([P, I, I64, I64, P, P, I, P, P, SZ, P], I),
@@ -192,6 +194,33 @@ def moe_route(logits: torch.Tensor, k: int, *, routing_map: bool = False,
         _p(logits), T, E, k, _p(out.topk_idx), _p(out.topk_w), _p(out.counts), _p(out.offsets),
         _p(out.group_list), _p(out.sorted_indices), _p(out.slot_pos), _p(out.permuted_probs),
         _p(out.routing_map), _p(ws), ws.numel(), _stream(stream)))
+    return out
+
+
+def moe_route_grouped(logits: torch.Tensor, k: int, n_groups: int, topk_groups: int, *,
+                      routing_map: bool = False, workspace: Optional[torch.Tensor] = None,
+                      out: Optional[RouteResult] = None, stream=None) -> RouteResult:
+    """Group-limited routing: keep the topk_groups best of n_groups consecutive
+    expert groups (scored by their largest logit), then route as moe_route."""
+    _cuda(logits, "logits", torch.float32, 2)
+    T, E = logits.shape
+    ws = _workspace(moe_route_workspace_size(T, E, k), logits,
+                    workspace if out is None else out.workspace)
+    if out is None:
+        i32 = torch.int32
+        out = RouteResult(
+            topk_idx=_empty((T, k), i32, logits), topk_w=_empty((T, k), torch.float32, logits),
+            counts=_empty((E,), i32, logits), offsets=_empty((E + 1,), i32, logits),
+            group_list=_empty((E,), i32, logits), sorted_indices=_empty((T * k,), i32, logits),
+            slot_pos=_empty((T, k), i32, logits),
+            permuted_probs=_empty((T * k,), torch.float32, logits),
+            routing_map=_empty((T, E), torch.uint8, logits) if routing_map else None,
+            workspace=ws)
+    _ok("moe_route_grouped", load_library().moe_route_grouped(
+        _p(logits), T, E, k, n_groups, topk_groups, _p(out.topk_idx), _p(out.topk_w),
+        _p(out.counts), _p(out.offsets), _p(out.group_list), _p(out.sorted_indices),
+        _p(out.slot_pos), _p(out.permuted_probs), _p(out.routing_map), _p(ws), ws.numel(),
+        _stream(stream)))
     return out
 
 

@@ -83,11 +83,17 @@ __host__ __device__ constexpr int topk_threads(int nv) {
     return nv <= 8 ? 1024 : nv <= 16 ? 512 : 256;
 }
 
-template <int NV>  // logits per lane: expert e = v*32 + lane, v < NV
+// GROUPED: group-limited routing ("从零理解 MoE 算子" §21).  The E experts form
+// n_groups consecutive groups (n_groups <= 32, one lane per group); a group's
+// score is its largest logit; the topk_groups best groups (equal scores: the
+// lower group id) are kept and the experts of the others are masked before
+// the top-k.
+template <int NV, bool GROUPED>  // logits per lane: expert e = v*32 + lane, v < NV
 __global__ void __launch_bounds__(topk_threads(NV))
 route_topk_kernel(const float* __restrict__ logits, int64_t T, int E, int k,
                   int32_t* __restrict__ topk_idx, float* __restrict__ topk_w,
-                  uint8_t* __restrict__ routing_map, int32_t* __restrict__ hist) {
+                  uint8_t* __restrict__ routing_map, int32_t* __restrict__ hist,
+                  int n_groups, int topk_groups) {
     constexpr int kTopkThreads = topk_threads(NV);
     constexpr int kTopkWarps = kTopkThreads / 32;
     __shared__ int s_hist[kMaxExperts];
@@ -120,6 +126,31 @@ route_topk_kernel(const float* __restrict__ logits, int64_t T, int E, int k,
         for (int v = 0; v < NV; ++v) {
             const int e = v * 32 + lane;
             key[v] = e < E ? value_key(cur[v]) : 0u;
+        }
+        if (GROUPED) {
+            const int gsize = E / n_groups;
+            int gv[NV];
+#pragma unroll
+            for (int v = 0; v < NV; ++v) gv[v] = (v * 32 + lane) / gsize;
+            uint32_t cand = 0;                     // lane g: group g's score
+            for (int g = 0; g < n_groups; ++g) {
+                uint32_t local = 0;
+#pragma unroll
+                for (int v = 0; v < NV; ++v)
+                    if (gv[v] == g && key[v] > local) local = key[v];
+                const uint32_t m = __reduce_max_sync(kFull, local);
+                if (lane == g) cand = m;
+            }
+            uint32_t kept = 0;                     // bit g: group g kept
+            for (int i = 0; i < topk_groups; ++i) {
+                const uint32_t m = __reduce_max_sync(kFull, cand);
+                const int g = int(__reduce_min_sync(kFull, cand == m ? uint32_t(lane) : 0xFFFFFFFFu));
+                kept |= 1u << g;
+                if (lane == g) cand = 0;
+            }
+#pragma unroll
+            for (int v = 0; v < NV; ++v)
+                if (!((kept >> gv[v]) & 1u)) key[v] = 0;   // padding lanes are 0 already
         }
         // this lane's best entry: largest key, lowest v (= lowest id) on ties
         uint32_t bk = 0;
@@ -493,9 +524,14 @@ moe_status_t validate_sizes(int64_t T, int E, int k) {
 
 template <int NV>
 void launch_topk(const float* logits, int64_t T, int E, int k, int32_t* topk_idx, float* topk_w,
-                 uint8_t* routing_map, int32_t* hist, cudaStream_t s) {
-    route_topk_kernel<NV><<<unsigned(num_blocks(T)), topk_threads(NV), 0, s>>>(
-        logits, T, E, k, topk_idx, topk_w, routing_map, hist);
+                 uint8_t* routing_map, int32_t* hist, int n_groups, int topk_groups,
+                 cudaStream_t s) {
+    if (n_groups > 0)
+        route_topk_kernel<NV, true><<<unsigned(num_blocks(T)), topk_threads(NV), 0, s>>>(
+            logits, T, E, k, topk_idx, topk_w, routing_map, hist, n_groups, topk_groups);
+    else
+        route_topk_kernel<NV, false><<<unsigned(num_blocks(T)), topk_threads(NV), 0, s>>>(
+            logits, T, E, k, topk_idx, topk_w, routing_map, hist, 0, 0);
 }
 
 moe_status_t finish_route(const int32_t* topk_idx, const float* topk_w, int64_t T, int E, int k,
@@ -549,11 +585,14 @@ extern "C" moe_status_t moe_route_workspace_size(int64_t T, int E, int k, size_t
     return MOE_OK;
 }
 
-extern "C" moe_status_t moe_route(const float* logits, int64_t T, int E, int k,
-                                  int32_t* topk_idx, float* topk_w, int32_t* counts,
-                                  int32_t* offsets, int32_t* group_list, int32_t* sorted_indices,
-                                  int32_t* slot_pos, float* permuted_probs, uint8_t* routing_map,
-                                  void* workspace, size_t workspace_bytes, void* stream) {
+namespace moe {
+namespace {
+moe_status_t route_from_logits(const float* logits, int64_t T, int E, int k, int n_groups,
+                               int topk_groups, int32_t* topk_idx, float* topk_w,
+                               int32_t* counts, int32_t* offsets, int32_t* group_list,
+                               int32_t* sorted_indices, int32_t* slot_pos, float* permuted_probs,
+                               uint8_t* routing_map, void* workspace, size_t workspace_bytes,
+                               void* stream) {
     moe_status_t st = validate_sizes(T, E, k);
     if (st != MOE_OK) return st;
     if (!counts || !offsets || !group_list) return MOE_ERR_INVALID_ARG;
@@ -567,16 +606,45 @@ extern "C" moe_status_t moe_route(const float* logits, int64_t T, int E, int k,
     int32_t* hist = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + kWsAlign);
     if (T > 0) {
         const int nv = (E + 31) / 32;
-        if (nv <= 1) launch_topk<1>(logits, T, E, k, topk_idx, topk_w, routing_map, hist, s);
-        else if (nv <= 2) launch_topk<2>(logits, T, E, k, topk_idx, topk_w, routing_map, hist, s);
-        else if (nv <= 4) launch_topk<4>(logits, T, E, k, topk_idx, topk_w, routing_map, hist, s);
-        else if (nv <= 8) launch_topk<8>(logits, T, E, k, topk_idx, topk_w, routing_map, hist, s);
-        else if (nv <= 16) launch_topk<16>(logits, T, E, k, topk_idx, topk_w, routing_map, hist, s);
-        else launch_topk<32>(logits, T, E, k, topk_idx, topk_w, routing_map, hist, s);
+        const int g = n_groups, kg = topk_groups;
+        if (nv <= 1) launch_topk<1>(logits, T, E, k, topk_idx, topk_w, routing_map, hist, g, kg, s);
+        else if (nv <= 2) launch_topk<2>(logits, T, E, k, topk_idx, topk_w, routing_map, hist, g, kg, s);
+        else if (nv <= 4) launch_topk<4>(logits, T, E, k, topk_idx, topk_w, routing_map, hist, g, kg, s);
+        else if (nv <= 8) launch_topk<8>(logits, T, E, k, topk_idx, topk_w, routing_map, hist, g, kg, s);
+        else if (nv <= 16) launch_topk<16>(logits, T, E, k, topk_idx, topk_w, routing_map, hist, g, kg, s);
+        else launch_topk<32>(logits, T, E, k, topk_idx, topk_w, routing_map, hist, g, kg, s);
         if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
     }
     return finish_route(topk_idx, topk_w, T, E, k, false, hist, header, counts, offsets,
                         group_list, sorted_indices, slot_pos, permuted_probs, s);
+}
+}  // namespace
+}  // namespace moe
+
+extern "C" moe_status_t moe_route(const float* logits, int64_t T, int E, int k,
+                                  int32_t* topk_idx, float* topk_w, int32_t* counts,
+                                  int32_t* offsets, int32_t* group_list, int32_t* sorted_indices,
+                                  int32_t* slot_pos, float* permuted_probs, uint8_t* routing_map,
+                                  void* workspace, size_t workspace_bytes, void* stream) {
+    return route_from_logits(logits, T, E, k, 0, 0, topk_idx, topk_w, counts, offsets,
+                             group_list, sorted_indices, slot_pos, permuted_probs, routing_map,
+                             workspace, workspace_bytes, stream);
+}
+
+extern "C" moe_status_t moe_route_grouped(const float* logits, int64_t T, int E, int k,
+                                          int n_groups, int topk_groups, int32_t* topk_idx,
+                                          float* topk_w, int32_t* counts, int32_t* offsets,
+                                          int32_t* group_list, int32_t* sorted_indices,
+                                          int32_t* slot_pos, float* permuted_probs,
+                                          uint8_t* routing_map, void* workspace,
+                                          size_t workspace_bytes, void* stream) {
+    if (n_groups < 1 || topk_groups < 1 || topk_groups > n_groups || E < 1 || E % n_groups != 0)
+        return MOE_ERR_INVALID_ARG;
+    if (n_groups > 32) return MOE_ERR_UNSUPPORTED;
+    if (int64_t(k) > int64_t(topk_groups) * (E / n_groups)) return MOE_ERR_INVALID_ARG;
+    return route_from_logits(logits, T, E, k, n_groups, topk_groups, topk_idx, topk_w, counts,
+                             offsets, group_list, sorted_indices, slot_pos, permuted_probs,
+                             routing_map, workspace, workspace_bytes, stream);
 }
 
 extern "C" moe_status_t moe_route_indices(const int32_t* topk_idx, const float* topk_w,
