@@ -176,6 +176,26 @@ def layer_flops_bytes(N, H, E, I):
     return flops, byts
 
 
+def parse_layout(spec):
+    """'cf=1.25,pad' or 'align=128' -> dict (empty: the plain layout)."""
+    out = {}
+    for part in (spec or "").split(","):
+        part = part.strip()
+        if not part:
+            continue
+        if part == "pad":
+            out["pad"] = True
+        elif part.startswith("cf="):
+            out["cf"] = float(part[3:])
+        elif part.startswith("align="):
+            out["align"] = int(part[6:])
+        else:
+            raise ValueError(f"unknown layout option {part!r}")
+    if out.get("pad") and not out.get("cf"):
+        raise ValueError("pad needs a capacity factor (cf=...)")
+    return out
+
+
 def measured_tensor_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -209,20 +229,27 @@ def run_ours(args, rank, world, local_rank):
     g = None if layer else h_g.to(dev)
 
     groups = tuple(int(v) for v in args.route_groups.split(":")) if args.route_groups else None
+    lay = parse_layout(args.layout)
+    cap = moe.moe_expert_capacity(T, k, E, lay["cf"]) if lay.get("cf") else 0
+    rows = (moe.moe_route_layout_rows(T, E, k, cap, lay.get("pad", False), lay.get("align", 1))
+            if lay else N)
     stream = torch.cuda.Stream(device=dev)
     with torch.cuda.stream(stream):
         r = moe.moe_route(logits, k)
-        xp = torch.empty((N, H), dtype=torch.bfloat16, device=dev)
+        rl = (moe.moe_route_layout(r.topk_idx, r.topk_w, E, capacity=cap, pad=lay.get("pad", False),
+                                   alignment=lay.get("align", 1), max_rows=rows, stream=stream)
+              if lay else None)
+        xp = torch.empty((rows, H), dtype=torch.bfloat16, device=dev)
         out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
         if layer:
             # one-time weight layout (model-load step, outside the timed region)
             up_p, down_p = moe.moe_grouped_swiglu_pack(bf(d["w_up"]).to(dev),
                                                        bf(d["w_down"]).to(dev), stream=stream)
-            y = torch.empty((N, H), dtype=torch.bfloat16, device=dev)
-            gs_ws = torch.empty(moe.moe_grouped_swiglu_workspace_size(N, E, H, W.I),
+            y = torch.empty((rows, H), dtype=torch.bfloat16, device=dev)
+            gs_ws = torch.empty(moe.moe_grouped_swiglu_workspace_size(rows, E, H, W.I),
                                 dtype=torch.uint8, device=dev)
         else:
-            gy = torch.empty((N, H), dtype=torch.bfloat16, device=dev)
+            gy = torch.empty((rows, H), dtype=torch.bfloat16, device=dev)
             gp = torch.empty((T, k), dtype=torch.float32, device=dev)
     names = (["route", "permute", "grouped_swiglu", "combine"] if layer else
              ["route", "permute", "combine", "combine_backward"])
@@ -236,18 +263,25 @@ def run_ours(args, rank, world, local_rank):
             moe.moe_route_grouped(lg, k, groups[0], groups[1], out=r, stream=stream)
         else:
             moe.moe_route(lg, k, out=r, stream=stream)
+        rr = r
+        if lay:
+            rr = moe.moe_route_layout(r.topk_idx, r.topk_w, E, capacity=cap,
+                                      pad=lay.get("pad", False), alignment=lay.get("align", 1),
+                                      max_rows=rows, workspace=rl.workspace, stream=stream)
         mark(1)
-        moe.moe_permute(xx, r.slot_pos, out=xp, stream=stream)
+        moe.moe_permute(xx, rr.slot_pos, out=xp, stream=stream)
+        if lay:
+            moe.moe_fill_pad_rows(xp, rr.offsets, rr.counts, stream=stream)
         mark(2)
         if layer:
-            moe.moe_grouped_swiglu(xp, up_p, down_p, r.offsets, out=y, workspace=gs_ws,
+            moe.moe_grouped_swiglu(xp, up_p, down_p, rr.offsets, out=y, workspace=gs_ws,
                                    stream=stream)
             mark(3)
-            moe.moe_combine(y, r.slot_pos, r.topk_w, out=out, stream=stream)
+            moe.moe_combine(y, rr.slot_pos, r.topk_w, out=out, stream=stream)
         else:
-            moe.moe_combine(xp, r.slot_pos, r.topk_w, out=out, stream=stream)
+            moe.moe_combine(xp, rr.slot_pos, r.topk_w, out=out, stream=stream)
             mark(3)
-            moe.moe_combine_backward(gg, xp, r.slot_pos, r.topk_w, grad_expert_out=gy,
+            moe.moe_combine_backward(gg, xp, rr.slot_pos, r.topk_w, grad_expert_out=gy,
                                      grad_probs=gp, stream=stream)
         mark(4)
 
@@ -280,6 +314,8 @@ def run_ours(args, rank, world, local_rank):
     max_elapsed = reduce_max(elapsed, dev)
     if layer:
         assert moe.moe_workspace_status(gs_ws, stream) == 0, "grouped SwiGLU pipeline timed out"
+    if lay:
+        assert moe.moe_workspace_status(rl.workspace, stream) == 0, "layout ran out of rows"
 
     # -------- end to end through the public API from pinned host buffers
     h_out = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
@@ -354,6 +390,11 @@ def run_ours(args, rank, world, local_rank):
         if groups:
             step_desc = step_desc.replace("moe_route", f"moe_route_grouped({groups[0]} groups, "
                                                        f"{groups[1]} kept)", 1)
+    if lay:
+        step_desc = step_desc.replace(" + moe_permute", f" + moe_route_layout(capacity={cap}, "
+                                      f"pad={lay.get('pad', False)}, alignment="
+                                      f"{lay.get('align', 1)}, rows={rows}) + moe_permute + "
+                                      "moe_fill_pad_rows", 1)
     launches = ROUTE_LAUNCHES + (1 + 3 + 1 if layer else 3)   # grouped SwiGLU: reset + 2 GEMMs
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -442,6 +483,8 @@ def main(argv=None):
     ap.add_argument("--tokens", type=int, default=None,
                     help="use only the first TOKENS tokens (small cases for profiling)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg")
+    ap.add_argument("--layout", default=None, metavar="SPEC",
+                    help="capacity / padded / aligned layout, e.g. 'cf=1.25,pad' or 'align=128'")
     ap.add_argument("--route-groups", default=None, metavar="G:KG",
                     help="route with group-limited routing: G expert groups, KG kept")
     ap.add_argument("--workload", choices=["skewed", "layer"], default=WORKLOAD,

@@ -64,7 +64,7 @@ typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype_t;
 /* Human-readable name of a status code (static string, never NULL). */
 const char* moe_status_string(moe_status_t status);
 
-/* ABI version of this header (bumped on any signature change). */
+/* ABI version of this header (bumped on any signature change): 2. */
 int moe_abi_version(void);
 
 /* ------------------------------------------------------------------ route
@@ -161,17 +161,65 @@ moe_status_t moe_route_noalloc(const float* logits, int64_t T, int E, int k,
                                int32_t* sorted_indices, int32_t* slot_pos,
                                float* permuted_probs, uint8_t* routing_map, void* stream);
 
+/* ------------------------------------------ capacity, drop and pad, alignment
+ * [MOE-OPS] §18 capacity, the drop_and_pad branch of [DISPATCH] §1.1 and the
+ * expert_alignment of the DeepEP dispatch in [COMBINE] §6.
+ *
+ * moe_expert_capacity (host): ceil(tokens * top_k / num_experts *
+ * capacity_factor) in double ([MOE-OPS] §18: 1024*2/8*1.25 -> 320).
+ *
+ * moe_route_layout: the index outputs of moe_route_indices for a bounded or
+ * padded layout of the permuted rows.
+ *  - the tokens of expert e, in token order, get ranks 0, 1, ...; with
+ *    capacity > 0 an expert keeps ranks < capacity and drops the rest (the
+ *    dropped slots' slot_pos is -1: they move no row and add nothing in the
+ *    combine; the kept weights are not renormalised)
+ *  - counts[e] = kept tokens
+ *  - expert e's segment is `capacity` rows if pad (capacity > 0), else
+ *    counts[e] rounded up to a multiple of alignment (>= 1)
+ *  - offsets [E+1] / group_list [E]: exclusive / inclusive prefix of the
+ *    segments
+ *  - sorted_indices and permuted_probs have max_rows entries; padding rows
+ *    and rows from offsets[E] on hold -1 / 0
+ * max_rows: the caller's capacity for rows, at least
+ * moe_route_layout_rows(...) (E*capacity when padding, else
+ * T*k + E*(alignment-1)); if the layout would still need more, rows past
+ * max_rows are not written and the workspace status is
+ * MOE_ERR_DEVICE_CHECK.  topk_idx may hold -1 (empty slots); invalid ids are
+ * handled as in moe_route_indices.  Workspace: moe_route_workspace_size.
+ *
+ * moe_fill_pad_rows: zero the padding rows [offsets[e] + counts[e],
+ * offsets[e+1]) (clipped to max_rows) of a permuted buffer [max_rows, H], so
+ * a grouped GEMM over the padded segments reads zeros there. */
+moe_status_t moe_expert_capacity(int64_t tokens, int top_k, int num_experts,
+                                 double capacity_factor, int64_t* capacity);
+
+moe_status_t moe_route_layout_rows(int64_t T, int E, int k, int capacity, int pad,
+                                   int alignment, int64_t* max_rows);
+
+moe_status_t moe_route_layout(const int32_t* topk_idx, const float* topk_w, int64_t T,
+                              int E, int k, int capacity, int pad, int alignment,
+                              int64_t max_rows, int32_t* counts, int32_t* offsets,
+                              int32_t* group_list, int32_t* sorted_indices,
+                              int32_t* slot_pos, float* permuted_probs,
+                              void* workspace, size_t workspace_bytes, void* stream);
+
+moe_status_t moe_fill_pad_rows(void* rows, moe_dtype_t dtype, int64_t max_rows, int64_t H,
+                               const int32_t* offsets, const int32_t* counts, int E,
+                               void* stream);
+
 /* ---------------------------------------------------------------- permute
  * [DISPATCH] §1.1 permuted_input = tokens.index_select(0, sorted_indices),
  * computed token by token: every row x[t] is read once and written to rows
  * slot_pos[t, 0..k-1] of `out` (the dedup form: one read, k writes).
- *   x [T,H] (dtype), slot_pos [T,k] (from moe_route), out [T*k,H] (dtype).
+ *   x [T,H] (dtype), slot_pos [T,k] (from moe_route*), out [n_rows,H] (dtype);
+ *   n_rows = T*k for the plain layout, max_rows for moe_route_layout.
  * Rows of `out` that no slot names are left untouched.  Entries of slot_pos
- * outside [0, T*k) are skipped.  Rows that are 16-byte multiples move with
+ * outside [0, n_rows) are skipped.  Rows that are 16-byte multiples move with
  * bulk copies (one load and one store instruction per row piece); a wait on
  * such a copy that gives up is reported by moe_device_status. */
 moe_status_t moe_permute(const void* x, moe_dtype_t dtype, int64_t T, int64_t H, int k,
-                         const int32_t* slot_pos, void* out, void* stream);
+                         int64_t n_rows, const int32_t* slot_pos, void* out, void* stream);
 
 /* ------------------------------------------------------------ sort_chunks
  * [COMBINE] §2.1 and [MOE-OPS] §11-13: cut `in` [N,H] into C consecutive
@@ -206,12 +254,13 @@ moe_status_t moe_chunk_idxs(int R, int L, int inverse, int32_t* idxs);
  * test; elements the test cannot certify are recomputed in double in the same
  * order.  The result is the double slot-order sum rounded once to `dtype`.
  * topk_w = NULL gives the plain sum (the unweighted combine, and the backward
- * of moe_permute).  Empty slots (-1) contribute nothing; a token with no valid
- * slot gets a zero row.
- *   expert_out [T*k,H], slot_pos [T,k], topk_w [T,k] or NULL, out [T,H]. */
+ * of moe_permute).  Empty or dropped slots (-1) contribute nothing; a token
+ * with no valid slot gets a zero row.
+ *   expert_out [n_rows,H] (n_rows = T*k, or max_rows of a padded layout),
+ *   slot_pos [T,k], topk_w [T,k] or NULL, out [T,H]. */
 moe_status_t moe_combine(const void* expert_out, moe_dtype_t dtype, int64_t T, int64_t H,
-                         int k, const int32_t* slot_pos, const float* topk_w, void* out,
-                         void* stream);
+                         int k, int64_t n_rows, const int32_t* slot_pos, const float* topk_w,
+                         void* out, void* stream);
 
 /* [COMBINE] §4: the combine is linear in expert_out and in the weights, so
  *   grad_expert_out[slot_pos[t,j]] = topk_w[t,j] * grad_out[t]
@@ -220,10 +269,10 @@ moe_status_t moe_combine(const void* expert_out, moe_dtype_t dtype, int64_t T, i
  *                     (float32 with error-free compensated summation)
  * topk_w = NULL means weights of 1.  Empty slots write no row and give
  * grad_probs 0.
- *   grad_out [T,H], expert_out [T*k,H], grad_expert_out [T*k,H] (dtype);
+ *   grad_out [T,H], expert_out and grad_expert_out [n_rows,H] (dtype);
  *   grad_probs [T,k] float32. */
 moe_status_t moe_combine_backward(const void* grad_out, const void* expert_out,
-                                  moe_dtype_t dtype, int64_t T, int64_t H, int k,
+                                  moe_dtype_t dtype, int64_t T, int64_t H, int k, int64_t n_rows,
                                   const int32_t* slot_pos, const float* topk_w,
                                   void* grad_expert_out, float* grad_probs, void* stream);
 

@@ -55,6 +55,7 @@ def _load():
                 "oracle_topk_softmax_grouped": [P, I64, I, I, I, I, P, P, P],
                 "oracle_route_indices": [P, P, I64, I, I, P, P, P, P, P, P, P],
                 "oracle_permute": [P, I, I64, I64, P, I64, P],
+                "oracle_route_layout": [P, P, I64, I, I, I, I, I, I64, P, P, P, P, P, P],
                 "oracle_chunk_idxs": [I, I, I, P],
                 "oracle_sort_chunks": [P, I64, I64, P, P, I, P],
                 "oracle_combine": [P, I, I64, I64, I, P, P, P, P],
@@ -67,6 +68,8 @@ def _load():
                 fn = getattr(lib, name)
                 fn.argtypes = args
                 fn.restype = ctypes.c_int
+            lib.oracle_expert_capacity.argtypes = [I64, I, I, ctypes.c_double]
+            lib.oracle_expert_capacity.restype = I64
             _lib = lib
     return _lib
 
@@ -144,6 +147,34 @@ def route_indices(topk_idx, topk_w, E):
         _ptr(topk_idx), _ptr(w), T, E, k, _ptr(out["routing_map"]), _ptr(out["counts"]),
         _ptr(out["offsets"]), _ptr(out["group_list"]), _ptr(out["sorted_indices"]),
         _ptr(out["slot_pos"]), _ptr(out["permuted_probs"])), "route_indices")
+    return out
+
+
+def expert_capacity(tokens, top_k, num_experts, capacity_factor):
+    c = _load().oracle_expert_capacity(int(tokens), int(top_k), int(num_experts),
+                                       float(capacity_factor))
+    _check(0 if c >= 0 else -1, "expert_capacity")
+    return int(c)
+
+
+def route_layout(topk_idx, topk_w, E, capacity=0, pad=False, alignment=1, max_rows=None):
+    """Capacity-bounded / padded / aligned routing layout (see oracle.h)."""
+    topk_idx = _c(topk_idx, np.int32)
+    T, k = topk_idx.shape
+    if max_rows is None:
+        max_rows = E * capacity if pad else T * k + E * (alignment - 1)
+    w = None if topk_w is None else _c(topk_w, np.float32)
+    out = {
+        "counts": np.empty(E, np.int32), "offsets": np.empty(E + 1, np.int32),
+        "group_list": np.empty(E, np.int32), "sorted_indices": np.empty(max_rows, np.int32),
+        "slot_pos": np.empty((T, k), np.int32),
+        "permuted_probs": None if w is None else np.empty(max_rows, np.float32),
+    }
+    _check(_load().oracle_route_layout(
+        _ptr(topk_idx), _ptr(w), T, E, k, int(capacity), int(bool(pad)), int(alignment),
+        int(max_rows), _ptr(out["counts"]), _ptr(out["offsets"]), _ptr(out["group_list"]),
+        _ptr(out["sorted_indices"]), _ptr(out["slot_pos"]), _ptr(out["permuted_probs"])),
+        "route_layout")
     return out
 
 

@@ -246,6 +246,72 @@ int oracle_route_indices(const int32_t* topk_idx, const float* topk_w,
     return 0;
 }
 
+/* ----------------------------------------------- capacity / padded layout */
+
+int64_t oracle_expert_capacity(int64_t tokens, int top_k, int num_experts,
+                               double capacity_factor) {
+    if (tokens < 0 || top_k < 1 || num_experts < 1 || !(capacity_factor > 0.0)) return -1;
+    return (int64_t)ceil((double)tokens * (double)top_k / (double)num_experts * capacity_factor);
+}
+
+int oracle_route_layout(const int32_t* topk_idx, const float* topk_w, int64_t T, int E, int k,
+                        int capacity, int pad, int alignment, int64_t max_rows,
+                        int32_t* counts, int32_t* offsets, int32_t* group_list,
+                        int32_t* sorted_indices, int32_t* slot_pos, float* permuted_probs) {
+    if (T < 0 || E < 1 || k < 1 || capacity < 0 || alignment < 1 || max_rows < 0) return -1;
+    if (pad && capacity < 1) return -1;
+    if (!counts || !offsets || !group_list) return -1;
+    if (T > 0 && (!topk_idx || !slot_pos)) return -1;
+    if (max_rows > 0 && !sorted_indices) return -1;
+    if (permuted_probs && !topk_w && T > 0) return -1;
+    /* rank of each (token, slot) inside its expert, tokens in order */
+    int64_t* seen = (int64_t*)calloc((size_t)E, sizeof(int64_t));
+    if (!seen) return -2;
+    for (int64_t t = 0; t < T; ++t) {
+        for (int j = 0; j < k; ++j) {
+            int32_t e = topk_idx[t * k + j];
+            slot_pos[t * k + j] = -1;
+            if (e == -1) continue;
+            int dup = 0;
+            for (int q = 0; q < j; ++q) dup |= topk_idx[t * k + q] == e;
+            if (e < -1 || e >= E || dup) { free(seen); return -1; }
+            int64_t r = seen[e]++;
+            /* keep the rank for now; turned into a row below */
+            slot_pos[t * k + j] = (capacity > 0 && r >= capacity) ? -1 : (int32_t)r;
+        }
+    }
+    /* segments and their prefixes */
+    int64_t run = 0;
+    offsets[0] = 0;
+    for (int e = 0; e < E; ++e) {
+        int64_t kept = capacity > 0 && seen[e] > capacity ? capacity : seen[e];
+        counts[e] = (int32_t)kept;
+        int64_t seg = pad ? capacity : (kept + alignment - 1) / alignment * alignment;
+        run += seg;
+        offsets[e + 1] = (int32_t)run;
+        group_list[e] = (int32_t)run;
+    }
+    free(seen);
+    if (run > max_rows) return -1;
+    for (int64_t p = 0; p < max_rows; ++p) {
+        sorted_indices[p] = -1;
+        if (permuted_probs) permuted_probs[p] = 0.0f;
+    }
+    /* rank r of expert e goes to row offsets[e] + r */
+    for (int64_t t = 0; t < T; ++t) {
+        for (int j = 0; j < k; ++j) {
+            int32_t r = slot_pos[t * k + j];
+            if (r < 0) continue;
+            int32_t e = topk_idx[t * k + j];
+            int64_t p = offsets[e] + r;
+            slot_pos[t * k + j] = (int32_t)p;
+            sorted_indices[p] = (int32_t)t;
+            if (permuted_probs) permuted_probs[p] = topk_w[t * k + j];
+        }
+    }
+    return 0;
+}
+
 /* --------------------------------------------------------------- permute */
 
 int oracle_permute(const void* x, int elem_size, int64_t T, int64_t H,

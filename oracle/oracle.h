@@ -82,6 +82,29 @@ int oracle_route_indices(const int32_t* topk_idx, const float* topk_w,
                          int32_t* sorted_indices, int32_t* slot_pos,
                          float* permuted_probs);
 
+/* [MOE-OPS] §18: expert_capacity = ceil(tokens * top_k / num_experts *
+ * capacity_factor), evaluated in double. */
+int64_t oracle_expert_capacity(int64_t tokens, int top_k, int num_experts,
+                               double capacity_factor);
+
+/* Capacity-bounded, padded or aligned layout of the permuted rows
+ * ([MOE-OPS] §18 capacity, [DISPATCH] §1.1 drop_and_pad, DeepEP
+ * expert_alignment in [COMBINE] §6):
+ *  - the tokens of expert e, in token order, get ranks 0, 1, ...; with
+ *    capacity > 0 only ranks < capacity are kept, the others dropped (their
+ *    slot_pos is -1; they contribute nothing downstream)
+ *  - counts[e] = kept tokens of expert e
+ *  - segment of e: capacity rows if pad, else counts[e] rounded up to a
+ *    multiple of alignment (>= 1)
+ *  - offsets / group_list: exclusive / inclusive prefix of the segments
+ *  - sorted_indices[offsets[e] + r] = token of rank r; padding rows and rows
+ *    from offsets[E] to max_rows are -1 (permuted_probs 0 there)
+ * Fails if offsets[E] would exceed max_rows. */
+int oracle_route_layout(const int32_t* topk_idx, const float* topk_w, int64_t T, int E, int k,
+                        int capacity, int pad, int alignment, int64_t max_rows,
+                        int32_t* counts, int32_t* offsets, int32_t* group_list,
+                        int32_t* sorted_indices, int32_t* slot_pos, float* permuted_probs);
+
 /* [DISPATCH] §1.1 permuted_input = tokens.index_select(0, sorted_indices):
  * out[p] = x[sorted_indices[p]] for p < n_rows; elem_size 4 or 2 bytes. */
 int oracle_permute(const void* x, int elem_size, int64_t T, int64_t H,

@@ -39,7 +39,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_status_strings_and_version(lib):
-    assert moe.moe_abi_version() >= 1
+    assert moe.moe_abi_version() == 2
     assert moe.moe_status_string(0) == "MOE_OK"
     assert moe.moe_status_string(6) == "MOE_ERR_DEVICE_CHECK"
     assert moe.moe_status_string(99) == "MOE_ERR_UNKNOWN"
@@ -81,11 +81,13 @@ def test_host_validation_rejects_before_launch(lib):
     assert lib.moe_route(fake, 10, 8, 2, fake, fake, fake, fake, fake, fake, fake, fake, None,
                          P(0x1000), 16, None) == 3
     # bad dtype, bad k, null pointers
-    assert lib.moe_permute(fake, 7, 10, 16, 2, fake, fake, None) == 1
-    assert lib.moe_permute(fake, 1, 10, 16, 33, fake, fake, None) == 2
-    assert lib.moe_permute(None, 1, 10, 16, 2, fake, fake, None) == 1
-    assert lib.moe_combine(fake, 1, 10, 16, 0, fake, None, fake, None) == 1
-    assert lib.moe_combine_backward(fake, fake, 1, 10, 16, 2, fake, None, fake, None, None) == 1
+    assert lib.moe_permute(fake, 7, 10, 16, 2, 20, fake, fake, None) == 1
+    assert lib.moe_permute(fake, 1, 10, 16, 33, 330, fake, fake, None) == 2
+    assert lib.moe_permute(None, 1, 10, 16, 2, 20, fake, fake, None) == 1
+    assert lib.moe_permute(fake, 1, 10, 16, 2, -1, fake, fake, None) == 1
+    assert lib.moe_combine(fake, 1, 10, 16, 0, 20, fake, None, fake, None) == 1
+    assert lib.moe_combine_backward(fake, fake, 1, 10, 16, 2, 20, fake, None, fake, None,
+                                    None) == 1
     assert lib.moe_sort_chunks(fake, 1, 10, 16, fake, fake, 0, fake, fake, 1 << 20, None) == 1
     assert lib.moe_sort_chunks(fake, 1, 10, 16, fake, fake, 4, fake, P(0x1001), 1 << 20,
                                None) == 3
@@ -93,9 +95,15 @@ def test_host_validation_rejects_before_launch(lib):
     assert lib.moe_expert_scale(fake, 1, 10, 16, 0, fake, fake, fake, None) == 1
     assert lib.moe_workspace_status(P(0x1003), None) == 3
     # empty problems are valid no-ops and launch nothing
-    assert lib.moe_permute(None, 1, 0, 16, 2, None, None, None) == 0
-    assert lib.moe_combine(None, 1, 0, 16, 2, None, None, None, None) == 0
-    assert lib.moe_combine(None, 1, 5, 0, 2, fake, None, None, None) == 0
+    assert lib.moe_permute(None, 1, 0, 16, 2, 0, None, None, None) == 0
+    assert lib.moe_combine(None, 1, 0, 16, 2, 0, None, None, None, None) == 0
+    assert lib.moe_combine(None, 1, 5, 0, 2, 10, fake, None, None, None) == 0
+    # layout helpers are host-only
+    assert lib.moe_route_layout_rows(100, 8, 2, 30, 1, 1, ctypes.byref(ctypes.c_int64())) == 0
+    assert lib.moe_route_layout_rows(100, 8, 2, 0, 1, 1, ctypes.byref(ctypes.c_int64())) == 1
+    cap = ctypes.c_int64()
+    assert lib.moe_expert_capacity(1024, 2, 8, ctypes.c_double(1.25), ctypes.byref(cap)) == 0
+    assert cap.value == 320
 
 
 def test_binding_rejects_cpu_tensors(lib):

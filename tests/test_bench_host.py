@@ -81,3 +81,13 @@ def test_recorded_traffic_is_void_for_a_changed_source(tmp_path, monkeypatch):
     assert bench.recorded_traffic("combine_backward", "0" * 16) is None
     got = bench.recorded_traffic("combine_backward", d)
     assert got is None or got > 1e9
+
+
+def test_parse_layout():
+    assert bench.parse_layout(None) == {}
+    assert bench.parse_layout("cf=1.25,pad") == {"cf": 1.25, "pad": True}
+    assert bench.parse_layout("align=128") == {"align": 128}
+    with pytest.raises(ValueError):
+        bench.parse_layout("pad")
+    with pytest.raises(ValueError):
+        bench.parse_layout("bogus=1")

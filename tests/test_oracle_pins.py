@@ -272,6 +272,65 @@ def test_route_all_tokens_one_expert():
     assert r["slot_pos"][:, 0].tolist() == list(range(T))
 
 
+# ------------------------------------------------ capacity / padded layout
+
+def test_capacity_worked_example(golden):
+    g = golden("moe_ops_capacity.json")
+    assert g["tokens_per_rank"] * g["top_k"] // g["num_experts"] == g["average_per_expert"]
+    assert oracle.expert_capacity(g["tokens_per_rank"], g["top_k"], g["num_experts"],
+                                  g["capacity_factor"]) == g["capacity"]
+    assert oracle.expert_capacity(1000, 3, 7, 1.0) == 429          # ceil(428.57...)
+    assert oracle.expert_capacity(100, 2, 8, 1.0) == 25
+
+
+def test_layout_without_limits_is_the_plain_route():
+    idx, w = wl.random_routing(31, 200, 12, 3, empty_frac=0.1)
+    a = oracle.route_indices(idx, w, 12)
+    b = oracle.route_layout(idx, w, 12, capacity=0, pad=False, alignment=1, max_rows=600)
+    for name in ("counts", "offsets", "group_list", "sorted_indices", "slot_pos", "permuted_probs"):
+        assert (a[name] == b[name]).all(), name
+
+
+def test_layout_capacity_drops_the_latest_tokens():
+    # all 10 tokens pick expert 2 first and expert 0 second; capacity 4
+    idx = np.tile(np.array([[2, 0]], np.int32), (10, 1))
+    w = np.tile(np.array([[0.75, 0.25]], np.float32), (10, 1))
+    r = oracle.route_layout(idx, w, 3, capacity=4, pad=False, alignment=1, max_rows=20)
+    assert r["counts"].tolist() == [4, 0, 4]
+    assert r["offsets"].tolist() == [0, 4, 4, 8]
+    assert r["sorted_indices"][:8].tolist() == [0, 1, 2, 3, 0, 1, 2, 3]
+    assert (r["slot_pos"][4:] == -1).all()                 # tokens 4..9 dropped everywhere
+    assert r["slot_pos"][:4, 0].tolist() == [4, 5, 6, 7] and r["slot_pos"][:4, 1].tolist() == [0, 1, 2, 3]
+
+
+def test_layout_pad_and_alignment_segments():
+    idx, w = wl.random_routing(32, 300, 8, 2)
+    cap = oracle.expert_capacity(300, 2, 8, 1.25)
+    p = oracle.route_layout(idx, w, 8, capacity=cap, pad=True)
+    assert p["offsets"].tolist() == [e * cap for e in range(9)]
+    a = oracle.route_layout(idx, w, 8, capacity=0, pad=False, alignment=128)
+    assert (a["offsets"] % 128 == 0).all()
+    assert (np.diff(a["offsets"]) >= a["counts"]).all() and (np.diff(a["offsets"]) - a["counts"] < 128).all()
+    plain = oracle.route_indices(idx, w, 8)
+    assert (a["counts"] == plain["counts"]).all()
+    for lay in (p, a):
+        n = int(lay["offsets"][-1])
+        si = lay["sorted_indices"]
+        for e in range(8):
+            s0, c = lay["offsets"][e], lay["counts"][e]
+            seg = si[s0:lay["offsets"][e + 1]]
+            assert (np.diff(seg[:c]) > 0).all() and (seg[c:] == -1).all()
+        assert (si[n:] == -1).all()
+        sp = lay["slot_pos"]
+        assert (si[sp[sp >= 0]] == np.nonzero(sp >= 0)[0]).all()
+
+
+def test_layout_rejects_overflowing_rows():
+    idx, w = wl.random_routing(33, 50, 4, 2)
+    with pytest.raises(ValueError):
+        oracle.route_layout(idx, w, 4, capacity=0, pad=False, alignment=64, max_rows=100)
+
+
 # ------------------------------------------------------------------- combine
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])

@@ -248,6 +248,22 @@ def test_combine_bit_exact_under_cancellation(k):
     assert d.max() == 0, f"max ulp {d.max()}, {np.count_nonzero(d)} mismatches"
 
 
+def test_combine_all_slots_empty_gives_positive_zero_rows():
+    T, H, E, k = 300, 1024, 8, 4
+    idx, w = wl.random_routing(77, T, E, k, empty_frac=0.0)
+    idx[::2] = -1                                   # every other token routes nowhere
+    r = moe.moe_route_indices(to_dev(idx), None, E)
+    y = wl.random_activation(78, (T * k, H), "bf16")
+    zero_rows = np.zeros((4, H), np.uint16)
+    y[:4] = zero_rows
+    y[4:8] = 0x8000                                 # negative zeros
+    out = to_host(moe.moe_combine(to_dev(y), r.slot_pos, to_dev(w)))
+    o = oracle.route_indices(idx, None, E)
+    ref, _ = oracle.combine(y, o["slot_pos"], w)
+    assert (out[::2] == 0).all()
+    assert bf16_ulp_diff(out, ref).max() == 0 and (out == ref).all()
+
+
 def test_combine_deterministic_and_stable_across_calls():
     T, H, E, k = 2000, 2048, 64, 8
     idx, w = wl.random_routing(1, T, E, k)

@@ -26,7 +26,8 @@ __all__ = [
     "moe_combine_backward", "moe_expert_scale", "moe_workspace_status", "RouteResult",
     "moe_route_noalloc", "MOE_ROUTE_NOALLOC_SCRATCH_BYTES", "moe_grouped_swiglu_pack",
     "moe_grouped_swiglu_workspace_size", "moe_grouped_swiglu", "moe_device_status",
-    "moe_route_grouped",
+    "moe_route_grouped", "moe_expert_capacity", "moe_route_layout_rows", "moe_route_layout",
+    "moe_fill_pad_rows",
 ]
 
 # Size of the library's built-in scratch array used by moe_route_noalloc.
@@ -70,13 +71,17 @@ def load_library():
             "moe_route": ([P, I64, I, I, P, P, P, P, P, P, P, P, P, P, SZ, P], I),
             "moe_route_indices": ([P, P, I64, I, I, P, P, P, P, P, P, P, P, SZ, P], I),
             "moe_route_noalloc": ([P, I64, I, I, P, P, P, P, P, P, P, P, P, P], I),
+            "moe_route_layout_rows": ([I64, I, I, I, I, I, ctypes.POINTER(I64)], I),
+            "moe_route_layout": ([P, P, I64, I, I, I, I, I, I64, P, P, P, P, P, P, P, SZ, P], I),
+            "moe_fill_pad_rows": ([P, I, I64, I64, P, P, I, P], I),
+            "moe_expert_capacity": ([I64, I, I, ctypes.c_double, ctypes.POINTER(I64)], I),
             "moe_route_grouped": ([P, I64, I, I, I, I, P, P, P, P, P, P, P, P, P, P, SZ, P], I),
-            "moe_permute": ([P, I, I64, I64, I, P, P, P], I),
+            "moe_permute": ([P, I, I64, I64, I, I64, P, P, P], I),
             "moe_sort_chunks_workspace_size": ([I, PSZ], I),
             "moe_sort_chunks": ([P, I, I64, I64, P, P, I, P, P, SZ, P], I),
             "moe_chunk_idxs": ([I, I, I, P], I),
-            "moe_combine": ([P, I, I64, I64, I, P, P, P, P], I),
-            "moe_combine_backward": ([P, P, I, I64, I64, I, P, P, P, P, P], I),
+            "moe_combine": ([P, I, I64, I64, I, I64, P, P, P, P], I),
+            "moe_combine_backward": ([P, P, I, I64, I64, I, I64, P, P, P, P, P], I),
             "moe_expert_scale": ([P, I, I64, I64, I, P, P, P, P], I),
             "moe_workspace_status": ([P, P], I),
             "moe_device_status": ([P], I),
@@ -275,12 +280,68 @@ def moe_route_noalloc(logits: torch.Tensor, k: int, *, routing_map: bool = False
     return r
 
 
+# ---------------------------------------------- capacity / padded layout
+
+def moe_expert_capacity(tokens: int, top_k: int, num_experts: int,
+                        capacity_factor: float) -> int:
+    c = ctypes.c_int64(0)
+    _ok("moe_expert_capacity", load_library().moe_expert_capacity(
+        tokens, top_k, num_experts, float(capacity_factor), ctypes.byref(c)))
+    return c.value
+
+
+def moe_route_layout_rows(T: int, E: int, k: int, capacity: int = 0, pad: bool = False,
+                          alignment: int = 1) -> int:
+    n = ctypes.c_int64(0)
+    _ok("moe_route_layout_rows", load_library().moe_route_layout_rows(
+        T, E, k, capacity, int(bool(pad)), alignment, ctypes.byref(n)))
+    return n.value
+
+
+def moe_route_layout(topk_idx: torch.Tensor, topk_w: Optional[torch.Tensor], E: int, *,
+                     capacity: int = 0, pad: bool = False, alignment: int = 1,
+                     max_rows: Optional[int] = None, workspace: Optional[torch.Tensor] = None,
+                     stream=None) -> RouteResult:
+    """Index outputs for a capacity-bounded, padded or aligned layout (moe.h)."""
+    _cuda(topk_idx, "topk_idx", torch.int32, 2)
+    T, k = topk_idx.shape
+    if topk_w is not None:
+        _cuda(topk_w, "topk_w", torch.float32, 2)
+    if max_rows is None:
+        max_rows = moe_route_layout_rows(T, E, k, capacity, pad, alignment)
+    ws = _workspace(moe_route_workspace_size(T, E, k), topk_idx, workspace)
+    i32 = torch.int32
+    r = RouteResult(
+        topk_idx=topk_idx, topk_w=topk_w, counts=_empty((E,), i32, topk_idx),
+        offsets=_empty((E + 1,), i32, topk_idx), group_list=_empty((E,), i32, topk_idx),
+        sorted_indices=_empty((max_rows,), i32, topk_idx), slot_pos=_empty((T, k), i32, topk_idx),
+        permuted_probs=_empty((max_rows,), torch.float32, topk_idx) if topk_w is not None else None,
+        routing_map=None, workspace=ws)
+    _ok("moe_route_layout", load_library().moe_route_layout(
+        _p(topk_idx), _p(topk_w), T, E, k, capacity, int(bool(pad)), alignment, max_rows,
+        _p(r.counts), _p(r.offsets), _p(r.group_list), _p(r.sorted_indices), _p(r.slot_pos),
+        _p(r.permuted_probs), _p(ws), ws.numel(), _stream(stream)))
+    return r
+
+
+def moe_fill_pad_rows(rows: torch.Tensor, offsets: torch.Tensor, counts: torch.Tensor,
+                      stream=None) -> torch.Tensor:
+    """Zero the padding rows of a padded / aligned permuted buffer."""
+    dt = _act(rows, "rows")
+    _cuda(offsets, "offsets", torch.int32, 1)
+    _cuda(counts, "counts", torch.int32, 1)
+    E = counts.numel()
+    _ok("moe_fill_pad_rows", load_library().moe_fill_pad_rows(
+        _p(rows), dt, rows.shape[0], rows.shape[1], _p(offsets), _p(counts), E, _stream(stream)))
+    return rows
+
+
 # ------------------------------------------------------------------ permute
 
 def moe_permute(x: torch.Tensor, slot_pos: torch.Tensor, out: Optional[torch.Tensor] = None,
-                stream=None) -> torch.Tensor:
-    """permuted[slot_pos[t,j]] = x[t]; out has T*k rows (rows no slot names
-    are left as they were)."""
+                n_rows: Optional[int] = None, stream=None) -> torch.Tensor:
+    """permuted[slot_pos[t,j]] = x[t]; out has n_rows rows (T*k by default, or
+    out's rows); rows no slot names are left as they were."""
     dt = _act(x, "x")
     _cuda(slot_pos, "slot_pos", torch.int32, 2)
     T, H = x.shape
@@ -288,13 +349,13 @@ def moe_permute(x: torch.Tensor, slot_pos: torch.Tensor, out: Optional[torch.Ten
     if slot_pos.shape[0] != T:
         raise ValueError("slot_pos must have one row per token")
     if out is None:
-        out = _empty((T * k, H), x.dtype, x)
+        out = _empty((T * k if n_rows is None else n_rows, H), x.dtype, x)
     else:
         _cuda(out, "out", x.dtype, 2)
-        if tuple(out.shape) != (T * k, H):
-            raise ValueError("out must be [T*k, H]")
-    _ok("moe_permute", load_library().moe_permute(_p(x), dt, T, H, k, _p(slot_pos), _p(out),
-                                                  _stream(stream)))
+        if out.shape[1] != H:
+            raise ValueError("out must have H columns")
+    _ok("moe_permute", load_library().moe_permute(_p(x), dt, T, H, k, out.shape[0], _p(slot_pos),
+                                                  _p(out), _stream(stream)))
     return out
 
 
@@ -350,9 +411,7 @@ def moe_combine(expert_out: torch.Tensor, slot_pos: torch.Tensor,
     dt = _act(expert_out, "expert_out")
     _cuda(slot_pos, "slot_pos", torch.int32, 2)
     T, k = slot_pos.shape
-    H = expert_out.shape[1]
-    if expert_out.shape[0] != T * k:
-        raise ValueError("expert_out must have T*k rows")
+    n_rows, H = expert_out.shape
     if topk_w is not None:
         _cuda(topk_w, "topk_w", torch.float32, 2)
         if tuple(topk_w.shape) != (T, k):
@@ -364,7 +423,7 @@ def moe_combine(expert_out: torch.Tensor, slot_pos: torch.Tensor,
         if tuple(out.shape) != (T, H):
             raise ValueError("out must be [T, H]")
     _ok("moe_combine", load_library().moe_combine(
-        _p(expert_out), dt, T, H, k, _p(slot_pos), _p(topk_w), _p(out), _stream(stream)))
+        _p(expert_out), dt, T, H, k, n_rows, _p(slot_pos), _p(topk_w), _p(out), _stream(stream)))
     return out
 
 
@@ -372,17 +431,18 @@ def moe_combine_backward(grad_out: torch.Tensor, expert_out: torch.Tensor,
                          slot_pos: torch.Tensor, topk_w: Optional[torch.Tensor] = None,
                          grad_expert_out: Optional[torch.Tensor] = None,
                          grad_probs: Optional[torch.Tensor] = None, stream=None):
-    """(grad_expert_out, grad_probs) of the combine; rows no slot names are
-    left as they were."""
+    """(grad_expert_out, grad_probs) of the combine; expert_out may have any
+    number of rows (T*k, or a padded layout's); rows no slot names are left as
+    they were."""
     dt = _act(expert_out, "expert_out")
     _act(grad_out, "grad_out")
     if grad_out.dtype != expert_out.dtype:
         raise ValueError("grad_out and expert_out must share a dtype")
     _cuda(slot_pos, "slot_pos", torch.int32, 2)
     T, k = slot_pos.shape
-    H = expert_out.shape[1]
-    if tuple(grad_out.shape) != (T, H) or expert_out.shape[0] != T * k:
-        raise ValueError("grad_out must be [T, H] and expert_out [T*k, H]")
+    n_rows, H = expert_out.shape
+    if tuple(grad_out.shape) != (T, H):
+        raise ValueError("grad_out must be [T, H]")
     if topk_w is not None:
         _cuda(topk_w, "topk_w", torch.float32, 2)
     if grad_expert_out is None:
@@ -394,7 +454,7 @@ def moe_combine_backward(grad_out: torch.Tensor, expert_out: torch.Tensor,
     else:
         _cuda(grad_probs, "grad_probs", torch.float32, 2)
     _ok("moe_combine_backward", load_library().moe_combine_backward(
-        _p(grad_out), _p(expert_out), dt, T, H, k, _p(slot_pos), _p(topk_w),
+        _p(grad_out), _p(expert_out), dt, T, H, k, n_rows, _p(slot_pos), _p(topk_w),
         _p(grad_expert_out), _p(grad_probs), _stream(stream)))
     return grad_expert_out, grad_probs
 

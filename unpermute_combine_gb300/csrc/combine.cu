@@ -73,6 +73,24 @@ __device__ __forceinline__ void set_word(uint4& d, int q, uint32_t v) {
     if (q == 0) d.x = v; else if (q == 1) d.y = v; else if (q == 2) d.z = v; else d.w = v;
 }
 
+// Interval that certainly holds both the exact slot-order sum and its double
+// evaluation, from the float sum s and a = sum |w|*|y|.  a == 0 means every
+// term is an exact zero: the sum is exactly +0 (a float or double chain of
+// zero products starting from +0 stays +0), so the interval is the point s.
+// Otherwise the float error is at most cbound * a, plus an absolute k*2^-149
+// for results in the subnormal range.
+__device__ __forceinline__ void certify_interval(float s, float a, float cbound, int k,
+                                                 float& lo, float& hi) {
+    if (a == 0.0f) {
+        lo = s;
+        hi = s;
+        return;
+    }
+    const float b = __fmaf_ru(a, cbound, float(k) * 0x1p-149f);
+    lo = __fsub_rd(s, b);
+    hi = __fadd_ru(s, b);
+}
+
 // Double path for one bf16 element: exact slot order, one rounding.
 __device__ __noinline__ uint16_t combine_elem_f64_bf16(const uint16_t* y, int64_t H, int64_t h,
                                                        const int32_t* s_pos, const float* s_w,
@@ -136,13 +154,12 @@ __device__ __forceinline__ bool dd_sum_bf16(const float* w, const float* y, cons
 // in double from the same registers (no reload).
 template <int KMAX>
 __global__ void __launch_bounds__(kThreads)
-combine_bf16_regs_kernel(const uint4* __restrict__ y, int64_t T, int64_t nvec, int k,
+combine_bf16_regs_kernel(const uint4* __restrict__ y, int64_t T, int64_t nvec, int k, int64_t n_rows,
                          const int32_t* __restrict__ slot_pos, const float* __restrict__ topk_w,
                          uint4* __restrict__ out, float cbound, float dd_bound) {
     __shared__ int32_t s_pos[kWarps][kMaxTopK];
     __shared__ float s_w[kWarps][kMaxTopK];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t n_rows = T * k;
     for (int64_t t = int64_t(blockIdx.x) * kWarps + warp; t < T;
          t += int64_t(gridDim.x) * kWarps) {
         stage_slots(s_pos[warp], s_w[warp], slot_pos, topk_w, t, k, n_rows, lane);
@@ -176,10 +193,11 @@ combine_bf16_regs_kernel(const uint4* __restrict__ y, int64_t T, int64_t nvec, i
             uint32_t open = 0;
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-                const float b0 = __fmaf_ru(a[2 * q], cbound, 0x1p-126f);
-                const float b1 = __fmaf_ru(a[2 * q + 1], cbound, 0x1p-126f);
-                const uint32_t lo = pack_bf16x2_rn(__fsub_rd(s[2 * q], b0), __fsub_rd(s[2 * q + 1], b1));
-                const uint32_t hi = pack_bf16x2_rn(__fadd_ru(s[2 * q], b0), __fadd_ru(s[2 * q + 1], b1));
+                float lo0, hi0, lo1, hi1;
+                certify_interval(s[2 * q], a[2 * q], cbound, k, lo0, hi0);
+                certify_interval(s[2 * q + 1], a[2 * q + 1], cbound, k, lo1, hi1);
+                const uint32_t lo = pack_bf16x2_rn(lo0, lo1);
+                const uint32_t hi = pack_bf16x2_rn(hi0, hi1);
                 set_word(res, q, lo);
                 if (lo != hi) open |= 1u << q;
             }
@@ -215,13 +233,12 @@ combine_bf16_regs_kernel(const uint4* __restrict__ y, int64_t T, int64_t nvec, i
 }
 
 __global__ void __launch_bounds__(kThreads)
-combine_bf16_vec_kernel(const uint4* __restrict__ y, int64_t T, int64_t nvec, int k,
+combine_bf16_vec_kernel(const uint4* __restrict__ y, int64_t T, int64_t nvec, int k, int64_t n_rows,
                         const int32_t* __restrict__ slot_pos, const float* __restrict__ topk_w,
                         uint4* __restrict__ out, float cbound) {
     __shared__ int32_t s_pos[kWarps][kMaxTopK];
     __shared__ float s_w[kWarps][kMaxTopK];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t n_rows = T * k;
     const int64_t H = nvec * 8;
     for (int64_t t = int64_t(blockIdx.x) * kWarps + warp; t < T;
          t += int64_t(gridDim.x) * kWarps) {
@@ -269,12 +286,11 @@ combine_bf16_vec_kernel(const uint4* __restrict__ y, int64_t T, int64_t nvec, in
                 uint32_t open = 0;           // bit q: word q not certified
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
-                    const float b0 = __fmaf_ru(a[u][2 * q], cbound, 0x1p-126f);
-                    const float b1 = __fmaf_ru(a[u][2 * q + 1], cbound, 0x1p-126f);
-                    const uint32_t lo = pack_bf16x2_rn(__fsub_rd(s[u][2 * q], b0),
-                                                       __fsub_rd(s[u][2 * q + 1], b1));
-                    const uint32_t hi = pack_bf16x2_rn(__fadd_ru(s[u][2 * q], b0),
-                                                       __fadd_ru(s[u][2 * q + 1], b1));
+                    float lo0, hi0, lo1, hi1;
+                    certify_interval(s[u][2 * q], a[u][2 * q], cbound, k, lo0, hi0);
+                    certify_interval(s[u][2 * q + 1], a[u][2 * q + 1], cbound, k, lo1, hi1);
+                    const uint32_t lo = pack_bf16x2_rn(lo0, lo1);
+                    const uint32_t hi = pack_bf16x2_rn(hi0, hi1);
                     set_word(res, q, lo);
                     if (lo != hi) open |= 1u << q;
                 }
@@ -301,13 +317,12 @@ combine_bf16_vec_kernel(const uint4* __restrict__ y, int64_t T, int64_t nvec, in
 // the double slot-order sum, rounded once.
 template <typename E>
 __global__ void __launch_bounds__(kThreads)
-combine_elem_kernel(const E* __restrict__ y, int64_t T, int64_t H, int k,
+combine_elem_kernel(const E* __restrict__ y, int64_t T, int64_t H, int k, int64_t n_rows,
                     const int32_t* __restrict__ slot_pos, const float* __restrict__ topk_w,
                     E* __restrict__ out) {
     __shared__ int32_t s_pos[kWarps][kMaxTopK];
     __shared__ float s_w[kWarps][kMaxTopK];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t n_rows = T * k;
     for (int64_t t = int64_t(blockIdx.x) * kWarps + warp; t < T;
          t += int64_t(gridDim.x) * kWarps) {
         stage_slots(s_pos[warp], s_w[warp], slot_pos, topk_w, t, k, n_rows, lane);
@@ -431,14 +446,14 @@ __device__ __forceinline__ uint32_t scale_pair_bf16_f2(f2_t w2, f2_t g2) {
 template <int KMAX>
 __global__ void __launch_bounds__(kThreads)
 combine_bwd_bf16_vec_kernel(const uint4* __restrict__ gout, const uint4* __restrict__ y,
-                            int64_t T, int64_t nvec, int k, const int32_t* __restrict__ slot_pos,
+                            int64_t T, int64_t nvec, int k, int64_t n_rows,
+                            const int32_t* __restrict__ slot_pos,
                             const float* __restrict__ topk_w, uint4* __restrict__ gy,
                             float* __restrict__ grad_probs) {
     static_assert(KMAX <= 8, "packed accumulators for up to 8 slots");
     __shared__ int32_t s_pos[kWarps][kMaxTopK];
     __shared__ float s_w[kWarps][kMaxTopK];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t n_rows = T * k;
     for (int64_t t = int64_t(blockIdx.x) * kWarps + warp; t < T;
          t += int64_t(gridDim.x) * kWarps) {
         stage_slots(s_pos[warp], s_w[warp], slot_pos, topk_w, t, k, n_rows, lane);
@@ -497,13 +512,12 @@ combine_bwd_bf16_vec_kernel(const uint4* __restrict__ gout, const uint4* __restr
 template <typename E, int KMAX>
 __global__ void __launch_bounds__(kThreads)
 combine_bwd_elem_kernel(const E* __restrict__ gout, const E* __restrict__ y, int64_t T,
-                        int64_t H, int k, const int32_t* __restrict__ slot_pos,
+                        int64_t H, int k, int64_t n_rows, const int32_t* __restrict__ slot_pos,
                         const float* __restrict__ topk_w, E* __restrict__ gy,
                         float* __restrict__ grad_probs) {
     __shared__ int32_t s_pos[kWarps][kMaxTopK];
     __shared__ float s_w[kWarps][kMaxTopK];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t n_rows = T * k;
     for (int64_t t = int64_t(blockIdx.x) * kWarps + warp; t < T;
          t += int64_t(gridDim.x) * kWarps) {
         stage_slots(s_pos[warp], s_w[warp], slot_pos, topk_w, t, k, n_rows, lane);
@@ -547,32 +561,33 @@ combine_bwd_elem_kernel(const E* __restrict__ gout, const E* __restrict__ y, int
 }
 
 moe_status_t check_common(const void* a, const void* b, moe_dtype_t dtype, int64_t T, int64_t H,
-                          int k, const int32_t* slot_pos) {
-    if (!dtype_ok(dtype) || T < 0 || H < 0 || k < 1) return MOE_ERR_INVALID_ARG;
-    if (k > kMaxTopK || T * int64_t(k) >= (int64_t(1) << 31)) return MOE_ERR_UNSUPPORTED;
+                          int k, int64_t n_rows, const int32_t* slot_pos) {
+    if (!dtype_ok(dtype) || T < 0 || H < 0 || k < 1 || n_rows < 0) return MOE_ERR_INVALID_ARG;
+    if (k > kMaxTopK || T * int64_t(k) >= (int64_t(1) << 31) || n_rows >= (int64_t(1) << 31))
+        return MOE_ERR_UNSUPPORTED;
     if (T > 0 && (!slot_pos || (H > 0 && (!a || !b)))) return MOE_ERR_INVALID_ARG;
     return MOE_OK;
 }
 
 template <int KMAX>
 void launch_bwd(const void* gout, const void* y, moe_dtype_t dtype, int64_t T, int64_t H, int k,
-                const int32_t* slot_pos, const float* topk_w, void* gy, float* gp,
+                int64_t n_rows, const int32_t* slot_pos, const float* topk_w, void* gy, float* gp,
                 bool vec, cudaStream_t s) {
     const int64_t want = (T + kWarps - 1) / kWarps;
     if (vec && KMAX <= 8) {
         const auto kern = combine_bwd_bf16_vec_kernel<(KMAX <= 8 ? KMAX : 8)>;
         kern<<<grid_for((const void*)kern, kThreads, want), kThreads, 0, s>>>(
-            static_cast<const uint4*>(gout), static_cast<const uint4*>(y), T, H / 8, k, slot_pos,
-            topk_w, static_cast<uint4*>(gy), gp);
+            static_cast<const uint4*>(gout), static_cast<const uint4*>(y), T, H / 8, k, n_rows,
+            slot_pos, topk_w, static_cast<uint4*>(gy), gp);
     } else if (dtype == MOE_F32) {
         const auto kern = combine_bwd_elem_kernel<float, KMAX>;
         kern<<<grid_for((const void*)kern, kThreads, want), kThreads, 0, s>>>(
-            static_cast<const float*>(gout), static_cast<const float*>(y), T, H, k, slot_pos,
-            topk_w, static_cast<float*>(gy), gp);
+            static_cast<const float*>(gout), static_cast<const float*>(y), T, H, k, n_rows,
+            slot_pos, topk_w, static_cast<float*>(gy), gp);
     } else {
         const auto kern = combine_bwd_elem_kernel<uint16_t, KMAX>;
         kern<<<grid_for((const void*)kern, kThreads, want), kThreads, 0, s>>>(
-            static_cast<const uint16_t*>(gout), static_cast<const uint16_t*>(y), T, H, k,
+            static_cast<const uint16_t*>(gout), static_cast<const uint16_t*>(y), T, H, k, n_rows,
             slot_pos, topk_w, static_cast<uint16_t*>(gy), gp);
     }
 }
@@ -583,9 +598,9 @@ void launch_bwd(const void* gout, const void* y, moe_dtype_t dtype, int64_t T, i
 using namespace moe;
 
 extern "C" moe_status_t moe_combine(const void* expert_out, moe_dtype_t dtype, int64_t T,
-                                    int64_t H, int k, const int32_t* slot_pos,
+                                    int64_t H, int k, int64_t n_rows, const int32_t* slot_pos,
                                     const float* topk_w, void* out, void* stream) {
-    const moe_status_t st = check_common(expert_out, out, dtype, T, H, k, slot_pos);
+    const moe_status_t st = check_common(expert_out, out, dtype, T, H, k, n_rows, slot_pos);
     if (st != MOE_OK) return st;
     if (T == 0 || H == 0) return MOE_OK;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -599,20 +614,21 @@ extern "C" moe_status_t moe_combine(const void* expert_out, moe_dtype_t dtype, i
             const auto kern = k <= 1 ? combine_bf16_regs_kernel<1> : k <= 2 ? combine_bf16_regs_kernel<2>
                             : k <= 4 ? combine_bf16_regs_kernel<4> : combine_bf16_regs_kernel<8>;
             kern<<<grid_for((const void*)kern, kThreads, want), kThreads, 0, s>>>(
-                yv, T, H / 8, k, slot_pos, topk_w, ov, cb, dd_bound_factor(k));
+                yv, T, H / 8, k, n_rows, slot_pos, topk_w, ov, cb, dd_bound_factor(k));
         } else {
             combine_bf16_vec_kernel<<<grid_for((const void*)combine_bf16_vec_kernel, kThreads, want),
-                                      kThreads, 0, s>>>(yv, T, H / 8, k, slot_pos, topk_w, ov, cb);
+                                      kThreads, 0, s>>>(yv, T, H / 8, k, n_rows, slot_pos, topk_w,
+                                                        ov, cb);
         }
     } else if (dtype == MOE_F32) {
         const auto kern = combine_elem_kernel<float>;
         kern<<<grid_for((const void*)kern, kThreads, want), kThreads, 0, s>>>(
-            static_cast<const float*>(expert_out), T, H, k, slot_pos, topk_w,
+            static_cast<const float*>(expert_out), T, H, k, n_rows, slot_pos, topk_w,
             static_cast<float*>(out));
     } else {
         const auto kern = combine_elem_kernel<uint16_t>;
         kern<<<grid_for((const void*)kern, kThreads, want), kThreads, 0, s>>>(
-            static_cast<const uint16_t*>(expert_out), T, H, k, slot_pos, topk_w,
+            static_cast<const uint16_t*>(expert_out), T, H, k, n_rows, slot_pos, topk_w,
             static_cast<uint16_t*>(out));
     }
     return launch_status();
@@ -620,10 +636,10 @@ extern "C" moe_status_t moe_combine(const void* expert_out, moe_dtype_t dtype, i
 
 extern "C" moe_status_t moe_combine_backward(const void* grad_out, const void* expert_out,
                                              moe_dtype_t dtype, int64_t T, int64_t H, int k,
-                                             const int32_t* slot_pos, const float* topk_w,
-                                             void* grad_expert_out, float* grad_probs,
-                                             void* stream) {
-    moe_status_t st = check_common(grad_out, expert_out, dtype, T, H, k, slot_pos);
+                                             int64_t n_rows, const int32_t* slot_pos,
+                                             const float* topk_w, void* grad_expert_out,
+                                             float* grad_probs, void* stream) {
+    moe_status_t st = check_common(grad_out, expert_out, dtype, T, H, k, n_rows, slot_pos);
     if (st != MOE_OK) return st;
     if (T == 0) return MOE_OK;
     if (!grad_probs || (H > 0 && !grad_expert_out)) return MOE_ERR_INVALID_ARG;
@@ -631,11 +647,11 @@ extern "C" moe_status_t moe_combine_backward(const void* grad_out, const void* e
     const size_t row = size_t(H) * elem_size(dtype);
     const bool vec = dtype == MOE_BF16 && row % 16 == 0 && aligned16(grad_out) &&
                      aligned16(expert_out) && aligned16(grad_expert_out);
-    if (k <= 1) launch_bwd<1>(grad_out, expert_out, dtype, T, H, k, slot_pos, topk_w, grad_expert_out, grad_probs, vec, s);
-    else if (k <= 2) launch_bwd<2>(grad_out, expert_out, dtype, T, H, k, slot_pos, topk_w, grad_expert_out, grad_probs, vec, s);
-    else if (k <= 4) launch_bwd<4>(grad_out, expert_out, dtype, T, H, k, slot_pos, topk_w, grad_expert_out, grad_probs, vec, s);
-    else if (k <= 8) launch_bwd<8>(grad_out, expert_out, dtype, T, H, k, slot_pos, topk_w, grad_expert_out, grad_probs, vec, s);
-    else if (k <= 16) launch_bwd<16>(grad_out, expert_out, dtype, T, H, k, slot_pos, topk_w, grad_expert_out, grad_probs, vec, s);
-    else launch_bwd<32>(grad_out, expert_out, dtype, T, H, k, slot_pos, topk_w, grad_expert_out, grad_probs, vec, s);
+    if (k <= 1) launch_bwd<1>(grad_out, expert_out, dtype, T, H, k, n_rows, slot_pos, topk_w, grad_expert_out, grad_probs, vec, s);
+    else if (k <= 2) launch_bwd<2>(grad_out, expert_out, dtype, T, H, k, n_rows, slot_pos, topk_w, grad_expert_out, grad_probs, vec, s);
+    else if (k <= 4) launch_bwd<4>(grad_out, expert_out, dtype, T, H, k, n_rows, slot_pos, topk_w, grad_expert_out, grad_probs, vec, s);
+    else if (k <= 8) launch_bwd<8>(grad_out, expert_out, dtype, T, H, k, n_rows, slot_pos, topk_w, grad_expert_out, grad_probs, vec, s);
+    else if (k <= 16) launch_bwd<16>(grad_out, expert_out, dtype, T, H, k, n_rows, slot_pos, topk_w, grad_expert_out, grad_probs, vec, s);
+    else launch_bwd<32>(grad_out, expert_out, dtype, T, H, k, n_rows, slot_pos, topk_w, grad_expert_out, grad_probs, vec, s);
     return launch_status();
 }

@@ -17,11 +17,10 @@ constexpr int kUnroll = 4;     // 16-byte vectors in flight per lane
 // One warp per token; lane l moves vectors l, l+32, ... of the row.
 template <typename V>
 __global__ void __launch_bounds__(kThreads)
-permute_kernel(const V* __restrict__ x, int64_t T, int64_t nvec, int k,
+permute_kernel(const V* __restrict__ x, int64_t T, int64_t nvec, int k, int64_t n_rows,
                const int32_t* __restrict__ slot_pos, V* __restrict__ out) {
     __shared__ int32_t s_pos[kWarps][kMaxTopK];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t n_rows = T * k;
     for (int64_t t = int64_t(blockIdx.x) * kWarps + warp; t < T;
          t += int64_t(gridDim.x) * kWarps) {
         if (lane < k) {
@@ -65,12 +64,11 @@ constexpr int kPermStages = 3;
 
 __global__ void __launch_bounds__(32)
 permute_bulk_kernel(const uint8_t* __restrict__ x, int64_t T, int64_t row_bytes, int piece,
-                    int pieces, int k, const int32_t* __restrict__ slot_pos,
+                    int pieces, int k, int64_t n_rows, const int32_t* __restrict__ slot_pos,
                     uint8_t* __restrict__ out, uint32_t* __restrict__ status) {
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ __align__(8) uint64_t full_bar[kPermStages];
     const int lane = threadIdx.x;
-    const int64_t n_rows = T * k;
     const int64_t total = T * pieces;
     const int64_t first = blockIdx.x;
     const int64_t my_items = first < total ? (total - first + gridDim.x - 1) / gridDim.x : 0;
@@ -339,16 +337,36 @@ expert_scale_kernel(const T* __restrict__ in, int64_t n_rows, int64_t H, int E,
     }
 }
 
+// Zero the padding rows of a padded / aligned layout: expert e's rows
+// [offsets[e] + counts[e], offsets[e+1]), clipped to max_rows.  One block per
+// expert (grid-stride), 16-byte stores when the rows allow.
+template <typename V>
+__global__ void __launch_bounds__(kThreads)
+fill_pad_rows_kernel(V* __restrict__ rows, int64_t max_rows, int64_t nvec,
+                     const int32_t* __restrict__ offsets, const int32_t* __restrict__ counts,
+                     int E) {
+    for (int e = blockIdx.x; e < E; e += gridDim.x) {
+        const int64_t p0 = int64_t(offsets[e]) + counts[e];
+        const int64_t p1 = min64(offsets[e + 1], max_rows);
+        if (p0 >= p1) continue;
+        const int64_t n = (p1 - p0) * nvec;
+        V* base = rows + p0 * nvec;
+        for (int64_t i = threadIdx.x; i < n; i += kThreads) base[i] = V{};
+    }
+}
+
 }  // namespace
 }  // namespace moe
 
 using namespace moe;
 
 extern "C" moe_status_t moe_permute(const void* x, moe_dtype_t dtype, int64_t T, int64_t H, int k,
-                                    const int32_t* slot_pos, void* out, void* stream) {
-    if (!dtype_ok(dtype) || T < 0 || H < 0 || k < 1) return MOE_ERR_INVALID_ARG;
-    if (k > kMaxTopK || T * int64_t(k) >= (int64_t(1) << 31)) return MOE_ERR_UNSUPPORTED;
-    if (T == 0 || H == 0) return MOE_OK;
+                                    int64_t n_rows, const int32_t* slot_pos, void* out,
+                                    void* stream) {
+    if (!dtype_ok(dtype) || T < 0 || H < 0 || k < 1 || n_rows < 0) return MOE_ERR_INVALID_ARG;
+    if (k > kMaxTopK || T * int64_t(k) >= (int64_t(1) << 31) || n_rows >= (int64_t(1) << 31))
+        return MOE_ERR_UNSUPPORTED;
+    if (T == 0 || H == 0 || n_rows == 0) return MOE_OK;
     if (!x || !slot_pos || !out) return MOE_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const size_t row = size_t(H) * elem_size(dtype);
@@ -368,16 +386,16 @@ extern "C" moe_status_t moe_permute(const void* x, moe_dtype_t dtype, int64_t T,
         const int64_t items = T * pieces;
         const int g = int(min64(items, int64_t(sm_count()) * 4));
         permute_bulk_kernel<<<g, 32, smem, s>>>(static_cast<const uint8_t*>(x), T, int64_t(row),
-                                                piece, pieces, k, slot_pos,
+                                                piece, pieces, k, n_rows, slot_pos,
                                                 static_cast<uint8_t*>(out), device_status_word());
     } else if (dtype == MOE_F32) {
         const int g = grid_for((const void*)permute_kernel<float>, kThreads, 0, blocks);
         permute_kernel<float><<<g, kThreads, 0, s>>>(
-            static_cast<const float*>(x), T, H, k, slot_pos, static_cast<float*>(out));
+            static_cast<const float*>(x), T, H, k, n_rows, slot_pos, static_cast<float*>(out));
     } else {
         const int g = grid_for((const void*)permute_kernel<uint16_t>, kThreads, 0, blocks);
         permute_kernel<uint16_t><<<g, kThreads, 0, s>>>(
-            static_cast<const uint16_t*>(x), T, H, k, slot_pos, static_cast<uint16_t*>(out));
+            static_cast<const uint16_t*>(x), T, H, k, n_rows, slot_pos, static_cast<uint16_t*>(out));
     }
     return launch_status();
 }
@@ -460,5 +478,28 @@ extern "C" moe_status_t moe_expert_scale(const void* in, moe_dtype_t dtype, int6
             static_cast<const uint16_t*>(in), n_rows, H, E, offsets, scale,
             static_cast<uint16_t*>(out));
     }
+    return launch_status();
+}
+
+extern "C" moe_status_t moe_fill_pad_rows(void* rows, moe_dtype_t dtype, int64_t max_rows,
+                                         int64_t H, const int32_t* offsets,
+                                         const int32_t* counts, int E, void* stream) {
+    if (!dtype_ok(dtype) || max_rows < 0 || H < 0 || E < 1) return MOE_ERR_INVALID_ARG;
+    if (E > kMaxExperts) return MOE_ERR_UNSUPPORTED;
+    if (!offsets || !counts) return MOE_ERR_INVALID_ARG;
+    if (max_rows == 0 || H == 0) return MOE_OK;
+    if (!rows) return MOE_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t row = size_t(H) * elem_size(dtype);
+    const int g = int(min64(E, int64_t(sm_count()) * 4));
+    if (row % 16 == 0 && aligned16(rows))
+        fill_pad_rows_kernel<uint4><<<g, kThreads, 0, s>>>(static_cast<uint4*>(rows), max_rows,
+                                                          int64_t(row / 16), offsets, counts, E);
+    else if (dtype == MOE_F32)
+        fill_pad_rows_kernel<float><<<g, kThreads, 0, s>>>(static_cast<float*>(rows), max_rows, H,
+                                                           offsets, counts, E);
+    else
+        fill_pad_rows_kernel<uint16_t><<<g, kThreads, 0, s>>>(static_cast<uint16_t*>(rows),
+                                                              max_rows, H, offsets, counts, E);
     return launch_status();
 }

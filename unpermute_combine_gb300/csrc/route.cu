@@ -21,6 +21,8 @@
 //       slot_pos, sorted_indices and permuted_probs.
 // Position of (t, e) = offsets[e] + #{t' < t : e in topk(t')}: exact integer
 // arithmetic, so the result is bit-exact and independent of scheduling.
+#include <cmath>
+
 #include "common.cuh"
 
 namespace moe {
@@ -59,8 +61,10 @@ __host__ __device__ inline int64_t num_blocks(int64_t T) {
     return (T + kTokensPerBlock - 1) / kTokensPerBlock;
 }
 
+// [B rows x (E+1)] block histograms (column E: error flags), then one row of
+// raw per-expert totals written by the scan kernel when it runs.
 size_t hist_bytes(int64_t T, int E) {
-    return align_up(size_t(num_blocks(T)) * size_t(E + 1) * sizeof(int32_t), kWsAlign);
+    return align_up(size_t(num_blocks(T) + 1) * size_t(E + 1) * sizeof(int32_t), kWsAlign);
 }
 
 // Order-preserving 32-bit key of a float: larger value -> larger key.  -0 is
@@ -257,8 +261,7 @@ route_check_kernel(const int32_t* __restrict__ topk_idx, int64_t T, int E, int k
 // Block x owns experts [32x, 32x+32); thread (g, c) owns expert 32x+c and
 // the row group g of the histogram.
 __global__ void __launch_bounds__(1024)
-route_scan_kernel(int32_t* __restrict__ hist, int64_t B, int E, int32_t* __restrict__ counts,
-                  WsHeader* __restrict__ header) {
+route_scan_kernel(int32_t* __restrict__ hist, int64_t B, int E, WsHeader* __restrict__ header) {
     wait_for_predecessor();
     __shared__ int32_t s_part[32][33];
     const int c = threadIdx.x & 31, g = threadIdx.x >> 5;
@@ -278,7 +281,7 @@ route_scan_kernel(int32_t* __restrict__ hist, int64_t B, int E, int32_t* __restr
             hist[b * (E + 1) + e] = run;
             run += v;
         }
-        if (g == 31) counts[e] = run;
+        if (g == 31) hist[B * (E + 1) + e] = run;      // raw totals row
     }
     if (blockIdx.x == 0) {                   // fold the per-block error flags
         __shared__ int s_bad;
@@ -341,6 +344,19 @@ __device__ void block_exclusive_scan(const int32_t* s_in, int32_t* s_out, int n)
 // status word.  Otherwise `hist` already holds R2's per-block prefixes.
 constexpr int kFusedMaxBlocks = 256;
 
+// Layout of the permuted rows ("从零理解 MoE 算子" §18 capacity, the
+// drop_and_pad branch of "token dispatcher + fuse_a2a" §1.1, DeepEP's
+// expert_alignment): an expert keeps its first `capacity` tokens in token
+// order (capacity 0: all); its segment is `capacity` rows when `pad`, else its
+// kept count rounded up to a multiple of `alignment`.  max_rows bounds the
+// rows the outputs may hold.
+struct Layout {
+    int capacity;
+    int pad;
+    int alignment;
+    int64_t max_rows;
+};
+
 template <bool FUSED>
 __global__ void __launch_bounds__(kThreads)
 route_scatter_kernel(const int32_t* __restrict__ topk_idx, const float* __restrict__ topk_w,
@@ -348,13 +364,15 @@ route_scatter_kernel(const int32_t* __restrict__ topk_idx, const float* __restri
                      const int32_t* __restrict__ hist, int32_t* __restrict__ counts,
                      int32_t* __restrict__ offsets, int32_t* __restrict__ group_list,
                      int32_t* __restrict__ sorted_indices, int32_t* __restrict__ slot_pos,
-                     float* __restrict__ permuted_probs, WsHeader* __restrict__ header) {
+                     float* __restrict__ permuted_probs, WsHeader* __restrict__ header,
+                     Layout lay) {
     wait_for_predecessor();
     extern __shared__ int32_t smem[];
     int32_t* s_cnt = smem;                                   // [kWarps][E] -> warp prefixes
     int32_t* s_off = s_cnt + kWarps * E;                     // [E+1]
     int32_t* s_bpre = s_off + (E + 1);                       // [E]
-    int32_t* s_idx = s_bpre + E;                             // [kTokensPerBlock*k]
+    int32_t* s_kept = s_bpre + E;                            // [E]
+    int32_t* s_idx = s_kept + E;                             // [kTokensPerBlock*k]
     int32_t* s_rank = s_idx + kTokensPerBlock * k;           // [kTokensPerBlock*k]
     float* s_w = reinterpret_cast<float*>(s_rank + kTokensPerBlock * k);   // [kTokensPerBlock*k]
     __shared__ int s_bad;
@@ -418,23 +436,36 @@ route_scatter_kernel(const int32_t* __restrict__ topk_idx, const float* __restri
         const bool has_hist = t0 < T;
         for (int e = threadIdx.x; e < E; e += kThreads) {
             s_bpre[e] = has_hist ? hist[int64_t(blockIdx.x) * (E + 1) + e] : 0;
-            s_off[e] = counts[e];
+            s_off[e] = hist[B * (E + 1) + e];              // raw totals from the scan kernel
         }
         for (int i = threadIdx.x; i < kWarps * E; i += kThreads) s_cnt[i] = 0;
     }
     __syncthreads();
-    if (FUSED && blockIdx.x == 0) {
-        for (int e = threadIdx.x; e < E; e += kThreads) counts[e] = s_off[e];
-        if (threadIdx.x == 0) {
+    // kept tokens and segment length of every expert
+    for (int e = threadIdx.x; e < E; e += kThreads) {
+        const int32_t total = s_off[e];
+        const int32_t kept = lay.capacity > 0 && total > lay.capacity ? lay.capacity : total;
+        s_kept[e] = kept;
+        s_off[e] = lay.pad ? lay.capacity : (kept + lay.alignment - 1) / lay.alignment * lay.alignment;
+    }
+    __syncthreads();
+    if (blockIdx.x == 0) {
+        for (int e = threadIdx.x; e < E; e += kThreads) counts[e] = s_kept[e];
+        if (FUSED && threadIdx.x == 0) {
             header->status = s_bad ? MOE_ERR_DEVICE_CHECK : MOE_OK;
             header->detail = 0;
         }
     }
-    // offsets = exclusive scan of counts (every block recomputes it)
+    // offsets = exclusive scan of the segments (every block recomputes it)
     block_exclusive_scan(s_off, s_off, E);
+    const bool overflow = int64_t(s_off[E]) > lay.max_rows;
     if (blockIdx.x == 0) {
         for (int e = threadIdx.x; e <= E; e += kThreads) offsets[e] = s_off[e];
         for (int e = threadIdx.x; e < E; e += kThreads) group_list[e] = s_off[e + 1];
+        if (overflow && threadIdx.x == 0) {
+            header->status = MOE_ERR_DEVICE_CHECK;     // rows past max_rows are not written
+            header->detail = 1;
+        }
     }
     if (check_ids) {
         bool bad = false;   // already reported by the check kernel
@@ -485,28 +516,33 @@ route_scatter_kernel(const int32_t* __restrict__ topk_idx, const float* __restri
         const int tl = i / k;
         const int e = s_idx[i];
         const int64_t t = t0 + tl;
-        if (e < 0) {
-            slot_pos[t * k + (i % k)] = -1;
+        const int32_t rank = e < 0 ? 0 : s_bpre[e] + s_cnt[(tl / kTokensPerWarp) * E + e] + s_rank[i];
+        const int64_t pos = e < 0 ? -1 : int64_t(s_off[e]) + rank;
+        if (e < 0 || (lay.capacity > 0 && rank >= lay.capacity) || pos >= lay.max_rows) {
+            slot_pos[t * k + (i % k)] = -1;                 // empty, dropped or out of room
             continue;
         }
-        const int w = tl / kTokensPerWarp;
-        const int32_t pos = s_off[e] + s_bpre[e] + s_cnt[w * E + e] + s_rank[i];
-        slot_pos[t * k + (i % k)] = pos;
+        slot_pos[t * k + (i % k)] = int32_t(pos);
         sorted_indices[pos] = int32_t(t);
         if (permuted_probs) permuted_probs[pos] = s_w[i];
     }
-    // rows past offsets[E] (empty slots shrink the routed count)
-    const int64_t n_valid = s_off[E];
-    const int64_t n_total = T * k;
-    for (int64_t p = n_valid + int64_t(blockIdx.x) * kThreads + threadIdx.x; p < n_total;
-         p += int64_t(gridDim.x) * kThreads) {
+    // padding rows inside the segments, then every row from offsets[E] on
+    for (int e = blockIdx.x; e < E; e += gridDim.x) {
+        const int64_t p1 = min64(s_off[e + 1], lay.max_rows);
+        for (int64_t p = int64_t(s_off[e]) + s_kept[e] + threadIdx.x; p < p1; p += kThreads) {
+            sorted_indices[p] = -1;
+            if (permuted_probs) permuted_probs[p] = 0.0f;
+        }
+    }
+    for (int64_t p = min64(s_off[E], lay.max_rows) + int64_t(blockIdx.x) * kThreads + threadIdx.x;
+         p < lay.max_rows; p += int64_t(gridDim.x) * kThreads) {
         sorted_indices[p] = -1;
         if (permuted_probs) permuted_probs[p] = 0.0f;
     }
 }
 
 size_t scatter_smem_bytes(int E, int k) {
-    return sizeof(int32_t) * (size_t(kWarps) * E + (E + 1) + size_t(E) +
+    return sizeof(int32_t) * (size_t(kWarps) * E + (E + 1) + 2 * size_t(E) +
                               3 * size_t(kTokensPerBlock) * k);
 }
 
@@ -537,11 +573,13 @@ void launch_topk(const float* logits, int64_t T, int E, int k, int32_t* topk_idx
 moe_status_t finish_route(const int32_t* topk_idx, const float* topk_w, int64_t T, int E, int k,
                           bool check_ids, int32_t* hist, WsHeader* header, int32_t* counts,
                           int32_t* offsets, int32_t* group_list, int32_t* sorted_indices,
-                          int32_t* slot_pos, float* permuted_probs, cudaStream_t s) {
+                          int32_t* slot_pos, float* permuted_probs, cudaStream_t s,
+                          Layout lay = Layout{0, 0, 1, -1}) {
     const int64_t B = num_blocks(T);
     const bool fused = B <= kFusedMaxBlocks;
+    if (lay.max_rows < 0) lay.max_rows = T * k;
     if (!fused && launch_dependent(route_scan_kernel, unsigned((E + 31) / 32), 1024, 0, s, hist,
-                                   B, E, counts, header) != cudaSuccess)
+                                   B, E, header) != cudaSuccess)
         return MOE_ERR_CUDA;
     const size_t smem = scatter_smem_bytes(E, k);
     static bool attr_set[64] = {};
@@ -559,10 +597,12 @@ moe_status_t finish_route(const int32_t* topk_idx, const float* topk_w, int64_t 
     const cudaError_t err = fused
         ? launch_dependent(route_scatter_kernel<true>, unsigned(B > 0 ? B : 1), kThreads, smem, s,
                            topk_idx, topk_w, T, E, k, check_ids, (const int32_t*)hist, counts,
-                           offsets, group_list, sorted_indices, slot_pos, permuted_probs, header)
+                           offsets, group_list, sorted_indices, slot_pos, permuted_probs, header,
+                           lay)
         : launch_dependent(route_scatter_kernel<false>, unsigned(B > 0 ? B : 1), kThreads, smem, s,
                            topk_idx, topk_w, T, E, k, check_ids, (const int32_t*)hist, counts,
-                           offsets, group_list, sorted_indices, slot_pos, permuted_probs, header);
+                           offsets, group_list, sorted_indices, slot_pos, permuted_probs, header,
+                           lay);
     return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
@@ -671,6 +711,71 @@ extern "C" moe_status_t moe_route_indices(const int32_t* topk_idx, const float* 
     }
     return finish_route(topk_idx, topk_w, T, E, k, true, hist, header, counts, offsets,
                         group_list, sorted_indices, slot_pos, permuted_probs, s);
+}
+
+// ------------------------------------------------- capacity / padded layout
+
+namespace moe {
+namespace {
+moe_status_t layout_rows(int64_t T, int E, int k, int capacity, int pad, int alignment,
+                         int64_t* rows) {
+    if (capacity < 0 || alignment < 1 || (pad && capacity < 1)) return MOE_ERR_INVALID_ARG;
+    const int64_t r = pad ? int64_t(E) * capacity : T * k + int64_t(E) * (alignment - 1);
+    if (r >= (int64_t(1) << 31)) return MOE_ERR_UNSUPPORTED;
+    *rows = r;
+    return MOE_OK;
+}
+}  // namespace
+}  // namespace moe
+
+extern "C" moe_status_t moe_expert_capacity(int64_t tokens, int top_k, int num_experts,
+                                            double capacity_factor, int64_t* capacity) {
+    if (!capacity || tokens < 0 || top_k < 1 || num_experts < 1 || !(capacity_factor > 0.0))
+        return MOE_ERR_INVALID_ARG;
+    const double c = std::ceil(double(tokens) * double(top_k) / double(num_experts) *
+                               capacity_factor);
+    if (c >= 2147483648.0) return MOE_ERR_UNSUPPORTED;
+    *capacity = int64_t(c);
+    return MOE_OK;
+}
+
+extern "C" moe_status_t moe_route_layout_rows(int64_t T, int E, int k, int capacity, int pad,
+                                              int alignment, int64_t* max_rows) {
+    if (!max_rows) return MOE_ERR_INVALID_ARG;
+    const moe_status_t st = validate_sizes(T, E, k);
+    if (st != MOE_OK) return st;
+    return layout_rows(T, E, k, capacity, pad, alignment, max_rows);
+}
+
+extern "C" moe_status_t moe_route_layout(const int32_t* topk_idx, const float* topk_w, int64_t T,
+                                         int E, int k, int capacity, int pad, int alignment,
+                                         int64_t max_rows, int32_t* counts, int32_t* offsets,
+                                         int32_t* group_list, int32_t* sorted_indices,
+                                         int32_t* slot_pos, float* permuted_probs,
+                                         void* workspace, size_t workspace_bytes, void* stream) {
+    moe_status_t st = validate_sizes(T, E, k);
+    if (st != MOE_OK) return st;
+    int64_t bound = 0;
+    st = layout_rows(T, E, k, capacity, pad, alignment, &bound);
+    if (st != MOE_OK) return st;
+    if (max_rows < 0 || max_rows >= (int64_t(1) << 31)) return MOE_ERR_INVALID_ARG;
+    if (!counts || !offsets || !group_list) return MOE_ERR_INVALID_ARG;
+    if (T > 0 && (!topk_idx || !slot_pos)) return MOE_ERR_INVALID_ARG;
+    if (max_rows > 0 && !sorted_indices) return MOE_ERR_INVALID_ARG;
+    if (permuted_probs && !topk_w && T > 0) return MOE_ERR_INVALID_ARG;
+    st = check_workspace(workspace, workspace_bytes, T, E);
+    if (st != MOE_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    WsHeader* header = static_cast<WsHeader*>(workspace);
+    int32_t* hist = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + kWsAlign);
+    if (T > 0) {
+        route_check_kernel<<<unsigned(num_blocks(T)), kThreads, check_smem_bytes(E, k), s>>>(
+            topk_idx, T, E, k, nullptr, hist);
+        if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
+    }
+    return finish_route(topk_idx, topk_w, T, E, k, true, hist, header, counts, offsets,
+                        group_list, sorted_indices, slot_pos, permuted_probs, s,
+                        Layout{capacity, pad, alignment, max_rows});
 }
 
 // ------------------------------------------------------- no-allocation route

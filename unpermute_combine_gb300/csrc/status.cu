@@ -52,7 +52,7 @@ extern "C" const char* moe_status_string(moe_status_t status) {
     return "MOE_ERR_UNKNOWN";
 }
 
-extern "C" int moe_abi_version(void) { return 1; }
+extern "C" int moe_abi_version(void) { return 2; }
 
 extern "C" moe_status_t moe_workspace_status(const void* workspace, void* stream) {
     if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & (moe::kWsAlign - 1)))
