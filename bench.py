@@ -52,6 +52,17 @@ def algorithmic_bytes(T, H, E, k, b):
     }
 
 
+def fp8_bytes(T, H, k, block=128):
+    """Algorithmic bytes of the FP8 dispatch stages (bf16 source rows, e4m3
+    rows, float scale rows of H/block columns)."""
+    N, nb = T * k, H // block
+    return {
+        "quantize_fp8": T * H * 2 + T * H + T * nb * 4,
+        "permute": T * H + N * H + (T + N) * nb * 4 + 2 * N * 4,
+        "dequantize_fp8": N * H + N * nb * 4 + N * H * 2,
+    }
+
+
 def job_value(units_per_rank_step: float, world: int, steps: int, max_elapsed_s: float) -> float:
     """Whole-job throughput: units every rank processed over the slowest rank's time."""
     return units_per_rank_step * world * steps / max_elapsed_s
@@ -86,6 +97,9 @@ KERNEL_SOURCES = {
     "combine": ("unpermute_combine_gb300/csrc/combine.cu", "unpermute_combine_gb300/csrc/common.cuh"),
     "combine_backward": ("unpermute_combine_gb300/csrc/combine.cu",
                          "unpermute_combine_gb300/csrc/common.cuh"),
+    "quantize_fp8": ("unpermute_combine_gb300/csrc/fp8.cu", "unpermute_combine_gb300/csrc/common.cuh"),
+    "dequantize_fp8": ("unpermute_combine_gb300/csrc/fp8.cu",
+                       "unpermute_combine_gb300/csrc/common.cuh"),
 }
 
 
@@ -240,6 +254,12 @@ def run_ours(args, rank, world, local_rank):
                                    alignment=lay.get("align", 1), max_rows=rows, stream=stream)
               if lay else None)
         xp = torch.empty((rows, H), dtype=torch.bfloat16, device=dev)
+        fp8 = bool(args.fp8)
+        if fp8:
+            fp8_tok = (torch.empty((T, H), dtype=torch.float8_e4m3fn, device=dev),
+                       torch.empty((T, H // 128), dtype=torch.float32, device=dev))
+            fp8_rows = (torch.empty((rows, H), dtype=torch.float8_e4m3fn, device=dev),
+                        torch.empty((rows, H // 128), dtype=torch.float32, device=dev))
         out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
         if layer:
             # one-time weight layout (model-load step, outside the timed region)
@@ -253,12 +273,17 @@ def run_ours(args, rank, world, local_rank):
             gp = torch.empty((T, k), dtype=torch.float32, device=dev)
     names = (["route", "permute", "grouped_swiglu", "combine"] if layer else
              ["route", "permute", "combine", "combine_backward"])
+    if fp8:
+        names[1:2] = ["quantize_fp8", "permute", "dequantize_fp8"]
 
     def step(lg, xx, gg, ev=None):
-        def mark(i):
+        n_marks = [0]
+
+        def mark():
             if ev is not None:
-                ev[i].record(stream)
-        mark(0)
+                ev[n_marks[0]].record(stream)
+            n_marks[0] += 1
+        mark()
         if groups:
             moe.moe_route_grouped(lg, k, groups[0], groups[1], out=r, stream=stream)
         else:
@@ -268,22 +293,31 @@ def run_ours(args, rank, world, local_rank):
             rr = moe.moe_route_layout(r.topk_idx, r.topk_w, E, capacity=cap,
                                       pad=lay.get("pad", False), alignment=lay.get("align", 1),
                                       max_rows=rows, workspace=rl.workspace, stream=stream)
-        mark(1)
-        moe.moe_permute(xx, rr.slot_pos, out=xp, stream=stream)
+        mark()
+        if fp8:
+            # FP8 dispatch: quantize, move e4m3 rows and scale rows, and
+            # dequantize in place of the expert's input conversion
+            moe.moe_quantize_fp8(xx, 128, out=fp8_tok, stream=stream)
+            mark()
+            moe.moe_permute_fp8(fp8_tok[0], fp8_tok[1], rr.slot_pos, out=fp8_rows, stream=stream)
+            mark()
+            moe.moe_dequantize_fp8(fp8_rows[0], fp8_rows[1], 128, out=xp, stream=stream)
+        else:
+            moe.moe_permute(xx, rr.slot_pos, out=xp, stream=stream)
         if lay:
             moe.moe_fill_pad_rows(xp, rr.offsets, rr.counts, stream=stream)
-        mark(2)
+        mark()
         if layer:
             moe.moe_grouped_swiglu(xp, up_p, down_p, rr.offsets, out=y, workspace=gs_ws,
                                    stream=stream)
-            mark(3)
+            mark()
             moe.moe_combine(y, rr.slot_pos, r.topk_w, out=out, stream=stream)
         else:
             moe.moe_combine(xp, rr.slot_pos, r.topk_w, out=out, stream=stream)
-            mark(3)
+            mark()
             moe.moe_combine_backward(gg, xp, rr.slot_pos, r.topk_w, grad_expert_out=gy,
                                      grad_probs=gp, stream=stream)
-        mark(4)
+        mark()
 
     import torch.distributed as dist
     dist_on = dist.is_available() and dist.is_initialized()
@@ -299,7 +333,8 @@ def run_ours(args, rank, world, local_rank):
     barrier()
 
     # -------- device-resident timed region
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)]
+           for _ in range(args.steps)]
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local_rank) as clk:
         barrier()
@@ -358,13 +393,16 @@ def run_ours(args, rank, world, local_rank):
     if layer:
         fl, by = layer_flops_bytes(N, H, E, W.I)
         alg["grouped_swiglu"] = by
+    if fp8:
+        alg.update(fp8_bytes(T, H, k))
     kern = {}
     for n in names:
         gbs = alg[n] / per[n] / 1e9
         kern[n] = {"us": round(per[n] * 1e6, 2), "alg_bytes": alg[n], "GB_s": round(gbs, 1),
                    "frac": round(gbs / peak, 4)}
     dominant = max(names, key=lambda n: per[n])
-    pc_time = per["permute"] + per["combine"]
+    pc_time = sum(per[n] for n in names if n in ("quantize_fp8", "permute", "dequantize_fp8",
+                                                  "combine"))
     if layer:
         t_sus, t_burst, t_kind = measured_tensor_peak()
         tf = fl / per["grouped_swiglu"] / 1e12
@@ -390,12 +428,19 @@ def run_ours(args, rank, world, local_rank):
         if groups:
             step_desc = step_desc.replace("moe_route", f"moe_route_grouped({groups[0]} groups, "
                                                        f"{groups[1]} kept)", 1)
+    if fp8:
+        step_desc = step_desc.replace("moe_permute", "moe_quantize_fp8(block 128) + "
+                                      "moe_permute_fp8(e4m3 rows + scale rows) + moe_dequantize_fp8", 1)
     if lay:
         step_desc = step_desc.replace(" + moe_permute", f" + moe_route_layout(capacity={cap}, "
                                       f"pad={lay.get('pad', False)}, alignment="
                                       f"{lay.get('align', 1)}, rows={rows}) + moe_permute + "
                                       "moe_fill_pad_rows", 1)
     launches = ROUTE_LAUNCHES + (1 + 3 + 1 if layer else 3)   # grouped SwiGLU: reset + 2 GEMMs
+    if fp8:
+        launches += 2                     # quantize, dequantize
+    if lay:
+        launches += 3                     # layout check + scatter, pad-row fill
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": max_elapsed / args.steps * 1e3,
@@ -483,6 +528,8 @@ def main(argv=None):
     ap.add_argument("--tokens", type=int, default=None,
                     help="use only the first TOKENS tokens (small cases for profiling)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg")
+    ap.add_argument("--fp8", action="store_true",
+                    help="FP8 dispatch: quantize, move e4m3 rows + scales, dequantize")
     ap.add_argument("--layout", default=None, metavar="SPEC",
                     help="capacity / padded / aligned layout, e.g. 'cf=1.25,pad' or 'align=128'")
     ap.add_argument("--route-groups", default=None, metavar="G:KG",

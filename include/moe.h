@@ -59,7 +59,10 @@ typedef enum {
     MOE_ERR_DEVICE_CHECK = 6   /* the device found invalid data (see above)    */
 } moe_status_t;
 
-typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype_t;
+/* Element types.  MOE_FP8_E4M3 (one byte: 1 sign, 4 exponent, 3 mantissa
+ * bits, no infinities) is accepted by the row-movement calls only
+ * (moe_permute, moe_sort_chunks, moe_fill_pad_rows). */
+typedef enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_FP8_E4M3 = 2 } moe_dtype_t;
 
 /* Human-readable name of a status code (static string, never NULL). */
 const char* moe_status_string(moe_status_t status);
@@ -316,6 +319,38 @@ moe_status_t moe_grouped_swiglu(const void* x, const void* w_up_packed,
                                 const void* w_down_packed, const int32_t* offsets,
                                 int64_t N, int E, int64_t H, int64_t I, void* y,
                                 void* workspace, size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------ FP8 dispatch
+ * [COMBINE] §3 (the dispatch moves FP8 rows with scales, the combine stays
+ * BF16) and the x_scales / num_scales of [DISPATCH]'s DeepEP dispatch.
+ * moe_quantize_fp8: per token and per block of `block` consecutive elements
+ * (block = 32, 64, 128 or 256; H a multiple of it), scale = amax / 448 (the
+ * largest finite e4m3 value; an all-zero block gets scale 1) and
+ * x_q = e4m3(x / scale), the float quotient rounded to nearest even e4m3 and
+ * saturated to +-448.  x bf16 [T,H]; x_q e4m3 bytes [T,H]; scales float
+ * [T, H/block].  Move x_q with moe_permute(dtype MOE_FP8_E4M3) and the
+ * scales with moe_permute(dtype MOE_F32, H/block columns) using the same
+ * slot_pos.
+ * moe_dequantize_fp8: out = bf16(x_q * scale), the exact product rounded
+ * once; x_q [N,H], scales [N, H/block], out bf16 [N,H].
+ * All buffers are device memory owned by the caller; bf16 pointers 16-byte,
+ * e4m3 pointers 8-byte and scales 4-byte aligned, else MOE_ERR_INVALID_ARG.
+ * A block size other than 32/64/128/256 is MOE_ERR_UNSUPPORTED. */
+moe_status_t moe_quantize_fp8(const void* x, int64_t T, int64_t H, int block, void* x_q,
+                              float* scales, void* stream);
+
+moe_status_t moe_dequantize_fp8(const void* x_q, const float* scales, int64_t N, int64_t H,
+                                int block, void* out, void* stream);
+
+/* moe_permute_fp8: moe_permute of the e4m3 rows x_q [T,H] and of their scale
+ * rows scales [T, H/block] with the same slot_pos, in one launch: each token's
+ * scale row travels in the same copy stage as its data row.  out_q
+ * [n_rows,H], out_scales [n_rows, H/block]; rows no slot names are left as
+ * they were; errors as moe_permute.  Buffers whose rows are not 16-byte
+ * multiples or not 16-byte aligned take two moe_permute launches instead. */
+moe_status_t moe_permute_fp8(const void* x_q, const float* scales, int64_t T, int64_t H,
+                             int block, int k, int64_t n_rows, const int32_t* slot_pos,
+                             void* out_q, float* out_scales, void* stream);
 
 /* ------------------------------------------------- workspace status word
  * Waits for `stream`, then reads the status a previous call left in

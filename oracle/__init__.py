@@ -55,6 +55,9 @@ def _load():
                 "oracle_topk_softmax_grouped": [P, I64, I, I, I, I, P, P, P],
                 "oracle_route_indices": [P, P, I64, I, I, P, P, P, P, P, P, P],
                 "oracle_permute": [P, I, I64, I64, P, I64, P],
+                "oracle_quantize_fp8": [P, I64, I64, I, P, P],
+                "oracle_dequantize_fp8": [P, P, I64, I64, I, P],
+                "oracle_e4m3_from_float": [P, I64, P],
                 "oracle_route_layout": [P, P, I64, I, I, I, I, I, I64, P, P, P, P, P, P],
                 "oracle_chunk_idxs": [I, I, I, P],
                 "oracle_sort_chunks": [P, I64, I64, P, P, I, P],
@@ -150,6 +153,33 @@ def route_indices(topk_idx, topk_w, E):
     return out
 
 
+def e4m3_from_float(v):
+    v = _c(v, np.float32)
+    out = np.empty(v.shape, np.uint8)
+    _check(_load().oracle_e4m3_from_float(_ptr(v), v.size, _ptr(out)), "e4m3_from_float")
+    return out
+
+
+def quantize_fp8(x, block=128):
+    """Per-token, per-block e4m3 quantization of bf16 rows (see oracle.h)."""
+    x = _c(x, np.uint16)
+    T, H = x.shape
+    q = np.empty((T, H), np.uint8)
+    sc = np.empty((T, H // block), np.float32)
+    _check(_load().oracle_quantize_fp8(_ptr(x), T, H, block, _ptr(q), _ptr(sc)), "quantize_fp8")
+    return q, sc
+
+
+def dequantize_fp8(q, scales, block=128):
+    q = _c(q, np.uint8)
+    sc = _c(scales, np.float32)
+    N, H = q.shape
+    out = np.empty((N, H), np.uint16)
+    _check(_load().oracle_dequantize_fp8(_ptr(q), _ptr(sc), N, H, block, _ptr(out)),
+           "dequantize_fp8")
+    return out
+
+
 def expert_capacity(tokens, top_k, num_experts, capacity_factor):
     c = _load().oracle_expert_capacity(int(tokens), int(top_k), int(num_experts),
                                        float(capacity_factor))
@@ -188,7 +218,8 @@ def route(logits, k):
 
 def permute(x, sorted_indices, n_rows=None):
     x = np.ascontiguousarray(x)
-    _dtype_code(x)
+    if x.dtype != np.uint8:
+        _dtype_code(x)
     T, H = x.shape
     si = _c(sorted_indices, np.int32)
     n = si.size if n_rows is None else int(n_rows)

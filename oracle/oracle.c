@@ -312,11 +312,84 @@ int oracle_route_layout(const int32_t* topk_idx, const float* topk_w, int64_t T,
     return 0;
 }
 
+/* -------------------------------------------------------------- FP8 e4m3 */
+
+/* e4m3fn: 1 sign, 4 exponent bits (bias 7), 3 mantissa bits; normal values
+ * (1 + m/8) * 2^(e-7) for e = 1..15 (e = 15, m = 7 is NaN), subnormals
+ * m/8 * 2^-6.  Round |f| to a multiple of its quantum (2^(lead-3), or 2^-9
+ * below 2^-6) with ties to even, saturate at 448, then encode. */
+static uint8_t e4m3_bits(float f) {
+    if (isnan(f)) return 0x7F;
+    uint8_t sign = signbit(f) ? 0x80 : 0x00;
+    double a = fabs((double)f);
+    if (a == 0.0) return sign;
+    int ex;
+    (void)frexp(a, &ex);
+    int lead = ex - 1;
+    if (lead < -6) lead = -6;
+    double q = ldexp(1.0, lead - 3);
+    double r = rint(a / q) * q;
+    if (r > 448.0) r = 448.0;
+    if (r < ldexp(1.0, -6)) return (uint8_t)(sign | (uint8_t)(r / ldexp(1.0, -9)));
+    (void)frexp(r, &ex);
+    int e = ex - 1;                                   /* r in [2^e, 2^(e+1)) */
+    int m = (int)(r / ldexp(1.0, e - 3)) - 8;         /* 0..7 */
+    return (uint8_t)(sign | ((e + 7) << 3) | m);
+}
+
+static double e4m3_value(uint8_t b) {
+    int e = (b >> 3) & 0xF, m = b & 7;
+    double v = e == 0 ? ldexp((double)m, -9) : ldexp(8.0 + m, e - 10);
+    return (b & 0x80) ? -v : v;
+}
+
+int oracle_e4m3_from_float(const float* v, int64_t n, uint8_t* out) {
+    if (n < 0 || (n > 0 && (!v || !out))) return -1;
+    for (int64_t i = 0; i < n; ++i) out[i] = e4m3_bits(v[i]);
+    return 0;
+}
+
+int oracle_quantize_fp8(const uint16_t* x, int64_t T, int64_t H, int block, uint8_t* q,
+                        float* scales) {
+    if (T < 0 || H < 0 || block < 1 || H % block != 0) return -1;
+    if (T > 0 && H > 0 && (!x || !q || !scales)) return -1;
+    int64_t nb = H / block;
+    for (int64_t t = 0; t < T; ++t) {
+        for (int64_t b = 0; b < nb; ++b) {
+            float amax = 0.0f;
+            for (int64_t i = 0; i < block; ++i) {
+                float v = fabsf((float)bf16_bits_to_double(x[t * H + b * block + i]));
+                if (v > amax) amax = v;
+            }
+            float s = amax > 0.0f ? amax / 448.0f : 1.0f;
+            scales[t * nb + b] = s;
+            for (int64_t i = 0; i < block; ++i) {
+                float v = (float)bf16_bits_to_double(x[t * H + b * block + i]);
+                q[t * H + b * block + i] = e4m3_bits(v / s);
+            }
+        }
+    }
+    return 0;
+}
+
+int oracle_dequantize_fp8(const uint8_t* q, const float* scales, int64_t N, int64_t H,
+                          int block, uint16_t* out) {
+    if (N < 0 || H < 0 || block < 1 || H % block != 0) return -1;
+    if (N > 0 && H > 0 && (!q || !scales || !out)) return -1;
+    int64_t nb = H / block;
+    for (int64_t r = 0; r < N; ++r)
+        for (int64_t h = 0; h < H; ++h)
+            out[r * H + h] = double_to_bf16_bits(e4m3_value(q[r * H + h]) *
+                                                 (double)scales[r * nb + h / block]);
+    return 0;
+}
+
 /* --------------------------------------------------------------- permute */
 
 int oracle_permute(const void* x, int elem_size, int64_t T, int64_t H,
                    const int32_t* sorted_indices, int64_t n_rows, void* out) {
-    if (T < 0 || H < 0 || n_rows < 0 || (elem_size != 2 && elem_size != 4)) return -1;
+    if (T < 0 || H < 0 || n_rows < 0 || (elem_size != 1 && elem_size != 2 && elem_size != 4))
+        return -1;
     if (n_rows > 0 && (!x || !sorted_indices || !out)) return -1;
     size_t row = (size_t)(H * elem_size);
     for (int64_t p = 0; p < n_rows; ++p) {

@@ -105,8 +105,26 @@ int oracle_route_layout(const int32_t* topk_idx, const float* topk_w, int64_t T,
                         int32_t* counts, int32_t* offsets, int32_t* group_list,
                         int32_t* sorted_indices, int32_t* slot_pos, float* permuted_probs);
 
+/* FP8 dispatch ([COMBINE] §3: the dispatch moves FP8 rows with scales, the
+ * combine stays BF16; [DISPATCH] names x_scales / num_scales): per token and
+ * per block of `block` consecutive elements, scale = amax / 448 (448 = the
+ * largest finite e4m3 value; an all-zero block gets scale 1), and each
+ * element becomes e4m3(x / scale): the float quotient rounded to nearest
+ * even e4m3, saturated to +-448.  x: bf16 [T,H]; q: e4m3 bytes [T,H];
+ * scales: float [T, H/block]. */
+int oracle_quantize_fp8(const uint16_t* x, int64_t T, int64_t H, int block, uint8_t* q,
+                        float* scales);
+
+/* out = bf16(q * scale): the exact product rounded once. */
+int oracle_dequantize_fp8(const uint8_t* q, const float* scales, int64_t N, int64_t H,
+                          int block, uint16_t* out);
+
+/* e4m3 (fn: no infinities, 0x7F/0xFF NaN) of a float: nearest, ties to even,
+ * saturated to +-448.  Exported for the pins. */
+int oracle_e4m3_from_float(const float* v, int64_t n, uint8_t* out);
+
 /* [DISPATCH] §1.1 permuted_input = tokens.index_select(0, sorted_indices):
- * out[p] = x[sorted_indices[p]] for p < n_rows; elem_size 4 or 2 bytes. */
+ * out[p] = x[sorted_indices[p]] for p < n_rows; elem_size 4, 2 or 1 bytes. */
 int oracle_permute(const void* x, int elem_size, int64_t T, int64_t H,
                    const int32_t* sorted_indices, int64_t n_rows, void* out);
 

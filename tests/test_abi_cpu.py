@@ -94,6 +94,18 @@ def test_host_validation_rejects_before_launch(lib):
     assert lib.moe_chunk_idxs(0, 4, 0, None) == 1
     assert lib.moe_expert_scale(fake, 1, 10, 16, 0, fake, fake, fake, None) == 1
     assert lib.moe_workspace_status(P(0x1003), None) == 3
+    # FP8: block sizes, divisibility and alignment
+    assert lib.moe_quantize_fp8(fake, 4, 256, 48, fake, fake, None) == 2
+    assert lib.moe_quantize_fp8(fake, 4, 200, 128, fake, fake, None) == 1
+    assert lib.moe_quantize_fp8(P(0x1008), 4, 256, 128, fake, fake, None) == 1
+    assert lib.moe_quantize_fp8(fake, 4, 256, 128, P(0x1004), fake, None) == 1
+    assert lib.moe_dequantize_fp8(fake, fake, 4, 256, 128, P(0x1008), None) == 1
+    assert lib.moe_dequantize_fp8(None, None, 0, 256, 128, None, None) == 0
+    assert lib.moe_permute_fp8(fake, fake, 4, 256, 100, 2, 8, fake, fake, fake, None) == 2
+    assert lib.moe_permute_fp8(fake, fake, 4, 200, 128, 2, 8, fake, fake, fake, None) == 1
+    assert lib.moe_permute_fp8(fake, None, 4, 256, 128, 2, 8, fake, fake, fake, None) == 1
+    assert lib.moe_permute_fp8(fake, fake, 4, 256, 128, 33, 8, fake, fake, fake, None) == 2
+    assert lib.moe_permute_fp8(None, None, 0, 256, 128, 2, 0, None, None, None, None) == 0
     # empty problems are valid no-ops and launch nothing
     assert lib.moe_permute(None, 1, 0, 16, 2, 0, None, None, None) == 0
     assert lib.moe_combine(None, 1, 0, 16, 2, 0, None, None, None, None) == 0

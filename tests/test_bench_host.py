@@ -61,6 +61,16 @@ def test_algorithmic_bytes_at_the_deepseek_shape():
     assert a["combine"] - a["permute"] == 4 * N
 
 
+def test_fp8_bytes_at_the_deepseek_shape():
+    f = bench.fp8_bytes(16384, 7168, 8)
+    T, H, N, nb = 16384, 7168, 16384 * 8, 56
+    assert f["quantize_fp8"] == 3 * T * H + 4 * T * nb
+    # the FP8 permute writes half the bf16 permute's row bytes
+    bf = bench.algorithmic_bytes(T, H, 256, 8, 2)["permute"]
+    assert f["permute"] < 0.52 * bf
+    assert f["dequantize_fp8"] == 3 * N * H + 4 * N * nb
+
+
 def test_clock_summary_parses_nvidia_smi_lines():
     c = bench.ClockSampler(0)
     c.out = ("0, 2070, 2070, 900.1, 0x0, Not Active, Not Active, Not Active, Not Active\n"

@@ -272,6 +272,50 @@ def test_route_all_tokens_one_expert():
     assert r["slot_pos"][:, 0].tolist() == list(range(T))
 
 
+# ------------------------------------------------------------------ FP8
+
+def test_e4m3_encoding_table():
+    v = np.array([0.0, -0.0, 1.0, -1.0, 0.5, 448.0, 500.0, -1e9, 2.0 ** -6, 2.0 ** -9,
+                  7 * 2.0 ** -9, 1.0625, 1.1875, 2.0 ** -10, 3 * 2.0 ** -10, 240.0, 17.0, 18.0],
+                 np.float32)
+    got = oracle.e4m3_from_float(v).tolist()
+    # 1.0625 is the midpoint of 1.0 and 1.125: ties to even -> 1.0 (0x38);
+    # 1.1875 is the midpoint of 1.125 and 1.25 -> 1.25 (0x3A); 2^-10 ties to 0;
+    # 3*2^-10 ties to 2*2^-10 -> 0x02; 17 ties 16|18 -> 16 (0x58); 500 saturates
+    assert got == [0x00, 0x80, 0x38, 0xB8, 0x30, 0x7E, 0x7E, 0xFE, 0x08, 0x01, 0x07, 0x38,
+                   0x3A, 0x00, 0x02, 0x77, 0x58, 0x59]
+
+
+def test_e4m3_matches_torch_in_range():
+    torch = pytest.importorskip("torch")
+    if not hasattr(torch, "float8_e4m3fn"):
+        pytest.skip("torch without float8")
+    rng = np.random.default_rng(5)
+    v = np.concatenate([rng.standard_normal(50000) * 30, rng.standard_normal(5000) * 1e-2,
+                        rng.uniform(-448, 448, 5000)]).astype(np.float32)
+    ref = torch.from_numpy(v).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert (oracle.e4m3_from_float(v) == ref).all()
+
+
+def test_fp8_quantize_round_trip_bounds():
+    x = wl.random_activation(6, (40, 512), "bf16")
+    x[3, :128] = 0                                     # an all-zero block
+    q, sc = oracle.quantize_fp8(x, 128)
+    assert sc.shape == (40, 4) and sc[3, 0] == 1.0 and (q[3, :128] == 0).all()
+    xf = wl.bf16_bits_to_f32(x).astype(np.float64)
+    amax = np.abs(xf.reshape(40, 4, 128)).max(axis=2)
+    np.testing.assert_array_equal(sc[amax > 0], (amax[amax > 0] / 448.0).astype(np.float32))
+    dq = wl.bf16_bits_to_f32(oracle.dequantize_fp8(q, sc, 128)).astype(np.float64)
+    s = np.repeat(sc.astype(np.float64), 128, axis=1)
+    # e4m3 keeps 4 significant bits: error <= 2^-4 relative, plus the
+    # subnormal quantum 2^-9 * scale, plus the final bf16 rounding
+    err = np.abs(dq - xf)
+    assert (err <= np.abs(xf) * 2.0 ** -4 + s * 2.0 ** -10 + np.abs(dq) * 2.0 ** -8 + 1e-30).all()
+    # the block maximum maps to +-448
+    qa = np.abs(q.reshape(40, 4, 128).astype(np.int32) & 0x7F).max(axis=2)
+    assert (qa[amax > 0] == 0x7E).all()
+
+
 # ------------------------------------------------ capacity / padded layout
 
 def test_capacity_worked_example(golden):

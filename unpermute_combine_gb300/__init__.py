@@ -27,7 +27,7 @@ __all__ = [
     "moe_route_noalloc", "MOE_ROUTE_NOALLOC_SCRATCH_BYTES", "moe_grouped_swiglu_pack",
     "moe_grouped_swiglu_workspace_size", "moe_grouped_swiglu", "moe_device_status",
     "moe_route_grouped", "moe_expert_capacity", "moe_route_layout_rows", "moe_route_layout",
-    "moe_fill_pad_rows",
+    "moe_fill_pad_rows", "moe_quantize_fp8", "moe_dequantize_fp8", "moe_permute_fp8",
 ]
 
 # Size of the library's built-in scratch array used by moe_route_noalloc.
@@ -35,6 +35,9 @@ MOE_ROUTE_NOALLOC_SCRATCH_BYTES = 1 << 20
 
 MOE_OK = 0
 _DT = {torch.float32: 0, torch.bfloat16: 1}
+_DT_MOVE = dict(_DT)
+if hasattr(torch, "float8_e4m3fn"):
+    _DT_MOVE[torch.float8_e4m3fn] = 2
 
 
 class MoeError(RuntimeError):
@@ -75,6 +78,9 @@ def load_library():
             "moe_route_layout": ([P, P, I64, I, I, I, I, I, I64, P, P, P, P, P, P, P, SZ, P], I),
             "moe_fill_pad_rows": ([P, I, I64, I64, P, P, I, P], I),
             "moe_expert_capacity": ([I64, I, I, ctypes.c_double, ctypes.POINTER(I64)], I),
+            "moe_quantize_fp8": ([P, I64, I64, I, P, P, P], I),
+            "moe_dequantize_fp8": ([P, P, I64, I64, I, P, P], I),
+            "moe_permute_fp8": ([P, P, I64, I64, I, I, I64, P, P, P, P], I),
             "moe_route_grouped": ([P, I64, I, I, I, I, P, P, P, P, P, P, P, P, P, P, SZ, P], I),
             "moe_permute": ([P, I, I64, I64, I, I64, P, P, P], I),
             "moe_sort_chunks_workspace_size": ([I, PSZ], I),
@@ -138,6 +144,13 @@ def _act(t, name):
     if t.dtype not in _DT:
         raise ValueError(f"{name} must be float32 or bfloat16, got {t.dtype}")
     return _DT[t.dtype]
+
+
+def _act_move(t, name):
+    _cuda(t, name, ndim=2)
+    if t.dtype not in _DT_MOVE:
+        raise ValueError(f"{name} must be float32, bfloat16 or float8_e4m3fn, got {t.dtype}")
+    return _DT_MOVE[t.dtype]
 
 
 def _empty(shape, dtype, like):
@@ -280,6 +293,68 @@ def moe_route_noalloc(logits: torch.Tensor, k: int, *, routing_map: bool = False
     return r
 
 
+# ------------------------------------------------------------ FP8 dispatch
+
+def moe_quantize_fp8(x: torch.Tensor, block: int = 128, out=None, stream=None):
+    """(x_q float8_e4m3fn [T,H], scales float32 [T,H/block]) of bf16 rows;
+    out: an optional (x_q, scales) pair to write into."""
+    _cuda(x, "x", torch.bfloat16, 2)
+    T, H = x.shape
+    if out is None:
+        q = torch.empty((T, H), dtype=torch.float8_e4m3fn, device=x.device)
+        sc = torch.empty((T, H // block if block else 0), dtype=torch.float32, device=x.device)
+    else:
+        q, sc = out
+        _cuda(q, "x_q", torch.float8_e4m3fn, 2)
+        _cuda(sc, "scales", torch.float32, 2)
+    _ok("moe_quantize_fp8", load_library().moe_quantize_fp8(_p(x), T, H, block, _p(q), _p(sc),
+                                                            _stream(stream)))
+    return q, sc
+
+
+def moe_dequantize_fp8(x_q: torch.Tensor, scales: torch.Tensor, block: int = 128,
+                       out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """bf16(x_q * scale) per block."""
+    _cuda(x_q, "x_q", torch.float8_e4m3fn, 2)
+    _cuda(scales, "scales", torch.float32, 2)
+    N, H = x_q.shape
+    if out is None:
+        out = torch.empty((N, H), dtype=torch.bfloat16, device=x_q.device)
+    _ok("moe_dequantize_fp8", load_library().moe_dequantize_fp8(
+        _p(x_q), _p(scales), N, H, block, _p(out), _stream(stream)))
+    return out
+
+
+def moe_permute_fp8(x_q: torch.Tensor, scales: torch.Tensor, slot_pos: torch.Tensor, out=None,
+                    n_rows: Optional[int] = None, stream=None):
+    """Move e4m3 rows and their scale rows to the slot rows slot_pos names, in
+    one launch; returns (out_q [n_rows,H], out_scales [n_rows,H/block])."""
+    _cuda(x_q, "x_q", torch.float8_e4m3fn, 2)
+    _cuda(scales, "scales", torch.float32, 2)
+    _cuda(slot_pos, "slot_pos", torch.int32, 2)
+    T, H = x_q.shape
+    k = slot_pos.shape[1]
+    if slot_pos.shape[0] != T or scales.shape[0] != T or scales.shape[1] == 0 or \
+            H % scales.shape[1] != 0:
+        raise ValueError("x_q, scales and slot_pos must have one row per token, "
+                         "and scales H/block columns")
+    block = H // scales.shape[1]
+    if out is None:
+        rows = T * k if n_rows is None else n_rows
+        oq = torch.empty((rows, H), dtype=torch.float8_e4m3fn, device=x_q.device)
+        osc = torch.empty((rows, scales.shape[1]), dtype=torch.float32, device=x_q.device)
+    else:
+        oq, osc = out
+        _cuda(oq, "out_q", torch.float8_e4m3fn, 2)
+        _cuda(osc, "out_scales", torch.float32, 2)
+        if oq.shape[0] != osc.shape[0] or oq.shape[1] != H or osc.shape[1] != scales.shape[1]:
+            raise ValueError("out_q / out_scales shapes do not match x_q / scales")
+    _ok("moe_permute_fp8", load_library().moe_permute_fp8(
+        _p(x_q), _p(scales), T, H, block, k, oq.shape[0], _p(slot_pos), _p(oq), _p(osc),
+        _stream(stream)))
+    return oq, osc
+
+
 # ---------------------------------------------- capacity / padded layout
 
 def moe_expert_capacity(tokens: int, top_k: int, num_experts: int,
@@ -327,7 +402,7 @@ def moe_route_layout(topk_idx: torch.Tensor, topk_w: Optional[torch.Tensor], E: 
 def moe_fill_pad_rows(rows: torch.Tensor, offsets: torch.Tensor, counts: torch.Tensor,
                       stream=None) -> torch.Tensor:
     """Zero the padding rows of a padded / aligned permuted buffer."""
-    dt = _act(rows, "rows")
+    dt = _act_move(rows, "rows")
     _cuda(offsets, "offsets", torch.int32, 1)
     _cuda(counts, "counts", torch.int32, 1)
     E = counts.numel()
@@ -342,7 +417,7 @@ def moe_permute(x: torch.Tensor, slot_pos: torch.Tensor, out: Optional[torch.Ten
                 n_rows: Optional[int] = None, stream=None) -> torch.Tensor:
     """permuted[slot_pos[t,j]] = x[t]; out has n_rows rows (T*k by default, or
     out's rows); rows no slot names are left as they were."""
-    dt = _act(x, "x")
+    dt = _act_move(x, "x")
     _cuda(slot_pos, "slot_pos", torch.int32, 2)
     T, H = x.shape
     k = slot_pos.shape[1]
@@ -373,7 +448,7 @@ def moe_sort_chunks(x: torch.Tensor, split_sizes: torch.Tensor, sorted_idxs: tor
                     stream=None) -> torch.Tensor:
     """out = cat([x.split(split_sizes)[i] for i in sorted_idxs]); split_sizes
     and sorted_idxs are int32 CUDA tensors (no host synchronisation)."""
-    dt = _act(x, "x")
+    dt = _act_move(x, "x")
     _cuda(split_sizes, "split_sizes", torch.int32, 1)
     _cuda(sorted_idxs, "sorted_idxs", torch.int32, 1)
     C = split_sizes.numel()

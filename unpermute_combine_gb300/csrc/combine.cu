@@ -369,21 +369,6 @@ __device__ __forceinline__ float dd_warp_sum(float hi, float lo) {
     return __fadd_rn(hi, lo);
 }
 
-// bf16 of the exact product a*b (see expert_scale in permute.cu for the
-// argument): the float product rounds correctly unless it sits on a midpoint.
-__device__ __forceinline__ uint32_t mul_bf16_rn_bits(float a, float b) {
-    const float p = __fmul_rn(a, b);
-    const uint32_t u = __float_as_uint(p);
-    if ((u & 0xFFFFu) == 0x8000u) {
-        const float e = __fmaf_rn(a, b, -p);
-        if (e != 0.0f) {
-            const bool same = ((__float_as_uint(e) ^ u) & 0x80000000u) == 0;
-            return (same ? u + 0x8000u : u - 0x8000u) >> 16;
-        }
-    }
-    return f32_to_bf16_rn(p);
-}
-
 // Two floats in one 64-bit register (low word = even element): Blackwell's
 // packed f32x2 add/sub/mul run two lanes of float arithmetic per instruction.
 typedef unsigned long long f2_t;
@@ -436,15 +421,17 @@ __device__ __forceinline__ uint32_t scale_pair_bf16_f2(f2_t w2, f2_t g2) {
         float w, w_hi, g0, g1;
         f2_unpack(w2, w, w_hi);
         f2_unpack(g2, g0, g1);
-        return mul_bf16_rn_bits(w, g0) | (mul_bf16_rn_bits(w, g1) << 16);
+        return mul_bf16_rn(w, g0) | (mul_bf16_rn(w, g1) << 16);
     }
     return pack_bf16x2_rn(p0, p1);
 }
 
 // k <= 8: every slot row of the current 16-byte column is loaded before any
-// arithmetic, so a lane keeps k loads in flight.
+// arithmetic, so a lane keeps k loads in flight.  Two CTAs per SM (at most
+// 128 registers a thread) keep enough loads in flight to cover HBM latency;
+// one CTA per SM loses a third of the bandwidth.
 template <int KMAX>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 2)
 combine_bwd_bf16_vec_kernel(const uint4* __restrict__ gout, const uint4* __restrict__ y,
                             int64_t T, int64_t nvec, int k, int64_t n_rows,
                             const int32_t* __restrict__ slot_pos,
@@ -545,7 +532,7 @@ combine_bwd_elem_kernel(const E* __restrict__ gout, const E* __restrict__ y, int
                     lo[j] = __fadd_rn(lo[j], eq);
                 } else {
                     yv = bf16_to_f32(y[at]);
-                    gy[at] = uint16_t(mul_bf16_rn_bits(w, g));
+                    gy[at] = uint16_t(mul_bf16_rn(w, g));
                     dd_add1(hi[j], lo[j], __fmul_rn(g, yv));
                 }
             }

@@ -17,9 +17,13 @@ constexpr size_t kWsAlign = 256;
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-inline size_t elem_size(moe_dtype_t d) { return d == MOE_F32 ? 4 : 2; }
+inline size_t elem_size(moe_dtype_t d) { return d == MOE_F32 ? 4 : d == MOE_BF16 ? 2 : 1; }
 
+// dtypes the arithmetic ops take
 inline bool dtype_ok(int d) { return d == MOE_F32 || d == MOE_BF16; }
+
+// dtypes the row-movement ops take (rows are moved as bytes)
+inline bool dtype_ok_move(int d) { return d == MOE_F32 || d == MOE_BF16 || d == MOE_FP8_E4M3; }
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -72,6 +76,24 @@ __device__ __forceinline__ uint16_t f64_to_bf16_rn(double v) {
 }
 
 __device__ __forceinline__ float f64_to_f32_rn(double v) { return __double2float_rn(v); }
+
+// bf16 of the exact product a*b.  p = fl(a*b) is within half a float ulp of
+// it, so p rounds like the exact product unless p sits exactly on a bf16
+// midpoint; then the sign of the product's error e = fma(a,b,-p) breaks the
+// tie (Dekker/Knuth error-free product).  The bf16 bits come back in the low
+// half of a 32-bit word (callers pack pairs of them).
+__device__ __forceinline__ uint32_t mul_bf16_rn(float a, float b) {
+    const float p = __fmul_rn(a, b);
+    const uint32_t u = __float_as_uint(p);
+    if ((u & 0xFFFFu) == 0x8000u) {
+        const float e = __fmaf_rn(a, b, -p);
+        if (e != 0.0f) {
+            const bool same = ((__float_as_uint(e) ^ u) & 0x80000000u) == 0;
+            return (same ? u + 0x8000u : u - 0x8000u) >> 16;
+        }
+    }
+    return f32_to_bf16_rn(p);
+}
 
 // Streaming 16-byte global accesses.
 __device__ __forceinline__ uint4 ld_nc_v4(const void* p) {

@@ -59,13 +59,20 @@ permute_kernel(const V* __restrict__ x, int64_t T, int64_t nvec, int k, int64_t 
 // stores from it have finished reading it (bulk wait_group.read).  Waits on
 // the stage mbarriers are bounded; a timeout stops the CTA and is recorded in
 // *status.
+//
+// An optional side row (side_bytes > 0: the FP8 scale row of the token) rides
+// in the same stage as the token's first piece and goes to the same slot rows
+// of side_out, so one launch moves both.
 constexpr int kPieceMax = 16384;
+constexpr int kSideMax = 4096;
 constexpr int kPermStages = 3;
 
 __global__ void __launch_bounds__(32)
 permute_bulk_kernel(const uint8_t* __restrict__ x, int64_t T, int64_t row_bytes, int piece,
                     int pieces, int k, int64_t n_rows, const int32_t* __restrict__ slot_pos,
-                    uint8_t* __restrict__ out, uint32_t* __restrict__ status) {
+                    uint8_t* __restrict__ out, const uint8_t* __restrict__ side,
+                    uint32_t side_bytes, uint8_t* __restrict__ side_out,
+                    uint32_t* __restrict__ status) {
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ __align__(8) uint64_t full_bar[kPermStages];
     const int lane = threadIdx.x;
@@ -73,6 +80,7 @@ permute_bulk_kernel(const uint8_t* __restrict__ x, int64_t T, int64_t row_bytes,
     const int64_t first = blockIdx.x;
     const int64_t my_items = first < total ? (total - first + gridDim.x - 1) / gridDim.x : 0;
     const uint32_t smem0 = smem_addr(smem);
+    const uint32_t stage_bytes = uint32_t(piece) + side_bytes;
     if (lane == 0) {
         for (int s = 0; s < kPermStages; ++s) mbar_init(smem_addr(&full_bar[s]), 1);
         mbar_fence_init();
@@ -91,8 +99,12 @@ permute_bulk_kernel(const uint8_t* __restrict__ x, int64_t T, int64_t row_bytes,
         item_coords(q, t, off, bytes);
         const int s = int(q % kPermStages);
         const uint32_t fb = smem_addr(&full_bar[s]);
-        mbar_expect_tx(fb, bytes);
-        bulk_load(smem0 + uint32_t(s) * uint32_t(piece), x + t * row_bytes + off, bytes, fb);
+        const bool with_side = side_bytes != 0 && off == 0;
+        mbar_expect_tx(fb, bytes + (with_side ? side_bytes : 0u));
+        bulk_load(smem0 + uint32_t(s) * stage_bytes, x + t * row_bytes + off, bytes, fb);
+        if (with_side)
+            bulk_load(smem0 + uint32_t(s) * stage_bytes + uint32_t(piece), side + t * side_bytes,
+                      side_bytes, fb);
     };
     auto slot_of = [&](int64_t q) -> int32_t {
         if (q >= my_items || lane >= k) return -1;
@@ -118,9 +130,13 @@ permute_bulk_kernel(const uint8_t* __restrict__ x, int64_t T, int64_t row_bytes,
         int64_t t;
         uint32_t off, bytes;
         item_coords(q, t, off, bytes);
-        if (p_cur >= 0)
-            bulk_store(out + int64_t(p_cur) * row_bytes + off, smem0 + uint32_t(s) * uint32_t(piece),
+        if (p_cur >= 0) {
+            bulk_store(out + int64_t(p_cur) * row_bytes + off, smem0 + uint32_t(s) * stage_bytes,
                        bytes);
+            if (side_bytes != 0 && off == 0)
+                bulk_store(side_out + int64_t(p_cur) * side_bytes,
+                           smem0 + uint32_t(s) * stage_bytes + uint32_t(piece), side_bytes);
+        }
         bulk_commit();
         // the stores of item q-1 have read their stage: refill it with item q-1+S
         bulk_wait_read<1>();
@@ -290,23 +306,6 @@ ChunkPlan chunk_plan(void* ws, int C) {
 }
 
 // -------------------------------------------------------------- expert scale
-// Round the exact product a*b to bf16.  p = fl(a*b) is within half a float
-// ulp of it, so p rounds like the exact product unless p sits exactly on a
-// bf16 midpoint; then the sign of the product's error e = fma(a,b,-p) breaks
-// the tie (Dekker/Knuth error-free product).
-__device__ __forceinline__ uint16_t mul_bf16_rn(float a, float b) {
-    const float p = __fmul_rn(a, b);
-    const uint32_t u = __float_as_uint(p);
-    if ((u & 0xFFFFu) == 0x8000u) {
-        const float e = __fmaf_rn(a, b, -p);
-        if (e != 0.0f) {
-            const bool same = ((__float_as_uint(e) ^ u) & 0x80000000u) == 0;
-            return uint16_t((same ? u + 0x8000u : u - 0x8000u) >> 16);
-        }
-    }
-    return f32_to_bf16_rn(p);
-}
-
 template <typename T>
 __global__ void __launch_bounds__(kThreads)
 expert_scale_kernel(const T* __restrict__ in, int64_t n_rows, int64_t H, int E,
@@ -331,7 +330,7 @@ expert_scale_kernel(const T* __restrict__ in, int64_t n_rows, int64_t H, int E,
             if constexpr (sizeof(T) == 4) {
                 out[p * H + h] = __fmul_rn(in[p * H + h], s);
             } else {
-                out[p * H + h] = mul_bf16_rn(bf16_to_f32(in[p * H + h]), s);
+                out[p * H + h] = uint16_t(mul_bf16_rn(bf16_to_f32(in[p * H + h]), s));
             }
         }
     }
@@ -355,15 +354,64 @@ fill_pad_rows_kernel(V* __restrict__ rows, int64_t max_rows, int64_t nvec,
     }
 }
 
+// Rows of row_bytes (a multiple of 16, 16-byte aligned buffers) plus an
+// optional side row of side_bytes (a multiple of 16, at most kSideMax).
+void launch_permute_bulk(const void* x, int64_t T, size_t row, int k, int64_t n_rows,
+                         const int32_t* slot_pos, void* out, const void* side, size_t side_bytes,
+                         void* side_out, cudaStream_t s) {
+    const int pieces = int((row + kPieceMax - 1) / kPieceMax);
+    const int piece = int(((row + pieces - 1) / pieces + 15) / 16 * 16);
+    const size_t smem = size_t(kPermStages) * (size_t(piece) + side_bytes);
+    static bool attr_set[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+        cudaFuncSetAttribute(permute_bulk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kPermStages * (kPieceMax + kSideMax));
+        attr_set[dev] = true;
+    }
+    const int64_t items = T * pieces;
+    const int g = int(min64(items, int64_t(sm_count()) * 4));
+    permute_bulk_kernel<<<g, 32, smem, s>>>(
+        static_cast<const uint8_t*>(x), T, int64_t(row), piece, pieces, k, n_rows, slot_pos,
+        static_cast<uint8_t*>(out), static_cast<const uint8_t*>(side), uint32_t(side_bytes),
+        static_cast<uint8_t*>(side_out), device_status_word());
+}
+
 }  // namespace
 }  // namespace moe
 
 using namespace moe;
 
+extern "C" moe_status_t moe_permute_fp8(const void* x_q, const float* scales, int64_t T,
+                                        int64_t H, int block, int k, int64_t n_rows,
+                                        const int32_t* slot_pos, void* out_q, float* out_scales,
+                                        void* stream) {
+    if (T < 0 || H < 0 || k < 1 || n_rows < 0) return MOE_ERR_INVALID_ARG;
+    if (block != 32 && block != 64 && block != 128 && block != 256) return MOE_ERR_UNSUPPORTED;
+    if (H % block != 0) return MOE_ERR_INVALID_ARG;
+    if (k > kMaxTopK || T * int64_t(k) >= (int64_t(1) << 31) || n_rows >= (int64_t(1) << 31))
+        return MOE_ERR_UNSUPPORTED;
+    if (T == 0 || H == 0 || n_rows == 0) return MOE_OK;
+    if (!x_q || !scales || !slot_pos || !out_q || !out_scales) return MOE_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t row = size_t(H), side = size_t(H / block) * sizeof(float);
+    if (row % 16 == 0 && side % 16 == 0 && side <= size_t(kSideMax) && aligned16(x_q) &&
+        aligned16(out_q) && aligned16(scales) && aligned16(out_scales)) {
+        launch_permute_bulk(x_q, T, row, k, n_rows, slot_pos, out_q, scales, side, out_scales, s);
+        return launch_status();
+    }
+    // rows the bulk path cannot take: the two row sets one after the other
+    const moe_status_t st = moe_permute(x_q, MOE_FP8_E4M3, T, H, k, n_rows, slot_pos, out_q,
+                                        stream);
+    if (st != MOE_OK) return st;
+    return moe_permute(scales, MOE_F32, T, H / block, k, n_rows, slot_pos, out_scales, stream);
+}
+
 extern "C" moe_status_t moe_permute(const void* x, moe_dtype_t dtype, int64_t T, int64_t H, int k,
                                     int64_t n_rows, const int32_t* slot_pos, void* out,
                                     void* stream) {
-    if (!dtype_ok(dtype) || T < 0 || H < 0 || k < 1 || n_rows < 0) return MOE_ERR_INVALID_ARG;
+    if (!dtype_ok_move(dtype) || T < 0 || H < 0 || k < 1 || n_rows < 0) return MOE_ERR_INVALID_ARG;
     if (k > kMaxTopK || T * int64_t(k) >= (int64_t(1) << 31) || n_rows >= (int64_t(1) << 31))
         return MOE_ERR_UNSUPPORTED;
     if (T == 0 || H == 0 || n_rows == 0) return MOE_OK;
@@ -372,30 +420,19 @@ extern "C" moe_status_t moe_permute(const void* x, moe_dtype_t dtype, int64_t T,
     const size_t row = size_t(H) * elem_size(dtype);
     const int64_t blocks = (T + kWarps - 1) / kWarps;
     if (row % 16 == 0 && aligned16(x) && aligned16(out)) {
-        const int pieces = int((row + kPieceMax - 1) / kPieceMax);
-        const int piece = int(((row + pieces - 1) / pieces + 15) / 16 * 16);
-        const size_t smem = size_t(kPermStages) * piece;
-        static bool attr_set[64] = {};
-        int dev = 0;
-        cudaGetDevice(&dev);
-        if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-            cudaFuncSetAttribute(permute_bulk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kPermStages * kPieceMax);
-            attr_set[dev] = true;
-        }
-        const int64_t items = T * pieces;
-        const int g = int(min64(items, int64_t(sm_count()) * 4));
-        permute_bulk_kernel<<<g, 32, smem, s>>>(static_cast<const uint8_t*>(x), T, int64_t(row),
-                                                piece, pieces, k, n_rows, slot_pos,
-                                                static_cast<uint8_t*>(out), device_status_word());
+        launch_permute_bulk(x, T, row, k, n_rows, slot_pos, out, nullptr, 0, nullptr, s);
     } else if (dtype == MOE_F32) {
         const int g = grid_for((const void*)permute_kernel<float>, kThreads, 0, blocks);
         permute_kernel<float><<<g, kThreads, 0, s>>>(
             static_cast<const float*>(x), T, H, k, n_rows, slot_pos, static_cast<float*>(out));
-    } else {
+    } else if (dtype == MOE_BF16) {
         const int g = grid_for((const void*)permute_kernel<uint16_t>, kThreads, 0, blocks);
         permute_kernel<uint16_t><<<g, kThreads, 0, s>>>(
             static_cast<const uint16_t*>(x), T, H, k, n_rows, slot_pos, static_cast<uint16_t*>(out));
+    } else {
+        const int g = grid_for((const void*)permute_kernel<uint8_t>, kThreads, 0, blocks);
+        permute_kernel<uint8_t><<<g, kThreads, 0, s>>>(
+            static_cast<const uint8_t*>(x), T, H, k, n_rows, slot_pos, static_cast<uint8_t*>(out));
     }
     return launch_status();
 }
@@ -411,7 +448,7 @@ extern "C" moe_status_t moe_sort_chunks(const void* in, moe_dtype_t dtype, int64
                                         const int32_t* split_sizes, const int32_t* sorted_idxs,
                                         int C, void* out, void* workspace,
                                         size_t workspace_bytes, void* stream) {
-    if (!dtype_ok(dtype) || N < 0 || H < 0 || C < 1) return MOE_ERR_INVALID_ARG;
+    if (!dtype_ok_move(dtype) || N < 0 || H < 0 || C < 1) return MOE_ERR_INVALID_ARG;
     if (C > kMaxChunks || N >= (int64_t(1) << 31)) return MOE_ERR_UNSUPPORTED;
     if (!split_sizes || !sorted_idxs) return MOE_ERR_INVALID_ARG;
     if (N > 0 && H > 0 && (!in || !out)) return MOE_ERR_INVALID_ARG;
@@ -436,11 +473,15 @@ extern "C" moe_status_t moe_sort_chunks(const void* in, moe_dtype_t dtype, int64
         const int g = grid_for((const void*)sort_chunks_copy_kernel<float>, kThreads, 0, want);
         sort_chunks_copy_kernel<float><<<g, kThreads, 0, s>>>(
             static_cast<const float*>(in), N, H, C, plan, header, static_cast<float*>(out));
-    } else {
+    } else if (dtype == MOE_BF16) {
         const int g = grid_for((const void*)sort_chunks_copy_kernel<uint16_t>, kThreads, 0, want);
         sort_chunks_copy_kernel<uint16_t><<<g, kThreads, 0, s>>>(
             static_cast<const uint16_t*>(in), N, H, C, plan, header,
             static_cast<uint16_t*>(out));
+    } else {
+        const int g = grid_for((const void*)sort_chunks_copy_kernel<uint8_t>, kThreads, 0, want);
+        sort_chunks_copy_kernel<uint8_t><<<g, kThreads, 0, s>>>(
+            static_cast<const uint8_t*>(in), N, H, C, plan, header, static_cast<uint8_t*>(out));
     }
     return launch_status();
 }
@@ -484,7 +525,7 @@ extern "C" moe_status_t moe_expert_scale(const void* in, moe_dtype_t dtype, int6
 extern "C" moe_status_t moe_fill_pad_rows(void* rows, moe_dtype_t dtype, int64_t max_rows,
                                          int64_t H, const int32_t* offsets,
                                          const int32_t* counts, int E, void* stream) {
-    if (!dtype_ok(dtype) || max_rows < 0 || H < 0 || E < 1) return MOE_ERR_INVALID_ARG;
+    if (!dtype_ok_move(dtype) || max_rows < 0 || H < 0 || E < 1) return MOE_ERR_INVALID_ARG;
     if (E > kMaxExperts) return MOE_ERR_UNSUPPORTED;
     if (!offsets || !counts) return MOE_ERR_INVALID_ARG;
     if (max_rows == 0 || H == 0) return MOE_OK;
@@ -498,8 +539,11 @@ extern "C" moe_status_t moe_fill_pad_rows(void* rows, moe_dtype_t dtype, int64_t
     else if (dtype == MOE_F32)
         fill_pad_rows_kernel<float><<<g, kThreads, 0, s>>>(static_cast<float*>(rows), max_rows, H,
                                                            offsets, counts, E);
-    else
+    else if (dtype == MOE_BF16)
         fill_pad_rows_kernel<uint16_t><<<g, kThreads, 0, s>>>(static_cast<uint16_t*>(rows),
                                                               max_rows, H, offsets, counts, E);
+    else
+        fill_pad_rows_kernel<uint8_t><<<g, kThreads, 0, s>>>(static_cast<uint8_t*>(rows),
+                                                             max_rows, H, offsets, counts, E);
     return launch_status();
 }
