@@ -52,6 +52,18 @@ def algorithmic_bytes(T, H, E, k, b):
     }
 
 
+def layout_bytes(T, H, k, b, kept, rows):
+    """Algorithmic bytes under a capacity / padded / aligned layout: only the
+    `kept` slot rows move, and the pad-row fill writes the other rows of the
+    expert segments (`rows` = offsets[E], the rows the segments span)."""
+    N = T * k
+    return {
+        "permute": T * H * b + kept * H * b + N * 4 + (rows - kept) * H * b,
+        "combine": kept * H * b + T * H * b + N * 8,
+        "combine_backward": T * H * b + 2 * kept * H * b + N * 12,
+    }
+
+
 def fp8_bytes(T, H, k, block=128):
     """Algorithmic bytes of the FP8 dispatch stages (bf16 source rows, e4m3
     rows, float scale rows of H/block columns)."""
@@ -395,6 +407,11 @@ def run_ours(args, rank, world, local_rank):
         alg["grouped_swiglu"] = by
     if fp8:
         alg.update(fp8_bytes(T, H, k))
+    if lay:
+        kept = int(rl.counts.sum().item())
+        segs = int(rl.offsets[-1].item())
+        lb = layout_bytes(T, H, k, b, kept, segs)
+        alg.update({n: v for n, v in lb.items() if n in names})
     kern = {}
     for n in names:
         gbs = alg[n] / per[n] / 1e9

@@ -35,8 +35,8 @@ def build(force: bool = False) -> str:
         for f in ("oracle.c", "oracle.h"))
     if force or stale:
         tmp = _LIB + f".{os.getpid()}.tmp"
-        subprocess.run(["gcc", "-std=c11", "-O2", "-fPIC", "-shared", "-Wall",
-                        "-Wextra", "-o", tmp, _SRC, "-lm"], check=True)
+        subprocess.run(["gcc", "-std=c11", "-O2", "-ffp-contract=off", "-fPIC", "-shared",
+                        "-Wall", "-Wextra", "-o", tmp, _SRC, "-lm"], check=True)
         os.replace(tmp, _LIB)
     return _LIB
 
@@ -55,6 +55,7 @@ def _load():
                 "oracle_topk_softmax_grouped": [P, I64, I, I, I, I, P, P, P],
                 "oracle_route_indices": [P, P, I64, I, I, P, P, P, P, P, P, P],
                 "oracle_permute": [P, I, I64, I64, P, I64, P],
+                "oracle_route_backward": [P, P, P, I64, I, I, P],
                 "oracle_quantize_fp8": [P, I64, I64, I, P, P],
                 "oracle_dequantize_fp8": [P, P, I64, I64, I, P],
                 "oracle_e4m3_from_float": [P, I64, P],
@@ -291,6 +292,19 @@ def combine_backward(grad_out, y, slot_pos, topk_w, grad_y_init=None):
                                            _ptr(w), _ptr(grad_y), _ptr(gp), _ptr(gp64)),
            "combine_backward")
     return grad_y, gp, gp64
+
+
+def route_backward(topk_idx, topk_w, grad_probs, E):
+    """grad_logits [T,E] float32 of the k-softmax router (zero off the chosen
+    experts)."""
+    idx = _c(topk_idx, np.int32)
+    T, k = idx.shape
+    w = _c(topk_w, np.float32)
+    g = _c(grad_probs, np.float32)
+    out = np.empty((T, E), np.float32)
+    _check(_load().oracle_route_backward(_ptr(idx), _ptr(w), _ptr(g), T, E, k, _ptr(out)),
+           "route_backward")
+    return out
 
 
 def expert_scale(x_perm, offsets, scale):

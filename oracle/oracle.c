@@ -523,6 +523,34 @@ int oracle_combine_backward(const void* grad_out, const void* y, int dtype,
     return 0;
 }
 
+/* ---------------------------------------------------------- router backward */
+
+int oracle_route_backward(const int32_t* topk_idx, const float* topk_w,
+                          const float* grad_probs, int64_t T, int E, int k,
+                          float* grad_logits) {
+    if (T < 0 || E < 1 || k < 1 || k > E) return -1;
+    if (T > 0 && (!topk_idx || !topk_w || !grad_probs || !grad_logits)) return -1;
+    for (int64_t t = 0; t < T; ++t) {
+        const int32_t* id = topk_idx + t * k;
+        for (int j = 0; j < k; ++j) {
+            if (id[j] < -1 || id[j] >= E) return -1;
+            for (int i = 0; i < j; ++i)
+                if (id[j] >= 0 && id[i] == id[j]) return -1;
+        }
+        double dot = 0.0;
+        for (int j = 0; j < k; ++j)
+            if (id[j] >= 0)
+                dot += (double)topk_w[t * k + j] * (double)grad_probs[t * k + j];
+        for (int e = 0; e < E; ++e) grad_logits[t * E + e] = 0.0f;
+        for (int i = 0; i < k; ++i) {
+            if (id[i] < 0) continue;
+            double d = (double)grad_probs[t * k + i] - dot;
+            grad_logits[t * E + id[i]] = (float)((double)topk_w[t * k + i] * d);
+        }
+    }
+    return 0;
+}
+
 /* ---------------------------------------------------------- stand-in expert */
 
 int oracle_expert_scale(const void* x_perm, int dtype, int64_t H, int E,

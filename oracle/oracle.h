@@ -159,6 +159,19 @@ int oracle_unpermute(const void* y, int dtype, int64_t T, int64_t H,
                      const int32_t* sorted_indices, const float* probs,
                      int64_t n_valid, void* out, double* out_f64);
 
+/* Router backward: only the chosen experts' probabilities carry gradient
+ * ([COMBINE] §6, backward pseudocode), and w is the softmax over the k chosen
+ * logits ([MOE-OPS] §3).  With g = dL/dw (grad_probs of the combine backward)
+ * the softmax Jacobian dw_j/ds_i = w_j (delta_ij - w_i) gives
+ *   grad_logits[t, topk_idx[t,i]] = w_i * (g_i - sum_j w_j g_j)
+ * and 0 for every expert not chosen.  Double arithmetic: the sum over the
+ * valid slots in slot order, then the difference, the product, one rounding
+ * to float.  Slots with id -1 are skipped.  Fails on an id >= E or < -1, or
+ * an id repeated within a token. */
+int oracle_route_backward(const int32_t* topk_idx, const float* topk_w,
+                          const float* grad_probs, int64_t T, int E, int k,
+                          float* grad_logits);
+
 /* [COMBINE] §4 (the backward of the linear combine is its transpose):
  *  grad_y[slot_pos[t,j]] = topk_w[t,j] * grad_out[t]      (rounded once)
  *  grad_probs[t,j]       = sum_h grad_out[t,h] * y[slot_pos[t,j],h]

@@ -71,6 +71,16 @@ def test_fp8_bytes_at_the_deepseek_shape():
     assert f["dequantize_fp8"] == 3 * N * H + 4 * N * nb
 
 
+def test_layout_bytes_count_only_kept_rows():
+    T, H, k, b = 16384, 7168, 8, 2
+    full = bench.algorithmic_bytes(T, H, 256, k, b)
+    same = bench.layout_bytes(T, H, k, b, T * k, T * k)
+    assert same == {n: full[n] for n in same}
+    capped = bench.layout_bytes(T, H, k, b, 50000, 163840)
+    assert capped["combine"] == 50000 * H * b + T * H * b + 8 * T * k
+    assert capped["permute"] == T * H * b + 163840 * H * b + 4 * T * k
+
+
 def test_clock_summary_parses_nvidia_smi_lines():
     c = bench.ClockSampler(0)
     c.out = ("0, 2070, 2070, 900.1, 0x0, Not Active, Not Active, Not Active, Not Active\n"

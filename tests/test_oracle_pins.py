@@ -176,6 +176,90 @@ def test_softmax_closed_forms():
     np.testing.assert_allclose(w2, w, atol=1e-6)
 
 
+# ------------------------------------------------------------ router backward
+
+def test_route_backward_hand_example():
+    # w = (3/4, 1/4), g = (1, 0): sum w g = 3/4, grads 3/4*(1-3/4), 1/4*(0-3/4)
+    # w = (1/2, 1/2), g = (2, -2): sum w g = 0, grads 1 and -1
+    idx = np.array([[2, 0], [1, 3]], np.int32)
+    w = np.array([[0.75, 0.25], [0.5, 0.5]], np.float32)
+    g = np.array([[1.0, 0.0], [2.0, -2.0]], np.float32)
+    got = oracle.route_backward(idx, w, g, 4)
+    exp = np.array([[-0.1875, 0, 0.1875, 0], [0, 1, 0, -1]], np.float32)
+    assert (got == exp).all()
+
+
+def test_route_backward_matches_finite_differences_of_the_router():
+    """d/ds of L = sum_j g_j w_j(s), with w from the oracle's own k-softmax."""
+    rng = np.random.default_rng(41)
+    T, E, k = 24, 12, 4
+    # distinct logits 0.375 apart on a 2^-3 grid: s +- 2^-10 is exact and
+    # keeps the selection and its order
+    logits = np.stack([rng.permutation(E) * 0.375 - 2.0 for _ in range(T)]).astype(np.float32)
+    g = rng.standard_normal((T, k)).astype(np.float32)
+    idx, w, _ = oracle.topk_softmax(logits, k)
+    grad = oracle.route_backward(idx, w, g, E)
+    h = 2.0 ** -10
+
+    def loss(lg):
+        i2, _, w64 = oracle.topk_softmax(lg, k)
+        assert (i2 == idx).all()
+        return (w64 * g.astype(np.float64)).sum(axis=1)
+
+    for e in range(E):
+        lp, lm = logits.copy(), logits.copy()
+        lp[:, e] += np.float32(h)
+        lm[:, e] -= np.float32(h)
+        fd = (loss(lp) - loss(lm)) / (2 * h)
+        np.testing.assert_allclose(grad[:, e], fd, atol=2e-5)
+
+
+def test_route_backward_invariants():
+    rng = np.random.default_rng(42)
+    T, E = 200, 64
+    logits = rng.standard_normal((T, E)).astype(np.float32)
+    for k in (1, 2, 8):
+        idx, w, _ = oracle.topk_softmax(logits, k)
+        g = rng.standard_normal((T, k)).astype(np.float32)
+        grad = oracle.route_backward(idx, w, g, E)
+        chosen = np.zeros((T, E), bool)
+        np.put_along_axis(chosen, idx, True, axis=1)
+        assert (grad[~chosen] == 0).all()                   # only chosen experts
+        if k == 1:
+            assert (grad == 0).all()                        # w = 1 identically
+            continue
+        # softmax is shift invariant: the gradient sums to zero over a token
+        scale = np.abs(w * g).sum(axis=1)
+        assert (np.abs(grad.sum(axis=1)) <= 1e-6 * scale + 1e-30).all()
+        if k == 2:
+            # logistic closed form w1 w2 (g1 - g2), which assumes w1 + w2 = 1;
+            # the float weights miss that by an ulp, hence the scaled bound
+            a = np.take_along_axis(grad, idx, axis=1)
+            w0, w1 = w[:, 0].astype(np.float64), w[:, 1].astype(np.float64)
+            g0, g1 = g[:, 0].astype(np.float64), g[:, 1].astype(np.float64)
+            ref = w0 * w1 * (g0 - g1)
+            bound = 1e-6 * w0 * (np.abs(g0) + np.abs(g1)) + 1e-30
+            assert (np.abs(a[:, 0] - ref) <= bound).all()
+            assert (np.abs(a[:, 1] + ref) <= bound).all()
+    # equal upstream gradients carry no signal through a softmax
+    idx, w, _ = oracle.topk_softmax(logits, 8)
+    grad = oracle.route_backward(idx, w, np.full((T, 8), 3.0, np.float32), E)
+    assert np.abs(grad).max() <= 3e-6
+
+
+def test_route_backward_empty_slots_and_bad_ids():
+    idx = np.array([[1, -1, 0]], np.int32)
+    w = np.array([[0.5, 0.0, 0.5]], np.float32)
+    g = np.array([[1.0, 7.0, 3.0]], np.float32)
+    got = oracle.route_backward(idx, w, g, 3)
+    # sum w g = 0.5 + 1.5 = 2 over the valid slots: expert 1 gets 0.5*(1-2),
+    # expert 0 gets 0.5*(3-2), expert 2 (the empty slot's) nothing
+    assert (got == np.array([[0.5, -0.5, 0.0]], np.float32)).all()
+    for bad in ([[1, 3, 0]], [[1, 1, 0]], [[1, -2, 0]]):
+        with pytest.raises(ValueError):
+            oracle.route_backward(np.array(bad, np.int32), w, g, 3)
+
+
 def test_grouped_topk_with_all_groups_is_plain_topk():
     rng = np.random.default_rng(21)
     logits = rng.standard_normal((50, 24)).astype(np.float32)
