@@ -110,6 +110,8 @@ KERNEL_SOURCES = {
     "combine_backward": ("unpermute_combine_gb300/csrc/combine.cu",
                          "unpermute_combine_gb300/csrc/common.cuh"),
     "quantize_fp8": ("unpermute_combine_gb300/csrc/fp8.cu", "unpermute_combine_gb300/csrc/common.cuh"),
+    "route_backward": ("unpermute_combine_gb300/csrc/route_bwd.cu",
+                       "unpermute_combine_gb300/csrc/common.cuh"),
     "dequantize_fp8": ("unpermute_combine_gb300/csrc/fp8.cu",
                        "unpermute_combine_gb300/csrc/common.cuh"),
 }
@@ -287,6 +289,11 @@ def run_ours(args, rank, world, local_rank):
              ["route", "permute", "combine", "combine_backward"])
     if fp8:
         names[1:2] = ["quantize_fp8", "permute", "dequantize_fp8"]
+    router_bwd = bool(args.router_bwd) and not layer
+    if router_bwd:
+        names.append("route_backward")
+        with torch.cuda.stream(stream):
+            gl = torch.empty((T, E), dtype=torch.float32, device=dev)
 
     def step(lg, xx, gg, ev=None):
         n_marks = [0]
@@ -329,6 +336,9 @@ def run_ours(args, rank, world, local_rank):
             mark()
             moe.moe_combine_backward(gg, xp, rr.slot_pos, r.topk_w, grad_expert_out=gy,
                                      grad_probs=gp, stream=stream)
+            if router_bwd:
+                mark()
+                moe.moe_route_backward(r.topk_idx, r.topk_w, gp, E, out=gl, stream=stream)
         mark()
 
     import torch.distributed as dist
@@ -407,6 +417,8 @@ def run_ours(args, rank, world, local_rank):
         alg["grouped_swiglu"] = by
     if fp8:
         alg.update(fp8_bytes(T, H, k))
+    if router_bwd:
+        alg["route_backward"] = T * E * 4 + T * k * 12
     if lay:
         kept = int(rl.counts.sum().item())
         segs = int(rl.offsets[-1].item())
@@ -445,6 +457,8 @@ def run_ours(args, rank, world, local_rank):
         if groups:
             step_desc = step_desc.replace("moe_route", f"moe_route_grouped({groups[0]} groups, "
                                                        f"{groups[1]} kept)", 1)
+    if router_bwd:
+        step_desc += " + moe_route_backward"
     if fp8:
         step_desc = step_desc.replace("moe_permute", "moe_quantize_fp8(block 128) + "
                                       "moe_permute_fp8(e4m3 rows + scale rows) + moe_dequantize_fp8", 1)
@@ -456,6 +470,8 @@ def run_ours(args, rank, world, local_rank):
     launches = ROUTE_LAUNCHES + (1 + 3 + 1 if layer else 3)   # grouped SwiGLU: reset + 2 GEMMs
     if fp8:
         launches += 2                     # quantize, dequantize
+    if router_bwd:
+        launches += 1
     if lay:
         launches += 3                     # layout check + scatter, pad-row fill
     line = {
@@ -545,6 +561,9 @@ def main(argv=None):
     ap.add_argument("--tokens", type=int, default=None,
                     help="use only the first TOKENS tokens (small cases for profiling)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg")
+    ap.add_argument("--router-bwd", action="store_true",
+                    help="append the router k-softmax backward (grad_probs -> grad_logits) "
+                         "to the training step")
     ap.add_argument("--fp8", action="store_true",
                     help="FP8 dispatch: quantize, move e4m3 rows + scales, dequantize")
     ap.add_argument("--layout", default=None, metavar="SPEC",

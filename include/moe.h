@@ -320,6 +320,23 @@ moe_status_t moe_grouped_swiglu(const void* x, const void* w_up_packed,
                                 int64_t N, int E, int64_t H, int64_t I, void* y,
                                 void* workspace, size_t workspace_bytes, void* stream);
 
+/* ------------------------------------------------------------ router backward
+ * Gradient of the router logits from the gradient of the routing weights.
+ * Only the chosen experts' probabilities carry gradient ([COMBINE] §6,
+ * backward pseudocode) and w is the softmax over the k chosen logits
+ * ([MOE-OPS] §3), so with g = grad_probs (moe_combine_backward's output):
+ *   grad_logits[t, topk_idx[t,i]] = w_i * (g_i - sum_j w_j g_j)
+ * and 0 for the other experts of the row.  Computed in double (the sum in
+ * slot order), rounded once to float.
+ * topk_idx int32 [T,k] (-1 = empty slot, skipped), topk_w and grad_probs
+ * float [T,k], grad_logits float [T,E] (every element written); all device
+ * memory owned by the caller.  1 <= k <= min(E, 32), E <= 1024.  Ids outside
+ * [0,E) other than -1, or repeated within a token, are skipped and recorded
+ * as MOE_ERR_DEVICE_CHECK in the device status word (moe_device_status). */
+moe_status_t moe_route_backward(const int32_t* topk_idx, const float* topk_w,
+                                const float* grad_probs, int64_t T, int E, int k,
+                                float* grad_logits, void* stream);
+
 /* ------------------------------------------------------------ FP8 dispatch
  * [COMBINE] §3 (the dispatch moves FP8 rows with scales, the combine stays
  * BF16) and the x_scales / num_scales of [DISPATCH]'s DeepEP dispatch.
@@ -359,9 +376,11 @@ moe_status_t moe_permute_fp8(const void* x_q, const float* scales, int64_t T, in
 moe_status_t moe_workspace_status(const void* workspace, void* stream);
 
 /* Waits for `stream`, then reads and clears the library's device status word
- * of the current device, which kernels that take no workspace (the bulk-copy
- * permute) set when one of their bounded pipeline waits gives up: MOE_OK or
- * MOE_ERR_TIMEOUT.  One word per device, shared by all streams. */
+ * of the current device, which kernels that take no workspace set: the
+ * bulk-copy permutes when one of their bounded pipeline waits gives up
+ * (MOE_ERR_TIMEOUT), moe_route_backward on an invalid or repeated expert id
+ * (MOE_ERR_DEVICE_CHECK); MOE_OK if neither happened since the last read.
+ * One word per device, shared by all streams. */
 moe_status_t moe_device_status(void* stream);
 
 #ifdef __cplusplus

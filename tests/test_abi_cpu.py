@@ -106,6 +106,12 @@ def test_host_validation_rejects_before_launch(lib):
     assert lib.moe_permute_fp8(fake, None, 4, 256, 128, 2, 8, fake, fake, fake, None) == 1
     assert lib.moe_permute_fp8(fake, fake, 4, 256, 128, 33, 8, fake, fake, fake, None) == 2
     assert lib.moe_permute_fp8(None, None, 0, 256, 128, 2, 0, None, None, None, None) == 0
+    # router backward
+    assert lib.moe_route_backward(fake, fake, fake, 10, 4, 5, fake, None) == 1
+    assert lib.moe_route_backward(fake, fake, fake, 10, 2048, 2, fake, None) == 2
+    assert lib.moe_route_backward(fake, fake, fake, 10, 64, 33, fake, None) == 2
+    assert lib.moe_route_backward(fake, None, fake, 10, 8, 2, fake, None) == 1
+    assert lib.moe_route_backward(None, None, None, 0, 8, 2, None, None) == 0
     # empty problems are valid no-ops and launch nothing
     assert lib.moe_permute(None, 1, 0, 16, 2, 0, None, None, None) == 0
     assert lib.moe_combine(None, 1, 0, 16, 2, 0, None, None, None, None) == 0

@@ -28,6 +28,7 @@ __all__ = [
     "moe_grouped_swiglu_workspace_size", "moe_grouped_swiglu", "moe_device_status",
     "moe_route_grouped", "moe_expert_capacity", "moe_route_layout_rows", "moe_route_layout",
     "moe_fill_pad_rows", "moe_quantize_fp8", "moe_dequantize_fp8", "moe_permute_fp8",
+    "moe_route_backward",
 ]
 
 # Size of the library's built-in scratch array used by moe_route_noalloc.
@@ -81,6 +82,7 @@ def load_library():
             "moe_quantize_fp8": ([P, I64, I64, I, P, P, P], I),
             "moe_dequantize_fp8": ([P, P, I64, I64, I, P, P], I),
             "moe_permute_fp8": ([P, P, I64, I64, I, I, I64, P, P, P, P], I),
+            "moe_route_backward": ([P, P, P, I64, I, I, P, P], I),
             "moe_route_grouped": ([P, I64, I, I, I, I, P, P, P, P, P, P, P, P, P, P, SZ, P], I),
             "moe_permute": ([P, I, I64, I64, I, I64, P, P, P], I),
             "moe_sort_chunks_workspace_size": ([I, PSZ], I),
@@ -294,6 +296,27 @@ def moe_route_noalloc(logits: torch.Tensor, k: int, *, routing_map: bool = False
 
 
 # ------------------------------------------------------------ FP8 dispatch
+
+def moe_route_backward(topk_idx: torch.Tensor, topk_w: torch.Tensor, grad_probs: torch.Tensor,
+                       E: int, out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """grad_logits [T,E] float32 of the k-softmax router (zero off the chosen
+    experts)."""
+    _cuda(topk_idx, "topk_idx", torch.int32, 2)
+    _cuda(topk_w, "topk_w", torch.float32, 2)
+    _cuda(grad_probs, "grad_probs", torch.float32, 2)
+    T, k = topk_idx.shape
+    if topk_w.shape != (T, k) or grad_probs.shape != (T, k):
+        raise ValueError("topk_idx, topk_w and grad_probs must all be [T, k]")
+    if out is None:
+        out = torch.empty((T, E), dtype=torch.float32, device=topk_idx.device)
+    else:
+        _cuda(out, "grad_logits", torch.float32, 2)
+        if tuple(out.shape) != (T, E):
+            raise ValueError("grad_logits must be [T, E]")
+    _ok("moe_route_backward", load_library().moe_route_backward(
+        _p(topk_idx), _p(topk_w), _p(grad_probs), T, E, k, _p(out), _stream(stream)))
+    return out
+
 
 def moe_quantize_fp8(x: torch.Tensor, block: int = 128, out=None, stream=None):
     """(x_q float8_e4m3fn [T,H], scales float32 [T,H/block]) of bf16 rows;

@@ -79,5 +79,6 @@ extern "C" moe_status_t moe_device_status(void* stream) {
         cudaMemsetAsync(word, 0, sizeof v, s) != cudaSuccess ||
         cudaStreamSynchronize(s) != cudaSuccess)
         return MOE_ERR_CUDA;
-    return v == 0 ? MOE_OK : MOE_ERR_TIMEOUT;
+    if (v == 0) return MOE_OK;
+    return v == uint32_t(MOE_ERR_DEVICE_CHECK) ? MOE_ERR_DEVICE_CHECK : MOE_ERR_TIMEOUT;
 }
