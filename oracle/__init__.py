@@ -56,6 +56,8 @@ def _load():
                 "oracle_route_indices": [P, P, I64, I, I, P, P, P, P, P, P, P],
                 "oracle_permute": [P, I, I64, I64, P, I64, P],
                 "oracle_route_backward": [P, P, P, I64, I, I, P],
+                "oracle_swiglu_dgrad": [P, P, P, P, P, I, I64, I64, P, I64, P, P, P, P],
+                "oracle_swiglu_wgrad_at": [P, P, P, P, P, I, I64, I64, I, P, I64, P],
                 "oracle_quantize_fp8": [P, I64, I64, I, P, P],
                 "oracle_dequantize_fp8": [P, P, I64, I64, I, P],
                 "oracle_e4m3_from_float": [P, I64, P],
@@ -66,7 +68,7 @@ def _load():
                 "oracle_unpermute": [P, I, I64, I64, P, P, I64, P, P],
                 "oracle_combine_backward": [P, P, I, I64, I64, I, P, P, P, P, P],
                 "oracle_expert_scale": [P, I, I64, I, P, P, P],
-                "oracle_grouped_swiglu": [P, P, P, P, I, I64, I64, P, I64, P, P],
+                "oracle_grouped_swiglu": [P, P, P, P, I, I64, I64, P, I64, P, P, P, P],
             }
             for name, args in sig.items():
                 fn = getattr(lib, name)
@@ -319,9 +321,10 @@ def expert_scale(x_perm, offsets, scale):
     return y
 
 
-def grouped_swiglu(x, w_up, w_down, offsets, rows=None):
+def grouped_swiglu(x, w_up, w_down, offsets, rows=None, save=False):
     """Per-expert GMM1 -> silu(gate)*up -> GMM2 on bf16 bit patterns.
-    rows: optional list of row ids to compute (others are left zero)."""
+    rows: optional list of row ids to compute (others are left zero).
+    save: also return the bf16 gate_up [N,2I] and hidden [N,I]."""
     x = _c(x, np.uint16)
     w_up = _c(w_up, np.uint16)
     w_down = _c(w_down, np.uint16)
@@ -330,8 +333,49 @@ def grouped_swiglu(x, w_up, w_down, offsets, rows=None):
     I = I2 // 2
     y = np.zeros_like(x)
     y64 = np.zeros(x.shape, np.float64)
+    gu = np.zeros((x.shape[0], 2 * I), np.uint16) if save else None
+    hid = np.zeros((x.shape[0], I), np.uint16) if save else None
     r = None if rows is None else _c(rows, np.int64)
     n = 0 if r is None else r.size
     _check(_load().oracle_grouped_swiglu(_ptr(x), _ptr(w_up), _ptr(w_down), _ptr(off), E, H, I,
-                                         _ptr(r), n, _ptr(y), _ptr(y64)), "grouped_swiglu")
-    return y, y64
+                                         _ptr(r), n, _ptr(y), _ptr(y64), _ptr(gu), _ptr(hid)),
+           "grouped_swiglu")
+    return (y, y64, gu, hid) if save else (y, y64)
+
+
+def swiglu_dgrad(dy, w_up, w_down, offsets, gate_up, rows=None):
+    """(dgate_up bf16 [N,2I], dgate_up f64, dx bf16 [N,H], dx f64) of the
+    grouped SwiGLU backward; rows as in grouped_swiglu."""
+    dy = _c(dy, np.uint16)
+    w_up = _c(w_up, np.uint16)
+    w_down = _c(w_down, np.uint16)
+    off = _c(offsets, np.int32)
+    gu = _c(gate_up, np.uint16)
+    E, H, I2 = w_up.shape
+    I = I2 // 2
+    N = dy.shape[0]
+    dgu = np.zeros((N, 2 * I), np.uint16)
+    dgu64 = np.zeros((N, 2 * I), np.float64)
+    dx = np.zeros((N, H), np.uint16)
+    dx64 = np.zeros((N, H), np.float64)
+    r = None if rows is None else _c(rows, np.int64)
+    n = 0 if r is None else r.size
+    _check(_load().oracle_swiglu_dgrad(_ptr(dy), _ptr(w_up), _ptr(w_down), _ptr(off), _ptr(gu),
+                                       E, H, I, _ptr(r), n, _ptr(dgu), _ptr(dgu64), _ptr(dx),
+                                       _ptr(dx64)), "swiglu_dgrad")
+    return dgu, dgu64, dx, dx64
+
+
+def swiglu_wgrad_at(which, coords, offsets, H, I, x=None, hidden=None, dy=None, dgate_up=None):
+    """Double weight gradients at coords [n,3] = (e, a, b): which 'up' gives
+    dW_up[e][h][c], 'down' gives dW_down[e][i][h]."""
+    off = _c(offsets, np.int32)
+    E = off.size - 1
+    co = _c(coords, np.int64).reshape(-1, 3)
+    out = np.zeros(co.shape[0], np.float64)
+    # keep the converted arrays referenced for the duration of the call
+    xs, hs, ds, gs = (None if a is None else _c(a, np.uint16) for a in (x, hidden, dy, dgate_up))
+    _check(_load().oracle_swiglu_wgrad_at(
+        _ptr(xs), _ptr(hs), _ptr(ds), _ptr(gs), _ptr(off), E, H, I, {"up": 0, "down": 1}[which],
+        _ptr(co), co.shape[0], _ptr(out)), "swiglu_wgrad_at")
+    return out

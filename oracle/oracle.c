@@ -579,7 +579,8 @@ int oracle_grouped_swiglu(const uint16_t* x, const uint16_t* w_up,
                           const uint16_t* w_down, const int32_t* offsets,
                           int E, int64_t H, int64_t I,
                           const int64_t* rows, int64_t n_rows,
-                          uint16_t* y, double* y_f64) {
+                          uint16_t* y, double* y_f64,
+                          uint16_t* gate_up_out, uint16_t* hidden_out) {
     if (E < 1 || H < 1 || I < 1 || !x || !w_up || !w_down || !offsets || !y) return -1;
     int64_t total = offsets[E];
     int64_t count = rows ? n_rows : total;
@@ -603,6 +604,11 @@ int oracle_grouped_swiglu(const uint16_t* x, const uint16_t* w_up,
         /* SwiGLU: first I columns are the gate, last I the up projection */
         for (int64_t i = 0; i < I; ++i)
             hidden[i] = bf16_bits_to_double(double_to_bf16_bits(silu(gate_up[i]) * gate_up[I + i]));
+        if (gate_up_out)
+            for (int64_t c = 0; c < 2 * I; ++c)
+                gate_up_out[p * 2 * I + c] = double_to_bf16_bits(gate_up[c]);
+        if (hidden_out)
+            for (int64_t i = 0; i < I; ++i) hidden_out[p * I + i] = double_to_bf16_bits(hidden[i]);
         /* GMM2: y[p] = hidden @ w_down[e] */
         for (int64_t h = 0; h < H; ++h) acc[h] = 0.0;
         for (int64_t i = 0; i < I; ++i) {
@@ -617,5 +623,85 @@ int oracle_grouped_swiglu(const uint16_t* x, const uint16_t* w_up,
     free(gate_up);
     free(hidden);
     free(acc);
+    return 0;
+}
+
+/* ------------------------------------------------- grouped SwiGLU backward */
+
+int oracle_swiglu_dgrad(const uint16_t* dy, const uint16_t* w_up, const uint16_t* w_down,
+                        const int32_t* offsets, const uint16_t* gate_up, int E, int64_t H,
+                        int64_t I, const int64_t* rows, int64_t n_rows, uint16_t* dgate_up,
+                        double* dgate_up_f64, uint16_t* dx, double* dx_f64) {
+    if (E < 1 || H < 1 || I < 1 || !dy || !w_up || !w_down || !offsets || !gate_up ||
+        !dgate_up || !dx)
+        return -1;
+    int64_t count = rows ? n_rows : offsets[E];
+    double* dh = (double*)malloc(sizeof(double) * (size_t)I);
+    double* dgu = (double*)malloc(sizeof(double) * (size_t)(2 * I));
+    if (!dh || !dgu) { free(dh); free(dgu); return -2; }
+    for (int64_t r = 0; r < count; ++r) {
+        int64_t p = rows ? rows[r] : r;
+        int e = expert_of_row(offsets, E, p);
+        if (e < 0) { free(dh); free(dgu); return -1; }
+        const uint16_t* up_e = w_up + (size_t)e * (size_t)(H * 2 * I);
+        const uint16_t* down_e = w_down + (size_t)e * (size_t)(I * H);
+        /* GMM2 backward: dh = dy[p] @ w_down[e]^T */
+        for (int64_t i = 0; i < I; ++i) {
+            double acc = 0.0;
+            for (int64_t h = 0; h < H; ++h)
+                acc += bf16_bits_to_double(dy[p * H + h]) * bf16_bits_to_double(down_e[i * H + h]);
+            dh[i] = acc;
+        }
+        /* SwiGLU backward at the stored gate / up values */
+        for (int64_t i = 0; i < I; ++i) {
+            double g = bf16_bits_to_double(gate_up[p * 2 * I + i]);
+            double u = bf16_bits_to_double(gate_up[p * 2 * I + I + i]);
+            double sg = 1.0 / (1.0 + exp(-g));
+            dgu[i] = dh[i] * u * sg * (1.0 + g * (1.0 - sg));
+            dgu[I + i] = dh[i] * g * sg;
+        }
+        for (int64_t c = 0; c < 2 * I; ++c) {
+            dgate_up[p * 2 * I + c] = double_to_bf16_bits(dgu[c]);
+            if (dgate_up_f64) dgate_up_f64[p * 2 * I + c] = dgu[c];
+        }
+        /* GMM1 backward from the stored (bf16) dgate_up: dx = dgate_up @ w_up[e]^T */
+        for (int64_t h = 0; h < H; ++h) {
+            double acc = 0.0;
+            for (int64_t c = 0; c < 2 * I; ++c)
+                acc += bf16_bits_to_double(dgate_up[p * 2 * I + c]) *
+                       bf16_bits_to_double(up_e[h * 2 * I + c]);
+            dx[p * H + h] = double_to_bf16_bits(acc);
+            if (dx_f64) dx_f64[p * H + h] = acc;
+        }
+    }
+    free(dh);
+    free(dgu);
+    return 0;
+}
+
+int oracle_swiglu_wgrad_at(const uint16_t* x, const uint16_t* hidden, const uint16_t* dy,
+                           const uint16_t* dgate_up, const int32_t* offsets, int E, int64_t H,
+                           int64_t I, int which, const int64_t* coords, int64_t n,
+                           double* out) {
+    if (E < 1 || H < 1 || I < 1 || !offsets || !coords || (n > 0 && !out)) return -1;
+    if (which != 0 && which != 1) return -1;
+    if (which == 0 && (!x || !dgate_up)) return -1;
+    if (which == 1 && (!hidden || !dy)) return -1;
+    for (int64_t q = 0; q < n; ++q) {
+        int64_t e = coords[3 * q], a = coords[3 * q + 1], b = coords[3 * q + 2];
+        if (e < 0 || e >= E || a < 0 || b < 0) return -1;
+        double acc = 0.0;
+        if (which == 0) {            /* dW_up[e][h=a][c=b] = sum_p x[p,h] dgate_up[p,c] */
+            if (a >= H || b >= 2 * I) return -1;
+            for (int64_t p = offsets[e]; p < offsets[e + 1]; ++p)
+                acc += bf16_bits_to_double(x[p * H + a]) *
+                       bf16_bits_to_double(dgate_up[p * 2 * I + b]);
+        } else {                     /* dW_down[e][i=a][h=b] = sum_p hidden[p,i] dy[p,h] */
+            if (a >= I || b >= H) return -1;
+            for (int64_t p = offsets[e]; p < offsets[e + 1]; ++p)
+                acc += bf16_bits_to_double(hidden[p * I + a]) * bf16_bits_to_double(dy[p * H + b]);
+        }
+        out[q] = acc;
+    }
     return 0;
 }

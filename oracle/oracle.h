@@ -196,12 +196,42 @@ int oracle_expert_scale(const void* x_perm, int dtype, int64_t H, int E,
  *  y_e = hidden @ w_down[e]           [n, H]   (double, rounded to bf16)
  * x [N,H], w_up [E,H,2I], w_down [E,I,H], y [N,H], all bf16 patterns.
  * rows (nullable): compute only these n_rows row ids; otherwise every row in
- * [0, offsets[E]).  y_f64 (nullable) has the same layout as y. */
+ * [0, offsets[E]).  y_f64 (nullable) has the same layout as y.
+ * gate_up_out [N,2I] and hidden_out [N,I] (nullable): the bf16 gate_up and
+ * hidden a training forward keeps for the backward. */
 int oracle_grouped_swiglu(const uint16_t* x, const uint16_t* w_up,
                           const uint16_t* w_down, const int32_t* offsets,
                           int E, int64_t H, int64_t I,
                           const int64_t* rows, int64_t n_rows,
-                          uint16_t* y, double* y_f64);
+                          uint16_t* y, double* y_f64,
+                          uint16_t* gate_up_out, uint16_t* hidden_out);
+
+/* Backward of the grouped SwiGLU, [MOE-OPS] §22 (GMM2 backward -> SwiGLU
+ * backward -> GMM1 backward, giving dX, dW1, dW2) and [COMBINE] §4.2 (dgrad
+ * m-grouped, wgrad k-grouped), per expert segment, from the stored bf16
+ * gate_up [N,2I] and upstream gradient dy [N,H]:
+ *  dh       = dy @ w_down[e]^T                               (double)
+ *  s        = sigmoid(gate)
+ *  d_gate   = dh * up * s * (1 + gate * (1 - s))   (derivative of gate*s)
+ *  d_up     = dh * gate * s                        (= dh * silu(gate))
+ *  dgate_up = [d_gate | d_up]                      rounded to bf16 (stored)
+ *  dx       = dgate_up @ w_up[e]^T   from the stored bf16 dgate_up, rounded
+ * rows (nullable) as in oracle_grouped_swiglu.  The *_f64 outputs
+ * (nullable) keep the unrounded doubles. */
+int oracle_swiglu_dgrad(const uint16_t* dy, const uint16_t* w_up, const uint16_t* w_down,
+                        const int32_t* offsets, const uint16_t* gate_up, int E, int64_t H,
+                        int64_t I, const int64_t* rows, int64_t n_rows, uint16_t* dgate_up,
+                        double* dgate_up_f64, uint16_t* dx, double* dx_f64);
+
+/* Weight gradients (the k-grouped GEMMs: a sum over each expert's rows), in
+ * double, at n coordinates (e, a, b) given as coords[3q..3q+2]:
+ *  which 0: dW_up[e][h=a][c=b]   = sum_{p in e} x[p,h] * dgate_up[p,c]
+ *  which 1: dW_down[e][i=a][h=b] = sum_{p in e} hidden[p,i] * dy[p,h]
+ * An expert with no rows has zero gradient. */
+int oracle_swiglu_wgrad_at(const uint16_t* x, const uint16_t* hidden, const uint16_t* dy,
+                           const uint16_t* dgate_up, const int32_t* offsets, int E, int64_t H,
+                           int64_t I, int which, const int64_t* coords, int64_t n,
+                           double* out);
 
 #ifdef __cplusplus
 }

@@ -647,3 +647,103 @@ def test_grouped_swiglu_reduces_to_dense_ffn():
     # sampled rows give the same values as the full computation
     ys, _ = oracle.grouped_swiglu(x, up, down, offsets, rows=np.array([11, 0, 6]))
     assert (ys[[11, 0, 6]] == y[[11, 0, 6]]).all()
+
+
+# ------------------------------------------------- grouped SwiGLU backward
+
+def _swiglu_case(seed=16):
+    rng = np.random.default_rng(seed)
+    E, H, I = 3, 24, 16
+    counts = [6, 0, 9]
+    N = sum(counts)
+    offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    x = wl.f32_to_bf16_bits(rng.standard_normal((N, H)).astype(np.float32))
+    up = wl.f32_to_bf16_bits((rng.standard_normal((E, H, 2 * I)) * 0.3).astype(np.float32))
+    down = wl.f32_to_bf16_bits((rng.standard_normal((E, I, H)) * 0.3).astype(np.float32))
+    dy = wl.f32_to_bf16_bits(rng.standard_normal((N, H)).astype(np.float32))
+    y, y64, gu, hid = oracle.grouped_swiglu(x, up, down, offsets, save=True)
+    return dict(E=E, H=H, I=I, N=N, offsets=offsets, x=x, up=up, down=down, dy=dy, y64=y64,
+                gu=gu, hid=hid)
+
+
+def _f64(bits):
+    return wl.bf16_bits_to_f32(bits).astype(np.float64)
+
+
+def test_forward_saves_the_stored_activations():
+    c = _swiglu_case()
+    gu, hid, I = _f64(c["gu"]), _f64(c["hid"]), c["I"]
+    # hidden is silu(gate) * up of the unrounded gate_up; from the rounded
+    # one it agrees to a few bf16 quanta
+    ref = gu[:, :I] / (1 + np.exp(-gu[:, :I])) * gu[:, I:]
+    assert np.abs(hid - ref).max() <= 2 ** -6 * np.abs(ref).max()
+
+
+def test_swiglu_dgrad_matches_autograd():
+    """dgate_up (before rounding) is the autograd gradient of
+    sum(dy * (silu(gate)*up) @ w_down[e]) at the stored gate / up."""
+    torch = pytest.importorskip("torch")
+    c = _swiglu_case()
+    dgu, dgu64, dx, dx64 = oracle.swiglu_dgrad(c["dy"], c["up"], c["down"], c["offsets"], c["gu"])
+    I, off = c["I"], c["offsets"]
+    for e in range(c["E"]):
+        a, b = off[e], off[e + 1]
+        if a == b:
+            continue
+        gu = torch.tensor(_f64(c["gu"][a:b]), requires_grad=True)
+        h = torch.nn.functional.silu(gu[:, :I]) * gu[:, I:]
+        y = h @ torch.tensor(_f64(c["down"][e]))
+        (y * torch.tensor(_f64(c["dy"][a:b]))).sum().backward()
+        np.testing.assert_allclose(dgu64[a:b], gu.grad.numpy(), rtol=1e-11, atol=1e-14)
+    # the stored dgate_up is its bf16 rounding
+    assert (dgu == wl.f32_to_bf16_bits(dgu64.astype(np.float32))).mean() > 0.99
+
+
+def test_swiglu_dx_is_the_adjoint_of_gmm1():
+    torch = pytest.importorskip("torch")
+    c = _swiglu_case()
+    dgu, _, dx, dx64 = oracle.swiglu_dgrad(c["dy"], c["up"], c["down"], c["offsets"], c["gu"])
+    off = c["offsets"]
+    xv = torch.zeros((c["N"], c["H"]), dtype=torch.float64, requires_grad=True)
+    loss = 0
+    for e in range(c["E"]):
+        a, b = off[e], off[e + 1]
+        loss = loss + (torch.tensor(_f64(dgu[a:b])) * (xv[a:b] @ torch.tensor(_f64(c["up"][e])))).sum()
+    loss.backward()
+    np.testing.assert_allclose(dx64, xv.grad.numpy(), rtol=1e-12, atol=1e-14)
+
+
+def test_swiglu_wgrad_up_matches_autograd():
+    torch = pytest.importorskip("torch")
+    c = _swiglu_case()
+    dgu, *_ = oracle.swiglu_dgrad(c["dy"], c["up"], c["down"], c["offsets"], c["gu"])
+    E, H, I, off = c["E"], c["H"], c["I"], c["offsets"]
+    wv = torch.zeros((E, H, 2 * I), dtype=torch.float64, requires_grad=True)
+    loss = 0
+    for e in range(E):
+        a, b = off[e], off[e + 1]
+        loss = loss + (torch.tensor(_f64(dgu[a:b])) * (torch.tensor(_f64(c["x"][a:b])) @ wv[e])).sum()
+    loss.backward()
+    coords = np.array([(e, h, j) for e in range(E) for h in range(H) for j in range(2 * I)])
+    got = oracle.swiglu_wgrad_at("up", coords, off, H, I, x=c["x"], dgate_up=dgu)
+    np.testing.assert_allclose(got.reshape(E, H, 2 * I), wv.grad.numpy(), rtol=1e-12, atol=1e-14)
+    assert (got.reshape(E, H, 2 * I)[1] == 0).all()                 # the empty expert
+
+
+def test_swiglu_wgrad_down_by_exact_finite_differences():
+    """y is linear in w_down at fixed hidden: changing one weight by delta
+    changes sum(dy * y) by exactly delta * dW_down (up to double rounding)."""
+    c = _swiglu_case()
+    off, H, I = c["offsets"], c["H"], c["I"]
+    base = (_f64(c["dy"]) * c["y64"]).sum()
+    rng = np.random.default_rng(5)
+    picks = [(e, int(rng.integers(I)), int(rng.integers(H))) for e in (0, 2) for _ in range(6)]
+    got = oracle.swiglu_wgrad_at("down", picks, off, H, I, hidden=c["hid"], dy=c["dy"])
+    for (e, i, h), g in zip(picks, got):
+        down = c["down"].copy()
+        old = wl.bf16_bits_to_f32(down[e, i, h:h + 1])[0]
+        down[e, i, h] = wl.f32_to_bf16_bits(np.array([old + 0.5], np.float32))[0]
+        delta = float(wl.bf16_bits_to_f32(down[e, i, h:h + 1])[0]) - float(old)
+        _, y64 = oracle.grouped_swiglu(c["x"], c["up"], down, off)
+        change = (_f64(c["dy"]) * y64).sum() - base
+        assert change == pytest.approx(delta * g, rel=1e-9, abs=1e-12)
