@@ -320,6 +320,52 @@ moe_status_t moe_grouped_swiglu(const void* x, const void* w_up_packed,
                                 int64_t N, int E, int64_t H, int64_t I, void* y,
                                 void* workspace, size_t workspace_bytes, void* stream);
 
+/* ------------------------------------------- grouped SwiGLU, training path
+ * [MOE-OPS] §22 (GMM2 backward -> SwiGLU backward -> GMM1 backward, giving
+ * dX, dW1 and dW2, with d_gate and d_up from hidden = silu(gate) * up) and
+ * [COMBINE] §4.2 / §5 (the expert backward is an m-grouped dgrad on the
+ * critical path plus a k-grouped wgrad that may be deferred).  Shapes and
+ * alignment as moe_grouped_swiglu (H a multiple of 256, I of 128, all bf16
+ * buffers 16-byte aligned); all buffers are caller-owned device memory.
+ * `workspace` here is only the status header: MOE_STATUS_WORKSPACE_BYTES,
+ * 256-byte aligned; read with moe_workspace_status (MOE_ERR_TIMEOUT if a
+ * bounded tensor-core pipeline wait gave up).
+ *
+ * moe_grouped_swiglu_save: the forward of moe_grouped_swiglu that keeps what
+ * the backward needs: hidden [N,I] (bf16, the GMM2 input) and gate_up [N,2I]
+ * (bf16 GMM1 output, gate columns first) in caller buffers.
+ *
+ * moe_grouped_swiglu_dgrad (m-grouped, per expert segment of offsets):
+ *   dh       = dy @ w_down[e]^T                 (fp32 accumulation)
+ *   s        = sigmoid(gate), gate / up from the stored gate_up
+ *   dgate_up = [dh*up*s*(1 + gate*(1-s)) | dh*gate*s]     -> bf16 [N,2I]
+ *   dx       = dgate_up @ w_up[e]^T             -> bf16 [N,H]
+ * w_up [E,H,2I] and w_down [E,I,H] in their ORIGINAL layouts (not packed):
+ * for these two products they are already K-major.
+ *
+ * moe_grouped_swiglu_wgrad (k-grouped: sums over each expert's rows):
+ *   dw_up[e]   = x_e^T @ dgate_up_e       fp32 [E,H,2I]
+ *   dw_down[e] = hidden_e^T @ dy_e        fp32 [E,I,H]
+ * Either output may be NULL (not computed).  Experts with no rows get zeros.
+ * Segments need no alignment. */
+#define MOE_STATUS_WORKSPACE_BYTES 256
+
+moe_status_t moe_grouped_swiglu_save(const void* x, const void* w_up_packed,
+                                     const void* w_down_packed, const int32_t* offsets,
+                                     int64_t N, int E, int64_t H, int64_t I, void* y,
+                                     void* hidden, void* gate_up, void* workspace,
+                                     size_t workspace_bytes, void* stream);
+
+moe_status_t moe_grouped_swiglu_dgrad(const void* dy, const void* w_up, const void* w_down,
+                                      const int32_t* offsets, const void* gate_up, int64_t N,
+                                      int E, int64_t H, int64_t I, void* dgate_up, void* dx,
+                                      void* workspace, size_t workspace_bytes, void* stream);
+
+moe_status_t moe_grouped_swiglu_wgrad(const void* x, const void* hidden, const void* dy,
+                                      const void* dgate_up, const int32_t* offsets, int64_t N,
+                                      int E, int64_t H, int64_t I, float* dw_up, float* dw_down,
+                                      void* workspace, size_t workspace_bytes, void* stream);
+
 /* ------------------------------------------------------------ router backward
  * Gradient of the router logits from the gradient of the routing weights.
  * Only the chosen experts' probabilities carry gradient ([COMBINE] §6,

@@ -28,8 +28,12 @@ __all__ = [
     "moe_grouped_swiglu_workspace_size", "moe_grouped_swiglu", "moe_device_status",
     "moe_route_grouped", "moe_expert_capacity", "moe_route_layout_rows", "moe_route_layout",
     "moe_fill_pad_rows", "moe_quantize_fp8", "moe_dequantize_fp8", "moe_permute_fp8",
-    "moe_route_backward",
+    "moe_route_backward", "moe_grouped_swiglu_save", "moe_grouped_swiglu_dgrad",
+    "moe_grouped_swiglu_wgrad", "MOE_STATUS_WORKSPACE_BYTES",
 ]
+
+# Bytes of the status-only workspace of the grouped SwiGLU training calls.
+MOE_STATUS_WORKSPACE_BYTES = 256
 
 # Size of the library's built-in scratch array used by moe_route_noalloc.
 MOE_ROUTE_NOALLOC_SCRATCH_BYTES = 1 << 20
@@ -96,6 +100,9 @@ def load_library():
             "moe_grouped_swiglu_pack": ([P, P, I, I64, I64, P, P, P], I),
             "moe_grouped_swiglu_workspace_size": ([I64, I, I64, I64, PSZ], I),
             "moe_grouped_swiglu": ([P, P, P, P, I64, I, I64, I64, P, P, SZ, P], I),
+            "moe_grouped_swiglu_save": ([P, P, P, P, I64, I, I64, I64, P, P, P, P, SZ, P], I),
+            "moe_grouped_swiglu_dgrad": ([P, P, P, P, P, I64, I, I64, I64, P, P, P, SZ, P], I),
+            "moe_grouped_swiglu_wgrad": ([P, P, P, P, P, I64, I, I64, I64, P, P, P, SZ, P], I),
         }
         for name, (args, res) in sigs.items():
             fn = getattr(lib, name)
@@ -622,6 +629,105 @@ def moe_grouped_swiglu(x: torch.Tensor, w_up_packed: torch.Tensor, w_down_packed
         ws.numel(), _stream(stream)))
     out._moe_workspace = ws
     return out
+
+
+def moe_grouped_swiglu_save(x: torch.Tensor, w_up_packed: torch.Tensor,
+                            w_down_packed: torch.Tensor, offsets: torch.Tensor, out=None,
+                            hidden=None, gate_up=None, workspace=None, stream=None):
+    """Training forward: (y [N,H], hidden [N,I], gate_up [N,2I]), all bf16."""
+    _cuda(x, "x", torch.bfloat16, 2)
+    _cuda(w_up_packed, "w_up_packed", torch.bfloat16, 3)
+    _cuda(w_down_packed, "w_down_packed", torch.bfloat16, 3)
+    _cuda(offsets, "offsets", torch.int32, 1)
+    N, H = x.shape
+    E, I2, H2 = w_up_packed.shape
+    I = I2 // 2
+    if H2 != H or tuple(w_down_packed.shape) != (E, H, I) or offsets.numel() != E + 1:
+        raise ValueError("packed weights / offsets do not match x")
+    out = torch.empty_like(x) if out is None else out
+    hidden = x.new_empty((N, I)) if hidden is None else hidden
+    gate_up = x.new_empty((N, 2 * I)) if gate_up is None else gate_up
+    for t, name, shape in ((out, "y", (N, H)), (hidden, "hidden", (N, I)),
+                           (gate_up, "gate_up", (N, 2 * I))):
+        _cuda(t, name, torch.bfloat16, 2)
+        if tuple(t.shape) != shape:
+            raise ValueError(f"{name} must be {list(shape)}")
+    ws = _workspace(MOE_STATUS_WORKSPACE_BYTES, x, workspace)
+    _ok("moe_grouped_swiglu_save", load_library().moe_grouped_swiglu_save(
+        _p(x), _p(w_up_packed), _p(w_down_packed), _p(offsets), N, E, H, I, _p(out), _p(hidden),
+        _p(gate_up), _p(ws), ws.numel(), _stream(stream)))
+    out._moe_workspace = ws
+    return out, hidden, gate_up
+
+
+def moe_grouped_swiglu_dgrad(dy: torch.Tensor, w_up: torch.Tensor, w_down: torch.Tensor,
+                             offsets: torch.Tensor, gate_up: torch.Tensor, dgate_up=None,
+                             dx=None, workspace=None, stream=None):
+    """(dgate_up [N,2I], dx [N,H]) bf16; w_up [E,H,2I] and w_down [E,I,H] in
+    their original (unpacked) layouts."""
+    _cuda(dy, "dy", torch.bfloat16, 2)
+    _cuda(w_up, "w_up", torch.bfloat16, 3)
+    _cuda(w_down, "w_down", torch.bfloat16, 3)
+    _cuda(offsets, "offsets", torch.int32, 1)
+    _cuda(gate_up, "gate_up", torch.bfloat16, 2)
+    N, H = dy.shape
+    E, H2, I2 = w_up.shape
+    I = I2 // 2
+    if H2 != H or tuple(w_down.shape) != (E, I, H) or offsets.numel() != E + 1 or \
+            tuple(gate_up.shape) != (N, 2 * I):
+        raise ValueError("weights / offsets / gate_up do not match dy")
+    dgate_up = dy.new_empty((N, 2 * I)) if dgate_up is None else dgate_up
+    dx = dy.new_empty((N, H)) if dx is None else dx
+    _cuda(dgate_up, "dgate_up", torch.bfloat16, 2)
+    _cuda(dx, "dx", torch.bfloat16, 2)
+    if tuple(dgate_up.shape) != (N, 2 * I) or tuple(dx.shape) != (N, H):
+        raise ValueError("dgate_up must be [N,2I] and dx [N,H]")
+    ws = _workspace(MOE_STATUS_WORKSPACE_BYTES, dy, workspace)
+    _ok("moe_grouped_swiglu_dgrad", load_library().moe_grouped_swiglu_dgrad(
+        _p(dy), _p(w_up), _p(w_down), _p(offsets), _p(gate_up), N, E, H, I, _p(dgate_up), _p(dx),
+        _p(ws), ws.numel(), _stream(stream)))
+    dx._moe_workspace = ws
+    return dgate_up, dx
+
+
+def moe_grouped_swiglu_wgrad(x: torch.Tensor, hidden: torch.Tensor, dy: torch.Tensor,
+                             dgate_up: torch.Tensor, offsets: torch.Tensor, dw_up=None,
+                             dw_down=None, up: bool = True, down: bool = True, workspace=None,
+                             stream=None):
+    """(dw_up fp32 [E,H,2I] or None, dw_down fp32 [E,I,H] or None)."""
+    _cuda(x, "x", torch.bfloat16, 2)
+    _cuda(hidden, "hidden", torch.bfloat16, 2)
+    _cuda(dy, "dy", torch.bfloat16, 2)
+    _cuda(dgate_up, "dgate_up", torch.bfloat16, 2)
+    _cuda(offsets, "offsets", torch.int32, 1)
+    N, H = x.shape
+    I = hidden.shape[1]
+    E = offsets.numel() - 1
+    if tuple(hidden.shape) != (N, I) or tuple(dy.shape) != (N, H) or \
+            tuple(dgate_up.shape) != (N, 2 * I):
+        raise ValueError("x, hidden, dy and dgate_up shapes do not agree")
+    f32 = torch.float32
+    if up and dw_up is None:
+        dw_up = torch.empty((E, H, 2 * I), dtype=f32, device=x.device)
+    if down and dw_down is None:
+        dw_down = torch.empty((E, I, H), dtype=f32, device=x.device)
+    if not up:
+        dw_up = None
+    if not down:
+        dw_down = None
+    for t, name, shape in ((dw_up, "dw_up", (E, H, 2 * I)), (dw_down, "dw_down", (E, I, H))):
+        if t is not None:
+            _cuda(t, name, f32, 3)
+            if tuple(t.shape) != shape:
+                raise ValueError(f"{name} must be {list(shape)}")
+    ws = _workspace(MOE_STATUS_WORKSPACE_BYTES, x, workspace)
+    _ok("moe_grouped_swiglu_wgrad", load_library().moe_grouped_swiglu_wgrad(
+        _p(x), _p(hidden), _p(dy), _p(dgate_up), _p(offsets), N, E, H, I, _p(dw_up),
+        _p(dw_down), _p(ws), ws.numel(), _stream(stream)))
+    for t in (dw_up, dw_down):
+        if t is not None:
+            t._moe_workspace = ws
+    return dw_up, dw_down
 
 
 def moe_workspace_status(workspace: torch.Tensor, stream=None) -> int:

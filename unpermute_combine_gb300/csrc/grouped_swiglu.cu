@@ -130,18 +130,56 @@ __device__ __forceinline__ void tile_coords(int t, const int* s_tile_start, cons
     m = r % s_mt[e];
 }
 
+// Epilogues of the m-grouped GEMM.
+enum Epi : int {
+    kPlain = 0,       // bf16 store of the accumulator (GMM2, GMM1 backward)
+    kSwiglu = 1,      // [gate | up] tile -> silu(gate) * up (GMM1)
+    kSwigluSave = 2,  // kSwiglu, and also store gate and up as bf16 for the backward
+    kSwigluBwd = 3,   // dh tile -> [d_gate | d_up] at the stored gate / up (GMM2 backward)
+};
+
 struct GemmArgs {
     const int32_t* offsets;     // [E+1] row segments
     int E;
-    int K;                      // reduction length (H for GMM1, I for GMM2)
+    int K;                      // reduction length
     int n_tiles;                // BN-column tiles per expert
-    int64_t w_rows_per_expert;  // rows of the packed weight per expert (2I or H)
+    int64_t w_rows_per_expert;  // rows of the (K-major) weight per expert
     void* out;                  // bf16 [N_rows, out_cols]
-    int64_t out_cols;           // I (GMM1, after SwiGLU) or H (GMM2)
+    int64_t out_cols;           // columns of out
+    int64_t valid_cols;         // accumulator columns that exist (kPlain / kSwigluBwd)
+    int64_t I;                  // intermediate size (kSwigluSave / kSwigluBwd)
+    const uint16_t* gate_up;    // kSwigluBwd: stored [N_rows, 2I] bf16
+    uint16_t* aux_out;          // kSwigluSave: gate_up [N_rows, 2I]
     WsHeader* header;
 };
 
-template <bool SWIGLU>
+// 32 floats -> 4 x 16-byte bf16 stores
+__device__ __forceinline__ void store_bf16x32(uint16_t* dst, const float* a) {
+    uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+        const int i0 = v * 8;
+        d[v] = make_uint4(pack_bf16x2_rn(a[i0], a[i0 + 1]), pack_bf16x2_rn(a[i0 + 2], a[i0 + 3]),
+                          pack_bf16x2_rn(a[i0 + 4], a[i0 + 5]), pack_bf16x2_rn(a[i0 + 6], a[i0 + 7]));
+    }
+}
+
+// 32 bf16 (16-byte aligned) -> floats
+__device__ __forceinline__ void load_bf16x32(const uint16_t* src, float* a) {
+    const uint4* s = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+        const uint4 w = s[v];
+        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+            a[v * 8 + 2 * h] = __uint_as_float(ws[h] << 16);
+            a[v * 8 + 2 * h + 1] = __uint_as_float(ws[h] & 0xFFFF0000u);
+        }
+    }
+}
+
+template <int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                     const __grid_constant__ CUtensorMap map_b, GemmArgs args) {
@@ -276,49 +314,281 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
             const int64_t row = int64_t(s_row0[e]) + m * BM + q * 32 + lane;
             const bool row_ok = row < s_row0[e + 1];
             uint16_t* out = static_cast<uint16_t*>(args.out);
-            if (SWIGLU) {
+            if (EPI == kSwiglu || EPI == kSwigluSave) {
                 // columns [0,128) gate, [128,256) up, for hidden j0 = n*128
+                const int64_t j0 = int64_t(n) * (BN / 2);
 #pragma unroll 1
                 for (int c = 0; c < BN / 2; c += 32) {
-                    float g[32], u[32];
+                    float g[32], u[32], hv[32];
                     tmem_ld32(tmem_acc + lane_base + c, g);
                     tmem_ld32(tmem_acc + lane_base + BN / 2 + c, u);
                     if (row_ok) {
-                        uint4* dst = reinterpret_cast<uint4*>(out + row * args.out_cols +
-                                                              int64_t(n) * (BN / 2) + c);
 #pragma unroll
-                        for (int v = 0; v < 4; ++v) {
-                            uint32_t w[4];
-#pragma unroll
-                            for (int h = 0; h < 4; ++h) {
-                                const int i0 = v * 8 + 2 * h;
-                                const float h0 = __fdividef(g[i0], 1.0f + __expf(-g[i0])) * u[i0];
-                                const float h1 =
-                                    __fdividef(g[i0 + 1], 1.0f + __expf(-g[i0 + 1])) * u[i0 + 1];
-                                w[h] = pack_bf16x2_rn(h0, h1);
-                            }
-                            dst[v] = make_uint4(w[0], w[1], w[2], w[3]);
+                        for (int i = 0; i < 32; ++i)
+                            hv[i] = __fdividef(g[i], 1.0f + __expf(-g[i])) * u[i];
+                        store_bf16x32(out + row * args.out_cols + j0 + c, hv);
+                        if (EPI == kSwigluSave) {
+                            uint16_t* gu = args.aux_out + row * 2 * args.I;
+                            store_bf16x32(gu + j0 + c, g);
+                            store_bf16x32(gu + args.I + j0 + c, u);
                         }
+                    }
+                }
+            } else if (EPI == kSwigluBwd) {
+                // accumulator columns = hidden columns j = n*BN + c (< I):
+                // d_up = dh*silu(g), d_gate = dh*u*s*(1 + g*(1-s)), s = sigmoid(g)
+#pragma unroll 1
+                for (int c = 0; c < BN; c += 32) {
+                    const int64_t j = int64_t(n) * BN + c;
+                    if (j >= args.valid_cols) break;              // uniform over the warp
+                    float dh[32];
+                    tmem_ld32(tmem_acc + lane_base + c, dh);
+                    if (row_ok) {
+                        const uint16_t* gu = args.gate_up + row * 2 * args.I;
+                        float g[32], u[32], dg[32], du[32];
+                        load_bf16x32(gu + j, g);
+                        load_bf16x32(gu + args.I + j, u);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) {
+                            const float sg = __fdividef(1.0f, 1.0f + __expf(-g[i]));
+                            du[i] = dh[i] * (g[i] * sg);
+                            dg[i] = dh[i] * u[i] * (sg * (1.0f + g[i] * (1.0f - sg)));
+                        }
+                        uint16_t* o = out + row * 2 * args.I;
+                        store_bf16x32(o + j, dg);
+                        store_bf16x32(o + args.I + j, du);
                     }
                 }
             } else {
 #pragma unroll 1
                 for (int c = 0; c < BN; c += 32) {
+                    const int64_t j = int64_t(n) * BN + c;
+                    if (j >= args.valid_cols) break;              // uniform over the warp
                     float a[32];
                     tmem_ld32(tmem_acc + lane_base + c, a);
-                    if (row_ok) {
-                        uint4* dst = reinterpret_cast<uint4*>(out + row * args.out_cols +
-                                                              int64_t(n) * BN + c);
-#pragma unroll
-                        for (int v = 0; v < 4; ++v) {
-                            const int i0 = v * 8;
-                            dst[v] = make_uint4(pack_bf16x2_rn(a[i0], a[i0 + 1]),
-                                                pack_bf16x2_rn(a[i0 + 2], a[i0 + 3]),
-                                                pack_bf16x2_rn(a[i0 + 4], a[i0 + 5]),
-                                                pack_bf16x2_rn(a[i0 + 6], a[i0 + 7]));
-                        }
-                    }
+                    if (row_ok) store_bf16x32(out + row * args.out_cols + j, a);
                 }
+            }
+            tc_fence_before();
+            mbar_arrive(smem_addr(&tmem_empty_bar[buf]));
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (s_failed && threadIdx.x == 0) {
+        args.header->status = MOE_ERR_TIMEOUT;
+        args.header->detail = blockIdx.x;
+    }
+    if (warp == 2) {
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;"
+                     :: "r"(tmem_base), "r"(kTmemCols) : "memory");
+    }
+}
+
+// ------------------------------------------------------ k-grouped wgrad
+// dW[e] = P_e^T Q_e over the rows of expert e's segment: P [N_rows, M] and
+// Q [N_rows, Ncols] row-major, dW [E, M, Ncols] fp32.  Both operands are read
+// MN-major: a stage holds 64 token rows (the reduction) of a 128-column P
+// panel (two 64-column TMA boxes) and a 256-column Q panel (four boxes), each
+// box 64 rows x 128 bytes with the 128-byte swizzle -- the canonical MN-major
+// SW128 layout, 8-row K groups 1024 bytes apart (SBO) and 64-element MN
+// blocks one box (8 KB) apart (LBO).  The instruction descriptor marks A and B
+// as MN-major.  Rows past the segment's end in its last stage belong to the
+// next expert: the producer warp zeroes them in shared memory (whole 128-byte
+// rows, so the swizzle does not matter) and publishes the stage on a second
+// barrier.  An expert with no rows gets zeros.
+constexpr int kBoxBytes = 64 * 128;
+constexpr int kWA = BM / 64;                   // P boxes per stage
+constexpr int kWB = BN / 64;                   // Q boxes per stage
+static_assert((kWA + kWB) * kBoxBytes == kStageBytes, "wgrad stage = forward stage");
+
+__device__ __forceinline__ uint64_t smem_desc_mn128(uint32_t addr) {
+    uint64_t d = 0;
+    d |= uint64_t((addr >> 4) & 0x3FFFu);
+    d |= uint64_t(kBoxBytes >> 4) << 16;       // LBO: next 64-element MN block
+    d |= uint64_t(1024 >> 4) << 32;            // SBO: next 8-row K group
+    d |= uint64_t(1) << 46;
+    d |= uint64_t(2) << 61;
+    return d;
+}
+
+constexpr uint32_t kIdescMN = kIdesc | (1u << 15) | (1u << 16);   // A and B MN-major
+
+__device__ __forceinline__ void mma_bf16_mn(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
+                                            uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}"
+        :: "r"(tmem_d), "l"(adesc), "l"(bdesc), "r"(kIdescMN), "r"(accumulate) : "memory");
+}
+
+struct WgradArgs {
+    const int32_t* offsets;
+    int E;
+    int M, Ncols;               // dW[e] is [M, Ncols]
+    int m_tiles, n_tiles;       // M / BM, Ncols / BN
+    float* out;                 // [E, M, Ncols]
+    WsHeader* header;
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+grouped_wgrad_kernel(const __grid_constant__ CUtensorMap map_p,
+                     const __grid_constant__ CUtensorMap map_q, WgradArgs args) {
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t full_bar[kStages];
+    __shared__ __align__(8) uint64_t ready_bar[kStages];
+    __shared__ __align__(8) uint64_t empty_bar[kStages];
+    __shared__ __align__(8) uint64_t tmem_full_bar[2];
+    __shared__ __align__(8) uint64_t tmem_empty_bar[2];
+    __shared__ uint32_t s_tmem_base;
+    __shared__ int s_failed;
+
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~uintptr_t(1023));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 32) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(smem_addr(&full_bar[s]), 1);
+            mbar_init(smem_addr(&ready_bar[s]), 1);
+            mbar_init(smem_addr(&empty_bar[s]), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_addr(&tmem_full_bar[b]), 1);
+            mbar_init(smem_addr(&tmem_empty_bar[b]), 128);
+        }
+        mbar_fence_init();
+        s_failed = 0;
+    }
+    if (warp == 2) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                     :: "r"(smem_addr(&s_tmem_base)), "r"(kTmemCols) : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+
+    const int per_expert = args.m_tiles * args.n_tiles;
+    const int total_tiles = args.E * per_expert;
+    const uint32_t tmem_base = s_tmem_base;
+    auto coords = [&](int t, int& e, int& m, int& n) {
+        e = t / per_expert;
+        const int r = t - e * per_expert;
+        n = r / args.m_tiles;
+        m = r - n * args.m_tiles;
+    };
+
+    if (warp == 0) {
+        // ------------------------------------------ TMA producer + tail fix-up
+        uint32_t it = 0, ready_phase = 0;
+        bool failed = false;
+        for (int t = blockIdx.x; t < total_tiles && !failed; t += gridDim.x) {
+            int e, m, n;
+            coords(t, e, m, n);
+            const int r0 = args.offsets[e], r1 = args.offsets[e + 1];
+            const int ksteps = r1 > r0 ? (r1 - r0 + 63) / 64 : 0;
+            for (int ks = 0; ks < ksteps; ++ks, ++it) {
+                const int s = it % kStages;
+                const uint32_t ph = (it / kStages) & 1u;
+                bool ok = true;
+                if (lane == 0) ok = mbar_wait(smem_addr(&empty_bar[s]), ph ^ 1u);
+                if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) { failed = true; break; }
+                const uint32_t base = smem_addr(smem + s * kStageBytes);
+                const uint32_t fb = smem_addr(&full_bar[s]);
+                const int row = r0 + ks * 64;
+                if (lane == 0) {
+                    mbar_expect_tx(fb, kStageBytes);
+                    for (int b = 0; b < kWA; ++b)
+                        tma_load_2d(base + b * kBoxBytes, &map_p, m * BM + b * 64, row, fb);
+                    for (int b = 0; b < kWB; ++b)
+                        tma_load_2d(base + (kWA + b) * kBoxBytes, &map_q, n * BN + b * 64, row, fb);
+                }
+                const int valid = min(64, r1 - row);
+                if (valid < 64) {
+                    // wait for the stage, zero rows [valid, 64) of every box, publish
+                    if (lane == 0) ok = mbar_wait(fb, ph);
+                    if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) { failed = true; break; }
+                    const int chunks = (64 - valid) * 8;          // 16-byte chunks per box
+                    for (int b = 0; b < kWA + kWB; ++b) {
+                        uint8_t* box = smem + s * kStageBytes + b * kBoxBytes + valid * 128;
+                        for (int c = lane; c < chunks; c += 32)
+                            *reinterpret_cast<uint4*>(box + c * 16) = make_uint4(0, 0, 0, 0);
+                    }
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_addr(&ready_bar[s]));
+                    ready_phase ^= 1u << s;
+                }
+            }
+        }
+        if (failed && lane == 0) s_failed = 1;
+    } else if (warp == 1 && lane == 0) {
+        // ------------------------------------------------------ MMA issuer
+        uint32_t it = 0, tile_iter = 0, ready_phase = 0;
+        for (int t = blockIdx.x; t < total_tiles && !s_failed; t += gridDim.x, ++tile_iter) {
+            int e, m, n;
+            coords(t, e, m, n);
+            const int r0 = args.offsets[e], r1 = args.offsets[e + 1];
+            const int ksteps = r1 > r0 ? (r1 - r0 + 63) / 64 : 0;
+            const uint32_t buf = tile_iter & 1u, use = tile_iter >> 1;
+            if (!mbar_wait(smem_addr(&tmem_empty_bar[buf]), (use & 1u) ^ 1u)) { s_failed = 1; break; }
+            tc_fence_after();
+            const uint32_t tmem_d = tmem_base + buf * BN;
+            for (int ks = 0; ks < ksteps; ++ks, ++it) {
+                const int s = it % kStages;
+                const uint32_t ph = (it / kStages) & 1u;
+                if (!mbar_wait(smem_addr(&full_bar[s]), ph)) { s_failed = 1; break; }
+                if (r1 - (r0 + ks * 64) < 64) {
+                    if (!mbar_wait(smem_addr(&ready_bar[s]), (ready_phase >> s) & 1u)) {
+                        s_failed = 1;
+                        break;
+                    }
+                    ready_phase ^= 1u << s;
+                }
+                tc_fence_after();
+                const uint32_t a_base = smem_addr(smem + s * kStageBytes);
+                const uint32_t b_base = a_base + kWA * kBoxBytes;
+#pragma unroll
+                for (int kk = 0; kk < 64 / 16; ++kk)      // 16 token rows = 2 K groups
+                    mma_bf16_mn(tmem_d, smem_desc_mn128(a_base + kk * 2048),
+                                smem_desc_mn128(b_base + kk * 2048), (ks | kk) != 0);
+                mma_commit(smem_addr(&empty_bar[s]));
+            }
+            if (s_failed) break;
+            mma_commit(smem_addr(&tmem_full_bar[buf]));
+        }
+    } else if (warp >= 4) {
+        // ------------------------------------------------------ epilogue
+        const int q = warp - 4;
+        const uint32_t lane_base = uint32_t(q * 32) << 16;
+        uint32_t tile_iter = 0;
+        for (int t = blockIdx.x; t < total_tiles; t += gridDim.x, ++tile_iter) {
+            const uint32_t buf = tile_iter & 1u, use = tile_iter >> 1;
+            if (s_failed || !mbar_wait(smem_addr(&tmem_full_bar[buf]), use & 1u)) {
+                s_failed = 1;
+                break;
+            }
+            tc_fence_after();
+            int e, m, n;
+            coords(t, e, m, n);
+            const bool empty = args.offsets[e + 1] <= args.offsets[e];
+            const int64_t row = int64_t(m) * BM + q * 32 + lane;
+            float4* dst = reinterpret_cast<float4*>(
+                args.out + (int64_t(e) * args.M + row) * args.Ncols + int64_t(n) * BN);
+            const uint32_t tmem_acc = tmem_base + buf * BN;
+#pragma unroll 1
+            for (int c = 0; c < BN; c += 32) {
+                float a[32];
+                if (!empty) {
+                    tmem_ld32(tmem_acc + lane_base + c, a);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) a[i] = 0.0f;
+                }
+#pragma unroll
+                for (int v = 0; v < 8; ++v)
+                    dst[c / 4 + v] = make_float4(a[4 * v], a[4 * v + 1], a[4 * v + 2], a[4 * v + 3]);
             }
             tc_fence_before();
             mbar_arrive(smem_addr(&tmem_empty_bar[buf]));
@@ -409,6 +679,35 @@ bool make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, in
            CUDA_SUCCESS;
 }
 
+// Opt every tensor-core kernel into kSmemBytes of dynamic shared memory, once
+// per device.
+bool smem_attrs_set() {
+    static bool done[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+    if (done[dev]) return true;
+    const void* kernels[] = {(const void*)grouped_gemm_kernel<kPlain>,
+                             (const void*)grouped_gemm_kernel<kSwiglu>,
+                             (const void*)grouped_gemm_kernel<kSwigluSave>,
+                             (const void*)grouped_gemm_kernel<kSwigluBwd>,
+                             (const void*)grouped_wgrad_kernel};
+    for (const void* k : kernels)
+        if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
+            cudaSuccess)
+            return false;
+    done[dev] = true;
+    return true;
+}
+
+// The status header a call resets and its kernels report into.
+moe_status_t status_workspace(void* workspace, size_t workspace_bytes, WsHeader** header) {
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & (kWsAlign - 1)) ||
+        workspace_bytes < kWsAlign)
+        return MOE_ERR_WORKSPACE;
+    *header = static_cast<WsHeader*>(workspace);
+    return MOE_OK;
+}
+
 moe_status_t check_shapes(int64_t N, int E, int64_t H, int64_t I) {
     if (N < 0 || E < 1 || H < 1 || I < 1) return MOE_ERR_INVALID_ARG;
     if (E > kMaxExperts || H % BN != 0 || I % 128 != 0 || H % BK != 0 || I % BK != 0)
@@ -480,22 +779,128 @@ extern "C" moe_status_t moe_grouped_swiglu(const void* x, const void* w_up_packe
         !make_map(&m_h, hidden, N, I, BM) || !make_map(&m_down, w_down_packed, int64_t(E) * H, I, BN))
         return MOE_ERR_CUDA;
 
-    static bool attr_set[64] = {};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-        if (cudaFuncSetAttribute(grouped_gemm_kernel<true>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess ||
-            cudaFuncSetAttribute(grouped_gemm_kernel<false>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess)
-            return MOE_ERR_CUDA;
-        attr_set[dev] = true;
-    }
+    if (!smem_attrs_set()) return MOE_ERR_CUDA;
     const int grid = sm_count();
-    GemmArgs a1{offsets, E, int(H), int(I / 128), 2 * I, hidden, I, header};
-    grouped_gemm_kernel<true><<<grid, kThreads, kSmemBytes, s>>>(m_x, m_up, a1);
+    GemmArgs a1{offsets, E, int(H), int(I / 128), 2 * I, hidden, I, I, I, nullptr, nullptr, header};
+    grouped_gemm_kernel<kSwiglu><<<grid, kThreads, kSmemBytes, s>>>(m_x, m_up, a1);
     if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
-    GemmArgs a2{offsets, E, int(I), int(H / BN), H, y, H, header};
-    grouped_gemm_kernel<false><<<grid, kThreads, kSmemBytes, s>>>(m_h, m_down, a2);
+    GemmArgs a2{offsets, E, int(I), int(H / BN), H, y, H, H, I, nullptr, nullptr, header};
+    grouped_gemm_kernel<kPlain><<<grid, kThreads, kSmemBytes, s>>>(m_h, m_down, a2);
     return launch_status();
+}
+
+extern "C" moe_status_t moe_grouped_swiglu_save(const void* x, const void* w_up_packed,
+                                                const void* w_down_packed, const int32_t* offsets,
+                                                int64_t N, int E, int64_t H, int64_t I, void* y,
+                                                void* hidden, void* gate_up, void* workspace,
+                                                size_t workspace_bytes, void* stream) {
+    moe_status_t st = check_shapes(N, E, H, I);
+    if (st != MOE_OK) return st;
+    if (!offsets || (N > 0 && (!x || !w_up_packed || !w_down_packed || !y || !hidden || !gate_up)))
+        return MOE_ERR_INVALID_ARG;
+    WsHeader* header = nullptr;
+    if ((st = status_workspace(workspace, workspace_bytes, &header)) != MOE_OK) return st;
+    if (!aligned16(x) || !aligned16(w_up_packed) || !aligned16(w_down_packed) || !aligned16(y) ||
+        !aligned16(hidden) || !aligned16(gate_up))
+        return MOE_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    reset_status_kernel<<<1, 1, 0, s>>>(header);
+    if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
+    if (N == 0) return MOE_OK;
+    CUtensorMap m_x, m_up, m_h, m_down;
+    if (!make_map(&m_x, x, N, H, BM) || !make_map(&m_up, w_up_packed, int64_t(E) * 2 * I, H, BN) ||
+        !make_map(&m_h, hidden, N, I, BM) || !make_map(&m_down, w_down_packed, int64_t(E) * H, I, BN))
+        return MOE_ERR_CUDA;
+    if (!smem_attrs_set()) return MOE_ERR_CUDA;
+    const int grid = sm_count();
+    GemmArgs a1{offsets, E, int(H), int(I / 128), 2 * I, hidden, I, I, I, nullptr,
+                static_cast<uint16_t*>(gate_up), header};
+    grouped_gemm_kernel<kSwigluSave><<<grid, kThreads, kSmemBytes, s>>>(m_x, m_up, a1);
+    if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
+    GemmArgs a2{offsets, E, int(I), int(H / BN), H, y, H, H, I, nullptr, nullptr, header};
+    grouped_gemm_kernel<kPlain><<<grid, kThreads, kSmemBytes, s>>>(m_h, m_down, a2);
+    return launch_status();
+}
+
+extern "C" moe_status_t moe_grouped_swiglu_dgrad(const void* dy, const void* w_up,
+                                                 const void* w_down, const int32_t* offsets,
+                                                 const void* gate_up, int64_t N, int E, int64_t H,
+                                                 int64_t I, void* dgate_up, void* dx,
+                                                 void* workspace, size_t workspace_bytes,
+                                                 void* stream) {
+    moe_status_t st = check_shapes(N, E, H, I);
+    if (st != MOE_OK) return st;
+    if (!offsets || (N > 0 && (!dy || !w_up || !w_down || !gate_up || !dgate_up || !dx)))
+        return MOE_ERR_INVALID_ARG;
+    WsHeader* header = nullptr;
+    if ((st = status_workspace(workspace, workspace_bytes, &header)) != MOE_OK) return st;
+    if (!aligned16(dy) || !aligned16(w_up) || !aligned16(w_down) || !aligned16(gate_up) ||
+        !aligned16(dgate_up) || !aligned16(dx))
+        return MOE_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    reset_status_kernel<<<1, 1, 0, s>>>(header);
+    if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
+    if (N == 0) return MOE_OK;
+    CUtensorMap m_dy, m_wd, m_dgu, m_wu;
+    if (!make_map(&m_dy, dy, N, H, BM) || !make_map(&m_wd, w_down, int64_t(E) * I, H, BN) ||
+        !make_map(&m_dgu, dgate_up, N, 2 * I, BM) || !make_map(&m_wu, w_up, int64_t(E) * H, 2 * I, BN))
+        return MOE_ERR_CUDA;
+    if (!smem_attrs_set()) return MOE_ERR_CUDA;
+    const int grid = sm_count();
+    // GMM2 backward + SwiGLU backward: dh = dy @ w_down[e]^T (w_down [E,I,H] is
+    // already K-major for this product), [d_gate | d_up] into dgate_up
+    GemmArgs d2{offsets, E, int(H), int((I + BN - 1) / BN), I, dgate_up, 2 * I, I, I,
+                static_cast<const uint16_t*>(gate_up), nullptr, header};
+    grouped_gemm_kernel<kSwigluBwd><<<grid, kThreads, kSmemBytes, s>>>(m_dy, m_wd, d2);
+    if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
+    // GMM1 backward: dx = dgate_up @ w_up[e]^T (w_up [E,H,2I] is K-major here)
+    GemmArgs d1{offsets, E, int(2 * I), int(H / BN), H, dx, H, H, I, nullptr, nullptr, header};
+    grouped_gemm_kernel<kPlain><<<grid, kThreads, kSmemBytes, s>>>(m_dgu, m_wu, d1);
+    return launch_status();
+}
+
+extern "C" moe_status_t moe_grouped_swiglu_wgrad(const void* x, const void* hidden,
+                                                 const void* dy, const void* dgate_up,
+                                                 const int32_t* offsets, int64_t N, int E,
+                                                 int64_t H, int64_t I, float* dw_up,
+                                                 float* dw_down, void* workspace,
+                                                 size_t workspace_bytes, void* stream) {
+    moe_status_t st = check_shapes(N, E, H, I);
+    if (st != MOE_OK) return st;
+    if (!offsets) return MOE_ERR_INVALID_ARG;
+    if (dw_up && N > 0 && (!x || !dgate_up)) return MOE_ERR_INVALID_ARG;
+    if (dw_down && N > 0 && (!hidden || !dy)) return MOE_ERR_INVALID_ARG;
+    WsHeader* header = nullptr;
+    if ((st = status_workspace(workspace, workspace_bytes, &header)) != MOE_OK) return st;
+    if ((dw_up && (!aligned16(dw_up) || (N > 0 && (!aligned16(x) || !aligned16(dgate_up))))) ||
+        (dw_down && (!aligned16(dw_down) || (N > 0 && (!aligned16(hidden) || !aligned16(dy))))))
+        return MOE_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    reset_status_kernel<<<1, 1, 0, s>>>(header);
+    if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
+    if (N == 0) {                        // no rows: every expert's gradient is zero
+        if (dw_up && cudaMemsetAsync(dw_up, 0, size_t(E) * H * 2 * I * sizeof(float), s) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        if (dw_down && cudaMemsetAsync(dw_down, 0, size_t(E) * I * H * sizeof(float), s) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        return MOE_OK;
+    }
+    if (!smem_attrs_set()) return MOE_ERR_CUDA;
+    const int grid = sm_count();
+    if (dw_down) {          // dW_down[e] [I,H] = hidden_e^T dy_e
+        CUtensorMap m_p, m_q;
+        if (!make_map(&m_p, hidden, N, I, 64) || !make_map(&m_q, dy, N, H, 64)) return MOE_ERR_CUDA;
+        WgradArgs a{offsets, E, int(I), int(H), int(I / BM), int(H / BN), dw_down, header};
+        grouped_wgrad_kernel<<<grid, kThreads, kSmemBytes, s>>>(m_p, m_q, a);
+        if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
+    }
+    if (dw_up) {            // dW_up[e] [H,2I] = x_e^T dgate_up_e
+        CUtensorMap m_p, m_q;
+        if (!make_map(&m_p, x, N, H, 64) || !make_map(&m_q, dgate_up, N, 2 * I, 64))
+            return MOE_ERR_CUDA;
+        WgradArgs a{offsets, E, int(H), int(2 * I), int(H / BM), int(2 * I / BN), dw_up, header};
+        grouped_wgrad_kernel<<<grid, kThreads, kSmemBytes, s>>>(m_p, m_q, a);
+        if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
+    }
+    return MOE_OK;
 }
