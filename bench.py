@@ -110,6 +110,10 @@ KERNEL_SOURCES = {
     "combine_backward": ("unpermute_combine_gb300/csrc/combine.cu",
                          "unpermute_combine_gb300/csrc/common.cuh"),
     "quantize_fp8": ("unpermute_combine_gb300/csrc/fp8.cu", "unpermute_combine_gb300/csrc/common.cuh"),
+    "swiglu_dgrad": ("unpermute_combine_gb300/csrc/grouped_swiglu.cu",
+                     "unpermute_combine_gb300/csrc/pipeline.cuh"),
+    "swiglu_wgrad": ("unpermute_combine_gb300/csrc/grouped_swiglu.cu",
+                     "unpermute_combine_gb300/csrc/pipeline.cuh"),
     "route_backward": ("unpermute_combine_gb300/csrc/route_bwd.cu",
                        "unpermute_combine_gb300/csrc/common.cuh"),
     "dequantize_fp8": ("unpermute_combine_gb300/csrc/fp8.cu",
@@ -204,6 +208,18 @@ def layer_flops_bytes(N, H, E, I):
     return flops, byts
 
 
+def train_flops_bytes(N, T, H, E, I, k):
+    """The backward GEMMs of the grouped SwiGLU, each 6*N*H*I flops:
+    dgrad  = dy @ w_down^T (2NHI) + dgate_up @ w_up^T (4NHI); bytes: dy,
+             w_down, gate_up read, dgate_up written and read, w_up, dx;
+    wgrad  = hidden^T dy (2NHI) + x^T dgate_up (4NHI); bytes: hidden, dy, x,
+             dgate_up read, both fp32 weight gradients written."""
+    flops = 6 * N * H * I
+    dgrad = (N * H * 2 + E * I * H * 2 + N * 2 * I * 2 * 3 + E * H * 2 * I * 2 + N * H * 2)
+    wgrad = (N * I * 2 + N * H * 2 * 2 + N * 2 * I * 2 + E * (I * H + H * 2 * I) * 4)
+    return flops, dgrad, wgrad
+
+
 def parse_layout(spec):
     """'cf=1.25,pad' or 'align=128' -> dict (empty: the plain layout)."""
     out = {}
@@ -244,7 +260,8 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     layer = args.workload == "layer"
-    d = wl.make(args.workload, with_grad=not layer, with_weights=layer, T=args.tokens)
+    train = layer and bool(args.train)
+    d = wl.make(args.workload, with_grad=not layer or train, with_weights=layer, T=args.tokens)
     W = d["workload"]
     T, H, E, k, b = d["x"].shape[0], W.H, W.E, W.k, 2
     N = T * k
@@ -252,9 +269,10 @@ def run_ours(args, rank, world, local_rank):
     bf = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)
     h_logits = torch.from_numpy(d["logits"]).pin_memory()
     h_x = bf(d["x"]).pin_memory()
-    h_g = None if layer else bf(d["grad_out"]).pin_memory()
+    has_grad = not layer or train
+    h_g = bf(d["grad_out"]).pin_memory() if has_grad else None
     logits, x = h_logits.to(dev), h_x.to(dev)
-    g = None if layer else h_g.to(dev)
+    g = h_g.to(dev) if has_grad else None
 
     groups = tuple(int(v) for v in args.route_groups.split(":")) if args.route_groups else None
     lay = parse_layout(args.layout)
@@ -282,11 +300,29 @@ def run_ours(args, rank, world, local_rank):
             y = torch.empty((rows, H), dtype=torch.bfloat16, device=dev)
             gs_ws = torch.empty(moe.moe_grouped_swiglu_workspace_size(rows, E, H, W.I),
                                 dtype=torch.uint8, device=dev)
+            if train:
+                I = W.I
+                w_up_d, w_down_d = bf(d["w_up"]).to(dev), bf(d["w_down"]).to(dev)
+                hid = torch.empty((rows, I), dtype=torch.bfloat16, device=dev)
+                gu = torch.empty((rows, 2 * I), dtype=torch.bfloat16, device=dev)
+                gy = torch.empty((rows, H), dtype=torch.bfloat16, device=dev)
+                gp = torch.empty((T, k), dtype=torch.float32, device=dev)
+                dgu = torch.empty((rows, 2 * I), dtype=torch.bfloat16, device=dev)
+                dxp = torch.empty((rows, H), dtype=torch.bfloat16, device=dev)
+                dwu = torch.empty((E, H, 2 * I), dtype=torch.float32, device=dev)
+                dwd = torch.empty((E, I, H), dtype=torch.float32, device=dev)
+                gx = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+                gl = torch.empty((T, E), dtype=torch.float32, device=dev)
+                ws_d = torch.empty(moe.MOE_STATUS_WORKSPACE_BYTES, dtype=torch.uint8, device=dev)
+                ws_w = torch.empty(moe.MOE_STATUS_WORKSPACE_BYTES, dtype=torch.uint8, device=dev)
         else:
             gy = torch.empty((rows, H), dtype=torch.bfloat16, device=dev)
             gp = torch.empty((T, k), dtype=torch.float32, device=dev)
     names = (["route", "permute", "grouped_swiglu", "combine"] if layer else
              ["route", "permute", "combine", "combine_backward"])
+    if train:
+        names += ["combine_backward", "swiglu_dgrad", "swiglu_wgrad", "permute_backward",
+                  "route_backward"]
     if fp8:
         names[1:2] = ["quantize_fp8", "permute", "dequantize_fp8"]
     router_bwd = bool(args.router_bwd) and not layer
@@ -326,7 +362,26 @@ def run_ours(args, rank, world, local_rank):
         if lay:
             moe.moe_fill_pad_rows(xp, rr.offsets, rr.counts, stream=stream)
         mark()
-        if layer:
+        if train:
+            # forward keeping the activations, then the whole layer backward
+            moe.moe_grouped_swiglu_save(xp, up_p, down_p, rr.offsets, out=y, hidden=hid,
+                                        gate_up=gu, workspace=gs_ws, stream=stream)
+            mark()
+            moe.moe_combine(y, rr.slot_pos, r.topk_w, out=out, stream=stream)
+            mark()
+            moe.moe_combine_backward(gg, y, rr.slot_pos, r.topk_w, grad_expert_out=gy,
+                                     grad_probs=gp, stream=stream)
+            mark()
+            moe.moe_grouped_swiglu_dgrad(gy, w_up_d, w_down_d, rr.offsets, gu, dgate_up=dgu,
+                                         dx=dxp, workspace=ws_d, stream=stream)
+            mark()
+            moe.moe_grouped_swiglu_wgrad(xp, hid, gy, dgu, rr.offsets, dw_up=dwu, dw_down=dwd,
+                                         workspace=ws_w, stream=stream)
+            mark()
+            moe.moe_combine(dxp, rr.slot_pos, None, out=gx, stream=stream)   # permute backward
+            mark()
+            moe.moe_route_backward(r.topk_idx, r.topk_w, gp, E, out=gl, stream=stream)
+        elif layer:
             moe.moe_grouped_swiglu(xp, up_p, down_p, rr.offsets, out=y, workspace=gs_ws,
                                    stream=stream)
             mark()
@@ -371,25 +426,28 @@ def run_ours(args, rank, world, local_rank):
     max_elapsed = reduce_max(elapsed, dev)
     if layer:
         assert moe.moe_workspace_status(gs_ws, stream) == 0, "grouped SwiGLU pipeline timed out"
+    if train:
+        assert moe.moe_workspace_status(ws_d, stream) == 0, "SwiGLU dgrad pipeline timed out"
+        assert moe.moe_workspace_status(ws_w, stream) == 0, "SwiGLU wgrad pipeline timed out"
     if lay:
         assert moe.moe_workspace_status(rl.workspace, stream) == 0, "layout ran out of rows"
 
     # -------- end to end through the public API from pinned host buffers
     h_out = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
-    h_gp = None if layer else torch.empty((T, k), dtype=torch.float32).pin_memory()
-    h2d = h_logits.numel() * 4 + h_x.numel() * 2 + (0 if layer else h_g.numel() * 2)
-    d2h = h_out.numel() * 2 + (0 if layer else h_gp.numel() * 4)
+    h_gp = torch.empty((T, k), dtype=torch.float32).pin_memory() if has_grad else None
+    h2d = h_logits.numel() * 4 + h_x.numel() * 2 + (h_g.numel() * 2 if has_grad else 0)
+    d2h = h_out.numel() * 2 + (h_gp.numel() * 4 if has_grad else 0)
     e2e_steps = 0 if args.no_e2e else max(1, min(args.steps, 20))
 
     def e2e_step():
         with torch.cuda.stream(stream):
             lg = h_logits.to(dev, non_blocking=True)
             xx = h_x.to(dev, non_blocking=True)
-            gg = None if layer else h_g.to(dev, non_blocking=True)
+            gg = h_g.to(dev, non_blocking=True) if has_grad else None
         step(lg, xx, gg)
         with torch.cuda.stream(stream):
             h_out.copy_(out, non_blocking=True)
-            if not layer:
+            if has_grad:
                 h_gp.copy_(gp, non_blocking=True)
 
     e2e_elapsed = float("nan")
@@ -415,6 +473,11 @@ def run_ours(args, rank, world, local_rank):
     if layer:
         fl, by = layer_flops_bytes(N, H, E, W.I)
         alg["grouped_swiglu"] = by
+    if train:
+        _, bd, bw = train_flops_bytes(N, T, H, E, W.I, k)
+        alg["swiglu_dgrad"], alg["swiglu_wgrad"] = bd, bw
+        alg["permute_backward"] = alg["combine"] - 4 * N          # unweighted combine
+        alg["route_backward"] = T * E * 4 + T * k * 12
     if fp8:
         alg.update(fp8_bytes(T, H, k))
     if router_bwd:
@@ -434,17 +497,28 @@ def run_ours(args, rank, world, local_rank):
                                                   "combine"))
     if layer:
         t_sus, t_burst, t_kind = measured_tensor_peak()
-        tf = fl / per["grouped_swiglu"] / 1e12
-        kern["grouped_swiglu"].update({"TFLOP_s": round(tf, 1), "flops": fl,
-                                       "frac_tensor_sustained": round(tf / t_sus, 4),
-                                       "frac_tensor_burst": round(tf / t_burst, 4)})
-        roof = {"bound": "tensor", "kernel": "grouped_swiglu", "achieved": round(tf, 1),
+        gemms = ["grouped_swiglu"] + (["swiglu_dgrad", "swiglu_wgrad"] if train else [])
+        for gname in gemms:                       # each is 6*N*H*I flops
+            tf_g = fl / per[gname] / 1e12
+            kern[gname].update({"TFLOP_s": round(tf_g, 1), "flops": fl,
+                                "frac_tensor_sustained": round(tf_g / t_sus, 4),
+                                "frac_tensor_burst": round(tf_g / t_burst, 4)})
+        top = max(gemms, key=lambda n_: per[n_])
+        tf = fl / per[top] / 1e12
+        roof = {"bound": "tensor", "kernel": top, "achieved": round(tf, 1),
                 "peak": t_sus, "unit": "TFLOP/s", "frac": round(tf / t_sus, 4),
                 "peak_source": f"{t_kind} bf16_tflops_sustained (burst {t_burst})",
-                "hbm_frac": kern["grouped_swiglu"]["frac"], "traffic": None}
+                "hbm_frac": kern[top]["frac"], "traffic": None}
         workload = (f"layer: T={T} H={H} E={E} k={k} I={W.I} bf16, full MoE layer forward "
                     "(route, permute, grouped SwiGLU on tcgen05, combine)")
         step_desc = "moe_route + moe_permute + moe_grouped_swiglu + moe_combine"
+        if train:
+            workload = (f"layer: T={T} H={H} E={E} k={k} I={W.I} bf16, MoE layer training step "
+                        "(forward keeping activations, then the whole backward)")
+            step_desc = ("moe_route + moe_permute + moe_grouped_swiglu_save + moe_combine + "
+                         "moe_combine_backward + moe_grouped_swiglu_dgrad + "
+                         "moe_grouped_swiglu_wgrad + moe_combine(unweighted: permute backward) + "
+                         "moe_route_backward")
     else:
         ach = alg[dominant] / per[dominant] / 1e9
         roof = {"bound": "hbm", "kernel": dominant, "achieved": round(ach, 1),
@@ -468,6 +542,8 @@ def run_ours(args, rank, world, local_rank):
                                       f"{lay.get('align', 1)}, rows={rows}) + moe_permute + "
                                       "moe_fill_pad_rows", 1)
     launches = ROUTE_LAUNCHES + (1 + 3 + 1 if layer else 3)   # grouped SwiGLU: reset + 2 GEMMs
+    if train:
+        launches += 1 + 3 + 3 + 1 + 1     # combine bwd, dgrad, wgrad (reset + 2 each), permute bwd, route bwd
     if fp8:
         launches += 2                     # quantize, dequantize
     if router_bwd:
@@ -561,6 +637,9 @@ def main(argv=None):
     ap.add_argument("--tokens", type=int, default=None,
                     help="use only the first TOKENS tokens (small cases for profiling)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg")
+    ap.add_argument("--train", action="store_true",
+                    help="layer workload: time a training step (forward keeping activations, "
+                         "combine backward, SwiGLU dgrad and wgrad, permute and router backward)")
     ap.add_argument("--router-bwd", action="store_true",
                     help="append the router k-softmax backward (grad_probs -> grad_logits) "
                          "to the training step")

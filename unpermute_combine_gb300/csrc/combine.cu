@@ -118,20 +118,28 @@ __device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
 // 2*(2k*2^-24)^2 * sum|w*y| (Ogita-Rump-Oishi Sum2 bound), plus the double
 // sum's own k*2^-53 * sum|w*y|; if the whole interval lies strictly between
 // the two midpoints of one bf16 value, that value is the rounding of the
-// double slot-order sum.  Returns false when it cannot decide.
+// double slot-order sum.  An interval cannot decide a sum that sits exactly
+// on a midpoint, which unweighted sums of bf16 rows often do, so the chain
+// also records whether every product and every partial sum was exact: then
+// each prefix of the slot-order sum is a float, the double chain computes the
+// same prefixes exactly, and the float sum rounds directly.  Returns false
+// when it cannot decide.
 __device__ __forceinline__ bool dd_sum_bf16(const float* w, const float* y, const bool* valid,
                                             int n, float dd_bound, uint16_t* out) {
     float hi = 0.0f, lo = 0.0f, a = 0.0f;
+    bool exact = true;
     for (int j = 0; j < n; ++j) {
         if (!valid[j]) continue;
         const float p = __fmul_rn(w[j], y[j]);
         const float ep = __fmaf_rn(w[j], y[j], -p);          // w*y == p + ep exactly
         float sum, es;
         two_sum(hi, p, sum, es);
+        exact = exact && ep == 0.0f && es == 0.0f;
         hi = sum;
         lo = __fadd_rn(lo, __fadd_rn(es, ep));
         a = __fmaf_rn(fabsf(w[j]), fabsf(y[j]), a);
     }
+    if (exact) { *out = f32_to_bf16_rn(hi); return true; }   // hi is the exact sum
     const float s = __fadd_rn(hi, lo);
     const float b = __fmaf_ru(a, dd_bound, 0x1p-126f);
     // r = bf16(s); its rounding midpoints m_lo < r < m_hi are exact floats

@@ -397,8 +397,18 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
 // as MN-major.  Rows past the segment's end in its last stage belong to the
 // next expert: the producer warp zeroes them in shared memory (whole 128-byte
 // rows, so the swizzle does not matter) and publishes the stage on a second
-// barrier.  An expert with no rows gets zeros.
+// barrier.  The fix-up is deferred: the producer keeps issuing later stages
+// and zeroes the pending partial stage only when it would otherwise block (a
+// ring slot not yet free, the next partial stage, the end), by which time
+// the stage has landed.  An expert with no rows gets zeros.  The epilogue
+// writes each 32x32 fp32 block of its quadrant into a 128-byte-swizzled
+// staging tile (two per warp) and hands it to the TMA store engine, so the
+// warp moves on to the next block while full 128-byte rows stream out.
 constexpr int kBoxBytes = 64 * 128;
+constexpr int kEpiTileBytes = 32 * 32 * 4;            // one 32x32 fp32 block
+constexpr int kWgradSmemBytes = kSmemBytes + 4 * 2 * kEpiTileBytes;
+static_assert(kWgradSmemBytes <= 227 * 1024 - 256, "wgrad shared memory");
+
 constexpr int kWA = BM / 64;                   // P boxes per stage
 constexpr int kWB = BN / 64;                   // Q boxes per stage
 static_assert((kWA + kWB) * kBoxBytes == kStageBytes, "wgrad stage = forward stage");
@@ -432,9 +442,15 @@ struct WgradArgs {
     WsHeader* header;
 };
 
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int c0, int c1, uint32_t src) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];"
+                 :: "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(src) : "memory");
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
 grouped_wgrad_kernel(const __grid_constant__ CUtensorMap map_p,
-                     const __grid_constant__ CUtensorMap map_q, WgradArgs args) {
+                     const __grid_constant__ CUtensorMap map_q,
+                     const __grid_constant__ CUtensorMap map_out, WgradArgs args) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t full_bar[kStages];
     __shared__ __align__(8) uint64_t ready_bar[kStages];
@@ -481,8 +497,28 @@ grouped_wgrad_kernel(const __grid_constant__ CUtensorMap map_p,
 
     if (warp == 0) {
         // ------------------------------------------ TMA producer + tail fix-up
-        uint32_t it = 0, ready_phase = 0;
+        uint32_t it = 0;
         bool failed = false;
+        bool pend = false;                 // a partial stage waiting for its fix-up
+        int pend_s = 0, pend_valid = 64;
+        uint32_t pend_ph = 0;
+        auto service = [&]() -> bool {
+            if (!pend) return true;
+            bool ok = true;
+            if (lane == 0) ok = mbar_wait(smem_addr(&full_bar[pend_s]), pend_ph);
+            if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) return false;
+            const int chunks = (64 - pend_valid) * 8;               // 16-byte chunks per box
+            for (int b = 0; b < kWA + kWB; ++b) {
+                uint8_t* box = smem + pend_s * kStageBytes + b * kBoxBytes + pend_valid * 128;
+                for (int c = lane; c < chunks; c += 32)
+                    *reinterpret_cast<uint4*>(box + c * 16) = make_uint4(0, 0, 0, 0);
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_addr(&ready_bar[pend_s]));
+            pend = false;
+            return true;
+        };
         for (int t = blockIdx.x; t < total_tiles && !failed; t += gridDim.x) {
             int e, m, n;
             coords(t, e, m, n);
@@ -492,6 +528,8 @@ grouped_wgrad_kernel(const __grid_constant__ CUtensorMap map_p,
                 const int s = it % kStages;
                 const uint32_t ph = (it / kStages) & 1u;
                 bool ok = true;
+                if (lane == 0) ok = mbar_test(smem_addr(&empty_bar[s]), ph ^ 1u);
+                if (!__shfl_sync(0xFFFFFFFFu, ok, 0) && !service()) { failed = true; break; }
                 if (lane == 0) ok = mbar_wait(smem_addr(&empty_bar[s]), ph ^ 1u);
                 if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) { failed = true; break; }
                 const uint32_t base = smem_addr(smem + s * kStageBytes);
@@ -506,22 +544,15 @@ grouped_wgrad_kernel(const __grid_constant__ CUtensorMap map_p,
                 }
                 const int valid = min(64, r1 - row);
                 if (valid < 64) {
-                    // wait for the stage, zero rows [valid, 64) of every box, publish
-                    if (lane == 0) ok = mbar_wait(fb, ph);
-                    if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) { failed = true; break; }
-                    const int chunks = (64 - valid) * 8;          // 16-byte chunks per box
-                    for (int b = 0; b < kWA + kWB; ++b) {
-                        uint8_t* box = smem + s * kStageBytes + b * kBoxBytes + valid * 128;
-                        for (int c = lane; c < chunks; c += 32)
-                            *reinterpret_cast<uint4*>(box + c * 16) = make_uint4(0, 0, 0, 0);
-                    }
-                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(smem_addr(&ready_bar[s]));
-                    ready_phase ^= 1u << s;
+                    if (!service()) { failed = true; break; }      // at most one pending
+                    pend = true;
+                    pend_s = s;
+                    pend_ph = ph;
+                    pend_valid = valid;
                 }
             }
         }
+        if (!failed && !service()) failed = true;
         if (failed && lane == 0) s_failed = 1;
     } else if (warp == 1 && lane == 0) {
         // ------------------------------------------------------ MMA issuer
@@ -562,6 +593,9 @@ grouped_wgrad_kernel(const __grid_constant__ CUtensorMap map_p,
         // ------------------------------------------------------ epilogue
         const int q = warp - 4;
         const uint32_t lane_base = uint32_t(q * 32) << 16;
+        // two staging tiles for this warp, 1024-byte aligned (128-byte swizzle)
+        const uint32_t stage0 = smem_addr(smem + kStages * kStageBytes + q * 2 * kEpiTileBytes);
+        uint32_t chunk_iter = 0;
         uint32_t tile_iter = 0;
         for (int t = blockIdx.x; t < total_tiles; t += gridDim.x, ++tile_iter) {
             const uint32_t buf = tile_iter & 1u, use = tile_iter >> 1;
@@ -573,12 +607,11 @@ grouped_wgrad_kernel(const __grid_constant__ CUtensorMap map_p,
             int e, m, n;
             coords(t, e, m, n);
             const bool empty = args.offsets[e + 1] <= args.offsets[e];
-            const int64_t row = int64_t(m) * BM + q * 32 + lane;
-            float4* dst = reinterpret_cast<float4*>(
-                args.out + (int64_t(e) * args.M + row) * args.Ncols + int64_t(n) * BN);
+            // this quadrant's 32 rows of dW[e] (rows of the [E*M, Ncols] output)
+            const int out_row = e * args.M + m * BM + q * 32;
             const uint32_t tmem_acc = tmem_base + buf * BN;
 #pragma unroll 1
-            for (int c = 0; c < BN; c += 32) {
+            for (int c = 0; c < BN; c += 32, ++chunk_iter) {
                 float a[32];
                 if (!empty) {
                     tmem_ld32(tmem_acc + lane_base + c, a);
@@ -586,13 +619,30 @@ grouped_wgrad_kernel(const __grid_constant__ CUtensorMap map_p,
 #pragma unroll
                     for (int i = 0; i < 32; ++i) a[i] = 0.0f;
                 }
+                // the store that last used this staging tile has finished reading it
+                if (lane == 0 && chunk_iter >= 2) bulk_wait_read<1>();
+                __syncwarp();
+                const uint32_t tile = stage0 + (chunk_iter & 1u) * kEpiTileBytes;
+                // row `lane`, 16-byte chunk j at j ^ (row % 8): the 128-byte swizzle
 #pragma unroll
-                for (int v = 0; v < 8; ++v)
-                    dst[c / 4 + v] = make_float4(a[4 * v], a[4 * v + 1], a[4 * v + 2], a[4 * v + 3]);
+                for (int j = 0; j < 8; ++j) {
+                    const uint32_t dst = tile + lane * 128 + ((j ^ (lane & 7)) << 4);
+                    asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};"
+                                 :: "r"(dst), "f"(a[4 * j]), "f"(a[4 * j + 1]), "f"(a[4 * j + 2]),
+                                    "f"(a[4 * j + 3]) : "memory");
+                }
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_2d(&map_out, n * BN + c, out_row, tile);
+                    bulk_commit();
+                }
             }
             tc_fence_before();
             mbar_arrive(smem_addr(&tmem_empty_bar[buf]));
         }
+        if (lane == 0) bulk_wait_all();                 // every store has landed
+        __syncwarp();
     }
     tc_fence_before();
     __syncthreads();
@@ -679,6 +729,20 @@ bool make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, in
            CUDA_SUCCESS;
 }
 
+// 2D fp32 map over the row-major [rows, cols] weight-gradient output, box
+// 32 x 32 with the 128-byte swizzle of the epilogue's staging tiles.
+bool make_out_map(CUtensorMap* map, float* base, int64_t rows, int64_t cols) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {cuuint64_t(cols), cuuint64_t(rows)};
+    const cuuint64_t strides[1] = {cuuint64_t(cols) * 4};
+    const cuuint32_t box[2] = {32, 32};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Opt every tensor-core kernel into kSmemBytes of dynamic shared memory, once
 // per device.
 bool smem_attrs_set() {
@@ -689,12 +753,15 @@ bool smem_attrs_set() {
     const void* kernels[] = {(const void*)grouped_gemm_kernel<kPlain>,
                              (const void*)grouped_gemm_kernel<kSwiglu>,
                              (const void*)grouped_gemm_kernel<kSwigluSave>,
-                             (const void*)grouped_gemm_kernel<kSwigluBwd>,
-                             (const void*)grouped_wgrad_kernel};
+                             (const void*)grouped_gemm_kernel<kSwigluBwd>};
     for (const void* k : kernels)
         if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
             cudaSuccess)
             return false;
+    if (cudaFuncSetAttribute((const void*)grouped_wgrad_kernel,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kWgradSmemBytes) !=
+        cudaSuccess)
+        return false;
     done[dev] = true;
     return true;
 }
@@ -888,18 +955,21 @@ extern "C" moe_status_t moe_grouped_swiglu_wgrad(const void* x, const void* hidd
     if (!smem_attrs_set()) return MOE_ERR_CUDA;
     const int grid = sm_count();
     if (dw_down) {          // dW_down[e] [I,H] = hidden_e^T dy_e
-        CUtensorMap m_p, m_q;
-        if (!make_map(&m_p, hidden, N, I, 64) || !make_map(&m_q, dy, N, H, 64)) return MOE_ERR_CUDA;
+        CUtensorMap m_p, m_q, m_o;
+        if (!make_map(&m_p, hidden, N, I, 64) || !make_map(&m_q, dy, N, H, 64) ||
+            !make_out_map(&m_o, dw_down, int64_t(E) * I, H))
+            return MOE_ERR_CUDA;
         WgradArgs a{offsets, E, int(I), int(H), int(I / BM), int(H / BN), dw_down, header};
-        grouped_wgrad_kernel<<<grid, kThreads, kSmemBytes, s>>>(m_p, m_q, a);
+        grouped_wgrad_kernel<<<grid, kThreads, kWgradSmemBytes, s>>>(m_p, m_q, m_o, a);
         if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
     }
     if (dw_up) {            // dW_up[e] [H,2I] = x_e^T dgate_up_e
-        CUtensorMap m_p, m_q;
-        if (!make_map(&m_p, x, N, H, 64) || !make_map(&m_q, dgate_up, N, 2 * I, 64))
+        CUtensorMap m_p, m_q, m_o;
+        if (!make_map(&m_p, x, N, H, 64) || !make_map(&m_q, dgate_up, N, 2 * I, 64) ||
+            !make_out_map(&m_o, dw_up, int64_t(E) * H, 2 * I))
             return MOE_ERR_CUDA;
         WgradArgs a{offsets, E, int(H), int(2 * I), int(H / BM), int(2 * I / BN), dw_up, header};
-        grouped_wgrad_kernel<<<grid, kThreads, kSmemBytes, s>>>(m_p, m_q, a);
+        grouped_wgrad_kernel<<<grid, kThreads, kWgradSmemBytes, s>>>(m_p, m_q, m_o, a);
         if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
     }
     return MOE_OK;

@@ -118,8 +118,8 @@ def make(name: str, *, T: int | None = None, with_grad: bool = False,
     """Inputs of a workload, optionally truncated to its first T tokens.
 
     Draw order (seed = workload seed): x [T,H], W [E,H], expert permutation
-    (zipf workloads), grad_out [T,H] (if requested), w_up [E,H,2I], w_down
-    [E,I,H] (layer, if requested).  Truncation draws the full-size arrays and
+    (zipf workloads), w_up [E,H,2I] and w_down [E,I,H] (layer, if
+    requested), grad_out [T,H] (if requested).  Truncation draws the full-size arrays and
     slices, so a prefix of a workload is the same bytes at any size."""
     wl = WORKLOADS[name]
     key = (name, with_grad, with_weights)
@@ -136,11 +136,11 @@ def make(name: str, *, T: int | None = None, with_grad: bool = False,
         del x32
         d = {"x": x, "W": W, "bias": bias, "expert_perm": perm,
              "logits": router_logits(x, W, bias)}
-        if with_grad:
-            d["grad_out"] = as_activation(_normal(rng, (wl.T, wl.H)), wl.dtype)
         if with_weights and wl.I:
             d["w_up"] = f32_to_bf16_bits(_normal(rng, (wl.E, wl.H, 2 * wl.I), std=0.02))
             d["w_down"] = f32_to_bf16_bits(_normal(rng, (wl.E, wl.I, wl.H), std=0.02))
+        if with_grad:
+            d["grad_out"] = as_activation(_normal(rng, (wl.T, wl.H)), wl.dtype)
         d["scale"] = stand_in_scale(wl.E)
         _CACHE.clear()  # keep at most one full-size workload resident
         _CACHE[key] = d
