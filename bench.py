@@ -52,15 +52,18 @@ def algorithmic_bytes(T, H, E, k, b):
     }
 
 
-def layout_bytes(T, H, k, b, kept, rows):
+def layout_bytes(T, H, k, b, kept, rows, live=None):
     """Algorithmic bytes under a capacity / padded / aligned layout: only the
-    `kept` slot rows move, and the pad-row fill writes the other rows of the
-    expert segments (`rows` = offsets[E], the rows the segments span)."""
+    `kept` slot rows move, the pad-row fill writes the other rows of the
+    expert segments (`rows` = offsets[E], the rows the segments span), and
+    only the `live` tokens (at least one kept slot; default all T) need their
+    x / grad_out row read.  The combine still writes every output row."""
     N = T * k
+    live = T if live is None else live
     return {
-        "permute": T * H * b + kept * H * b + N * 4 + (rows - kept) * H * b,
+        "permute": live * H * b + kept * H * b + N * 4 + (rows - kept) * H * b,
         "combine": kept * H * b + T * H * b + N * 8,
-        "combine_backward": T * H * b + 2 * kept * H * b + N * 12,
+        "combine_backward": live * H * b + 2 * kept * H * b + N * 12,
     }
 
 
@@ -485,7 +488,8 @@ def run_ours(args, rank, world, local_rank):
     if lay:
         kept = int(rl.counts.sum().item())
         segs = int(rl.offsets[-1].item())
-        lb = layout_bytes(T, H, k, b, kept, segs)
+        live = int((rl.slot_pos >= 0).any(dim=1).sum().item())
+        lb = layout_bytes(T, H, k, b, kept, segs, live)
         alg.update({n: v for n, v in lb.items() if n in names})
     kern = {}
     for n in names:

@@ -79,6 +79,9 @@ def test_layout_bytes_count_only_kept_rows():
     capped = bench.layout_bytes(T, H, k, b, 50000, 163840)
     assert capped["combine"] == 50000 * H * b + T * H * b + 8 * T * k
     assert capped["permute"] == T * H * b + 163840 * H * b + 4 * T * k
+    sparse = bench.layout_bytes(T, H, k, b, 50000, 163840, live=9000)
+    assert sparse["combine_backward"] == 9000 * H * b + 2 * 50000 * H * b + 12 * T * k
+    assert sparse["combine"] == capped["combine"]
 
 
 def test_clock_summary_parses_nvidia_smi_lines():

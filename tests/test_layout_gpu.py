@@ -5,7 +5,7 @@ import pytest
 
 import oracle
 import workloads as wl
-from moe_testutil import bf16_ulp_diff, to_dev, to_host
+from moe_testutil import bf16_ulp_diff, to_dev, to_host, within_one_bf16_ulp
 
 pytestmark = pytest.mark.gpu
 
@@ -104,10 +104,11 @@ def test_capacity_drops_reach_the_combine():
     assert bf16_ulp_diff(out, ref).max() == 0
     g = wl.random_activation(13, (T, H), "bf16")
     gy, gp = moe.moe_combine_backward(to_dev(g), to_dev(y), r.slot_pos, to_dev(w))
-    gy_o, gp_o, _ = oracle.combine_backward(g, y, o["slot_pos"], w)
+    gy_o, gp_o, gp64 = oracle.combine_backward(g, y, o["slot_pos"], w)
     valid = o["slot_pos"][o["slot_pos"] >= 0]
     assert (to_host(gy)[valid] == gy_o[valid]).all()
     assert (to_host(gp)[o["slot_pos"] < 0] == 0).all()
+    assert within_one_bf16_ulp(to_host(gp), gp64).all()
 
 
 def test_aligned_layout_pipeline_equals_plain_pipeline():

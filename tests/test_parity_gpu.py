@@ -264,6 +264,37 @@ def test_combine_all_slots_empty_gives_positive_zero_rows():
     assert bf16_ulp_diff(out, ref).max() == 0 and (out == ref).all()
 
 
+@pytest.mark.parametrize("weighted", [True, False])
+def test_combine_and_backward_with_mostly_empty_slots(weighted):
+    """Tokens with zero or one live slot take their own paths (capacity
+    drops make them common): bit-exact combine including the +0 a zero
+    product gives, and the backward's grad_y / grad_probs."""
+    T, H, E, k = 900, 7168, 64, 8
+    idx, w = wl.random_routing(31, T, E, k, empty_frac=0.85)
+    w = np.random.default_rng(32).uniform(-1.5, 1.5, (T, k)).astype(np.float32)   # signed
+    if not weighted:
+        w = None
+    r = moe.moe_route_indices(to_dev(idx), None, E)
+    o = oracle.route_indices(idx, None, E)
+    live = (idx >= 0).sum(axis=1)
+    assert (live == 0).any() and (live == 1).sum() > T // 4
+    y = wl.random_activation(33, (T * k, H), "bf16")
+    y[:, ::97] = 0x8000                                    # negative zeros
+    y[:, 1::89] = 0
+    wd = None if w is None else to_dev(w)
+    out = to_host(moe.moe_combine(to_dev(y), r.slot_pos, wd))
+    ref, _ = oracle.combine(y, o["slot_pos"], w)
+    assert (out == ref).all(), f"{np.count_nonzero(out != ref)} mismatches"
+    g = wl.random_activation(34, (T, H), "bf16")
+    gy, gp = moe.moe_combine_backward(to_dev(g), to_dev(y), r.slot_pos, wd)
+    gy, gp = to_host(gy), to_host(gp)
+    gy_o, gp_o, gp64 = oracle.combine_backward(g, y, o["slot_pos"], w)
+    n = int(o["offsets"][E])
+    assert gy[:n].tobytes() == gy_o[:n].tobytes()
+    assert within_one_bf16_ulp(gp, gp64).all()
+    assert (gp[o["slot_pos"] < 0] == 0).all()
+
+
 def test_combine_deterministic_and_stable_across_calls():
     T, H, E, k = 2000, 2048, 64, 8
     idx, w = wl.random_routing(1, T, E, k)

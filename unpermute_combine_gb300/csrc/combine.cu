@@ -59,6 +59,71 @@ __device__ __forceinline__ void stage_slots(int32_t* s_pos, float* s_w, const in
     __syncwarp();
 }
 
+// Two floats in one 64-bit register (low word = even element): Blackwell's
+// packed f32x2 add/sub/mul run two lanes of float arithmetic per instruction.
+typedef unsigned long long f2_t;
+
+__device__ __forceinline__ f2_t f2_pack(float lo, float hi) {
+    f2_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2_unpack(f2_t v, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ f2_t f2_add(f2_t a, f2_t b) {
+    f2_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ f2_t f2_sub(f2_t a, f2_t b) {
+    f2_t r;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ f2_t f2_mul(f2_t a, f2_t b) {
+    f2_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+// bf16 pair (low half = even element) -> two floats
+__device__ __forceinline__ f2_t f2_from_bf16x2(uint32_t p) {
+    return f2_pack(bf16lo_to_f32(p), bf16hi_to_f32(p));
+}
+// Knuth TwoSum on both lanes: (hi, lo) += q with the rounding error of
+// hi + q kept exactly in lo's input.
+__device__ __forceinline__ void f2_two_sum_acc(f2_t& hi, f2_t& lo, f2_t q) {
+    const f2_t s = f2_add(hi, q);
+    const f2_t bp = f2_sub(s, hi);
+    const f2_t e = f2_add(f2_sub(hi, f2_sub(s, bp)), f2_sub(q, bp));
+    hi = s;
+    lo = f2_add(lo, e);
+}
+
+// w * (g0, g1) -> bf16 pair of the exact products.  The packed float products
+// are correctly rounded floats; a bf16 midpoint (low half 0x8000) in either
+// one sends the pair to the error-free tie break.
+__device__ __forceinline__ uint32_t scale_pair_bf16_f2(f2_t w2, f2_t g2) {
+    float p0, p1;
+    f2_unpack(f2_mul(w2, g2), p0, p1);
+    const uint32_t lows = __byte_perm(__float_as_uint(p0), __float_as_uint(p1), 0x5410) ^ 0x80008000u;
+    if (((lows - 0x00010001u) & ~lows & 0x80008000u) != 0) {   // a half equal to 0x8000
+        float w, w_hi, g0, g1;
+        f2_unpack(w2, w, w_hi);
+        f2_unpack(g2, g0, g1);
+        return mul_bf16_rn(w, g0) | (mul_bf16_rn(w, g1) << 16);
+    }
+    return pack_bf16x2_rn(p0, p1);
+}
+
+// A bf16 pair with any -0 half turned into +0 (a sum that starts from +0
+// never ends on -0).
+__device__ __forceinline__ uint32_t plus_zero_bf16x2(uint32_t r) {
+    if ((r & 0xFFFFu) == 0x8000u) r &= 0xFFFF0000u;
+    if ((r >> 16) == 0x8000u) r &= 0x0000FFFFu;
+    return r;
+}
+
 // -------------------------------------------------------- combine, bf16 rows
 
 constexpr int kU = 2;   // 16-byte vectors per lane per batch
@@ -173,10 +238,44 @@ combine_bf16_regs_kernel(const uint4* __restrict__ y, int64_t T, int64_t nvec, i
         stage_slots(s_pos[warp], s_w[warp], slot_pos, topk_w, t, k, n_rows, lane);
         int32_t pj[KMAX];
         float wj[KMAX];
+        int nv = 0, j0 = 0;
 #pragma unroll
         for (int j = 0; j < KMAX; ++j) {
             pj[j] = j < k ? s_pos[warp][j] : -1;
             wj[j] = j < k ? s_w[warp][j] : 0.0f;
+            if (pj[j] >= 0 && nv++ == 0) j0 = j;
+        }
+        if (nv <= 1) {
+            // at most one term: the double slot-order sum is fma(w, y, +0), the
+            // exact product (a zero product gives +0), rounded once; 4 vectors
+            // in flight per lane (a lone row per step would leave the warp
+            // latency-bound)
+            const int64_t p = nv ? int64_t(s_pos[warp][j0]) : 0;
+            const float w = nv ? s_w[warp][j0] : 0.0f;
+            const f2_t w2 = f2_pack(w, w);
+            for (int64_t v0 = lane; v0 < nvec; v0 += 32 * 4) {
+                uint4 d[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int64_t v = v0 + 32 * u;
+                    d[u] = (nv && v < nvec) ? __ldcs(y + p * nvec + v) : make_uint4(0, 0, 0, 0);
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int64_t v = v0 + 32 * u;
+                    if (v >= nvec) break;
+                    uint4 r = make_uint4(0, 0, 0, 0);
+                    if (nv) {
+                        r.x = plus_zero_bf16x2(scale_pair_bf16_f2(w2, f2_from_bf16x2(d[u].x)));
+                        r.y = plus_zero_bf16x2(scale_pair_bf16_f2(w2, f2_from_bf16x2(d[u].y)));
+                        r.z = plus_zero_bf16x2(scale_pair_bf16_f2(w2, f2_from_bf16x2(d[u].z)));
+                        r.w = plus_zero_bf16x2(scale_pair_bf16_f2(w2, f2_from_bf16x2(d[u].w)));
+                    }
+                    __stcs(out + t * nvec + v, r);
+                }
+            }
+            __syncwarp();
+            continue;
         }
         for (int64_t v = lane; v < nvec; v += 32) {
             uint4 d[KMAX];
@@ -377,62 +476,6 @@ __device__ __forceinline__ float dd_warp_sum(float hi, float lo) {
     return __fadd_rn(hi, lo);
 }
 
-// Two floats in one 64-bit register (low word = even element): Blackwell's
-// packed f32x2 add/sub/mul run two lanes of float arithmetic per instruction.
-typedef unsigned long long f2_t;
-
-__device__ __forceinline__ f2_t f2_pack(float lo, float hi) {
-    f2_t r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-    return r;
-}
-__device__ __forceinline__ void f2_unpack(f2_t v, float& lo, float& hi) {
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-}
-__device__ __forceinline__ f2_t f2_add(f2_t a, f2_t b) {
-    f2_t r;
-    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-    return r;
-}
-__device__ __forceinline__ f2_t f2_sub(f2_t a, f2_t b) {
-    f2_t r;
-    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-    return r;
-}
-__device__ __forceinline__ f2_t f2_mul(f2_t a, f2_t b) {
-    f2_t r;
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-    return r;
-}
-// bf16 pair (low half = even element) -> two floats
-__device__ __forceinline__ f2_t f2_from_bf16x2(uint32_t p) {
-    return f2_pack(bf16lo_to_f32(p), bf16hi_to_f32(p));
-}
-// Knuth TwoSum on both lanes: (hi, lo) += q with the rounding error of
-// hi + q kept exactly in lo's input.
-__device__ __forceinline__ void f2_two_sum_acc(f2_t& hi, f2_t& lo, f2_t q) {
-    const f2_t s = f2_add(hi, q);
-    const f2_t bp = f2_sub(s, hi);
-    const f2_t e = f2_add(f2_sub(hi, f2_sub(s, bp)), f2_sub(q, bp));
-    hi = s;
-    lo = f2_add(lo, e);
-}
-
-// w * (g0, g1) -> bf16 pair of the exact products.  The packed float products
-// are correctly rounded floats; a bf16 midpoint (low half 0x8000) in either
-// one sends the pair to the error-free tie break.
-__device__ __forceinline__ uint32_t scale_pair_bf16_f2(f2_t w2, f2_t g2) {
-    float p0, p1;
-    f2_unpack(f2_mul(w2, g2), p0, p1);
-    const uint32_t lows = __byte_perm(__float_as_uint(p0), __float_as_uint(p1), 0x5410) ^ 0x80008000u;
-    if (((lows - 0x00010001u) & ~lows & 0x80008000u) != 0) {   // a half equal to 0x8000
-        float w, w_hi, g0, g1;
-        f2_unpack(w2, w, w_hi);
-        f2_unpack(g2, g0, g1);
-        return mul_bf16_rn(w, g0) | (mul_bf16_rn(w, g1) << 16);
-    }
-    return pack_bf16x2_rn(p0, p1);
-}
 
 // k <= 8: every slot row of the current 16-byte column is loaded before any
 // arithmetic, so a lane keeps k loads in flight.  Two CTAs per SM (at most
@@ -454,13 +497,65 @@ combine_bwd_bf16_vec_kernel(const uint4* __restrict__ gout, const uint4* __restr
         stage_slots(s_pos[warp], s_w[warp], slot_pos, topk_w, t, k, n_rows, lane);
         int32_t pj[KMAX];
         f2_t wj[KMAX], hi[KMAX], lo[KMAX];
+        int nv = 0, j0 = 0;
 #pragma unroll
         for (int j = 0; j < KMAX; ++j) {
             pj[j] = j < k ? s_pos[warp][j] : -1;
+            if (pj[j] >= 0 && nv++ == 0) j0 = j;
             const float w = j < k ? s_w[warp][j] : 0.0f;
             wj[j] = f2_pack(w, w);
             hi[j] = 0ull;
             lo[j] = 0ull;
+        }
+        if (nv == 0) {              // every slot empty or dropped: nothing reads grad_out
+            if (lane < k) grad_probs[t * k + lane] = 0.0f;
+            __syncwarp();
+            continue;
+        }
+        if (nv == 1) {
+            // one live slot: the same per-lane accumulation order, 4 column
+            // vectors in flight per lane instead of one row pair per step
+            const int64_t p = s_pos[warp][j0];
+            const float w = s_w[warp][j0];
+            const f2_t w2 = f2_pack(w, w);
+            f2_t h1 = 0ull, l1 = 0ull;
+            for (int64_t v0 = lane; v0 < nvec; v0 += 32 * 4) {
+                uint4 gv[4], yv[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int64_t v = v0 + 32 * u;
+                    const bool in = v < nvec;
+                    gv[u] = in ? __ldcs(gout + t * nvec + v) : make_uint4(0, 0, 0, 0);
+                    yv[u] = in ? __ldcs(y + p * nvec + v) : make_uint4(0, 0, 0, 0);
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int64_t v = v0 + 32 * u;
+                    if (v >= nvec) break;
+                    const f2_t g0 = f2_from_bf16x2(gv[u].x), g1 = f2_from_bf16x2(gv[u].y);
+                    const f2_t g2 = f2_from_bf16x2(gv[u].z), g3 = f2_from_bf16x2(gv[u].w);
+                    uint4 r;
+                    r.x = scale_pair_bf16_f2(w2, g0);
+                    r.y = scale_pair_bf16_f2(w2, g1);
+                    r.z = scale_pair_bf16_f2(w2, g2);
+                    r.w = scale_pair_bf16_f2(w2, g3);
+                    __stcs(gy + p * nvec + v, r);
+                    f2_two_sum_acc(h1, l1, f2_mul(g0, f2_from_bf16x2(yv[u].x)));
+                    f2_two_sum_acc(h1, l1, f2_mul(g1, f2_from_bf16x2(yv[u].y)));
+                    f2_two_sum_acc(h1, l1, f2_mul(g2, f2_from_bf16x2(yv[u].z)));
+                    f2_two_sum_acc(h1, l1, f2_mul(g3, f2_from_bf16x2(yv[u].w)));
+                }
+            }
+            float a0, a1, b0, b1;
+            f2_unpack(h1, a0, a1);
+            f2_unpack(l1, b0, b1);
+            float s1, e1;
+            two_sum(a0, a1, s1, e1);
+            e1 = __fadd_rn(e1, __fadd_rn(b0, b1));
+            const float r = dd_warp_sum(s1, e1);
+            if (lane < k) grad_probs[t * k + lane] = lane == j0 ? r : 0.0f;
+            __syncwarp();
+            continue;
         }
         for (int64_t v = lane; v < nvec; v += 32) {
             const uint4 gv = __ldcs(gout + t * nvec + v);
