@@ -577,6 +577,173 @@ def run_ours(args, rank, world, local_rank):
     return line
 
 
+# ------------------------------------------------------------ sort_chunks
+
+def vep_bytes(N, H, b, C):
+    """sort_chunks, per direction: every row read once and written once, plus
+    the split sizes and chunk order (4 bytes each) of every chunk."""
+    return 2 * N * H * b + 8 * C
+
+
+def run_vep8(args, rank, world, local_rank):
+    """The rank-major <-> expert-major reorder of an 8-rank x 8-local-expert
+    virtual expert-parallel layout: for each virtual rank, moe_sort_chunks
+    forward (rank-major receive buffer -> expert-major) and back."""
+    import numpy as np
+    import torch
+
+    import unpermute_combine_gb300 as moe
+    import workloads as wl
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    d = wl.make("vep8")
+    W = d["workload"]
+    R = L = W.ranks
+    T, H, k = W.T, W.H, W.k
+    bf = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)
+    stream = torch.cuda.Stream(device=dev)
+    # set-up (untimed): route on the GPU, then each virtual rank's split matrix
+    # M_r[src, le] (tokens of source slice src routed to expert r*L + le) and its
+    # rank-major receive buffer (for src, then le: those tokens' rows, ascending)
+    with torch.cuda.stream(stream):
+        r = moe.moe_route(torch.from_numpy(d["logits"]).to(dev), k, stream=stream)
+    stream.synchronize()
+    idx = r.topk_idx.cpu().numpy()
+    x = bf(d["x"]).to(dev)
+    per = T // R
+    fwd_idx = torch.tensor(moe.moe_chunk_idxs(R, L, False), dtype=torch.int32, device=dev)
+    inv_idx = torch.tensor(moe.moe_chunk_idxs(R, L, True), dtype=torch.int32, device=dev)
+    ranks = []
+    for rr in range(R):
+        M = np.zeros((R, L), np.int32)
+        rows = []
+        for src in range(R):
+            toks = np.arange(src * per, (src + 1) * per)
+            for le in range(L):
+                sel = toks[(idx[toks] == rr * L + le).any(axis=1)]
+                M[src, le] = sel.size
+                rows.append(sel)
+        order = torch.from_numpy(np.concatenate(rows).astype(np.int64)).to(dev)
+        buf = x.index_select(0, order)
+        ranks.append(dict(buf=buf, em=torch.empty_like(buf), back=torch.empty_like(buf),
+                          sp=torch.from_numpy(M.ravel().copy()).to(dev),
+                          spt=torch.from_numpy(M.T.ravel().copy()).to(dev),
+                          ws_f=torch.empty(moe.moe_sort_chunks_workspace_size(R * L),
+                                           dtype=torch.uint8, device=dev),
+                          ws_b=torch.empty(moe.moe_sort_chunks_workspace_size(R * L),
+                                           dtype=torch.uint8, device=dev)))
+    N = sum(int(q["buf"].shape[0]) for q in ranks)
+    names = ["sort_chunks", "sort_chunks_inverse"]
+
+    def step(ev=None, bufs=None):
+        if ev is not None:
+            ev[0].record(stream)
+        for q, src in zip(ranks, bufs or [q["buf"] for q in ranks]):
+            moe.moe_sort_chunks(src, q["sp"], fwd_idx, out=q["em"], workspace=q["ws_f"],
+                                stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+        for q in ranks:
+            moe.moe_sort_chunks(q["em"], q["spt"], inv_idx, out=q["back"], workspace=q["ws_b"],
+                                stream=stream)
+        if ev is not None:
+            ev[2].record(stream)
+
+    import torch.distributed as dist
+    dist_on = dist.is_available() and dist.is_initialized()
+
+    def barrier():
+        torch.cuda.synchronize(dev)
+        if dist_on:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    for _ in range(args.warmup):
+        step()
+    barrier()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local_rank) as clk:
+        barrier()
+        t0.record(stream)
+        for i in range(args.steps):
+            step(evs[i])
+        t1.record(stream)
+        barrier()
+    elapsed = t0.elapsed_time(t1) / 1e3
+    per_t = {n: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(args.steps))
+             / 1e3 for j, n in enumerate(names)}
+    for q in ranks:
+        assert moe.moe_workspace_status(q["ws_f"], stream) == 0, "sort_chunks plan rejected"
+        assert moe.moe_workspace_status(q["ws_b"], stream) == 0, "sort_chunks plan rejected"
+    max_elapsed = reduce_max(elapsed, dev)
+
+    # end to end: the rank-major buffers from pinned host memory, the step,
+    # the expert-major buffers back to the host
+    h_in = [q["buf"].cpu().pin_memory() for q in ranks]
+    h_out = [torch.empty_like(q["buf"], device="cpu").pin_memory() for q in ranks]
+    d_in = [torch.empty_like(q["buf"]) for q in ranks]
+    e2e_steps = 0 if args.no_e2e else max(1, min(args.steps, 20))
+
+    def e2e_step():
+        with torch.cuda.stream(stream):
+            for hi, di in zip(h_in, d_in):
+                di.copy_(hi, non_blocking=True)
+        step(bufs=d_in)
+        with torch.cuda.stream(stream):
+            for ho, q in zip(h_out, ranks):
+                ho.copy_(q["em"], non_blocking=True)
+
+    e2e_value = None
+    if e2e_steps:
+        for _ in range(2):
+            e2e_step()
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        barrier()
+        e2e_value = job_value(N, world, e2e_steps, reduce_max(e0.elapsed_time(e1) / 1e3, dev))
+    if rank != 0:
+        return None
+    peak, peak_kind = measured_peak()
+    alg = vep_bytes(N, H, 2, R * L * R)
+    kern = {}
+    for n in names:
+        gbs = alg / per_t[n] / 1e9
+        kern[n] = {"us": round(per_t[n] * 1e6, 2), "alg_bytes": alg, "GB_s": round(gbs, 1),
+                   "frac": round(gbs / peak, 4), "launches": R}
+    dominant = max(names, key=lambda n_: per_t[n_])
+    ach = alg / per_t[dominant] / 1e9
+    io = sum(t.numel() * 2 for t in h_in)
+    return {
+        "metric": METRIC, "value": job_value(N, world, args.steps, max_elapsed), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": max_elapsed / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded; virtual expert-parallel layout from the GPU route)",
+        "config": {"workload": f"vep8: T={T} H={H} E={R * L} k={k} bf16, {R} virtual ranks x "
+                               f"{L} local experts, {per}-token source slices",
+                   "routed_rows_per_step": N,
+                   "step": f"moe_sort_chunks rank-major -> expert-major for each of {R} virtual "
+                           "ranks, then expert-major -> rank-major",
+                   "l2": "no flush: the step moves 537 MB each way, > 129 MB L2",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "roofline": {"bound": "hbm", "kernel": dominant, "achieved": round(ach, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(ach / peak, 4),
+                     "peak_source": f"{peak_kind} hbm_gbs", "traffic": None},
+        "kernels": kern,
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": io,
+                "d2h_bytes_per_step": io, "steps": e2e_steps,
+                "path": "pinned rank-major buffers -> device -> step -> expert-major to host"},
+        "gpu_launches": 2 * R * args.steps,              # one fused launch per call (C <= 1024)
+        "clocks": clk.summary(),
+    }
+
+
 # ------------------------------------------------------------ oracle timing
 
 def cpu_baseline(tokens: int):
@@ -653,9 +820,10 @@ def main(argv=None):
                     help="capacity / padded / aligned layout, e.g. 'cf=1.25,pad' or 'align=128'")
     ap.add_argument("--route-groups", default=None, metavar="G:KG",
                     help="route with group-limited routing: G expert groups, KG kept")
-    ap.add_argument("--workload", choices=["skewed", "layer"], default=WORKLOAD,
+    ap.add_argument("--workload", choices=["skewed", "layer", "vep8"], default=WORKLOAD,
                     help="skewed: the dispatch/combine step (default); layer: the full MoE "
-                         "layer forward with the grouped SwiGLU")
+                         "layer forward with the grouped SwiGLU; vep8: sort_chunks forward "
+                         "and inverse on an 8-rank x 8-expert virtual EP layout")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("at least 3 warm-up steps")
@@ -671,7 +839,7 @@ def main(argv=None):
             import torch.distributed as dist
             torch.cuda.set_device(local_rank)
             dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
-        line = run_ours(args, rank, world, local_rank)
+        line = (run_vep8 if args.workload == "vep8" else run_ours)(args, rank, world, local_rank)
         if world > 1:
             import torch.distributed as dist
             dist.destroy_process_group()

@@ -231,7 +231,9 @@ moe_status_t moe_permute(const void* x, moe_dtype_t dtype, int64_t T, int64_t H,
  *   split_sizes [C] int32 (device), sorted_idxs [C] int32 (device).
  * If the sizes do not add up to N, or sorted_idxs is not a permutation of
  * 0..C-1, nothing is written and the workspace status becomes
- * MOE_ERR_DEVICE_CHECK.  1 <= C <= 65536.
+ * MOE_ERR_DEVICE_CHECK.  1 <= C <= 65536.  Up to 1024 chunks of rows that
+ * are 16-byte multiples take one launch that copies with bulk copies; a
+ * bounded wait there that gives up is reported by moe_device_status.
  * Workspace: moe_sort_chunks_workspace_size(C) bytes. */
 moe_status_t moe_sort_chunks_workspace_size(int C, size_t* bytes);
 

@@ -84,6 +84,11 @@ def test_layout_bytes_count_only_kept_rows():
     assert sparse["combine"] == capped["combine"]
 
 
+def test_vep_bytes_at_the_virtual_ep_shape():
+    # 32768 routed rows of 4096 bf16 each way: 536.9 MB per direction
+    assert abs(bench.vep_bytes(32768, 4096, 2, 512) / 1e6 - 536.9) < 0.1
+
+
 def test_clock_summary_parses_nvidia_smi_lines():
     c = bench.ClockSampler(0)
     c.out = ("0, 2070, 2070, 900.1, 0x0, Not Active, Not Active, Not Active, Not Active\n"

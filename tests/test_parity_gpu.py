@@ -394,7 +394,9 @@ def test_sort_chunks_virtual_ep8_round_trip():
 
 
 @pytest.mark.parametrize("R,L,H,dtype", [(3, 5, 100, "bf16"), (2, 2, 16, "f32"), (1, 9, 64, "bf16"),
-                                         (16, 16, 1024, "bf16")])
+                                         (16, 16, 1024, "bf16"),
+                                         (40, 40, 64, "bf16"),       # C > 1024: plan kernel path
+                                         (8, 8, 12000, "bf16")])     # rows of 24000 B: 2 pieces
 def test_sort_chunks_asymmetric(R, L, H, dtype):
     rng = np.random.default_rng(R * 100 + L)
     M = rng.integers(0, 40, (R, L)).astype(np.int32)

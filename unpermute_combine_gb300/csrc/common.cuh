@@ -95,6 +95,29 @@ __device__ __forceinline__ uint32_t mul_bf16_rn(float a, float b) {
     return f32_to_bf16_rn(p);
 }
 
+// Programmatic dependent launch: the kernel may start while its predecessor
+// in the stream is finishing; it must call wait_for_predecessor() before it
+// touches anything the predecessor writes (or reads what it may overwrite).
+__device__ __forceinline__ void wait_for_predecessor() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(KArgs...), unsigned grid, unsigned block, size_t smem,
+                             cudaStream_t stream, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // Streaming 16-byte global accesses.
 __device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
     uint4 r;

@@ -296,6 +296,156 @@ sort_chunks_copy_kernel(const V* __restrict__ in, int64_t N, int64_t nvec, int C
     }
 }
 
+// ------------------------------------------------- sort_chunks, fused bulk
+// Every chunk is one contiguous run of rows in the input and in the output,
+// so for up to kFusedChunks chunks of 16-byte-multiple rows one launch does
+// everything: each single-warp CTA builds and checks the chunk plan in shared
+// memory (two warp scans over the C split sizes -- cheaper than a separate
+// plan launch), then copies its share of the output as pieces of at most
+// kScPiece bytes, each inside one chunk, through a ring of shared-memory
+// stages with bulk copies (one bulk load and one bulk store per piece).
+// Every CTA reaches the same verdict on the plan; an invalid plan writes
+// nothing and CTA 0 records MOE_ERR_DEVICE_CHECK.  Launched as a
+// programmatic dependent of the previous kernel in the stream.
+constexpr int kFusedChunks = 1024;
+constexpr int kScPiece = 16384;
+constexpr int kScStages = 3;
+
+__device__ __forceinline__ int32_t warp_incl_scan(int32_t v, int lane) {
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int32_t o = __shfl_up_sync(0xFFFFFFFFu, v, off);
+        if (lane >= off) v += o;
+    }
+    return v;
+}
+
+__global__ void __launch_bounds__(32)
+sort_chunks_bulk_kernel(const uint8_t* __restrict__ in, int64_t N, int64_t row_bytes,
+                        const int32_t* __restrict__ split_sizes,
+                        const int32_t* __restrict__ sorted_idxs, int C, uint8_t* __restrict__ out,
+                        WsHeader* __restrict__ header, uint32_t* __restrict__ status) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ __align__(8) uint64_t full_bar[kScStages];
+    __shared__ int32_t s_srcpre[kFusedChunks];     // first input row of input chunk c
+    __shared__ int32_t s_src[kFusedChunks];        // first input row of output chunk j
+    __shared__ int32_t s_dst[kFusedChunks + 1];    // first output row of output chunk j
+    __shared__ int32_t s_item[kFusedChunks + 1];   // first piece of output chunk j
+    __shared__ uint32_t s_seen[kFusedChunks / 32];
+    const int lane = threadIdx.x;
+    const uint32_t full = 0xFFFFFFFFu;
+    wait_for_predecessor();
+
+    // ---- plan
+    for (int i = lane; i < kFusedChunks / 32; i += 32) s_seen[i] = 0;
+    bool bad = false;
+    int64_t carry = 0;
+    for (int base = 0; base < C; base += 32) {
+        const int i = base + lane;
+        int32_t v = i < C ? split_sizes[i] : 0;
+        if (v < 0) { bad = true; v = 0; }
+        const int32_t incl = warp_incl_scan(v, lane);
+        if (i < C) s_srcpre[i] = int32_t(carry + incl - v);
+        carry += __shfl_sync(full, incl, 31);
+    }
+    if (carry != N) bad = true;
+    __syncwarp();
+    int64_t rcarry = 0, icarry = 0;
+    for (int base = 0; base < C; base += 32) {
+        const int j = base + lane;
+        int32_t rows = 0, c = -1;
+        if (j < C) {
+            c = sorted_idxs[j];
+            if (c < 0 || c >= C) {
+                bad = true;
+                c = -1;
+            } else {
+                const uint32_t bit = 1u << (c & 31);
+                if (atomicOr(&s_seen[c >> 5], bit) & bit) bad = true;     // named twice
+                rows = max(split_sizes[c], 0);
+            }
+        }
+        const int32_t items = int32_t((int64_t(rows) * row_bytes + kScPiece - 1) / kScPiece);
+        const int32_t rincl = warp_incl_scan(rows, lane);
+        const int32_t iincl = warp_incl_scan(items, lane);
+        if (j < C) {
+            s_dst[j] = int32_t(rcarry + rincl - rows);
+            s_src[j] = c >= 0 ? s_srcpre[c] : 0;
+            s_item[j] = int32_t(icarry + iincl - items);
+        }
+        rcarry += __shfl_sync(full, rincl, 31);
+        icarry += __shfl_sync(full, iincl, 31);
+    }
+    if (lane == 0) {
+        s_dst[C] = int32_t(rcarry);
+        s_item[C] = int32_t(icarry);
+    }
+    bad = __any_sync(full, bad);
+    if (blockIdx.x == 0 && lane == 0) {
+        header->status = bad ? MOE_ERR_DEVICE_CHECK : MOE_OK;
+        header->detail = 0;
+    }
+    if (bad) return;
+    __syncwarp();
+
+    // ---- copy
+    const int64_t total = s_item[C];
+    const int64_t first = blockIdx.x;
+    const int64_t my_items = first < total ? (total - first + gridDim.x - 1) / gridDim.x : 0;
+    const uint32_t smem0 = smem_addr(smem);
+    if (lane == 0) {
+        for (int st = 0; st < kScStages; ++st) mbar_init(smem_addr(&full_bar[st]), 1);
+        mbar_fence_init();
+    }
+    __syncwarp();
+    auto piece_of = [&](int64_t q, int64_t& src, int64_t& dst, uint32_t& bytes) {
+        const int32_t item = int32_t(first + q * gridDim.x);
+        int lo = 0, hi = C - 1;                        // last chunk starting at or before item
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (s_item[mid] <= item) lo = mid; else hi = mid - 1;
+        }
+        const int64_t off = int64_t(item - s_item[lo]) * kScPiece;
+        const int64_t cbytes = int64_t(s_dst[lo + 1] - s_dst[lo]) * row_bytes;
+        bytes = uint32_t(min64(kScPiece, cbytes - off));
+        src = int64_t(s_src[lo]) * row_bytes + off;
+        dst = int64_t(s_dst[lo]) * row_bytes + off;
+    };
+    auto issue_load = [&](int64_t q) {
+        int64_t src, dst;
+        uint32_t bytes;
+        piece_of(q, src, dst, bytes);
+        const int st = int(q % kScStages);
+        const uint32_t fb = smem_addr(&full_bar[st]);
+        mbar_expect_tx(fb, bytes);
+        bulk_load(smem0 + uint32_t(st) * kScPiece, in + src, bytes, fb);
+    };
+    if (lane == 0)
+        for (int64_t q = 0; q < my_items && q < kScStages; ++q) issue_load(q);
+    bool failed = false;
+    for (int64_t q = 0; q < my_items; ++q) {
+        const int st = int(q % kScStages);
+        const uint32_t ph = uint32_t(q / kScStages) & 1u;
+        if (!__all_sync(full, mbar_wait(smem_addr(&full_bar[st]), ph))) {
+            failed = true;
+            break;
+        }
+        if (lane == 0) {
+            int64_t src, dst;
+            uint32_t bytes;
+            piece_of(q, src, dst, bytes);
+            bulk_store(out + dst, smem0 + uint32_t(st) * kScPiece, bytes);
+            bulk_commit();
+            // the store of piece q-1 has read its stage: refill it with piece q-1+S
+            bulk_wait_read<1>();
+            if (q >= 1 && q - 1 + kScStages < my_items) issue_load(q - 1 + kScStages);
+        }
+        __syncwarp();
+    }
+    if (lane == 0) bulk_wait_all();
+    if (failed && lane == 0 && status) atomicExch(status, uint32_t(MOE_ERR_TIMEOUT));
+}
+
 size_t chunk_plan_bytes(int C) {
     return align_up(sizeof(int32_t) * (size_t(C + 1) * 2 + size_t(C)), kWsAlign);
 }
@@ -457,6 +607,27 @@ extern "C" moe_status_t moe_sort_chunks(const void* in, moe_dtype_t dtype, int64
         return MOE_ERR_WORKSPACE;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     WsHeader* header = static_cast<WsHeader*>(workspace);
+    const size_t row_b = size_t(H) * elem_size(dtype);
+    if (C <= kFusedChunks && row_b % 16 == 0 && (N == 0 || H == 0 || (aligned16(in) && aligned16(out)))) {
+        static bool attr_set[64] = {};
+        int dev = 0;
+        cudaGetDevice(&dev);
+        if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+            if (cudaFuncSetAttribute(sort_chunks_bulk_kernel,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     kScStages * kScPiece) != cudaSuccess)
+                return MOE_ERR_CUDA;
+            attr_set[dev] = true;
+        }
+        const int64_t pieces = (N * int64_t(row_b) + kScPiece - 1) / kScPiece + C;
+        const int g = int(max64(1, min64(pieces, int64_t(sm_count()) * 3)));
+        if (launch_dependent(sort_chunks_bulk_kernel, unsigned(g), 32, size_t(kScStages) * kScPiece,
+                             s, static_cast<const uint8_t*>(in), N, int64_t(row_b), split_sizes,
+                             sorted_idxs, C, static_cast<uint8_t*>(out), header,
+                             device_status_word()) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        return MOE_OK;
+    }
     const ChunkPlan plan = chunk_plan(workspace, C);
     sort_chunks_prep_kernel<<<1, kPrepThreads, 0, s>>>(split_sizes, sorted_idxs, C, N, plan,
                                                       header);

@@ -34,28 +34,6 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kTokensPerWarp = kTokensPerBlock / kWarps;   // R3: 8 tokens per warp
 constexpr uint32_t kFull = 0xFFFFFFFFu;
 
-// Programmatic dependent launch: the kernel may start while its predecessor
-// in the stream is finishing; it must call wait_for_predecessor() before it
-// touches anything the predecessor writes.
-__device__ __forceinline__ void wait_for_predecessor() {
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-}
-
-template <typename... KArgs, typename... Args>
-cudaError_t launch_dependent(void (*kernel)(KArgs...), unsigned grid, unsigned block, size_t smem,
-                             cudaStream_t stream, Args... args) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(block);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
-}
 
 __host__ __device__ inline int64_t num_blocks(int64_t T) {
     return (T + kTokensPerBlock - 1) / kTokensPerBlock;
