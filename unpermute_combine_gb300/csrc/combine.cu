@@ -30,12 +30,16 @@ constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr uint32_t kFull = 0xFFFFFFFFu;
 
-int grid_for(const void* kernel, int threads, int64_t work_blocks) {
+int grid_for(const void* kernel, int threads, size_t smem, int64_t work_blocks) {
     int per_sm = 0;
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, 0);
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem);
     if (per_sm < 1) per_sm = 1;
     const int64_t cap = int64_t(sm_count()) * per_sm;
     return int(work_blocks < cap ? (work_blocks > 0 ? work_blocks : 1) : cap);
+}
+
+int grid_for(const void* kernel, int threads, int64_t work_blocks) {
+    return grid_for(kernel, threads, 0, work_blocks);
 }
 
 // Float error bound factor for a k-term FMA chain, rounded up (see header).
@@ -122,6 +126,21 @@ __device__ __forceinline__ uint32_t plus_zero_bf16x2(uint32_t r) {
     if ((r & 0xFFFFu) == 0x8000u) r &= 0xFFFF0000u;
     if ((r >> 16) == 0x8000u) r &= 0x0000FFFFu;
     return r;
+}
+
+constexpr int kBwdStages = 3;
+
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;"
+                 :: "r"(static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst))), "l"(gsrc)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory");
 }
 
 // -------------------------------------------------------- combine, bf16 rows
@@ -224,7 +243,8 @@ __device__ __forceinline__ bool dd_sum_bf16(const float* w, const float* y, cons
 
 // k <= 8: one 16-byte column per lane step with every slot row of it held in
 // registers, so an element whose rounding cannot be certified is recomputed
-// in double from the same registers (no reload).
+// in double from the same registers (no reload).  (A cp.async ring as in
+// the backward measured slower here: 352 vs 345 us at T=16384, H=7168, k=8.)
 template <int KMAX>
 __global__ void __launch_bounds__(kThreads)
 combine_bf16_regs_kernel(const uint4* __restrict__ y, int64_t T, int64_t nvec, int k, int64_t n_rows,
@@ -477,10 +497,12 @@ __device__ __forceinline__ float dd_warp_sum(float hi, float lo) {
 }
 
 
-// k <= 8: every slot row of the current 16-byte column is loaded before any
-// arithmetic, so a lane keeps k loads in flight.  Two CTAs per SM (at most
-// 128 registers a thread) keep enough loads in flight to cover HBM latency;
-// one CTA per SM loses a third of the bandwidth.
+// k <= 8: one 16-byte column per lane step; the k slot rows and grad_out of
+// a step are fetched kBwdStages - 1 steps ahead into a per-warp shared-memory
+// ring with cp.async (16-byte LDGSTS), so the loads in flight do not occupy
+// registers.  Two CTAs per SM (at most 128 registers a thread).
+template <int KMAX>
+constexpr size_t bwd_ring_bytes() { return size_t(kWarps) * kBwdStages * (KMAX + 1) * 32 * 16; }
 template <int KMAX>
 __global__ void __launch_bounds__(kThreads, 2)
 combine_bwd_bf16_vec_kernel(const uint4* __restrict__ gout, const uint4* __restrict__ y,
@@ -489,9 +511,11 @@ combine_bwd_bf16_vec_kernel(const uint4* __restrict__ gout, const uint4* __restr
                             const float* __restrict__ topk_w, uint4* __restrict__ gy,
                             float* __restrict__ grad_probs) {
     static_assert(KMAX <= 8, "packed accumulators for up to 8 slots");
+    extern __shared__ uint4 bwd_ring[];               // [kWarps][kBwdStages][KMAX + 1][32]
     __shared__ int32_t s_pos[kWarps][kMaxTopK];
     __shared__ float s_w[kWarps][kMaxTopK];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    uint4* ring = bwd_ring + warp * kBwdStages * (KMAX + 1) * 32;
     for (int64_t t = int64_t(blockIdx.x) * kWarps + warp; t < T;
          t += int64_t(gridDim.x) * kWarps) {
         stage_slots(s_pos[warp], s_w[warp], slot_pos, topk_w, t, k, n_rows, lane);
@@ -557,12 +581,35 @@ combine_bwd_bf16_vec_kernel(const uint4* __restrict__ gout, const uint4* __restr
             __syncwarp();
             continue;
         }
-        for (int64_t v = lane; v < nvec; v += 32) {
-            const uint4 gv = __ldcs(gout + t * nvec + v);
+        // software pipeline over this lane's column steps: the loads of step
+        // i + kBwdStages - 1 go to the warp's shared-memory ring (cp.async)
+        // while step i is computed, so the bytes in flight live in shared
+        // memory, not registers; each lane reads back only its own copies
+        const int64_t nsteps = (nvec + 31) / 32;
+        auto issue = [&](int64_t i) {
+            const int64_t v = lane + 32 * i;
+            if (i < nsteps && v < nvec) {
+                uint4* st = ring + (i % kBwdStages) * (KMAX + 1) * 32;
+#pragma unroll
+                for (int j = 0; j < KMAX; ++j)
+                    if (pj[j] >= 0) cp_async16(st + j * 32 + lane, y + int64_t(pj[j]) * nvec + v);
+                cp_async16(st + KMAX * 32 + lane, gout + t * nvec + v);
+            }
+            cp_async_commit();
+        };
+#pragma unroll
+        for (int i = 0; i < kBwdStages - 1; ++i) issue(i);
+        for (int64_t i = 0; i < nsteps; ++i) {
+            issue(i + kBwdStages - 1);
+            cp_async_wait<kBwdStages - 1>();               // step i has landed
+            const int64_t v = lane + 32 * i;
+            if (v >= nvec) continue;
+            const uint4* st = ring + (i % kBwdStages) * (KMAX + 1) * 32;
+            const uint4 gv = st[KMAX * 32 + lane];
             uint4 yv[KMAX];
 #pragma unroll
             for (int j = 0; j < KMAX; ++j)
-                yv[j] = pj[j] >= 0 ? __ldcs(y + int64_t(pj[j]) * nvec + v) : make_uint4(0, 0, 0, 0);
+                yv[j] = pj[j] >= 0 ? st[j * 32 + lane] : make_uint4(0, 0, 0, 0);
             const f2_t g0 = f2_from_bf16x2(gv.x), g1 = f2_from_bf16x2(gv.y);
             const f2_t g2 = f2_from_bf16x2(gv.z), g3 = f2_from_bf16x2(gv.w);
 #pragma unroll
@@ -581,6 +628,7 @@ combine_bwd_bf16_vec_kernel(const uint4* __restrict__ gout, const uint4* __restr
                 f2_two_sum_acc(hi[j], lo[j], f2_mul(g3, f2_from_bf16x2(yv[j].w)));
             }
         }
+        cp_async_wait<0>();
 #pragma unroll
         for (int j = 0; j < KMAX; ++j) {
             if (j >= k) break;
@@ -665,8 +713,18 @@ void launch_bwd(const void* gout, const void* y, moe_dtype_t dtype, int64_t T, i
                 bool vec, cudaStream_t s) {
     const int64_t want = (T + kWarps - 1) / kWarps;
     if (vec && KMAX <= 8) {
-        const auto kern = combine_bwd_bf16_vec_kernel<(KMAX <= 8 ? KMAX : 8)>;
-        kern<<<grid_for((const void*)kern, kThreads, want), kThreads, 0, s>>>(
+        constexpr int KV = KMAX <= 8 ? KMAX : 8;
+        const auto kern = combine_bwd_bf16_vec_kernel<KV>;
+        constexpr size_t smem = bwd_ring_bytes<KV>();
+        static bool attr_set[64] = {};
+        int dev = 0;
+        cudaGetDevice(&dev);
+        if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+            cudaFuncSetAttribute((const void*)kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 int(smem));
+            attr_set[dev] = true;
+        }
+        kern<<<grid_for((const void*)kern, kThreads, smem, want), kThreads, smem, s>>>(
             static_cast<const uint4*>(gout), static_cast<const uint4*>(y), T, H / 8, k, n_rows,
             slot_pos, topk_w, static_cast<uint4*>(gy), gp);
     } else if (dtype == MOE_F32) {
