@@ -283,6 +283,7 @@ def run_ours(args, rank, world, local_rank):
     rows = (moe.moe_route_layout_rows(T, E, k, cap, lay.get("pad", False), lay.get("align", 1))
             if lay else N)
     stream = torch.cuda.Stream(device=dev)
+    gp = None
     with torch.cuda.stream(stream):
         r = moe.moe_route(logits, k)
         rl = (moe.moe_route_layout(r.topk_idx, r.topk_w, E, capacity=cap, pad=lay.get("pad", False),
@@ -334,7 +335,9 @@ def run_ours(args, rank, world, local_rank):
         with torch.cuda.stream(stream):
             gl = torch.empty((T, E), dtype=torch.float32, device=dev)
 
-    def step(lg, xx, gg, ev=None):
+    def step(lg, xx, gg, ev=None, ob=None):
+        # ob: (out, grad_probs) buffers of this step's results (default: the shared ones)
+        o_out, o_gp = ob if ob is not None else (out, gp)
         n_marks = [0]
 
         def mark():
@@ -370,10 +373,10 @@ def run_ours(args, rank, world, local_rank):
             moe.moe_grouped_swiglu_save(xp, up_p, down_p, rr.offsets, out=y, hidden=hid,
                                         gate_up=gu, workspace=gs_ws, stream=stream)
             mark()
-            moe.moe_combine(y, rr.slot_pos, r.topk_w, out=out, stream=stream)
+            moe.moe_combine(y, rr.slot_pos, r.topk_w, out=o_out, stream=stream)
             mark()
             moe.moe_combine_backward(gg, y, rr.slot_pos, r.topk_w, grad_expert_out=gy,
-                                     grad_probs=gp, stream=stream)
+                                     grad_probs=o_gp, stream=stream)
             mark()
             moe.moe_grouped_swiglu_dgrad(gy, w_up_d, w_down_d, rr.offsets, gu, dgate_up=dgu,
                                          dx=dxp, workspace=ws_d, stream=stream)
@@ -383,20 +386,20 @@ def run_ours(args, rank, world, local_rank):
             mark()
             moe.moe_combine(dxp, rr.slot_pos, None, out=gx, stream=stream)   # permute backward
             mark()
-            moe.moe_route_backward(r.topk_idx, r.topk_w, gp, E, out=gl, stream=stream)
+            moe.moe_route_backward(r.topk_idx, r.topk_w, o_gp, E, out=gl, stream=stream)
         elif layer:
             moe.moe_grouped_swiglu(xp, up_p, down_p, rr.offsets, out=y, workspace=gs_ws,
                                    stream=stream)
             mark()
-            moe.moe_combine(y, rr.slot_pos, r.topk_w, out=out, stream=stream)
+            moe.moe_combine(y, rr.slot_pos, r.topk_w, out=o_out, stream=stream)
         else:
-            moe.moe_combine(xp, rr.slot_pos, r.topk_w, out=out, stream=stream)
+            moe.moe_combine(xp, rr.slot_pos, r.topk_w, out=o_out, stream=stream)
             mark()
             moe.moe_combine_backward(gg, xp, rr.slot_pos, r.topk_w, grad_expert_out=gy,
-                                     grad_probs=gp, stream=stream)
+                                     grad_probs=o_gp, stream=stream)
             if router_bwd:
                 mark()
-                moe.moe_route_backward(r.topk_idx, r.topk_w, gp, E, out=gl, stream=stream)
+                moe.moe_route_backward(r.topk_idx, r.topk_w, o_gp, E, out=gl, stream=stream)
         mark()
 
     import torch.distributed as dist
@@ -435,34 +438,57 @@ def run_ours(args, rank, world, local_rank):
     if lay:
         assert moe.moe_workspace_status(rl.workspace, stream) == 0, "layout ran out of rows"
 
-    # -------- end to end through the public API from pinned host buffers
-    h_out = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
-    h_gp = torch.empty((T, k), dtype=torch.float32).pin_memory() if has_grad else None
+    # -------- end to end through the public API from pinned host buffers:
+    # every step copies its inputs host -> device and its results device ->
+    # host inside the timed region; steps are pipelined over two buffer sets
+    # (inputs on one copy stream, the step on its own stream, results on a
+    # third), so the copies of step i+1 and i-1 overlap the kernels of step i
+    n_sets = 2
+    h_out = [torch.empty((T, H), dtype=torch.bfloat16).pin_memory() for _ in range(n_sets)]
+    h_gp = ([torch.empty((T, k), dtype=torch.float32).pin_memory() for _ in range(n_sets)]
+            if has_grad else [None] * n_sets)
     h2d = h_logits.numel() * 4 + h_x.numel() * 2 + (h_g.numel() * 2 if has_grad else 0)
-    d2h = h_out.numel() * 2 + (h_gp.numel() * 4 if has_grad else 0)
+    d2h = h_out[0].numel() * 2 + (h_gp[0].numel() * 4 if has_grad else 0)
     e2e_steps = 0 if args.no_e2e else max(1, min(args.steps, 20))
-
-    def e2e_step():
-        with torch.cuda.stream(stream):
-            lg = h_logits.to(dev, non_blocking=True)
-            xx = h_x.to(dev, non_blocking=True)
-            gg = h_g.to(dev, non_blocking=True) if has_grad else None
-        step(lg, xx, gg)
-        with torch.cuda.stream(stream):
-            h_out.copy_(out, non_blocking=True)
-            if has_grad:
-                h_gp.copy_(gp, non_blocking=True)
-
     e2e_elapsed = float("nan")
     if e2e_steps:
-        for _ in range(2):
-            e2e_step()
+        with torch.cuda.stream(stream):
+            d_in = [(torch.empty_like(logits), torch.empty_like(x),
+                     torch.empty_like(g) if has_grad else None) for _ in range(n_sets)]
+            d_out = [(torch.empty_like(out), torch.empty_like(gp) if has_grad else None)
+                     for _ in range(n_sets)]
+        s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+        ev_in = [torch.cuda.Event() for _ in range(n_sets)]
+        ev_comp = [torch.cuda.Event() for _ in range(n_sets)]
+        ev_out = [torch.cuda.Event() for _ in range(n_sets)]
+
+        def e2e_step(i):
+            b = i % n_sets
+            s_in.wait_event(ev_comp[b])              # step i-2 has read this input set
+            with torch.cuda.stream(s_in):
+                for dst, src in zip(d_in[b], (h_logits, h_x, h_g)):
+                    if dst is not None:
+                        dst.copy_(src, non_blocking=True)
+            ev_in[b].record(s_in)
+            stream.wait_event(ev_in[b])
+            stream.wait_event(ev_out[b])             # step i-2's results have left this set
+            step(*d_in[b], ob=d_out[b])
+            ev_comp[b].record(stream)
+            s_out.wait_event(ev_comp[b])
+            with torch.cuda.stream(s_out):
+                h_out[b].copy_(d_out[b][0], non_blocking=True)
+                if has_grad:
+                    h_gp[b].copy_(d_out[b][1], non_blocking=True)
+            ev_out[b].record(s_out)
+
+        for i in range(2):
+            e2e_step(i)
         barrier()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(e2e_steps):
-            e2e_step()
-        e1.record(stream)
+        e0.record(s_in)
+        for i in range(e2e_steps):
+            e2e_step(i)
+        e1.record(s_out)
         barrier()
         e2e_elapsed = reduce_max(e0.elapsed_time(e1) / 1e3, dev)
 
@@ -568,7 +594,8 @@ def run_ours(args, rank, world, local_rank):
         "permute_combine_routed_tokens_per_s": N / pc_time,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps,
-                "path": "pinned host inputs -> device -> step -> outputs to host"},
+                "path": "pinned host inputs -> device -> step -> outputs to host, steps "
+                        "pipelined over two buffer sets on three streams"},
         "gpu_launches": launches * args.steps,
         "clocks": clk.summary(),
     }
@@ -636,16 +663,17 @@ def run_vep8(args, rank, world, local_rank):
     N = sum(int(q["buf"].shape[0]) for q in ranks)
     names = ["sort_chunks", "sort_chunks_inverse"]
 
-    def step(ev=None, bufs=None):
+    def step(ev=None, bufs=None, ems=None):
+        ems = ems or [q["em"] for q in ranks]
         if ev is not None:
             ev[0].record(stream)
-        for q, src in zip(ranks, bufs or [q["buf"] for q in ranks]):
-            moe.moe_sort_chunks(src, q["sp"], fwd_idx, out=q["em"], workspace=q["ws_f"],
+        for q, src, em in zip(ranks, bufs or [q["buf"] for q in ranks], ems):
+            moe.moe_sort_chunks(src, q["sp"], fwd_idx, out=em, workspace=q["ws_f"],
                                 stream=stream)
         if ev is not None:
             ev[1].record(stream)
-        for q in ranks:
-            moe.moe_sort_chunks(q["em"], q["spt"], inv_idx, out=q["back"], workspace=q["ws_b"],
+        for q, em in zip(ranks, ems):
+            moe.moe_sort_chunks(em, q["spt"], inv_idx, out=q["back"], workspace=q["ws_b"],
                                 stream=stream)
         if ev is not None:
             ev[2].record(stream)
@@ -680,31 +708,47 @@ def run_vep8(args, rank, world, local_rank):
     max_elapsed = reduce_max(elapsed, dev)
 
     # end to end: the rank-major buffers from pinned host memory, the step,
-    # the expert-major buffers back to the host
+    # the expert-major buffers back to the host, pipelined over two buffer
+    # sets on three streams like the main step's end-to-end leg
+    n_sets = 2
     h_in = [q["buf"].cpu().pin_memory() for q in ranks]
-    h_out = [torch.empty_like(q["buf"], device="cpu").pin_memory() for q in ranks]
-    d_in = [torch.empty_like(q["buf"]) for q in ranks]
+    h_out = [[torch.empty_like(q["buf"], device="cpu").pin_memory() for q in ranks]
+             for _ in range(n_sets)]
     e2e_steps = 0 if args.no_e2e else max(1, min(args.steps, 20))
-
-    def e2e_step():
-        with torch.cuda.stream(stream):
-            for hi, di in zip(h_in, d_in):
-                di.copy_(hi, non_blocking=True)
-        step(bufs=d_in)
-        with torch.cuda.stream(stream):
-            for ho, q in zip(h_out, ranks):
-                ho.copy_(q["em"], non_blocking=True)
-
     e2e_value = None
     if e2e_steps:
-        for _ in range(2):
-            e2e_step()
+        d_in = [[torch.empty_like(q["buf"]) for q in ranks] for _ in range(n_sets)]
+        d_em = [[torch.empty_like(q["buf"]) for q in ranks] for _ in range(n_sets)]
+        s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+        ev_in = [torch.cuda.Event() for _ in range(n_sets)]
+        ev_comp = [torch.cuda.Event() for _ in range(n_sets)]
+        ev_out = [torch.cuda.Event() for _ in range(n_sets)]
+
+        def e2e_step(i):
+            b = i % n_sets
+            s_in.wait_event(ev_comp[b])
+            with torch.cuda.stream(s_in):
+                for hi, di in zip(h_in, d_in[b]):
+                    di.copy_(hi, non_blocking=True)
+            ev_in[b].record(s_in)
+            stream.wait_event(ev_in[b])
+            stream.wait_event(ev_out[b])
+            step(bufs=d_in[b], ems=d_em[b])
+            ev_comp[b].record(stream)
+            s_out.wait_event(ev_comp[b])
+            with torch.cuda.stream(s_out):
+                for ho, em in zip(h_out[b], d_em[b]):
+                    ho.copy_(em, non_blocking=True)
+            ev_out[b].record(s_out)
+
+        for i in range(2):
+            e2e_step(i)
         barrier()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(e2e_steps):
-            e2e_step()
-        e1.record(stream)
+        e0.record(s_in)
+        for i in range(e2e_steps):
+            e2e_step(i)
+        e1.record(s_out)
         barrier()
         e2e_value = job_value(N, world, e2e_steps, reduce_max(e0.elapsed_time(e1) / 1e3, dev))
     if rank != 0:
@@ -738,7 +782,8 @@ def run_vep8(args, rank, world, local_rank):
         "kernels": kern,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": io,
                 "d2h_bytes_per_step": io, "steps": e2e_steps,
-                "path": "pinned rank-major buffers -> device -> step -> expert-major to host"},
+                "path": "pinned rank-major buffers -> device -> step -> expert-major to host, "
+                        "steps pipelined over two buffer sets on three streams"},
         "gpu_launches": 2 * R * args.steps,              # one fused launch per call (C <= 1024)
         "clocks": clk.summary(),
     }
