@@ -50,15 +50,15 @@ def test_layout_matches_oracle(T, E, k, cap, pad, align, drop):
 def test_layout_skewed_routing_capacity():
     d = wl.make("skewed")
     W = d["workload"]
-    r0 = moe.moe_route(to_dev(d["logits"]), W.k)
     cap = moe.moe_expert_capacity(W.T, W.k, W.E, 1.25)
     assert cap == oracle.expert_capacity(W.T, W.k, W.E, 1.25)
-    r, o, rows = None, None, None
     rows = moe.moe_route_layout_rows(W.T, W.E, W.k, cap, True, 1)
-    r = moe.moe_route_layout(r0.topk_idx, r0.topk_w, W.E, capacity=cap, pad=True, max_rows=rows)
-    torch.cuda.synchronize()
+    # the oracle's routing of the DeepSeek-shaped logits, given to both sides
     oi = oracle.route(d["logits"], W.k)
-    o = oracle.route_layout(oi["topk_idx"], to_host(r0.topk_w), W.E, capacity=cap, pad=True,
+    r = moe.moe_route_layout(to_dev(oi["topk_idx"]), to_dev(oi["topk_w"]), W.E, capacity=cap,
+                             pad=True, max_rows=rows)
+    torch.cuda.synchronize()
+    o = oracle.route_layout(oi["topk_idx"], oi["topk_w"], W.E, capacity=cap, pad=True,
                             max_rows=rows)
     for name in ("counts", "offsets", "sorted_indices", "slot_pos", "permuted_probs"):
         assert (to_host(getattr(r, name)) == o[name]).all(), name

@@ -426,16 +426,18 @@ def test_sort_chunks_rejects_bad_splits_on_device():
 
 # ------------------------------------------------------------------ pipelines
 
-def _pipeline_gpu(d, with_grad):
+def _pipeline_gpu(d, with_grad, weights=None):
+    """The GPU chain; `weights` (host, [T,k]) replaces the route's own topk_w
+    in the combine and backward, so they see the same inputs as the oracle."""
     w_ = d["workload"]
     r = moe.moe_route(to_dev(d["logits"]), w_.k)
+    w = r.topk_w if weights is None else to_dev(weights)
     xp = moe.moe_permute(to_dev(d["x"]), r.slot_pos)
     y = moe.moe_expert_scale(xp, r.offsets, to_dev(d["scale"]))
-    out = moe.moe_combine(y, r.slot_pos, r.topk_w)
+    out = moe.moe_combine(y, r.slot_pos, w)
     res = {"r": r, "xp": xp, "y": y, "out": out}
     if with_grad:
-        res["gy"], res["gp"] = moe.moe_combine_backward(to_dev(d["grad_out"]), y, r.slot_pos,
-                                                        r.topk_w)
+        res["gy"], res["gp"] = moe.moe_combine_backward(to_dev(d["grad_out"]), y, r.slot_pos, w)
     torch.cuda.synchronize()
     return res
 
@@ -474,8 +476,10 @@ def test_pipeline_skewed_sampled():
     of tokens for the row outputs."""
     d = wl.make("skewed", with_grad=True)
     w_ = d["workload"]
-    g = _pipeline_gpu(d, with_grad=True)
     o = oracle.route(d["logits"], w_.k)
+    # the combine and backward take the oracle's weights: identical inputs on
+    # both sides (the route's own weights are checked within 1e-6 above)
+    g = _pipeline_gpu(d, with_grad=True, weights=o["topk_w"])
     _assert_route_equal(g["r"], o, w_.E)
     counts = o["counts"]
     assert (counts == 0).sum() > 0 and counts.max() > 4 * w_.N / w_.E   # skewed as intended
@@ -486,13 +490,18 @@ def test_pipeline_skewed_sampled():
     rows = sp.ravel()
     xp = to_host(g["xp"][torch.from_numpy(rows).long().cuda()])
     assert (xp == d["x"][np.repeat(toks, w_.k)]).all()
-    y_rows = to_host(g["y"])                      # whole buffer, host copy
-    w_gpu = to_host(g["r"].topk_w)[toks]
-    # combine on the sampled tokens: same y and weights as the GPU used -> bit-exact
+    # the oracle's stand-in rows for the sample: each row its own segment,
+    # scaled by its expert's factor
+    experts = np.searchsorted(o["offsets"], rows, side="right") - 1
+    y_o = oracle.expert_scale(np.ascontiguousarray(d["x"][np.repeat(toks, w_.k)]),
+                              np.arange(rows.size + 1, dtype=np.int32),
+                              np.ascontiguousarray(d["scale"][experts]))
+    assert (to_host(g["y"][torch.from_numpy(rows).long().cuda()]) == y_o).all()
+    w_o = np.ascontiguousarray(o["topk_w"][toks])
     sp_local = np.arange(toks.size * w_.k, dtype=np.int32).reshape(toks.size, w_.k)
-    out_o, _ = oracle.combine(np.ascontiguousarray(y_rows[rows]), sp_local, w_gpu)
+    out_o, _ = oracle.combine(y_o, sp_local, w_o)
     assert (to_host(g["out"])[toks] == out_o).all()
-    gy_o, gp_o, gp64 = oracle.combine_backward(np.ascontiguousarray(d["grad_out"][toks]),
-                                               np.ascontiguousarray(y_rows[rows]), sp_local, w_gpu)
+    gy_o, gp_o, gp64 = oracle.combine_backward(np.ascontiguousarray(d["grad_out"][toks]), y_o,
+                                               sp_local, w_o)
     assert (to_host(g["gy"][torch.from_numpy(rows).long().cuda()]) == gy_o).all()
     assert within_one_bf16_ulp(to_host(g["gp"])[toks], gp64).all()

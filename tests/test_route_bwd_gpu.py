@@ -33,8 +33,7 @@ def _both(idx, w, g, E):
 def test_route_backward_on_routed_workloads(name):
     d = wl.make(name)
     W = d["workload"]
-    r = moe.moe_route(to_dev(d["logits"]), W.k)
-    idx, w = to_host(r.topk_idx), to_host(r.topk_w)
+    idx, w, _ = oracle.topk_softmax(d["logits"], W.k)      # the workload's routing
     g = np.random.default_rng(len(name)).standard_normal((W.T, W.k)).astype(np.float32)
     got, exp = _both(idx, w, g, W.E)
     assert got.view(np.uint32).tobytes() == exp.view(np.uint32).tobytes()
@@ -53,14 +52,17 @@ def test_route_backward_edge_shapes(T, E, k, empty):
 
 
 def test_route_backward_after_the_combine_backward():
-    """The grad_probs a real backward produces, on the DeepSeek-shaped routing."""
+    """grad_probs as a backward produces them (the oracle's own chain on the
+    DeepSeek-shaped routing), given to both sides."""
     d = wl.make("skewed", T=2048, with_grad=True)
     W = d["workload"]
-    r = moe.moe_route(to_dev(d["logits"]), W.k)
-    xp = moe.moe_permute(to_dev(d["x"]), r.slot_pos)
-    _, gp = moe.moe_combine_backward(to_dev(d["grad_out"]), xp, r.slot_pos, r.topk_w)
-    gl = to_host(moe.moe_route_backward(r.topk_idx, r.topk_w, gp, W.E))
-    exp = oracle.route_backward(to_host(r.topk_idx), to_host(r.topk_w), to_host(gp), W.E)
+    o = oracle.route(d["logits"], W.k)
+    n = int(o["offsets"][W.E])
+    xp = oracle.permute(d["x"], o["sorted_indices"], n)
+    _, gp, _ = oracle.combine_backward(d["grad_out"], xp, o["slot_pos"], o["topk_w"])
+    gl = to_host(moe.moe_route_backward(to_dev(o["topk_idx"]), to_dev(o["topk_w"]), to_dev(gp),
+                                        W.E))
+    exp = oracle.route_backward(o["topk_idx"], o["topk_w"], gp, W.E)
     assert gl.view(np.uint32).tobytes() == exp.view(np.uint32).tobytes()
 
 

@@ -156,7 +156,9 @@ def test_layer_workload_training_path():
     d = wl.make("layer", with_weights=True)
     W = d["workload"]
     r = moe.moe_route(to_dev(d["logits"]), W.k)
-    off = to_host(r.offsets)
+    o = oracle.route(d["logits"], W.k)
+    off = o["offsets"]
+    assert (to_host(r.offsets) == off).all()                # same row layout on both sides
     N = int(off[-1])
     xp = moe.moe_permute(to_dev(d["x"]), r.slot_pos)
     up, down = to_dev(d["w_up"]), to_dev(d["w_down"])
@@ -169,10 +171,11 @@ def test_layer_workload_training_path():
     torch.cuda.synchronize()
     for t in (y, dx, dw_up):
         assert moe.moe_workspace_status(t._moe_workspace) == 0
+    x_o = oracle.permute(d["x"], o["sorted_indices"], N)     # the oracle's expert input
     x_h = to_host(xp)
     rows = np.random.default_rng(10).choice(N, 48, replace=False)
     rows = np.concatenate([rows, off[1:-1][off[1:-1] < N][:8], [N - 1]]).astype(np.int64)
-    _, y64, gu_o, hid_o = oracle.grouped_swiglu(x_h, d["w_up"], d["w_down"], off, rows=rows,
+    _, y64, gu_o, hid_o = oracle.grouped_swiglu(x_o, d["w_up"], d["w_down"], off, rows=rows,
                                                 save=True)
     _bf16_close(to_host(gu)[rows], _f(gu_o[rows]), "gate_up", rel=2.0 ** -7)
     # y from the GPU's own hidden: each hidden may sit one bf16 ulp from the
