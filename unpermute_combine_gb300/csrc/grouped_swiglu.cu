@@ -164,9 +164,8 @@ __device__ __forceinline__ void store_bf16x32(uint16_t* dst, const float* a) {
     }
 }
 
-// 32 bf16 (16-byte aligned) -> floats
-__device__ __forceinline__ void load_bf16x32(const uint16_t* src, float* a) {
-    const uint4* s = reinterpret_cast<const uint4*>(src);
+// 32 bf16 held as four 16-byte words -> floats
+__device__ __forceinline__ void unpack_bf16x32(const uint4* s, float* a) {
 #pragma unroll
     for (int v = 0; v < 4; ++v) {
         const uint4 w = s[v];
@@ -303,16 +302,32 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
         uint32_t tile_iter = 0;
         for (int t = blockIdx.x; t < total_tiles; t += gridDim.x, ++tile_iter) {
             const uint32_t buf = tile_iter & 1u, use = tile_iter >> 1;
+            int e, m, n;
+            tile_coords(t, s_tile_start, s_mt, E, args.n_tiles, e, m, n);
+            const int64_t row = int64_t(s_row0[e]) + m * BM + q * 32 + lane;
+            const bool row_ok = row < s_row0[e + 1];
+            // kSwigluBwd: the first chunk's stored gate/up, fetched while the
+            // accumulator is still being computed
+            uint4 cg[4], cu[4];
+            int nchunks = 0;
+            if (EPI == kSwigluBwd) {
+                const int64_t left = args.valid_cols - int64_t(n) * BN;
+                nchunks = int((left < BN ? left : BN) / 32);
+                if (row_ok && nchunks > 0) {
+                    const uint4* gp = reinterpret_cast<const uint4*>(
+                        args.gate_up + row * 2 * args.I + int64_t(n) * BN);
+                    const uint4* up = reinterpret_cast<const uint4*>(
+                        args.gate_up + row * 2 * args.I + args.I + int64_t(n) * BN);
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) { cg[v] = gp[v]; cu[v] = up[v]; }
+                }
+            }
             if (s_failed || !mbar_wait(smem_addr(&tmem_full_bar[buf]), use & 1u)) {
                 s_failed = 1;
                 break;
             }
             tc_fence_after();
             const uint32_t tmem_acc = tmem_base + buf * BN;
-            int e, m, n;
-            tile_coords(t, s_tile_start, s_mt, E, args.n_tiles, e, m, n);
-            const int64_t row = int64_t(s_row0[e]) + m * BM + q * 32 + lane;
-            const bool row_ok = row < s_row0[e + 1];
             uint16_t* out = static_cast<uint16_t*>(args.out);
             if (EPI == kSwiglu || EPI == kSwigluSave) {
                 // columns [0,128) gate, [128,256) up, for hidden j0 = n*128
@@ -336,18 +351,27 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                 }
             } else if (EPI == kSwigluBwd) {
                 // accumulator columns = hidden columns j = n*BN + c (< I):
-                // d_up = dh*silu(g), d_gate = dh*u*s*(1 + g*(1-s)), s = sigmoid(g)
+                // d_up = dh*silu(g), d_gate = dh*u*s*(1 + g*(1-s)), s = sigmoid(g);
+                // the stored gate/up of chunk c+1 load while chunk c is computed
 #pragma unroll 1
-                for (int c = 0; c < BN; c += 32) {
+                for (int ci = 0; ci < nchunks; ++ci) {
+                    const int c = ci * 32;
                     const int64_t j = int64_t(n) * BN + c;
-                    if (j >= args.valid_cols) break;              // uniform over the warp
+                    uint4 ng[4], nu[4];
+                    if (row_ok && ci + 1 < nchunks) {
+                        const uint4* gp = reinterpret_cast<const uint4*>(
+                            args.gate_up + row * 2 * args.I + j + 32);
+                        const uint4* up = reinterpret_cast<const uint4*>(
+                            args.gate_up + row * 2 * args.I + args.I + j + 32);
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) { ng[v] = gp[v]; nu[v] = up[v]; }
+                    }
                     float dh[32];
                     tmem_ld32(tmem_acc + lane_base + c, dh);
                     if (row_ok) {
-                        const uint16_t* gu = args.gate_up + row * 2 * args.I;
                         float g[32], u[32], dg[32], du[32];
-                        load_bf16x32(gu + j, g);
-                        load_bf16x32(gu + args.I + j, u);
+                        unpack_bf16x32(cg, g);
+                        unpack_bf16x32(cu, u);
 #pragma unroll
                         for (int i = 0; i < 32; ++i) {
                             const float sg = __fdividef(1.0f, 1.0f + __expf(-g[i]));
@@ -358,6 +382,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                         store_bf16x32(o + j, dg);
                         store_bf16x32(o + args.I + j, du);
                     }
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) { cg[v] = ng[v]; cu[v] = nu[v]; }
                 }
             } else {
 #pragma unroll 1
