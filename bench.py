@@ -449,7 +449,7 @@ def run_ours(args, rank, world, local_rank):
             if has_grad else [None] * n_sets)
     h2d = h_logits.numel() * 4 + h_x.numel() * 2 + (h_g.numel() * 2 if has_grad else 0)
     d2h = h_out[0].numel() * 2 + (h_gp[0].numel() * 4 if has_grad else 0)
-    e2e_steps = 0 if args.no_e2e else max(1, min(args.steps, 20))
+    e2e_steps = 0 if args.no_e2e else max(1, min(args.steps, 50))
     e2e_elapsed = float("nan")
     if e2e_steps:
         with torch.cuda.stream(stream):
@@ -714,7 +714,7 @@ def run_vep8(args, rank, world, local_rank):
     h_in = [q["buf"].cpu().pin_memory() for q in ranks]
     h_out = [[torch.empty_like(q["buf"], device="cpu").pin_memory() for q in ranks]
              for _ in range(n_sets)]
-    e2e_steps = 0 if args.no_e2e else max(1, min(args.steps, 20))
+    e2e_steps = 0 if args.no_e2e else max(1, min(args.steps, 50))
     e2e_value = None
     if e2e_steps:
         d_in = [[torch.empty_like(q["buf"]) for q in ranks] for _ in range(n_sets)]

@@ -708,7 +708,7 @@ moe_status_t check_common(const void* a, const void* b, moe_dtype_t dtype, int64
 }
 
 template <int KMAX>
-void launch_bwd(const void* gout, const void* y, moe_dtype_t dtype, int64_t T, int64_t H, int k,
+moe_status_t launch_bwd(const void* gout, const void* y, moe_dtype_t dtype, int64_t T, int64_t H, int k,
                 int64_t n_rows, const int32_t* slot_pos, const float* topk_w, void* gy, float* gp,
                 bool vec, cudaStream_t s) {
     const int64_t want = (T + kWarps - 1) / kWarps;
@@ -716,14 +716,7 @@ void launch_bwd(const void* gout, const void* y, moe_dtype_t dtype, int64_t T, i
         constexpr int KV = KMAX <= 8 ? KMAX : 8;
         const auto kern = combine_bwd_bf16_vec_kernel<KV>;
         constexpr size_t smem = bwd_ring_bytes<KV>();
-        static bool attr_set[64] = {};
-        int dev = 0;
-        cudaGetDevice(&dev);
-        if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-            cudaFuncSetAttribute((const void*)kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 int(smem));
-            attr_set[dev] = true;
-        }
+        if (!opt_in_smem((const void*)kern, int(smem))) return MOE_ERR_CUDA;
         kern<<<grid_for((const void*)kern, kThreads, smem, want), kThreads, smem, s>>>(
             static_cast<const uint4*>(gout), static_cast<const uint4*>(y), T, H / 8, k, n_rows,
             slot_pos, topk_w, static_cast<uint4*>(gy), gp);
@@ -738,6 +731,7 @@ void launch_bwd(const void* gout, const void* y, moe_dtype_t dtype, int64_t T, i
             static_cast<const uint16_t*>(gout), static_cast<const uint16_t*>(y), T, H, k, n_rows,
             slot_pos, topk_w, static_cast<uint16_t*>(gy), gp);
     }
+    return launch_status();
 }
 
 }  // namespace
@@ -795,11 +789,10 @@ extern "C" moe_status_t moe_combine_backward(const void* grad_out, const void* e
     const size_t row = size_t(H) * elem_size(dtype);
     const bool vec = dtype == MOE_BF16 && row % 16 == 0 && aligned16(grad_out) &&
                      aligned16(expert_out) && aligned16(grad_expert_out);
-    if (k <= 1) launch_bwd<1>(grad_out, expert_out, dtype, T, H, k, n_rows, slot_pos, topk_w, grad_expert_out, grad_probs, vec, s);
-    else if (k <= 2) launch_bwd<2>(grad_out, expert_out, dtype, T, H, k, n_rows, slot_pos, topk_w, grad_expert_out, grad_probs, vec, s);
-    else if (k <= 4) launch_bwd<4>(grad_out, expert_out, dtype, T, H, k, n_rows, slot_pos, topk_w, grad_expert_out, grad_probs, vec, s);
-    else if (k <= 8) launch_bwd<8>(grad_out, expert_out, dtype, T, H, k, n_rows, slot_pos, topk_w, grad_expert_out, grad_probs, vec, s);
-    else if (k <= 16) launch_bwd<16>(grad_out, expert_out, dtype, T, H, k, n_rows, slot_pos, topk_w, grad_expert_out, grad_probs, vec, s);
-    else launch_bwd<32>(grad_out, expert_out, dtype, T, H, k, n_rows, slot_pos, topk_w, grad_expert_out, grad_probs, vec, s);
-    return launch_status();
+    if (k <= 1) return launch_bwd<1>(grad_out, expert_out, dtype, T, H, k, n_rows, slot_pos, topk_w, grad_expert_out, grad_probs, vec, s);
+    else if (k <= 2) return launch_bwd<2>(grad_out, expert_out, dtype, T, H, k, n_rows, slot_pos, topk_w, grad_expert_out, grad_probs, vec, s);
+    else if (k <= 4) return launch_bwd<4>(grad_out, expert_out, dtype, T, H, k, n_rows, slot_pos, topk_w, grad_expert_out, grad_probs, vec, s);
+    else if (k <= 8) return launch_bwd<8>(grad_out, expert_out, dtype, T, H, k, n_rows, slot_pos, topk_w, grad_expert_out, grad_probs, vec, s);
+    else if (k <= 16) return launch_bwd<16>(grad_out, expert_out, dtype, T, H, k, n_rows, slot_pos, topk_w, grad_expert_out, grad_probs, vec, s);
+    return launch_bwd<32>(grad_out, expert_out, dtype, T, H, k, n_rows, slot_pos, topk_w, grad_expert_out, grad_probs, vec, s);
 }

@@ -30,6 +30,10 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 // Number of SMs of the current device (cached per device id).
 int sm_count();
 
+// Raise a kernel's dynamic shared-memory limit to `bytes` on the current
+// device (once per device, kernel and size; safe from several host threads).
+bool opt_in_smem(const void* kernel, int bytes);
+
 // Launch-error check after a kernel launch.
 inline moe_status_t launch_status() {
     return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;

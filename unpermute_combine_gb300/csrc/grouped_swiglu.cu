@@ -773,27 +773,15 @@ bool make_out_map(CUtensorMap* map, float* base, int64_t rows, int64_t cols) {
               CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Opt every tensor-core kernel into kSmemBytes of dynamic shared memory, once
-// per device.
+// Opt every tensor-core kernel into its dynamic shared memory.
 bool smem_attrs_set() {
-    static bool done[64] = {};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
-    if (done[dev]) return true;
     const void* kernels[] = {(const void*)grouped_gemm_kernel<kPlain>,
                              (const void*)grouped_gemm_kernel<kSwiglu>,
                              (const void*)grouped_gemm_kernel<kSwigluSave>,
                              (const void*)grouped_gemm_kernel<kSwigluBwd>};
     for (const void* k : kernels)
-        if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
-            cudaSuccess)
-            return false;
-    if (cudaFuncSetAttribute((const void*)grouped_wgrad_kernel,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, kWgradSmemBytes) !=
-        cudaSuccess)
-        return false;
-    done[dev] = true;
-    return true;
+        if (!opt_in_smem(k, kSmemBytes)) return false;
+    return opt_in_smem((const void*)grouped_wgrad_kernel, kWgradSmemBytes);
 }
 
 // The status header a call resets and its kernels report into.

@@ -506,26 +506,21 @@ fill_pad_rows_kernel(V* __restrict__ rows, int64_t max_rows, int64_t nvec,
 
 // Rows of row_bytes (a multiple of 16, 16-byte aligned buffers) plus an
 // optional side row of side_bytes (a multiple of 16, at most kSideMax).
-void launch_permute_bulk(const void* x, int64_t T, size_t row, int k, int64_t n_rows,
+bool launch_permute_bulk(const void* x, int64_t T, size_t row, int k, int64_t n_rows,
                          const int32_t* slot_pos, void* out, const void* side, size_t side_bytes,
                          void* side_out, cudaStream_t s) {
     const int pieces = int((row + kPieceMax - 1) / kPieceMax);
     const int piece = int(((row + pieces - 1) / pieces + 15) / 16 * 16);
     const size_t smem = size_t(kPermStages) * (size_t(piece) + side_bytes);
-    static bool attr_set[64] = {};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-        cudaFuncSetAttribute(permute_bulk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kPermStages * (kPieceMax + kSideMax));
-        attr_set[dev] = true;
-    }
+    if (!opt_in_smem((const void*)permute_bulk_kernel, kPermStages * (kPieceMax + kSideMax)))
+        return false;
     const int64_t items = T * pieces;
     const int g = int(min64(items, int64_t(sm_count()) * 4));
     permute_bulk_kernel<<<g, 32, smem, s>>>(
         static_cast<const uint8_t*>(x), T, int64_t(row), piece, pieces, k, n_rows, slot_pos,
         static_cast<uint8_t*>(out), static_cast<const uint8_t*>(side), uint32_t(side_bytes),
         static_cast<uint8_t*>(side_out), device_status_word());
+    return true;
 }
 
 }  // namespace
@@ -548,7 +543,9 @@ extern "C" moe_status_t moe_permute_fp8(const void* x_q, const float* scales, in
     const size_t row = size_t(H), side = size_t(H / block) * sizeof(float);
     if (row % 16 == 0 && side % 16 == 0 && side <= size_t(kSideMax) && aligned16(x_q) &&
         aligned16(out_q) && aligned16(scales) && aligned16(out_scales)) {
-        launch_permute_bulk(x_q, T, row, k, n_rows, slot_pos, out_q, scales, side, out_scales, s);
+        if (!launch_permute_bulk(x_q, T, row, k, n_rows, slot_pos, out_q, scales, side,
+                                 out_scales, s))
+            return MOE_ERR_CUDA;
         return launch_status();
     }
     // rows the bulk path cannot take: the two row sets one after the other
@@ -570,7 +567,8 @@ extern "C" moe_status_t moe_permute(const void* x, moe_dtype_t dtype, int64_t T,
     const size_t row = size_t(H) * elem_size(dtype);
     const int64_t blocks = (T + kWarps - 1) / kWarps;
     if (row % 16 == 0 && aligned16(x) && aligned16(out)) {
-        launch_permute_bulk(x, T, row, k, n_rows, slot_pos, out, nullptr, 0, nullptr, s);
+        if (!launch_permute_bulk(x, T, row, k, n_rows, slot_pos, out, nullptr, 0, nullptr, s))
+            return MOE_ERR_CUDA;
     } else if (dtype == MOE_F32) {
         const int g = grid_for((const void*)permute_kernel<float>, kThreads, 0, blocks);
         permute_kernel<float><<<g, kThreads, 0, s>>>(
@@ -609,16 +607,8 @@ extern "C" moe_status_t moe_sort_chunks(const void* in, moe_dtype_t dtype, int64
     WsHeader* header = static_cast<WsHeader*>(workspace);
     const size_t row_b = size_t(H) * elem_size(dtype);
     if (C <= kFusedChunks && row_b % 16 == 0 && (N == 0 || H == 0 || (aligned16(in) && aligned16(out)))) {
-        static bool attr_set[64] = {};
-        int dev = 0;
-        cudaGetDevice(&dev);
-        if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-            if (cudaFuncSetAttribute(sort_chunks_bulk_kernel,
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     kScStages * kScPiece) != cudaSuccess)
-                return MOE_ERR_CUDA;
-            attr_set[dev] = true;
-        }
+        if (!opt_in_smem((const void*)sort_chunks_bulk_kernel, kScStages * kScPiece))
+            return MOE_ERR_CUDA;
         const int64_t pieces = (N * int64_t(row_b) + kScPiece - 1) / kScPiece + C;
         const int g = int(max64(1, min64(pieces, int64_t(sm_count()) * 3)));
         if (launch_dependent(sort_chunks_bulk_kernel, unsigned(g), 32, size_t(kScStages) * kScPiece,

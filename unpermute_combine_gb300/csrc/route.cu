@@ -560,18 +560,10 @@ moe_status_t finish_route(const int32_t* topk_idx, const float* topk_w, int64_t 
                                    B, E, header) != cudaSuccess)
         return MOE_ERR_CUDA;
     const size_t smem = scatter_smem_bytes(E, k);
-    static bool attr_set[64] = {};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-        const int max_smem = int(scatter_smem_bytes(kMaxExperts, kMaxTopK));
-        if (cudaFuncSetAttribute(route_scatter_kernel<true>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem) != cudaSuccess ||
-            cudaFuncSetAttribute(route_scatter_kernel<false>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem) != cudaSuccess)
-            return MOE_ERR_CUDA;
-        attr_set[dev] = true;
-    }
+    const int max_smem = int(scatter_smem_bytes(kMaxExperts, kMaxTopK));
+    if (!opt_in_smem((const void*)route_scatter_kernel<true>, max_smem) ||
+        !opt_in_smem((const void*)route_scatter_kernel<false>, max_smem))
+        return MOE_ERR_CUDA;
     const cudaError_t err = fused
         ? launch_dependent(route_scatter_kernel<true>, unsigned(B > 0 ? B : 1), kThreads, smem, s,
                            topk_idx, topk_w, T, E, k, check_ids, (const int32_t*)hist, counts,

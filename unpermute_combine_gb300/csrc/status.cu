@@ -1,6 +1,9 @@
-// status.cu -- status strings, ABI version, workspace status read-back, and
-// the per-device SM count used to size persistent grids.
+// status.cu -- status strings, ABI version, workspace status read-back, the
+// per-device SM count used to size persistent grids, and the one-time
+// dynamic shared-memory opt-in of the kernels that need more than 48 KB.
 #include <mutex>
+#include <set>
+#include <tuple>
 
 #include "pipeline.cuh"
 
@@ -22,6 +25,21 @@ uint32_t* device_status_word() {
         cached[dev] = static_cast<uint32_t*>(p);
     }
     return cached[dev];
+}
+
+bool opt_in_smem(const void* kernel, int bytes) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    static std::mutex m;
+    static std::set<std::tuple<int, const void*, int>> done;
+    std::lock_guard<std::mutex> lock(m);
+    const auto key = std::make_tuple(dev, kernel, bytes);
+    if (done.count(key)) return true;
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) !=
+        cudaSuccess)
+        return false;
+    done.insert(key);
+    return true;
 }
 
 int sm_count() {
