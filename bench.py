@@ -377,6 +377,8 @@ def run_ours(args, rank, world, local_rank):
             mark()
             moe.moe_combine_backward(gg, y, rr.slot_pos, r.topk_w, grad_expert_out=gy,
                                      grad_probs=o_gp, stream=stream)
+            if lay:     # pad rows of the expert-output gradient must be zero for the GEMMs
+                moe.moe_fill_pad_rows(gy, rr.offsets, rr.counts, stream=stream)
             mark()
             moe.moe_grouped_swiglu_dgrad(gy, w_up_d, w_down_d, rr.offsets, gu, dgate_up=dgu,
                                          dx=dxp, workspace=ws_d, stream=stream)
@@ -574,6 +576,8 @@ def run_ours(args, rank, world, local_rank):
     launches = ROUTE_LAUNCHES + (1 + 3 + 1 if layer else 3)   # grouped SwiGLU: reset + 2 GEMMs
     if train:
         launches += 1 + 3 + 3 + 1 + 1     # combine bwd, dgrad, wgrad (reset + 2 each), permute bwd, route bwd
+        if lay:
+            launches += 1                 # pad rows of the expert-output gradient
     if fp8:
         launches += 2                     # quantize, dequantize
     if router_bwd:

@@ -349,7 +349,12 @@ moe_status_t moe_grouped_swiglu(const void* x, const void* w_up_packed,
  *   dw_up[e]   = x_e^T @ dgate_up_e       fp32 [E,H,2I]
  *   dw_down[e] = hidden_e^T @ dy_e        fp32 [E,I,H]
  * Either output may be NULL (not computed).  Experts with no rows get zeros.
- * Segments need no alignment. */
+ * Segments need no alignment; segments that are multiples of 64 rows (an
+ * aligned layout, moe_route_layout) skip the in-kernel zeroing of a
+ * segment's last partial stage.  With padded or aligned layouts the pad rows
+ * of x, dy and dgate_up must be zero (moe_fill_pad_rows; dgrad keeps
+ * dgate_up's pad rows zero when gate_up's are, since d_gate and d_up vanish
+ * where gate and up do). */
 #define MOE_STATUS_WORKSPACE_BYTES 256
 
 moe_status_t moe_grouped_swiglu_save(const void* x, const void* w_up_packed,
