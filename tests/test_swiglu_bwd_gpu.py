@@ -209,3 +209,53 @@ def test_layer_workload_training_path():
         g = np.array([got[e, a, b] for e, a, b in coords], np.float64)
         bound = _wgrad_bound(Pf, Qf, off, coords)
         assert (np.abs(g - ref) <= bound).all(), which
+
+
+def test_training_on_an_aligned_layout_equals_the_plain_layout():
+    """Expert segments padded to 64 rows with zero pad rows (the layout that
+    spares the wgrad its partial stages): every row output is bit-identical
+    to the plain layout's, and the weight gradients agree within the fp32
+    summation bound (same products, different K stages)."""
+    rng = np.random.default_rng(21)
+    T, H, I, E, k = 700, 256, 128, 8, 2
+    idx, w = wl.random_routing(22, T, E, k)
+    x = to_dev(wl.f32_to_bf16_bits(rng.standard_normal((T, H)).astype(np.float32)))
+    up_h = wl.f32_to_bf16_bits((rng.standard_normal((E, H, 2 * I)) * 0.05).astype(np.float32))
+    down_h = wl.f32_to_bf16_bits((rng.standard_normal((E, I, H)) * 0.05).astype(np.float32))
+    g = to_dev(wl.f32_to_bf16_bits(rng.standard_normal((T, H)).astype(np.float32)))
+    up, down = to_dev(up_h), to_dev(down_h)
+    up_p, down_p = moe.moe_grouped_swiglu_pack(up, down)
+
+    def chain(r, rows):
+        xp = moe.moe_permute(x, r.slot_pos, n_rows=rows)
+        moe.moe_fill_pad_rows(xp, r.offsets, r.counts)
+        y, hid, gu = moe.moe_grouped_swiglu_save(xp, up_p, down_p, r.offsets)
+        gy, _ = moe.moe_combine_backward(g, y, r.slot_pos, to_dev(w))
+        moe.moe_fill_pad_rows(gy, r.offsets, r.counts)
+        dgu, dx = moe.moe_grouped_swiglu_dgrad(gy, up, down, r.offsets, gu)
+        dwu, dwd = moe.moe_grouped_swiglu_wgrad(xp, hid, gy, dgu, r.offsets)
+        torch.cuda.synchronize()
+        for t_ in (y, dx, dwu):
+            assert moe.moe_workspace_status(t_._moe_workspace) == 0
+        return dict(xp=to_host(xp), y=to_host(y), gu=to_host(gu), hid=to_host(hid),
+                    gy=to_host(gy), dgu=to_host(dgu), dx=to_host(dx), dwu=to_host(dwu),
+                    dwd=to_host(dwd), sp=to_host(r.slot_pos))
+
+    plain_rows = T * k
+    rp = moe.moe_route_layout(to_dev(idx), to_dev(w), E, max_rows=plain_rows)
+    a_rows = moe.moe_route_layout_rows(T, E, k, 0, False, 64)
+    ra = moe.moe_route_layout(to_dev(idx), to_dev(w), E, alignment=64, max_rows=a_rows)
+    p, a = chain(rp, plain_rows), chain(ra, a_rows)
+    assert (to_host(ra.offsets) % 64 == 0).all()
+    # the same token slot lands on row sp_plain[t,j] and row sp_aligned[t,j]
+    sp_p, sp_a = p["sp"].ravel(), a["sp"].ravel()
+    for name in ("y", "gu", "hid", "dgu", "dx"):
+        assert (p[name][sp_p] == a[name][sp_a]).all(), name
+    for name, P, Q in (("dwu", "xp", "dgu"), ("dwd", "hid", "gy")):
+        Pf, Qf = _f(p[P][sp_p]), _f(p[Q][sp_p])
+        e_of = idx.ravel()
+        diff = np.abs(p[name].astype(np.float64) - a[name].astype(np.float64))
+        for e in range(E):
+            rows_e = e_of == e
+            bound = 8 * max(rows_e.sum(), 1) * 2.0 ** -24 * (np.abs(Pf[rows_e]).T @ np.abs(Qf[rows_e]))
+            assert (diff[e] <= bound + 1e-30).all(), (name, e)
