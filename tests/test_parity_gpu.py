@@ -221,11 +221,13 @@ def test_combine_bit_exact(dtype, T, H, E, k, drop, weighted):
     assert d.max() == 0, f"max ulp {d.max()}, {np.count_nonzero(d)} mismatches"
 
 
-@pytest.mark.parametrize("k", [2, 4, 8])
-def test_combine_bit_exact_under_cancellation(k):
+@pytest.mark.parametrize("k,weighted", [(2, True), (4, True), (8, True), (2, False), (6, False),
+                                        (8, False)])
+def test_combine_bit_exact_under_cancellation(k, weighted):
     """Rows built to cancel (exactly, or down to a few ulps): every tier of
-    the combine -- float fast path, double-float middle tier, double last
-    resort -- must still give the oracle's double slot-order sum rounded once."""
+    the combine -- float fast path (or, unweighted, the exact TwoSum chain),
+    double-float middle tier, double last resort -- must still give the
+    oracle's double slot-order sum rounded once."""
     T, H, E = 700, 512, 16
     rng = np.random.default_rng(100 + k)
     idx, _ = wl.random_routing(200 + k, T, E, k)
@@ -233,6 +235,8 @@ def test_combine_bit_exact_under_cancellation(k):
     o = oracle.route_indices(idx, None, E)
     w = np.full((T, k), 0.5, np.float32)
     w[:, 1::2] = rng.choice([0.5, 0.25, 0.375], size=(T, k // 2)).astype(np.float32)
+    if not weighted:
+        w[:] = 1.0
     base = rng.standard_normal((T, H)).astype(np.float32)
     y32 = np.zeros((T * k, H), np.float32)
     for t in range(T):
@@ -242,8 +246,10 @@ def test_combine_bit_exact_under_cancellation(k):
             wiggle = 1.0 + (rng.integers(-3, 4) * 2.0 ** -8 if t % 3 else 0.0)
             y32[p] = sign * base[t] * (0.5 / w[t, j]) * wiggle
     y = wl.f32_to_bf16_bits(y32)
-    out = to_host(moe.moe_combine(to_dev(y), r.slot_pos, to_dev(w)))
-    ref, _ = oracle.combine(y, o["slot_pos"], w)
+    if not weighted:                                  # very different magnitudes too
+        y[::5] = wl.f32_to_bf16_bits(y32[::5] * np.float32(2.0 ** 20))
+    out = to_host(moe.moe_combine(to_dev(y), r.slot_pos, to_dev(w) if weighted else None))
+    ref, _ = oracle.combine(y, o["slot_pos"], w if weighted else None)
     d = bf16_ulp_diff(out, ref)
     assert d.max() == 0, f"max ulp {d.max()}, {np.count_nonzero(d)} mismatches"
 

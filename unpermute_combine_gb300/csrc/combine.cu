@@ -245,7 +245,7 @@ __device__ __forceinline__ bool dd_sum_bf16(const float* w, const float* y, cons
 // registers, so an element whose rounding cannot be certified is recomputed
 // in double from the same registers (no reload).  (A cp.async ring as in
 // the backward measured slower here: 352 vs 345 us at T=16384, H=7168, k=8.)
-template <int KMAX>
+template <int KMAX, bool PLAIN>   // PLAIN: topk_w == NULL (plain sum)
 __global__ void __launch_bounds__(kThreads)
 combine_bf16_regs_kernel(const uint4* __restrict__ y, int64_t T, int64_t nvec, int k, int64_t n_rows,
                          const int32_t* __restrict__ slot_pos, const float* __restrict__ topk_w,
@@ -302,6 +302,46 @@ combine_bf16_regs_kernel(const uint4* __restrict__ y, int64_t T, int64_t nvec, i
 #pragma unroll
             for (int j = 0; j < KMAX; ++j)
                 d[j] = pj[j] >= 0 ? __ldcs(y + int64_t(pj[j]) * nvec + v) : make_uint4(0, 0, 0, 0);
+            if (PLAIN) {
+                // plain sum (permute backward): every product is exact, so a
+                // TwoSum chain shows whether the float sum is the exact
+                // slot-order sum (then the double chain computes the same
+                // prefixes and it rounds directly); the rare inexact element
+                // goes through the certified tiers
+                uint4 res;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    uint16_t half[2];
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int i = 2 * q + h;
+                        float hi = 0.0f, yv[KMAX];
+                        bool inexact = false, valid[KMAX];
+#pragma unroll
+                        for (int j = 0; j < KMAX; ++j) {
+                            valid[j] = pj[j] >= 0;
+                            yv[j] = unpack_bf16(d[j], i);
+                            if (!valid[j]) continue;
+                            float sum, e;
+                            two_sum(hi, yv[j], sum, e);
+                            hi = sum;
+                            inexact |= e != 0.0f;
+                        }
+                        if (!inexact) {
+                            half[h] = f32_to_bf16_rn(hi);
+                        } else if (!dd_sum_bf16(wj, yv, valid, KMAX, dd_bound, &half[h])) {
+                            double acc = 0.0;
+#pragma unroll
+                            for (int j = 0; j < KMAX; ++j)
+                                if (valid[j]) acc = fma(double(wj[j]), double(yv[j]), acc);
+                            half[h] = f64_to_bf16_rn(acc);
+                        }
+                    }
+                    set_word(res, q, uint32_t(half[0]) | (uint32_t(half[1]) << 16));
+                }
+                __stcs(out + t * nvec + v, res);
+                continue;
+            }
             float s[8], a[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) { s[i] = 0.0f; a[i] = 0.0f; }
@@ -753,8 +793,12 @@ extern "C" moe_status_t moe_combine(const void* expert_out, moe_dtype_t dtype, i
         uint4* ov = static_cast<uint4*>(out);
         const float cb = combine_bound_factor(k);
         if (k <= 8) {
-            const auto kern = k <= 1 ? combine_bf16_regs_kernel<1> : k <= 2 ? combine_bf16_regs_kernel<2>
-                            : k <= 4 ? combine_bf16_regs_kernel<4> : combine_bf16_regs_kernel<8>;
+            const bool plain = topk_w == nullptr;
+            const auto kern =
+                k <= 1 ? (plain ? combine_bf16_regs_kernel<1, true> : combine_bf16_regs_kernel<1, false>)
+                : k <= 2 ? (plain ? combine_bf16_regs_kernel<2, true> : combine_bf16_regs_kernel<2, false>)
+                : k <= 4 ? (plain ? combine_bf16_regs_kernel<4, true> : combine_bf16_regs_kernel<4, false>)
+                         : (plain ? combine_bf16_regs_kernel<8, true> : combine_bf16_regs_kernel<8, false>);
             kern<<<grid_for((const void*)kern, kThreads, want), kThreads, 0, s>>>(
                 yv, T, H / 8, k, n_rows, slot_pos, topk_w, ov, cb, dd_bound_factor(k));
         } else {
