@@ -97,7 +97,8 @@ def test_fp8_rows_through_sort_chunks_and_pad_fill():
     (513, 4096, 32, 4, 16, 0),       # 512-byte scale rows
     (300, 96, 32, 2, 8, 0),          # 12-byte scale rows: the two-launch path
     (700, 2048, 128, 6, 32, 100),    # capacity drops: unnamed rows stay untouched
-    (4, 256, 256, 1, 2, 0)])       # 4-byte scale rows
+    (4, 256, 256, 1, 2, 0),        # 4-byte scale rows
+    (50, 20480, 128, 4, 16, 0)])   # 20 KB e4m3 rows: 2 pieces, the scale row with the first
 def test_permute_fp8_matches_oracle(T, H, block, k, E, cap):
     idx, w = wl.random_routing(T + H + k, T, E, k)
     rows = moe.moe_route_layout_rows(T, E, k, cap, False, 1)

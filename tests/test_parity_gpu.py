@@ -170,7 +170,9 @@ def test_route_indices_flags_invalid_ids():
 
 @pytest.mark.parametrize("dtype,T,H,E,k", [("bf16", 1000, 4096, 64, 2), ("bf16", 257, 7168, 256, 8),
                                            ("f32", 256, 128, 8, 2), ("bf16", 100, 13, 8, 3),
-                                           ("f32", 129, 7, 16, 4), ("bf16", 64, 8, 4, 4)])
+                                           ("f32", 129, 7, 16, 4), ("bf16", 64, 8, 4, 4),
+                                           ("bf16", 300, 12000, 32, 4),   # 24000-byte rows: 2 pieces
+                                           ("f32", 200, 9000, 16, 3)])    # 36000-byte rows: 3 pieces
 def test_permute_bit_exact(dtype, T, H, E, k):
     x = wl.random_activation(T + H, (T, H), dtype)
     idx, _ = wl.random_routing(T * 3 + k, T, E, k, empty_frac=0.1)
