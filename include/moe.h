@@ -349,6 +349,9 @@ moe_status_t moe_grouped_swiglu(const void* x, const void* w_up_packed,
  *   dw_up[e]   = x_e^T @ dgate_up_e       fp32 [E,H,2I]
  *   dw_down[e] = hidden_e^T @ dy_e        fp32 [E,I,H]
  * Either output may be NULL (not computed).  Experts with no rows get zeros.
+ * For all three calls, offsets outside [0, N] or decreasing are clamped into
+ * [0, N] (no row outside the buffers is read or written) and reported as
+ * MOE_ERR_DEVICE_CHECK in the workspace status.
  * Segments need no alignment; segments that are multiples of 64 rows (an
  * aligned layout, moe_route_layout) skip the in-kernel zeroing of a
  * segment's last partial stage.  With padded or aligned layouts the pad rows

@@ -259,3 +259,42 @@ def test_training_on_an_aligned_layout_equals_the_plain_layout():
             rows_e = e_of == e
             bound = 8 * max(rows_e.sum(), 1) * 2.0 ** -24 * (np.abs(Pf[rows_e]).T @ np.abs(Qf[rows_e]))
             assert (diff[e] <= bound + 1e-30).all(), (name, e)
+
+
+def test_invalid_offsets_are_reported_and_writes_stay_in_bounds():
+    """Offsets past the buffer or decreasing: every call reports
+    MOE_ERR_DEVICE_CHECK and no row outside the buffers is written (the
+    outputs are views into larger buffers whose guard rows must survive)."""
+    rng = np.random.default_rng(31)
+    N, H, I, E = 256, 256, 128, 3
+    bad = to_dev(np.array([0, 100, 400, 300], np.int32))   # past N, then decreasing
+    x = to_dev(wl.f32_to_bf16_bits(rng.standard_normal((N, H)).astype(np.float32)))
+    up = to_dev(wl.f32_to_bf16_bits((rng.standard_normal((E, H, 2 * I)) * 0.05).astype(np.float32)))
+    down = to_dev(wl.f32_to_bf16_bits((rng.standard_normal((E, I, H)) * 0.05).astype(np.float32)))
+    up_p, down_p = moe.moe_grouped_swiglu_pack(up, down)
+    guard = 64
+    sentinel = 12345
+
+    def big(cols):
+        t = torch.full((N + guard, cols), sentinel, dtype=torch.int16, device="cuda")
+        return t.view(torch.bfloat16)
+
+    yb, hb, gb = big(H), big(I), big(2 * I)
+    y, hid, gu = moe.moe_grouped_swiglu_save(x, up_p, down_p, bad, out=yb[:N], hidden=hb[:N],
+                                             gate_up=gb[:N])
+    assert moe.moe_workspace_status(y._moe_workspace) == 6
+    dgb, dxb = big(2 * I), big(H)
+    dgu, dx = moe.moe_grouped_swiglu_dgrad(x, up, down, bad, gu, dgate_up=dgb[:N], dx=dxb[:N])
+    assert moe.moe_workspace_status(dx._moe_workspace) == 6
+    dwu, dwd = moe.moe_grouped_swiglu_wgrad(x, hid, x, dgu, bad)
+    assert moe.moe_workspace_status(dwu._moe_workspace) == 6
+    torch.cuda.synchronize()
+    for b in (yb, hb, gb, dgb, dxb):
+        assert (b.view(torch.int16)[N:] == sentinel).all()
+    # pad-row fill with a negative offset writes nothing before the buffer
+    rows = big(H)
+    moe.moe_fill_pad_rows(rows[8:8 + 100], to_dev(np.array([-5, 10, 20], np.int32)),
+                          to_dev(np.array([0, 3], np.int32)))
+    torch.cuda.synchronize()
+    assert (rows.view(torch.int16)[:8] == sentinel).all()
+    assert (rows.view(torch.int16)[8 + 20:] == sentinel).all()

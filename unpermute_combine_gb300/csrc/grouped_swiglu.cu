@@ -140,6 +140,7 @@ enum Epi : int {
 
 struct GemmArgs {
     const int32_t* offsets;     // [E+1] row segments
+    int64_t n_rows;             // rows of the activation buffers: segments are clamped to it
     int E;
     int K;                      // reduction length
     int n_tiles;                // BN-column tiles per expert
@@ -192,20 +193,27 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
     __shared__ int s_mt[kMaxExperts];
     __shared__ int s_row0[kMaxExperts + 1];
     __shared__ int s_failed;
+    __shared__ int s_bad;
 
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int E = args.E;
 
-    // schedule from the device-side offsets (single warp scan, E <= 1024)
+    // schedule from the device-side offsets (single warp scan, E <= 1024);
+    // offsets are clamped into [0, n_rows], so no row outside the buffers is
+    // ever written, and offsets that needed it are reported
     if (warp == 0) {
         int carry = 0;
+        bool bad = false;
+        const int nr = int(args.n_rows);
         for (int base = 0; base < E; base += 32) {
             const int e = base + lane;
             int mt = 0;
             if (e < E) {
-                const int r0 = args.offsets[e], r1 = args.offsets[e + 1];
+                const int raw0 = args.offsets[e], raw1 = args.offsets[e + 1];
+                bad |= raw0 < 0 || raw1 < raw0 || raw1 > nr;
+                const int r0 = min(max(raw0, 0), nr), r1 = min(max(raw1, 0), nr);
                 mt = r1 > r0 ? (r1 - r0 + BM - 1) / BM : 0;
                 s_mt[e] = mt > 0 ? mt : 1;
                 s_row0[e] = r0;
@@ -219,10 +227,12 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
             if (e < E) s_tile_start[e] = carry + incl - mt * args.n_tiles;
             carry += __shfl_sync(0xFFFFFFFFu, incl, 31);
         }
+        bad = __any_sync(0xFFFFFFFFu, bad);
         if (lane == 0) {
             s_tile_start[E] = carry;
-            s_row0[E] = args.offsets[E];
+            s_row0[E] = min(max(args.offsets[E], 0), nr);
             s_failed = 0;
+            s_bad = bad;
         }
     }
     if (threadIdx.x == 32) {
@@ -405,6 +415,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
     if (s_failed && threadIdx.x == 0) {
         args.header->status = MOE_ERR_TIMEOUT;
         args.header->detail = blockIdx.x;
+    } else if (s_bad && threadIdx.x == 0 && blockIdx.x == 0) {
+        atomicCAS(&args.header->status, uint32_t(MOE_OK), uint32_t(MOE_ERR_DEVICE_CHECK));
     }
     if (warp == 2) {
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;"
@@ -465,6 +477,7 @@ __device__ __forceinline__ void mma_bf16_mn(uint32_t tmem_d, uint64_t adesc, uin
 
 struct WgradArgs {
     const int32_t* offsets;
+    int64_t n_rows;             // rows of the operands (rows past it read as zeros)
     int E;
     int M, Ncols;               // dW[e] is [M, Ncols]
     int m_tiles, n_tiles;       // M / BM, Ncols / BN
@@ -489,10 +502,20 @@ grouped_wgrad_kernel(const __grid_constant__ CUtensorMap map_p,
     __shared__ __align__(8) uint64_t tmem_empty_bar[2];
     __shared__ uint32_t s_tmem_base;
     __shared__ int s_failed;
+    __shared__ int s_bad;
 
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (warp == 3) {            // offsets outside [0, n_rows] or decreasing are reported
+        bool bad = false;
+        for (int e = lane; e < args.E; e += 32) {
+            const int64_t raw0 = args.offsets[e], raw1 = args.offsets[e + 1];
+            bad |= raw0 < 0 || raw1 < raw0 || raw1 > args.n_rows;
+        }
+        bad = __any_sync(0xFFFFFFFFu, bad);
+        if (lane == 0) s_bad = bad;
+    }
     if (threadIdx.x == 32) {
         for (int s = 0; s < kWStages; ++s) {
             mbar_init(smem_addr(&full_bar[s]), 1);
@@ -680,6 +703,8 @@ grouped_wgrad_kernel(const __grid_constant__ CUtensorMap map_p,
     if (s_failed && threadIdx.x == 0) {
         args.header->status = MOE_ERR_TIMEOUT;
         args.header->detail = blockIdx.x;
+    } else if (s_bad && threadIdx.x == 0 && blockIdx.x == 0) {
+        atomicCAS(&args.header->status, uint32_t(MOE_OK), uint32_t(MOE_ERR_DEVICE_CHECK));
     }
     if (warp == 2) {
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;"
@@ -866,10 +891,10 @@ extern "C" moe_status_t moe_grouped_swiglu(const void* x, const void* w_up_packe
 
     if (!smem_attrs_set()) return MOE_ERR_CUDA;
     const int grid = sm_count();
-    GemmArgs a1{offsets, E, int(H), int(I / 128), 2 * I, hidden, I, I, I, nullptr, nullptr, header};
+    GemmArgs a1{offsets, N, E, int(H), int(I / 128), 2 * I, hidden, I, I, I, nullptr, nullptr, header};
     grouped_gemm_kernel<kSwiglu><<<grid, kThreads, kSmemBytes, s>>>(m_x, m_up, a1);
     if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
-    GemmArgs a2{offsets, E, int(I), int(H / BN), H, y, H, H, I, nullptr, nullptr, header};
+    GemmArgs a2{offsets, N, E, int(I), int(H / BN), H, y, H, H, I, nullptr, nullptr, header};
     grouped_gemm_kernel<kPlain><<<grid, kThreads, kSmemBytes, s>>>(m_h, m_down, a2);
     return launch_status();
 }
@@ -898,11 +923,11 @@ extern "C" moe_status_t moe_grouped_swiglu_save(const void* x, const void* w_up_
         return MOE_ERR_CUDA;
     if (!smem_attrs_set()) return MOE_ERR_CUDA;
     const int grid = sm_count();
-    GemmArgs a1{offsets, E, int(H), int(I / 128), 2 * I, hidden, I, I, I, nullptr,
+    GemmArgs a1{offsets, N, E, int(H), int(I / 128), 2 * I, hidden, I, I, I, nullptr,
                 static_cast<uint16_t*>(gate_up), header};
     grouped_gemm_kernel<kSwigluSave><<<grid, kThreads, kSmemBytes, s>>>(m_x, m_up, a1);
     if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
-    GemmArgs a2{offsets, E, int(I), int(H / BN), H, y, H, H, I, nullptr, nullptr, header};
+    GemmArgs a2{offsets, N, E, int(I), int(H / BN), H, y, H, H, I, nullptr, nullptr, header};
     grouped_gemm_kernel<kPlain><<<grid, kThreads, kSmemBytes, s>>>(m_h, m_down, a2);
     return launch_status();
 }
@@ -934,12 +959,12 @@ extern "C" moe_status_t moe_grouped_swiglu_dgrad(const void* dy, const void* w_u
     const int grid = sm_count();
     // GMM2 backward + SwiGLU backward: dh = dy @ w_down[e]^T (w_down [E,I,H] is
     // already K-major for this product), [d_gate | d_up] into dgate_up
-    GemmArgs d2{offsets, E, int(H), int((I + BN - 1) / BN), I, dgate_up, 2 * I, I, I,
+    GemmArgs d2{offsets, N, E, int(H), int((I + BN - 1) / BN), I, dgate_up, 2 * I, I, I,
                 static_cast<const uint16_t*>(gate_up), nullptr, header};
     grouped_gemm_kernel<kSwigluBwd><<<grid, kThreads, kSmemBytes, s>>>(m_dy, m_wd, d2);
     if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
     // GMM1 backward: dx = dgate_up @ w_up[e]^T (w_up [E,H,2I] is K-major here)
-    GemmArgs d1{offsets, E, int(2 * I), int(H / BN), H, dx, H, H, I, nullptr, nullptr, header};
+    GemmArgs d1{offsets, N, E, int(2 * I), int(H / BN), H, dx, H, H, I, nullptr, nullptr, header};
     grouped_gemm_kernel<kPlain><<<grid, kThreads, kSmemBytes, s>>>(m_dgu, m_wu, d1);
     return launch_status();
 }
@@ -977,7 +1002,7 @@ extern "C" moe_status_t moe_grouped_swiglu_wgrad(const void* x, const void* hidd
         if (!make_map(&m_p, hidden, N, I, 64) || !make_map(&m_q, dy, N, H, 64) ||
             !make_out_map(&m_o, dw_down, int64_t(E) * I, H))
             return MOE_ERR_CUDA;
-        WgradArgs a{offsets, E, int(I), int(H), int(I / BM), int(H / BN), dw_down, header};
+        WgradArgs a{offsets, N, E, int(I), int(H), int(I / BM), int(H / BN), dw_down, header};
         grouped_wgrad_kernel<<<grid, kThreads, kWgradSmemBytes, s>>>(m_p, m_q, m_o, a);
         if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
     }
@@ -986,7 +1011,7 @@ extern "C" moe_status_t moe_grouped_swiglu_wgrad(const void* x, const void* hidd
         if (!make_map(&m_p, x, N, H, 64) || !make_map(&m_q, dgate_up, N, 2 * I, 64) ||
             !make_out_map(&m_o, dw_up, int64_t(E) * H, 2 * I))
             return MOE_ERR_CUDA;
-        WgradArgs a{offsets, E, int(H), int(2 * I), int(H / BM), int(2 * I / BN), dw_up, header};
+        WgradArgs a{offsets, N, E, int(H), int(2 * I), int(H / BM), int(2 * I / BN), dw_up, header};
         grouped_wgrad_kernel<<<grid, kThreads, kWgradSmemBytes, s>>>(m_p, m_q, m_o, a);
         if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
     }

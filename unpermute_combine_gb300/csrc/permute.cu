@@ -495,7 +495,8 @@ fill_pad_rows_kernel(V* __restrict__ rows, int64_t max_rows, int64_t nvec,
                      const int32_t* __restrict__ offsets, const int32_t* __restrict__ counts,
                      int E) {
     for (int e = blockIdx.x; e < E; e += gridDim.x) {
-        const int64_t p0 = int64_t(offsets[e]) + counts[e];
+        // first pad row and the segment end, kept inside [0, max_rows)
+        const int64_t p0 = max64(int64_t(offsets[e]) + max64(counts[e], 0), 0);
         const int64_t p1 = min64(offsets[e + 1], max_rows);
         if (p0 >= p1) continue;
         const int64_t n = (p1 - p0) * nvec;
