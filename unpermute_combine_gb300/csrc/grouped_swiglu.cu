@@ -444,16 +444,20 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
 // the warp moves on to the next block while full 128-byte rows stream out.
 constexpr int kBoxBytes = 64 * 128;
 constexpr int kEpiTileBytes = 32 * 32 * 4;            // one 32x32 fp32 block
-// Load stages and staging tiles per epilogue warp (3 stages with 4 staging
-// tiles measured 7% slower: the load side needs the depth).
-constexpr int kWStages = 4;
+// A tile is 256 rows of dW (two 128-row halves with their own TMEM
+// accumulators, all 512 columns) x 256 columns: both halves share every Q
+// panel, so a stage of 64 token rows (P 256 columns + Q 256 columns = 64 KB)
+// feeds twice the MMA work of a 128-row tile, and there are half as many
+// tiles (and partial last stages).  The price: one accumulator set, so a
+// tile's MMAs wait for the previous tile's epilogue.
+constexpr int kWM = 256;                       // dW rows per tile
+constexpr int kWStages = 3;
 constexpr int kEpiBufs = 2;
-constexpr int kWgradSmemBytes = kWStages * kStageBytes + 4 * kEpiBufs * kEpiTileBytes + 1024;
-static_assert(kWgradSmemBytes <= 227 * 1024 - 256, "wgrad shared memory");
-
-constexpr int kWA = BM / 64;                   // P boxes per stage
+constexpr int kWA = kWM / 64;                  // P boxes per stage (2 per half)
 constexpr int kWB = BN / 64;                   // Q boxes per stage
-static_assert((kWA + kWB) * kBoxBytes == kStageBytes, "wgrad stage = forward stage");
+constexpr int kWStageBytes = (kWA + kWB) * kBoxBytes;
+constexpr int kWgradSmemBytes = kWStages * kWStageBytes + 4 * kEpiBufs * kEpiTileBytes + 1024;
+static_assert(kWgradSmemBytes <= 227 * 1024 - 256, "wgrad shared memory");
 
 __device__ __forceinline__ uint64_t smem_desc_mn128(uint32_t addr) {
     uint64_t d = 0;
@@ -480,7 +484,7 @@ struct WgradArgs {
     int64_t n_rows;             // rows of the operands (rows past it read as zeros)
     int E;
     int M, Ncols;               // dW[e] is [M, Ncols]
-    int m_tiles, n_tiles;       // M / BM, Ncols / BN
+    int m_tiles, n_tiles;       // ceil(M / kWM), Ncols / BN
     float* out;                 // [E, M, Ncols]
     WsHeader* header;
 };
@@ -498,8 +502,8 @@ grouped_wgrad_kernel(const __grid_constant__ CUtensorMap map_p,
     __shared__ __align__(8) uint64_t full_bar[kWStages];
     __shared__ __align__(8) uint64_t ready_bar[kWStages];
     __shared__ __align__(8) uint64_t empty_bar[kWStages];
-    __shared__ __align__(8) uint64_t tmem_full_bar[2];
-    __shared__ __align__(8) uint64_t tmem_empty_bar[2];
+    __shared__ __align__(8) uint64_t tmem_full_bar;
+    __shared__ __align__(8) uint64_t tmem_empty_bar;
     __shared__ uint32_t s_tmem_base;
     __shared__ int s_failed;
     __shared__ int s_bad;
@@ -522,10 +526,8 @@ grouped_wgrad_kernel(const __grid_constant__ CUtensorMap map_p,
             mbar_init(smem_addr(&ready_bar[s]), 1);
             mbar_init(smem_addr(&empty_bar[s]), 1);
         }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(smem_addr(&tmem_full_bar[b]), 1);
-            mbar_init(smem_addr(&tmem_empty_bar[b]), 128);
-        }
+        mbar_init(smem_addr(&tmem_full_bar), 1);
+        mbar_init(smem_addr(&tmem_empty_bar), 128);
         mbar_fence_init();
         s_failed = 0;
     }
@@ -562,7 +564,7 @@ grouped_wgrad_kernel(const __grid_constant__ CUtensorMap map_p,
             if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) return false;
             const int chunks = (64 - pend_valid) * 8;               // 16-byte chunks per box
             for (int b = 0; b < kWA + kWB; ++b) {
-                uint8_t* box = smem + pend_s * kStageBytes + b * kBoxBytes + pend_valid * 128;
+                uint8_t* box = smem + pend_s * kWStageBytes + b * kBoxBytes + pend_valid * 128;
                 for (int c = lane; c < chunks; c += 32)
                     *reinterpret_cast<uint4*>(box + c * 16) = make_uint4(0, 0, 0, 0);
             }
@@ -585,13 +587,13 @@ grouped_wgrad_kernel(const __grid_constant__ CUtensorMap map_p,
                 if (!__shfl_sync(0xFFFFFFFFu, ok, 0) && !service()) { failed = true; break; }
                 if (lane == 0) ok = mbar_wait(smem_addr(&empty_bar[s]), ph ^ 1u);
                 if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) { failed = true; break; }
-                const uint32_t base = smem_addr(smem + s * kStageBytes);
+                const uint32_t base = smem_addr(smem + s * kWStageBytes);
                 const uint32_t fb = smem_addr(&full_bar[s]);
                 const int row = r0 + ks * 64;
                 if (lane == 0) {
-                    mbar_expect_tx(fb, kStageBytes);
+                    mbar_expect_tx(fb, kWStageBytes);
                     for (int b = 0; b < kWA; ++b)
-                        tma_load_2d(base + b * kBoxBytes, &map_p, m * BM + b * 64, row, fb);
+                        tma_load_2d(base + b * kBoxBytes, &map_p, m * kWM + b * 64, row, fb);
                     for (int b = 0; b < kWB; ++b)
                         tma_load_2d(base + (kWA + b) * kBoxBytes, &map_q, n * BN + b * 64, row, fb);
                 }
@@ -615,10 +617,9 @@ grouped_wgrad_kernel(const __grid_constant__ CUtensorMap map_p,
             coords(t, e, m, n);
             const int r0 = args.offsets[e], r1 = args.offsets[e + 1];
             const int ksteps = r1 > r0 ? (r1 - r0 + 63) / 64 : 0;
-            const uint32_t buf = tile_iter & 1u, use = tile_iter >> 1;
-            if (!mbar_wait(smem_addr(&tmem_empty_bar[buf]), (use & 1u) ^ 1u)) { s_failed = 1; break; }
+            // the previous tile's epilogue has drained both accumulators
+            if (!mbar_wait(smem_addr(&tmem_empty_bar), (tile_iter & 1u) ^ 1u)) { s_failed = 1; break; }
             tc_fence_after();
-            const uint32_t tmem_d = tmem_base + buf * BN;
             for (int ks = 0; ks < ksteps; ++ks, ++it) {
                 const int s = it % kWStages;
                 const uint32_t ph = (it / kWStages) & 1u;
@@ -631,28 +632,32 @@ grouped_wgrad_kernel(const __grid_constant__ CUtensorMap map_p,
                     ready_phase ^= 1u << s;
                 }
                 tc_fence_after();
-                const uint32_t a_base = smem_addr(smem + s * kStageBytes);
+                const uint32_t a_base = smem_addr(smem + s * kWStageBytes);
                 const uint32_t b_base = a_base + kWA * kBoxBytes;
 #pragma unroll
-                for (int kk = 0; kk < 64 / 16; ++kk)      // 16 token rows = 2 K groups
-                    mma_bf16_mn(tmem_d, smem_desc_mn128(a_base + kk * 2048),
-                                smem_desc_mn128(b_base + kk * 2048), (ks | kk) != 0);
+                for (int kk = 0; kk < 64 / 16; ++kk) {    // 16 token rows = 2 K groups
+                    const uint64_t bdesc = smem_desc_mn128(b_base + kk * 2048);
+#pragma unroll
+                    for (int h = 0; h < 2; ++h)           // rows [128h, 128h+128) of the tile
+                        mma_bf16_mn(tmem_base + h * BN,
+                                    smem_desc_mn128(a_base + h * 2 * kBoxBytes + kk * 2048), bdesc,
+                                    (ks | kk) != 0);
+                }
                 mma_commit(smem_addr(&empty_bar[s]));
             }
             if (s_failed) break;
-            mma_commit(smem_addr(&tmem_full_bar[buf]));
+            mma_commit(smem_addr(&tmem_full_bar));
         }
     } else if (warp >= 4) {
         // ------------------------------------------------------ epilogue
         const int q = warp - 4;
         const uint32_t lane_base = uint32_t(q * 32) << 16;
         // kEpiBufs staging tiles for this warp, 1024-byte aligned (128-byte swizzle)
-        const uint32_t stage0 = smem_addr(smem + kWStages * kStageBytes + q * kEpiBufs * kEpiTileBytes);
+        const uint32_t stage0 = smem_addr(smem + kWStages * kWStageBytes + q * kEpiBufs * kEpiTileBytes);
         uint32_t chunk_iter = 0;
         uint32_t tile_iter = 0;
         for (int t = blockIdx.x; t < total_tiles; t += gridDim.x, ++tile_iter) {
-            const uint32_t buf = tile_iter & 1u, use = tile_iter >> 1;
-            if (s_failed || !mbar_wait(smem_addr(&tmem_full_bar[buf]), use & 1u)) {
+            if (s_failed || !mbar_wait(smem_addr(&tmem_full_bar), tile_iter & 1u)) {
                 s_failed = 1;
                 break;
             }
@@ -660,39 +665,43 @@ grouped_wgrad_kernel(const __grid_constant__ CUtensorMap map_p,
             int e, m, n;
             coords(t, e, m, n);
             const bool empty = args.offsets[e + 1] <= args.offsets[e];
-            // this quadrant's 32 rows of dW[e] (rows of the [E*M, Ncols] output)
-            const int out_row = e * args.M + m * BM + q * 32;
-            const uint32_t tmem_acc = tmem_base + buf * BN;
 #pragma unroll 1
-            for (int c = 0; c < BN; c += 32, ++chunk_iter) {
-                float a[32];
-                if (!empty) {
-                    tmem_ld32(tmem_acc + lane_base + c, a);
-                } else {
+            for (int h = 0; h < 2; ++h) {
+                const int row_in = m * kWM + h * BM + q * 32;   // this quadrant's first dW row
+                if (row_in >= args.M) continue;                // past M (a partial last tile)
+                const int out_row = e * args.M + row_in;
+                const uint32_t tmem_acc = tmem_base + h * BN;
+#pragma unroll 1
+                for (int c = 0; c < BN; c += 32, ++chunk_iter) {
+                    float a[32];
+                    if (!empty) {
+                        tmem_ld32(tmem_acc + lane_base + c, a);
+                    } else {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) a[i] = 0.0f;
-                }
-                // the store that last used this staging tile has finished reading it
-                if (lane == 0 && chunk_iter >= kEpiBufs) bulk_wait_read<kEpiBufs - 1>();
-                __syncwarp();
-                const uint32_t tile = stage0 + (chunk_iter % kEpiBufs) * kEpiTileBytes;
-                // row `lane`, 16-byte chunk j at j ^ (row % 8): the 128-byte swizzle
+                        for (int i = 0; i < 32; ++i) a[i] = 0.0f;
+                    }
+                    // the store that last used this staging tile has finished reading it
+                    if (lane == 0 && chunk_iter >= kEpiBufs) bulk_wait_read<kEpiBufs - 1>();
+                    __syncwarp();
+                    const uint32_t tile = stage0 + (chunk_iter % kEpiBufs) * kEpiTileBytes;
+                    // row `lane`, 16-byte chunk j at j ^ (row % 8): the 128-byte swizzle
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const uint32_t dst = tile + lane * 128 + ((j ^ (lane & 7)) << 4);
-                    asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};"
-                                 :: "r"(dst), "f"(a[4 * j]), "f"(a[4 * j + 1]), "f"(a[4 * j + 2]),
-                                    "f"(a[4 * j + 3]) : "memory");
-                }
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                __syncwarp();
-                if (lane == 0) {
-                    tma_store_2d(&map_out, n * BN + c, out_row, tile);
-                    bulk_commit();
+                    for (int j = 0; j < 8; ++j) {
+                        const uint32_t dst = tile + lane * 128 + ((j ^ (lane & 7)) << 4);
+                        asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};"
+                                     :: "r"(dst), "f"(a[4 * j]), "f"(a[4 * j + 1]), "f"(a[4 * j + 2]),
+                                        "f"(a[4 * j + 3]) : "memory");
+                    }
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&map_out, n * BN + c, out_row, tile);
+                        bulk_commit();
+                    }
                 }
             }
             tc_fence_before();
-            mbar_arrive(smem_addr(&tmem_empty_bar[buf]));
+            mbar_arrive(smem_addr(&tmem_empty_bar));
         }
         if (lane == 0) bulk_wait_all();                 // every store has landed
         __syncwarp();
@@ -1002,7 +1011,8 @@ extern "C" moe_status_t moe_grouped_swiglu_wgrad(const void* x, const void* hidd
         if (!make_map(&m_p, hidden, N, I, 64) || !make_map(&m_q, dy, N, H, 64) ||
             !make_out_map(&m_o, dw_down, int64_t(E) * I, H))
             return MOE_ERR_CUDA;
-        WgradArgs a{offsets, N, E, int(I), int(H), int(I / BM), int(H / BN), dw_down, header};
+        WgradArgs a{offsets, N, E, int(I), int(H), int((I + kWM - 1) / kWM), int(H / BN), dw_down,
+                    header};
         grouped_wgrad_kernel<<<grid, kThreads, kWgradSmemBytes, s>>>(m_p, m_q, m_o, a);
         if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
     }
@@ -1011,7 +1021,8 @@ extern "C" moe_status_t moe_grouped_swiglu_wgrad(const void* x, const void* hidd
         if (!make_map(&m_p, x, N, H, 64) || !make_map(&m_q, dgate_up, N, 2 * I, 64) ||
             !make_out_map(&m_o, dw_up, int64_t(E) * H, 2 * I))
             return MOE_ERR_CUDA;
-        WgradArgs a{offsets, N, E, int(H), int(2 * I), int(H / BM), int(2 * I / BN), dw_up, header};
+        WgradArgs a{offsets, N, E, int(H), int(2 * I), int((H + kWM - 1) / kWM), int(2 * I / BN),
+                    dw_up, header};
         grouped_wgrad_kernel<<<grid, kThreads, kWgradSmemBytes, s>>>(m_p, m_q, m_o, a);
         if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
     }
