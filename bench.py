@@ -605,6 +605,8 @@ def run_ours(args, rank, world, local_rank):
     }
     if not args.no_cpu_baseline and not layer:
         line["cpu_baseline"] = cpu_baseline(args.cpu_tokens)
+    elif not args.no_cpu_baseline and layer and not train:
+        line["cpu_baseline"] = cpu_baseline_layer(args.cpu_layer_tokens)
     return line
 
 
@@ -790,6 +792,7 @@ def run_vep8(args, rank, world, local_rank):
                         "steps pipelined over two buffer sets on three streams"},
         "gpu_launches": 2 * R * args.steps,              # one fused launch per call (C <= 1024)
         "clocks": clk.summary(),
+        **({} if args.no_cpu_baseline else {"cpu_baseline": cpu_baseline_vep8()}),
     }
 
 
@@ -815,6 +818,67 @@ def cpu_baseline(tokens: int):
     n = tokens * W.k
     return {"value": n / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
             "sample": f"first {tokens} of {W.T} tokens ({n} routed rows), one full step, "
+                      f"{dt:.1f} s single-threaded C (host has {os.cpu_count()} cores)"}
+
+
+def cpu_baseline_layer(tokens: int):
+    """The CPU oracle on the layer workload's first `tokens` tokens: route,
+    permute, the grouped SwiGLU of those tokens' rows, combine;
+    single-threaded."""
+    import numpy as np
+
+    import oracle
+    import workloads as wl
+
+    d = wl.make("layer", with_weights=True)
+    W = d["workload"]
+    x, lg = d["x"][:tokens], d["logits"][:tokens]
+    t0 = time.perf_counter()
+    r = oracle.route(lg, W.k)
+    xp = oracle.permute(x, r["sorted_indices"])
+    y, _ = oracle.grouped_swiglu(xp, d["w_up"], d["w_down"], r["offsets"])
+    oracle.combine(y, r["slot_pos"], r["topk_w"])
+    dt = time.perf_counter() - t0
+    n = tokens * W.k
+    return {"value": n / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"first {tokens} of {W.T} tokens ({n} routed rows), one layer forward, "
+                      f"{dt:.1f} s single-threaded C (host has {os.cpu_count()} cores)"}
+
+
+def cpu_baseline_vep8():
+    """The CPU oracle's sort_chunks forward and inverse for every virtual
+    rank of the virtual expert-parallel layout, single-threaded."""
+    import numpy as np
+
+    import oracle
+    import workloads as wl
+
+    d = wl.make("vep8")
+    W = d["workload"]
+    R = L = W.ranks
+    per = W.T // R
+    idx, _, _ = oracle.topk_softmax(d["logits"], W.k)
+    bufs = []
+    for rr in range(R):
+        M = np.zeros((R, L), np.int32)
+        rows = []
+        for src in range(R):
+            toks = np.arange(src * per, (src + 1) * per)
+            for le in range(L):
+                sel = toks[(idx[toks] == rr * L + le).any(axis=1)]
+                M[src, le] = sel.size
+                rows.append(sel)
+        bufs.append((M, np.ascontiguousarray(d["x"][np.concatenate(rows)])))
+    fwd, inv = oracle.chunk_idxs(R, L, False), oracle.chunk_idxs(R, L, True)
+    t0 = time.perf_counter()
+    n = 0
+    for M, buf in bufs:
+        em = oracle.sort_chunks(buf, M.ravel(), fwd)
+        oracle.sort_chunks(em, M.T.ravel(), inv)
+        n += buf.shape[0]
+    dt = time.perf_counter() - t0
+    return {"value": n / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"all {R} virtual ranks ({n} routed rows), forward + inverse, "
                       f"{dt:.1f} s single-threaded C (host has {os.cpu_count()} cores)"}
 
 
@@ -853,6 +917,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-tokens", type=int, default=16384)
     ap.add_argument("--ref-tokens", type=int, default=2048)
+    ap.add_argument("--cpu-layer-tokens", type=int, default=256,
+                    help="tokens of the layer workload the CPU oracle baseline runs")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--tokens", type=int, default=None,
                     help="use only the first TOKENS tokens (small cases for profiling)")
