@@ -85,6 +85,9 @@ CASES = [
     (1, [37, 0, 129, 300], 256, 128),     # ragged, empty expert, 64-row tails, half N tile
     (2, [64, 200, 1, 63], 512, 384),      # 1.5 N tiles, single-row expert
     (3, [130], 256, 256),                  # one expert
+    # last stages of 16, 48, 32, 16, 17, 33 rows: whole 16-row MMA groups with
+    # no zeroed tail next to ragged ones
+    (4, [16, 48, 96, 80, 17, 33], 256, 128),
 ]
 
 

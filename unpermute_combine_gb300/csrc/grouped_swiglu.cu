@@ -427,21 +427,26 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
 // ------------------------------------------------------ k-grouped wgrad
 // dW[e] = P_e^T Q_e over the rows of expert e's segment: P [N_rows, M] and
 // Q [N_rows, Ncols] row-major, dW [E, M, Ncols] fp32.  Both operands are read
-// MN-major: a stage holds 64 token rows (the reduction) of a 128-column P
-// panel (two 64-column TMA boxes) and a 256-column Q panel (four boxes), each
-// box 64 rows x 128 bytes with the 128-byte swizzle -- the canonical MN-major
+// MN-major: a stage holds 64 token rows (the reduction) of a 256-column P
+// panel (four 64-column TMA boxes, two per 128-row half of the tile) and a
+// 256-column Q panel (four boxes), each box 64 rows x 128 bytes with the
+// 128-byte swizzle -- the canonical MN-major
 // SW128 layout, 8-row K groups 1024 bytes apart (SBO) and 64-element MN
 // blocks one box (8 KB) apart (LBO).  The instruction descriptor marks A and B
 // as MN-major.  Rows past the segment's end in its last stage belong to the
-// next expert: the producer warp zeroes them in shared memory (whole 128-byte
-// rows, so the swizzle does not matter) and publishes the stage on a second
-// barrier.  The fix-up is deferred: the producer keeps issuing later stages
-// and zeroes the pending partial stage only when it would otherwise block (a
-// ring slot not yet free, the next partial stage, the end), by which time
-// the stage has landed.  An expert with no rows gets zeros.  The epilogue
-// writes each 32x32 fp32 block of its quadrant into a 128-byte-swizzled
-// staging tile (kEpiBufs per warp) and hands it to the TMA store engine, so
-// the warp moves on to the next block while full 128-byte rows stream out.
+// next expert.  One MMA reduces 16 token rows, so the last stage issues MMAs
+// only up to the first multiple of 16 at or past the segment's end, and only
+// the rows between the end and that multiple (at most 15) must read as zero:
+// the producer warp zeroes them in shared memory (whole 128-byte rows, so the
+// swizzle does not matter) and publishes the stage on a second barrier.  A
+// segment that ends on a 16-row boundary needs no fix-up.  The producer never
+// waits on a stage it has issued: while it waits for a free ring slot it
+// polls the partial stages in flight and fixes up each one once it lands, so
+// the next tile's loads go out as early as they would without a fix-up.  An
+// expert with no rows gets zeros.  The epilogue writes each 32x32 fp32 block
+// of its quadrant into a 128-byte-swizzled staging tile (kEpiBufs per warp)
+// and hands it to the TMA store engine, so the warp moves on to the next
+// block while full 128-byte rows stream out.
 constexpr int kBoxBytes = 64 * 128;
 constexpr int kEpiTileBytes = 32 * 32 * 4;            // one 32x32 fp32 block
 // A tile is 256 rows of dW (two 128-row halves with their own TMEM
@@ -452,6 +457,9 @@ constexpr int kEpiTileBytes = 32 * 32 * 4;            // one 32x32 fp32 block
 // tile's MMAs wait for the previous tile's epilogue.
 constexpr int kWM = 256;                       // dW rows per tile
 constexpr int kWStages = 3;
+// bound on the producer's non-blocking polls for a free ring slot (each poll
+// is at least two shared-memory round trips: well over half a second)
+constexpr uint32_t kPollLimit = 1u << 24;
 constexpr int kEpiBufs = 2;
 constexpr int kWA = kWM / 64;                  // P boxes per stage (2 per half)
 constexpr int kWB = BN / 64;                   // Q boxes per stage
@@ -552,27 +560,35 @@ grouped_wgrad_kernel(const __grid_constant__ CUtensorMap map_p,
 
     if (warp == 0) {
         // ------------------------------------------ TMA producer + tail fix-up
+        // Any ring slot may hold a partial stage awaiting its fix-up: bit s of
+        // `pend`, with the stage's full-barrier parity and valid-row count in
+        // byte s of `pend_info` (parity << 7 | valid, valid < 64).  While it
+        // waits for a free slot the warp polls the pending stages and fixes up
+        // each one as soon as it lands, so it never parks on a stage it has
+        // just issued while later loads could be going out.
         uint32_t it = 0;
         bool failed = false;
-        bool pend = false;                 // a partial stage waiting for its fix-up
-        int pend_s = 0, pend_valid = 64;
-        uint32_t pend_ph = 0;
-        auto service = [&]() -> bool {
-            if (!pend) return true;
-            bool ok = true;
-            if (lane == 0) ok = mbar_wait(smem_addr(&full_bar[pend_s]), pend_ph);
-            if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) return false;
-            const int chunks = (64 - pend_valid) * 8;               // 16-byte chunks per box
-            for (int b = 0; b < kWA + kWB; ++b) {
-                uint8_t* box = smem + pend_s * kWStageBytes + b * kBoxBytes + pend_valid * 128;
-                for (int c = lane; c < chunks; c += 32)
-                    *reinterpret_cast<uint4*>(box + c * 16) = make_uint4(0, 0, 0, 0);
+        uint32_t pend = 0, pend_info = 0;
+        auto poll = [&]() {
+            for (int ps = 0; ps < kWStages; ++ps) {
+                if (!((pend >> ps) & 1u)) continue;
+                const uint32_t info = (pend_info >> (8 * ps)) & 0xFFu;
+                bool landed = false;
+                if (lane == 0) landed = mbar_test(smem_addr(&full_bar[ps]), info >> 7);
+                if (!__shfl_sync(0xFFFFFFFFu, landed, 0)) continue;
+                // zero rows [valid, next multiple of 16) of every box: 16-byte chunks
+                const int valid = int(info & 63u);
+                const int chunks = (((valid + 15) & ~15) - valid) * 8;
+                for (int b = 0; b < kWA + kWB; ++b) {
+                    uint8_t* box = smem + ps * kWStageBytes + b * kBoxBytes + valid * 128;
+                    for (int c = lane; c < chunks; c += 32)
+                        *reinterpret_cast<uint4*>(box + c * 16) = make_uint4(0, 0, 0, 0);
+                }
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_addr(&ready_bar[ps]));
+                pend &= ~(1u << ps);
             }
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_addr(&ready_bar[pend_s]));
-            pend = false;
-            return true;
         };
         for (int t = blockIdx.x; t < total_tiles && !failed; t += gridDim.x) {
             int e, m, n;
@@ -582,11 +598,16 @@ grouped_wgrad_kernel(const __grid_constant__ CUtensorMap map_p,
             for (int ks = 0; ks < ksteps; ++ks, ++it) {
                 const int s = it % kWStages;
                 const uint32_t ph = (it / kWStages) & 1u;
-                bool ok = true;
-                if (lane == 0) ok = mbar_test(smem_addr(&empty_bar[s]), ph ^ 1u);
-                if (!__shfl_sync(0xFFFFFFFFu, ok, 0) && !service()) { failed = true; break; }
-                if (lane == 0) ok = mbar_wait(smem_addr(&empty_bar[s]), ph ^ 1u);
-                if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) { failed = true; break; }
+                // slot s is free once the MMAs of its last stage have completed
+                // (that stage, if partial, was fixed up here first)
+                bool got = false;
+                for (uint32_t i = 0; i < kPollLimit && !got; ++i) {
+                    poll();
+                    bool ok = false;
+                    if (lane == 0) ok = mbar_test(smem_addr(&empty_bar[s]), ph ^ 1u);
+                    got = __shfl_sync(0xFFFFFFFFu, ok, 0);
+                }
+                if (!got) { failed = true; break; }
                 const uint32_t base = smem_addr(smem + s * kWStageBytes);
                 const uint32_t fb = smem_addr(&full_bar[s]);
                 const int row = r0 + ks * 64;
@@ -598,16 +619,15 @@ grouped_wgrad_kernel(const __grid_constant__ CUtensorMap map_p,
                         tma_load_2d(base + (kWA + b) * kBoxBytes, &map_q, n * BN + b * 64, row, fb);
                 }
                 const int valid = min(64, r1 - row);
-                if (valid < 64) {
-                    if (!service()) { failed = true; break; }      // at most one pending
-                    pend = true;
-                    pend_s = s;
-                    pend_ph = ph;
-                    pend_valid = valid;
+                if (valid % 16 != 0) {
+                    pend |= 1u << s;
+                    pend_info = (pend_info & ~(0xFFu << (8 * s))) |
+                                (((ph << 7) | uint32_t(valid)) << (8 * s));
                 }
             }
         }
-        if (!failed && !service()) failed = true;
+        for (uint32_t i = 0; i < kPollLimit && pend && !failed; ++i) poll();
+        if (pend) failed = true;
         if (failed && lane == 0) s_failed = 1;
     } else if (warp == 1 && lane == 0) {
         // ------------------------------------------------------ MMA issuer
@@ -624,7 +644,8 @@ grouped_wgrad_kernel(const __grid_constant__ CUtensorMap map_p,
                 const int s = it % kWStages;
                 const uint32_t ph = (it / kWStages) & 1u;
                 if (!mbar_wait(smem_addr(&full_bar[s]), ph)) { s_failed = 1; break; }
-                if (r1 - (r0 + ks * 64) < 64) {
+                const int valid = min(64, r1 - (r0 + ks * 64));
+                if (valid % 16 != 0) {
                     if (!mbar_wait(smem_addr(&ready_bar[s]), (ready_phase >> s) & 1u)) {
                         s_failed = 1;
                         break;
@@ -634,8 +655,10 @@ grouped_wgrad_kernel(const __grid_constant__ CUtensorMap map_p,
                 tc_fence_after();
                 const uint32_t a_base = smem_addr(smem + s * kWStageBytes);
                 const uint32_t b_base = a_base + kWA * kBoxBytes;
+                const int nk = (valid + 15) / 16;
 #pragma unroll
                 for (int kk = 0; kk < 64 / 16; ++kk) {    // 16 token rows = 2 K groups
+                    if (kk >= nk) break;
                     const uint64_t bdesc = smem_desc_mn128(b_base + kk * 2048);
 #pragma unroll
                     for (int h = 0; h < 2; ++h)           // rows [128h, 128h+128) of the tile
