@@ -668,19 +668,58 @@ def run_vep8(args, rank, world, local_rank):
                                            dtype=torch.uint8, device=dev)))
     N = sum(int(q["buf"].shape[0]) for q in ranks)
     names = ["sort_chunks", "sort_chunks_inverse"]
+    # the virtual ranks' reorders are independent problems: each direction
+    # forks them over S streams and joins back onto `stream`, so one call's
+    # ramp-up overlaps another's tail
+    S = max(1, args.vep_streams)
+    side = [torch.cuda.Stream(device=dev) for _ in range(S)] if S > 1 else [stream]
+
+    def direction(srcs, dsts, splits, ws_key, idx):
+        if S > 1:
+            for st in side:
+                st.wait_stream(stream)
+        for i, (q, a, b) in enumerate(zip(ranks, srcs, dsts)):
+            moe.moe_sort_chunks(a, q[splits], idx, out=b, workspace=q[ws_key],
+                                stream=side[i % S])
+        if S > 1:
+            for st in side:
+                stream.wait_stream(st)
+
+    def fwd(bufs=None, ems=None):
+        direction(bufs or [q["buf"] for q in ranks], ems or [q["em"] for q in ranks], "sp",
+                  "ws_f", fwd_idx)
+
+    def inv(ems=None):
+        direction(ems or [q["em"] for q in ranks], [q["back"] for q in ranks], "spt", "ws_b",
+                  inv_idx)
+
+    # each direction of the timed step is one CUDA graph of its 8 launches
+    for _ in range(2):
+        fwd()
+        inv()
+    stream.synchronize()
+    graphs = []
+    for fn in (fwd, inv):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            fn()
+        graphs.append(g)
 
     def step(ev=None, bufs=None, ems=None):
-        ems = ems or [q["em"] for q in ranks]
         if ev is not None:
             ev[0].record(stream)
-        for q, src, em in zip(ranks, bufs or [q["buf"] for q in ranks], ems):
-            moe.moe_sort_chunks(src, q["sp"], fwd_idx, out=em, workspace=q["ws_f"],
-                                stream=stream)
+        if bufs is None:
+            with torch.cuda.stream(stream):
+                graphs[0].replay()
+        else:
+            fwd(bufs, ems)
         if ev is not None:
             ev[1].record(stream)
-        for q, em in zip(ranks, ems):
-            moe.moe_sort_chunks(em, q["spt"], inv_idx, out=q["back"], workspace=q["ws_b"],
-                                stream=stream)
+        if bufs is None:
+            with torch.cuda.stream(stream):
+                graphs[1].replay()
+        else:
+            inv(ems)
         if ev is not None:
             ev[2].record(stream)
 
@@ -780,6 +819,8 @@ def run_vep8(args, rank, world, local_rank):
                    "routed_rows_per_step": N,
                    "step": f"moe_sort_chunks rank-major -> expert-major for each of {R} virtual "
                            "ranks, then expert-major -> rank-major",
+                   "launch": f"each direction one CUDA graph of its {R} calls over {S} "
+                             f"stream{'s' if S > 1 else ''}",
                    "l2": "no flush: the step moves 537 MB each way, > 129 MB L2",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "roofline": {"bound": "hbm", "kernel": dominant, "achieved": round(ach, 1), "peak": peak,
@@ -935,6 +976,8 @@ def main(argv=None):
                     help="capacity / padded / aligned layout, e.g. 'cf=1.25,pad' or 'align=128'")
     ap.add_argument("--route-groups", default=None, metavar="G:KG",
                     help="route with group-limited routing: G expert groups, KG kept")
+    ap.add_argument("--vep-streams", type=int, default=4, metavar="S",
+                    help="vep8: streams the virtual ranks' calls are forked over")
     ap.add_argument("--workload", choices=["skewed", "layer", "vep8"], default=WORKLOAD,
                     help="skewed: the dispatch/combine step (default); layer: the full MoE "
                          "layer forward with the grouped SwiGLU; vep8: sort_chunks forward "

@@ -401,6 +401,65 @@ def test_sort_chunks_virtual_ep8_round_trip():
         assert to_host(back).tobytes() == buf.tobytes()
 
 
+def test_sort_chunks_virtual_ranks_concurrently_in_a_cuda_graph():
+    """The 8 virtual ranks' reorders forked over 4 streams and captured in
+    CUDA graphs (as the virtual-EP benchmark runs them): every rank's output
+    is still the oracle's, byte for byte, after repeated replays."""
+    d = wl.make("vep8")
+    R = L = 8
+    fwd = to_dev(np.array(moe.moe_chunk_idxs(R, L, False), np.int32))
+    inv = to_dev(np.array(moe.moe_chunk_idxs(R, L, True), np.int32))
+    ranks = []
+    for M, buf in _virtual_rank_buffers(d, R, L):
+        xd = to_dev(buf)
+        ranks.append(dict(M=M, buf=buf, x=xd, em=torch.empty_like(xd), back=torch.empty_like(xd),
+                          sp=to_dev(M.ravel().copy()), spt=to_dev(M.T.ravel().copy()),
+                          wf=torch.empty(moe.moe_sort_chunks_workspace_size(R * L),
+                                         dtype=torch.uint8, device="cuda"),
+                          wb=torch.empty(moe.moe_sort_chunks_workspace_size(R * L),
+                                         dtype=torch.uint8, device="cuda")))
+    main = torch.cuda.Stream()
+    side = [torch.cuda.Stream() for _ in range(4)]
+
+    def both():
+        for st in side:
+            st.wait_stream(main)
+        for i, q in enumerate(ranks):
+            moe.moe_sort_chunks(q["x"], q["sp"], fwd, out=q["em"], workspace=q["wf"],
+                                stream=side[i % 4])
+        for st in side:
+            main.wait_stream(st)
+        for st in side:
+            st.wait_stream(main)
+        for i, q in enumerate(ranks):
+            moe.moe_sort_chunks(q["em"], q["spt"], inv, out=q["back"], workspace=q["wb"],
+                                stream=side[i % 4])
+        for st in side:
+            main.wait_stream(st)
+
+    with torch.cuda.stream(main):
+        both()                                   # eager, then captured
+    main.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=main):
+        both()
+    for q in ranks:
+        q["em"].zero_()
+        q["back"].zero_()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(main):
+        for _ in range(3):
+            g.replay()
+    main.synchronize()
+    fwd_o = oracle.chunk_idxs(R, L, False)
+    for q in ranks:
+        assert moe.moe_workspace_status(q["wf"]) == 0
+        assert moe.moe_workspace_status(q["wb"]) == 0
+        ref = oracle.sort_chunks(q["buf"], q["M"].ravel(), fwd_o)
+        assert to_host(q["em"]).tobytes() == ref.tobytes()
+        assert to_host(q["back"]).tobytes() == q["buf"].tobytes()
+
+
 @pytest.mark.parametrize("R,L,H,dtype", [(3, 5, 100, "bf16"), (2, 2, 16, "f32"), (1, 9, 64, "bf16"),
                                          (16, 16, 1024, "bf16"),
                                          (40, 40, 64, "bf16"),       # C > 1024: plan kernel path
