@@ -203,6 +203,8 @@ def test_permute_then_unweighted_combine_k1_identity():
                          [("bf16", 1000, 4096, 64, 2, 0.0, True),
                           ("bf16", 300, 7168, 256, 8, 0.1, True),
                           ("bf16", 500, 1000, 32, 6, 0.2, False),
+                          ("bf16", 700, 2048, 64, 6, 0.1, True),   # the layer shape's k
+                          ("bf16", 333, 512, 16, 5, 0.0, True),
                           ("bf16", 129, 36, 8, 3, 0.0, True),    # 72-byte rows: element path
                           ("f32", 256, 128, 8, 2, 0.0, True),
                           ("f32", 99, 33, 8, 5, 0.3, True),
@@ -223,8 +225,8 @@ def test_combine_bit_exact(dtype, T, H, E, k, drop, weighted):
     assert d.max() == 0, f"max ulp {d.max()}, {np.count_nonzero(d)} mismatches"
 
 
-@pytest.mark.parametrize("k,weighted", [(2, True), (4, True), (8, True), (2, False), (6, False),
-                                        (8, False)])
+@pytest.mark.parametrize("k,weighted", [(2, True), (4, True), (5, True), (6, True), (8, True),
+                                        (2, False), (5, False), (6, False), (8, False)])
 def test_combine_bit_exact_under_cancellation(k, weighted):
     """Rows built to cancel (exactly, or down to a few ulps): every tier of
     the combine -- float fast path (or, unweighted, the exact TwoSum chain),

@@ -798,6 +798,7 @@ extern "C" moe_status_t moe_combine(const void* expert_out, moe_dtype_t dtype, i
                 k <= 1 ? (plain ? combine_bf16_regs_kernel<1, true> : combine_bf16_regs_kernel<1, false>)
                 : k <= 2 ? (plain ? combine_bf16_regs_kernel<2, true> : combine_bf16_regs_kernel<2, false>)
                 : k <= 4 ? (plain ? combine_bf16_regs_kernel<4, true> : combine_bf16_regs_kernel<4, false>)
+                : k <= 6 ? (plain ? combine_bf16_regs_kernel<6, true> : combine_bf16_regs_kernel<6, false>)
                          : (plain ? combine_bf16_regs_kernel<8, true> : combine_bf16_regs_kernel<8, false>);
             kern<<<grid_for((const void*)kern, kThreads, want), kThreads, 0, s>>>(
                 yv, T, H / 8, k, n_rows, slot_pos, topk_w, ov, cb, dd_bound_factor(k));
