@@ -245,8 +245,13 @@ __device__ __forceinline__ bool dd_sum_bf16(const float* w, const float* y, cons
 // registers, so an element whose rounding cannot be certified is recomputed
 // in double from the same registers (no reload).  (A cp.async ring as in
 // the backward measured slower here: 352 vs 345 us at T=16384, H=7168, k=8.)
+// Up to six slots the kernel is held to 64 registers (4 blocks, 32 warps per
+// SM; a few bytes of rare-path spill): at one wave of tokens it is bound by
+// instruction latency, which more resident warps hide.  Eight slots keep
+// up to 128 (2 blocks, 16 warps per SM: the DeepSeek-shaped workload is
+// HBM-bound there).
 template <int KMAX, bool PLAIN>   // PLAIN: topk_w == NULL (plain sum)
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, KMAX <= 6 ? 4 : 2)
 combine_bf16_regs_kernel(const uint4* __restrict__ y, int64_t T, int64_t nvec, int k, int64_t n_rows,
                          const int32_t* __restrict__ slot_pos, const float* __restrict__ topk_w,
                          uint4* __restrict__ out, float cbound, float dd_bound) {
