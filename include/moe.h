@@ -439,6 +439,21 @@ moe_status_t moe_workspace_status(const void* workspace, void* stream);
  * One word per device, shared by all streams. */
 moe_status_t moe_device_status(void* stream);
 
+/* Health check of the failure path that the pipelined kernels (the grouped
+ * GEMMs and the bulk-copy permutes) rely on; no counterpart on the pages.
+ * One block waits on an mbarrier that nothing completes, through the same
+ * bounded poll loop those kernels use but limited to `polls` polls
+ * (1 <= polls <= 2^20; each poll of mbarrier.try_wait suspends the thread for
+ * at most a short hardware-defined time), gives up, records MOE_ERR_TIMEOUT
+ * in the workspace status word (detail = polls) and returns normally, so the
+ * context stays usable.  Read the outcome with moe_workspace_status().
+ *   workspace: device memory, 256-byte aligned, >= 256 bytes (only its
+ *   status header is written).
+ * Returns MOE_ERR_WORKSPACE or MOE_ERR_INVALID_ARG before any launch on bad
+ * arguments, MOE_ERR_CUDA if the launch fails. */
+moe_status_t moe_selftest_timeout(void* workspace, size_t workspace_bytes, uint32_t polls,
+                                  void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -130,3 +130,14 @@ def test_binding_rejects_cpu_tensors(lib):
         moe.moe_route(torch.zeros((4, 8)), 2)
     with pytest.raises(ValueError):
         moe.moe_combine(torch.zeros((8, 4)), torch.zeros((4, 2), dtype=torch.int32))
+
+
+def test_timeout_selftest_validates_before_launch(lib):
+    P = ctypes.c_void_p
+    # no, misaligned or too small a workspace; a poll count of 0 or past the
+    # pipelines' own limit (2^20)
+    assert lib.moe_selftest_timeout(None, 256, 16, None) == 3
+    assert lib.moe_selftest_timeout(P(0x1010), 256, 16, None) == 3
+    assert lib.moe_selftest_timeout(P(0x1000), 128, 16, None) == 3
+    assert lib.moe_selftest_timeout(P(0x1000), 256, 0, None) == 1
+    assert lib.moe_selftest_timeout(P(0x1000), 256, (1 << 20) + 1, None) == 1

@@ -29,7 +29,7 @@ __all__ = [
     "moe_route_grouped", "moe_expert_capacity", "moe_route_layout_rows", "moe_route_layout",
     "moe_fill_pad_rows", "moe_quantize_fp8", "moe_dequantize_fp8", "moe_permute_fp8",
     "moe_route_backward", "moe_grouped_swiglu_save", "moe_grouped_swiglu_dgrad",
-    "moe_grouped_swiglu_wgrad", "MOE_STATUS_WORKSPACE_BYTES",
+    "moe_grouped_swiglu_wgrad", "MOE_STATUS_WORKSPACE_BYTES", "moe_selftest_timeout",
 ]
 
 # Bytes of the status-only workspace of the grouped SwiGLU training calls.
@@ -97,6 +97,7 @@ def load_library():
             "moe_expert_scale": ([P, I, I64, I64, I, P, P, P, P], I),
             "moe_workspace_status": ([P, P], I),
             "moe_device_status": ([P], I),
+            "moe_selftest_timeout": ([P, SZ, ctypes.c_uint32, P], I),
             "moe_grouped_swiglu_pack": ([P, P, I, I64, I64, P, P, P], I),
             "moe_grouped_swiglu_workspace_size": ([I64, I, I64, I64, PSZ], I),
             "moe_grouped_swiglu": ([P, P, P, P, I64, I, I64, I64, P, P, SZ, P], I),
@@ -741,3 +742,17 @@ def moe_device_status(stream=None) -> int:
     """Synchronise the stream, then read and clear the library's device status
     word (0 = MOE_OK, 5 = MOE_ERR_TIMEOUT from a kernel without a workspace)."""
     return load_library().moe_device_status(_stream(stream))
+
+
+def moe_selftest_timeout(polls: int = 1024, workspace: Optional[torch.Tensor] = None,
+                         device=None, stream=None) -> int:
+    """Run the bounded-wait health check (moe.h): a kernel waits on a barrier
+    nothing completes, gives up after `polls` polls and records the timeout;
+    returns the workspace status it left (5 = MOE_ERR_TIMEOUT expected)."""
+    if workspace is None:
+        workspace = torch.empty(MOE_STATUS_WORKSPACE_BYTES, dtype=torch.uint8,
+                                device=device if device is not None else "cuda")
+    _cuda(workspace, "workspace", torch.uint8)
+    _ok("moe_selftest_timeout", load_library().moe_selftest_timeout(
+        _p(workspace), workspace.numel(), polls, _stream(stream)))
+    return moe_workspace_status(workspace, stream)

@@ -55,7 +55,35 @@ int sm_count() {
     return cached[dev];
 }
 
+namespace {
+
+// One block waits on an mbarrier that nothing completes, through the same
+// bounded poll loop as the pipelined kernels, gives up after `polls` polls
+// and records the timeout in the workspace header.  Nothing is in flight on
+// the barrier, so the block simply returns.
+__global__ void timeout_selftest_kernel(WsHeader* header, uint32_t polls) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x != 0) return;
+    mbar_init(smem_addr(&bar), 1);
+    mbar_fence_init();
+    const bool done = mbar_wait_bounded(smem_addr(&bar), 0, polls);
+    header->status = done ? MOE_OK : MOE_ERR_TIMEOUT;
+    header->detail = done ? 0u : polls;
+}
+
+}  // namespace
 }  // namespace moe
+
+extern "C" moe_status_t moe_selftest_timeout(void* workspace, size_t workspace_bytes,
+                                             uint32_t polls, void* stream) {
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & (moe::kWsAlign - 1)) ||
+        workspace_bytes < moe::kWsAlign)
+        return MOE_ERR_WORKSPACE;
+    if (polls < 1 || polls > moe::kSpinLimit) return MOE_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    moe::timeout_selftest_kernel<<<1, 32, 0, s>>>(static_cast<moe::WsHeader*>(workspace), polls);
+    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
 
 extern "C" const char* moe_status_string(moe_status_t status) {
     switch (status) {
