@@ -119,3 +119,32 @@ def test_permute_fp8_matches_oracle(T, H, block, k, E, cap):
     exp_s[si >= 0] = sc_o[si[si >= 0]]
     assert (_fp8_host(oq) == exp_q).all()
     assert (to_host(osc).view(np.uint32) == exp_s.view(np.uint32)).all()
+
+
+def test_quantize_on_and_near_e4m3_midpoints():
+    """Quotients on an e4m3 rounding midpoint (ties to even) or within a few
+    float ulps of one, where the code depends on the last bits of the IEEE
+    quotient; bit-exact against the oracle."""
+    rng = np.random.default_rng(77)
+    T, H, block = 512, 4096, 128
+    x = rng.standard_normal((T, H)).astype(np.float32)
+    # rows 0-15: every block has amax = 448 (scale exactly 1) and its other
+    # values on midpoints 2^e (1 + (2m+1)/16), e = -6..7, with random signs
+    e = rng.integers(-6, 8, (16, H))
+    m = rng.integers(0, 8, (16, H))
+    x[:16] = np.ldexp(1.0 + (2 * m + 1) / 16.0, e) * rng.choice([-1.0, 1.0], (16, H))
+    x[:16, ::block] = 448.0
+    xb = wl.f32_to_bf16_bits(x)
+    # the random rows must reach quotients within 8 float ulps of a midpoint
+    xf = wl.bf16_bits_to_f32(xb).reshape(T, H // block, block)
+    amax = np.abs(xf).max(axis=2, keepdims=True)
+    s = np.where(amax > 0, amax / np.float32(448.0), np.float32(1.0)).astype(np.float32)
+    q0 = (xf * (np.float32(1.0) / s)).astype(np.float32)
+    bits = q0.view(np.uint32)
+    mag = bits & 0x7FFFFFFF
+    near = (np.abs((bits & 0xFFFFF).astype(np.int64) - 0x80000) <= 8) & (mag >= 0x3C800000)
+    assert near[16:].sum() >= 5 and near[:16].sum() > 1000
+    q, sc = moe.moe_quantize_fp8(to_dev(xb), block)
+    q_o, sc_o = oracle.quantize_fp8(xb, block)
+    assert (to_host(sc).view(np.uint32) == sc_o.view(np.uint32)).all()
+    assert (_fp8_host(q) == q_o).all()
