@@ -73,6 +73,7 @@ def fp8_bytes(T, H, k, block=128):
     N, nb = T * k, H // block
     return {
         "quantize_fp8": T * H * 2 + T * H + T * nb * 4,
+        "permute_quantize_fp8": T * H * 2 + N * H + N * nb * 4 + N * 4,
         "permute": T * H + N * H + (T + N) * nb * 4 + 2 * N * 4,
         "dequantize_fp8": N * H + N * nb * 4 + N * H * 2,
     }
@@ -113,6 +114,9 @@ KERNEL_SOURCES = {
     "combine_backward": ("unpermute_combine_gb300/csrc/combine.cu",
                          "unpermute_combine_gb300/csrc/common.cuh"),
     "quantize_fp8": ("unpermute_combine_gb300/csrc/fp8.cu", "unpermute_combine_gb300/csrc/common.cuh"),
+    "permute_quantize_fp8": ("unpermute_combine_gb300/csrc/fp8.cu",
+                             "unpermute_combine_gb300/csrc/pipeline.cuh",
+                             "unpermute_combine_gb300/csrc/common.cuh"),
     "swiglu_dgrad": ("unpermute_combine_gb300/csrc/grouped_swiglu.cu",
                      "unpermute_combine_gb300/csrc/pipeline.cuh"),
     "swiglu_wgrad": ("unpermute_combine_gb300/csrc/grouped_swiglu.cu",
@@ -290,7 +294,8 @@ def run_ours(args, rank, world, local_rank):
                                    alignment=lay.get("align", 1), max_rows=rows, stream=stream)
               if lay else None)
         xp = torch.empty((rows, H), dtype=torch.bfloat16, device=dev)
-        fp8 = bool(args.fp8)
+        fp8 = bool(args.fp8 or args.fp8_split)
+        fp8_fused = fp8 and not args.fp8_split and H * 2 <= 16384
         if fp8:
             fp8_tok = (torch.empty((T, H), dtype=torch.float8_e4m3fn, device=dev),
                        torch.empty((T, H // 128), dtype=torch.float32, device=dev))
@@ -328,7 +333,8 @@ def run_ours(args, rank, world, local_rank):
         names += ["combine_backward", "swiglu_dgrad", "swiglu_wgrad", "permute_backward",
                   "route_backward"]
     if fp8:
-        names[1:2] = ["quantize_fp8", "permute", "dequantize_fp8"]
+        names[1:2] = (["permute_quantize_fp8", "dequantize_fp8"] if fp8_fused else
+                      ["quantize_fp8", "permute", "dequantize_fp8"])
     router_bwd = bool(args.router_bwd) and not layer
     if router_bwd:
         names.append("route_backward")
@@ -358,9 +364,13 @@ def run_ours(args, rank, world, local_rank):
         if fp8:
             # FP8 dispatch: quantize, move e4m3 rows and scale rows, and
             # dequantize in place of the expert's input conversion
-            moe.moe_quantize_fp8(xx, 128, out=fp8_tok, stream=stream)
-            mark()
-            moe.moe_permute_fp8(fp8_tok[0], fp8_tok[1], rr.slot_pos, out=fp8_rows, stream=stream)
+            if fp8_fused:
+                moe.moe_permute_quantize_fp8(xx, rr.slot_pos, 128, out=fp8_rows, stream=stream)
+            else:
+                moe.moe_quantize_fp8(xx, 128, out=fp8_tok, stream=stream)
+                mark()
+                moe.moe_permute_fp8(fp8_tok[0], fp8_tok[1], rr.slot_pos, out=fp8_rows,
+                                    stream=stream)
             mark()
             moe.moe_dequantize_fp8(fp8_rows[0], fp8_rows[1], 128, out=xp, stream=stream)
         else:
@@ -526,7 +536,7 @@ def run_ours(args, rank, world, local_rank):
                    "frac": round(gbs / peak, 4)}
     dominant = max(names, key=lambda n: per[n])
     pc_time = sum(per[n] for n in names if n in ("quantize_fp8", "permute", "dequantize_fp8",
-                                                  "combine"))
+                                                  "permute_quantize_fp8", "combine"))
     if layer:
         t_sus, t_burst, t_kind = measured_tensor_peak()
         gemms = ["grouped_swiglu"] + (["swiglu_dgrad", "swiglu_wgrad"] if train else [])
@@ -566,8 +576,11 @@ def run_ours(args, rank, world, local_rank):
     if router_bwd:
         step_desc += " + moe_route_backward"
     if fp8:
-        step_desc = step_desc.replace("moe_permute", "moe_quantize_fp8(block 128) + "
-                                      "moe_permute_fp8(e4m3 rows + scale rows) + moe_dequantize_fp8", 1)
+        step_desc = step_desc.replace(
+            "moe_permute", ("moe_permute_quantize_fp8(block 128: bf16 rows -> e4m3 rows + scale "
+                            "rows in the slots) + moe_dequantize_fp8") if fp8_fused else
+            ("moe_quantize_fp8(block 128) + moe_permute_fp8(e4m3 rows + scale rows) + "
+             "moe_dequantize_fp8"), 1)
     if lay:
         step_desc = step_desc.replace(" + moe_permute", f" + moe_route_layout(capacity={cap}, "
                                       f"pad={lay.get('pad', False)}, alignment="
@@ -579,7 +592,7 @@ def run_ours(args, rank, world, local_rank):
         if lay:
             launches += 1                 # pad rows of the expert-output gradient
     if fp8:
-        launches += 2                     # quantize, dequantize
+        launches += 1 if fp8_fused else 2   # (quantize,) dequantize
     if router_bwd:
         launches += 1
     if lay:
@@ -975,7 +988,10 @@ def main(argv=None):
                     help="append the router k-softmax backward (grad_probs -> grad_logits) "
                          "to the training step")
     ap.add_argument("--fp8", action="store_true",
-                    help="FP8 dispatch: quantize, move e4m3 rows + scales, dequantize")
+                    help="FP8 dispatch: quantize into the slot rows (one fused launch), "
+                         "dequantize")
+    ap.add_argument("--fp8-split", action="store_true",
+                    help="FP8 dispatch as separate quantize and e4m3 permute launches")
     ap.add_argument("--layout", default=None, metavar="SPEC",
                     help="capacity / padded / aligned layout, e.g. 'cf=1.25,pad' or 'align=128'")
     ap.add_argument("--route-groups", default=None, metavar="G:KG",

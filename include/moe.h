@@ -425,6 +425,21 @@ moe_status_t moe_permute_fp8(const void* x_q, const float* scales, int64_t T, in
                              int block, int k, int64_t n_rows, const int32_t* slot_pos,
                              void* out_q, float* out_scales, void* stream);
 
+/* moe_permute_quantize_fp8: moe_quantize_fp8 then moe_permute_fp8 in one
+ * launch, with no token-order e4m3 copy in between: each token's bf16 row
+ * x [T,H] is read once, quantized (the same scales and codes as
+ * moe_quantize_fp8, bit for bit) and written to every slot row slot_pos
+ * [T,k] names: out_q [n_rows,H] e4m3, out_scales [n_rows, H/block] float.
+ * Slots outside [0, n_rows) (dropped, -1) are skipped; rows no slot names are
+ * left as they were.  Requires x and out_q 16-byte aligned, out_scales 4-byte
+ * aligned (else MOE_ERR_INVALID_ARG) and H <= 8192 (else
+ * MOE_ERR_UNSUPPORTED: use the two calls); block and H as moe_quantize_fp8;
+ * 1 <= k <= 32.  A bounded copy wait that gives up is reported by
+ * moe_device_status. */
+moe_status_t moe_permute_quantize_fp8(const void* x, int64_t T, int64_t H, int block, int k,
+                                      int64_t n_rows, const int32_t* slot_pos, void* out_q,
+                                      float* out_scales, void* stream);
+
 /* ------------------------------------------------- workspace status word
  * Waits for `stream`, then reads the status a previous call left in
  * `workspace`: MOE_OK, MOE_ERR_DEVICE_CHECK or MOE_ERR_TIMEOUT.  Each call

@@ -141,3 +141,19 @@ def test_timeout_selftest_validates_before_launch(lib):
     assert lib.moe_selftest_timeout(P(0x1000), 128, 16, None) == 3
     assert lib.moe_selftest_timeout(P(0x1000), 256, 0, None) == 1
     assert lib.moe_selftest_timeout(P(0x1000), 256, (1 << 20) + 1, None) == 1
+
+
+def test_permute_quantize_fp8_validates_before_launch(lib):
+    P = ctypes.c_void_p
+    f = P(0x1000)
+    # block not 32/64/128/256; H not a multiple of block; k out of range;
+    # H beyond one shared-memory stage; a missing or misaligned buffer
+    assert lib.moe_permute_quantize_fp8(f, 4, 480, 48, 2, 8, f, f, f, None) == 2
+    assert lib.moe_permute_quantize_fp8(f, 4, 200, 128, 2, 8, f, f, f, None) == 1
+    assert lib.moe_permute_quantize_fp8(f, 4, 256, 128, 0, 8, f, f, f, None) == 1
+    assert lib.moe_permute_quantize_fp8(f, 4, 256, 128, 33, 8, f, f, f, None) == 1
+    assert lib.moe_permute_quantize_fp8(f, 4, 16384, 128, 2, 8, f, f, f, None) == 2
+    assert lib.moe_permute_quantize_fp8(f, 4, 256, 128, 2, 8, None, f, f, None) == 1
+    assert lib.moe_permute_quantize_fp8(P(0x1008), 4, 256, 128, 2, 8, f, f, f, None) == 1
+    assert lib.moe_permute_quantize_fp8(f, 4, 256, 128, 2, 8, f, P(0x1008), f, None) == 1
+    assert lib.moe_permute_quantize_fp8(f, 0, 256, 128, 2, 8, None, None, None, None) == 0

@@ -69,6 +69,9 @@ def test_fp8_bytes_at_the_deepseek_shape():
     bf = bench.algorithmic_bytes(T, H, 256, 8, 2)["permute"]
     assert f["permute"] < 0.52 * bf
     assert f["dequantize_fp8"] == 3 * N * H + 4 * N * nb
+    # fused: bf16 rows read once, e4m3 + scale rows written to every slot
+    assert f["permute_quantize_fp8"] == 2 * T * H + N * H + 4 * N * nb + 4 * N
+    assert f["permute_quantize_fp8"] < f["quantize_fp8"] + f["permute"]
 
 
 def test_layout_bytes_count_only_kept_rows():

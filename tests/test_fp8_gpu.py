@@ -148,3 +148,32 @@ def test_quantize_on_and_near_e4m3_midpoints():
     q_o, sc_o = oracle.quantize_fp8(xb, block)
     assert (to_host(sc).view(np.uint32) == sc_o.view(np.uint32)).all()
     assert (_fp8_host(q) == q_o).all()
+
+
+@pytest.mark.parametrize("T,H,block,k,E,cap", [
+    (1000, 7168, 128, 8, 64, 0),     # the DeepSeek row width
+    (5000, 2048, 128, 6, 64, 0),     # many tokens per CTA: the ring wraps many times
+    (513, 4096, 32, 4, 16, 0),
+    (300, 96, 32, 2, 8, 0),          # a 192-byte row
+    (700, 2048, 64, 6, 32, 100),     # capacity drops: unnamed rows stay untouched
+    (64, 8192, 256, 3, 8, 0),        # the widest row one stage holds
+    (4, 512, 128, 1, 2, 0)])         # fewer tokens than CTAs
+def test_permute_quantize_fp8_matches_quantize_then_permute(T, H, block, k, E, cap):
+    idx, w = wl.random_routing(T + H + 3 * k, T, E, k)
+    rows = moe.moe_route_layout_rows(T, E, k, cap, False, 1)
+    r = moe.moe_route_layout(to_dev(idx), to_dev(w), E, capacity=cap, max_rows=rows)
+    o = oracle.route_layout(idx, w, E, capacity=cap, max_rows=rows)
+    x = _tricky_rows(T * 5 + H, T, H)
+    oq = _fp8_dev(np.full((rows, H), 0x3C, np.uint8))
+    osc = torch.full((rows, H // block), -2.0, dtype=torch.float32, device="cuda")
+    moe.moe_permute_quantize_fp8(to_dev(x), r.slot_pos, block, out=(oq, osc))
+    torch.cuda.synchronize()
+    assert moe.moe_device_status() == 0
+    q_o, sc_o = oracle.quantize_fp8(x, block)
+    si = o["sorted_indices"]
+    exp_q = np.full((rows, H), 0x3C, np.uint8)
+    exp_s = np.full((rows, H // block), -2.0, np.float32)
+    exp_q[si >= 0] = q_o[si[si >= 0]]
+    exp_s[si >= 0] = sc_o[si[si >= 0]]
+    assert (_fp8_host(oq) == exp_q).all()
+    assert (to_host(osc).view(np.uint32) == exp_s.view(np.uint32)).all()

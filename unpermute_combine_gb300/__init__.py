@@ -30,6 +30,7 @@ __all__ = [
     "moe_fill_pad_rows", "moe_quantize_fp8", "moe_dequantize_fp8", "moe_permute_fp8",
     "moe_route_backward", "moe_grouped_swiglu_save", "moe_grouped_swiglu_dgrad",
     "moe_grouped_swiglu_wgrad", "MOE_STATUS_WORKSPACE_BYTES", "moe_selftest_timeout",
+    "moe_permute_quantize_fp8",
 ]
 
 # Bytes of the status-only workspace of the grouped SwiGLU training calls.
@@ -86,6 +87,7 @@ def load_library():
             "moe_quantize_fp8": ([P, I64, I64, I, P, P, P], I),
             "moe_dequantize_fp8": ([P, P, I64, I64, I, P, P], I),
             "moe_permute_fp8": ([P, P, I64, I64, I, I, I64, P, P, P, P], I),
+            "moe_permute_quantize_fp8": ([P, I64, I64, I, I, I64, P, P, P, P], I),
             "moe_route_backward": ([P, P, P, I64, I, I, P, P], I),
             "moe_route_grouped": ([P, I64, I, I, I, I, P, P, P, P, P, P, P, P, P, P, SZ, P], I),
             "moe_permute": ([P, I, I64, I64, I, I64, P, P, P], I),
@@ -383,6 +385,35 @@ def moe_permute_fp8(x_q: torch.Tensor, scales: torch.Tensor, slot_pos: torch.Ten
     _ok("moe_permute_fp8", load_library().moe_permute_fp8(
         _p(x_q), _p(scales), T, H, block, k, oq.shape[0], _p(slot_pos), _p(oq), _p(osc),
         _stream(stream)))
+    return oq, osc
+
+
+def moe_permute_quantize_fp8(x: torch.Tensor, slot_pos: torch.Tensor, block: int = 128,
+                             out=None, n_rows: Optional[int] = None, stream=None):
+    """Quantize bf16 token rows to e4m3 with per-block scales and move them to
+    the slot rows slot_pos names, in one launch (the same bytes as
+    moe_quantize_fp8 followed by moe_permute_fp8); returns
+    (out_q [n_rows,H] e4m3, out_scales [n_rows,H/block] float32)."""
+    _cuda(x, "x", torch.bfloat16, 2)
+    _cuda(slot_pos, "slot_pos", torch.int32, 2)
+    T, H = x.shape
+    k = slot_pos.shape[1]
+    if slot_pos.shape[0] != T:
+        raise ValueError("slot_pos must have one row per token")
+    if block <= 0 or H % block != 0:
+        raise ValueError("H must be a multiple of block")
+    if out is None:
+        rows = T * k if n_rows is None else n_rows
+        oq = torch.empty((rows, H), dtype=torch.float8_e4m3fn, device=x.device)
+        osc = torch.empty((rows, H // block), dtype=torch.float32, device=x.device)
+    else:
+        oq, osc = out
+        _cuda(oq, "out_q", torch.float8_e4m3fn, 2)
+        _cuda(osc, "out_scales", torch.float32, 2)
+        if oq.shape[0] != osc.shape[0] or oq.shape[1] != H or osc.shape[1] != H // block:
+            raise ValueError("out_q must be [n_rows, H] and out_scales [n_rows, H/block]")
+    _ok("moe_permute_quantize_fp8", load_library().moe_permute_quantize_fp8(
+        _p(x), T, H, block, k, oq.shape[0], _p(slot_pos), _p(oq), _p(osc), _stream(stream)))
     return oq, osc
 
 

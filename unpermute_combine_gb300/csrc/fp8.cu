@@ -20,6 +20,7 @@
 #include <cuda_fp16.h>
 
 #include "common.cuh"
+#include "pipeline.cuh"
 
 namespace moe {
 namespace {
@@ -120,6 +121,126 @@ dequantize_fp8_kernel(const uint2* __restrict__ q, const float* __restrict__ sca
     }
 }
 
+// ------------------------------------------- fused quantize + permute
+// One CTA of 8 warps per token at a time.  Thread 0 bulk-loads the token's
+// bf16 row into a ring stage; all threads quantize it into the stage's e4m3
+// area with the arithmetic of quantize_fp8_kernel (16-byte vectors, lane
+// groups of G owning a block, IEEE quotient, cvt.rn.satfinite); the scale of
+// each block goes straight to the token's slot rows of out_scales, and lanes
+// 0..k-1 of warp 0 each bulk-store the e4m3 row to their slot row.  The
+// input area is refilled as soon as every thread has read it; the output
+// area is written again only after the stores from it have read it.  So the
+// row is read from HBM once and written k times in e4m3, with no
+// token-order e4m3 copy in between.  (Measured at T=16384, H=7168, k=8:
+// 8 warps and 3 stages 193 us; 4 warps 235 us, 16 warps 208 us; 2 stages
+// 210-212 us, 4 stages 316 us.)
+constexpr int kPQThreads = 256;
+constexpr int kPQStages = 3;
+constexpr int kPQRowMax = 16384;              // bf16 bytes of a row in one stage (H <= 8192)
+
+template <int G>
+__global__ void __launch_bounds__(kPQThreads)
+permute_quantize_fp8_kernel(const uint8_t* __restrict__ x, int64_t T, int H, int k,
+                            int64_t n_rows, const int32_t* __restrict__ slot_pos,
+                            uint8_t* __restrict__ out_q, float* __restrict__ out_scales,
+                            uint32_t* __restrict__ status) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ __align__(8) uint64_t full_bar[kPQStages];
+    __shared__ int32_t s_slot[2][kMaxTopK];
+    __shared__ int s_failed;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const uint32_t in_bytes = uint32_t(H) * 2u, stage_bytes = uint32_t(H) * 3u;
+    const int nvec = H / 8;                    // 16-byte bf16 vectors of a row
+    const int nb = H / (8 * G);                // scale blocks of a row
+    const int64_t first = blockIdx.x;
+    const int64_t my = first < T ? (T - first + gridDim.x - 1) / gridDim.x : 0;
+    const uint32_t smem0 = smem_addr(smem);
+    if (tid == 0) {
+        for (int st = 0; st < kPQStages; ++st) mbar_init(smem_addr(&full_bar[st]), 1);
+        mbar_fence_init();
+        s_failed = 0;
+    }
+    __syncthreads();
+    auto issue_load = [&](int64_t q) {
+        const int64_t t = first + q * int64_t(gridDim.x);
+        const int st = int(q % kPQStages);
+        const uint32_t fb = smem_addr(&full_bar[st]);
+        mbar_expect_tx(fb, in_bytes);
+        bulk_load(smem0 + uint32_t(st) * stage_bytes, x + t * int64_t(in_bytes), in_bytes, fb);
+    };
+    if (tid == 0)
+        for (int64_t q = 0; q < my && q < kPQStages; ++q) issue_load(q);
+
+    for (int64_t q = 0; q < my; ++q) {
+        const int64_t t = first + q * int64_t(gridDim.x);
+        const int st = int(q % kPQStages);
+        const uint32_t ph = uint32_t(q / kPQStages) & 1u;
+        int32_t* slots = s_slot[q & 1];
+        int32_t p = -1;
+        if (warp == 0 && lane < k) {
+            // this lane's store of token q - kPQStages (same stage) has read it
+            bulk_wait_read<kPQStages - 1>();
+            p = slot_pos[t * k + lane];
+            if (p < 0 || p >= n_rows) p = -1;
+            slots[lane] = p;
+        }
+        if (!mbar_wait(smem_addr(&full_bar[st]), ph)) s_failed = 1;
+        __syncthreads();
+        if (s_failed) break;
+
+        const uint8_t* in = smem + uint32_t(st) * stage_bytes;
+        uint8_t* outq = smem + uint32_t(st) * stage_bytes + in_bytes;
+        // warp-uniform trip count; a G-group is wholly inside or outside the row
+        for (int v0 = warp * 32; v0 < nvec; v0 += kPQThreads) {
+            const int v = v0 + lane;
+            const bool live = v < nvec;
+            const uint4 xv = live ? *reinterpret_cast<const uint4*>(in + v * 16)
+                                  : make_uint4(0, 0, 0, 0);
+            const uint32_t w[4] = {xv.x, xv.y, xv.z, xv.w};
+            float f[8];
+            uint32_t m = 0;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                f[2 * i] = __uint_as_float(w[i] << 16);
+                f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+                m = max(m, max((w[i] << 16) & 0x7FFFFFFFu, w[i] & 0x7FFF0000u));
+            }
+#pragma unroll
+            for (int off = G / 2; off > 0; off >>= 1)
+                m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, off));
+            const float amax = __uint_as_float(m);
+            const float sc = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+            if (live) {
+                *reinterpret_cast<uint2*>(outq + v * 8) = make_uint2(q4(f, sc), q4(f + 4, sc));
+                if ((lane & (G - 1)) == 0) {
+                    const int blk = v / G;
+                    for (int j = 0; j < k; ++j) {
+                        const int32_t pj = slots[j];
+                        if (pj >= 0) out_scales[int64_t(pj) * nb + blk] = sc;
+                    }
+                }
+            }
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncthreads();
+        if (warp == 0 && lane < k) {
+            if (p >= 0) bulk_store(out_q + int64_t(p) * H, smem_addr(outq), uint32_t(H));
+            bulk_commit();
+        }
+        if (tid == 0 && q + kPQStages < my) issue_load(q + kPQStages);
+    }
+    if (warp == 0 && lane < k) bulk_wait_all();
+    if (tid == 0 && s_failed && status) atomicExch(status, uint32_t(MOE_ERR_TIMEOUT));
+}
+
+int grid_pq(const void* kernel, size_t smem, int64_t T) {
+    int per_sm = 0;
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kPQThreads, smem);
+    if (per_sm < 1) per_sm = 1;
+    const int64_t cap = int64_t(sm_count()) * per_sm;
+    return int(T < cap ? (T > 0 ? T : 1) : cap);
+}
+
 int grid_for(const void* kernel, int64_t nvec, int unroll) {
     int per_sm = 0;
     cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, 0);
@@ -191,5 +312,38 @@ extern "C" moe_status_t moe_dequantize_fp8(const void* x_q, const float* scales,
         default: MOE_DEQUANT(32); break;
     }
 #undef MOE_DEQUANT
+    return launch_status();
+}
+
+extern "C" moe_status_t moe_permute_quantize_fp8(const void* x, int64_t T, int64_t H, int block,
+                                                 int k, int64_t n_rows,
+                                                 const int32_t* slot_pos, void* out_q,
+                                                 float* out_scales, void* stream) {
+    const moe_status_t st = check_block(T, H, block);
+    if (st != MOE_OK) return st;
+    if (k < 1 || k > kMaxTopK || n_rows < 0) return MOE_ERR_INVALID_ARG;
+    if (T == 0 || H == 0) return MOE_OK;
+    if (H * 2 > kPQRowMax) return MOE_ERR_UNSUPPORTED;
+    if (!x || !slot_pos || !out_q || !out_scales) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(out_q) || (reinterpret_cast<uintptr_t>(out_scales) & 3))
+        return MOE_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t smem = size_t(kPQStages) * size_t(H) * 3;
+    const uint8_t* xb = static_cast<const uint8_t*>(x);
+    uint8_t* qb = static_cast<uint8_t*>(out_q);
+#define MOE_PQ(G_)                                                                              \
+    do {                                                                                        \
+        const void* kern = (const void*)permute_quantize_fp8_kernel<G_>;                        \
+        if (!opt_in_smem(kern, int(smem))) return MOE_ERR_CUDA;                                 \
+        permute_quantize_fp8_kernel<G_><<<grid_pq(kern, smem, T), kPQThreads, smem, s>>>(        \
+            xb, T, int(H), k, n_rows, slot_pos, qb, out_scales, device_status_word());         \
+    } while (0)
+    switch (block) {
+        case 32: MOE_PQ(4); break;
+        case 64: MOE_PQ(8); break;
+        case 128: MOE_PQ(16); break;
+        default: MOE_PQ(32); break;
+    }
+#undef MOE_PQ
     return launch_status();
 }
