@@ -84,14 +84,26 @@ def test_route_edge_shapes(T, E, k):
     _assert_route_equal(r, o, E)
 
 
-def test_route_all_tokens_on_one_expert():
-    T, E, k = 1000, 64, 1
-    logits = np.random.default_rng(1).standard_normal((T, E)).astype(np.float32)
-    logits[:, 37] += 100.0
+@pytest.mark.parametrize("T,E,hot", [(1000, 64, [37]),
+                                     (40000, 256, [3, 17, 42, 99, 100, 200, 201, 255])])
+def test_route_all_tokens_on_the_same_experts(T, E, hot):
+    """Every token picks the same k experts: k segments of T rows each and
+    every other expert empty (T = 40000 is beyond the fused scan)."""
+    k = len(hot)
+    logits = np.random.default_rng(T + E).standard_normal((T, E)).astype(np.float32)
+    logits[:, hot] += 100.0
     r, o = _route_both(logits, k)
     _assert_route_equal(r, o, E)
     c = to_host(r.counts)
-    assert c[37] == T and c.sum() == T
+    assert (c[hot] == T).all() and c.sum() == T * k
+    # the permute and the combine on this layout, bit-exact
+    x = wl.random_activation(E + k, (T, 64), "bf16")
+    xp = moe.moe_permute(to_dev(x), r.slot_pos)
+    out = to_host(moe.moe_combine(xp, r.slot_pos, to_dev(o["topk_w"])))
+    xp_o = oracle.permute(x, o["sorted_indices"], T * k)
+    assert to_host(xp).tobytes() == xp_o.tobytes()
+    ref, _ = oracle.combine(xp_o, o["slot_pos"], o["topk_w"])
+    assert out.tobytes() == ref.tobytes()
 
 
 @pytest.mark.parametrize("T,E,k,G,KG,ties", [(16384, 256, 8, 8, 4, False), (3000, 64, 6, 4, 2, False),
