@@ -216,6 +216,8 @@ def test_permute_then_unweighted_combine_k1_identity():
                           ("bf16", 300, 7168, 256, 8, 0.1, True),
                           ("bf16", 500, 1000, 32, 6, 0.2, False),
                           ("bf16", 700, 2048, 64, 6, 0.1, True),   # the layer shape's k
+                          ("bf16", 200, 4104, 64, 8, 0.2, True),   # rows in 2 column parts, ragged
+                          ("bf16", 150, 5000, 32, 7, 0.0, False),
                           ("bf16", 333, 512, 16, 5, 0.0, True),
                           ("bf16", 129, 36, 8, 3, 0.0, True),    # 72-byte rows: element path
                           ("f32", 256, 128, 8, 2, 0.0, True),

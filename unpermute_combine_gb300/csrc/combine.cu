@@ -21,6 +21,8 @@
 // (Knuth TwoSum) accumulation per lane followed by a fixed butterfly of
 // double-float additions, so it is deterministic and far more accurate than
 // a plain float dot.
+#include <algorithm>
+
 #include "common.cuh"
 
 namespace moe {
@@ -254,12 +256,22 @@ template <int KMAX, bool PLAIN>   // PLAIN: topk_w == NULL (plain sum)
 __global__ void __launch_bounds__(kThreads, KMAX <= 6 ? 4 : 2)
 combine_bf16_regs_kernel(const uint4* __restrict__ y, int64_t T, int64_t nvec, int k, int64_t n_rows,
                          const int32_t* __restrict__ slot_pos, const float* __restrict__ topk_w,
-                         uint4* __restrict__ out, float cbound, float dd_bound) {
+                         uint4* __restrict__ out, float cbound, float dd_bound, int parts) {
     __shared__ int32_t s_pos[kWarps][kMaxTopK];
     __shared__ float s_w[kWarps][kMaxTopK];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    for (int64_t t = int64_t(blockIdx.x) * kWarps + warp; t < T;
-         t += int64_t(gridDim.x) * kWarps) {
+    // work item = (token, column part): consecutive warps take the parts of
+    // one token, so a token whose every slot is live does not hold one warp
+    // for its whole row while lighter tokens finish elsewhere (capacity drops
+    // leave a few such tokens among many with none).  Eight-slot only; the
+    // smaller instantiations keep whole rows (parts = 1 folds away).
+    const int64_t P = KMAX >= 8 ? parts : 1;
+    const int64_t chunk = ((nvec + P - 1) / P + 31) / 32 * 32;
+    for (int64_t item = int64_t(blockIdx.x) * kWarps + warp; item < T * P;
+         item += int64_t(gridDim.x) * kWarps) {
+        const int64_t t = item / P;
+        const int64_t vb = (item - t * P) * chunk, ve = min64(vb + chunk, nvec);
+        if (vb >= ve) continue;
         stage_slots(s_pos[warp], s_w[warp], slot_pos, topk_w, t, k, n_rows, lane);
         int32_t pj[KMAX];
         float wj[KMAX];
@@ -278,17 +290,17 @@ combine_bf16_regs_kernel(const uint4* __restrict__ y, int64_t T, int64_t nvec, i
             const int64_t p = nv ? int64_t(s_pos[warp][j0]) : 0;
             const float w = nv ? s_w[warp][j0] : 0.0f;
             const f2_t w2 = f2_pack(w, w);
-            for (int64_t v0 = lane; v0 < nvec; v0 += 32 * 4) {
+            for (int64_t v0 = vb + lane; v0 < ve; v0 += 32 * 4) {
                 uint4 d[4];
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
                     const int64_t v = v0 + 32 * u;
-                    d[u] = (nv && v < nvec) ? __ldcs(y + p * nvec + v) : make_uint4(0, 0, 0, 0);
+                    d[u] = (nv && v < ve) ? __ldcs(y + p * nvec + v) : make_uint4(0, 0, 0, 0);
                 }
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
                     const int64_t v = v0 + 32 * u;
-                    if (v >= nvec) break;
+                    if (v >= ve) break;
                     uint4 r = make_uint4(0, 0, 0, 0);
                     if (nv) {
                         r.x = plus_zero_bf16x2(scale_pair_bf16_f2(w2, f2_from_bf16x2(d[u].x)));
@@ -302,7 +314,7 @@ combine_bf16_regs_kernel(const uint4* __restrict__ y, int64_t T, int64_t nvec, i
             __syncwarp();
             continue;
         }
-        for (int64_t v = lane; v < nvec; v += 32) {
+        for (int64_t v = vb + lane; v < ve; v += 32) {
             uint4 d[KMAX];
 #pragma unroll
             for (int j = 0; j < KMAX; ++j)
@@ -805,8 +817,12 @@ extern "C" moe_status_t moe_combine(const void* expert_out, moe_dtype_t dtype, i
                 : k <= 4 ? (plain ? combine_bf16_regs_kernel<4, true> : combine_bf16_regs_kernel<4, false>)
                 : k <= 6 ? (plain ? combine_bf16_regs_kernel<6, true> : combine_bf16_regs_kernel<6, false>)
                          : (plain ? combine_bf16_regs_kernel<8, true> : combine_bf16_regs_kernel<8, false>);
-            kern<<<grid_for((const void*)kern, kThreads, want), kThreads, 0, s>>>(
-                yv, T, H / 8, k, n_rows, slot_pos, topk_w, ov, cb, dd_bound_factor(k));
+            // eight-slot rows in parts of about 7 column steps (4 at H = 7168)
+            const int64_t steps = (H / 8 + 31) / 32;
+            const int parts = k > 6 ? int(std::min<int64_t>(4, std::max<int64_t>(1, steps / 7))) : 1;
+            const int64_t want_p = (T * parts + kWarps - 1) / kWarps;
+            kern<<<grid_for((const void*)kern, kThreads, want_p), kThreads, 0, s>>>(
+                yv, T, H / 8, k, n_rows, slot_pos, topk_w, ov, cb, dd_bound_factor(k), parts);
         } else {
             combine_bf16_vec_kernel<<<grid_for((const void*)combine_bf16_vec_kernel, kThreads, want),
                                       kThreads, 0, s>>>(yv, T, H / 8, k, n_rows, slot_pos, topk_w,
