@@ -337,6 +337,9 @@ def test_combine_deterministic_and_stable_across_calls():
 @pytest.mark.parametrize("dtype,T,H,E,k,drop,weighted",
                          [("bf16", 600, 4096, 64, 2, 0.0, True),
                           ("bf16", 300, 7168, 256, 8, 0.1, True),
+                          ("bf16", 300, 4104, 64, 8, 0.3, True),   # rows in 2 ragged column parts
+                          ("bf16", 129, 7168, 32, 6, 0.0, False),  # 4 parts, unweighted
+                          ("bf16", 400, 7168, 64, 5, 0.6, True),   # 4 parts, mostly 0-1 live slots
                           ("bf16", 200, 1000, 16, 4, 0.0, False),
                           ("bf16", 77, 20, 8, 3, 0.2, True),     # element path
                           ("f32", 256, 128, 8, 2, 0.0, True),

@@ -53,6 +53,20 @@ float dd_bound_factor(int k) {
     return 4.0f * n * n * 0x1p-48f + float(k) * 0x1p-52f;
 }
 
+// Column parts of an eight-slot row: about 7 lane steps of 32 vectors each,
+// and a power of two that divides the block's warps (1, 2 or 4).  The
+// backward stops at 2: each part restarts its copy pipeline and meets its
+// sibling parts at two barriers, which at 4 parts cost more than the balance
+// gains when every slot is live (DeepSeek shape: 1 part 687 us, 2 parts
+// 665 us, 4 parts 705 us; the forward: 343, 341, 338 us).
+int column_parts(int64_t nvec) {
+    const int64_t steps = (nvec + 31) / 32;
+    return steps >= 28 ? 4 : steps >= 14 ? 2 : 1;
+}
+
+int column_parts_bwd(int64_t nvec) { return column_parts(nvec) >= 2 ? 2 : 1; }
+static_assert(kWarps % 4 == 0, "column parts divide the block's warps");
+
 // Stage the token's slot rows and weights in shared memory (lanes < k).
 __device__ __forceinline__ void stage_slots(int32_t* s_pos, float* s_w, const int32_t* slot_pos,
                                             const float* topk_w, int64_t t, int k,
@@ -319,7 +333,7 @@ combine_bf16_regs_kernel(const uint4* __restrict__ y, int64_t T, int64_t nvec, i
 #pragma unroll
             for (int j = 0; j < KMAX; ++j)
                 d[j] = pj[j] >= 0 ? __ldcs(y + int64_t(pj[j]) * nvec + v) : make_uint4(0, 0, 0, 0);
-            if (PLAIN) {
+            if constexpr (PLAIN) {
                 // plain sum (permute backward): every product is exact, so a
                 // TwoSum chain shows whether the float sum is the exact
                 // slot-order sum (then the double chain computes the same
@@ -357,60 +371,60 @@ combine_bf16_regs_kernel(const uint4* __restrict__ y, int64_t T, int64_t nvec, i
                     set_word(res, q, uint32_t(half[0]) | (uint32_t(half[1]) << 16));
                 }
                 __stcs(out + t * nvec + v, res);
-                continue;
-            }
-            float s[8], a[8];
+            } else {
+                float s[8], a[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) { s[i] = 0.0f; a[i] = 0.0f; }
+                for (int i = 0; i < 8; ++i) { s[i] = 0.0f; a[i] = 0.0f; }
 #pragma unroll
-            for (int j = 0; j < KMAX; ++j) {
-                if (pj[j] < 0) continue;
-                const float w = wj[j], aw = fabsf(w);
+                for (int j = 0; j < KMAX; ++j) {
+                    if (pj[j] < 0) continue;
+                    const float w = wj[j], aw = fabsf(w);
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const float yv = unpack_bf16(d[j], i);
-                    s[i] = __fmaf_rn(w, yv, s[i]);
-                    a[i] = __fmaf_rn(aw, fabsf(yv), a[i]);
+                    for (int i = 0; i < 8; ++i) {
+                        const float yv = unpack_bf16(d[j], i);
+                        s[i] = __fmaf_rn(w, yv, s[i]);
+                        a[i] = __fmaf_rn(aw, fabsf(yv), a[i]);
+                    }
                 }
-            }
-            uint4 res;
-            uint32_t open = 0;
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                float lo0, hi0, lo1, hi1;
-                certify_interval(s[2 * q], a[2 * q], cbound, k, lo0, hi0);
-                certify_interval(s[2 * q + 1], a[2 * q + 1], cbound, k, lo1, hi1);
-                const uint32_t lo = pack_bf16x2_rn(lo0, lo1);
-                const uint32_t hi = pack_bf16x2_rn(hi0, hi1);
-                set_word(res, q, lo);
-                if (lo != hi) open |= 1u << q;
-            }
-            if (open) {
-                bool valid[KMAX];
-#pragma unroll
-                for (int j = 0; j < KMAX; ++j) valid[j] = pj[j] >= 0;
+                uint4 res;
+                uint32_t open = 0;
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
-                    if (!(open & (1u << q))) continue;
-                    uint16_t half[2];
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        float yv[KMAX];
-#pragma unroll
-                        for (int j = 0; j < KMAX; ++j) yv[j] = unpack_bf16(d[j], 2 * q + h);
-                        if (!dd_sum_bf16(wj, yv, valid, KMAX, dd_bound, &half[h])) {
-                            // last resort: double, slot order, one rounding
-                            double acc = 0.0;
-#pragma unroll
-                            for (int j = 0; j < KMAX; ++j)
-                                if (valid[j]) acc = fma(double(wj[j]), double(yv[j]), acc);
-                            half[h] = f64_to_bf16_rn(acc);
-                        }
-                    }
-                    set_word(res, q, uint32_t(half[0]) | (uint32_t(half[1]) << 16));
+                    float lo0, hi0, lo1, hi1;
+                    certify_interval(s[2 * q], a[2 * q], cbound, k, lo0, hi0);
+                    certify_interval(s[2 * q + 1], a[2 * q + 1], cbound, k, lo1, hi1);
+                    const uint32_t lo = pack_bf16x2_rn(lo0, lo1);
+                    const uint32_t hi = pack_bf16x2_rn(hi0, hi1);
+                    set_word(res, q, lo);
+                    if (lo != hi) open |= 1u << q;
                 }
+                if (open) {
+                    bool valid[KMAX];
+#pragma unroll
+                    for (int j = 0; j < KMAX; ++j) valid[j] = pj[j] >= 0;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        if (!(open & (1u << q))) continue;
+                        uint16_t half[2];
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            float yv[KMAX];
+#pragma unroll
+                            for (int j = 0; j < KMAX; ++j) yv[j] = unpack_bf16(d[j], 2 * q + h);
+                            if (!dd_sum_bf16(wj, yv, valid, KMAX, dd_bound, &half[h])) {
+                                // last resort: double, slot order, one rounding
+                                double acc = 0.0;
+#pragma unroll
+                                for (int j = 0; j < KMAX; ++j)
+                                    if (valid[j]) acc = fma(double(wj[j]), double(yv[j]), acc);
+                                half[h] = f64_to_bf16_rn(acc);
+                            }
+                        }
+                        set_word(res, q, uint32_t(half[0]) | (uint32_t(half[1]) << 16));
+                    }
+                }
+                __stcs(out + t * nvec + v, res);
             }
-            __stcs(out + t * nvec + v, res);
         }
         __syncwarp();
     }
@@ -539,7 +553,7 @@ __device__ __forceinline__ void dd_add1(float& hi, float& lo, float q) {
 
 // Butterfly sum of a double-float over the warp; every lane ends with the
 // same bits (TwoSum's error term does not depend on operand order).
-__device__ __forceinline__ float dd_warp_sum(float hi, float lo) {
+__device__ __forceinline__ void dd_warp_sum_pair(float& hi, float& lo) {
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
         const float h2 = __shfl_xor_sync(kFull, hi, off);
@@ -550,7 +564,30 @@ __device__ __forceinline__ float dd_warp_sum(float hi, float lo) {
         hi = __fadd_rn(s, e);
         lo = __fsub_rn(e, __fsub_rn(hi, s));
     }
+}
+
+__device__ __forceinline__ float dd_warp_sum(float hi, float lo) {
+    dd_warp_sum_pair(hi, lo);
     return __fadd_rn(hi, lo);
+}
+
+// Double-float partial sums of a dot product, one per column part of the row,
+// added in part order (fixed, so the result is deterministic).
+__device__ __forceinline__ float dd_parts_sum(const float (*part)[8][2], int nparts, int j) {
+    float hi = part[0][j][0], lo = part[0][j][1];
+    for (int q = 1; q < nparts; ++q) {
+        float s, e;
+        two_sum(hi, part[q][j][0], s, e);
+        e = __fadd_rn(e, __fadd_rn(lo, part[q][j][1]));
+        hi = __fadd_rn(s, e);
+        lo = __fsub_rn(e, __fsub_rn(hi, s));
+    }
+    return __fadd_rn(hi, lo);
+}
+
+// the P warps that hold the column parts of one token (named barrier 1 + warp / P)
+__device__ __forceinline__ void parts_sync(int warp, int nparts) {
+    asm volatile("bar.sync %0, %1;" :: "r"(1 + warp / nparts), "r"(32 * nparts) : "memory");
 }
 
 
@@ -566,15 +603,29 @@ combine_bwd_bf16_vec_kernel(const uint4* __restrict__ gout, const uint4* __restr
                             int64_t T, int64_t nvec, int k, int64_t n_rows,
                             const int32_t* __restrict__ slot_pos,
                             const float* __restrict__ topk_w, uint4* __restrict__ gy,
-                            float* __restrict__ grad_probs) {
+                            float* __restrict__ grad_probs, int parts) {
     static_assert(KMAX <= 8, "packed accumulators for up to 8 slots");
     extern __shared__ uint4 bwd_ring[];               // [kWarps][kBwdStages][KMAX + 1][32]
     __shared__ int32_t s_pos[kWarps][kMaxTopK];
     __shared__ float s_w[kWarps][kMaxTopK];
+    __shared__ float s_part[kWarps][8][2];            // per-warp partial dots (parts > 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     uint4* ring = bwd_ring + warp * kBwdStages * (KMAX + 1) * 32;
-    for (int64_t t = int64_t(blockIdx.x) * kWarps + warp; t < T;
-         t += int64_t(gridDim.x) * kWarps) {
+    // work item = (token, column part), as in the forward combine (eight-slot
+    // rows only).  parts divides the block's warps and every stride of the
+    // item loop, so the parts of one token are warps part_base..part_base+P-1
+    // of one block in the same round; each leaves its partial dot products in
+    // s_part and the first of them adds them up in part order.  Every warp of
+    // such a group takes the same branches (the token and its slots are
+    // shared), so the group barriers always meet.
+    const int P = KMAX >= 8 ? parts : 1;
+    const int64_t chunk = ((nvec + P - 1) / P + 31) / 32 * 32;
+    const int part_base = (warp / P) * P;
+    for (int64_t item = int64_t(blockIdx.x) * kWarps + warp; item < T * P;
+         item += int64_t(gridDim.x) * kWarps) {
+        const int64_t t = item / P;
+        const int part = int(item - t * P);
+        const int64_t vb = part * chunk, ve = min64(vb + chunk, nvec);
         stage_slots(s_pos[warp], s_w[warp], slot_pos, topk_w, t, k, n_rows, lane);
         int32_t pj[KMAX];
         f2_t wj[KMAX], hi[KMAX], lo[KMAX];
@@ -589,7 +640,7 @@ combine_bwd_bf16_vec_kernel(const uint4* __restrict__ gout, const uint4* __restr
             lo[j] = 0ull;
         }
         if (nv == 0) {              // every slot empty or dropped: nothing reads grad_out
-            if (lane < k) grad_probs[t * k + lane] = 0.0f;
+            if (part == 0 && lane < k) grad_probs[t * k + lane] = 0.0f;
             __syncwarp();
             continue;
         }
@@ -600,19 +651,19 @@ combine_bwd_bf16_vec_kernel(const uint4* __restrict__ gout, const uint4* __restr
             const float w = s_w[warp][j0];
             const f2_t w2 = f2_pack(w, w);
             f2_t h1 = 0ull, l1 = 0ull;
-            for (int64_t v0 = lane; v0 < nvec; v0 += 32 * 4) {
+            for (int64_t v0 = vb + lane; v0 < ve; v0 += 32 * 4) {
                 uint4 gv[4], yv[4];
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
                     const int64_t v = v0 + 32 * u;
-                    const bool in = v < nvec;
+                    const bool in = v < ve;
                     gv[u] = in ? __ldcs(gout + t * nvec + v) : make_uint4(0, 0, 0, 0);
                     yv[u] = in ? __ldcs(y + p * nvec + v) : make_uint4(0, 0, 0, 0);
                 }
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
                     const int64_t v = v0 + 32 * u;
-                    if (v >= nvec) break;
+                    if (v >= ve) break;
                     const f2_t g0 = f2_from_bf16x2(gv[u].x), g1 = f2_from_bf16x2(gv[u].y);
                     const f2_t g2 = f2_from_bf16x2(gv[u].z), g3 = f2_from_bf16x2(gv[u].w);
                     uint4 r;
@@ -633,8 +684,22 @@ combine_bwd_bf16_vec_kernel(const uint4* __restrict__ gout, const uint4* __restr
             float s1, e1;
             two_sum(a0, a1, s1, e1);
             e1 = __fadd_rn(e1, __fadd_rn(b0, b1));
-            const float r = dd_warp_sum(s1, e1);
-            if (lane < k) grad_probs[t * k + lane] = lane == j0 ? r : 0.0f;
+            dd_warp_sum_pair(s1, e1);
+            if (P == 1) {
+                const float r = __fadd_rn(s1, e1);
+                if (lane < k) grad_probs[t * k + lane] = lane == j0 ? r : 0.0f;
+            } else {
+                if (lane == 0) {
+                    s_part[warp][0][0] = s1;
+                    s_part[warp][0][1] = e1;
+                }
+                parts_sync(warp, P);
+                if (part == 0 && lane < k) {
+                    const float r = dd_parts_sum(&s_part[part_base], P, 0);
+                    grad_probs[t * k + lane] = lane == j0 ? r : 0.0f;
+                }
+                parts_sync(warp, P);
+            }
             __syncwarp();
             continue;
         }
@@ -642,10 +707,10 @@ combine_bwd_bf16_vec_kernel(const uint4* __restrict__ gout, const uint4* __restr
         // i + kBwdStages - 1 go to the warp's shared-memory ring (cp.async)
         // while step i is computed, so the bytes in flight live in shared
         // memory, not registers; each lane reads back only its own copies
-        const int64_t nsteps = (nvec + 31) / 32;
+        const int64_t nsteps = ve > vb ? (ve - vb + 31) / 32 : 0;
         auto issue = [&](int64_t i) {
-            const int64_t v = lane + 32 * i;
-            if (i < nsteps && v < nvec) {
+            const int64_t v = vb + lane + 32 * i;
+            if (i < nsteps && v < ve) {
                 uint4* st = ring + (i % kBwdStages) * (KMAX + 1) * 32;
 #pragma unroll
                 for (int j = 0; j < KMAX; ++j)
@@ -659,8 +724,8 @@ combine_bwd_bf16_vec_kernel(const uint4* __restrict__ gout, const uint4* __restr
         for (int64_t i = 0; i < nsteps; ++i) {
             issue(i + kBwdStages - 1);
             cp_async_wait<kBwdStages - 1>();               // step i has landed
-            const int64_t v = lane + 32 * i;
-            if (v >= nvec) continue;
+            const int64_t v = vb + lane + 32 * i;
+            if (v >= ve) continue;
             const uint4* st = ring + (i % kBwdStages) * (KMAX + 1) * 32;
             const uint4 gv = st[KMAX * 32 + lane];
             uint4 yv[KMAX];
@@ -695,8 +760,20 @@ combine_bwd_bf16_vec_kernel(const uint4* __restrict__ gout, const uint4* __restr
             float s, e;
             two_sum(h0, h1, s, e);                     // fold the odd lane into the even one
             e = __fadd_rn(e, __fadd_rn(l0, l1));
-            const float r = dd_warp_sum(s, e);
-            if (lane == 0) grad_probs[t * k + j] = pj[j] >= 0 ? r : 0.0f;
+            dd_warp_sum_pair(s, e);
+            if (P == 1) {
+                if (lane == 0) grad_probs[t * k + j] = pj[j] >= 0 ? __fadd_rn(s, e) : 0.0f;
+            } else if (lane == 0) {
+                s_part[warp][j][0] = s;
+                s_part[warp][j][1] = e;
+            }
+        }
+        if (P > 1) {
+            parts_sync(warp, P);
+            if (part == 0 && lane < k)
+                grad_probs[t * k + lane] =
+                    s_pos[warp][lane] >= 0 ? dd_parts_sum(&s_part[part_base], P, lane) : 0.0f;
+            parts_sync(warp, P);
         }
         __syncwarp();
     }
@@ -774,9 +851,11 @@ moe_status_t launch_bwd(const void* gout, const void* y, moe_dtype_t dtype, int6
         const auto kern = combine_bwd_bf16_vec_kernel<KV>;
         constexpr size_t smem = bwd_ring_bytes<KV>();
         if (!opt_in_smem((const void*)kern, int(smem))) return MOE_ERR_CUDA;
-        kern<<<grid_for((const void*)kern, kThreads, smem, want), kThreads, smem, s>>>(
+        const int parts = KV >= 8 ? column_parts_bwd(H / 8) : 1;
+        const int64_t want_p = (T * parts + kWarps - 1) / kWarps;
+        kern<<<grid_for((const void*)kern, kThreads, smem, want_p), kThreads, smem, s>>>(
             static_cast<const uint4*>(gout), static_cast<const uint4*>(y), T, H / 8, k, n_rows,
-            slot_pos, topk_w, static_cast<uint4*>(gy), gp);
+            slot_pos, topk_w, static_cast<uint4*>(gy), gp, parts);
     } else if (dtype == MOE_F32) {
         const auto kern = combine_bwd_elem_kernel<float, KMAX>;
         kern<<<grid_for((const void*)kern, kThreads, want), kThreads, 0, s>>>(
@@ -817,9 +896,7 @@ extern "C" moe_status_t moe_combine(const void* expert_out, moe_dtype_t dtype, i
                 : k <= 4 ? (plain ? combine_bf16_regs_kernel<4, true> : combine_bf16_regs_kernel<4, false>)
                 : k <= 6 ? (plain ? combine_bf16_regs_kernel<6, true> : combine_bf16_regs_kernel<6, false>)
                          : (plain ? combine_bf16_regs_kernel<8, true> : combine_bf16_regs_kernel<8, false>);
-            // eight-slot rows in parts of about 7 column steps (4 at H = 7168)
-            const int64_t steps = (H / 8 + 31) / 32;
-            const int parts = k > 6 ? int(std::min<int64_t>(4, std::max<int64_t>(1, steps / 7))) : 1;
+            const int parts = k > 6 ? column_parts(H / 8) : 1;
             const int64_t want_p = (T * parts + kWarps - 1) / kWarps;
             kern<<<grid_for((const void*)kern, kThreads, want_p), kThreads, 0, s>>>(
                 yv, T, H / 8, k, n_rows, slot_pos, topk_w, ov, cb, dd_bound_factor(k), parts);
