@@ -218,6 +218,8 @@ def test_permute_then_unweighted_combine_k1_identity():
                           ("bf16", 700, 2048, 64, 6, 0.1, True),   # the layer shape's k
                           ("bf16", 200, 4104, 64, 8, 0.2, True),   # rows in 2 column parts, ragged
                           ("bf16", 150, 5000, 32, 7, 0.0, False),
+                          ("bf16", 1, 7168, 16, 8, 0.0, True),     # one token in 4 parts
+                          ("bf16", 3, 4104, 16, 8, 0.5, False),
                           ("bf16", 333, 512, 16, 5, 0.0, True),
                           ("bf16", 129, 36, 8, 3, 0.0, True),    # 72-byte rows: element path
                           ("f32", 256, 128, 8, 2, 0.0, True),
@@ -340,6 +342,8 @@ def test_combine_deterministic_and_stable_across_calls():
                           ("bf16", 300, 4104, 64, 8, 0.3, True),   # rows in 2 ragged column parts
                           ("bf16", 129, 7168, 32, 6, 0.0, False),  # 4 parts, unweighted
                           ("bf16", 400, 7168, 64, 5, 0.6, True),   # 4 parts, mostly 0-1 live slots
+                          ("bf16", 1, 7168, 16, 8, 0.0, True),     # one token, one part pair
+                          ("bf16", 3, 4104, 16, 8, 0.5, False),
                           ("bf16", 200, 1000, 16, 4, 0.0, False),
                           ("bf16", 77, 20, 8, 3, 0.2, True),     # element path
                           ("f32", 256, 128, 8, 2, 0.0, True),
