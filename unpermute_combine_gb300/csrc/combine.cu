@@ -2,8 +2,9 @@
 //
 // The combine of "03 · Combine 与 forward / backward 对称性" §1,
 //   out[t] = sum_j w[t,j] * y[slot_pos[t,j]],
-// done as a deterministic gather-reduce (one warp per token reads its k rows
-// and writes one) instead of the scatter-add of §2.3.
+// done as a deterministic gather-reduce (a warp reads a token's k rows and
+// writes its output row; eight-slot rows are cut into column parts taken by
+// neighbouring warps) instead of the scatter-add of §2.3.
 //
 // Accuracy contract: the result is the double-precision slot-order sum
 // rounded once to the output type.  The fast path accumulates s = sum w*y
@@ -19,10 +20,9 @@
 // product rounded once (float product plus an error-free tie check), and
 // grad_probs[t,j] = <grad_out[t], y[slot_pos[t,j]]> is a double-float
 // (Knuth TwoSum) accumulation per lane followed by a fixed butterfly of
-// double-float additions, so it is deterministic and far more accurate than
-// a plain float dot.
-#include <algorithm>
-
+// double-float additions (and, for a row cut into column parts, the parts'
+// double-float partials added in part order), so it is deterministic and far
+// more accurate than a plain float dot.
 #include "common.cuh"
 
 namespace moe {
