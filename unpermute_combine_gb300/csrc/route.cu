@@ -134,12 +134,19 @@ route_topk_kernel(const float* __restrict__ logits, int64_t T, int E, int k,
             for (int v = 0; v < NV; ++v)
                 if (!((kept >> gv[v]) & 1u)) key[v] = 0;   // padding lanes are 0 already
         }
-        // this lane's best entry: largest key, lowest v (= lowest id) on ties
-        uint32_t bk = 0;
-        int bv = 0;
+        // this lane's two best entries (largest key, lowest v = lowest id on
+        // ties): the head bk/bv and the runner-up b2/v2
+        uint32_t bk = 0, b2 = 0;
+        int bv = 0, v2 = 0;
 #pragma unroll
-        for (int v = 0; v < NV; ++v)
-            if (key[v] > bk) { bk = key[v]; bv = v; }
+        for (int v = 0; v < NV; ++v) {
+            if (key[v] > bk) {
+                b2 = bk; v2 = bv; bk = key[v]; bv = v;
+            } else if (key[v] > b2) {
+                b2 = key[v]; v2 = v;
+            }
+        }
+        bool have2 = true;       // b2/v2 is the runner-up of what is left
 
         uint32_t taken = 0;      // bit v: my expert v*32+lane was chosen
         int my_e = -1;           // lane j keeps slot j
@@ -151,12 +158,22 @@ route_topk_kernel(const float* __restrict__ logits, int64_t T, int E, int k,
             if (lane == j) { my_e = e; my_val = key_to_value(m); }
             if ((e & 31) == lane) {            // the owner drops the winner
                 taken |= 1u << bv;
-                bk = 0;
-                bv = 0;
+                if (have2) {                   // the runner-up is the new head
+                    bk = b2;
+                    bv = v2;
+                    have2 = false;
+                } else {                       // a second pop: rescan what is left
+                    bk = 0; bv = 0; b2 = 0; v2 = 0;
 #pragma unroll
-                for (int v = 0; v < NV; ++v) {
-                    if ((taken >> v) & 1u) continue;
-                    if (key[v] > bk) { bk = key[v]; bv = v; }
+                    for (int v = 0; v < NV; ++v) {
+                        if ((taken >> v) & 1u) continue;
+                        if (key[v] > bk) {
+                            b2 = bk; v2 = bv; bk = key[v]; bv = v;
+                        } else if (key[v] > b2) {
+                            b2 = key[v]; v2 = v;
+                        }
+                    }
+                    have2 = true;
                 }
             }
         }
