@@ -177,3 +177,32 @@ def test_permute_quantize_fp8_matches_quantize_then_permute(T, H, block, k, E, c
     exp_s[si >= 0] = sc_o[si[si >= 0]]
     assert (_fp8_host(oq) == exp_q).all()
     assert (to_host(osc).view(np.uint32) == exp_s.view(np.uint32)).all()
+
+
+def test_permute_quantize_fp8_skips_slots_outside_the_rows():
+    """Slots naming a row outside [0, n_rows) (negative other than -1, or
+    past the buffer) move nothing; every other slot row is the oracle's."""
+    T, H, E, k, block = 300, 1024, 16, 4, 128
+    idx, w = wl.random_routing(41, T, E, k)
+    o = oracle.route_indices(idx, w, E)
+    sp = o["slot_pos"].copy()
+    rows = T * k
+    bad = np.random.default_rng(42).random(sp.shape) < 0.1
+    sp[bad] = np.where(np.random.default_rng(43).random(bad.sum()) < 0.5, rows + 5, -7)
+    x = _tricky_rows(44, T, H)
+    oq = _fp8_dev(np.full((rows, H), 0x3C, np.uint8))
+    osc = torch.full((rows, H // block), -2.0, dtype=torch.float32, device="cuda")
+    moe.moe_permute_quantize_fp8(to_dev(x), to_dev(sp), block, out=(oq, osc))
+    torch.cuda.synchronize()
+    assert moe.moe_device_status() == 0
+    q_o, sc_o = oracle.quantize_fp8(x, block)
+    exp_q = np.full((rows, H), 0x3C, np.uint8)
+    exp_s = np.full((rows, H // block), -2.0, np.float32)
+    for t in range(T):
+        for j in range(k):
+            p = sp[t, j]
+            if 0 <= p < rows:
+                exp_q[p] = q_o[t]
+                exp_s[p] = sc_o[t]
+    assert (_fp8_host(oq) == exp_q).all()
+    assert (to_host(osc).view(np.uint32) == exp_s.view(np.uint32)).all()
