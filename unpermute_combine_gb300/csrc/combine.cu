@@ -338,29 +338,44 @@ combine_bf16_regs_kernel(const uint4* __restrict__ y, int64_t T, int64_t nvec, i
                 // TwoSum chain shows whether the float sum is the exact
                 // slot-order sum (then the double chain computes the same
                 // prefixes and it rounds directly); the rare inexact element
-                // goes through the certified tiers
+                // goes through the certified tiers.  The chain runs on both
+                // elements of a 32-bit word at once (packed f32x2 add/sub
+                // round each half like the scalar operations).
                 uint4 res;
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
+                    f2_t hi2 = 0ull;
+                    uint32_t err0 = 0, err1 = 0;      // error terms' magnitude bits
+#pragma unroll
+                    for (int j = 0; j < KMAX; ++j) {
+                        if (pj[j] < 0) continue;
+                        const uint32_t wd = q == 0 ? d[j].x : q == 1 ? d[j].y : q == 2 ? d[j].z : d[j].w;
+                        const f2_t y2 = f2_from_bf16x2(wd);
+                        const f2_t s2 = f2_add(hi2, y2);
+                        const f2_t bp = f2_sub(s2, hi2);
+                        const f2_t e2 = f2_add(f2_sub(hi2, f2_sub(s2, bp)), f2_sub(y2, bp));
+                        hi2 = s2;
+                        err0 |= uint32_t(e2) & 0x7FFFFFFFu;
+                        err1 |= uint32_t(e2 >> 32) & 0x7FFFFFFFu;
+                    }
+                    float hsum[2];
+                    f2_unpack(hi2, hsum[0], hsum[1]);
                     uint16_t half[2];
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
                         const int i = 2 * q + h;
-                        float hi = 0.0f, yv[KMAX];
-                        bool inexact = false, valid[KMAX];
+                        if ((h == 0 ? err0 : err1) == 0) {
+                            half[h] = f32_to_bf16_rn(hsum[h]);
+                            continue;
+                        }
+                        float yv[KMAX];
+                        bool valid[KMAX];
 #pragma unroll
                         for (int j = 0; j < KMAX; ++j) {
                             valid[j] = pj[j] >= 0;
                             yv[j] = unpack_bf16(d[j], i);
-                            if (!valid[j]) continue;
-                            float sum, e;
-                            two_sum(hi, yv[j], sum, e);
-                            hi = sum;
-                            inexact |= e != 0.0f;
                         }
-                        if (!inexact) {
-                            half[h] = f32_to_bf16_rn(hi);
-                        } else if (!dd_sum_bf16(wj, yv, valid, KMAX, dd_bound, &half[h])) {
+                        if (!dd_sum_bf16(wj, yv, valid, KMAX, dd_bound, &half[h])) {
                             double acc = 0.0;
 #pragma unroll
                             for (int j = 0; j < KMAX; ++j)
