@@ -10,6 +10,14 @@ about 4.5 GB, far larger than the 129 MB L2, so no L2 flush is needed.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
+After the main step the default run also times, each with its own clock
+record, the other workloads under the key "workloads": the full MoE layer
+forward (T=4096, H=2048, E=64, k=6, I=1408: route, permute, grouped SwiGLU
+on the tensor cores, combine), the virtual expert-parallel sort_chunks
+(8 ranks x 8 local experts, forward and inverse) and the two stand-in
+pipelines mid (T=8192, H=4096, E=64, k=2) and tiny (T=256, H=128, E=8, k=2,
+fp32): route, permute, per-expert scale, combine.  --no-extra skips them.
+
 For N > 1 launch under torchrun: every rank runs an independent replica of
 the workload on its own GPU (the path has no cross-GPU exchange), timing is
 bracketed by a barrier and the max over ranks is reported.
@@ -850,6 +858,146 @@ def run_vep8(args, rank, world, local_rank):
     }
 
 
+# ------------------------------------------------------- stand-in pipelines
+
+def run_stand_in(args, rank, world, local_rank, name):
+    """tiny / mid: moe_route, moe_permute, the stand-in expert (rows of
+    expert e scaled by (e+1)/E, moe_expert_scale) and the weighted
+    moe_combine, timed per call like the main step."""
+    import numpy as np
+    import torch
+
+    import unpermute_combine_gb300 as moe
+    import workloads as wl
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    d = wl.make(name)
+    W = d["workload"]
+    T, H, E, k = W.T, W.H, W.E, W.k
+    N = T * k
+    f32 = W.dtype == "f32"
+    b = 4 if f32 else 2
+    if f32:
+        x = torch.from_numpy(d["x"]).to(dev)
+    else:
+        x = torch.from_numpy(d["x"].view(np.int16)).view(torch.bfloat16).to(dev)
+    logits = torch.from_numpy(d["logits"]).to(dev)
+    scale = torch.from_numpy(d["scale"]).to(dev)
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        r = moe.moe_route(logits, k, stream=stream)
+        xp = torch.empty((N, H), dtype=x.dtype, device=dev)
+        y = torch.empty_like(xp)
+        out = torch.empty((T, H), dtype=x.dtype, device=dev)
+    names = ["route", "permute", "expert_scale", "combine"]
+
+    def step(ev=None):
+        def mark(i):
+            if ev is not None:
+                ev[i].record(stream)
+        mark(0)
+        moe.moe_route(logits, k, out=r, stream=stream)
+        mark(1)
+        moe.moe_permute(x, r.slot_pos, out=xp, stream=stream)
+        mark(2)
+        moe.moe_expert_scale(xp, r.offsets, scale, out=y, stream=stream)
+        mark(3)
+        moe.moe_combine(y, r.slot_pos, r.topk_w, out=out, stream=stream)
+        mark(4)
+
+    import torch.distributed as dist
+    dist_on = dist.is_available() and dist.is_initialized()
+
+    def barrier():
+        torch.cuda.synchronize(dev)
+        if dist_on:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    for _ in range(args.warmup):
+        step()
+    barrier()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local_rank) as clk:
+        barrier()
+        t0.record(stream)
+        for i in range(args.steps):
+            step(evs[i])
+        t1.record(stream)
+        barrier()
+    max_elapsed = reduce_max(t0.elapsed_time(t1) / 1e3, dev)
+    per = {n: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(args.steps))
+           / 1e3 for j, n in enumerate(names)}
+    if rank != 0:
+        return None
+    peak, peak_kind = measured_peak()
+    alg = algorithmic_bytes(T, H, E, k, b)
+    alg["expert_scale"] = 2 * N * H * b + (E + 1) * 4 + E * 4
+    kern = {}
+    for n in names:
+        gbs = alg[n] / per[n] / 1e9
+        kern[n] = {"us": round(per[n] * 1e6, 2), "alg_bytes": alg[n], "GB_s": round(gbs, 1),
+                   "frac": round(gbs / peak, 4)}
+    dominant = max(names, key=lambda n_: per[n_])
+    ach = alg[dominant] / per[dominant] / 1e9
+    pc = per["permute"] + per["combine"]
+    small = alg[dominant] < 2 * 129e6      # fits in L2 between steps: latency-bound
+    return {
+        "value": job_value(N, world, args.steps, max_elapsed), "unit": UNIT,
+        "ms_per_step": max_elapsed / args.steps * 1e3, "steps": args.steps,
+        "warmup": args.warmup, "dtype": W.dtype,
+        "config": {"workload": f"{name}: T={T} H={H} E={E} k={k} {W.dtype}, {W.note}",
+                   "routed_tokens_per_step": N,
+                   "step": "moe_route + moe_permute + moe_expert_scale + moe_combine",
+                   "l2": ("no flush; the step's few MB stay in the 129 MB L2: latency-bound, "
+                          "read the microseconds" if small else
+                          "no flush: permute and combine each move > 129 MB")},
+        "roofline": {"bound": "latency" if small else "hbm", "kernel": dominant,
+                     "achieved": round(ach, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(ach / peak, 4), "peak_source": f"{peak_kind} hbm_gbs",
+                     "traffic": None},
+        "kernels": kern,
+        "permute_combine_routed_tokens_per_s": N / pc,
+        "gpu_launches": (ROUTE_LAUNCHES + 3) * args.steps,
+        "clocks": clk.summary(),
+        **({} if args.no_cpu_baseline else
+           {"cpu_baseline": cpu_baseline_stand_in(name, min(T, args.cpu_mid_tokens))}),
+    }
+
+
+EXTRA_WORKLOADS = ("layer", "vep8", "mid", "tiny")
+
+
+def run_extras(args, rank, world, local_rank):
+    """The other workloads, each timed after the main step with its own clock
+    record: the full layer forward (grouped SwiGLU on the tensor cores), the
+    virtual expert-parallel sort_chunks, and the two stand-in pipelines."""
+    out = {}
+    for name in EXTRA_WORKLOADS:
+        sub = argparse.Namespace(**vars(args))
+        sub.workload = name
+        sub.steps = max(1, min(args.steps, args.extra_steps))
+        sub.no_e2e = True
+        sub.train = False
+        sub.tokens = None
+        if name == "layer":
+            line = run_ours(sub, rank, world, local_rank)
+        elif name == "vep8":
+            line = run_vep8(sub, rank, world, local_rank)
+        else:
+            line = run_stand_in(sub, rank, world, local_rank, name)
+        if line is None:
+            continue
+        keep = ("value", "unit", "ms_per_step", "steps", "config", "roofline", "kernels",
+                "permute_combine_routed_tokens_per_s", "gpu_launches", "clocks",
+                "cpu_baseline")
+        out[name] = {key: line[key] for key in keep if key in line}
+        out[name]["steps"] = sub.steps
+    return out
+
+
 # ------------------------------------------------------------ oracle timing
 
 def cpu_baseline(tokens: int):
@@ -875,10 +1023,14 @@ def cpu_baseline(tokens: int):
                       f"{dt:.1f} s single-threaded C (host has {os.cpu_count()} cores)"}
 
 
-def cpu_baseline_layer(tokens: int):
+def cpu_baseline_layer(tokens: int, threads: int = 0):
     """The CPU oracle on the layer workload's first `tokens` tokens: route,
-    permute, the grouped SwiGLU of those tokens' rows, combine;
-    single-threaded."""
+    permute, the grouped SwiGLU of those tokens' rows, combine.  The grouped
+    SwiGLU (all but a sliver of the work) runs the oracle unchanged on
+    disjoint row sets in `threads` host threads (default: every core this
+    process may use); the other steps are single-threaded."""
+    import concurrent.futures as cf
+
     import numpy as np
 
     import oracle
@@ -887,16 +1039,52 @@ def cpu_baseline_layer(tokens: int):
     d = wl.make("layer", with_weights=True)
     W = d["workload"]
     x, lg = d["x"][:tokens], d["logits"][:tokens]
+    cores = threads or len(os.sched_getaffinity(0))
     t0 = time.perf_counter()
     r = oracle.route(lg, W.k)
     xp = oracle.permute(x, r["sorted_indices"])
-    y, _ = oracle.grouped_swiglu(xp, d["w_up"], d["w_down"], r["offsets"])
+    n_rows = xp.shape[0]
+    parts = [np.arange(i, n_rows, cores, dtype=np.int64) for i in range(min(cores, n_rows))]
+    # the oracle call holds no Python lock while it runs (ctypes), so the
+    # row sets are computed in parallel; each row is written by one call
+    with cf.ThreadPoolExecutor(max_workers=len(parts)) as ex:
+        ys = list(ex.map(lambda rows: oracle.grouped_swiglu(xp, d["w_up"], d["w_down"],
+                                                            r["offsets"], rows=rows)[0], parts))
+    y = np.zeros_like(xp)
+    for rows, yp in zip(parts, ys):
+        y[rows] = yp[rows]
     oracle.combine(y, r["slot_pos"], r["topk_w"])
     dt = time.perf_counter() - t0
     n = tokens * W.k
-    return {"value": n / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
+    return {"value": n / dt, "unit": UNIT, "cores": len(parts), "kind": "oracle",
             "sample": f"first {tokens} of {W.T} tokens ({n} routed rows), one layer forward, "
-                      f"{dt:.1f} s single-threaded C (host has {os.cpu_count()} cores)"}
+                      f"{dt:.1f} s; the grouped SwiGLU over {len(parts)} host threads "
+                      f"(host has {os.cpu_count()} cores)"}
+
+
+def cpu_baseline_stand_in(name: str, tokens: int):
+    """The CPU oracle's route, permute, stand-in expert and combine on the
+    first `tokens` tokens of a stand-in workload, single-threaded."""
+    import oracle
+    import workloads as wl
+
+    d = wl.make(name)
+    W = d["workload"]
+    x, lg = d["x"][:tokens], d["logits"][:tokens]
+    t0 = time.perf_counter()
+    passes = n = 0
+    while passes == 0 or time.perf_counter() - t0 < 1.0:
+        r = oracle.route(lg, W.k)
+        xp = oracle.permute(x, r["sorted_indices"])
+        y = oracle.expert_scale(xp, r["offsets"], d["scale"])
+        oracle.combine(y, r["slot_pos"], r["topk_w"])
+        n += tokens * W.k
+        passes += 1
+    dt = time.perf_counter() - t0
+    return {"value": n / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"first {tokens} of {W.T} tokens, route + permute + stand-in expert + "
+                      f"combine, {passes} pass{'es' if passes > 1 else ''} in {dt:.2f} s, "
+                      f"single-threaded C (host has {os.cpu_count()} cores)"}
 
 
 def cpu_baseline_vep8():
@@ -975,9 +1163,16 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-tokens", type=int, default=16384)
     ap.add_argument("--ref-tokens", type=int, default=2048)
-    ap.add_argument("--cpu-layer-tokens", type=int, default=256,
+    ap.add_argument("--cpu-layer-tokens", type=int, default=1024,
                     help="tokens of the layer workload the CPU oracle baseline runs")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-mid-tokens", type=int, default=2048,
+                    help="tokens of the stand-in workloads the CPU oracle baseline runs")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="time only the main step (skip the layer, vep8, mid and tiny "
+                         "workloads that follow it by default)")
+    ap.add_argument("--extra-steps", type=int, default=50,
+                    help="timed steps of each extra workload (at most --steps)")
     ap.add_argument("--tokens", type=int, default=None,
                     help="use only the first TOKENS tokens (small cases for profiling)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg")
@@ -998,10 +1193,12 @@ def main(argv=None):
                     help="route with group-limited routing: G expert groups, KG kept")
     ap.add_argument("--vep-streams", type=int, default=4, metavar="S",
                     help="vep8: streams the virtual ranks' calls are forked over")
-    ap.add_argument("--workload", choices=["skewed", "layer", "vep8"], default=WORKLOAD,
+    ap.add_argument("--workload", choices=["skewed", "layer", "vep8", "mid", "tiny"],
+                    default=WORKLOAD,
                     help="skewed: the dispatch/combine step (default); layer: the full MoE "
                          "layer forward with the grouped SwiGLU; vep8: sort_chunks forward "
-                         "and inverse on an 8-rank x 8-expert virtual EP layout")
+                         "and inverse on an 8-rank x 8-expert virtual EP layout; mid / tiny: "
+                         "route, permute, stand-in expert and combine")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("at least 3 warm-up steps")
@@ -1017,7 +1214,25 @@ def main(argv=None):
             import torch.distributed as dist
             torch.cuda.set_device(local_rank)
             dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
-        line = (run_vep8 if args.workload == "vep8" else run_ours)(args, rank, world, local_rank)
+        if args.workload in ("mid", "tiny"):
+            line = run_stand_in(args, rank, world, local_rank, args.workload)
+            if line is not None:
+                line = {"metric": METRIC, "n_gpus": world, "higher_is_better": True,
+                        "scaling": "weak", "vs_baseline": None,
+                        "data": "synthetic (seeded)", **line,
+                        "e2e": {"value": None, "unit": UNIT, "h2d_bytes_per_step": 0,
+                                "d2h_bytes_per_step": 0,
+                                "path": "not measured for the stand-in workloads"}}
+        else:
+            line = (run_vep8 if args.workload == "vep8" else run_ours)(args, rank, world,
+                                                                       local_rank)
+        plain = (args.workload == WORKLOAD and not (args.fp8 or args.fp8_split or args.layout or
+                                                    args.route_groups or args.router_bwd or
+                                                    args.tokens or args.train))
+        if plain and not args.no_extra:
+            extra = run_extras(args, rank, world, local_rank)
+            if line is not None:
+                line["workloads"] = extra
         if world > 1:
             import torch.distributed as dist
             dist.destroy_process_group()
