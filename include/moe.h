@@ -96,7 +96,11 @@ int moe_abi_version(void);
  *                          offsets[E]
  *   routing_map [T,E] u8   1 where token t picked expert e (NULL: not written)
  * Every integer output is bit-exact and independent of launch order.
- * Workspace: moe_route_workspace_size(T, E, k) bytes. */
+ * Workspace: moe_route_workspace_size(T, E, k) bytes (nothing in it needs to
+ * be cleared: every call writes the scratch it reads).  Device status: up to
+ * 256 experts the logits reach shared memory through bounded bulk-copy
+ * waits; one that gives up records MOE_ERR_TIMEOUT in the library's device
+ * status word (moe_device_status). */
 moe_status_t moe_route_workspace_size(int64_t T, int E, int k, size_t* bytes);
 
 moe_status_t moe_route(const float* logits, int64_t T, int E, int k,
@@ -144,18 +148,24 @@ moe_status_t moe_route_indices(const int32_t* topk_idx, const float* topk_w,
  * MOE_ROUTE_NOALLOC_SCRATCH_BYTES inside the library, which every GPU that
  * loads the library keeps until the process exits.
  *  - Problems needing more than that (moe_route_workspace_size(T, E, k) >
- *    MOE_ROUTE_NOALLOC_SCRATCH_BYTES; e.g. T = 16384, E = 256 needs 132 KB)
- *    return MOE_ERR_UNSUPPORTED before anything runs.
+ *    MOE_ROUTE_NOALLOC_SCRATCH_BYTES; e.g. T = 16384, E = 256 needs 769 KB,
+ *    and at E = 256 the limit is about 87,000 tokens) return
+ *    MOE_ERR_UNSUPPORTED before anything runs.
  *  - It allocates nothing: no cudaMalloc, no cudaFree, no allocating library
  *    call.  Its first call on each device looks up the array's device address
  *    (once per device, with that device current); make that first call before
- *    any stream capture.
+ *    any stream capture.  The address is kept for the life of the process:
+ *    after cudaDeviceReset (or anything else that destroys and re-creates the
+ *    device's primary context) it is stale, so do not use this entry point
+ *    on a device that has been reset.  (moe_device_status caches the address
+ *    of the device status word the same way.)
  *  - Every call shares the one array.  Each call writes all the scratch it
  *    reads, so nothing has to be cleared between calls, but calls that
  *    overlap on the GPU (other streams, other host threads) race: serialise
  *    them.
- *  - Routing from logits records no device-side status, so there is no
- *    workspace to pass to moe_workspace_status. */
+ *  - There is no workspace to pass to moe_workspace_status; a bulk-copy
+ *    wait that gives up is recorded in the device status word as for
+ *    moe_route (moe_device_status). */
 #define MOE_ROUTE_NOALLOC_SCRATCH_BYTES (1u << 20)
 
 moe_status_t moe_route_noalloc(const float* logits, int64_t T, int E, int k,

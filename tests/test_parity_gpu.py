@@ -370,8 +370,10 @@ def test_combine_backward(dtype, T, H, E, k, drop, weighted):
 
 
 def test_expert_scale_bit_exact():
-    for dtype in ("bf16", "f32"):
-        T, H, E, k = 300, 520, 16, 4
+    # 16-byte-multiple bf16 rows (vector kernel, one with a ragged last batch
+    # of vectors), an odd bf16 row (element kernel) and float32 rows
+    for dtype, H in (("bf16", 520), ("bf16", 4104), ("bf16", 13), ("f32", 520)):
+        T, E, k = 300, 16, 4
         idx, _ = wl.random_routing(4, T, E, k, empty_frac=0.1)
         o = oracle.route_indices(idx, None, E)
         r = moe.moe_route_indices(to_dev(idx), None, E)

@@ -59,7 +59,10 @@ def test_noalloc_route_matches_route_on_two_calls_in_a_row(lib):
     stream = torch.cuda.current_stream()
     # two different problems back to back: the second call reuses the
     # scratch the first one left behind
-    for T, E, k, seed in [(16384, 256, 8, 11), (3001, 64, 6, 12), (16384, 256, 8, 13)]:
+    # (40000 tokens: more than 256 token blocks, so the route runs its scan
+    # kernel and keeps per-block prefixes in the shared array as well)
+    for T, E, k, seed in [(16384, 256, 8, 11), (3001, 64, 6, 12), (16384, 256, 8, 13),
+                          (40000, 256, 8, 14)]:
         g = np.random.default_rng(seed)
         logits = torch.from_numpy(g.standard_normal((T, E)).astype(np.float32)).cuda()
         rc, got = _call_noalloc(lib, logits, k, stream)

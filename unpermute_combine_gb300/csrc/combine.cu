@@ -23,7 +23,7 @@
 // double-float additions (and, for a row cut into column parts, the parts'
 // double-float partials added in part order), so it is deterministic and far
 // more accurate than a plain float dot.
-#include "common.cuh"
+#include "pipeline.cuh"
 
 namespace moe {
 namespace {
@@ -257,6 +257,153 @@ __device__ __forceinline__ bool dd_sum_bf16(const float* w, const float* y, cons
     return false;
 }
 
+// At most one live term: the double slot-order sum is fma(w, y, +0), the
+// exact product (a zero product gives +0), rounded once; 4 vectors in flight
+// per lane (a lone row per step would leave the warp latency-bound).  Writes
+// columns [vb, ve) of the token's output row.
+__device__ __forceinline__ void combine_single(const uint4* __restrict__ y, int64_t nvec,
+                                               int64_t vb, int64_t ve, int lane, bool live,
+                                               int64_t p, float w, uint4* __restrict__ orow) {
+    const f2_t w2 = f2_pack(w, w);
+    for (int64_t v0 = vb + lane; v0 < ve; v0 += 32 * 4) {
+        uint4 d[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int64_t v = v0 + 32 * u;
+            d[u] = (live && v < ve) ? __ldcs(y + p * nvec + v) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int64_t v = v0 + 32 * u;
+            if (v >= ve) break;
+            uint4 r = make_uint4(0, 0, 0, 0);
+            if (live) {
+                r.x = plus_zero_bf16x2(scale_pair_bf16_f2(w2, f2_from_bf16x2(d[u].x)));
+                r.y = plus_zero_bf16x2(scale_pair_bf16_f2(w2, f2_from_bf16x2(d[u].y)));
+                r.z = plus_zero_bf16x2(scale_pair_bf16_f2(w2, f2_from_bf16x2(d[u].z)));
+                r.w = plus_zero_bf16x2(scale_pair_bf16_f2(w2, f2_from_bf16x2(d[u].w)));
+            }
+            __stcs(orow + v, r);
+        }
+    }
+}
+
+// One 16-byte column (8 bf16 elements) of a token's combine from its k slot
+// vectors d[j] (rows pj[j] < 0 are empty): the certified float sum, else the
+// double-float tier, else double -- the double slot-order sum rounded once.
+template <int KMAX, bool PLAIN>   // PLAIN: unit weights (plain sum)
+__device__ __forceinline__ uint4 combine_vector(const uint4 (&d)[KMAX], const int32_t (&pj)[KMAX],
+                                                const float (&wj)[KMAX], int k, float cbound,
+                                                float dd_bound) {
+    if constexpr (PLAIN) {
+        // plain sum (permute backward): every product is exact, so a
+        // TwoSum chain shows whether the float sum is the exact
+        // slot-order sum (then the double chain computes the same
+        // prefixes and it rounds directly); the rare inexact element
+        // goes through the certified tiers.  The chain runs on both
+        // elements of a 32-bit word at once (packed f32x2 add/sub
+        // round each half like the scalar operations).
+        uint4 res;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            f2_t hi2 = 0ull;
+            uint32_t err0 = 0, err1 = 0;      // error terms' magnitude bits
+#pragma unroll
+            for (int j = 0; j < KMAX; ++j) {
+                if (pj[j] < 0) continue;
+                const uint32_t wd = q == 0 ? d[j].x : q == 1 ? d[j].y : q == 2 ? d[j].z : d[j].w;
+                const f2_t y2 = f2_from_bf16x2(wd);
+                const f2_t s2 = f2_add(hi2, y2);
+                const f2_t bp = f2_sub(s2, hi2);
+                const f2_t e2 = f2_add(f2_sub(hi2, f2_sub(s2, bp)), f2_sub(y2, bp));
+                hi2 = s2;
+                err0 |= uint32_t(e2) & 0x7FFFFFFFu;
+                err1 |= uint32_t(e2 >> 32) & 0x7FFFFFFFu;
+            }
+            float hsum[2];
+            f2_unpack(hi2, hsum[0], hsum[1]);
+            uint16_t half[2];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int i = 2 * q + h;
+                if ((h == 0 ? err0 : err1) == 0) {
+                    half[h] = f32_to_bf16_rn(hsum[h]);
+                    continue;
+                }
+                float yv[KMAX];
+                bool valid[KMAX];
+#pragma unroll
+                for (int j = 0; j < KMAX; ++j) {
+                    valid[j] = pj[j] >= 0;
+                    yv[j] = unpack_bf16(d[j], i);
+                }
+                if (!dd_sum_bf16(wj, yv, valid, KMAX, dd_bound, &half[h])) {
+                    double acc = 0.0;
+#pragma unroll
+                    for (int j = 0; j < KMAX; ++j)
+                        if (valid[j]) acc = fma(double(wj[j]), double(yv[j]), acc);
+                    half[h] = f64_to_bf16_rn(acc);
+                }
+            }
+            set_word(res, q, uint32_t(half[0]) | (uint32_t(half[1]) << 16));
+        }
+        return res;
+    } else {
+        float s[8], a[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) { s[i] = 0.0f; a[i] = 0.0f; }
+#pragma unroll
+        for (int j = 0; j < KMAX; ++j) {
+            if (pj[j] < 0) continue;
+            const float w = wj[j], aw = fabsf(w);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float yv = unpack_bf16(d[j], i);
+                s[i] = __fmaf_rn(w, yv, s[i]);
+                a[i] = __fmaf_rn(aw, fabsf(yv), a[i]);
+            }
+        }
+        uint4 res;
+        uint32_t open = 0;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            float lo0, hi0, lo1, hi1;
+            certify_interval(s[2 * q], a[2 * q], cbound, k, lo0, hi0);
+            certify_interval(s[2 * q + 1], a[2 * q + 1], cbound, k, lo1, hi1);
+            const uint32_t lo = pack_bf16x2_rn(lo0, lo1);
+            const uint32_t hi = pack_bf16x2_rn(hi0, hi1);
+            set_word(res, q, lo);
+            if (lo != hi) open |= 1u << q;
+        }
+        if (open) {
+            bool valid[KMAX];
+#pragma unroll
+            for (int j = 0; j < KMAX; ++j) valid[j] = pj[j] >= 0;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                if (!(open & (1u << q))) continue;
+                uint16_t half[2];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    float yv[KMAX];
+#pragma unroll
+                    for (int j = 0; j < KMAX; ++j) yv[j] = unpack_bf16(d[j], 2 * q + h);
+                    if (!dd_sum_bf16(wj, yv, valid, KMAX, dd_bound, &half[h])) {
+                        // last resort: double, slot order, one rounding
+                        double acc = 0.0;
+#pragma unroll
+                        for (int j = 0; j < KMAX; ++j)
+                            if (valid[j]) acc = fma(double(wj[j]), double(yv[j]), acc);
+                        half[h] = f64_to_bf16_rn(acc);
+                    }
+                }
+                set_word(res, q, uint32_t(half[0]) | (uint32_t(half[1]) << 16));
+            }
+        }
+        return res;
+    }
+}
+
 // k <= 8: one 16-byte column per lane step with every slot row of it held in
 // registers, so an element whose rounding cannot be certified is recomputed
 // in double from the same registers (no reload).  (A cp.async ring as in
@@ -297,34 +444,8 @@ combine_bf16_regs_kernel(const uint4* __restrict__ y, int64_t T, int64_t nvec, i
             if (pj[j] >= 0 && nv++ == 0) j0 = j;
         }
         if (nv <= 1) {
-            // at most one term: the double slot-order sum is fma(w, y, +0), the
-            // exact product (a zero product gives +0), rounded once; 4 vectors
-            // in flight per lane (a lone row per step would leave the warp
-            // latency-bound)
-            const int64_t p = nv ? int64_t(s_pos[warp][j0]) : 0;
-            const float w = nv ? s_w[warp][j0] : 0.0f;
-            const f2_t w2 = f2_pack(w, w);
-            for (int64_t v0 = vb + lane; v0 < ve; v0 += 32 * 4) {
-                uint4 d[4];
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int64_t v = v0 + 32 * u;
-                    d[u] = (nv && v < ve) ? __ldcs(y + p * nvec + v) : make_uint4(0, 0, 0, 0);
-                }
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int64_t v = v0 + 32 * u;
-                    if (v >= ve) break;
-                    uint4 r = make_uint4(0, 0, 0, 0);
-                    if (nv) {
-                        r.x = plus_zero_bf16x2(scale_pair_bf16_f2(w2, f2_from_bf16x2(d[u].x)));
-                        r.y = plus_zero_bf16x2(scale_pair_bf16_f2(w2, f2_from_bf16x2(d[u].y)));
-                        r.z = plus_zero_bf16x2(scale_pair_bf16_f2(w2, f2_from_bf16x2(d[u].z)));
-                        r.w = plus_zero_bf16x2(scale_pair_bf16_f2(w2, f2_from_bf16x2(d[u].w)));
-                    }
-                    __stcs(out + t * nvec + v, r);
-                }
-            }
+            combine_single(y, nvec, vb, ve, lane, nv > 0, nv ? int64_t(s_pos[warp][j0]) : 0,
+                           nv ? s_w[warp][j0] : 0.0f, out + t * nvec);
             __syncwarp();
             continue;
         }
@@ -333,115 +454,100 @@ combine_bf16_regs_kernel(const uint4* __restrict__ y, int64_t T, int64_t nvec, i
 #pragma unroll
             for (int j = 0; j < KMAX; ++j)
                 d[j] = pj[j] >= 0 ? __ldcs(y + int64_t(pj[j]) * nvec + v) : make_uint4(0, 0, 0, 0);
-            if constexpr (PLAIN) {
-                // plain sum (permute backward): every product is exact, so a
-                // TwoSum chain shows whether the float sum is the exact
-                // slot-order sum (then the double chain computes the same
-                // prefixes and it rounds directly); the rare inexact element
-                // goes through the certified tiers.  The chain runs on both
-                // elements of a 32-bit word at once (packed f32x2 add/sub
-                // round each half like the scalar operations).
-                uint4 res;
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    f2_t hi2 = 0ull;
-                    uint32_t err0 = 0, err1 = 0;      // error terms' magnitude bits
-#pragma unroll
-                    for (int j = 0; j < KMAX; ++j) {
-                        if (pj[j] < 0) continue;
-                        const uint32_t wd = q == 0 ? d[j].x : q == 1 ? d[j].y : q == 2 ? d[j].z : d[j].w;
-                        const f2_t y2 = f2_from_bf16x2(wd);
-                        const f2_t s2 = f2_add(hi2, y2);
-                        const f2_t bp = f2_sub(s2, hi2);
-                        const f2_t e2 = f2_add(f2_sub(hi2, f2_sub(s2, bp)), f2_sub(y2, bp));
-                        hi2 = s2;
-                        err0 |= uint32_t(e2) & 0x7FFFFFFFu;
-                        err1 |= uint32_t(e2 >> 32) & 0x7FFFFFFFu;
-                    }
-                    float hsum[2];
-                    f2_unpack(hi2, hsum[0], hsum[1]);
-                    uint16_t half[2];
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const int i = 2 * q + h;
-                        if ((h == 0 ? err0 : err1) == 0) {
-                            half[h] = f32_to_bf16_rn(hsum[h]);
-                            continue;
-                        }
-                        float yv[KMAX];
-                        bool valid[KMAX];
-#pragma unroll
-                        for (int j = 0; j < KMAX; ++j) {
-                            valid[j] = pj[j] >= 0;
-                            yv[j] = unpack_bf16(d[j], i);
-                        }
-                        if (!dd_sum_bf16(wj, yv, valid, KMAX, dd_bound, &half[h])) {
-                            double acc = 0.0;
-#pragma unroll
-                            for (int j = 0; j < KMAX; ++j)
-                                if (valid[j]) acc = fma(double(wj[j]), double(yv[j]), acc);
-                            half[h] = f64_to_bf16_rn(acc);
-                        }
-                    }
-                    set_word(res, q, uint32_t(half[0]) | (uint32_t(half[1]) << 16));
-                }
-                __stcs(out + t * nvec + v, res);
-            } else {
-                float s[8], a[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) { s[i] = 0.0f; a[i] = 0.0f; }
-#pragma unroll
-                for (int j = 0; j < KMAX; ++j) {
-                    if (pj[j] < 0) continue;
-                    const float w = wj[j], aw = fabsf(w);
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const float yv = unpack_bf16(d[j], i);
-                        s[i] = __fmaf_rn(w, yv, s[i]);
-                        a[i] = __fmaf_rn(aw, fabsf(yv), a[i]);
-                    }
-                }
-                uint4 res;
-                uint32_t open = 0;
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    float lo0, hi0, lo1, hi1;
-                    certify_interval(s[2 * q], a[2 * q], cbound, k, lo0, hi0);
-                    certify_interval(s[2 * q + 1], a[2 * q + 1], cbound, k, lo1, hi1);
-                    const uint32_t lo = pack_bf16x2_rn(lo0, lo1);
-                    const uint32_t hi = pack_bf16x2_rn(hi0, hi1);
-                    set_word(res, q, lo);
-                    if (lo != hi) open |= 1u << q;
-                }
-                if (open) {
-                    bool valid[KMAX];
-#pragma unroll
-                    for (int j = 0; j < KMAX; ++j) valid[j] = pj[j] >= 0;
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        if (!(open & (1u << q))) continue;
-                        uint16_t half[2];
-#pragma unroll
-                        for (int h = 0; h < 2; ++h) {
-                            float yv[KMAX];
-#pragma unroll
-                            for (int j = 0; j < KMAX; ++j) yv[j] = unpack_bf16(d[j], 2 * q + h);
-                            if (!dd_sum_bf16(wj, yv, valid, KMAX, dd_bound, &half[h])) {
-                                // last resort: double, slot order, one rounding
-                                double acc = 0.0;
-#pragma unroll
-                                for (int j = 0; j < KMAX; ++j)
-                                    if (valid[j]) acc = fma(double(wj[j]), double(yv[j]), acc);
-                                half[h] = f64_to_bf16_rn(acc);
-                            }
-                        }
-                        set_word(res, q, uint32_t(half[0]) | (uint32_t(half[1]) << 16));
-                    }
-                }
-                __stcs(out + t * nvec + v, res);
-            }
+            __stcs(out + t * nvec + v, combine_vector<KMAX, PLAIN>(d, pj, wj, k, cbound, dd_bound));
         }
         __syncwarp();
+    }
+}
+
+// k <= 8 with a token's slot rows together at most kCbStageMax bytes (the
+// layer, mid and virtual-EP shapes): one CTA of 8 warps per token at a time.
+// Lanes 0..k-1 of warp 0 each bulk-copy one whole slot row (cp.async.bulk,
+// a few KB contiguous, so HBM sees long runs instead of 512-byte pieces of
+// scattered rows) into a ring stage; every thread then takes 16-byte columns
+// of the token from shared memory through the same column arithmetic as the
+// register kernel and writes the output row.  The ring holds kCbStages
+// tokens, so the next tokens' rows stream in while one is combined.
+constexpr int kCbStages = 3;
+constexpr int kCbStageMax = 32768;
+constexpr int kCbThreads = 256;
+
+template <int KMAX, bool PLAIN>
+__global__ void __launch_bounds__(kCbThreads)
+combine_bf16_bulk_kernel(const uint8_t* __restrict__ y, int64_t T, int64_t nvec, int k,
+                         int64_t n_rows, const int32_t* __restrict__ slot_pos,
+                         const float* __restrict__ topk_w, uint4* __restrict__ out, float cbound,
+                         float dd_bound, uint32_t* __restrict__ status) {
+    extern __shared__ __align__(128) uint8_t cb_smem[];         // [kCbStages][KMAX][row]
+    __shared__ __align__(8) uint64_t full_bar[kCbStages];
+    __shared__ int32_t s_pos[kCbStages][KMAX];
+    __shared__ float s_w[kCbStages][KMAX];
+    __shared__ int s_failed;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t row_bytes = uint32_t(nvec) * 16u;
+    const int64_t first = blockIdx.x;
+    const int64_t my = first < T ? (T - first + gridDim.x - 1) / gridDim.x : 0;
+    const uint32_t smem0 = smem_addr(cb_smem);
+    if (tid == 0) {
+        for (int s = 0; s < kCbStages; ++s) mbar_init(smem_addr(&full_bar[s]), 1);
+        mbar_fence_init();
+        s_failed = 0;
+    }
+    __syncthreads();
+    // warp 0: slot rows and weights of token q into stage q % kCbStages
+    auto issue = [&](int64_t q) {
+        const int64_t t = first + q * int64_t(gridDim.x);
+        const int st = int(q % kCbStages);
+        int32_t p = -1;
+        if (lane < k) {
+            p = slot_pos[t * k + lane];
+            if (p < 0 || p >= n_rows) p = -1;
+            s_pos[st][lane] = p;
+            s_w[st][lane] = PLAIN ? 1.0f : topk_w[t * k + lane];
+        }
+        const uint32_t live = __ballot_sync(0xFFFFFFFFu, p >= 0);
+        const uint32_t bar = smem_addr(&full_bar[st]);
+        if (lane == 0) mbar_expect_tx(bar, uint32_t(__popc(live)) * row_bytes);
+        __syncwarp();
+        if (p >= 0)
+            bulk_load(smem0 + (uint32_t(st) * KMAX + uint32_t(lane)) * row_bytes,
+                      y + int64_t(p) * row_bytes, row_bytes, bar);
+    };
+    if (warp == 0)
+        for (int64_t q = 0; q < my && q < kCbStages; ++q) issue(q);
+    int64_t q_fail = -1;
+    for (int64_t q = 0; q < my; ++q) {
+        const int64_t t = first + q * int64_t(gridDim.x);
+        const int st = int(q % kCbStages);
+        if (!mbar_wait(smem_addr(&full_bar[st]), uint32_t(q / kCbStages) & 1u)) s_failed = 1;
+        __syncthreads();
+        if (s_failed) {
+            q_fail = q;
+            break;
+        }
+        int32_t pj[KMAX];
+        float wj[KMAX];
+#pragma unroll
+        for (int j = 0; j < KMAX; ++j) {
+            pj[j] = j < k ? s_pos[st][j] : -1;
+            wj[j] = j < k ? s_w[st][j] : 0.0f;
+        }
+        const uint4* stage = reinterpret_cast<const uint4*>(cb_smem + size_t(st) * KMAX * row_bytes);
+        for (int64_t v = tid; v < nvec; v += kCbThreads) {
+            uint4 d[KMAX];
+#pragma unroll
+            for (int j = 0; j < KMAX; ++j)
+                d[j] = pj[j] >= 0 ? stage[j * nvec + v] : make_uint4(0, 0, 0, 0);
+            __stcs(out + t * nvec + v, combine_vector<KMAX, PLAIN>(d, pj, wj, k, cbound, dd_bound));
+        }
+        __syncthreads();                        // every thread is done with the stage
+        if (warp == 0 && q + kCbStages < my) issue(q + kCbStages);
+    }
+    if (q_fail >= 0 && tid == 0) {
+        // rows still landing in the stages of tokens q_fail .. q_fail + stages - 1
+        for (int64_t i = q_fail; i < my && i < q_fail + kCbStages; ++i)
+            mbar_wait(smem_addr(&full_bar[i % kCbStages]), uint32_t(i / kCbStages) & 1u);
+        if (status) atomicExch(status, uint32_t(MOE_ERR_TIMEOUT));
     }
 }
 
@@ -903,8 +1009,23 @@ extern "C" moe_status_t moe_combine(const void* expert_out, moe_dtype_t dtype, i
         const uint4* yv = static_cast<const uint4*>(expert_out);
         uint4* ov = static_cast<uint4*>(out);
         const float cb = combine_bound_factor(k);
-        if (k <= 8) {
-            const bool plain = topk_w == nullptr;
+        const bool plain = topk_w == nullptr;
+        const size_t stage_bytes = size_t(k <= 2 ? 2 : k <= 4 ? 4 : k <= 6 ? 6 : 8) * row;
+        // the staged kernel wins on rows of at most two slots (mid shape: 63.6 ->
+        // 42.1 us); at six slots of 4 KB rows the register kernel is faster
+        // (32 vs 41 us), so wider slot counts keep it
+        if (k >= 2 && k <= 4 && stage_bytes <= size_t(kCbStageMax)) {
+            const auto kern =
+                k <= 2 ? (plain ? combine_bf16_bulk_kernel<2, true> : combine_bf16_bulk_kernel<2, false>)
+                : k <= 4 ? (plain ? combine_bf16_bulk_kernel<4, true> : combine_bf16_bulk_kernel<4, false>)
+                : k <= 6 ? (plain ? combine_bf16_bulk_kernel<6, true> : combine_bf16_bulk_kernel<6, false>)
+                         : (plain ? combine_bf16_bulk_kernel<8, true> : combine_bf16_bulk_kernel<8, false>);
+            const size_t smem = kCbStages * stage_bytes;
+            if (!opt_in_smem((const void*)kern, int(kCbStages * kCbStageMax))) return MOE_ERR_CUDA;
+            kern<<<grid_for((const void*)kern, kCbThreads, smem, T), kCbThreads, smem, s>>>(
+                static_cast<const uint8_t*>(expert_out), T, H / 8, k, n_rows, slot_pos, topk_w, ov,
+                cb, dd_bound_factor(k), device_status_word());
+        } else if (k <= 8) {
             const auto kern =
                 k <= 1 ? (plain ? combine_bf16_regs_kernel<1, true> : combine_bf16_regs_kernel<1, false>)
                 : k <= 2 ? (plain ? combine_bf16_regs_kernel<2, true> : combine_bf16_regs_kernel<2, false>)

@@ -171,6 +171,7 @@ permute_quantize_fp8_kernel(const uint8_t* __restrict__ x, int64_t T, int H, int
     if (tid == 0)
         for (int64_t q = 0; q < my && q < kPQStages; ++q) issue_load(q);
 
+    int64_t q_fail = 0;
     for (int64_t q = 0; q < my; ++q) {
         const int64_t t = first + q * int64_t(gridDim.x);
         const int st = int(q % kPQStages);
@@ -186,7 +187,10 @@ permute_quantize_fp8_kernel(const uint8_t* __restrict__ x, int64_t T, int H, int
         }
         if (!mbar_wait(smem_addr(&full_bar[st]), ph)) s_failed = 1;
         __syncthreads();
-        if (s_failed) break;
+        if (s_failed) {
+            q_fail = q;
+            break;
+        }
 
         const uint8_t* in = smem + uint32_t(st) * stage_bytes;
         uint8_t* outq = smem + uint32_t(st) * stage_bytes + in_bytes;
@@ -230,7 +234,14 @@ permute_quantize_fp8_kernel(const uint8_t* __restrict__ x, int64_t T, int H, int
         if (tid == 0 && q + kPQStages < my) issue_load(q + kPQStages);
     }
     if (warp == 0 && lane < k) bulk_wait_all();
-    if (tid == 0 && s_failed && status) atomicExch(status, uint32_t(MOE_ERR_TIMEOUT));
+    if (tid == 0 && s_failed) {
+        // loads issued but never consumed (items q_fail .. q_fail + stages - 1)
+        // may still be landing in this CTA's shared memory: wait for each
+        // (bounded) before the CTA exits and the memory is reused
+        for (int64_t i = q_fail; i < my && i < q_fail + kPQStages; ++i)
+            mbar_wait(smem_addr(&full_bar[i % kPQStages]), uint32_t(i / kPQStages) & 1u);
+        if (status) atomicExch(status, uint32_t(MOE_ERR_TIMEOUT));
+    }
 }
 
 int grid_pq(const void* kernel, size_t smem, int64_t T) {

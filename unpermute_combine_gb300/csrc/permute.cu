@@ -119,12 +119,14 @@ permute_bulk_kernel(const uint8_t* __restrict__ x, int64_t T, int64_t row_bytes,
         for (int64_t q = 0; q < my_items && q < kPermStages; ++q) issue_load(q);
     int32_t p_cur = slot_of(0);
     bool failed = false;
+    int64_t q_fail = 0;
     for (int64_t q = 0; q < my_items; ++q) {
         const int32_t p_next = slot_of(q + 1);               // in flight meanwhile
         const int s = int(q % kPermStages);
         const uint32_t ph = uint32_t(q / kPermStages) & 1u;
         if (!__all_sync(0xFFFFFFFFu, mbar_wait(smem_addr(&full_bar[s]), ph))) {
             failed = true;
+            q_fail = q;
             break;
         }
         int64_t t;
@@ -145,7 +147,15 @@ permute_bulk_kernel(const uint8_t* __restrict__ x, int64_t T, int64_t row_bytes,
         p_cur = p_next;
     }
     bulk_wait_all();
-    if (failed && lane == 0 && status) atomicExch(status, uint32_t(MOE_ERR_TIMEOUT));
+    if (failed && lane == 0) {
+        // loads issued but never consumed (items q_fail .. the last one
+        // issued) may still be landing in this CTA's shared memory: wait for
+        // each (bounded) before the CTA exits and the memory is reused
+        const int64_t last = min64(my_items - 1, max64(kPermStages - 1, q_fail + kPermStages - 2));
+        for (int64_t i = q_fail; i <= last; ++i)
+            mbar_wait(smem_addr(&full_bar[i % kPermStages]), uint32_t(i / kPermStages) & 1u);
+        if (status) atomicExch(status, uint32_t(MOE_ERR_TIMEOUT));
+    }
 }
 
 int grid_for(const void* kernel, int threads, size_t smem, int64_t work_blocks) {
@@ -423,11 +433,13 @@ sort_chunks_bulk_kernel(const uint8_t* __restrict__ in, int64_t N, int64_t row_b
     if (lane == 0)
         for (int64_t q = 0; q < my_items && q < kScStages; ++q) issue_load(q);
     bool failed = false;
+    int64_t q_fail = 0;
     for (int64_t q = 0; q < my_items; ++q) {
         const int st = int(q % kScStages);
         const uint32_t ph = uint32_t(q / kScStages) & 1u;
         if (!__all_sync(full, mbar_wait(smem_addr(&full_bar[st]), ph))) {
             failed = true;
+            q_fail = q;
             break;
         }
         if (lane == 0) {
@@ -443,7 +455,14 @@ sort_chunks_bulk_kernel(const uint8_t* __restrict__ in, int64_t N, int64_t row_b
         __syncwarp();
     }
     if (lane == 0) bulk_wait_all();
-    if (failed && lane == 0 && status) atomicExch(status, uint32_t(MOE_ERR_TIMEOUT));
+    if (failed && lane == 0) {
+        // pieces loaded but never stored may still be landing in this CTA's
+        // shared memory: wait for each (bounded) before the CTA exits
+        const int64_t last = min64(my_items - 1, max64(kScStages - 1, q_fail + kScStages - 2));
+        for (int64_t i = q_fail; i <= last; ++i)
+            mbar_wait(smem_addr(&full_bar[i % kScStages]), uint32_t(i / kScStages) & 1u);
+        if (status) atomicExch(status, uint32_t(MOE_ERR_TIMEOUT));
+    }
 }
 
 size_t chunk_plan_bytes(int C) {
@@ -481,6 +500,53 @@ expert_scale_kernel(const T* __restrict__ in, int64_t n_rows, int64_t H, int E,
                 out[p * H + h] = __fmul_rn(in[p * H + h], s);
             } else {
                 out[p * H + h] = uint16_t(mul_bf16_rn(bf16_to_f32(in[p * H + h]), s));
+            }
+        }
+    }
+}
+
+// bf16 rows that are 16-byte multiples: one warp per row, 16-byte vectors,
+// four in flight per lane; each element is the exact product rounded once
+// (the same arithmetic as expert_scale_kernel).
+__global__ void __launch_bounds__(kThreads)
+expert_scale_vec_kernel(const uint4* __restrict__ in, int64_t n_rows, int64_t nvec, int E,
+                        const int32_t* __restrict__ offsets, const float* __restrict__ scale,
+                        uint4* __restrict__ out) {
+    __shared__ int32_t s_off[kMaxExperts + 1];
+    __shared__ float s_scale[kMaxExperts];
+    for (int e = threadIdx.x; e <= E; e += kThreads) s_off[e] = offsets[e];
+    for (int e = threadIdx.x; e < E; e += kThreads) s_scale[e] = scale[e];
+    __syncthreads();
+    const int64_t rows = min64(n_rows, s_off[E]);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int64_t p = int64_t(blockIdx.x) * kWarps + warp; p < rows;
+         p += int64_t(gridDim.x) * kWarps) {
+        int lo = 0, hi = E - 1;          // last e with offsets[e] <= p
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (s_off[mid] <= p) lo = mid; else hi = mid - 1;
+        }
+        const float sc = s_scale[lo];
+        const uint4* src = in + p * nvec;
+        uint4* dst = out + p * nvec;
+        for (int64_t v0 = lane; v0 < nvec; v0 += 32 * 4) {
+            uint4 d[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int64_t v = v0 + 32 * u;
+                d[u] = v < nvec ? __ldcs(src + v) : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int64_t v = v0 + 32 * u;
+                if (v >= nvec) break;
+                const uint32_t w[4] = {d[u].x, d[u].y, d[u].z, d[u].w};
+                uint32_t r[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    r[i] = mul_bf16_rn(bf16lo_to_f32(w[i]), sc) |
+                           (mul_bf16_rn(bf16hi_to_f32(w[i]), sc) << 16);
+                __stcs(dst + v, make_uint4(r[0], r[1], r[2], r[3]));
             }
         }
     }
@@ -675,6 +741,11 @@ extern "C" moe_status_t moe_expert_scale(const void* in, moe_dtype_t dtype, int6
         const int g = grid_for((const void*)expert_scale_kernel<float>, kThreads, 0, want);
         expert_scale_kernel<float><<<g, kThreads, 0, s>>>(
             static_cast<const float*>(in), n_rows, H, E, offsets, scale, static_cast<float*>(out));
+    } else if ((H * 2) % 16 == 0 && aligned16(in) && aligned16(out)) {
+        const int g = grid_for((const void*)expert_scale_vec_kernel, kThreads, 0, want);
+        expert_scale_vec_kernel<<<g, kThreads, 0, s>>>(
+            static_cast<const uint4*>(in), n_rows, H / 8, E, offsets, scale,
+            static_cast<uint4*>(out));
     } else {
         const int g = grid_for((const void*)expert_scale_kernel<uint16_t>, kThreads, 0, want);
         expert_scale_kernel<uint16_t><<<g, kThreads, 0, s>>>(

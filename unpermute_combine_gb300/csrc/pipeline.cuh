@@ -1,9 +1,9 @@
 // pipeline.cuh -- mbarrier and bulk-copy (TMA) helpers for the staged kernels.
 //
-// Every wait is bounded: mbar_wait gives up after kSpinLimit polls of
-// mbarrier.try_wait (each poll suspends the thread for at most a short,
-// hardware-defined time), so a pipeline that never completes ends with an
-// error status instead of hanging the GPU.  Bulk (non-tensor) copies are
+// Every wait is bounded: mbar_wait gives up after 2 s of wall time (global
+// timer) or kSpinLimit polls of mbarrier.try_wait (each with a 2 us
+// suspend-time hint), so a pipeline that never completes ends with an error
+// status within seconds instead of hanging the GPU.  Bulk (non-tensor) copies are
 // kept for staged kernels; the grouped GEMM uses the mbarrier helpers.
 #pragma once
 
@@ -47,23 +47,47 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
     return done != 0;
 }
 
-// Bounded wait for the phase of the given parity: at most `limit` polls of
-// mbarrier.try_wait; false if it gave up.
+// Nanoseconds of the GPU's global timer.
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// A pipeline wait gives up after this much wall time.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;      // 2 s
+// Suspend-time hint of one mbarrier.try_wait poll.
+constexpr uint32_t kPollHintNs = 2000;
+
+// One poll: mbarrier.try_wait with a short suspend-time hint.
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n"
+        " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+        " selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(done) : "r"(bar), "r"(parity), "n"(kPollHintNs) : "memory");
+    return done != 0;
+}
+
+// Bounded wait for the phase of the given parity: at most `limit` polls;
+// false if it gave up.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint32_t limit) {
-    for (uint32_t i = 0; i < limit; ++i) {
-        uint32_t done;
-        asm volatile(
-            "{\n .reg .pred p;\n"
-            " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-            " selp.u32 %0, 1, 0, p;\n}"
-            : "=r"(done) : "r"(bar), "r"(parity) : "memory");
-        if (done) return true;
-    }
+    for (uint32_t i = 0; i < limit; ++i)
+        if (mbar_try(bar, parity)) return true;
     return false;
 }
 
+// The pipelines' wait: gives up after kWaitLimitNs of wall time (or
+// kSpinLimit polls, whichever comes first); false if it gave up.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-    return mbar_wait_bounded(bar, parity, kSpinLimit);
+    if (mbar_try(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    for (uint32_t i = 1; i < kSpinLimit; ++i) {
+        if (mbar_try(bar, parity)) return true;
+        if (global_ns() - t0 > kWaitLimitNs) return false;
+    }
+    return false;
 }
 
 // Bulk copy global -> shared (both 16-byte aligned, size a multiple of 16),

@@ -24,6 +24,7 @@
 #include <cmath>
 
 #include "common.cuh"
+#include "route_fast.cuh"
 
 namespace moe {
 namespace {
@@ -593,9 +594,17 @@ moe_status_t finish_route(const int32_t* topk_idx, const float* topk_w, int64_t 
     return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
+// Scratch after the header: the larger of what the general kernels and the
+// route_fast kernels (up to 256 experts) need.
+size_t route_hist_bytes(int64_t T, int E) {
+    const size_t a = hist_bytes(T, E);
+    const size_t b = E <= kFastMaxExperts ? fast_hist_bytes(T, E) : 0;
+    return a > b ? a : b;
+}
+
 moe_status_t check_workspace(const void* ws, size_t ws_bytes, int64_t T, int E) {
     if (!ws || (reinterpret_cast<uintptr_t>(ws) & (kWsAlign - 1))) return MOE_ERR_WORKSPACE;
-    if (ws_bytes < kWsAlign + hist_bytes(T, E)) return MOE_ERR_WORKSPACE;
+    if (ws_bytes < kWsAlign + route_hist_bytes(T, E)) return MOE_ERR_WORKSPACE;
     return MOE_OK;
 }
 
@@ -608,7 +617,7 @@ extern "C" moe_status_t moe_route_workspace_size(int64_t T, int E, int k, size_t
     if (!bytes) return MOE_ERR_INVALID_ARG;
     const moe_status_t st = validate_sizes(T, E, k);
     if (st != MOE_OK) return st;
-    *bytes = kWsAlign + hist_bytes(T, E);
+    *bytes = kWsAlign + route_hist_bytes(T, E);
     return MOE_OK;
 }
 
@@ -631,6 +640,10 @@ moe_status_t route_from_logits(const float* logits, int64_t T, int E, int k, int
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     WsHeader* header = static_cast<WsHeader*>(workspace);
     int32_t* hist = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + kWsAlign);
+    if (fast_route_supported(E, n_groups))
+        return fast_route(logits, T, E, k, n_groups, topk_groups, topk_idx, topk_w, counts,
+                          offsets, group_list, sorted_indices, slot_pos, permuted_probs,
+                          routing_map, header, hist, s);
     if (T > 0) {
         const int nv = (E + 31) / 32;
         const int g = n_groups, kg = topk_groups;
@@ -806,7 +819,8 @@ extern "C" moe_status_t moe_route_noalloc(const float* logits, int64_t T, int E,
                                           void* stream) {
     const moe_status_t st = validate_sizes(T, E, k);
     if (st != MOE_OK) return st;
-    if (kWsAlign + hist_bytes(T, E) > MOE_ROUTE_NOALLOC_SCRATCH_BYTES) return MOE_ERR_UNSUPPORTED;
+    if (kWsAlign + route_hist_bytes(T, E) > MOE_ROUTE_NOALLOC_SCRATCH_BYTES)
+        return MOE_ERR_UNSUPPORTED;
     void* scratch = nullptr;
     const moe_status_t sst = noalloc_scratch(&scratch);
     if (sst != MOE_OK) return sst;

@@ -1,0 +1,1007 @@
+// route_fast.cu -- moe_route / moe_route_grouped for up to 256 experts.
+//
+// The same outputs as the general route in route.cu: top-k over the router
+// logits with a softmax over the k chosen scores ("从零理解 MoE 算子" §3;
+// group-limited variant §21), tokens per expert and their prefixes
+// (group_list, §7), and the expert-major, token-ascending sorted_indices of a
+// masked_select over the transposed routing map ("token dispatcher +
+// fuse_a2a" §1.1) with its inverse slot_pos.  Two launches:
+//
+//   K1  one block of 32 warps per SM, each block a contiguous run of at most
+//       128 tokens.  The block's logits arrive in shared memory by bulk copy
+//       (four 32-token chunks, one mbarrier each), so every byte the block
+//       needs is in flight from the start.  A warp ranks one token at a time:
+//       lane l holds experts [l*V, l*V + V) as unique 32-bit keys -- the top
+//       24 bits of the order-preserving bit pattern of the logit above the
+//       8-bit complement of the expert id -- so one warp max-reduction names
+//       the round's winner and its owner.  Each lane keeps its best two keys
+//       and rescans only when it is popped a second time.  The truncated
+//       keys order exactly unless two candidates share a 24-bit bucket with
+//       different logits; the k winners and the (k+1)-th are checked for that
+//       and such a token (rare: ~1e-3 of tokens on continuous logits, never
+//       for exact ties) is ranked again on the exact 32-bit patterns.  Then
+//       the fp32 softmax, and for every slot a bit in a per-expert token mask
+//       of the block: an expert's count is the popcount of its mask, a slot's
+//       rank inside the block the popcount of the bits below its token.
+//       Writes topk_idx, topk_w, a histogram row per block and the in-block
+//       rank of every slot (into slot_pos, overwritten by K2).
+//   K2  (programmatic dependent launch) per block: the per-expert totals and
+//       the sum of the earlier blocks' rows (read straight from the rows for
+//       up to 256 blocks, else from a scan kernel's exclusive prefixes), the
+//       exclusive scan of the totals (offsets), and the final position
+//       offsets[e] + before[e] + rank of every slot.
+//
+// Position of (t, e) = offsets[e] + #{t' < t : e in topk(t')}: integer
+// arithmetic throughout, so the result is bit-exact and independent of
+// scheduling.  No kernel waits on another block.
+#include <cmath>
+
+#include "pipeline.cuh"
+#include "route_fast.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kKThreads = 1024;                  // K1: 32 warps
+constexpr int kKWarps = kKThreads / 32;
+constexpr int kMinTokens = 32;                   // tokens per K1 block, at least
+constexpr int kMaxTokens = 128;                  // ... at most: 4 mask words per expert
+constexpr int kChunkTokens = 8;                  // tokens per bulk-load chunk
+constexpr int kChunks = kMaxTokens / kChunkTokens;
+constexpr int kSizingSms = 512;                  // SM count assumed when sizing the workspace
+constexpr int kFusedMaxBlocks = 256;             // K2 sums the histogram rows itself up to here
+constexpr int kPThreads = 1024;                  // K2
+constexpr uint32_t kFull = 0xFFFFFFFFu;
+
+// 16-bit histogram counts, rows padded to 16 bytes
+__host__ __device__ inline int hist_stride(int E) { return (E + 7) & ~7; }
+
+int values_per_lane(int E) { return E <= 32 ? 1 : E <= 64 ? 2 : E <= 128 ? 4 : 8; }
+
+int64_t tokens_per_block(int64_t T, int sms) {
+    const int64_t tpb = (T + sms - 1) / sms;
+    return tpb < kMinTokens ? kMinTokens : tpb > kMaxTokens ? kMaxTokens : tpb;
+}
+
+// Histogram rows any T can need: G = ceil(T / tpb) with tpb as above and at
+// most kSizingSms SMs, so G <= max(min(kSizingSms, ceil(T/32)), ceil(T/128)).
+int64_t max_blocks(int64_t T) {
+    const int64_t a = (T + kMinTokens - 1) / kMinTokens;
+    const int64_t b = (T + kMaxTokens - 1) / kMaxTokens;
+    const int64_t lo = a < kSizingSms ? a : kSizingSms;
+    return lo > b ? lo : b;
+}
+
+// Order-preserving 32-bit pattern of a float (larger value -> larger
+// pattern); -0 is folded onto +0 so the two compare equal.  Every finite
+// value maps above 0.
+__device__ __forceinline__ uint32_t exact_key(float f) {
+    const uint32_t u = __float_as_uint(f + 0.0f);
+    return u ^ (uint32_t(int32_t(u) >> 31) | 0x80000000u);
+}
+
+__device__ __forceinline__ float exact_key_value(uint32_t k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
+// ------------------------------------------------------------------------ K1
+
+// Best two keys of a lane (h > r, 0 where there are fewer).
+template <int V>
+__device__ __forceinline__ void top2(const uint32_t (&key)[V], uint32_t& h, uint32_t& r) {
+    h = 0u;
+    r = 0u;
+#pragma unroll
+    for (int v = 0; v < V; ++v) {
+        const uint32_t lo = min(h, key[v]);
+        h = max(h, key[v]);
+        r = max(r, lo);
+    }
+}
+
+// Best two keys of a lane below `below`.
+template <int V>
+__device__ __forceinline__ void top2_below(const uint32_t (&key)[V], uint32_t below, uint32_t& h,
+                                           uint32_t& r) {
+    h = 0u;
+    r = 0u;
+#pragma unroll
+    for (int v = 0; v < V; ++v) {
+        const uint32_t x = key[v] < below ? key[v] : 0u;
+        const uint32_t lo = min(h, x);
+        h = max(h, x);
+        r = max(r, lo);
+    }
+}
+
+// V logits per lane (expert e = lane*V + v); up to KMAX slots (rounds
+// unrolled); FULL: E == 32*V (no lane holds a missing expert).
+template <int V, int KMAX, bool GROUPED, bool FULL>
+__global__ void __launch_bounds__(kKThreads, 1)
+route_fast_topk_kernel(const float* __restrict__ logits, int64_t T, int E, int k, int tpb,
+                       bool bulk, int32_t* __restrict__ topk_idx, float* __restrict__ topk_w,
+                       uint8_t* __restrict__ routing_map, uint16_t* __restrict__ hist,
+                       int32_t* __restrict__ rank_out, int n_groups, int topk_groups,
+                       uint32_t* __restrict__ dev_status) {
+    // the scatter kernel may be scheduled now; it waits for this grid to end
+    asm volatile("griddepcontrol.launch_dependents;");
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    __shared__ __align__(8) uint64_t bars[kChunks];
+    __shared__ uint32_t s_m[kKWarps][KMAX + 2];      // the rounds' winning keys, per warp
+    __shared__ int s_fail;
+    const int W = (tpb + 31) >> 5;                                   // mask words per expert
+    float* s_logits = reinterpret_cast<float*>(smem_raw);          // [tpb*E + 32*V] if bulk
+    uint32_t* s_mask = reinterpret_cast<uint32_t*>(
+        smem_raw + (bulk ? (size_t(tpb) * E + 32 * V) * sizeof(float) : 0));   // [E][W]
+    int32_t* s_idx = reinterpret_cast<int32_t*>(s_mask + size_t(E) * W);        // [tpb*k]
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t t0 = int64_t(blockIdx.x) * tpb;
+    const int nt = int(min64(tpb, T - t0));
+    const int nchunks = (nt + kChunkTokens - 1) / kChunkTokens;
+    if (threadIdx.x == 0) {
+        s_fail = 0;
+        if (bulk) {
+            for (int c = 0; c < nchunks; ++c) mbar_init(smem_addr(&bars[c]), 1);
+            mbar_fence_init();
+        }
+    }
+    for (int i = threadIdx.x; i < E * W; i += kKThreads) s_mask[i] = 0u;
+    for (int i = threadIdx.x; i < nt * k; i += kKThreads) s_idx[i] = -1;
+    __syncthreads();
+    if (bulk && threadIdx.x == 0) {
+        for (int c = 0; c < nchunks; ++c) {
+            const int n = min(kChunkTokens, nt - kChunkTokens * c);
+            const uint32_t bytes = uint32_t(n) * uint32_t(E) * 4u;
+            const uint32_t bar = smem_addr(&bars[c]);
+            mbar_expect_tx(bar, bytes);
+            bulk_load(smem_addr(s_logits + size_t(kChunkTokens * c) * E),
+                      logits + (t0 + kChunkTokens * c) * E, bytes, bar);
+        }
+    }
+
+    // group-limited routing: lanes per group (a power of two)
+    const int lpg = GROUPED ? E / n_groups / V : 1;
+    // low byte of every key: 255 - expert id
+    uint32_t nid[V];
+#pragma unroll
+    for (int v = 0; v < V; ++v) nid[v] = uint32_t(255 - (lane * V + v));
+    uint32_t* sm = s_m[warp];
+
+    for (int tl = warp; tl < nt; tl += kKWarps) {
+        const int64_t t = t0 + tl;
+        const float* grow = logits + t * E;
+        const float* srow = s_logits + size_t(tl) * E;
+        float val[V];
+        if (bulk) {
+            const bool ok = __all_sync(kFull, mbar_wait(smem_addr(&bars[tl / kChunkTokens]), 0));
+            if (!ok) {
+                if (lane == 0) s_fail = 1;
+                continue;
+            }
+            if (V >= 4) {
+#pragma unroll
+                for (int q = 0; q < V / 4; ++q) {
+                    const float4 f = *reinterpret_cast<const float4*>(srow + lane * V + 4 * q);
+                    val[4 * q] = f.x; val[4 * q + 1] = f.y; val[4 * q + 2] = f.z; val[4 * q + 3] = f.w;
+                }
+            } else if (V == 2) {
+                const float2 f = *reinterpret_cast<const float2*>(srow + lane * V);
+                val[0] = f.x;
+                val[V - 1] = f.y;
+            } else {
+                val[0] = srow[lane];
+            }
+        } else {
+#pragma unroll
+            for (int v = 0; v < V; ++v) {
+                const int e = lane * V + v;
+                val[v] = (FULL || e < E) ? __ldg(grow + e) : 0.0f;
+            }
+        }
+        uint32_t key[V];
+#pragma unroll
+        for (int v = 0; v < V; ++v) {
+            key[v] = (exact_key(val[v]) & 0xFFFFFF00u) | nid[v];
+            if (!FULL && lane * V + v >= E) key[v] = 0u;
+        }
+        if (GROUPED) {
+            // group score = largest logit of the group (exact patterns); keep
+            // the topk_groups best groups, equal scores to the lower group id
+            uint32_t gm = 0u;
+#pragma unroll
+            for (int v = 0; v < V; ++v)
+                if (FULL || lane * V + v < E) gm = max(gm, exact_key(val[v]));
+            for (int off = 1; off < lpg; off <<= 1) gm = max(gm, __shfl_xor_sync(kFull, gm, off));
+            const bool lead = (lane & (lpg - 1)) == 0 && lane * V < E;
+            uint32_t cand = lead ? gm : 0u;
+            uint32_t kept = 0u;
+            for (int i = 0; i < topk_groups; ++i) {
+                const uint32_t m = __reduce_max_sync(kFull, cand);
+                const uint32_t l = __reduce_min_sync(kFull, cand == m ? uint32_t(lane) : 32u);
+                kept |= 1u << l;
+                if (uint32_t(lane) == l) cand = 0u;
+            }
+            if (!((kept >> (lane & ~(lpg - 1))) & 1u)) {
+#pragma unroll
+                for (int v = 0; v < V; ++v) key[v] = 0u;
+            }
+        }
+
+        // k + 1 rounds, each one warp max: round j's key is the j-th largest
+        // (kept in sm[j]); the last round finds the runner-up that the
+        // exactness check needs.  Once every candidate is taken the max is 0
+        // and nothing changes.
+        uint32_t h, r;
+        top2(key, h, r);
+        bool rvalid = true;
+#pragma unroll
+        for (int j = 0; j <= KMAX; ++j) {
+            if (j > k) break;
+            const uint32_t m = __reduce_max_sync(kFull, h);
+            if (lane == 0) sm[j] = m;
+            const bool own = h == m;
+            const bool scan = own && !rvalid;
+            h = own ? r : h;
+            rvalid = rvalid && !own;
+            if (__any_sync(kFull, scan)) {
+                if (scan) {                      // second pop: the best two below m
+                    top2_below(key, m, h, r);
+                    rvalid = true;
+                }
+            }
+        }
+        __syncwarp();
+        const uint32_t mine = lane < k ? sm[lane] : 0u;
+        const uint32_t nkey = sm[lane + 1 <= KMAX ? lane + 1 : KMAX];
+        const uint32_t mk = sm[k - 1], mk1 = sm[k];
+        int ej = lane < k ? 255 - int(mine & 0xFFu) : 0;
+        float fj = 0.0f;
+        if (lane < k) fj = bulk ? srow[ej] : __ldg(grow + ej);
+        // exact order: adjacent winners that share a bucket must be equal
+        const uint32_t vkj = exact_key(fj);
+        const uint32_t nvk = __shfl_down_sync(kFull, vkj, 1);
+        bool bad = lane + 1 < k && (mine >> 8) == (nkey >> 8) && vkj != nvk;
+        // exact set: if the (k+1)-th shares the k-th's bucket, every
+        // candidate of that bucket must hold the same logit
+        if (mk1 != 0u && (mk1 >> 8) == (mk >> 8)) {
+            const uint32_t beta = mk >> 8;
+            uint32_t lo = 0xFFFFFFFFu, hi = 0u;
+#pragma unroll
+            for (int v = 0; v < V; ++v) {
+                if (key[v] != 0u && (key[v] >> 8) == beta) {
+                    const uint32_t x = exact_key(val[v]);
+                    lo = min(lo, x);
+                    hi = max(hi, x);
+                }
+            }
+            if (__reduce_min_sync(kFull, lo) != __reduce_max_sync(kFull, hi)) bad = true;
+        }
+        if (__any_sync(kFull, bad)) {
+            // rank this token again on the exact patterns: largest value,
+            // then the lowest expert id holding it
+            uint32_t taken = 0u;
+            for (int j = 0; j < k; ++j) {
+                uint32_t bk = 0u;
+                int bv = 0;
+#pragma unroll
+                for (int v = 0; v < V; ++v) {
+                    if (key[v] == 0u || ((taken >> v) & 1u)) continue;
+                    const uint32_t x = exact_key(val[v]);
+                    if (x > bk) { bk = x; bv = v; }
+                }
+                const uint32_t m = __reduce_max_sync(kFull, bk);
+                const int e = int(__reduce_min_sync(kFull, bk == m && bk != 0u
+                                                              ? uint32_t(lane * V + bv) : kFull));
+                if (lane == j) { ej = e; fj = exact_key_value(m); }
+                if (e >= 0 && e / V == lane) taken |= 1u << (e % V);
+            }
+        }
+        // softmax over the k chosen scores, stabilised by the largest (slot 0)
+        const float s0 = __shfl_sync(kFull, fj, 0);
+        const float ex = lane < k ? expf(fj - s0) : 0.0f;
+        float total = ex;
+#pragma unroll
+        for (int off = KMAX >= 32 ? 16 : KMAX / 2; off > 0; off >>= 1)
+            total += __shfl_xor_sync(kFull, total, off);
+        if (lane < k) {
+            topk_idx[t * k + lane] = ej;
+            topk_w[t * k + lane] = ex / total;
+            s_idx[tl * k + lane] = ej;
+            atomicOr(&s_mask[ej * W + (tl >> 5)], 1u << (tl & 31));
+        }
+        if (routing_map) {
+            uint8_t* mrow = routing_map + t * E;
+#pragma unroll
+            for (int v = 0; v < V; ++v)
+                if (FULL || lane * V + v < E) mrow[lane * V + v] = 0;
+            __syncwarp();
+            if (lane < k) mrow[ej] = 1;
+        }
+        __syncwarp();                    // sm is rewritten by the next token
+    }
+    __syncthreads();
+    if (bulk && threadIdx.x == 0) {
+        // a chunk whose wait gave up may still be landing: wait for every
+        // chunk (bounded) before the block's shared memory is released
+        for (int c = 0; c < nchunks; ++c) mbar_wait(smem_addr(&bars[c]), 0);
+    }
+    if (s_fail && threadIdx.x == 0 && dev_status) atomicExch(dev_status, uint32_t(MOE_ERR_TIMEOUT));
+    // this block's histogram row: 16-bit counts (at most tpb <= 128 each)
+    const int stride = hist_stride(E);
+    uint16_t* hrow = hist + int64_t(blockIdx.x) * stride;
+    for (int e = threadIdx.x; e < stride; e += kKThreads) {
+        int32_t c = 0;
+        if (e < E)
+            for (int w = 0; w < W; ++w) c += __popc(s_mask[e * W + w]);
+        hrow[e] = uint16_t(c);
+    }
+    for (int i = threadIdx.x; i < nt * k; i += kKThreads) {
+        const int tl = i / k;
+        const int e = s_idx[i];
+        int32_t rank = -1;
+        if (e >= 0 && e < E) {
+            const uint32_t* m = s_mask + e * W;
+            const int q = tl >> 5;
+            rank = __popc(m[q] & ((1u << (tl & 31)) - 1u));
+            for (int w = 0; w < q; ++w) rank += __popc(m[w]);
+        }
+        rank_out[t0 * k + i] = rank;
+    }
+}
+
+// ------------------------------------------------- K1, four threads a token
+// For k <= 8 without group limits.  Thread q of a token keeps a sorted top 8
+// of its NG*8 experts [q*NG*8, (q+1)*NG*8): each group of 8 keys is sorted by
+// a 19-comparator network (Batcher's odd-even merge sort) and merged into the
+// running list (the larger of list[i] and group[7-i] form a bitonic sequence
+// holding the top 8 of both, sorted by a 12-comparator half-cleaner; the
+// smaller ones are the rejects, whose maximum is kept as the best key outside
+// the list).  Two butterfly merges over the token's four lanes leave every
+// lane with the token's top 8 and its ninth key.  No per-round warp
+// reduction: the work is compare-exchanges, with every lane busy.  A token
+// whose truncated keys may not order like the logits (the check of the warp
+// version) is queued and ranked after the main pass by a warp on the exact
+// patterns.
+
+constexpr int kCThreads = 512;                   // 128 tokens x 4 threads
+
+__device__ __forceinline__ void cex(uint32_t& a, uint32_t& b) {   // a >= b afterwards
+    const uint32_t hi = max(a, b);
+    b = min(a, b);
+    a = hi;
+}
+
+__device__ __forceinline__ void sort8_desc(uint32_t (&c)[8]) {
+    cex(c[0], c[1]); cex(c[2], c[3]); cex(c[4], c[5]); cex(c[6], c[7]);
+    cex(c[0], c[2]); cex(c[1], c[3]); cex(c[4], c[6]); cex(c[5], c[7]);
+    cex(c[1], c[2]); cex(c[5], c[6]);
+    cex(c[0], c[4]); cex(c[1], c[5]); cex(c[2], c[6]); cex(c[3], c[7]);
+    cex(c[2], c[4]); cex(c[3], c[5]);
+    cex(c[1], c[2]); cex(c[3], c[4]); cex(c[5], c[6]);
+}
+
+__device__ __forceinline__ void bitonic8_desc(uint32_t (&m)[8]) {
+    cex(m[0], m[4]); cex(m[1], m[5]); cex(m[2], m[6]); cex(m[3], m[7]);
+    cex(m[0], m[2]); cex(m[1], m[3]); cex(m[4], m[6]); cex(m[5], m[7]);
+    cex(m[0], m[1]); cex(m[2], m[3]); cex(m[4], m[5]); cex(m[6], m[7]);
+}
+
+// list <- top 8 of list and c (both sorted descending); ninth <- the largest
+// key that is in neither the new list nor below an earlier ninth.
+__device__ __forceinline__ void merge8(uint32_t (&list)[8], const uint32_t (&c)[8],
+                                       uint32_t& ninth) {
+    uint32_t m[8], rej = 0u;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        m[i] = max(list[i], c[7 - i]);
+        rej = max(rej, min(list[i], c[7 - i]));
+    }
+    ninth = max(ninth, rej);
+    bitonic8_desc(m);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) list[i] = m[i];
+}
+
+template <int NG, bool FULL>   // NG groups of 8 experts per thread; E <= 32*NG
+__global__ void __launch_bounds__(kCThreads, 1)
+route_coop_topk_kernel(const float* __restrict__ logits, int64_t T, int E, int k, int tpb,
+                       bool bulk, int32_t* __restrict__ topk_idx, float* __restrict__ topk_w,
+                       uint8_t* __restrict__ routing_map, uint16_t* __restrict__ hist,
+                       int32_t* __restrict__ rank_out, uint32_t* __restrict__ dev_status) {
+    asm volatile("griddepcontrol.launch_dependents;");
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    __shared__ __align__(8) uint64_t bars[kChunks];
+    __shared__ int s_fail, s_nfb;
+    __shared__ int s_fb[kMaxTokens];                 // tokens left for the exact pass
+    constexpr int V = NG * 8 * 4 / 32;               // experts per lane in the exact pass
+    const int W = (tpb + 31) >> 5;
+    float* s_logits = reinterpret_cast<float*>(smem_raw);          // [tpb*E + 32*V] if bulk
+    uint32_t* s_mask = reinterpret_cast<uint32_t*>(
+        smem_raw + (bulk ? (size_t(tpb) * E + 32 * V) * sizeof(float) : 0));   // [E][W]
+    int32_t* s_idx = reinterpret_cast<int32_t*>(s_mask + size_t(E) * W);        // [tpb*k]
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int tl = threadIdx.x >> 2, q = threadIdx.x & 3;
+    const int64_t t0 = int64_t(blockIdx.x) * tpb;
+    const int nt = int(min64(tpb, T - t0));
+    const int nchunks = (nt + kChunkTokens - 1) / kChunkTokens;
+    if (threadIdx.x == 0) {
+        s_fail = 0;
+        s_nfb = 0;
+        if (bulk) {
+            for (int c = 0; c < nchunks; ++c) mbar_init(smem_addr(&bars[c]), 1);
+            mbar_fence_init();
+        }
+    }
+    for (int i = threadIdx.x; i < E * W; i += kCThreads) s_mask[i] = 0u;
+    for (int i = threadIdx.x; i < nt * k; i += kCThreads) s_idx[i] = -1;
+    __syncthreads();
+    if (bulk && threadIdx.x == 0) {
+        for (int c = 0; c < nchunks; ++c) {
+            const int n = min(kChunkTokens, nt - kChunkTokens * c);
+            const uint32_t bytes = uint32_t(n) * uint32_t(E) * 4u;
+            const uint32_t bar = smem_addr(&bars[c]);
+            mbar_expect_tx(bar, bytes);
+            bulk_load(smem_addr(s_logits + size_t(kChunkTokens * c) * E),
+                      logits + (t0 + kChunkTokens * c) * E, bytes, bar);
+        }
+    }
+
+    // warp w holds tokens 8w .. 8w+7: chunk w
+    const bool active = tl < nt;
+    bool ok = true;
+    if (bulk && warp < nchunks) ok = __all_sync(kFull, mbar_wait(smem_addr(&bars[warp]), 0));
+    if (!ok && lane == 0) s_fail = 1;
+    if (ok && warp * kChunkTokens < nt) {
+        const int64_t t = t0 + (active ? tl : 0);
+        const float* grow = logits + t * E;
+        const float* srow = s_logits + size_t(active ? tl : 0) * E;
+        const int ebase = q * NG * 8;
+        uint32_t list[8], ninth = 0u;
+#pragma unroll
+        for (int g = 0; g < NG; ++g) {
+            // groups taken in an order rotated by q, so the four lanes of a
+            // token read different shared-memory banks
+            const int gg = (g + q) & (NG - 1);
+            const int e0 = ebase + gg * 8;
+            float f[8];
+            if (bulk) {
+                const float4 a = *reinterpret_cast<const float4*>(srow + e0);
+                const float4 b = *reinterpret_cast<const float4*>(srow + e0 + 4);
+                f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+                f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+            } else {
+#pragma unroll
+                for (int v = 0; v < 8; ++v) f[v] = (FULL || e0 + v < E) ? __ldg(grow + e0 + v) : 0.0f;
+            }
+            uint32_t c[8];
+#pragma unroll
+            for (int v = 0; v < 8; ++v) {
+                c[v] = (exact_key(f[v]) & 0xFFFFFF00u) | uint32_t(255 - (e0 + v));
+                if (!FULL && e0 + v >= E) c[v] = 0u;
+            }
+            sort8_desc(c);
+            if (g == 0) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) list[i] = c[i];
+            } else {
+                merge8(list, c, ninth);
+            }
+        }
+#pragma unroll
+        for (int off = 1; off <= 2; off <<= 1) {      // the token's four lanes
+            uint32_t c[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) c[i] = __shfl_xor_sync(kFull, list[i], off);
+            const uint32_t n2 = __shfl_xor_sync(kFull, ninth, off);
+            merge8(list, c, ninth);
+            ninth = max(ninth, n2);
+        }
+        // the k-th key (smallest of the first k), the (k+1)-th (largest of
+        // the rest and the ninth), and this lane's slots 2q, 2q+1 -- as
+        // reductions and masks, so the list stays in registers
+        uint32_t kth = 0xFFFFFFFFu, k1th = ninth, a = 0u, b = 0u;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            kth = i < k ? min(kth, list[i]) : kth;
+            k1th = i >= k ? max(k1th, list[i]) : k1th;
+        }
+#pragma unroll
+        for (int qq = 0; qq < 4; ++qq) {
+            const uint32_t sel = q == qq ? 0xFFFFFFFFu : 0u;
+            a |= list[2 * qq] & sel;
+            b |= list[2 * qq + 1] & sel;
+        }
+        const int j0 = 2 * q, j1 = 2 * q + 1;
+        const int e_a = 255 - int(a & 0xFFu), e_b = 255 - int(b & 0xFFu);
+        float fa = 0.0f, fb = 0.0f;
+        if (active && j0 < k) fa = bulk ? srow[e_a] : __ldg(grow + e_a);
+        if (active && j1 < k) fb = bulk ? srow[e_b] : __ldg(grow + e_b);
+        const uint32_t vka = exact_key(fa), vkb = exact_key(fb);
+        // exact order: adjacent winners that share a bucket must be equal
+        const uint32_t na = __shfl_down_sync(kFull, a, 1), nvka = __shfl_down_sync(kFull, vka, 1);
+        bool bad = (j1 < k && (a >> 8) == (b >> 8) && vka != vkb) ||
+                   (q < 3 && j1 + 1 < k && (b >> 8) == (na >> 8) && vkb != nvka);
+        // exact set: if the (k+1)-th shares the k-th's bucket, every
+        // candidate of that bucket must hold the same logit
+        const bool amb = k1th != 0u && (k1th >> 8) == (kth >> 8);
+        if (__any_sync(kFull, amb)) {
+            uint32_t lo = 0xFFFFFFFFu, hi = 0u;
+            if (amb) {
+                const uint32_t beta = kth >> 8;
+#pragma unroll 8
+                for (int i = 0; i < NG * 8; ++i) {
+                    const int e = ebase + i;
+                    if (!FULL && e >= E) break;
+                    const uint32_t x = exact_key(bulk ? srow[e] : __ldg(grow + e));
+                    const bool in = (x >> 8) == beta;
+                    lo = in ? min(lo, x) : lo;
+                    hi = in ? max(hi, x) : hi;
+                }
+            }
+#pragma unroll
+            for (int off = 1; off <= 2; off <<= 1) {
+                lo = min(lo, __shfl_xor_sync(kFull, lo, off));
+                hi = max(hi, __shfl_xor_sync(kFull, hi, off));
+            }
+            if (amb && lo != hi) bad = true;
+        }
+        // (every lane takes part in both shuffles: no short-circuit)
+        const int bad1 = __shfl_xor_sync(kFull, int(bad), 1);
+        bad = bad || bad1 != 0;
+        const int bad2 = __shfl_xor_sync(kFull, int(bad), 2);
+        bad = bad || bad2 != 0;
+        if (active && bad && q == 0) s_fb[atomicAdd(&s_nfb, 1)] = tl;
+        // softmax over the k chosen scores, stabilised by the largest (slot 0)
+        const float s0 = __shfl_sync(kFull, fa, lane & ~3);
+        const float xa = j0 < k ? expf(fa - s0) : 0.0f;
+        const float xb = j1 < k ? expf(fb - s0) : 0.0f;
+        float total = xa + xb;
+        total += __shfl_xor_sync(kFull, total, 1);
+        total += __shfl_xor_sync(kFull, total, 2);
+        if (active && !bad) {
+            if (j0 < k) {
+                topk_idx[t * k + j0] = e_a;
+                topk_w[t * k + j0] = xa / total;
+                s_idx[tl * k + j0] = e_a;
+                atomicOr(&s_mask[e_a * W + (tl >> 5)], 1u << (tl & 31));
+            }
+            if (j1 < k) {
+                topk_idx[t * k + j1] = e_b;
+                topk_w[t * k + j1] = xb / total;
+                s_idx[tl * k + j1] = e_b;
+                atomicOr(&s_mask[e_b * W + (tl >> 5)], 1u << (tl & 31));
+            }
+        }
+        if (routing_map && active && !bad) {
+            uint8_t* mrow = routing_map + t * E;
+            for (int e = ebase; e < ebase + NG * 8; ++e)
+                if (FULL || e < E) mrow[e] = 0;
+        }
+        __syncwarp();
+        if (routing_map && active && !bad) {
+            uint8_t* mrow = routing_map + t * E;
+            if (j0 < k) mrow[e_a] = 1;
+            if (j1 < k) mrow[e_b] = 1;
+        }
+    }
+    __syncthreads();
+    // the queued tokens, one warp each, ranked on the exact patterns: the
+    // largest value, then the lowest expert id holding it
+    for (int i = warp; i < s_nfb; i += kCThreads / 32) {
+        const int ftl = s_fb[i];
+        const int64_t t = t0 + ftl;
+        const float* grow = logits + t * E;
+        const float* srow = s_logits + size_t(ftl) * E;
+        uint32_t ek[V];
+#pragma unroll
+        for (int v = 0; v < V; ++v) {
+            const int e = lane * V + v;
+            ek[v] = (FULL || e < E) ? exact_key(bulk ? srow[e] : __ldg(grow + e)) : 0u;
+        }
+        uint32_t taken = 0u;
+        int ej = 0;
+        float fj = 0.0f;
+        for (int j = 0; j < k; ++j) {
+            uint32_t bk = 0u;
+            int bv = 0;
+#pragma unroll
+            for (int v = 0; v < V; ++v) {
+                if ((taken >> v) & 1u) continue;
+                if (ek[v] > bk) { bk = ek[v]; bv = v; }
+            }
+            const uint32_t m = __reduce_max_sync(kFull, bk);
+            const int e = int(__reduce_min_sync(kFull, bk == m && bk != 0u
+                                                          ? uint32_t(lane * V + bv) : kFull));
+            if (lane == j) { ej = e; fj = exact_key_value(m); }
+            if (e >= 0 && e / V == lane) taken |= 1u << (e % V);
+        }
+        const float s0 = __shfl_sync(kFull, fj, 0);
+        const float ex = lane < k ? expf(fj - s0) : 0.0f;
+        float total = ex;
+#pragma unroll
+        for (int off = 4; off > 0; off >>= 1) total += __shfl_xor_sync(kFull, total, off);
+        if (lane < k) {
+            topk_idx[t * k + lane] = ej;
+            topk_w[t * k + lane] = ex / total;
+            s_idx[ftl * k + lane] = ej;
+            atomicOr(&s_mask[ej * W + (ftl >> 5)], 1u << (ftl & 31));
+        }
+        if (routing_map) {
+            uint8_t* mrow = routing_map + t * E;
+#pragma unroll
+            for (int v = 0; v < V; ++v)
+                if (FULL || lane * V + v < E) mrow[lane * V + v] = 0;
+            __syncwarp();
+            if (lane < k) mrow[ej] = 1;
+        }
+    }
+    __syncthreads();
+    if (bulk && threadIdx.x == 0)
+        for (int c = 0; c < nchunks; ++c) mbar_wait(smem_addr(&bars[c]), 0);
+    if (s_fail && threadIdx.x == 0 && dev_status) atomicExch(dev_status, uint32_t(MOE_ERR_TIMEOUT));
+    const int stride = hist_stride(E);
+    uint16_t* hrow = hist + int64_t(blockIdx.x) * stride;
+    for (int e = threadIdx.x; e < stride; e += kCThreads) {
+        int32_t c = 0;
+        if (e < E)
+            for (int w = 0; w < W; ++w) c += __popc(s_mask[e * W + w]);
+        hrow[e] = uint16_t(c);
+    }
+    for (int i = threadIdx.x; i < nt * k; i += kCThreads) {
+        const int tk = i / k;
+        const int e = s_idx[i];
+        int32_t rank = -1;
+        if (e >= 0 && e < E) {
+            const uint32_t* m = s_mask + e * W;
+            const int qw = tk >> 5;
+            rank = __popc(m[qw] & ((1u << (tk & 31)) - 1u));
+            for (int w = 0; w < qw; ++w) rank += __popc(m[w]);
+        }
+        rank_out[t0 * k + i] = rank;
+    }
+}
+
+// ------------------------------------------------------- scan (beyond K2's reach)
+// Block x owns experts [32x, 32x+32); thread (g, c) owns expert 32x+c and row
+// group g: pre[b][e] = sum of rows before b (exclusive prefix), pre[G][e] =
+// the total.
+__global__ void __launch_bounds__(1024)
+route_fast_scan_kernel(const uint16_t* __restrict__ hist, int32_t* __restrict__ pre, int64_t G,
+                       int E) {
+    wait_for_predecessor();
+    __shared__ int32_t s_part[32][33];
+    const int stride = hist_stride(E);
+    const int c = threadIdx.x & 31, g = threadIdx.x >> 5;
+    const int e = blockIdx.x * 32 + c;
+    const int64_t rows = (G + 31) / 32;
+    const int64_t b0 = min64(G, g * rows), b1 = min64(G, b0 + rows);
+    int32_t sum = 0;
+    if (e < E)
+        for (int64_t b = b0; b < b1; ++b) sum += hist[b * stride + e];
+    s_part[g][c] = sum;
+    __syncthreads();
+    int32_t run = 0;
+    for (int q = 0; q < g; ++q) run += s_part[q][c];
+    if (e < E) {
+        for (int64_t b = b0; b < b1; ++b) {
+            pre[b * E + e] = run;
+            run += hist[b * stride + e];
+        }
+        if (g == 31) pre[G * E + e] = run;
+    }
+}
+
+// ------------------------------------------------------------------------ K2
+
+// Exclusive scan of s_in[0..n) into s_out[0..n] (s_out[n] = total), n <= 1024;
+// every thread of the block calls it.
+__device__ void scan_experts(const int32_t* s_in, int32_t* s_out, int n) {
+    __shared__ int32_t s_warp[kPThreads / 32];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int32_t v = int(threadIdx.x) < n ? s_in[threadIdx.x] : 0;
+    int32_t incl = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int32_t o = __shfl_up_sync(kFull, incl, off);
+        if (lane >= off) incl += o;
+    }
+    if (lane == 31) s_warp[warp] = incl;
+    __syncthreads();
+    int32_t pre = 0;
+    for (int q = 0; q < warp; ++q) pre += s_warp[q];
+    if (int(threadIdx.x) < n) s_out[threadIdx.x] = pre + incl - v;
+    if (int(threadIdx.x) == n - 1) s_out[n] = pre + incl;
+    if (n == 0 && threadIdx.x == 0) s_out[0] = 0;
+    __syncthreads();
+}
+
+template <bool FUSED>
+__global__ void __launch_bounds__(kPThreads)
+route_fast_place_kernel(const int32_t* __restrict__ topk_idx, const float* __restrict__ topk_w,
+                        int64_t T, int E, int k, int tpb, int64_t G,
+                        const uint16_t* __restrict__ hist, const int32_t* __restrict__ pre,
+                        int32_t* __restrict__ counts,
+                        int32_t* __restrict__ offsets, int32_t* __restrict__ group_list,
+                        int32_t* __restrict__ sorted_indices, int32_t* __restrict__ slot_pos,
+                        float* __restrict__ permuted_probs, WsHeader* __restrict__ header) {
+    wait_for_predecessor();
+    __shared__ __align__(16) uint32_t s_ptot[kPThreads * 4];   // [P][stride/2] packed partial totals
+    __shared__ __align__(16) uint32_t s_pbef[kPThreads * 4];   // [P][stride/2] packed "before"
+    __shared__ int32_t s_tot[kFastMaxExperts];
+    __shared__ int32_t s_bef[kFastMaxExperts];
+    __shared__ int32_t s_off[kFastMaxExperts + 1];
+    const int stride = hist_stride(E);
+    const int64_t b = blockIdx.x;
+    const int64_t t0 = b * tpb;
+    const int nt = int(max64(0, min64(tpb, T - t0)));
+
+    // this block's slots, fetched before the histogram work (at most
+    // tpb*k/kPThreads = 4 per thread)
+    constexpr int kPer = kMaxTokens * kMaxTopK / kPThreads;
+    int32_t se[kPer], sr[kPer];
+    float sw[kPer];
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+        const int i = threadIdx.x + u * kPThreads;
+        se[u] = -1;
+        sr[u] = -1;
+        sw[u] = 0.0f;
+        if (i < nt * k) {
+            se[u] = topk_idx[t0 * k + i];
+            sr[u] = slot_pos[t0 * k + i];
+            sw[u] = topk_w[t0 * k + i];
+        }
+    }
+
+    if (FUSED) {
+        // rows of 16-bit counts: Q 16-byte columns of 8 counts per row, P rows
+        // at a time, up to 8 loads in flight.  Counts are summed as packed
+        // 16-bit pairs (no carry crosses a half: every sum is at most
+        // T <= kFusedMaxBlocks * kMaxTokens = 32768).
+        const int Q = stride >> 3;
+        const int P = kPThreads / Q;
+        const int q = threadIdx.x % Q, p = threadIdx.x / Q;
+        uint4 tot = make_uint4(0, 0, 0, 0), bef = make_uint4(0, 0, 0, 0);
+        if (p < P) {
+            for (int64_t r0 = p; r0 < G; r0 += 8 * int64_t(P)) {
+                uint4 v[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int64_t r = r0 + int64_t(u) * P;
+                    v[u] = r < G ? __ldg(reinterpret_cast<const uint4*>(hist + r * stride) + q)
+                                 : make_uint4(0, 0, 0, 0);
+                }
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int64_t r = r0 + int64_t(u) * P;
+                    tot.x += v[u].x; tot.y += v[u].y; tot.z += v[u].z; tot.w += v[u].w;
+                    if (r < b) {
+                        bef.x += v[u].x; bef.y += v[u].y; bef.z += v[u].z; bef.w += v[u].w;
+                    }
+                }
+            }
+            reinterpret_cast<uint4*>(s_ptot)[p * Q + q] = tot;
+            reinterpret_cast<uint4*>(s_pbef)[p * Q + q] = bef;
+        }
+        __syncthreads();
+        // word w of a row holds experts 2w (low half) and 2w+1 (high half)
+        for (int w = threadIdx.x; w < (E + 1) / 2; w += kPThreads) {
+            uint32_t a = 0u, c = 0u;
+            for (int pp = 0; pp < P; ++pp) {
+                a += s_ptot[pp * (stride / 2) + w];
+                c += s_pbef[pp * (stride / 2) + w];
+            }
+            s_tot[2 * w] = int32_t(a & 0xFFFFu);
+            s_bef[2 * w] = int32_t(c & 0xFFFFu);
+            if (2 * w + 1 < E) {
+                s_tot[2 * w + 1] = int32_t(a >> 16);
+                s_bef[2 * w + 1] = int32_t(c >> 16);
+            }
+        }
+    } else {
+        for (int e = threadIdx.x; e < E; e += kPThreads) {
+            s_bef[e] = b < G ? pre[b * E + e] : 0;
+            s_tot[e] = pre[G * E + e];
+        }
+    }
+    __syncthreads();
+    scan_experts(s_tot, s_off, E);
+    if (b == 0) {
+        for (int e = threadIdx.x; e < E; e += kPThreads) {
+            counts[e] = s_tot[e];
+            offsets[e] = s_off[e];
+            group_list[e] = s_off[e + 1];
+        }
+        if (threadIdx.x == 0) {
+            offsets[E] = s_off[E];
+            header->status = MOE_OK;
+            header->detail = 0;
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+        const int i = threadIdx.x + u * kPThreads;
+        if (i >= nt * k) continue;
+        const int e = se[u];
+        if (e < 0 || e >= E || sr[u] < 0) {          // a token whose logits never arrived
+            slot_pos[t0 * k + i] = -1;
+            continue;
+        }
+        const int32_t pos = s_off[e] + s_bef[e] + sr[u];
+        slot_pos[t0 * k + i] = pos;
+        sorted_indices[pos] = int32_t(t0 + i / k);
+        if (permuted_probs) permuted_probs[pos] = sw[u];
+    }
+}
+
+size_t topk_smem_bytes(int64_t tpb, int E, int k, int V, bool bulk) {
+    const int W = int((tpb + 31) / 32);
+    return (bulk ? (size_t(tpb) * E + 32 * V) * sizeof(float) : 0) +
+           sizeof(uint32_t) * size_t(E) * W + sizeof(int32_t) * size_t(tpb) * k;
+}
+
+template <int V, int KMAX, bool GROUPED, bool FULL>
+moe_status_t launch_topk(const float* logits, int64_t T, int E, int k, int tpb, int64_t G,
+                         bool bulk, int32_t* topk_idx, float* topk_w, uint8_t* routing_map,
+                         uint16_t* hist, int32_t* rank_out, int n_groups, int topk_groups,
+                         cudaStream_t s) {
+    const auto kern = route_fast_topk_kernel<V, KMAX, GROUPED, FULL>;
+    const int max_smem = int(topk_smem_bytes(kMaxTokens, kFastMaxExperts, kMaxTopK, 8, true));
+    if (!opt_in_smem((const void*)kern, max_smem)) return MOE_ERR_CUDA;
+    kern<<<unsigned(G), kKThreads, topk_smem_bytes(tpb, E, k, V, bulk), s>>>(
+        logits, T, E, k, tpb, bulk, topk_idx, topk_w, routing_map, hist, rank_out, n_groups,
+        topk_groups, device_status_word());
+    return launch_status();
+}
+
+template <int V, bool GROUPED, bool FULL>
+moe_status_t launch_topk_k(const float* logits, int64_t T, int E, int k, int tpb, int64_t G,
+                           bool bulk, int32_t* topk_idx, float* topk_w, uint8_t* routing_map,
+                           uint16_t* hist, int32_t* rank_out, int n_groups, int topk_groups,
+                           cudaStream_t s) {
+    return k <= 8
+        ? launch_topk<V, 8, GROUPED, FULL>(logits, T, E, k, tpb, G, bulk, topk_idx, topk_w,
+                                           routing_map, hist, rank_out, n_groups, topk_groups, s)
+        : launch_topk<V, kMaxTopK, GROUPED, FULL>(logits, T, E, k, tpb, G, bulk, topk_idx, topk_w,
+                                                  routing_map, hist, rank_out, n_groups,
+                                                  topk_groups, s);
+}
+
+template <int NG, bool FULL>
+moe_status_t launch_coop(const float* logits, int64_t T, int E, int k, int tpb, int64_t G,
+                         bool bulk, int32_t* topk_idx, float* topk_w, uint8_t* routing_map,
+                         uint16_t* hist, int32_t* rank_out, cudaStream_t s) {
+    const auto kern = route_coop_topk_kernel<NG, FULL>;
+    const int max_smem = int(topk_smem_bytes(kMaxTokens, kFastMaxExperts, kMaxTopK, 8, true));
+    if (!opt_in_smem((const void*)kern, max_smem)) return MOE_ERR_CUDA;
+    constexpr int V = NG * 8 * 4 / 32;
+    kern<<<unsigned(G), kCThreads, topk_smem_bytes(tpb, E, k, V, bulk), s>>>(
+        logits, T, E, k, tpb, bulk, topk_idx, topk_w, routing_map, hist, rank_out,
+        device_status_word());
+    return launch_status();
+}
+
+template <int NG>
+moe_status_t launch_coop_ng(const float* logits, int64_t T, int E, int k, int tpb, int64_t G,
+                            bool bulk, int32_t* topk_idx, float* topk_w, uint8_t* routing_map,
+                            uint16_t* hist, int32_t* rank_out, cudaStream_t s) {
+    return E == 32 * NG
+        ? launch_coop<NG, true>(logits, T, E, k, tpb, G, bulk, topk_idx, topk_w, routing_map,
+                                hist, rank_out, s)
+        : launch_coop<NG, false>(logits, T, E, k, tpb, G, bulk, topk_idx, topk_w, routing_map,
+                                 hist, rank_out, s);
+}
+
+template <int V>
+moe_status_t launch_topk_v(const float* logits, int64_t T, int E, int k, int tpb, int64_t G,
+                           bool bulk, int32_t* topk_idx, float* topk_w, uint8_t* routing_map,
+                           uint16_t* hist, int32_t* rank_out, int n_groups, int topk_groups,
+                           cudaStream_t s) {
+    const bool full = E == 32 * V;
+    if (n_groups > 0)
+        return full ? launch_topk_k<V, true, true>(logits, T, E, k, tpb, G, bulk, topk_idx, topk_w,
+                                                   routing_map, hist, rank_out, n_groups,
+                                                   topk_groups, s)
+                    : launch_topk_k<V, true, false>(logits, T, E, k, tpb, G, bulk, topk_idx,
+                                                    topk_w, routing_map, hist, rank_out, n_groups,
+                                                    topk_groups, s);
+    return full ? launch_topk_k<V, false, true>(logits, T, E, k, tpb, G, bulk, topk_idx, topk_w,
+                                                routing_map, hist, rank_out, 0, 0, s)
+                : launch_topk_k<V, false, false>(logits, T, E, k, tpb, G, bulk, topk_idx, topk_w,
+                                                 routing_map, hist, rank_out, 0, 0, s);
+}
+
+// Workspace after the header: 16-bit histogram rows [G][stride], then (when
+// G can exceed kFusedMaxBlocks) the scan kernel's int32 prefixes [G+1][E].
+size_t counts_bytes(int64_t T, int E) {
+    return align_up(size_t(max_blocks(T)) * size_t(hist_stride(E)) * sizeof(uint16_t), kWsAlign);
+}
+size_t prefix_bytes(int64_t T, int E) {
+    const int64_t g = max_blocks(T);
+    return g > kFusedMaxBlocks ? align_up(size_t(g + 1) * size_t(E) * sizeof(int32_t), kWsAlign)
+                               : 0;
+}
+
+}  // namespace
+
+bool fast_route_supported(int E, int n_groups) {
+    if (E < 1 || E > kFastMaxExperts) return false;
+    if (n_groups > 0) {
+        const int V = values_per_lane(E);
+        const int gsize = E / n_groups;
+        if (gsize % V != 0) return false;
+        const int lpg = gsize / V;
+        if (lpg & (lpg - 1)) return false;
+    }
+    return true;
+}
+
+size_t fast_hist_bytes(int64_t T, int E) { return counts_bytes(T, E) + prefix_bytes(T, E); }
+
+moe_status_t fast_route(const float* logits, int64_t T, int E, int k, int n_groups,
+                        int topk_groups, int32_t* topk_idx, float* topk_w, int32_t* counts,
+                        int32_t* offsets, int32_t* group_list, int32_t* sorted_indices,
+                        int32_t* slot_pos, float* permuted_probs, uint8_t* routing_map,
+                        WsHeader* header, int32_t* scratch, cudaStream_t s) {
+    int sms = sm_count();
+    if (sms > kSizingSms) sms = kSizingSms;
+    const int64_t tpb = T > 0 ? tokens_per_block(T, sms) : kMinTokens;
+    const int64_t G = (T + tpb - 1) / tpb;
+    const bool bulk = E % 4 == 0 && aligned16(logits);
+    uint16_t* hist = reinterpret_cast<uint16_t*>(scratch);
+    int32_t* pre = reinterpret_cast<int32_t*>(reinterpret_cast<char*>(scratch) +
+                                              counts_bytes(T, E));
+    if (G > 0 && n_groups == 0 && k <= 8) {
+        // four threads a token, compare-exchange networks
+        const int NG = values_per_lane(E);      // groups of 8 per thread = logits per lane
+        moe_status_t st;
+        if (NG == 1)
+            st = launch_coop_ng<1>(logits, T, E, k, int(tpb), G, bulk, topk_idx, topk_w,
+                                   routing_map, hist, slot_pos, s);
+        else if (NG == 2)
+            st = launch_coop_ng<2>(logits, T, E, k, int(tpb), G, bulk, topk_idx, topk_w,
+                                   routing_map, hist, slot_pos, s);
+        else if (NG == 4)
+            st = launch_coop_ng<4>(logits, T, E, k, int(tpb), G, bulk, topk_idx, topk_w,
+                                   routing_map, hist, slot_pos, s);
+        else
+            st = launch_coop_ng<8>(logits, T, E, k, int(tpb), G, bulk, topk_idx, topk_w,
+                                   routing_map, hist, slot_pos, s);
+        if (st != MOE_OK) return st;
+    } else if (G > 0) {
+        const int V = values_per_lane(E);
+        const int g = n_groups, kg = topk_groups;
+        moe_status_t st;
+        if (V == 1)
+            st = launch_topk_v<1>(logits, T, E, k, int(tpb), G, bulk, topk_idx, topk_w,
+                                  routing_map, hist, slot_pos, g, kg, s);
+        else if (V == 2)
+            st = launch_topk_v<2>(logits, T, E, k, int(tpb), G, bulk, topk_idx, topk_w,
+                                  routing_map, hist, slot_pos, g, kg, s);
+        else if (V == 4)
+            st = launch_topk_v<4>(logits, T, E, k, int(tpb), G, bulk, topk_idx, topk_w,
+                                  routing_map, hist, slot_pos, g, kg, s);
+        else
+            st = launch_topk_v<8>(logits, T, E, k, int(tpb), G, bulk, topk_idx, topk_w,
+                                  routing_map, hist, slot_pos, g, kg, s);
+        if (st != MOE_OK) return st;
+    }
+    const bool fused = G <= kFusedMaxBlocks;
+    if (!fused && launch_dependent(route_fast_scan_kernel, unsigned((E + 31) / 32), 1024, 0, s,
+                                   (const uint16_t*)hist, pre, G, E) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    const cudaError_t err = fused
+        ? launch_dependent(route_fast_place_kernel<true>, unsigned(G > 0 ? G : 1), kPThreads, 0,
+                           s, (const int32_t*)topk_idx, (const float*)topk_w, T, E, k, int(tpb),
+                           G, (const uint16_t*)hist, (const int32_t*)pre, counts, offsets,
+                           group_list, sorted_indices, slot_pos, permuted_probs, header)
+        : launch_dependent(route_fast_place_kernel<false>, unsigned(G), kPThreads, 0, s,
+                           (const int32_t*)topk_idx, (const float*)topk_w, T, E, k, int(tpb), G,
+                           (const uint16_t*)hist, (const int32_t*)pre, counts, offsets,
+                           group_list, sorted_indices, slot_pos, permuted_probs, header);
+    return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+}  // namespace moe
