@@ -999,6 +999,7 @@ using namespace moe;
 extern "C" moe_status_t moe_combine(const void* expert_out, moe_dtype_t dtype, int64_t T,
                                     int64_t H, int k, int64_t n_rows, const int32_t* slot_pos,
                                     const float* topk_w, void* out, void* stream) {
+    MOE_TRACE(__func__);
     const moe_status_t st = check_common(expert_out, out, dtype, T, H, k, n_rows, slot_pos);
     if (st != MOE_OK) return st;
     if (T == 0 || H == 0) return MOE_OK;
@@ -1060,6 +1061,7 @@ extern "C" moe_status_t moe_combine_backward(const void* grad_out, const void* e
                                              int64_t n_rows, const int32_t* slot_pos,
                                              const float* topk_w, void* grad_expert_out,
                                              float* grad_probs, void* stream) {
+    MOE_TRACE(__func__);
     moe_status_t st = check_common(grad_out, expert_out, dtype, T, H, k, n_rows, slot_pos);
     if (st != MOE_OK) return st;
     if (T == 0) return MOE_OK;

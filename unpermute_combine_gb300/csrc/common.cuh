@@ -3,6 +3,7 @@
 
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
+#include <nvtx3/nvToolsExt.h>
 #include <stdint.h>
 
 #include "moe.h"
@@ -16,6 +17,17 @@ constexpr int kMaxExperts = 1024;
 constexpr size_t kWsAlign = 256;
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// NVTX range around one C-ABI call (named after the entry point), so a
+// profiler's timeline shows which library call launched which kernels.
+// Without a tool attached a push/pop is a check of a null function pointer.
+struct NvtxScope {
+    explicit NvtxScope(const char* name) { nvtxRangePushA(name); }
+    ~NvtxScope() { nvtxRangePop(); }
+    NvtxScope(const NvtxScope&) = delete;
+    NvtxScope& operator=(const NvtxScope&) = delete;
+};
+#define MOE_TRACE(name) ::moe::NvtxScope moe_trace_scope_(name)
 
 inline size_t elem_size(moe_dtype_t d) { return d == MOE_F32 ? 4 : d == MOE_BF16 ? 2 : 1; }
 

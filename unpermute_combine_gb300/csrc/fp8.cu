@@ -276,6 +276,7 @@ using namespace moe;
 
 extern "C" moe_status_t moe_quantize_fp8(const void* x, int64_t T, int64_t H, int block,
                                          void* x_q, float* scales, void* stream) {
+    MOE_TRACE(__func__);
     const moe_status_t st = check_block(T, H, block);
     if (st != MOE_OK) return st;
     if (T == 0 || H == 0) return MOE_OK;
@@ -302,6 +303,7 @@ extern "C" moe_status_t moe_quantize_fp8(const void* x, int64_t T, int64_t H, in
 
 extern "C" moe_status_t moe_dequantize_fp8(const void* x_q, const float* scales, int64_t N,
                                            int64_t H, int block, void* out, void* stream) {
+    MOE_TRACE(__func__);
     const moe_status_t st = check_block(N, H, block);
     if (st != MOE_OK) return st;
     if (N == 0 || H == 0) return MOE_OK;
@@ -330,6 +332,7 @@ extern "C" moe_status_t moe_permute_quantize_fp8(const void* x, int64_t T, int64
                                                  int k, int64_t n_rows,
                                                  const int32_t* slot_pos, void* out_q,
                                                  float* out_scales, void* stream) {
+    MOE_TRACE(__func__);
     const moe_status_t st = check_block(T, H, block);
     if (st != MOE_OK) return st;
     if (k < 1 || k > kMaxTopK || n_rows < 0) return MOE_ERR_INVALID_ARG;

@@ -868,6 +868,7 @@ using namespace moe;
 extern "C" moe_status_t moe_grouped_swiglu_pack(const void* w_up, const void* w_down, int E,
                                                 int64_t H, int64_t I, void* w_up_packed,
                                                 void* w_down_packed, void* stream) {
+    MOE_TRACE(__func__);
     const moe_status_t st = check_shapes(0, E, H, I);
     if (st != MOE_OK) return st;
     if (!w_up || !w_down || !w_up_packed || !w_down_packed) return MOE_ERR_INVALID_ARG;
@@ -898,6 +899,7 @@ extern "C" moe_status_t moe_grouped_swiglu(const void* x, const void* w_up_packe
                                            int64_t N, int E, int64_t H, int64_t I, void* y,
                                            void* workspace, size_t workspace_bytes,
                                            void* stream) {
+    MOE_TRACE(__func__);
     moe_status_t st = check_shapes(N, E, H, I);
     if (st != MOE_OK) return st;
     if (!offsets || (N > 0 && (!x || !w_up_packed || !w_down_packed || !y)))
@@ -936,6 +938,7 @@ extern "C" moe_status_t moe_grouped_swiglu_save(const void* x, const void* w_up_
                                                 int64_t N, int E, int64_t H, int64_t I, void* y,
                                                 void* hidden, void* gate_up, void* workspace,
                                                 size_t workspace_bytes, void* stream) {
+    MOE_TRACE(__func__);
     moe_status_t st = check_shapes(N, E, H, I);
     if (st != MOE_OK) return st;
     if (!offsets || (N > 0 && (!x || !w_up_packed || !w_down_packed || !y || !hidden || !gate_up)))
@@ -970,6 +973,7 @@ extern "C" moe_status_t moe_grouped_swiglu_dgrad(const void* dy, const void* w_u
                                                  int64_t I, void* dgate_up, void* dx,
                                                  void* workspace, size_t workspace_bytes,
                                                  void* stream) {
+    MOE_TRACE(__func__);
     moe_status_t st = check_shapes(N, E, H, I);
     if (st != MOE_OK) return st;
     if (!offsets || (N > 0 && (!dy || !w_up || !w_down || !gate_up || !dgate_up || !dx)))
@@ -1007,6 +1011,7 @@ extern "C" moe_status_t moe_grouped_swiglu_wgrad(const void* x, const void* hidd
                                                  int64_t H, int64_t I, float* dw_up,
                                                  float* dw_down, void* workspace,
                                                  size_t workspace_bytes, void* stream) {
+    MOE_TRACE(__func__);
     moe_status_t st = check_shapes(N, E, H, I);
     if (st != MOE_OK) return st;
     if (!offsets) return MOE_ERR_INVALID_ARG;

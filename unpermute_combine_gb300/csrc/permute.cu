@@ -599,6 +599,7 @@ extern "C" moe_status_t moe_permute_fp8(const void* x_q, const float* scales, in
                                         int64_t H, int block, int k, int64_t n_rows,
                                         const int32_t* slot_pos, void* out_q, float* out_scales,
                                         void* stream) {
+    MOE_TRACE(__func__);
     if (T < 0 || H < 0 || k < 1 || n_rows < 0) return MOE_ERR_INVALID_ARG;
     if (block != 32 && block != 64 && block != 128 && block != 256) return MOE_ERR_UNSUPPORTED;
     if (H % block != 0) return MOE_ERR_INVALID_ARG;
@@ -625,6 +626,7 @@ extern "C" moe_status_t moe_permute_fp8(const void* x_q, const float* scales, in
 extern "C" moe_status_t moe_permute(const void* x, moe_dtype_t dtype, int64_t T, int64_t H, int k,
                                     int64_t n_rows, const int32_t* slot_pos, void* out,
                                     void* stream) {
+    MOE_TRACE(__func__);
     if (!dtype_ok_move(dtype) || T < 0 || H < 0 || k < 1 || n_rows < 0) return MOE_ERR_INVALID_ARG;
     if (k > kMaxTopK || T * int64_t(k) >= (int64_t(1) << 31) || n_rows >= (int64_t(1) << 31))
         return MOE_ERR_UNSUPPORTED;
@@ -663,6 +665,7 @@ extern "C" moe_status_t moe_sort_chunks(const void* in, moe_dtype_t dtype, int64
                                         const int32_t* split_sizes, const int32_t* sorted_idxs,
                                         int C, void* out, void* workspace,
                                         size_t workspace_bytes, void* stream) {
+    MOE_TRACE(__func__);
     if (!dtype_ok_move(dtype) || N < 0 || H < 0 || C < 1) return MOE_ERR_INVALID_ARG;
     if (C > kMaxChunks || N >= (int64_t(1) << 31)) return MOE_ERR_UNSUPPORTED;
     if (!split_sizes || !sorted_idxs) return MOE_ERR_INVALID_ARG;
@@ -730,6 +733,7 @@ extern "C" moe_status_t moe_chunk_idxs(int R, int L, int inverse, int32_t* idxs)
 extern "C" moe_status_t moe_expert_scale(const void* in, moe_dtype_t dtype, int64_t n_rows,
                                          int64_t H, int E, const int32_t* offsets,
                                          const float* scale, void* out, void* stream) {
+    MOE_TRACE(__func__);
     if (!dtype_ok(dtype) || n_rows < 0 || H < 0 || E < 1) return MOE_ERR_INVALID_ARG;
     if (E > kMaxExperts || n_rows >= (int64_t(1) << 31)) return MOE_ERR_UNSUPPORTED;
     if (!offsets || !scale) return MOE_ERR_INVALID_ARG;
@@ -758,6 +762,7 @@ extern "C" moe_status_t moe_expert_scale(const void* in, moe_dtype_t dtype, int6
 extern "C" moe_status_t moe_fill_pad_rows(void* rows, moe_dtype_t dtype, int64_t max_rows,
                                          int64_t H, const int32_t* offsets,
                                          const int32_t* counts, int E, void* stream) {
+    MOE_TRACE(__func__);
     if (!dtype_ok_move(dtype) || max_rows < 0 || H < 0 || E < 1) return MOE_ERR_INVALID_ARG;
     if (E > kMaxExperts) return MOE_ERR_UNSUPPORTED;
     if (!offsets || !counts) return MOE_ERR_INVALID_ARG;

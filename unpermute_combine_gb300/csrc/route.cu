@@ -666,6 +666,7 @@ extern "C" moe_status_t moe_route(const float* logits, int64_t T, int E, int k,
                                   int32_t* offsets, int32_t* group_list, int32_t* sorted_indices,
                                   int32_t* slot_pos, float* permuted_probs, uint8_t* routing_map,
                                   void* workspace, size_t workspace_bytes, void* stream) {
+    MOE_TRACE(__func__);
     return route_from_logits(logits, T, E, k, 0, 0, topk_idx, topk_w, counts, offsets,
                              group_list, sorted_indices, slot_pos, permuted_probs, routing_map,
                              workspace, workspace_bytes, stream);
@@ -678,6 +679,7 @@ extern "C" moe_status_t moe_route_grouped(const float* logits, int64_t T, int E,
                                           int32_t* slot_pos, float* permuted_probs,
                                           uint8_t* routing_map, void* workspace,
                                           size_t workspace_bytes, void* stream) {
+    MOE_TRACE(__func__);
     if (n_groups < 1 || topk_groups < 1 || topk_groups > n_groups || E < 1 || E % n_groups != 0)
         return MOE_ERR_INVALID_ARG;
     if (n_groups > 32) return MOE_ERR_UNSUPPORTED;
@@ -694,6 +696,7 @@ extern "C" moe_status_t moe_route_indices(const int32_t* topk_idx, const float* 
                                           float* permuted_probs, uint8_t* routing_map,
                                           void* workspace, size_t workspace_bytes,
                                           void* stream) {
+    MOE_TRACE(__func__);
     moe_status_t st = validate_sizes(T, E, k);
     if (st != MOE_OK) return st;
     if (!counts || !offsets || !group_list) return MOE_ERR_INVALID_ARG;
@@ -753,6 +756,7 @@ extern "C" moe_status_t moe_route_layout(const int32_t* topk_idx, const float* t
                                          int32_t* group_list, int32_t* sorted_indices,
                                          int32_t* slot_pos, float* permuted_probs,
                                          void* workspace, size_t workspace_bytes, void* stream) {
+    MOE_TRACE(__func__);
     moe_status_t st = validate_sizes(T, E, k);
     if (st != MOE_OK) return st;
     int64_t bound = 0;
@@ -817,6 +821,7 @@ extern "C" moe_status_t moe_route_noalloc(const float* logits, int64_t T, int E,
                                           int32_t* sorted_indices, int32_t* slot_pos,
                                           float* permuted_probs, uint8_t* routing_map,
                                           void* stream) {
+    MOE_TRACE(__func__);
     const moe_status_t st = validate_sizes(T, E, k);
     if (st != MOE_OK) return st;
     if (kWsAlign + route_hist_bytes(T, E) > MOE_ROUTE_NOALLOC_SCRATCH_BYTES)

@@ -151,6 +151,7 @@ using namespace moe;
 extern "C" moe_status_t moe_route_backward(const int32_t* topk_idx, const float* topk_w,
                                            const float* grad_probs, int64_t T, int E, int k,
                                            float* grad_logits, void* stream) {
+    MOE_TRACE(__func__);
     if (T < 0 || E < 1 || k < 1 || k > E) return MOE_ERR_INVALID_ARG;
     if (E > kMaxExperts || k > kMaxTopK || T * int64_t(E) >= (int64_t(1) << 40))
         return MOE_ERR_UNSUPPORTED;

@@ -7,24 +7,28 @@
 // masked_select over the transposed routing map ("token dispatcher +
 // fuse_a2a" §1.1) with its inverse slot_pos.  Two launches:
 //
-//   K1  one block of 32 warps per SM, each block a contiguous run of at most
-//       128 tokens.  The block's logits arrive in shared memory by bulk copy
-//       (four 32-token chunks, one mbarrier each), so every byte the block
-//       needs is in flight from the start.  A warp ranks one token at a time:
-//       lane l holds experts [l*V, l*V + V) as unique 32-bit keys -- the top
-//       24 bits of the order-preserving bit pattern of the logit above the
-//       8-bit complement of the expert id -- so one warp max-reduction names
-//       the round's winner and its owner.  Each lane keeps its best two keys
-//       and rescans only when it is popped a second time.  The truncated
-//       keys order exactly unless two candidates share a 24-bit bucket with
-//       different logits; the k winners and the (k+1)-th are checked for that
-//       and such a token (rare: ~1e-3 of tokens on continuous logits, never
-//       for exact ties) is ranked again on the exact 32-bit patterns.  Then
-//       the fp32 softmax, and for every slot a bit in a per-expert token mask
-//       of the block: an expert's count is the popcount of its mask, a slot's
-//       rank inside the block the popcount of the bits below its token.
-//       Writes topk_idx, topk_w, a histogram row per block and the in-block
-//       rank of every slot (into slot_pos, overwritten by K2).
+//   K1  one block per SM, each a contiguous run of at most 128 tokens.  The
+//       block's logits arrive in shared memory by bulk copy (8-token chunks,
+//       one mbarrier each), so every byte the block needs is in flight from
+//       the start.  Every expert gets a unique 32-bit key: the top 24 bits of
+//       the order-preserving bit pattern of its logit above the 8-bit
+//       complement of its id, so equal keys cannot occur and a larger key is
+//       a larger logit (or an equal one with a lower id) -- except that two
+//       logits in the same 24-bit bucket order by id rather than by value.
+//       The k winners and the (k+1)-th are checked for that, and such a token
+//       (about 1e-3 of tokens on continuous logits, none on exact ties) is
+//       ranked again on the exact 32-bit patterns.
+//         k <= 8, no group limit: four threads a token, each keeping a
+//         sorted top 8 of its quarter of the experts with compare-exchange
+//         networks, merged over the four lanes (route_coop_topk_kernel).
+//         Otherwise: a warp a token, k+1 rounds of one warp max-reduction
+//         each, every lane keeping its best two keys and rescanning only
+//         when popped a second time (route_fast_topk_kernel).
+//       Then the fp32 softmax, and for every slot a bit in a per-expert token
+//       mask of the block: an expert's count is the popcount of its mask, a
+//       slot's rank inside the block the popcount of the bits below its
+//       token.  Writes topk_idx, topk_w, a row of 16-bit counts per block and
+//       the in-block rank of every slot (into slot_pos, overwritten by K2).
 //   K2  (programmatic dependent launch) per block: the per-expert totals and
 //       the sum of the earlier blocks' rows (read straight from the rows for
 //       up to 256 blocks, else from a scan kernel's exclusive prefixes), the

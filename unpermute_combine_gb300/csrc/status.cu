@@ -76,6 +76,7 @@ __global__ void timeout_selftest_kernel(WsHeader* header, uint32_t polls) {
 
 extern "C" moe_status_t moe_selftest_timeout(void* workspace, size_t workspace_bytes,
                                              uint32_t polls, void* stream) {
+    MOE_TRACE(__func__);
     if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & (moe::kWsAlign - 1)) ||
         workspace_bytes < moe::kWsAlign)
         return MOE_ERR_WORKSPACE;
