@@ -858,6 +858,61 @@ def run_vep8(args, rank, world, local_rank):
     }
 
 
+# ------------------------------------------------------------------ route alone
+
+def run_route_only(args, rank, world, local_rank):
+    """moe_route (or moe_route_grouped) alone on a workload's logits: the
+    route's own timing and a small device footprint (logits and the index
+    outputs only) for profiling its kernels."""
+    import torch
+
+    import unpermute_combine_gb300 as moe
+    import workloads as wl
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    d = wl.make(args.workload, T=args.tokens)
+    W = d["workload"]
+    T, E, k = d["logits"].shape[0], W.E, W.k
+    logits = torch.from_numpy(d["logits"]).to(dev)
+    groups = tuple(int(v) for v in args.route_groups.split(":")) if args.route_groups else None
+    stream = torch.cuda.Stream(device=dev)
+
+    def route(out=None):
+        if groups:
+            return moe.moe_route_grouped(logits, k, groups[0], groups[1], out=out, stream=stream)
+        return moe.moe_route(logits, k, out=out, stream=stream)
+
+    with torch.cuda.stream(stream):
+        r = route()
+    for _ in range(args.warmup):
+        route(r)
+    torch.cuda.synchronize(dev)
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    with ClockSampler(local_rank) as clk:
+        torch.cuda.synchronize(dev)
+        for i in range(args.steps):
+            evs[i].record(stream)
+            route(r)
+        evs[args.steps].record(stream)
+        torch.cuda.synchronize(dev)
+    ts = [evs[i].elapsed_time(evs[i + 1]) * 1e3 for i in range(args.steps)]
+    if rank != 0:
+        return None
+    alg = algorithmic_bytes(T, 1, E, k, 2)["route"]
+    us = statistics.median(ts)
+    return {"metric": "moe_route microseconds per call", "value": us, "unit": "us",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32", "data": "synthetic (seeded)",
+            "config": {"workload": f"{args.workload}: T={T} E={E} k={k}, router logits only",
+                       "step": ("moe_route_grouped" if groups else "moe_route") +
+                               ", back to back on one stream (CUDA events around each call)"},
+            "route_us": {"median": us, "min": min(ts), "max": max(ts)},
+            "alg_bytes": alg, "GB_s": alg / us / 1e3, "gpu_launches": 2 * args.steps,
+            "clocks": clk.summary()}
+
+
 # ------------------------------------------------------- stand-in pipelines
 
 def run_stand_in(args, rank, world, local_rank, name):
@@ -1168,6 +1223,9 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-mid-tokens", type=int, default=2048,
                     help="tokens of the stand-in workloads the CPU oracle baseline runs")
+    ap.add_argument("--route-only", action="store_true",
+                    help="time moe_route alone on the workload's logits (small device "
+                         "footprint, for profiling the route kernels)")
     ap.add_argument("--no-extra", action="store_true",
                     help="time only the main step (skip the layer, vep8, mid and tiny "
                          "workloads that follow it by default)")
@@ -1214,7 +1272,9 @@ def main(argv=None):
             import torch.distributed as dist
             torch.cuda.set_device(local_rank)
             dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
-        if args.workload in ("mid", "tiny"):
+        if args.route_only:
+            line = run_route_only(args, rank, world, local_rank)
+        elif args.workload in ("mid", "tiny"):
             line = run_stand_in(args, rank, world, local_rank, args.workload)
             if line is not None:
                 line = {"metric": METRIC, "n_gpus": world, "higher_is_better": True,
@@ -1228,7 +1288,8 @@ def main(argv=None):
                                                                        local_rank)
         plain = (args.workload == WORKLOAD and not (args.fp8 or args.fp8_split or args.layout or
                                                     args.route_groups or args.router_bwd or
-                                                    args.tokens or args.train))
+                                                    args.tokens or args.train or
+                                                    args.route_only))
         if plain and not args.no_extra:
             extra = run_extras(args, rank, world, local_rank)
             if line is not None:
