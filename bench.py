@@ -43,7 +43,15 @@ METRIC = "permute+combine routed-tokens/s and achieved HBM GB/s vs GB300 peak (1
 UNIT = "routed-tokens/s"
 WORKLOAD = "skewed"
 FALLBACK_HBM_GBS = 6800.0
-ROUTE_LAUNCHES = 2       # top-k, scatter (the scan is fused for up to 256 token blocks)
+def route_launches(T, E, k, grouped=False, sms=152):
+    """Kernels one moe_route call launches: a single cooperative kernel when
+    every token block fits on the GPU at once (up to 256 experts, k <= 8, no
+    group limit, T <= sms * 128); otherwise top-k + placement, plus a scan
+    kernel beyond 256 token blocks."""
+    if E <= 256 and k <= 8 and not grouped and 0 < T <= sms * 128:
+        return 1
+    tpb = min(128, max(32, -(-T // sms))) if E <= 256 else 128
+    return 2 + (1 if -(-T // tpb) > 256 else 0)
 
 
 # ------------------------------------------------------------ host-side logic
@@ -594,7 +602,7 @@ def run_ours(args, rank, world, local_rank):
                                       f"pad={lay.get('pad', False)}, alignment="
                                       f"{lay.get('align', 1)}, rows={rows}) + moe_permute + "
                                       "moe_fill_pad_rows", 1)
-    launches = ROUTE_LAUNCHES + (1 + 3 + 1 if layer else 3)   # grouped SwiGLU: reset + 2 GEMMs
+    launches = route_launches(T, E, k, bool(groups)) + (1 + 3 + 1 if layer else 3)   # grouped SwiGLU: reset + 2 GEMMs
     if train:
         launches += 1 + 3 + 3 + 1 + 1     # combine bwd, dgrad, wgrad (reset + 2 each), permute bwd, route bwd
         if lay:
@@ -909,7 +917,8 @@ def run_route_only(args, rank, world, local_rank):
                        "step": ("moe_route_grouped" if groups else "moe_route") +
                                ", back to back on one stream (CUDA events around each call)"},
             "route_us": {"median": us, "min": min(ts), "max": max(ts)},
-            "alg_bytes": alg, "GB_s": alg / us / 1e3, "gpu_launches": 2 * args.steps,
+            "alg_bytes": alg, "GB_s": alg / us / 1e3,
+            "gpu_launches": route_launches(T, E, k, bool(groups)) * args.steps,
             "clocks": clk.summary()}
 
 
@@ -1015,7 +1024,7 @@ def run_stand_in(args, rank, world, local_rank, name):
                      "traffic": None},
         "kernels": kern,
         "permute_combine_routed_tokens_per_s": N / pc,
-        "gpu_launches": (ROUTE_LAUNCHES + 3) * args.steps,
+        "gpu_launches": (route_launches(T, E, k) + 3) * args.steps,
         "clocks": clk.summary(),
         **({} if args.no_cpu_baseline else
            {"cpu_baseline": cpu_baseline_stand_in(name, min(T, args.cpu_mid_tokens))}),

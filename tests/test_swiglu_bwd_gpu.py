@@ -198,19 +198,19 @@ def test_layer_workload_training_path():
     _bf16_close(dgu2_h[rows], dgu64[rows], "dgate_up")
     extra = _dx_extra(dgu2_h[rows], dgu_o[rows], d["w_up"], off, rows)
     _bf16_close(to_host(dx2)[rows], dx64[rows], "dx", extra=extra)
-    # wgrad at sampled coordinates, from the GPU's own activations (a
-    # property of the GPU chain: each element is the sum over the expert's rows)
+    # wgrad at sampled coordinates: the oracle's weight gradient (double sum
+    # over the expert's rows) of the GPU chain's own activations, so only the
+    # wgrad kernel's arithmetic is under test here
     rng = np.random.default_rng(11)
     hid_h, dgu_h = to_host(hid), to_host(dgu)
     for which, got, P, Q, A, B in (("up", to_host(dw_up), x_h, dgu_h, W.H, 2 * W.I),
                                    ("down", to_host(dw_down), hid_h, dy_h, W.I, W.H)):
         coords = [(int(rng.integers(W.E)), int(rng.integers(A)), int(rng.integers(B)))
                   for _ in range(200)]
-        Pf, Qf = _f(P), _f(Q)
-        ref = np.array([(Pf[off[e]:off[e + 1], a] * Qf[off[e]:off[e + 1], b]).sum()
-                        for e, a, b in coords])
+        ref = oracle.swiglu_wgrad_at(which, np.array(coords), off, W.H, W.I, x=x_h, hidden=hid_h,
+                                     dy=dy_h, dgate_up=dgu_h)
         g = np.array([got[e, a, b] for e, a, b in coords], np.float64)
-        bound = _wgrad_bound(Pf, Qf, off, coords)
+        bound = _wgrad_bound(_f(P), _f(Q), off, coords)
         assert (np.abs(g - ref) <= bound).all(), which
 
 

@@ -5,7 +5,8 @@
 // group-limited variant §21), tokens per expert and their prefixes
 // (group_list, §7), and the expert-major, token-ascending sorted_indices of a
 // masked_select over the transposed routing map ("token dispatcher +
-// fuse_a2a" §1.1) with its inverse slot_pos.  Two launches:
+// fuse_a2a" §1.1) with its inverse slot_pos.  K1 then K2, as one
+// cooperative launch when every block fits on the GPU at once:
 //
 //   K1  one block per SM, each a contiguous run of at most 128 tokens.  The
 //       block's logits arrive in shared memory by bulk copy (8-token chunks,
@@ -18,26 +19,32 @@
 //       The k winners and the (k+1)-th are checked for that, and such a token
 //       (about 1e-3 of tokens on continuous logits, none on exact ties) is
 //       ranked again on the exact 32-bit patterns.
-//         k <= 8, no group limit: four threads a token, each keeping a
-//         sorted top 8 of its quarter of the experts with compare-exchange
-//         networks, merged over the four lanes (route_coop_topk_kernel).
+//         k <= 8, no group limit: four (E <= 32) or eight threads a token,
+//         each keeping a sorted top 8 of its share of the experts with
+//         compare-exchange networks, merged over the token's lanes
+//         (route_coop_topk_kernel).
 //         Otherwise: a warp a token, k+1 rounds of one warp max-reduction
 //         each, every lane keeping its best two keys and rescanning only
 //         when popped a second time (route_fast_topk_kernel).
 //       Then the fp32 softmax, and for every slot a bit in a per-expert token
 //       mask of the block: an expert's count is the popcount of its mask, a
 //       slot's rank inside the block the popcount of the bits below its
-//       token.  Writes topk_idx, topk_w, a row of 16-bit counts per block and
-//       the in-block rank of every slot (into slot_pos, overwritten by K2).
-//   K2  (programmatic dependent launch) per block: the per-expert totals and
-//       the sum of the earlier blocks' rows (read straight from the rows for
-//       up to 256 blocks, else from a scan kernel's exclusive prefixes), the
-//       exclusive scan of the totals (offsets), and the final position
-//       offsets[e] + before[e] + rank of every slot.
+//       token.  Writes topk_idx, topk_w and a row of 16-bit counts per block.
+//   K2  per block: the per-expert totals and the sum of the earlier blocks'
+//       rows (read straight from the rows for up to 256 blocks, else from a
+//       scan kernel's exclusive prefixes), the exclusive scan of the totals
+//       (offsets), and the final position offsets[e] + before[e] + rank of
+//       every slot.
+//   Fused (k <= 8, no group limit, every block resident): K2 runs in the
+//       same blocks after a grid barrier, from the masks and ranks still in
+//       shared memory.  Otherwise K1 leaves the in-block ranks in slot_pos
+//       and K2 is a programmatic dependent launch.
 //
 // Position of (t, e) = offsets[e] + #{t' < t : e in topk(t')}: integer
 // arithmetic throughout, so the result is bit-exact and independent of
-// scheduling.  No kernel waits on another block.
+// scheduling.  Only the fused launch waits on other blocks, all of them
+// resident, with a time limit.
+#include <atomic>
 #include <cmath>
 
 #include "pipeline.cuh"
@@ -354,7 +361,162 @@ route_fast_topk_kernel(const float* __restrict__ logits, int64_t T, int E, int k
     }
 }
 
-// ------------------------------------------------- K1, four threads a token
+// Exclusive scan of s_in[0..n) into s_out[0..n] (s_out[n] = total), n <= 1024;
+// every thread of the block calls it.
+__device__ void scan_experts(const int32_t* s_in, int32_t* s_out, int n) {
+    __shared__ int32_t s_warp[32];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int32_t v = int(threadIdx.x) < n ? s_in[threadIdx.x] : 0;
+    int32_t incl = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int32_t o = __shfl_up_sync(kFull, incl, off);
+        if (lane >= off) incl += o;
+    }
+    if (lane == 31) s_warp[warp] = incl;
+    __syncthreads();
+    // the totals of the warps before this one: one load a lane, one add-reduce
+    const int32_t pre = int32_t(__reduce_add_sync(
+        kFull, uint32_t(lane < warp && 32 * lane < n ? s_warp[lane] : 0)));
+    if (int(threadIdx.x) < n) s_out[threadIdx.x] = pre + incl - v;
+    if (int(threadIdx.x) == n - 1) s_out[n] = pre + incl;
+    if (n == 0 && threadIdx.x == 0) s_out[0] = 0;
+    __syncthreads();
+}
+
+// Outputs of the placement, for the fused route.
+struct PlaceOut {
+    int32_t* counts;
+    int32_t* offsets;
+    int32_t* group_list;
+    int32_t* sorted_indices;
+    int32_t* slot_pos;
+    float* permuted_probs;
+    WsHeader* header;
+    uint64_t* flags;            // [G] arrival flags of the grid barrier (workspace)
+    uint64_t epoch;             // this call's flag value (distinct for every call)
+};
+
+// The placement of route_fast_place_kernel inside the fused route, from this
+// block's shared memory: wait until every block has written its count row
+// (a grid barrier; every block is resident, so the wait is only for blocks
+// still ranking, and it gives up after kWaitLimitNs), sum the rows -- all of
+// them for the totals, those before this block for its prefix -- scan the
+// totals into offsets and place this block's slots.
+__device__ void place_from_block(const uint16_t* __restrict__ hist, int E, int k, int tpb,
+                                 int64_t T, const uint32_t* s_mask, int W, const int32_t* s_idx,
+                                 const float* s_w, const PlaceOut& po,
+                                 uint32_t* __restrict__ dev_status) {
+    __shared__ __align__(16) uint32_t s_ptot[kPThreads * 4];   // [P][stride/2] packed partials
+    __shared__ __align__(16) uint32_t s_pbef[kPThreads * 4];
+    __shared__ int32_t s_tot[kFastMaxExperts];
+    __shared__ int32_t s_bef[kFastMaxExperts];
+    __shared__ int32_t s_off[kFastMaxExperts + 1];
+    const int G = int(gridDim.x), b = int(blockIdx.x), nthreads = int(blockDim.x);
+    const int stride = hist_stride(E);
+    const int64_t t0 = int64_t(b) * tpb;
+    const int nt = int(max64(0, min64(tpb, T - t0)));
+    // the grid barrier: each block stores this call's epoch in its own flag,
+    // which releases its count row (written before the __syncthreads below)
+    // at GPU scope, and waits until all G flags hold it.  No flag needs
+    // clearing between calls: a flag left by an earlier call holds that
+    // call's epoch, and the epochs never repeat.
+    __syncthreads();
+    if (threadIdx.x == 0)
+        asm volatile("st.release.gpu.global.u64 [%0], %1;" :: "l"(po.flags + b), "l"(po.epoch)
+                     : "memory");
+    const uint64_t start = global_ns();
+    for (;;) {
+        uint64_t v = po.epoch;
+        if (int(threadIdx.x) < G)
+            asm volatile("ld.acquire.gpu.global.u64 %0, [%1];"
+                         : "=l"(v) : "l"(po.flags + threadIdx.x) : "memory");
+        if (__syncthreads_and(v == po.epoch)) break;
+        const bool late = threadIdx.x == 0 && global_ns() - start > kWaitLimitNs;
+        if (__syncthreads_or(late)) {
+            if (threadIdx.x == 0 && dev_status) atomicExch(dev_status, uint32_t(MOE_ERR_TIMEOUT));
+            return;
+        }
+        __nanosleep(32);
+    }
+    // rows of 16-bit counts, summed as packed pairs (every sum is at most
+    // T <= 152 * kMaxTokens: no carry crosses a half); the rows were written
+    // in this launch, so they are read through L2 (ld.global.cg)
+    const int Q = stride >> 3;
+    const int P = nthreads / Q;
+    const int qc = threadIdx.x % Q, p = threadIdx.x / Q;
+    if (p < P) {
+        uint4 tot = make_uint4(0, 0, 0, 0), bef = make_uint4(0, 0, 0, 0);
+        for (int r0 = p; r0 < G; r0 += 8 * P) {
+            uint4 v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int r = r0 + u * P;
+                v[u] = r < G ? __ldcg(reinterpret_cast<const uint4*>(hist + int64_t(r) * stride) + qc)
+                             : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int r = r0 + u * P;
+                tot.x += v[u].x; tot.y += v[u].y; tot.z += v[u].z; tot.w += v[u].w;
+                if (r < b) {
+                    bef.x += v[u].x; bef.y += v[u].y; bef.z += v[u].z; bef.w += v[u].w;
+                }
+            }
+        }
+        reinterpret_cast<uint4*>(s_ptot)[p * Q + qc] = tot;
+        reinterpret_cast<uint4*>(s_pbef)[p * Q + qc] = bef;
+    }
+    __syncthreads();
+    // word w of a row holds experts 2w (low half) and 2w+1 (high half); one
+    // thread a word adds its P partials (a measured tie with splitting the P
+    // over several lanes, which needs one more block barrier)
+    for (int w = threadIdx.x; w < (E + 1) / 2; w += nthreads) {
+        uint32_t a = 0u, c = 0u;
+        for (int pp = 0; pp < P; ++pp) {
+            a += s_ptot[pp * (stride / 2) + w];
+            c += s_pbef[pp * (stride / 2) + w];
+        }
+        s_tot[2 * w] = int32_t(a & 0xFFFFu);
+        s_bef[2 * w] = int32_t(c & 0xFFFFu);
+        if (2 * w + 1 < E) {
+            s_tot[2 * w + 1] = int32_t(a >> 16);
+            s_bef[2 * w + 1] = int32_t(c >> 16);
+        }
+    }
+    __syncthreads();
+    scan_experts(s_tot, s_off, E);
+    if (b == 0) {
+        for (int e = threadIdx.x; e < E; e += nthreads) {
+            po.counts[e] = s_tot[e];
+            po.offsets[e] = s_off[e];
+            po.group_list[e] = s_off[e + 1];
+        }
+        if (threadIdx.x == 0) {
+            po.offsets[E] = s_off[E];
+            po.header->status = MOE_OK;
+            po.header->detail = 0;
+        }
+    }
+    for (int i = threadIdx.x; i < nt * k; i += nthreads) {
+        const int tk = i / k;
+        const int e = s_idx[i];
+        if (e < 0 || e >= E) {                           // a token whose logits never arrived
+            po.slot_pos[t0 * k + i] = -1;
+            continue;
+        }
+        const uint32_t* m = s_mask + e * W;
+        const int qw = tk >> 5;
+        int32_t rank = __popc(m[qw] & ((1u << (tk & 31)) - 1u));
+        for (int w = 0; w < qw; ++w) rank += __popc(m[w]);
+        const int32_t pos = s_off[e] + s_bef[e] + rank;
+        po.slot_pos[t0 * k + i] = pos;
+        po.sorted_indices[pos] = int32_t(t0 + tk);
+        if (po.permuted_probs) po.permuted_probs[pos] = s_w[i];
+    }
+}
+
+// ------------------------------------------- K1, four or eight threads a token
 // For k <= 8 without group limits.  Thread q of a token keeps a sorted top 8
 // of its NG*8 experts [q*NG*8, (q+1)*NG*8): each group of 8 keys is sorted by
 // a 19-comparator network (Batcher's odd-even merge sort) and merged into the
@@ -368,7 +530,6 @@ route_fast_topk_kernel(const float* __restrict__ logits, int64_t T, int E, int k
 // version) is queued and ranked after the main pass by a warp on the exact
 // patterns.
 
-constexpr int kCThreads = 512;                   // 128 tokens x 4 threads
 
 __device__ __forceinline__ void cex(uint32_t& a, uint32_t& b) {   // a >= b afterwards
     const uint32_t hi = max(a, b);
@@ -407,26 +568,37 @@ __device__ __forceinline__ void merge8(uint32_t (&list)[8], const uint32_t (&c)[
     for (int i = 0; i < 8; ++i) list[i] = m[i];
 }
 
-template <int NG, bool FULL>   // NG groups of 8 experts per thread; E <= 32*NG
-__global__ void __launch_bounds__(kCThreads, 1)
+// FUSED: the whole route in this one launch -- all blocks resident at once
+// (a cooperative launch), a grid barrier after the count rows are written,
+// then the placement of route_fast_place_kernel straight from this block's
+// shared memory (place_from_block below).
+// TPT threads a token (4 or 8), each with NG groups of 8 experts:
+// E <= 8 * NG * TPT.
+template <int NG, int TPT, bool FULL, bool FUSED>
+__global__ void __launch_bounds__(kMaxTokens * TPT, 1)
 route_coop_topk_kernel(const float* __restrict__ logits, int64_t T, int E, int k, int tpb,
                        bool bulk, int32_t* __restrict__ topk_idx, float* __restrict__ topk_w,
                        uint8_t* __restrict__ routing_map, uint16_t* __restrict__ hist,
-                       int32_t* __restrict__ rank_out, uint32_t* __restrict__ dev_status) {
-    asm volatile("griddepcontrol.launch_dependents;");
+                       int32_t* __restrict__ rank_out, uint32_t* __restrict__ dev_status,
+                       PlaceOut po) {
+    if (!FUSED) asm volatile("griddepcontrol.launch_dependents;");
     extern __shared__ __align__(16) unsigned char smem_raw[];
     __shared__ __align__(8) uint64_t bars[kChunks];
     __shared__ int s_fail, s_nfb;
     __shared__ int s_fb[kMaxTokens];                 // tokens left for the exact pass
-    constexpr int V = NG * 8 * 4 / 32;               // experts per lane in the exact pass
+    constexpr int V = NG * 8 * TPT / 32;             // experts per lane in the exact pass
+    constexpr int SPT = 8 / TPT;                     // slots per thread (k <= 8)
+    constexpr int TPW = 32 / TPT;                    // tokens per warp
+    const int nthreads = int(blockDim.x);
     const int W = (tpb + 31) >> 5;
     float* s_logits = reinterpret_cast<float*>(smem_raw);          // [tpb*E + 32*V] if bulk
     uint32_t* s_mask = reinterpret_cast<uint32_t*>(
         smem_raw + (bulk ? (size_t(tpb) * E + 32 * V) * sizeof(float) : 0));   // [E][W]
     int32_t* s_idx = reinterpret_cast<int32_t*>(s_mask + size_t(E) * W);        // [tpb*k]
+    float* s_w = reinterpret_cast<float*>(s_idx + size_t(tpb) * k);              // [tpb*k] if FUSED
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int tl = threadIdx.x >> 2, q = threadIdx.x & 3;
+    const int tl = threadIdx.x / TPT, q = threadIdx.x % TPT;
     const int64_t t0 = int64_t(blockIdx.x) * tpb;
     const int nt = int(min64(tpb, T - t0));
     const int nchunks = (nt + kChunkTokens - 1) / kChunkTokens;
@@ -434,30 +606,31 @@ route_coop_topk_kernel(const float* __restrict__ logits, int64_t T, int E, int k
         s_fail = 0;
         s_nfb = 0;
         if (bulk) {
+            // the logits go out first, before the block's shared-memory set-up
             for (int c = 0; c < nchunks; ++c) mbar_init(smem_addr(&bars[c]), 1);
             mbar_fence_init();
+            for (int c = 0; c < nchunks; ++c) {
+                const int n = min(kChunkTokens, nt - kChunkTokens * c);
+                const uint32_t bytes = uint32_t(n) * uint32_t(E) * 4u;
+                const uint32_t bar = smem_addr(&bars[c]);
+                mbar_expect_tx(bar, bytes);
+                bulk_load(smem_addr(s_logits + size_t(kChunkTokens * c) * E),
+                          logits + (t0 + kChunkTokens * c) * E, bytes, bar);
+            }
         }
     }
-    for (int i = threadIdx.x; i < E * W; i += kCThreads) s_mask[i] = 0u;
-    for (int i = threadIdx.x; i < nt * k; i += kCThreads) s_idx[i] = -1;
+    for (int i = threadIdx.x; i < E * W; i += nthreads) s_mask[i] = 0u;
+    for (int i = threadIdx.x; i < nt * k; i += nthreads) s_idx[i] = -1;
     __syncthreads();
-    if (bulk && threadIdx.x == 0) {
-        for (int c = 0; c < nchunks; ++c) {
-            const int n = min(kChunkTokens, nt - kChunkTokens * c);
-            const uint32_t bytes = uint32_t(n) * uint32_t(E) * 4u;
-            const uint32_t bar = smem_addr(&bars[c]);
-            mbar_expect_tx(bar, bytes);
-            bulk_load(smem_addr(s_logits + size_t(kChunkTokens * c) * E),
-                      logits + (t0 + kChunkTokens * c) * E, bytes, bar);
-        }
-    }
 
-    // warp w holds tokens 8w .. 8w+7: chunk w
+    // warp w holds tokens TPW*w .. TPW*w + TPW - 1, all in one 8-token chunk
     const bool active = tl < nt;
+    const bool warp_live = warp * TPW < nt;
     bool ok = true;
-    if (bulk && warp < nchunks) ok = __all_sync(kFull, mbar_wait(smem_addr(&bars[warp]), 0));
+    if (bulk && warp_live)
+        ok = __all_sync(kFull, mbar_wait(smem_addr(&bars[warp * TPW / kChunkTokens]), 0));
     if (!ok && lane == 0) s_fail = 1;
-    if (ok && warp * kChunkTokens < nt) {
+    if (ok && warp_live) {
         const int64_t t = t0 + (active ? tl : 0);
         const float* grow = logits + t * E;
         const float* srow = s_logits + size_t(active ? tl : 0) * E;
@@ -494,7 +667,7 @@ route_coop_topk_kernel(const float* __restrict__ logits, int64_t T, int E, int k
             }
         }
 #pragma unroll
-        for (int off = 1; off <= 2; off <<= 1) {      // the token's four lanes
+        for (int off = 1; off < TPT; off <<= 1) {     // the token's TPT lanes
             uint32_t c[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) c[i] = __shfl_xor_sync(kFull, list[i], off);
@@ -503,7 +676,7 @@ route_coop_topk_kernel(const float* __restrict__ logits, int64_t T, int E, int k
             ninth = max(ninth, n2);
         }
         // the k-th key (smallest of the first k), the (k+1)-th (largest of
-        // the rest and the ninth), and this lane's slots 2q, 2q+1 -- as
+        // the rest and the ninth), and this lane's slots q*SPT .. -- as
         // reductions and masks, so the list stays in registers
         uint32_t kth = 0xFFFFFFFFu, k1th = ninth, a = 0u, b = 0u;
 #pragma unroll
@@ -512,24 +685,29 @@ route_coop_topk_kernel(const float* __restrict__ logits, int64_t T, int E, int k
             k1th = i >= k ? max(k1th, list[i]) : k1th;
         }
 #pragma unroll
-        for (int qq = 0; qq < 4; ++qq) {
+        for (int qq = 0; qq < TPT; ++qq) {
             const uint32_t sel = q == qq ? 0xFFFFFFFFu : 0u;
-            a |= list[2 * qq] & sel;
-            b |= list[2 * qq + 1] & sel;
+            a |= list[SPT * qq] & sel;
+            if (SPT == 2) b |= list[SPT * qq + 1] & sel;
         }
-        const int j0 = 2 * q, j1 = 2 * q + 1;
-        const int e_a = 255 - int(a & 0xFFu), e_b = 255 - int(b & 0xFFu);
+        const int j0 = SPT * q, j1 = SPT == 2 ? SPT * q + 1 : 8;   // 8: no second slot
+        int e_a = 255 - int(a & 0xFFu);
+        const int e_b = 255 - int(b & 0xFFu);
         float fa = 0.0f, fb = 0.0f;
         if (active && j0 < k) fa = bulk ? srow[e_a] : __ldg(grow + e_a);
         if (active && j1 < k) fb = bulk ? srow[e_b] : __ldg(grow + e_b);
-        const uint32_t vka = exact_key(fa), vkb = exact_key(fb);
+        uint32_t vka = exact_key(fa);
+        const uint32_t vkb = exact_key(fb);
         // exact order: adjacent winners that share a bucket must be equal
         const uint32_t na = __shfl_down_sync(kFull, a, 1), nvka = __shfl_down_sync(kFull, vka, 1);
-        bool bad = (j1 < k && (a >> 8) == (b >> 8) && vka != vkb) ||
-                   (q < 3 && j1 + 1 < k && (b >> 8) == (na >> 8) && vkb != nvka);
+        bool bad_order = SPT == 2
+            ? (j1 < k && (a >> 8) == (b >> 8) && vka != vkb) ||
+              (q < TPT - 1 && j1 + 1 < k && (b >> 8) == (na >> 8) && vkb != nvka)
+            : (q < TPT - 1 && j0 + 1 < k && (a >> 8) == (na >> 8) && vka != nvka);
         // exact set: if the (k+1)-th shares the k-th's bucket, every
         // candidate of that bucket must hold the same logit
         const bool amb = k1th != 0u && (k1th >> 8) == (kth >> 8);
+        bool bad_set = false;
         if (__any_sync(kFull, amb)) {
             uint32_t lo = 0xFFFFFFFFu, hi = 0u;
             if (amb) {
@@ -545,36 +723,68 @@ route_coop_topk_kernel(const float* __restrict__ logits, int64_t T, int E, int k
                 }
             }
 #pragma unroll
-            for (int off = 1; off <= 2; off <<= 1) {
+            for (int off = 1; off < TPT; off <<= 1) {
                 lo = min(lo, __shfl_xor_sync(kFull, lo, off));
                 hi = max(hi, __shfl_xor_sync(kFull, hi, off));
             }
-            if (amb && lo != hi) bad = true;
+            if (amb && lo != hi) bad_set = true;
         }
-        // (every lane takes part in both shuffles: no short-circuit)
-        const int bad1 = __shfl_xor_sync(kFull, int(bad), 1);
-        bad = bad || bad1 != 0;
-        const int bad2 = __shfl_xor_sync(kFull, int(bad), 2);
-        bad = bad || bad2 != 0;
+        // both flags token-wide (every lane takes part in every shuffle: no
+        // short-circuit)
+#pragma unroll
+        for (int off = 1; off < TPT; off <<= 1) {
+            const int o1 = __shfl_xor_sync(kFull, int(bad_order), off);
+            const int o2 = __shfl_xor_sync(kFull, int(bad_set), off);
+            bad_order = bad_order || o1 != 0;
+            bad_set = bad_set || o2 != 0;
+        }
+        const bool any_order_only = __any_sync(kFull, bad_order && !bad_set);
+        if (TPT == 8 && any_order_only) {
+            // the set is right and only the order within a bucket is not:
+            // sort the token's winners (one per lane) on the exact key --
+            // value, then the lower id -- with a bitonic network over its
+            // eight lanes.  A token already in order comes out unchanged.
+            uint64_t key = j0 < k ? (uint64_t(vka) << 32) | uint64_t(0xFFFFFFFFu - uint32_t(e_a))
+                                  : 0ull;
+#pragma unroll
+            for (int size = 2; size <= 8; size <<= 1) {
+#pragma unroll
+                for (int st = size >> 1; st > 0; st >>= 1) {
+                    const uint64_t other = __shfl_xor_sync(kFull, key, st);
+                    const bool take_max = ((q & st) == 0) != ((q & size) != 0);
+                    key = take_max ? (key > other ? key : other) : (key < other ? key : other);
+                }
+            }
+            if (bad_order && !bad_set && j0 < k) {
+                vka = uint32_t(key >> 32);
+                e_a = int(0xFFFFFFFFu - uint32_t(key));
+                fa = exact_key_value(vka);
+            }
+        }
+        const bool bad = bad_set || (TPT != 8 && bad_order);
         if (active && bad && q == 0) s_fb[atomicAdd(&s_nfb, 1)] = tl;
         // softmax over the k chosen scores, stabilised by the largest (slot 0)
-        const float s0 = __shfl_sync(kFull, fa, lane & ~3);
+        const float s0 = __shfl_sync(kFull, fa, lane & ~(TPT - 1));
         const float xa = j0 < k ? expf(fa - s0) : 0.0f;
         const float xb = j1 < k ? expf(fb - s0) : 0.0f;
         float total = xa + xb;
-        total += __shfl_xor_sync(kFull, total, 1);
-        total += __shfl_xor_sync(kFull, total, 2);
+#pragma unroll
+        for (int off = 1; off < TPT; off <<= 1) total += __shfl_xor_sync(kFull, total, off);
         if (active && !bad) {
             if (j0 < k) {
+                const float w = xa / total;
                 topk_idx[t * k + j0] = e_a;
-                topk_w[t * k + j0] = xa / total;
+                topk_w[t * k + j0] = w;
                 s_idx[tl * k + j0] = e_a;
+                if (FUSED) s_w[tl * k + j0] = w;
                 atomicOr(&s_mask[e_a * W + (tl >> 5)], 1u << (tl & 31));
             }
             if (j1 < k) {
+                const float w = xb / total;
                 topk_idx[t * k + j1] = e_b;
-                topk_w[t * k + j1] = xb / total;
+                topk_w[t * k + j1] = w;
                 s_idx[tl * k + j1] = e_b;
+                if (FUSED) s_w[tl * k + j1] = w;
                 atomicOr(&s_mask[e_b * W + (tl >> 5)], 1u << (tl & 31));
             }
         }
@@ -593,7 +803,7 @@ route_coop_topk_kernel(const float* __restrict__ logits, int64_t T, int E, int k
     __syncthreads();
     // the queued tokens, one warp each, ranked on the exact patterns: the
     // largest value, then the lowest expert id holding it
-    for (int i = warp; i < s_nfb; i += kCThreads / 32) {
+    for (int i = warp; i < s_nfb; i += nthreads / 32) {
         const int ftl = s_fb[i];
         const int64_t t = t0 + ftl;
         const float* grow = logits + t * E;
@@ -627,9 +837,11 @@ route_coop_topk_kernel(const float* __restrict__ logits, int64_t T, int E, int k
 #pragma unroll
         for (int off = 4; off > 0; off >>= 1) total += __shfl_xor_sync(kFull, total, off);
         if (lane < k) {
+            const float w = ex / total;
             topk_idx[t * k + lane] = ej;
-            topk_w[t * k + lane] = ex / total;
+            topk_w[t * k + lane] = w;
             s_idx[ftl * k + lane] = ej;
+            if (FUSED) s_w[ftl * k + lane] = w;
             atomicOr(&s_mask[ej * W + (ftl >> 5)], 1u << (ftl & 31));
         }
         if (routing_map) {
@@ -642,28 +854,32 @@ route_coop_topk_kernel(const float* __restrict__ logits, int64_t T, int E, int k
         }
     }
     __syncthreads();
-    if (bulk && threadIdx.x == 0)
+    if (bulk && s_fail && threadIdx.x == 0)          // a chunk that never arrived may still land
         for (int c = 0; c < nchunks; ++c) mbar_wait(smem_addr(&bars[c]), 0);
     if (s_fail && threadIdx.x == 0 && dev_status) atomicExch(dev_status, uint32_t(MOE_ERR_TIMEOUT));
     const int stride = hist_stride(E);
     uint16_t* hrow = hist + int64_t(blockIdx.x) * stride;
-    for (int e = threadIdx.x; e < stride; e += kCThreads) {
+    for (int e = threadIdx.x; e < stride; e += nthreads) {
         int32_t c = 0;
         if (e < E)
             for (int w = 0; w < W; ++w) c += __popc(s_mask[e * W + w]);
         hrow[e] = uint16_t(c);
     }
-    for (int i = threadIdx.x; i < nt * k; i += kCThreads) {
-        const int tk = i / k;
-        const int e = s_idx[i];
-        int32_t rank = -1;
-        if (e >= 0 && e < E) {
-            const uint32_t* m = s_mask + e * W;
-            const int qw = tk >> 5;
-            rank = __popc(m[qw] & ((1u << (tk & 31)) - 1u));
-            for (int w = 0; w < qw; ++w) rank += __popc(m[w]);
+    if constexpr (FUSED) {
+        place_from_block(hist, E, k, tpb, T, s_mask, W, s_idx, s_w, po, dev_status);
+    } else {
+        for (int i = threadIdx.x; i < nt * k; i += nthreads) {
+            const int tk = i / k;
+            const int e = s_idx[i];
+            int32_t rank = -1;
+            if (e >= 0 && e < E) {
+                const uint32_t* m = s_mask + e * W;
+                const int qw = tk >> 5;
+                rank = __popc(m[qw] & ((1u << (tk & 31)) - 1u));
+                for (int w = 0; w < qw; ++w) rank += __popc(m[w]);
+            }
+            rank_out[t0 * k + i] = rank;
         }
-        rank_out[t0 * k + i] = rank;
     }
 }
 
@@ -698,28 +914,6 @@ route_fast_scan_kernel(const uint16_t* __restrict__ hist, int32_t* __restrict__ 
 }
 
 // ------------------------------------------------------------------------ K2
-
-// Exclusive scan of s_in[0..n) into s_out[0..n] (s_out[n] = total), n <= 1024;
-// every thread of the block calls it.
-__device__ void scan_experts(const int32_t* s_in, int32_t* s_out, int n) {
-    __shared__ int32_t s_warp[kPThreads / 32];
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int32_t v = int(threadIdx.x) < n ? s_in[threadIdx.x] : 0;
-    int32_t incl = v;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        const int32_t o = __shfl_up_sync(kFull, incl, off);
-        if (lane >= off) incl += o;
-    }
-    if (lane == 31) s_warp[warp] = incl;
-    __syncthreads();
-    int32_t pre = 0;
-    for (int q = 0; q < warp; ++q) pre += s_warp[q];
-    if (int(threadIdx.x) < n) s_out[threadIdx.x] = pre + incl - v;
-    if (int(threadIdx.x) == n - 1) s_out[n] = pre + incl;
-    if (n == 0 && threadIdx.x == 0) s_out[0] = 0;
-    __syncthreads();
-}
 
 template <bool FUSED>
 __global__ void __launch_bounds__(kPThreads)
@@ -840,10 +1034,11 @@ route_fast_place_kernel(const int32_t* __restrict__ topk_idx, const float* __res
     }
 }
 
+// logits [tpb*E + 32*V] (bulk), masks [E][W], ids [tpb*k], weights [tpb*k]
 size_t topk_smem_bytes(int64_t tpb, int E, int k, int V, bool bulk) {
     const int W = int((tpb + 31) / 32);
     return (bulk ? (size_t(tpb) * E + 32 * V) * sizeof(float) : 0) +
-           sizeof(uint32_t) * size_t(E) * W + sizeof(int32_t) * size_t(tpb) * k;
+           sizeof(uint32_t) * size_t(E) * W + 2 * sizeof(int32_t) * size_t(tpb) * k;
 }
 
 template <int V, int KMAX, bool GROUPED, bool FULL>
@@ -873,29 +1068,80 @@ moe_status_t launch_topk_k(const float* logits, int64_t T, int E, int k, int tpb
                                                   topk_groups, s);
 }
 
-template <int NG, bool FULL>
-moe_status_t launch_coop(const float* logits, int64_t T, int E, int k, int tpb, int64_t G,
-                         bool bulk, int32_t* topk_idx, float* topk_w, uint8_t* routing_map,
-                         uint16_t* hist, int32_t* rank_out, cudaStream_t s) {
-    const auto kern = route_coop_topk_kernel<NG, FULL>;
-    const int max_smem = int(topk_smem_bytes(kMaxTokens, kFastMaxExperts, kMaxTopK, 8, true));
-    if (!opt_in_smem((const void*)kern, max_smem)) return MOE_ERR_CUDA;
-    constexpr int V = NG * 8 * 4 / 32;
-    kern<<<unsigned(G), kCThreads, topk_smem_bytes(tpb, E, k, V, bulk), s>>>(
-        logits, T, E, k, tpb, bulk, topk_idx, topk_w, routing_map, hist, rank_out,
-        device_status_word());
-    return launch_status();
+// A distinct 64-bit flag value for every fused route call in the process:
+// the SplitMix64 output function (Steele, Lea and Flood, "Fast splittable
+// pseudorandom number generators", OOPSLA 2014) of a call counter.  Both of
+// its steps -- the odd Weyl increment and the xor-shift-multiply mix -- are
+// bijections of 64-bit words, so no two calls share a value, and leftover
+// workspace bytes from any other use match one only by a 2^-64 chance.
+uint64_t next_epoch() {
+    static std::atomic<uint64_t> calls{0};
+    uint64_t z = (calls.fetch_add(1, std::memory_order_relaxed) + 1) * 0x9E3779B97F4A7C15ull;
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+    return z ^ (z >> 31);
 }
 
-template <int NG>
-moe_status_t launch_coop_ng(const float* logits, int64_t T, int E, int k, int tpb, int64_t G,
-                            bool bulk, int32_t* topk_idx, float* topk_w, uint8_t* routing_map,
-                            uint16_t* hist, int32_t* rank_out, cudaStream_t s) {
-    return E == 32 * NG
-        ? launch_coop<NG, true>(logits, T, E, k, tpb, G, bulk, topk_idx, topk_w, routing_map,
-                                hist, rank_out, s)
-        : launch_coop<NG, false>(logits, T, E, k, tpb, G, bulk, topk_idx, topk_w, routing_map,
-                                 hist, rank_out, s);
+// The few-threads-a-token top-k (TPT threads a token, NG groups of 8
+// experts each).  When every block can be resident at once the whole route
+// runs in this one cooperative launch (*fused = true); otherwise the kernel
+// leaves count rows and in-block ranks for the place kernel.
+template <int NG, int TPT, bool FULL>
+moe_status_t launch_coop(const float* logits, int64_t T, int E, int k, int tpb, int64_t G,
+                         bool bulk, int32_t* topk_idx, float* topk_w, uint8_t* routing_map,
+                         uint16_t* hist, int32_t* rank_out, const PlaceOut& po, bool* fused,
+                         cudaStream_t s) {
+    constexpr int V = NG * 8 * TPT / 32;
+    constexpr int threads = kMaxTokens * TPT;
+    static_assert(threads <= kPThreads, "place_from_block sizes its arrays for kPThreads");
+    const int max_smem = int(topk_smem_bytes(kMaxTokens, kFastMaxExperts, 8, 8, true));
+    const size_t smem = topk_smem_bytes(tpb, E, k, V, bulk);
+    const auto kfused = route_coop_topk_kernel<NG, TPT, FULL, true>;
+    const auto kplain = route_coop_topk_kernel<NG, TPT, FULL, false>;
+    if (!opt_in_smem((const void*)kfused, max_smem) || !opt_in_smem((const void*)kplain, max_smem))
+        return MOE_ERR_CUDA;
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kfused, threads, smem) !=
+        cudaSuccess)
+        return MOE_ERR_CUDA;
+    uint32_t* dev_status = device_status_word();
+    *fused = G <= int64_t(per_sm) * sm_count() && G <= kFusedMaxBlocks;
+    if (!*fused) {
+        kplain<<<unsigned(G), threads, smem, s>>>(logits, T, E, k, tpb, bulk, topk_idx, topk_w,
+                                                 routing_map, hist, rank_out, dev_status, po);
+        return launch_status();
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(G));
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    PlaceOut pe = po;
+    pe.epoch = next_epoch();
+    return cudaLaunchKernelEx(&cfg, kfused, logits, T, E, k, tpb, bulk, topk_idx, topk_w,
+                              routing_map, hist, rank_out, dev_status, pe) == cudaSuccess
+               ? MOE_OK : MOE_ERR_CUDA;
+}
+
+// E <= 32: four threads a token, one group each; more experts: eight threads
+// a token (twice the resident warps of four, half the chain per thread)
+template <int V>
+moe_status_t launch_coop_v(const float* logits, int64_t T, int E, int k, int tpb, int64_t G,
+                           bool bulk, int32_t* topk_idx, float* topk_w, uint8_t* routing_map,
+                           uint16_t* hist, int32_t* rank_out, const PlaceOut& po, bool* fused,
+                           cudaStream_t s) {
+    constexpr int TPT = V == 1 ? 4 : 8;
+    constexpr int NG = V * 4 / TPT;
+    return E == 32 * V
+        ? launch_coop<NG, TPT, true>(logits, T, E, k, tpb, G, bulk, topk_idx, topk_w,
+                                     routing_map, hist, rank_out, po, fused, s)
+        : launch_coop<NG, TPT, false>(logits, T, E, k, tpb, G, bulk, topk_idx, topk_w,
+                                      routing_map, hist, rank_out, po, fused, s);
 }
 
 template <int V>
@@ -917,8 +1163,11 @@ moe_status_t launch_topk_v(const float* logits, int64_t T, int E, int k, int tpb
                                                  routing_map, hist, rank_out, 0, 0, s);
 }
 
-// Workspace after the header: 16-bit histogram rows [G][stride], then (when
-// G can exceed kFusedMaxBlocks) the scan kernel's int32 prefixes [G+1][E].
+// Workspace after the header: 16-bit histogram rows [G][stride], the fused
+// route's barrier flags [kFusedMaxBlocks] (uint64), then (when G can exceed
+// kFusedMaxBlocks) the scan kernel's int32 prefixes [G+1][E].
+constexpr size_t kFlagsBytes = kFusedMaxBlocks * sizeof(uint64_t);
+static_assert(kFlagsBytes % kWsAlign == 0, "flags keep the prefixes aligned");
 size_t counts_bytes(int64_t T, int E) {
     return align_up(size_t(max_blocks(T)) * size_t(hist_stride(E)) * sizeof(uint16_t), kWsAlign);
 }
@@ -942,7 +1191,9 @@ bool fast_route_supported(int E, int n_groups) {
     return true;
 }
 
-size_t fast_hist_bytes(int64_t T, int E) { return counts_bytes(T, E) + prefix_bytes(T, E); }
+size_t fast_hist_bytes(int64_t T, int E) {
+    return counts_bytes(T, E) + kFlagsBytes + prefix_bytes(T, E);
+}
 
 moe_status_t fast_route(const float* logits, int64_t T, int E, int k, int n_groups,
                         int topk_groups, int32_t* topk_idx, float* topk_w, int32_t* counts,
@@ -955,25 +1206,30 @@ moe_status_t fast_route(const float* logits, int64_t T, int E, int k, int n_grou
     const int64_t G = (T + tpb - 1) / tpb;
     const bool bulk = E % 4 == 0 && aligned16(logits);
     uint16_t* hist = reinterpret_cast<uint16_t*>(scratch);
-    int32_t* pre = reinterpret_cast<int32_t*>(reinterpret_cast<char*>(scratch) +
-                                              counts_bytes(T, E));
+    uint64_t* flags = reinterpret_cast<uint64_t*>(reinterpret_cast<char*>(scratch) +
+                                                  counts_bytes(T, E));
+    int32_t* pre = reinterpret_cast<int32_t*>(reinterpret_cast<char*>(flags) + kFlagsBytes);
     if (G > 0 && n_groups == 0 && k <= 8) {
-        // four threads a token, compare-exchange networks
-        const int NG = values_per_lane(E);      // groups of 8 per thread = logits per lane
+        // a few threads a token, compare-exchange networks; the whole route
+        // in one cooperative launch when every block fits at once
+        const int NG = values_per_lane(E);      // logits per lane of a 32-lane token
+        const PlaceOut po{counts, offsets, group_list, sorted_indices, slot_pos, permuted_probs,
+                          header, flags, 0};
+        bool fused = false;
         moe_status_t st;
         if (NG == 1)
-            st = launch_coop_ng<1>(logits, T, E, k, int(tpb), G, bulk, topk_idx, topk_w,
-                                   routing_map, hist, slot_pos, s);
+            st = launch_coop_v<1>(logits, T, E, k, int(tpb), G, bulk, topk_idx, topk_w,
+                                   routing_map, hist, slot_pos, po, &fused, s);
         else if (NG == 2)
-            st = launch_coop_ng<2>(logits, T, E, k, int(tpb), G, bulk, topk_idx, topk_w,
-                                   routing_map, hist, slot_pos, s);
+            st = launch_coop_v<2>(logits, T, E, k, int(tpb), G, bulk, topk_idx, topk_w,
+                                   routing_map, hist, slot_pos, po, &fused, s);
         else if (NG == 4)
-            st = launch_coop_ng<4>(logits, T, E, k, int(tpb), G, bulk, topk_idx, topk_w,
-                                   routing_map, hist, slot_pos, s);
+            st = launch_coop_v<4>(logits, T, E, k, int(tpb), G, bulk, topk_idx, topk_w,
+                                   routing_map, hist, slot_pos, po, &fused, s);
         else
-            st = launch_coop_ng<8>(logits, T, E, k, int(tpb), G, bulk, topk_idx, topk_w,
-                                   routing_map, hist, slot_pos, s);
-        if (st != MOE_OK) return st;
+            st = launch_coop_v<8>(logits, T, E, k, int(tpb), G, bulk, topk_idx, topk_w,
+                                   routing_map, hist, slot_pos, po, &fused, s);
+        if (st != MOE_OK || fused) return st;
     } else if (G > 0) {
         const int V = values_per_lane(E);
         const int g = n_groups, kg = topk_groups;
