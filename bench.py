@@ -312,6 +312,8 @@ def run_ours(args, rank, world, local_rank):
         xp = torch.empty((rows, H), dtype=torch.bfloat16, device=dev)
         fp8 = bool(args.fp8 or args.fp8_split)
         fp8_fused = fp8 and not args.fp8_split and H * 2 <= 16384
+        # --fp8-gemm: the layer forward feeds the e4m3 slot rows straight to GMM1
+        fp8_gemm = bool(args.fp8_gemm) and fp8_fused and layer and not train and not lay
         if fp8:
             fp8_tok = (torch.empty((T, H), dtype=torch.float8_e4m3fn, device=dev),
                        torch.empty((T, H // 128), dtype=torch.float32, device=dev))
@@ -349,7 +351,8 @@ def run_ours(args, rank, world, local_rank):
         names += ["combine_backward", "swiglu_dgrad", "swiglu_wgrad", "permute_backward",
                   "route_backward"]
     if fp8:
-        names[1:2] = (["permute_quantize_fp8", "dequantize_fp8"] if fp8_fused else
+        names[1:2] = (["permute_quantize_fp8"] if fp8_gemm else
+                      ["permute_quantize_fp8", "dequantize_fp8"] if fp8_fused else
                       ["quantize_fp8", "permute", "dequantize_fp8"])
     router_bwd = bool(args.router_bwd) and not layer
     if router_bwd:
@@ -387,8 +390,9 @@ def run_ours(args, rank, world, local_rank):
                 mark()
                 moe.moe_permute_fp8(fp8_tok[0], fp8_tok[1], rr.slot_pos, out=fp8_rows,
                                     stream=stream)
-            mark()
-            moe.moe_dequantize_fp8(fp8_rows[0], fp8_rows[1], 128, out=xp, stream=stream)
+            if not fp8_gemm:
+                mark()
+                moe.moe_dequantize_fp8(fp8_rows[0], fp8_rows[1], 128, out=xp, stream=stream)
         else:
             moe.moe_permute(xx, rr.slot_pos, out=xp, stream=stream)
         if lay:
@@ -416,8 +420,12 @@ def run_ours(args, rank, world, local_rank):
             mark()
             moe.moe_route_backward(r.topk_idx, r.topk_w, o_gp, E, out=gl, stream=stream)
         elif layer:
-            moe.moe_grouped_swiglu(xp, up_p, down_p, rr.offsets, out=y, workspace=gs_ws,
-                                   stream=stream)
+            if fp8_gemm:
+                moe.moe_grouped_swiglu_fp8(fp8_rows[0], fp8_rows[1], up_p, down_p, rr.offsets,
+                                           out=y, workspace=gs_ws, stream=stream)
+            else:
+                moe.moe_grouped_swiglu(xp, up_p, down_p, rr.offsets, out=y, workspace=gs_ws,
+                                       stream=stream)
             mark()
             moe.moe_combine(y, rr.slot_pos, r.topk_w, out=o_out, stream=stream)
         else:
@@ -537,6 +545,8 @@ def run_ours(args, rank, world, local_rank):
         alg["route_backward"] = T * E * 4 + T * k * 12
     if fp8:
         alg.update(fp8_bytes(T, H, k))
+        if fp8_gemm:     # GMM1 reads e4m3 codes and their scales instead of bf16 rows
+            alg["grouped_swiglu"] += N * H + N * (H // 128) * 4 - N * H * 2
     if router_bwd:
         alg["route_backward"] = T * E * 4 + T * k * 12
     if lay:
@@ -591,7 +601,13 @@ def run_ours(args, rank, world, local_rank):
                                                        f"{groups[1]} kept)", 1)
     if router_bwd:
         step_desc += " + moe_route_backward"
-    if fp8:
+    if fp8_gemm:
+        step_desc = step_desc.replace(
+            "moe_permute + moe_grouped_swiglu",
+            "moe_permute_quantize_fp8(block 128: bf16 rows -> e4m3 rows + scale rows in the "
+            "slots) + moe_grouped_swiglu_fp8(GMM1 from the e4m3 rows)", 1)
+        workload = workload.replace("full MoE layer forward", "MoE layer forward with FP8 dispatch")
+    elif fp8:
         step_desc = step_desc.replace(
             "moe_permute", ("moe_permute_quantize_fp8(block 128: bf16 rows -> e4m3 rows + scale "
                             "rows in the slots) + moe_dequantize_fp8") if fp8_fused else
@@ -607,7 +623,7 @@ def run_ours(args, rank, world, local_rank):
         launches += 1 + 3 + 3 + 1 + 1     # combine bwd, dgrad, wgrad (reset + 2 each), permute bwd, route bwd
         if lay:
             launches += 1                 # pad rows of the expert-output gradient
-    if fp8:
+    if fp8 and not fp8_gemm:
         launches += 1 if fp8_fused else 2   # (quantize,) dequantize
     if router_bwd:
         launches += 1
@@ -1252,6 +1268,9 @@ def main(argv=None):
     ap.add_argument("--fp8", action="store_true",
                     help="FP8 dispatch: quantize into the slot rows (one fused launch), "
                          "dequantize")
+    ap.add_argument("--fp8-gemm", action="store_true",
+                    help="with --workload layer --fp8: GMM1 reads the e4m3 slot rows and block "
+                         "scales itself (moe_grouped_swiglu_fp8) instead of a dequantize pass")
     ap.add_argument("--fp8-split", action="store_true",
                     help="FP8 dispatch as separate quantize and e4m3 permute launches")
     ap.add_argument("--layout", default=None, metavar="SPEC",

@@ -332,6 +332,23 @@ moe_status_t moe_grouped_swiglu(const void* x, const void* w_up_packed,
                                 int64_t N, int E, int64_t H, int64_t I, void* y,
                                 void* workspace, size_t workspace_bytes, void* stream);
 
+/* moe_grouped_swiglu_fp8: moe_grouped_swiglu with the activations in FP8
+ * dispatch form ([COMBINE] §3: e4m3 rows with per-block scales, as
+ * moe_permute_quantize_fp8 leaves them): x_q [N,H] e4m3 codes and scales
+ * [N, H/128] float (block = 128).  GMM1 reads the codes and converts each
+ * stage in shared memory to bf16(code * scale), the exact product rounded
+ * once -- the values moe_dequantize_fp8 would write -- so y and hidden are
+ * bit for bit those of moe_grouped_swiglu on moe_dequantize_fp8(x_q,
+ * scales), with no dequantized copy in memory.  H a multiple of 512 (the
+ * scale rows are read by TMA, 16 bytes at a time; else MOE_ERR_UNSUPPORTED),
+ * x_q and scales 16-byte aligned (else MOE_ERR_INVALID_ARG); weights,
+ * offsets, y, the other shapes and workspace as moe_grouped_swiglu. */
+moe_status_t moe_grouped_swiglu_fp8(const void* x_q, const float* scales,
+                                    const void* w_up_packed, const void* w_down_packed,
+                                    const int32_t* offsets, int64_t N, int E, int64_t H,
+                                    int64_t I, void* y, void* workspace, size_t workspace_bytes,
+                                    void* stream);
+
 /* ------------------------------------------- grouped SwiGLU, training path
  * [MOE-OPS] §22 (GMM2 backward -> SwiGLU backward -> GMM1 backward, giving
  * dX, dW1 and dW2, with d_gate and d_up from hidden = silu(gate) * up) and

@@ -157,3 +157,19 @@ def test_permute_quantize_fp8_validates_before_launch(lib):
     assert lib.moe_permute_quantize_fp8(P(0x1008), 4, 256, 128, 2, 8, f, f, f, None) == 1
     assert lib.moe_permute_quantize_fp8(f, 4, 256, 128, 2, 8, f, P(0x1008), f, None) == 1
     assert lib.moe_permute_quantize_fp8(f, 0, 256, 128, 2, 8, None, None, None, None) == 0
+
+
+def test_grouped_swiglu_fp8_validates_before_launch(lib):
+    """Shapes the FP8 expert FFN cannot take are refused on the host."""
+    P = ctypes.c_void_p
+    f = P(0x1000)                                      # never dereferenced
+    ws = P(0x2000)
+    big = ctypes.c_size_t(1 << 40)
+    call = lib.moe_grouped_swiglu_fp8
+    assert call(f, f, f, f, f, 64, 4, 256, 128, f, ws, big, None) == 2   # H not a multiple of 512
+    assert call(f, f, f, f, f, 64, 4, 512, 100, f, ws, big, None) == 2   # I not a multiple of 128
+    assert call(f, f, f, f, f, 64, 0, 512, 128, f, ws, big, None) == 1   # no experts
+    assert call(f, None, f, f, f, 64, 4, 512, 128, f, ws, big, None) == 1
+    assert call(f, f, f, f, f, 64, 4, 512, 128, f, None, big, None) == 3
+    assert call(f, f, f, f, f, 64, 4, 512, 128, f, ws, 16, None) == 3
+    assert call(f, P(0x1004), f, f, f, 64, 4, 512, 128, f, ws, big, None) == 1   # scales unaligned

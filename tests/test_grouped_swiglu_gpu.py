@@ -129,3 +129,70 @@ def test_grouped_swiglu_e1_is_a_dense_ffn():
     h = (torch.nn.functional.silu(gu[:, :I]) * gu[:, I:]).bfloat16().float()
     ref = (h @ to_dev(down).float()[0]).double().cpu().numpy()
     assert _rel_frob(to_host(y), ref) <= TOL
+
+
+def _dequant_oracle(q_dev, sc_dev):
+    q = q_dev.view(torch.uint8).cpu().numpy()
+    return oracle.dequantize_fp8(q, sc_dev.cpu().numpy(), 128)
+
+
+@pytest.mark.parametrize("counts,H,I", [([128], 512, 128),
+                                        ([130, 0, 300], 512, 128),    # ragged, an empty expert
+                                        ([1, 255, 0, 0, 77], 1024, 256),
+                                        ([0, 0, 64], 512, 384)])
+def test_grouped_swiglu_fp8_is_the_bf16_path_on_dequantized_rows(counts, H, I):
+    """GMM1 from e4m3 codes and block scales: bit for bit moe_grouped_swiglu
+    on moe_dequantize_fp8's rows, and within the bar of the oracle fed the
+    oracle's dequantized rows."""
+    E = len(counts)
+    N = sum(counts)
+    offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    rng = np.random.default_rng(3 * N + H + I)
+    # rows of mixed magnitude, so the block scales differ along a row
+    x32 = rng.standard_normal((N, H)).astype(np.float32)
+    x32 *= np.exp2(rng.integers(-6, 7, size=(N, H // 128))).repeat(128, axis=1).astype(np.float32)
+    x = wl.f32_to_bf16_bits(x32)
+    up, down = _weights(N + 2 * E, E, H, I)
+    up_p, down_p = moe.moe_grouped_swiglu_pack(to_dev(up), to_dev(down))
+    q, sc = moe.moe_quantize_fp8(to_dev(x), 128)
+    off = to_dev(offsets)
+    sentinel = torch.full((N + 3, H), 5.0, dtype=torch.bfloat16, device="cuda")
+    y8 = moe.moe_grouped_swiglu_fp8(q, sc, up_p, down_p, off, out=sentinel[:N] if N else None)
+    yd = moe.moe_grouped_swiglu(moe.moe_dequantize_fp8(q, sc, 128), up_p, down_p, off)
+    torch.cuda.synchronize()
+    assert moe.moe_workspace_status(y8._moe_workspace) == 0
+    assert (to_host(y8) == to_host(yd)).all()
+    assert (to_host(sentinel[N:]) == wl.f32_to_bf16_bits(np.full((3, H), 5.0, np.float32))).all()
+    if N:
+        xd_o = _dequant_oracle(q, sc)
+        y_o, y64 = oracle.grouped_swiglu(xd_o, up, down, offsets)
+        assert _rel_frob(to_host(y8), y64) <= TOL
+
+
+def test_grouped_swiglu_fp8_layer_workload():
+    """Full-size layer workload with FP8 dispatch: GPU route -> fused
+    quantize-into-slots -> grouped SwiGLU from the e4m3 rows -> combine; the
+    expert outputs equal the bf16 path on the dequantized rows bit for bit,
+    and sampled tokens match the oracle on the oracle's dequantized rows."""
+    d = wl.make("layer", with_weights=True)
+    W = d["workload"]
+    r = moe.moe_route(to_dev(d["logits"]), W.k)
+    q, sc = moe.moe_permute_quantize_fp8(to_dev(d["x"]), r.slot_pos, 128)
+    up_p, down_p = moe.moe_grouped_swiglu_pack(to_dev(d["w_up"]), to_dev(d["w_down"]))
+    y8 = moe.moe_grouped_swiglu_fp8(q, sc, up_p, down_p, r.offsets)
+    yd = moe.moe_grouped_swiglu(moe.moe_dequantize_fp8(q, sc, 128), up_p, down_p, r.offsets)
+    out = moe.moe_combine(y8, r.slot_pos, r.topk_w)
+    torch.cuda.synchronize()
+    assert moe.moe_workspace_status(y8._moe_workspace) == 0
+    assert (to_host(y8) == to_host(yd)).all()
+
+    o = oracle.route(d["logits"], W.k)
+    rng = np.random.default_rng(78)
+    toks = np.sort(rng.choice(W.T, 16, replace=False))
+    rows = o["slot_pos"][toks].ravel()
+    xd_o = _dequant_oracle(q, sc)
+    y_o, y64 = oracle.grouped_swiglu(xd_o, d["w_up"], d["w_down"], o["offsets"], rows=rows)
+    assert _rel_frob(to_host(y8)[rows], y64[rows]) <= TOL
+    sp_local = np.arange(rows.size, dtype=np.int32).reshape(toks.size, W.k)
+    out_o, out64 = oracle.combine(np.ascontiguousarray(y_o[rows]), sp_local, o["topk_w"][toks])
+    assert _rel_frob(to_host(out)[toks], out64) <= TOL

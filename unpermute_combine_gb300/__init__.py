@@ -25,7 +25,8 @@ __all__ = [
     "moe_sort_chunks_workspace_size", "moe_sort_chunks", "moe_chunk_idxs", "moe_combine",
     "moe_combine_backward", "moe_expert_scale", "moe_workspace_status", "RouteResult",
     "moe_route_noalloc", "MOE_ROUTE_NOALLOC_SCRATCH_BYTES", "moe_grouped_swiglu_pack",
-    "moe_grouped_swiglu_workspace_size", "moe_grouped_swiglu", "moe_device_status",
+    "moe_grouped_swiglu_workspace_size", "moe_grouped_swiglu", "moe_grouped_swiglu_fp8",
+    "moe_device_status",
     "moe_route_grouped", "moe_expert_capacity", "moe_route_layout_rows", "moe_route_layout",
     "moe_fill_pad_rows", "moe_quantize_fp8", "moe_dequantize_fp8", "moe_permute_fp8",
     "moe_route_backward", "moe_grouped_swiglu_save", "moe_grouped_swiglu_dgrad",
@@ -103,6 +104,7 @@ def load_library():
             "moe_grouped_swiglu_pack": ([P, P, I, I64, I64, P, P, P], I),
             "moe_grouped_swiglu_workspace_size": ([I64, I, I64, I64, PSZ], I),
             "moe_grouped_swiglu": ([P, P, P, P, I64, I, I64, I64, P, P, SZ, P], I),
+            "moe_grouped_swiglu_fp8": ([P, P, P, P, P, I64, I, I64, I64, P, P, SZ, P], I),
             "moe_grouped_swiglu_save": ([P, P, P, P, I64, I, I64, I64, P, P, P, P, SZ, P], I),
             "moe_grouped_swiglu_dgrad": ([P, P, P, P, P, I64, I, I64, I64, P, P, P, SZ, P], I),
             "moe_grouped_swiglu_wgrad": ([P, P, P, P, P, I64, I, I64, I64, P, P, P, SZ, P], I),
@@ -659,6 +661,34 @@ def moe_grouped_swiglu(x: torch.Tensor, w_up_packed: torch.Tensor, w_down_packed
     _ok("moe_grouped_swiglu", load_library().moe_grouped_swiglu(
         _p(x), _p(w_up_packed), _p(w_down_packed), _p(offsets), N, E, H, I, _p(out), _p(ws),
         ws.numel(), _stream(stream)))
+    out._moe_workspace = ws
+    return out
+
+
+def moe_grouped_swiglu_fp8(x_q: torch.Tensor, scales: torch.Tensor, w_up_packed: torch.Tensor,
+                           w_down_packed: torch.Tensor, offsets: torch.Tensor,
+                           out: Optional[torch.Tensor] = None,
+                           workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """moe_grouped_swiglu on e4m3 rows x_q [N,H] (float8_e4m3fn) and their
+    per-128-column scales [N, H/128] float32; returns y [N,H] bf16."""
+    _cuda(x_q, "x_q", torch.float8_e4m3fn, 2)
+    _cuda(scales, "scales", torch.float32, 2)
+    _cuda(w_up_packed, "w_up_packed", torch.bfloat16, 3)
+    _cuda(w_down_packed, "w_down_packed", torch.bfloat16, 3)
+    _cuda(offsets, "offsets", torch.int32, 1)
+    N, H = x_q.shape
+    E, I2, H2 = w_up_packed.shape
+    I = I2 // 2
+    if H2 != H or tuple(w_down_packed.shape) != (E, H, I) or offsets.numel() != E + 1:
+        raise ValueError("packed weights / offsets do not match x_q")
+    if H % 128 or tuple(scales.shape) != (N, H // 128):
+        raise ValueError("scales must be [N, H/128] (block = 128)")
+    if out is None:
+        out = torch.empty((N, H), dtype=torch.bfloat16, device=x_q.device)
+    ws = _workspace(moe_grouped_swiglu_workspace_size(N, E, H, I), x_q, workspace)
+    _ok("moe_grouped_swiglu_fp8", load_library().moe_grouped_swiglu_fp8(
+        _p(x_q), _p(scales), _p(w_up_packed), _p(w_down_packed), _p(offsets), N, E, H, I,
+        _p(out), _p(ws), ws.numel(), _stream(stream)))
     out._moe_workspace = ws
     return out
 

@@ -3,6 +3,7 @@
 
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <nvtx3/nvToolsExt.h>
 #include <stdint.h>
 
@@ -92,6 +93,15 @@ __device__ __forceinline__ uint16_t f64_to_bf16_rn(double v) {
 }
 
 __device__ __forceinline__ float f64_to_f32_rn(double v) { return __double2float_rn(v); }
+
+// Two e4m3 codes (low byte first) -> their exact float values
+// (cvt.rn.f16x2.e4m3x2 is exact: every e4m3 value is an f16 value).
+__device__ __forceinline__ void e4m3x2_to_f32(uint32_t v, float& a, float& b) {
+    uint32_t h2;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(uint16_t(v)));
+    a = __half2float(__ushort_as_half(uint16_t(h2 & 0xFFFFu)));
+    b = __half2float(__ushort_as_half(uint16_t(h2 >> 16)));
+}
 
 // bf16 of the exact product a*b.  p = fl(a*b) is within half a float ulp of
 // it, so p rounds like the exact product unless p sits exactly on a bf16

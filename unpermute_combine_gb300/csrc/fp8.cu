@@ -36,14 +36,7 @@ __device__ __forceinline__ uint32_t e4m3x2(float a, float b) {
     return r;
 }
 
-// two e4m3 bytes (low byte first) -> two floats (exact)
-__device__ __forceinline__ void e4m3x2_to_f32(uint32_t v, float& a, float& b) {
-    uint32_t h2;
-    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(uint16_t(v)));
-    a = __half2float(__ushort_as_half(uint16_t(h2 & 0xFFFFu)));
-    b = __half2float(__ushort_as_half(uint16_t(h2 >> 16)));
-}
-
+// four floats -> four e4m3 bytes of f / s
 __device__ __forceinline__ uint32_t q4(const float* f, float s) {
     return e4m3x2(__fdiv_rn(f[0], s), __fdiv_rn(f[1], s)) |
            (e4m3x2(__fdiv_rn(f[2], s), __fdiv_rn(f[3], s)) << 16);

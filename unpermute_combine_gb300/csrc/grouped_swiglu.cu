@@ -36,11 +36,19 @@ constexpr int BN = 256;             // columns per tile (TMEM columns)
 constexpr int BK = 64;              // K per stage: one 128-byte swizzle row
 constexpr int kStages = 4;
 constexpr int kThreads = 256;
+constexpr int kConvWarps = 8;       // converter warps of the e4m3-A kernel (2 a row)
+constexpr int kThreadsA8 = kThreads + 32 * kConvWarps;
+constexpr int kConvPerRow = 32 * kConvWarps / 128;   // threads sharing one A row
 constexpr int kTileABytes = BM * BK * 2;      // 16 KB
 constexpr int kTileBBytes = BN * BK * 2;      // 32 KB
 constexpr int kStageBytes = kTileABytes + kTileBBytes;
 constexpr int kSmemBytes = kStages * kStageBytes + 1024;  // + alignment slack
 constexpr int kTmemCols = 2 * BN;              // double-buffered accumulator
+constexpr int kTileA8Bytes = BM * BK;          // 8 KB of e4m3 A codes
+constexpr int kA8Offset = kTileABytes - kTileA8Bytes;   // where they land in the A slot
+constexpr int kScaleBox = 4;                   // scale columns per TMA box (16 bytes)
+constexpr int kScaleBytes = BM * kScaleBox * 4;           // a stage's scale box: 2 KB
+constexpr int kSmemBytesA8 = kSmemBytes + kStages * kScaleBytes;
 
 // ------------------------------------------------------------- PTX helpers
 
@@ -113,6 +121,71 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// Or-reduction of `v` over the `nthreads` threads (whole warps) that meet at
+// named barrier `id`; every one of them gets the result.
+__device__ __forceinline__ bool bar_red_or(int id, int nthreads, bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n .reg .pred p, q;\n setp.ne.u32 q, %1, 0;\n"
+        " bar.red.or.pred p, %2, %3, q;\n selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(r) : "r"(uint32_t(v)), "r"(id), "r"(nthreads) : "memory");
+    return r != 0;
+}
+
+// The float value of the e4m3 code in byte k of w by integer arithmetic (the
+// hardware conversions through f16 measured about 2 codes per SM cycle,
+// several times slower than the tensor cores consume them): the code moved
+// to the top byte and shifted right by 4 (arithmetic) leaves the sign in bit
+// 31 and exponent:mantissa in bits 26..20; adding (127 - 7) << 23 rebiases a
+// normal code's exponent.  Selects take an exponent field of 0 (subnormal:
+// 2^-6 (1 + m/8) - 2^-6, exact; a zero keeps its sign) and the NaN codes.
+template <int K>
+__device__ __forceinline__ float e4m3_to_f32(uint32_t w) {
+    const uint32_t t = __byte_perm(w, 0u, (K << 12) | 0x0444);
+    const uint32_t a = uint32_t(int32_t(t) >> 4) & 0x87F00000u;
+    const uint32_t sign = t & 0x80000000u;
+    const float f = (t & 0x78000000u) ? __uint_as_float(a + (120u << 23))
+                                      : __fsub_rn(__uint_as_float(a + (121u << 23)),
+                                                  __uint_as_float(sign | (121u << 23)));
+    const float z = (t & 0x7F000000u) ? f : __uint_as_float(sign);
+    return (t & 0x7F000000u) == 0x7F000000u ? __uint_as_float(0x7FC00000u) : z;
+}
+
+// bf16 pairs (lo, hi) of bf16(code * sc) for the four e4m3 codes of w, each
+// the exact product rounded once to nearest even, with no branch (branches
+// here measured several times slower): the four products in packed float
+// multiplies, their rounding errors in packed FMAs; a product whose float
+// value lies exactly on a bf16 rounding midpoint while the exact product does
+// not -- 2% of products, as the block scales amax/448 share 1/7's repeating
+// bits -- moves one float ulp toward the exact product, so the packed
+// conversion rounds as the exact product would (mul_bf16_rn's rule).
+__device__ __forceinline__ uint32_t nudge_off_midpoint(float p, float e) {
+    const uint32_t u = __float_as_uint(p);
+    const bool tie = (u & 0xFFFFu) == 0x8000u && e != 0.0f;
+    const uint32_t toward = ((__float_as_uint(e) ^ u) >> 31) ? 0xFFFFFFFFu : 1u;   // -1 or +1
+    return u + (tie ? toward : 0u);
+}
+
+__device__ __forceinline__ void e4m3x4_scaled_bf16(uint32_t w, float sc, uint32_t& lo,
+                                                   uint32_t& hi) {
+    const float f0 = e4m3_to_f32<0>(w), f1 = e4m3_to_f32<1>(w);
+    const float f2 = e4m3_to_f32<2>(w), f3 = e4m3_to_f32<3>(w);
+    float p0, p1, p2, p3, e0, e1, e2, e3;
+    asm("{\n .reg .b64 x, y, s, p, q, np, nq, r, t;\n mov.b64 x, {%8, %9};\n"
+        " mov.b64 y, {%10, %11};\n mov.b64 s, {%12, %12};\n"
+        " mul.rn.f32x2 p, x, s;\n mul.rn.f32x2 q, y, s;\n"
+        " xor.b64 np, p, 0x8000000080000000;\n xor.b64 nq, q, 0x8000000080000000;\n"
+        " fma.rn.f32x2 r, x, s, np;\n fma.rn.f32x2 t, y, s, nq;\n"
+        " mov.b64 {%0, %1}, p;\n mov.b64 {%2, %3}, q;\n"
+        " mov.b64 {%4, %5}, r;\n mov.b64 {%6, %7}, t;\n}"
+        : "=f"(p0), "=f"(p1), "=f"(p2), "=f"(p3), "=f"(e0), "=f"(e1), "=f"(e2), "=f"(e3)
+        : "f"(f0), "f"(f1), "f"(f2), "f"(f3), "f"(sc));
+    lo = pack_bf16x2_rn(__uint_as_float(nudge_off_midpoint(p0, e0)),
+                        __uint_as_float(nudge_off_midpoint(p1, e1)));
+    hi = pack_bf16x2_rn(__uint_as_float(nudge_off_midpoint(p2, e2)),
+                        __uint_as_float(nudge_off_midpoint(p3, e3)));
+}
+
 // ------------------------------------------------------------- tile schedule
 
 // Tile t -> (expert e, m tile m, n tile n).  s_tile_start[e] = first tile of
@@ -152,6 +225,7 @@ struct GemmArgs {
     const uint16_t* gate_up;    // kSwigluBwd: stored [N_rows, 2I] bf16
     uint16_t* aux_out;          // kSwigluSave: gate_up [N_rows, 2I]
     WsHeader* header;
+    const float* a_scales;      // e4m3 A operand: one scale per 128 columns, [N_rows, K/128]
 };
 
 // 32 floats -> 4 x 16-byte bf16 stores
@@ -179,13 +253,23 @@ __device__ __forceinline__ void unpack_bf16x32(const uint4* s, float* a) {
     }
 }
 
-template <int EPI>
-__global__ void __launch_bounds__(kThreads, 1)
+// A8: the A operand is e4m3 codes with per-128-column scales (map_a over
+// the codes, map_s over the scales).  TMA brings a stage's 128 x 64 codes
+// into the upper half of its A slot and the scale columns around its block
+// into a small ring; kConvWarps converter warps (kConvPerRow threads an A
+// row) read them, meet at a named barrier (the bf16 rows they write overlap
+// the codes), write bf16(code * scale) -- the exact product rounded once, as
+// moe_dequantize_fp8 -- in the 128-byte-swizzled layout the MMA reads, and
+// release the stage to the MMA issuer on conv_bar.
+template <int EPI, bool A8 = false>
+__global__ void __launch_bounds__(A8 ? kThreadsA8 : kThreads, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
-                    const __grid_constant__ CUtensorMap map_b, GemmArgs args) {
+                    const __grid_constant__ CUtensorMap map_b, GemmArgs args,
+                    const __grid_constant__ CUtensorMap map_s) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t full_bar[kStages];
     __shared__ __align__(8) uint64_t empty_bar[kStages];
+    __shared__ __align__(8) uint64_t conv_bar[kStages];
     __shared__ __align__(8) uint64_t tmem_full_bar[2];
     __shared__ __align__(8) uint64_t tmem_empty_bar[2];
     __shared__ uint32_t s_tmem_base;
@@ -197,6 +281,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
 
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
+    float* s_scale = reinterpret_cast<float*>(smem + kStages * kStageBytes);   // A8: [stage][BM][4]
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int E = args.E;
 
@@ -239,6 +324,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
         for (int s = 0; s < kStages; ++s) {
             mbar_init(smem_addr(&full_bar[s]), 1);
             mbar_init(smem_addr(&empty_bar[s]), 1);
+            mbar_init(smem_addr(&conv_bar[s]), kConvWarps);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_addr(&tmem_full_bar[b]), 1);
@@ -274,9 +360,12 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                 const uint32_t a_dst = smem_addr(smem + s * kStageBytes);
                 const uint32_t b_dst = a_dst + kTileABytes;
                 const uint32_t fb = smem_addr(&full_bar[s]);
-                mbar_expect_tx(fb, kStageBytes);
-                tma_load_2d(a_dst, &map_a, ks * BK, row_a, fb);
+                mbar_expect_tx(fb, A8 ? kTileA8Bytes + kTileBBytes + kScaleBytes : kStageBytes);
+                tma_load_2d(A8 ? a_dst + kA8Offset : a_dst, &map_a, ks * BK, row_a, fb);
                 tma_load_2d(b_dst, &map_b, ks * BK, row_b, fb);
+                if (A8)   // the 4 scale columns around this stage's block (x a multiple of 4)
+                    tma_load_2d(smem_addr(s_scale + s * BM * kScaleBox), &map_s,
+                                ((ks * BK) / 128) & ~(kScaleBox - 1), row_a, fb);
             }
         }
     } else if (warp == 1 && lane == 0) {
@@ -290,7 +379,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
             for (int ks = 0; ks < k_steps; ++ks, ++it) {
                 const int s = it % kStages;
                 const uint32_t ph = (it / kStages) & 1u;
-                if (!mbar_wait(smem_addr(&full_bar[s]), ph)) { s_failed = 1; break; }
+                // (A8: the converters waited for the TMA of this stage)
+                if (!mbar_wait(smem_addr(A8 ? &conv_bar[s] : &full_bar[s]), ph)) {
+                    s_failed = 1;
+                    break;
+                }
                 tc_fence_after();
                 const uint32_t a_base = smem_addr(smem + s * kStageBytes);
                 const uint32_t b_base = a_base + kTileABytes;
@@ -305,7 +398,57 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
             if (s_failed) break;
             mma_commit(smem_addr(&tmem_full_bar[buf]));   // the tile's accumulator is ready
         }
-    } else if (warp >= 4) {
+    } else if (A8 && warp >= 8) {
+        // ------------------------------------------------------ e4m3 -> bf16
+        // kConvPerRow threads a row: thread (r, part) converts columns
+        // [part, part + 1) * BK / kConvPerRow of A row r
+        const int ct = int(threadIdx.x) - kThreads;
+        const int r = ct / kConvPerRow, part = ct % kConvPerRow;
+        constexpr int kCodes = BK / kConvPerRow;          // codes a thread converts
+        constexpr int kVecs = kCodes / 16;                // 16-byte code vectors
+        constexpr int kChunks = kCodes / 8;               // 16-byte bf16 chunks
+        uint32_t it = 0;
+        bool stop = false;
+        for (int t = blockIdx.x; t < total_tiles && !stop; t += gridDim.x) {
+            for (int ks = 0; ks < k_steps; ++ks, ++it) {
+                const int s = it % kStages;
+                const uint32_t ph = (it / kStages) & 1u;
+                const bool ok = mbar_wait(smem_addr(&full_bar[s]), ph);
+                uint8_t* slot = smem + s * kStageBytes;
+                uint4 q[kVecs];
+                float sc = 0.0f;
+                if (ok) {
+                    const uint4* src =
+                        reinterpret_cast<const uint4*>(slot + kA8Offset + r * BK + part * kCodes);
+#pragma unroll
+                    for (int v = 0; v < kVecs; ++v) q[v] = src[v];
+                    sc = s_scale[(s * BM + r) * kScaleBox + (((ks * BK) / 128) & (kScaleBox - 1))];
+                }
+                // every converter has its codes before any bf16 row is
+                // written over them; a failure anywhere stops all of them
+                stop = bar_red_or(1, 32 * kConvWarps, !ok || s_failed);
+                if (stop) break;
+                uint8_t* row = slot + r * (BK * 2);
+#pragma unroll
+                for (int c = 0; c < kChunks; ++c) {       // chunk: 8 columns, 2 code words
+                    const uint4 v = q[c >> 1];
+                    const uint32_t w0 = (c & 1) ? v.z : v.x, w1 = (c & 1) ? v.w : v.y;
+                    uint32_t o0, o1, o2, o3;
+                    e4m3x4_scaled_bf16(w0, sc, o0, o1);
+                    e4m3x4_scaled_bf16(w1, sc, o2, o3);
+                    // 128-byte swizzle: chunk j of row r sits at chunk j ^ (r % 8)
+                    const int j = part * kChunks + c;
+                    *reinterpret_cast<uint4*>(row + ((j ^ (r & 7)) << 4)) = make_uint4(o0, o1, o2, o3);
+                }
+                // each thread orders its own writes before the tensor core's
+                // reads; the warp's lane 0 then arrives for all 32
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_addr(&conv_bar[s]));
+            }
+        }
+        if (stop) s_failed = 1;
+    } else if (warp >= 4 && warp < 8) {
         // ------------------------------------------------------ epilogue
         const int q = warp - 4;                           // TMEM lane quadrant
         const uint32_t lane_base = uint32_t(q * 32) << 16;
@@ -816,6 +959,36 @@ bool make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, in
            CUDA_SUCCESS;
 }
 
+// 2D map over row-major e4m3 codes [rows, cols] (one byte each), box
+// [box_rows, 64 codes], no swizzle (the converter warps place the bf16 rows);
+// reads past the last row return zeros.
+bool make_map_u8(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {cuuint64_t(cols), cuuint64_t(rows)};
+    const cuuint64_t strides[1] = {cuuint64_t(cols)};
+    const cuuint32_t box[2] = {cuuint32_t(BK), cuuint32_t(box_rows)};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+}
+
+// 2D fp32 map over the block scales [rows, cols] of e4m3 rows, box
+// [box rows BM, kScaleBox columns] (cols * 4 bytes must be a multiple of 16).
+bool make_map_scales(CUtensorMap* map, const float* base, int64_t rows, int64_t cols) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {cuuint64_t(cols), cuuint64_t(rows)};
+    const cuuint64_t strides[1] = {cuuint64_t(cols) * 4};
+    const cuuint32_t box[2] = {cuuint32_t(kScaleBox), cuuint32_t(BM)};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(base), dims, strides,
+              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+              CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // 2D fp32 map over the row-major [rows, cols] weight-gradient output, box
 // 32 x 32 with the 128-byte swizzle of the epilogue's staging tiles.
 bool make_out_map(CUtensorMap* map, float* base, int64_t rows, int64_t cols) {
@@ -838,6 +1011,7 @@ bool smem_attrs_set() {
                              (const void*)grouped_gemm_kernel<kSwigluBwd>};
     for (const void* k : kernels)
         if (!opt_in_smem(k, kSmemBytes)) return false;
+    if (!opt_in_smem((const void*)grouped_gemm_kernel<kSwiglu, true>, kSmemBytesA8)) return false;
     return opt_in_smem((const void*)grouped_wgrad_kernel, kWgradSmemBytes);
 }
 
@@ -926,10 +1100,53 @@ extern "C" moe_status_t moe_grouped_swiglu(const void* x, const void* w_up_packe
     if (!smem_attrs_set()) return MOE_ERR_CUDA;
     const int grid = sm_count();
     GemmArgs a1{offsets, N, E, int(H), int(I / 128), 2 * I, hidden, I, I, I, nullptr, nullptr, header};
-    grouped_gemm_kernel<kSwiglu><<<grid, kThreads, kSmemBytes, s>>>(m_x, m_up, a1);
+    grouped_gemm_kernel<kSwiglu><<<grid, kThreads, kSmemBytes, s>>>(m_x, m_up, a1, m_x);
     if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
     GemmArgs a2{offsets, N, E, int(I), int(H / BN), H, y, H, H, I, nullptr, nullptr, header};
-    grouped_gemm_kernel<kPlain><<<grid, kThreads, kSmemBytes, s>>>(m_h, m_down, a2);
+    grouped_gemm_kernel<kPlain><<<grid, kThreads, kSmemBytes, s>>>(m_h, m_down, a2, m_h);
+    return launch_status();
+}
+
+extern "C" moe_status_t moe_grouped_swiglu_fp8(const void* x_q, const float* scales,
+                                               const void* w_up_packed, const void* w_down_packed,
+                                               const int32_t* offsets, int64_t N, int E,
+                                               int64_t H, int64_t I, void* y, void* workspace,
+                                               size_t workspace_bytes, void* stream) {
+    MOE_TRACE(__func__);
+    moe_status_t st = check_shapes(N, E, H, I);
+    if (st != MOE_OK) return st;
+    if (H % 512 != 0) return MOE_ERR_UNSUPPORTED;        // scale rows of a multiple of 16 bytes
+    if (!offsets || (N > 0 && (!x_q || !scales || !w_up_packed || !w_down_packed || !y)))
+        return MOE_ERR_INVALID_ARG;
+    size_t need = 0;
+    moe_grouped_swiglu_workspace_size(N, E, H, I, &need);
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & (kWsAlign - 1)) ||
+        workspace_bytes < need)
+        return MOE_ERR_WORKSPACE;
+    if (!aligned16(x_q) || !aligned16(scales) ||
+        !aligned16(w_up_packed) || !aligned16(w_down_packed) || !aligned16(y))
+        return MOE_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    WsHeader* header = static_cast<WsHeader*>(workspace);
+    reset_status_kernel<<<1, 1, 0, s>>>(header);
+    if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
+    if (N == 0) return MOE_OK;
+    void* hidden = static_cast<char*>(workspace) + kWsAlign;
+
+    CUtensorMap m_x, m_up, m_h, m_down, m_s;
+    if (!make_map_u8(&m_x, x_q, N, H, BM) || !make_map_scales(&m_s, scales, N, H / 128) ||
+        !make_map(&m_up, w_up_packed, int64_t(E) * 2 * I, H, BN) ||
+        !make_map(&m_h, hidden, N, I, BM) || !make_map(&m_down, w_down_packed, int64_t(E) * H, I, BN))
+        return MOE_ERR_CUDA;
+
+    if (!smem_attrs_set()) return MOE_ERR_CUDA;
+    const int grid = sm_count();
+    GemmArgs a1{offsets, N, E, int(H), int(I / 128), 2 * I, hidden, I, I, I, nullptr, nullptr,
+                header, scales};
+    grouped_gemm_kernel<kSwiglu, true><<<grid, kThreadsA8, kSmemBytesA8, s>>>(m_x, m_up, a1, m_s);
+    if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
+    GemmArgs a2{offsets, N, E, int(I), int(H / BN), H, y, H, H, I, nullptr, nullptr, header};
+    grouped_gemm_kernel<kPlain><<<grid, kThreads, kSmemBytes, s>>>(m_h, m_down, a2, m_h);
     return launch_status();
 }
 
@@ -960,10 +1177,10 @@ extern "C" moe_status_t moe_grouped_swiglu_save(const void* x, const void* w_up_
     const int grid = sm_count();
     GemmArgs a1{offsets, N, E, int(H), int(I / 128), 2 * I, hidden, I, I, I, nullptr,
                 static_cast<uint16_t*>(gate_up), header};
-    grouped_gemm_kernel<kSwigluSave><<<grid, kThreads, kSmemBytes, s>>>(m_x, m_up, a1);
+    grouped_gemm_kernel<kSwigluSave><<<grid, kThreads, kSmemBytes, s>>>(m_x, m_up, a1, m_x);
     if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
     GemmArgs a2{offsets, N, E, int(I), int(H / BN), H, y, H, H, I, nullptr, nullptr, header};
-    grouped_gemm_kernel<kPlain><<<grid, kThreads, kSmemBytes, s>>>(m_h, m_down, a2);
+    grouped_gemm_kernel<kPlain><<<grid, kThreads, kSmemBytes, s>>>(m_h, m_down, a2, m_h);
     return launch_status();
 }
 
@@ -997,11 +1214,11 @@ extern "C" moe_status_t moe_grouped_swiglu_dgrad(const void* dy, const void* w_u
     // already K-major for this product), [d_gate | d_up] into dgate_up
     GemmArgs d2{offsets, N, E, int(H), int((I + BN - 1) / BN), I, dgate_up, 2 * I, I, I,
                 static_cast<const uint16_t*>(gate_up), nullptr, header};
-    grouped_gemm_kernel<kSwigluBwd><<<grid, kThreads, kSmemBytes, s>>>(m_dy, m_wd, d2);
+    grouped_gemm_kernel<kSwigluBwd><<<grid, kThreads, kSmemBytes, s>>>(m_dy, m_wd, d2, m_dy);
     if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
     // GMM1 backward: dx = dgate_up @ w_up[e]^T (w_up [E,H,2I] is K-major here)
     GemmArgs d1{offsets, N, E, int(2 * I), int(H / BN), H, dx, H, H, I, nullptr, nullptr, header};
-    grouped_gemm_kernel<kPlain><<<grid, kThreads, kSmemBytes, s>>>(m_dgu, m_wu, d1);
+    grouped_gemm_kernel<kPlain><<<grid, kThreads, kSmemBytes, s>>>(m_dgu, m_wu, d1, m_dgu);
     return launch_status();
 }
 

@@ -2,8 +2,7 @@
 // per-device SM count used to size persistent grids, and the one-time
 // dynamic shared-memory opt-in of the kernels that need more than 48 KB.
 #include <mutex>
-#include <set>
-#include <tuple>
+#include <map>
 
 #include "pipeline.cuh"
 
@@ -31,14 +30,18 @@ bool opt_in_smem(const void* kernel, int bytes) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return false;
     static std::mutex m;
-    static std::set<std::tuple<int, const void*, int>> done;
+    // the largest limit set so far per (device, kernel): the attribute is
+    // only ever raised, so a call with a smaller row size can never lower it
+    // under a size an earlier call still launches with
+    static std::map<std::pair<int, const void*>, int> limit;
     std::lock_guard<std::mutex> lock(m);
-    const auto key = std::make_tuple(dev, kernel, bytes);
-    if (done.count(key)) return true;
+    const auto key = std::make_pair(dev, kernel);
+    const auto it = limit.find(key);
+    if (it != limit.end() && it->second >= bytes) return true;
     if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) !=
         cudaSuccess)
         return false;
-    done.insert(key);
+    limit[key] = bytes;
     return true;
 }
 
