@@ -206,3 +206,21 @@ def test_permute_quantize_fp8_skips_slots_outside_the_rows():
                 exp_s[p] = sc_o[t]
     assert (_fp8_host(oq) == exp_q).all()
     assert (to_host(osc).view(np.uint32) == exp_s.view(np.uint32)).all()
+
+
+def test_shared_memory_limit_only_grows():
+    """A kernel's dynamic shared-memory limit is raised for the largest row it
+    has seen and never lowered: a wide call, a narrow call, then the wide one
+    again must all launch (a narrower call once lowered the limit under the
+    wide call's stage size, and the third launch failed)."""
+    T, k, E, block = 64, 2, 8, 128
+    idx, w = wl.random_routing(7, T, E, k)
+    r = moe.moe_route_indices(to_dev(idx), to_dev(w), E)
+    for H in (2048, 512, 2048):
+        x = _tricky_rows(H + 1, T, H)
+        oq, osc = moe.moe_permute_quantize_fp8(to_dev(x), r.slot_pos, block)
+        torch.cuda.synchronize()
+        q_o, sc_o = oracle.quantize_fp8(x, block)
+        si = oracle.route_indices(idx, w, E)["sorted_indices"]
+        assert (_fp8_host(oq) == q_o[si]).all()
+        assert (to_host(osc).view(np.uint32) == sc_o[si].view(np.uint32)).all()
