@@ -148,7 +148,7 @@ moe_status_t moe_route_indices(const int32_t* topk_idx, const float* topk_w,
  * MOE_ROUTE_NOALLOC_SCRATCH_BYTES inside the library, which every GPU that
  * loads the library keeps until the process exits.
  *  - Problems needing more than that (moe_route_workspace_size(T, E, k) >
- *    MOE_ROUTE_NOALLOC_SCRATCH_BYTES; e.g. T = 16384, E = 256 needs 771 KB,
+ *    MOE_ROUTE_NOALLOC_SCRATCH_BYTES; e.g. T = 16384, E = 256 needs 772 KB,
  *    and at E = 256 the limit is about 87,000 tokens) return
  *    MOE_ERR_UNSUPPORTED before anything runs.
  *  - It allocates nothing: no cudaMalloc, no cudaFree, no allocating library

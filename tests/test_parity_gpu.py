@@ -66,6 +66,34 @@ def test_route_full_workloads(name):
     assert moe.moe_workspace_status(r.workspace) == 0
 
 
+def test_route_barrier_with_any_workspace_state():
+    """The fused route's grid barrier needs no cleared workspace: a workspace
+    of random bytes, the same one reused (the count left at zero by the
+    previous call), its barrier area overwritten by other data, and two
+    workspaces taking turns all give the oracle's routing."""
+    d = wl.make("skewed", T=4096)
+    W = d["workload"]
+    lg = to_dev(d["logits"])
+    o = oracle.route(d["logits"], W.k)
+    nbytes = moe.moe_route_workspace_size(4096, W.E, W.k)
+    gen = torch.Generator(device="cuda").manual_seed(5)
+
+    def noise():
+        return torch.randint(0, 256, (nbytes,), dtype=torch.uint8, device="cuda", generator=gen)
+
+    moe.moe_device_status()                 # start from a clear status word
+    ws_a, ws_b = noise(), noise()
+    order = [ws_a, ws_a, ws_a, ws_b, ws_a, ws_b, ws_b]
+    for i, ws in enumerate(order):
+        if i == 5:
+            ws.copy_(noise())               # another user's data lands in the workspace
+        r = moe.moe_route(lg, W.k, workspace=ws, routing_map=True)
+        torch.cuda.synchronize()
+        _assert_route_equal(r, o, W.E)
+        assert moe.moe_workspace_status(ws) == 0
+        assert moe.moe_device_status() == 0
+
+
 @pytest.mark.parametrize("T,E,k", [(1, 64, 6), (127, 256, 8), (129, 64, 6), (1000, 256, 8),
                                    (333, 9, 3), (77, 33, 5)])
 def test_route_forced_ties(T, E, k):

@@ -45,6 +45,8 @@
 // scheduling.  Only the fused launch waits on other blocks, all of them
 // resident, with a time limit.
 #include <cmath>
+#include <map>
+#include <mutex>
 
 #include "pipeline.cuh"
 #include "route_fast.cuh"
@@ -392,7 +394,11 @@ struct PlaceOut {
     int32_t* slot_pos;
     float* permuted_probs;
     WsHeader* header;
-    uint32_t* barrier;          // grid-barrier arrival count (workspace), zeroed before the launch
+    uint32_t* counter;          // grid-barrier count (workspace): arrivals, then departures
+    uint64_t* marker;           // tag of the last call whose blocks all left the barrier
+    uint64_t* flags;            // [G] arrival flags, for a workspace in an unknown state
+    uint64_t tag;               // this call's tag (distinct for every call in the process)
+    uint64_t expect;            // the marker a clean workspace holds (the previous call's tag)
 };
 
 // The placement of route_fast_place_kernel inside the fused route, from this
@@ -403,7 +409,7 @@ struct PlaceOut {
 // totals into offsets and place this block's slots.
 __device__ void place_from_block(const uint16_t* __restrict__ hist, int E, int k, int tpb,
                                  int64_t T, const uint32_t* s_mask, int W, const int32_t* s_idx,
-                                 const float* s_w, const PlaceOut& po,
+                                 const float* s_w, const PlaceOut& po, const int* s_fast,
                                  uint32_t* __restrict__ dev_status) {
     __shared__ __align__(16) uint32_t s_ptot[kPThreads * 4];   // [P][stride/2] packed partials
     __shared__ __align__(16) uint32_t s_pbef[kPThreads * 4];
@@ -414,31 +420,80 @@ __device__ void place_from_block(const uint16_t* __restrict__ hist, int E, int k
     const int stride = hist_stride(E);
     const int64_t t0 = int64_t(b) * tpb;
     const int nt = int(max64(0, min64(tpb, T - t0)));
-    // the grid barrier: thread 0 adds the block's arrival with a release
-    // reduction, which releases the block's count row (written before the
-    // __syncthreads below) at GPU scope, then polls the count with acquire
-    // loads until every block has arrived.  (Per-block arrival flags measured
-    // 1.1 us slower to release -- 152 pollers each reading all 152 flags --
-    // and a self-initialising compare-and-swap count 90 us slower.)
+    // The grid barrier, one of two ways, chosen alike by every block from the
+    // marker (*s_fast, set by thread 0 from the marker it loaded when the
+    // block started; only the last block of a call writes the marker, after
+    // every block has passed the barrier):
+    //  - the marker holds the previous call's tag (the workspace is as that
+    //    call left it): the count is zero.  Thread 0 adds its arrival with a
+    //    release reduction (releasing the block's count row, written before
+    //    the __syncthreads below, at GPU scope) and polls the count with
+    //    acquire loads until all G blocks have arrived.  Leaving, each block
+    //    adds 1 more; the last of the 2G resets the count to zero and stores
+    //    this call's tag, so the next call needs no clearing either.
+    //  - anything else (a new workspace, other data, a call that timed out):
+    //    each block stores this call's tag in its own flag (release) and warp
+    //    0 polls the G flags until all hold it -- correct whatever the
+    //    workspace held, as a foreign flag matches the tag only by a 2^-64
+    //    chance.  Block 0 then zeroes the count and stores the tag.
+    // (A memset of the count before every call measured 1.9 us per call; a
+    // self-initialising compare-and-swap count was 90 us slower.)
     __shared__ int s_ok;
     __syncthreads();
-    if (threadIdx.x == 0) {
-        asm volatile("red.release.gpu.global.add.u32 [%0], 1;" :: "l"(po.barrier) : "memory");
-        const uint64_t start = global_ns();
-        bool ok = true;
-        for (;;) {
-            uint32_t v;
-            asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(po.barrier) : "memory");
-            if (v >= uint32_t(G)) break;
-            if (global_ns() - start > kWaitLimitNs) { ok = false; break; }
-            __nanosleep(32);
+    const bool fast = *s_fast != 0;
+    if (fast) {
+        if (threadIdx.x == 0) {
+            asm volatile("red.release.gpu.global.add.u32 [%0], 1;" :: "l"(po.counter) : "memory");
+            const uint64_t start = global_ns();
+            bool ok = true;
+            for (;;) {
+                uint32_t v;
+                asm volatile("ld.acquire.gpu.global.u32 %0, [%1];"
+                             : "=r"(v) : "l"(po.counter) : "memory");
+                if (v >= uint32_t(G)) break;
+                if (global_ns() - start > kWaitLimitNs) { ok = false; break; }
+                __nanosleep(32);
+            }
+            s_ok = ok;
         }
-        s_ok = ok;
+    } else {
+        if (threadIdx.x == 0)
+            asm volatile("st.release.gpu.global.u64 [%0], %1;" :: "l"(po.flags + b), "l"(po.tag)
+                         : "memory");
+        if (threadIdx.x < 32) {
+            const uint64_t start = global_ns();
+            bool ok = true;
+            for (;;) {
+                bool mine = true;
+                for (int i = int(threadIdx.x); i < G; i += 32) {
+                    uint64_t v;
+                    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];"
+                                 : "=l"(v) : "l"(po.flags + i) : "memory");
+                    mine = mine && v == po.tag;
+                }
+                if (__all_sync(kFull, mine)) break;
+                const bool late = global_ns() - start > kWaitLimitNs;
+                if (__any_sync(kFull, late)) { ok = false; break; }
+                __nanosleep(32);
+            }
+            if (threadIdx.x == 0) s_ok = ok;
+        }
     }
     __syncthreads();
     if (!s_ok) {
         if (threadIdx.x == 0 && dev_status) atomicExch(dev_status, uint32_t(MOE_ERR_TIMEOUT));
         return;
+    }
+    if (threadIdx.x == 0) {                  // leaving: leave the count zero for the next call
+        if (fast) {
+            if (atomicAdd(po.counter, 1u) == 2u * uint32_t(G) - 1u) {
+                *po.counter = 0u;
+                *po.marker = po.tag;
+            }
+        } else if (b == 0) {
+            *po.counter = 0u;
+            *po.marker = po.tag;
+        }
     }
     // rows of 16-bit counts, summed as packed pairs (every sum is at most
     // T <= 152 * kMaxTokens: no carry crosses a half); the rows were written
@@ -585,7 +640,7 @@ route_coop_topk_kernel(const float* __restrict__ logits, int64_t T, int E, int k
     if (!FUSED) asm volatile("griddepcontrol.launch_dependents;");
     extern __shared__ __align__(16) unsigned char smem_raw[];
     __shared__ __align__(8) uint64_t bars[kChunks];
-    __shared__ int s_fail, s_nfb;
+    __shared__ int s_fail, s_nfb, s_fast;
     __shared__ int s_fb[kMaxTokens];                 // tokens left for the exact pass
     constexpr int V = NG * 8 * TPT / 32;             // experts per lane in the exact pass
     constexpr int SPT = 8 / TPT;                     // slots per thread (k <= 8)
@@ -603,6 +658,11 @@ route_coop_topk_kernel(const float* __restrict__ logits, int64_t T, int E, int k
     const int64_t t0 = int64_t(blockIdx.x) * tpb;
     const int nt = int(min64(tpb, T - t0));
     const int nchunks = (nt + kChunkTokens - 1) / kChunkTokens;
+    // the fused barrier's way (place_from_block): the marker is loaded before
+    // anything else and used only at the barrier, so its latency hides
+    uint64_t marker = 0;
+    if (FUSED && threadIdx.x == 0)
+        asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(marker) : "l"(po.marker) : "memory");
     if (threadIdx.x == 0) {
         s_fail = 0;
         s_nfb = 0;
@@ -867,7 +927,8 @@ route_coop_topk_kernel(const float* __restrict__ logits, int64_t T, int E, int k
         hrow[e] = uint16_t(c);
     }
     if constexpr (FUSED) {
-        place_from_block(hist, E, k, tpb, T, s_mask, W, s_idx, s_w, po, dev_status);
+        if (threadIdx.x == 0) s_fast = marker == po.expect;   // seen after the next barrier
+        place_from_block(hist, E, k, tpb, T, s_mask, W, s_idx, s_w, po, &s_fast, dev_status);
     } else {
         for (int i = threadIdx.x; i < nt * k; i += nthreads) {
             const int tk = i / k;
@@ -1069,6 +1130,30 @@ moe_status_t launch_topk_k(const float* logits, int64_t T, int E, int k, int tpb
                                                   topk_groups, s);
 }
 
+// The fused route's barrier tags: a distinct value for every call in the
+// process (the SplitMix64 output function -- Steele, Lea and Flood, "Fast
+// splittable pseudorandom number generators", OOPSLA 2014 -- of a call
+// counter: its odd Weyl step and xor-shift-multiply mix are bijections of
+// 64-bit words), and the tag the previous call on the same workspace
+// received, which the workspace's marker holds if that call completed.
+void barrier_tags(const void* workspace, uint64_t* tag, uint64_t* expect) {
+    static std::mutex m;
+    static std::map<std::pair<int, const void*>, uint64_t> last;
+    static uint64_t calls = 0;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    std::lock_guard<std::mutex> lock(m);
+    uint64_t z = (++calls) * 0x9E3779B97F4A7C15ull;
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+    *tag = z ^ (z >> 31);
+    const auto key = std::make_pair(dev, workspace);
+    const auto it = last.find(key);
+    *expect = it != last.end() ? it->second : ~*tag;    // unknown workspace: no match
+    if (it == last.end() && last.size() >= 4096) last.clear();
+    last[key] = *tag;
+}
+
 // The few-threads-a-token top-k (TPT threads a token, NG groups of 8
 // experts each).  When every block can be resident at once the whole route
 // runs in this one cooperative launch (*fused = true); otherwise the kernel
@@ -1108,11 +1193,10 @@ moe_status_t launch_coop(const float* logits, int64_t T, int E, int k, int tpb, 
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    // the barrier count starts at zero (a stream memory write of the zero,
-    // cuStreamWriteValue32, measured 2-3 us slower per call than this memset)
-    if (cudaMemsetAsync(po.barrier, 0, sizeof(uint32_t), s) != cudaSuccess) return MOE_ERR_CUDA;
+    PlaceOut pt = po;
+    barrier_tags(po.counter, &pt.tag, &pt.expect);
     return cudaLaunchKernelEx(&cfg, kfused, logits, T, E, k, tpb, bulk, topk_idx, topk_w,
-                              routing_map, hist, rank_out, dev_status, po) == cudaSuccess
+                              routing_map, hist, rank_out, dev_status, pt) == cudaSuccess
                ? MOE_OK : MOE_ERR_CUDA;
 }
 
@@ -1152,9 +1236,10 @@ moe_status_t launch_topk_v(const float* logits, int64_t T, int E, int k, int tpb
 }
 
 // Workspace after the header: 16-bit histogram rows [G][stride], the fused
-// route's barrier count (one 256-byte unit), then (when G can exceed
+// route's barrier (a 256-byte unit holding the count at 0 and the marker at
+// 8, then kFusedMaxBlocks uint64 flags), then (when G can exceed
 // kFusedMaxBlocks) the scan kernel's int32 prefixes [G+1][E].
-constexpr size_t kBarrierBytes = kWsAlign;
+constexpr size_t kBarrierBytes = kWsAlign + kFusedMaxBlocks * sizeof(uint64_t);
 static_assert(kBarrierBytes % kWsAlign == 0, "the barrier word keeps the prefixes aligned");
 size_t counts_bytes(int64_t T, int E) {
     return align_up(size_t(max_blocks(T)) * size_t(hist_stride(E)) * sizeof(uint16_t), kWsAlign);
@@ -1194,15 +1279,16 @@ moe_status_t fast_route(const float* logits, int64_t T, int E, int k, int n_grou
     const int64_t G = (T + tpb - 1) / tpb;
     const bool bulk = E % 4 == 0 && aligned16(logits);
     uint16_t* hist = reinterpret_cast<uint16_t*>(scratch);
-    uint32_t* barrier = reinterpret_cast<uint32_t*>(reinterpret_cast<char*>(scratch) +
-                                                  counts_bytes(T, E));
-    int32_t* pre = reinterpret_cast<int32_t*>(reinterpret_cast<char*>(barrier) + kBarrierBytes);
+    char* barrier = reinterpret_cast<char*>(scratch) + counts_bytes(T, E);
+    int32_t* pre = reinterpret_cast<int32_t*>(barrier + kBarrierBytes);
     if (G > 0 && n_groups == 0 && k <= 8) {
         // a few threads a token, compare-exchange networks; the whole route
         // in one cooperative launch when every block fits at once
         const int NG = values_per_lane(E);      // logits per lane of a 32-lane token
         const PlaceOut po{counts, offsets, group_list, sorted_indices, slot_pos, permuted_probs,
-                          header, barrier};
+                          header, reinterpret_cast<uint32_t*>(barrier),
+                          reinterpret_cast<uint64_t*>(barrier + 8),
+                          reinterpret_cast<uint64_t*>(barrier + kWsAlign), 0, 0};
         bool fused = false;
         moe_status_t st;
         if (NG == 1)
