@@ -1,4 +1,5 @@
-// grouped_swiglu.cu -- moe_grouped_swiglu_pack, moe_grouped_swiglu.
+// grouped_swiglu.cu -- moe_grouped_swiglu_pack, moe_grouped_swiglu,
+// moe_grouped_swiglu_fp8, and the training path (save, dgrad, wgrad).
 //
 // The expert FFN of "从零理解 MoE 算子" §8 over expert-contiguous rows
 // (group_list segments, §7): GMM1 (x @ w_up[e], [n,2I]) -> hidden =
@@ -17,6 +18,9 @@
 //   warps 4..7   epilogue: tcgen05.ld of their 32-lane quadrant, SwiGLU (GMM1)
 //                or conversion (GMM2), bf16 stores, rows past the expert's
 //                segment masked
+//   warps 8..15  (moe_grouped_swiglu_fp8's GMM1 only) turn each stage's e4m3
+//                codes and block scales into the bf16 A tile before the MMA
+//                issuer may use it
 // Both operands are K-major: moe_grouped_swiglu_pack lays the weights out
 // once as w_up_packed [E, 2I, H] (rows in 128-blocks [gate j0..j0+127 | up
 // j0..j0+127], so one 256-column tile holds matching gate and up columns) and
