@@ -69,8 +69,9 @@ def test_route_full_workloads(name):
 def test_route_barrier_with_any_workspace_state():
     """The fused route's grid barrier needs no cleared workspace: a workspace
     of random bytes, the same one reused (the count left at zero by the
-    previous call), its barrier area overwritten by other data, and two
-    workspaces taking turns all give the oracle's routing."""
+    previous call), its barrier area overwritten by other data, only its
+    count overwritten, and two workspaces taking turns all give the oracle's
+    routing."""
     d = wl.make("skewed", T=4096)
     W = d["workload"]
     lg = to_dev(d["logits"])
@@ -83,15 +84,31 @@ def test_route_barrier_with_any_workspace_state():
 
     moe.moe_device_status()                 # start from a clear status word
     ws_a, ws_b = noise(), noise()
-    order = [ws_a, ws_a, ws_a, ws_b, ws_a, ws_b, ws_b]
+    # the barrier count sits after the 256-byte header and 128 rows of 256
+    # 16-bit counts (T = 4096: blocks of 32 tokens); poking it alone leaves the
+    # marker saying the workspace is clean
+    count_at = 256 + 128 * 256 * 2
+    order = [ws_a, ws_a, ws_a, ws_b, ws_a, ws_b, ws_b, ws_b, ws_b]
+    # the way each call takes: the count where the previous call on this
+    # workspace left it clean, else the flags (a workspace not seen before,
+    # or written over since)
+    ways = ["flags", "count", "count", "flags", "count", "flags", "count", "flags", "count"]
     for i, ws in enumerate(order):
         if i == 5:
             ws.copy_(noise())               # another user's data lands in the workspace
+        if i == 7:
+            ws[count_at:count_at + 4] = torch.tensor([3, 0, 0, 0], dtype=torch.uint8)
         r = moe.moe_route(lg, W.k, workspace=ws, routing_map=True)
         torch.cuda.synchronize()
         _assert_route_equal(r, o, W.E)
         assert moe.moe_workspace_status(ws) == 0
         assert moe.moe_device_status() == 0
+        # after the call: the count back at zero, the marker holding the
+        # call's tag and `go` the tag (count) or the tag ^ 1 (flags)
+        words = ws[count_at:count_at + 24].cpu().numpy().view("<u8")
+        assert int(words[0]) & 0xFFFFFFFF == 0
+        go, marker = int(words[1]), int(words[2])
+        assert go ^ marker == (0 if ways[i] == "count" else 1), (i, ways[i])
 
 
 @pytest.mark.parametrize("T,E,k", [(1, 64, 6), (127, 256, 8), (129, 64, 6), (1000, 256, 8),

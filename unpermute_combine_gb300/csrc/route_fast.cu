@@ -395,6 +395,8 @@ struct PlaceOut {
     float* permuted_probs;
     WsHeader* header;
     uint32_t* counter;          // grid-barrier count (workspace): arrivals, then departures
+    uint32_t* go;               // [2] this call's way, published by block 0 (tag: count,
+                                // tag ^ 1: flags), 8 bytes after the count: one load reads both
     uint64_t* marker;           // tag of the last call whose blocks all left the barrier
     uint64_t* flags;            // [G] arrival flags, for a workspace in an unknown state
     uint64_t tag;               // this call's tag (distinct for every call in the process)
@@ -409,7 +411,7 @@ struct PlaceOut {
 // totals into offsets and place this block's slots.
 __device__ void place_from_block(const uint16_t* __restrict__ hist, int E, int k, int tpb,
                                  int64_t T, const uint32_t* s_mask, int W, const int32_t* s_idx,
-                                 const float* s_w, const PlaceOut& po, const int* s_fast,
+                                 const float* s_w, const PlaceOut& po, const uint32_t* s_count0,
                                  uint32_t* __restrict__ dev_status) {
     __shared__ __align__(16) uint32_t s_ptot[kPThreads * 4];   // [P][stride/2] packed partials
     __shared__ __align__(16) uint32_t s_pbef[kPThreads * 4];
@@ -420,64 +422,77 @@ __device__ void place_from_block(const uint16_t* __restrict__ hist, int E, int k
     const int stride = hist_stride(E);
     const int64_t t0 = int64_t(b) * tpb;
     const int nt = int(max64(0, min64(tpb, T - t0)));
-    // The grid barrier, one of two ways, chosen alike by every block from the
-    // marker (*s_fast, set by thread 0 from the marker it loaded when the
-    // block started; only the last block of a call writes the marker, after
-    // every block has passed the barrier):
-    //  - the marker holds the previous call's tag (the workspace is as that
-    //    call left it): the count is zero.  Thread 0 adds its arrival with a
-    //    release reduction (releasing the block's count row, written before
-    //    the __syncthreads below, at GPU scope) and polls the count with
-    //    acquire loads until all G blocks have arrived.  Leaving, each block
-    //    adds 1 more; the last of the 2G resets the count to zero and stores
-    //    this call's tag, so the next call needs no clearing either.
-    //  - anything else (a new workspace, other data, a call that timed out):
-    //    each block stores this call's tag in its own flag (release) and warp
-    //    0 polls the G flags until all hold it -- correct whatever the
-    //    workspace held, as a foreign flag matches the tag only by a 2^-64
-    //    chance.  Block 0 then zeroes the count and stores the tag.
+    // The grid barrier, without clearing the workspace between calls.  Block 0
+    // loaded the count and the marker (the tag of the last call whose blocks
+    // all left the barrier) when it started, before any block of this call
+    // could arrive, and published the way in the word `go` after its top-k:
+    // this call's tag for the count (the marker held the tag of the previous
+    // call on this workspace and the count was zero), the tag ^ 1 for the
+    // flags.  (With the marker alone, a write over the count that left the
+    // marker intact would let blocks through before every row is written.)
+    // Every block adds 1 to the count after one fence
+    // (which releases the block's count row, written before the __syncthreads
+    // below, at GPU scope, to readers of any write that follows it), then
+    // reads `go` and the count together: the count is done once all G blocks
+    // have arrived; on the flags way the block stores the tag in its own flag
+    // and warp 0 polls the G flags until all hold it.
+    //  - count: leaving, each block adds 1 more, and the last of the 2G resets
+    //    the count to zero and stores the tag in the marker.
+    //  - flags (a new workspace, other data written over it or over its count,
+    //    a call that timed out): correct whatever the workspace held, as a foreign flag or `go`
+    //    matches only by a 2^-63 chance.  Block 0 then takes *s_count0 (the
+    //    count it found) plus G off the count -- zero once every arrival has
+    //    landed, in whatever order -- and stores the marker.  (Should an
+    //    arrival have come before block 0 read the count, the count ends
+    //    nonzero and the next call takes the flags again, which clears it.)
     // (A memset of the count before every call measured 1.9 us per call; a
     // self-initialising compare-and-swap count was 90 us slower.)
-    __shared__ int s_ok;
+    __shared__ int s_ok, s_way;
     __syncthreads();
-    const bool fast = *s_fast != 0;
-    if (fast) {
+    if (threadIdx.x < 32) {
+        const uint64_t start = global_ns();
+        bool ok = true;
+        int way = 0;                         // 0 not yet published, 1 count, 2 flags
         if (threadIdx.x == 0) {
-            asm volatile("red.release.gpu.global.add.u32 [%0], 1;" :: "l"(po.counter) : "memory");
-            const uint64_t start = global_ns();
-            bool ok = true;
+            // one fence, then relaxed writes (here and the flag below): the
+            // fence releases the count row to readers of each of them
+            asm volatile("fence.acq_rel.gpu;" ::: "memory");
+            asm volatile("red.relaxed.gpu.global.add.u32 [%0], 1;" :: "l"(po.counter) : "memory");
             for (;;) {
-                uint32_t v;
-                asm volatile("ld.acquire.gpu.global.u32 %0, [%1];"
-                             : "=r"(v) : "l"(po.counter) : "memory");
-                if (v >= uint32_t(G)) break;
+                // the count and `go` in one load (two loads would be two
+                // round trips: an acquire load holds back every later load)
+                uint32_t c, pad, glo, ghi;
+                asm volatile("ld.acquire.gpu.global.v4.u32 {%0, %1, %2, %3}, [%4];"
+                             : "=r"(c), "=r"(pad), "=r"(glo), "=r"(ghi) : "l"(po.counter)
+                             : "memory");
+                (void)pad;
+                const uint64_t g = (uint64_t(ghi) << 32) | glo;
+                if (g == (po.tag ^ 1u)) { way = 2; break; }
+                if (g == po.tag) way = 1;
+                if (way == 1 && c >= uint32_t(G)) break;
                 if (global_ns() - start > kWaitLimitNs) { ok = false; break; }
                 __nanosleep(32);
             }
-            s_ok = ok;
+            if (way == 2)
+                asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" :: "l"(po.flags + b),
+                             "l"(po.tag) : "memory");
         }
-    } else {
-        if (threadIdx.x == 0)
-            asm volatile("st.release.gpu.global.u64 [%0], %1;" :: "l"(po.flags + b), "l"(po.tag)
-                         : "memory");
-        if (threadIdx.x < 32) {
-            const uint64_t start = global_ns();
-            bool ok = true;
-            for (;;) {
-                bool mine = true;
-                for (int i = int(threadIdx.x); i < G; i += 32) {
-                    uint64_t v;
-                    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];"
-                                 : "=l"(v) : "l"(po.flags + i) : "memory");
-                    mine = mine && v == po.tag;
-                }
-                if (__all_sync(kFull, mine)) break;
-                const bool late = global_ns() - start > kWaitLimitNs;
-                if (__any_sync(kFull, late)) { ok = false; break; }
-                __nanosleep(32);
+        way = __shfl_sync(kFull, way, 0);
+        ok = __shfl_sync(kFull, int(ok), 0) != 0;
+        while (way == 2 && ok) {             // the whole warp polls the G flags
+            bool mine = true;
+            for (int i = int(threadIdx.x); i < G; i += 32) {
+                uint64_t v;
+                asm volatile("ld.acquire.gpu.global.u64 %0, [%1];"
+                             : "=l"(v) : "l"(po.flags + i) : "memory");
+                mine = mine && v == po.tag;
             }
-            if (threadIdx.x == 0) s_ok = ok;
+            if (__all_sync(kFull, mine)) break;
+            const bool late = global_ns() - start > kWaitLimitNs;
+            if (__any_sync(kFull, late)) { ok = false; break; }
+            __nanosleep(32);
         }
+        if (threadIdx.x == 0) { s_ok = ok; s_way = way; }
     }
     __syncthreads();
     if (!s_ok) {
@@ -485,13 +500,14 @@ __device__ void place_from_block(const uint16_t* __restrict__ hist, int E, int k
         return;
     }
     if (threadIdx.x == 0) {                  // leaving: leave the count zero for the next call
-        if (fast) {
+        if (s_way == 1) {
             if (atomicAdd(po.counter, 1u) == 2u * uint32_t(G) - 1u) {
                 *po.counter = 0u;
                 *po.marker = po.tag;
             }
         } else if (b == 0) {
-            *po.counter = 0u;
+            // the count is *s_count0 plus the G arrivals, whenever they land
+            atomicSub(po.counter, *s_count0 + uint32_t(G));
             *po.marker = po.tag;
         }
     }
@@ -640,7 +656,8 @@ route_coop_topk_kernel(const float* __restrict__ logits, int64_t T, int E, int k
     if (!FUSED) asm volatile("griddepcontrol.launch_dependents;");
     extern __shared__ __align__(16) unsigned char smem_raw[];
     __shared__ __align__(8) uint64_t bars[kChunks];
-    __shared__ int s_fail, s_nfb, s_fast;
+    __shared__ int s_fail, s_nfb;
+    __shared__ uint32_t s_count0;
     __shared__ int s_fb[kMaxTokens];                 // tokens left for the exact pass
     constexpr int V = NG * 8 * TPT / 32;             // experts per lane in the exact pass
     constexpr int SPT = 8 / TPT;                     // slots per thread (k <= 8)
@@ -658,11 +675,15 @@ route_coop_topk_kernel(const float* __restrict__ logits, int64_t T, int E, int k
     const int64_t t0 = int64_t(blockIdx.x) * tpb;
     const int nt = int(min64(tpb, T - t0));
     const int nchunks = (nt + kChunkTokens - 1) / kChunkTokens;
-    // the fused barrier's way (place_from_block): the marker is loaded before
-    // anything else and used only at the barrier, so its latency hides
+    // the fused barrier's way (place_from_block): block 0 loads the marker and
+    // the count before anything else -- before any block of this call can
+    // arrive -- and publishes the way after its top-k
     uint64_t marker = 0;
-    if (FUSED && threadIdx.x == 0)
+    uint32_t count0 = 0;
+    if (FUSED && threadIdx.x == 0 && blockIdx.x == 0) {
         asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(marker) : "l"(po.marker) : "memory");
+        asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(count0) : "l"(po.counter) : "memory");
+    }
     if (threadIdx.x == 0) {
         s_fail = 0;
         s_nfb = 0;
@@ -862,6 +883,16 @@ route_coop_topk_kernel(const float* __restrict__ logits, int64_t T, int E, int k
         }
     }
     __syncthreads();
+    if (FUSED && threadIdx.x == 0 && blockIdx.x == 0) {
+        // the way, published after the top-k: by now the two loads are long
+        // back (storing it at the start would hold this block's first warp,
+        // and with it the block, until they were)
+        const bool clean = marker == po.expect && count0 == 0u;
+        const uint64_t g = clean ? po.tag : po.tag ^ 1u;
+        asm volatile("st.relaxed.gpu.global.v2.u32 [%0], {%1, %2};"
+                     :: "l"(po.go), "r"(uint32_t(g)), "r"(uint32_t(g >> 32)) : "memory");
+        s_count0 = count0;
+    }
     // the queued tokens, one warp each, ranked on the exact patterns: the
     // largest value, then the lowest expert id holding it
     for (int i = warp; i < s_nfb; i += nthreads / 32) {
@@ -927,8 +958,7 @@ route_coop_topk_kernel(const float* __restrict__ logits, int64_t T, int E, int k
         hrow[e] = uint16_t(c);
     }
     if constexpr (FUSED) {
-        if (threadIdx.x == 0) s_fast = marker == po.expect;   // seen after the next barrier
-        place_from_block(hist, E, k, tpb, T, s_mask, W, s_idx, s_w, po, &s_fast, dev_status);
+        place_from_block(hist, E, k, tpb, T, s_mask, W, s_idx, s_w, po, &s_count0, dev_status);
     } else {
         for (int i = threadIdx.x; i < nt * k; i += nthreads) {
             const int tk = i / k;
@@ -1236,8 +1266,8 @@ moe_status_t launch_topk_v(const float* logits, int64_t T, int E, int k, int tpb
 }
 
 // Workspace after the header: 16-bit histogram rows [G][stride], the fused
-// route's barrier (a 256-byte unit holding the count at 0 and the marker at
-// 8, then kFusedMaxBlocks uint64 flags), then (when G can exceed
+// route's barrier (a 256-byte unit holding the count at 0, `go` at 8 and
+// the marker at 16, then kFusedMaxBlocks uint64 flags), then (when G can exceed
 // kFusedMaxBlocks) the scan kernel's int32 prefixes [G+1][E].
 constexpr size_t kBarrierBytes = kWsAlign + kFusedMaxBlocks * sizeof(uint64_t);
 static_assert(kBarrierBytes % kWsAlign == 0, "the barrier word keeps the prefixes aligned");
@@ -1287,7 +1317,8 @@ moe_status_t fast_route(const float* logits, int64_t T, int E, int k, int n_grou
         const int NG = values_per_lane(E);      // logits per lane of a 32-lane token
         const PlaceOut po{counts, offsets, group_list, sorted_indices, slot_pos, permuted_probs,
                           header, reinterpret_cast<uint32_t*>(barrier),
-                          reinterpret_cast<uint64_t*>(barrier + 8),
+                          reinterpret_cast<uint32_t*>(barrier + 8),
+                          reinterpret_cast<uint64_t*>(barrier + 16),
                           reinterpret_cast<uint64_t*>(barrier + kWsAlign), 0, 0};
         bool fused = false;
         moe_status_t st;
