@@ -461,12 +461,12 @@ __device__ void place_from_block(const uint16_t* __restrict__ hist, int E, int k
             for (;;) {
                 // the count and `go` in one load (two loads would be two
                 // round trips: an acquire load holds back every later load)
-                uint32_t c, pad, glo, ghi;
+                uint32_t w[4];               // count, unused, `go` low, `go` high
                 asm volatile("ld.acquire.gpu.global.v4.u32 {%0, %1, %2, %3}, [%4];"
-                             : "=r"(c), "=r"(pad), "=r"(glo), "=r"(ghi) : "l"(po.counter)
-                             : "memory");
-                (void)pad;
-                const uint64_t g = (uint64_t(ghi) << 32) | glo;
+                             : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+                             : "l"(po.counter) : "memory");
+                const uint32_t c = w[0];
+                const uint64_t g = (uint64_t(w[3]) << 32) | w[2];
                 if (g == (po.tag ^ 1u)) { way = 2; break; }
                 if (g == po.tag) way = 1;
                 if (way == 1 && c >= uint32_t(G)) break;
