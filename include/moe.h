@@ -96,11 +96,17 @@ int moe_abi_version(void);
  *                          offsets[E]
  *   routing_map [T,E] u8   1 where token t picked expert e (NULL: not written)
  * Every integer output is bit-exact and independent of launch order.
- * Workspace: moe_route_workspace_size(T, E, k) bytes (nothing in it needs to
- * be cleared: every call writes the scratch it reads).  Device status: up to
- * 256 experts the logits reach shared memory through bounded bulk-copy
- * waits; one that gives up records MOE_ERR_TIMEOUT in the library's device
- * status word (moe_device_status). */
+ * Workspace: moe_route_workspace_size(T, E, k) bytes.  Nothing in it needs to
+ * be cleared, and between calls it may hold anything (other data, random
+ * bytes): every call writes the scratch it reads, except the fused route's
+ * grid-barrier count and marker.  A call checks those against what the
+ * previous call on this workspace left; if either differs, it passes the
+ * barrier by per-block flags, which are correct for any contents (about
+ * 1 us slower), and leaves the count and marker ready for the next call.
+ * Calls that share a workspace must not overlap on the GPU.  Device status:
+ * up to 256 experts the logits reach shared memory through bounded
+ * bulk-copy waits; one that gives up records MOE_ERR_TIMEOUT in the
+ * library's device status word (moe_device_status). */
 moe_status_t moe_route_workspace_size(int64_t T, int E, int k, size_t* bytes);
 
 moe_status_t moe_route(const float* logits, int64_t T, int E, int k,
