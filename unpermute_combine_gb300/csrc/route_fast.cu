@@ -430,9 +430,9 @@ __device__ void place_from_block(const uint16_t* __restrict__ hist, int E, int k
     // call on this workspace and the count was zero), the tag ^ 1 for the
     // flags.  (With the marker alone, a write over the count that left the
     // marker intact would let blocks through before every row is written.)
-    // Every block adds 1 to the count after one fence
-    // (which releases the block's count row, written before the __syncthreads
-    // below, at GPU scope, to readers of any write that follows it), then
+    // Every block adds 1 to the count with a release reduction (which
+    // releases the block's count row, written before the __syncthreads below,
+    // at GPU scope), then
     // reads `go` and the count together: the count is done once all G blocks
     // have arrived; on the flags way the block stores the tag in its own flag
     // and warp 0 polls the G flags until all hold it.
@@ -454,10 +454,9 @@ __device__ void place_from_block(const uint16_t* __restrict__ hist, int E, int k
         bool ok = true;
         int way = 0;                         // 0 not yet published, 1 count, 2 flags
         if (threadIdx.x == 0) {
-            // one fence, then relaxed writes (here and the flag below): the
-            // fence releases the count row to readers of each of them
-            asm volatile("fence.acq_rel.gpu;" ::: "memory");
-            asm volatile("red.relaxed.gpu.global.add.u32 [%0], 1;" :: "l"(po.counter) : "memory");
+            // a release reduction (a fence plus a relaxed add measured 0.3 us
+            // slower); the flag below, on the flags way only, is a release store
+            asm volatile("red.release.gpu.global.add.u32 [%0], 1;" :: "l"(po.counter) : "memory");
             for (;;) {
                 // the count and `go` in one load (two loads would be two
                 // round trips: an acquire load holds back every later load)
@@ -474,7 +473,7 @@ __device__ void place_from_block(const uint16_t* __restrict__ hist, int E, int k
                 __nanosleep(32);
             }
             if (way == 2)
-                asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" :: "l"(po.flags + b),
+                asm volatile("st.release.gpu.global.u64 [%0], %1;" :: "l"(po.flags + b),
                              "l"(po.tag) : "memory");
         }
         way = __shfl_sync(kFull, way, 0);
