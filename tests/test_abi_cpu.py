@@ -173,3 +173,112 @@ def test_grouped_swiglu_fp8_validates_before_launch(lib):
     assert call(f, f, f, f, f, 64, 4, 512, 128, f, None, big, None) == 3
     assert call(f, f, f, f, f, 64, 4, 512, 128, f, ws, 16, None) == 3
     assert call(f, P(0x1004), f, f, f, 64, 4, 512, 128, f, ws, big, None) == 1   # scales unaligned
+
+
+def test_route_variants_validate_before_launch(lib):
+    """moe_route_grouped, moe_route_indices, moe_route_layout and
+    moe_fill_pad_rows refuse bad groups, sizes, pointers and workspaces on
+    the host."""
+    P = ctypes.c_void_p
+    f = P(0x1000)                                      # never dereferenced
+    ws = P(0x2000)
+    big = ctypes.c_size_t(1 << 40)
+
+    def grouped(E, k, g, kg, counts=f, ws_=ws, nbytes=big):
+        return lib.moe_route_grouped(f, 64, E, k, g, kg, f, f, counts, f, f, f, f, f, None,
+                                     ws_, nbytes, None)
+    assert grouped(64, 2, 0, 1) == 1                   # no groups
+    assert grouped(64, 2, 8, 9) == 1                   # more kept groups than groups
+    assert grouped(10, 2, 4, 2) == 1                   # E not a multiple of the groups
+    assert grouped(128, 2, 64, 4) == 2                 # more than 32 groups
+    assert grouped(64, 9, 8, 1) == 1                   # k above the kept groups' experts
+    assert grouped(64, 2, 8, 4, counts=None) == 1
+    assert grouped(64, 2, 8, 4, ws_=None) == 3
+    assert grouped(64, 2, 8, 4, ws_=P(0x2010)) == 3    # workspace not 256-byte aligned
+    assert grouped(64, 2, 8, 4, nbytes=16) == 3
+
+    def indices(E, k, idx=f, w=f, probs=f, counts=f, ws_=ws):
+        return lib.moe_route_indices(idx, w, 64, E, k, counts, f, f, f, f, probs, None,
+                                     ws_, big, None)
+    assert indices(4, 5) == 2                          # k > E
+    assert indices(0, 1) == 1
+    assert indices(8, 2, counts=None) == 1
+    assert indices(8, 2, idx=None) == 1
+    assert indices(8, 2, w=None) == 1                  # permuted_probs without weights
+    assert indices(8, 2, ws_=P(0x2080)) == 3
+
+    def layout(cap, pad, align, max_rows=256, E=8, sorted_=f, slot=f, nbytes=big):
+        return lib.moe_route_layout(f, f, 64, E, 2, cap, pad, align, max_rows, f, f, f,
+                                    sorted_, slot, f, ws, nbytes, None)
+    assert layout(0, 0, 0) == 1                        # alignment below 1
+    assert layout(0, 1, 1) == 1                        # padding needs a capacity
+    assert layout(-1, 0, 1) == 1
+    assert layout(16, 1, 1, max_rows=-1) == 1
+    assert layout(1 << 21, 1, 1, E=1024) == 2          # E * capacity rows >= 2^31
+    assert layout(16, 1, 1, sorted_=None) == 1
+    assert layout(16, 1, 1, slot=None) == 1
+    assert layout(16, 1, 1, nbytes=16) == 3
+
+    def fill(dtype, max_rows, H, E, rows=f, offsets=f):
+        return lib.moe_fill_pad_rows(rows, dtype, max_rows, H, offsets, f, E, None)
+    assert fill(3, 64, 16, 4) == 1                     # no such dtype
+    assert fill(1, 64, 16, 0) == 1
+    assert fill(1, 64, 16, 1025) == 2
+    assert fill(1, 64, 16, 4, offsets=None) == 1
+    assert fill(1, 64, 16, 4, rows=None) == 1
+    assert fill(1, 0, 16, 4, rows=None) == 0           # nothing to fill: no launch
+    assert fill(2, 64, 0, 4, rows=None) == 0
+
+
+def test_grouped_swiglu_family_validates_before_launch(lib):
+    """The grouped SwiGLU forward, its pack, save, dgrad and wgrad refuse
+    shapes the tensor-core tiles cannot take, missing or unaligned buffers and
+    short workspaces on the host; the workspace size is the status header
+    plus the bf16 hidden rows."""
+    P = ctypes.c_void_p
+    f = P(0x1000)                                      # never dereferenced
+    odd = P(0x1008)                                    # not 16-byte aligned
+    ws = P(0x2000)
+    big = ctypes.c_size_t(1 << 40)
+    sz = ctypes.c_size_t()
+    size = lib.moe_grouped_swiglu_workspace_size
+    assert size(64, 4, 256, 128, ctypes.byref(sz)) == 0 and sz.value == 256 + 64 * 128 * 2
+    assert size(0, 4, 256, 128, ctypes.byref(sz)) == 0 and sz.value == 256 + 256
+    assert size(64, 4, 128, 128, ctypes.byref(sz)) == 2      # H not a multiple of 256
+    assert size(64, 4, 256, 64, ctypes.byref(sz)) == 2       # I not a multiple of 128
+    assert size(64, 0, 256, 128, ctypes.byref(sz)) == 1
+    assert size(64, 1025, 256, 128, ctypes.byref(sz)) == 2
+    assert size(-1, 4, 256, 128, ctypes.byref(sz)) == 1
+    assert size(1 << 31, 4, 256, 128, ctypes.byref(sz)) == 2
+    assert size(64, 4, 256, 128, None) == 1
+
+    fwd = lib.moe_grouped_swiglu
+    assert fwd(f, f, f, None, 64, 4, 256, 128, f, ws, big, None) == 1    # no offsets
+    assert fwd(None, f, f, f, 64, 4, 256, 128, f, ws, big, None) == 1
+    assert fwd(f, f, f, f, 64, 4, 256, 128, f, None, big, None) == 3
+    assert fwd(f, f, f, f, 64, 4, 256, 128, f, P(0x2010), big, None) == 3
+    assert fwd(f, f, f, f, 64, 4, 256, 128, f, ws, 16640 - 1, None) == 3
+    assert fwd(odd, f, f, f, 64, 4, 256, 128, f, ws, big, None) == 1
+
+    pack = lib.moe_grouped_swiglu_pack
+    assert pack(f, f, 0, 256, 128, f, f, None) == 1
+    assert pack(f, f, 4, 100, 128, f, f, None) == 2
+    assert pack(None, f, 4, 256, 128, f, f, None) == 1
+
+    save = lib.moe_grouped_swiglu_save
+    assert save(f, f, f, f, 64, 4, 256, 128, f, None, f, ws, big, None) == 1   # no hidden
+    assert save(f, f, f, f, 64, 4, 256, 128, f, f, f, None, big, None) == 3
+    assert save(f, f, f, f, 64, 4, 256, 128, f, f, f, ws, 16, None) == 3
+    assert save(f, f, f, f, 64, 4, 256, 128, f, f, odd, ws, big, None) == 1
+
+    dgrad = lib.moe_grouped_swiglu_dgrad
+    assert dgrad(f, f, f, f, f, 64, 4, 256, 128, f, None, ws, big, None) == 1   # no dx
+    assert dgrad(f, f, f, f, f, 64, 4, 256, 128, f, f, None, big, None) == 3
+    assert dgrad(odd, f, f, f, f, 64, 4, 256, 128, f, f, ws, big, None) == 1
+
+    wgrad = lib.moe_grouped_swiglu_wgrad
+    assert wgrad(f, f, f, f, None, 64, 4, 256, 128, f, f, ws, big, None) == 1  # no offsets
+    assert wgrad(None, f, f, f, f, 64, 4, 256, 128, f, None, ws, big, None) == 1
+    assert wgrad(f, f, None, f, f, 64, 4, 256, 128, None, f, ws, big, None) == 1
+    assert wgrad(f, f, f, f, f, 64, 4, 256, 128, f, f, None, big, None) == 3
+    assert wgrad(f, f, f, f, f, 64, 4, 256, 128, P(0x1004), None, ws, big, None) == 1
