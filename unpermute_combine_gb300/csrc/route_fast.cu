@@ -432,19 +432,19 @@ __device__ void place_from_block(const uint16_t* __restrict__ hist, int E, int k
     // marker intact would let blocks through before every row is written.)
     // Every block adds 1 to the count with a release reduction (which
     // releases the block's count row, written before the __syncthreads below,
-    // at GPU scope), then
-    // reads `go` and the count together: the count is done once all G blocks
-    // have arrived; on the flags way the block stores the tag in its own flag
-    // and warp 0 polls the G flags until all hold it.
-    //  - count: leaving, each block adds 1 more, and the last of the 2G resets
-    //    the count to zero and stores the tag in the marker.
-    //  - flags (a new workspace, other data written over it or over its count,
-    //    a call that timed out): correct whatever the workspace held, as a foreign flag or `go`
-    //    matches only by a 2^-63 chance.  Block 0 then takes *s_count0 (the
-    //    count it found) plus G off the count -- zero once every arrival has
-    //    landed, in whatever order -- and stores the marker.  (Should an
-    //    arrival have come before block 0 read the count, the count ends
-    //    nonzero and the next call takes the flags again, which clears it.)
+    // at GPU scope), then reads `go` and the count together:
+    //  - count: done once all G blocks have arrived.  Leaving, each block adds
+    //    1 more, and the last of the 2G resets the count to zero and stores
+    //    the tag in the marker.
+    //  - flags (a new workspace, other data written over it or over its
+    //    count, a call that timed out): the block stores the tag in its own
+    //    flag and warp 0 polls the G flags until all hold it -- correct
+    //    whatever the workspace held, as a foreign flag or `go` matches only
+    //    by a 2^-63 chance.  Block 0 then takes *s_count0 (the count it
+    //    found) plus G off the count -- zero once every arrival has landed,
+    //    in whatever order -- and stores the marker.  (Should an arrival have
+    //    come before block 0 read the count, the count ends nonzero and the
+    //    next call takes the flags again, which clears it.)
     // (A memset of the count before every call measured 1.9 us per call; a
     // self-initialising compare-and-swap count was 90 us slower.)
     __shared__ int s_ok, s_way;
